@@ -1,0 +1,179 @@
+"""CPU oracle for KATA rank-one PSD causal linear attention.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package; the CUDA library and its Python
+binding never do, and share no code with it.
+
+The arithmetic lives in ``kata_oracle.c`` (plain C, double precision, OpenMP
+over independent rows/heads).  This module compiles it with gcc on first use and
+marshals numpy arrays.  Every function takes float64 arrays in the layouts
+
+    q, k : [B, H, T, d]      v, out : [B, H, T, dv]
+    S    : [B, H, n, dv]     z      : [B, H, n]        n = d(d+1)/2
+
+and follows the paper "Kernelized Linear Attention: Breaking the Capacity Wall
+with Symmetric Cones" (KATA): Eq. 2 (normalised linear attention and its additive
+recurrence), Sec. 3.1 (rank-one PSD lift), Sec. 4.1 (packed width, Eq. 17-20) and
+App. D.2 Algorithm 1 (chunkwise forward).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kata_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkata_oracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            i = ctypes.c_int
+            lib.kata_oracle_feature_dim.argtypes = [i]
+            lib.kata_oracle_feature_dim.restype = i
+            lib.kata_oracle_set_threads.argtypes = [i]
+            lib.kata_oracle_get_threads.restype = i
+            lib.kata_oracle_lift.argtypes = [_D, ctypes.c_int64, i, _D]
+            lib.kata_oracle_forward.argtypes = [_D, _D, _D, _D, i, i, i, i]
+            lib.kata_oracle_forward_rows.argtypes = [_D, _D, _D, _I64, ctypes.c_int64,
+                                                     _D, i, i, i, i]
+            lib.kata_oracle_recurrent.argtypes = [_D, _D, _D, _D, i, i, i, i]
+            lib.kata_oracle_chunked.argtypes = [_D, _D, _D, _D, i, i, i, i, i]
+            lib.kata_oracle_prefix_state.argtypes = [_D, _D, _D, _D, i, i, i, i]
+            lib.kata_oracle_decode_step.argtypes = [_D, _D, _D, _D, _D, _D, i, i, i]
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the oracle uses (0 = all cores)."""
+    _load().kata_oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().kata_oracle_get_threads())
+
+
+def feature_dim(d: int) -> int:
+    """Packed width n = d(d+1)/2 of the rank-one PSD lift (Sec. 4.1)."""
+    return int(_load().kata_oracle_feature_dim(int(d)))
+
+
+def lift(x) -> np.ndarray:
+    """Rank-one PSD lift psi(x) = vech(x x^T), sqrt(2) on off-diagonals (Sec. 3.1)."""
+    x = _f64(x)
+    d = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    n = feature_dim(d)
+    out = np.empty(x.shape[:-1] + (n,), dtype=np.float64)
+    _load().kata_oracle_lift(_p(x), rows, d, _p(out))
+    return out
+
+
+def _dims(q, v):
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    return B, H, T, d, dv
+
+
+def forward(q, k, v) -> np.ndarray:
+    """Direct O(T^2) definition: o_t = sum_{s<=t} (q_t.k_s)^2 v_s / sum_{s<=t} (q_t.k_s)^2."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_forward(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv)
+    return out
+
+
+def forward_rows(q, k, v, rows) -> np.ndarray:
+    """The direct definition at sampled rows; rows are flat (b*H + h)*T + t indices."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((rows.shape[0], dv), dtype=np.float64)
+    _load().kata_oracle_forward_rows(_p(q), _p(k), _p(v), rows.ctypes.data_as(_I64),
+                                     rows.shape[0], _p(out), B * H, T, d, dv)
+    return out
+
+
+def recurrent(q, k, v) -> np.ndarray:
+    """Self-check form: explicit feature-state recurrence of Eq. 2."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_recurrent(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv)
+    return out
+
+
+def chunked(q, k, v, C: int) -> np.ndarray:
+    """Self-check form: App. D.2 Algorithm 1 with Eq. 17-20 at chunk size C."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_chunked(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv, int(C))
+    return out
+
+
+def prefix_state(k, v):
+    """(S_T, Z_T) after all T tokens, by the additive recurrence (Eq. 2, App. D.1)."""
+    k, v = _f64(k), _f64(v)
+    B, H, T, d = k.shape
+    dv = v.shape[-1]
+    n = feature_dim(d)
+    S = np.empty((B, H, n, dv), dtype=np.float64)
+    z = np.empty((B, H, n), dtype=np.float64)
+    _load().kata_oracle_prefix_state(_p(k), _p(v), _p(S), _p(z), B * H, T, d, dv)
+    return S, z
+
+
+def decode_step(S, z, q, k, v):
+    """One recurrent step (App. D.1): returns (S', z', o) without modifying inputs.
+
+    q, k: [B, H, d]; v: [B, H, dv]; S: [B, H, n, dv]; z: [B, H, n]."""
+    S = _f64(S).copy()
+    z = _f64(z).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    out = np.empty((B, H, dv), dtype=np.float64)
+    _load().kata_oracle_decode_step(_p(S), _p(z), _p(q), _p(k), _p(v), _p(out), B * H,
+                                    d, dv)
+    return S, z, out

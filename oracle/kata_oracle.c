@@ -1,0 +1,313 @@
+/*
+ * kata_oracle.c -- plain CPU oracle for causal kernelized linear attention with
+ * the rank-one PSD feature map (KATA).  TEST INFRASTRUCTURE ONLY: the product
+ * path never links, loads or calls this file; only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg do.
+ *
+ * Everything here is computed in double precision with no blocking, fusion or
+ * reordering beyond what the cited definitions state, so that each function can
+ * be checked against the paper by eye.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * Source: "Kernelized Linear Attention: Breaking the Capacity Wall with
+ * Symmetric Cones" (KATA, arXiv 2607.17419v1):
+ *   - Sec. 2, Eq. 2: normalised linear attention
+ *       o_t = psi(q_t)^T S_t / psi(q_t)^T Z_t,
+ *       S_t = sum_{i<=t} psi(k_i) v_i^T,  Z_t = sum_{i<=t} psi(k_i),
+ *     with the additive recurrence S_t = S_{t-1} + psi(k_t) v_t^T,
+ *     Z_t = Z_{t-1} + psi(k_t); the readout is defined when the denominator
+ *     is positive.
+ *   - Sec. 3.1: rank-one PSD lift psi(u) = u u^T with
+ *     <u u^T, v v^T>_F = (u^T v)^2, in the n = p(p+1)/2 dimensional ambient
+ *     space of symmetric matrices under the Frobenius inner product.
+ *   - Sec. 4.1: n = d(d+1)/2 unique coordinates after symmetry packing;
+ *     chunkwise forward Eq. 17-20.
+ *   - App. D.2, Algorithm 1: chunkwise forward for one head (pad the final
+ *     chunk, S_0 = 0, Z_0 = 0, per chunk: expand psi, output via Eq. 20, then
+ *     update the state via Eq. 17, truncate to T).
+ *   - App. D.1 "Plain KATA": the additive recurrence (used for decoding).
+ *
+ * Readings where the paper is silent (each is listed with its reason in the
+ * design notes of the repository):
+ *   - packing: upper triangle (i <= j), row-major order
+ *       f(i,j) = i*d - i*(i-1)/2 + (j - i),
+ *     diagonal entries x_i^2, off-diagonal entries sqrt(2) x_i x_j, which makes
+ *     the packed vector an isometric image of x x^T under the Frobenius norm.
+ *   - the causal sum is inclusive (s <= t), as in Eq. 1-2;
+ *   - no 1/sqrt(d) or temperature is applied;
+ *   - a zero denominator gives a zero output row.
+ *
+ * Layouts: q, k are [B*H][T][d], v and out are [B*H][T][dv], all contiguous
+ * double.  The decode state is S [B*H][n][dv] and z [B*H][n].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int g_threads = 0; /* 0: OpenMP default */
+
+void kata_oracle_set_threads(int n) { g_threads = n; }
+
+int kata_oracle_get_threads(void) {
+#ifdef _OPENMP
+    return g_threads > 0 ? g_threads : omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* n = d(d+1)/2: the packed width of a symmetric d x d matrix (Sec. 4.1). */
+int kata_oracle_feature_dim(int d) { return d * (d + 1) / 2; }
+
+/* Rank-one PSD lift of one vector x in R^d (Sec. 3.1, packed as Sec. 4.1). */
+static void lift_one(const double *x, int d, double *phi) {
+    const double r2 = sqrt(2.0);
+    int f = 0;
+    for (int i = 0; i < d; ++i) {
+        for (int j = i; j < d; ++j) {
+            phi[f] = (i == j) ? x[i] * x[i] : r2 * x[i] * x[j];
+            ++f;
+        }
+    }
+}
+
+/* Lift `rows` vectors: x [rows][d] -> phi [rows][n]. */
+void kata_oracle_lift(const double *x, int64_t rows, int d, double *phi) {
+    const int n = kata_oracle_feature_dim(d);
+    for (int64_t r = 0; r < rows; ++r) lift_one(x + r * d, d, phi + r * n);
+}
+
+/* The direct definition (Eq. 2 with psi the rank-one lift) for one output row:
+ * w_s = (q_t . k_s)^2 for s <= t, o_t = sum_s w_s v_s / sum_s w_s. */
+static void direct_row(const double *q, const double *k, const double *v, int t, int d,
+                       int dv, double *o) {
+    const double *qt = q + (int64_t)t * d;
+    double den = 0.0;
+    for (int j = 0; j < dv; ++j) o[j] = 0.0;
+    for (int s = 0; s <= t; ++s) {
+        const double *ks = k + (int64_t)s * d;
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i) dot += qt[i] * ks[i];
+        const double w = dot * dot;
+        den += w;
+        const double *vs = v + (int64_t)s * dv;
+        for (int j = 0; j < dv; ++j) o[j] += w * vs[j];
+    }
+    for (int j = 0; j < dv; ++j) o[j] = den > 0.0 ? o[j] / den : 0.0;
+}
+
+/* Full causal forward by the direct O(T^2) definition. */
+void kata_oracle_forward(const double *q, const double *k, const double *v, double *out,
+                         int BH, int T, int d, int dv) {
+    const int64_t total = (int64_t)BH * T;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(kata_oracle_get_threads())
+    for (int64_t r = 0; r < total; ++r) {
+        const int64_t bh = r / T;
+        const int t = (int)(r % T);
+        direct_row(q + bh * T * d, k + bh * T * d, v + bh * T * dv, t, d, dv,
+                   out + r * dv);
+    }
+}
+
+/* The same definition evaluated only at sampled rows.  rows[i] = bh*T + t;
+ * out is [nrows][dv]. */
+void kata_oracle_forward_rows(const double *q, const double *k, const double *v,
+                              const int64_t *rows, int64_t nrows, double *out, int BH,
+                              int T, int d, int dv) {
+    (void)BH;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t bh = rows[i] / T;
+        const int t = (int)(rows[i] % T);
+        direct_row(q + bh * T * d, k + bh * T * d, v + bh * T * dv, t, d, dv,
+                   out + i * dv);
+    }
+}
+
+/* Self-check form 1: the explicit feature-state recurrence of Eq. 2,
+ * S_t = S_{t-1} + psi(k_t) v_t^T, Z_t = Z_{t-1} + psi(k_t),
+ * o_t = psi(q_t)^T S_t / psi(q_t)^T Z_t. */
+void kata_oracle_recurrent(const double *q, const double *k, const double *v,
+                           double *out, int BH, int T, int d, int dv) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)n * dv, sizeof(double));
+        double *Z = calloc((size_t)n, sizeof(double));
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            lift_one(k + row * d, d, pk);
+            lift_one(q + row * d, d, pq);
+            const double *vt = v + row * dv;
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j) S[(size_t)f * dv + j] += pk[f] * vt[j];
+                Z[f] += pk[f];
+            }
+            double den = 0.0;
+            for (int f = 0; f < n; ++f) den += pq[f] * Z[f];
+            double *o = out + row * dv;
+            for (int j = 0; j < dv; ++j) {
+                double num = 0.0;
+                for (int f = 0; f < n; ++f) num += pq[f] * S[(size_t)f * dv + j];
+                o[j] = den > 0.0 ? num / den : 0.0;
+            }
+        }
+        free(S);
+        free(Z);
+        free(pk);
+        free(pq);
+    }
+}
+
+/* Self-check form 2: Algorithm 1 (App. D.2) with the chunk equations 17-20.
+ * N_C = ceil(T/C); the final chunk is padded with zero rows; S = 0, Z = 0;
+ * per chunk: Psi(Q), Psi(K); P = (Psi(Q) Psi(K)^T) .* M (M lower-triangular,
+ * diagonal included); N = Psi(Q) S + P V; D = Psi(Q) Z + P 1; O = diag(D)^-1 N;
+ * then S += Psi(K)^T V, Z += Psi(K)^T 1; finally truncate to T rows. */
+void kata_oracle_chunked(const double *q, const double *k, const double *v, double *out,
+                         int BH, int T, int d, int dv, int C) {
+    const int n = kata_oracle_feature_dim(d);
+    const int NC = (T + C - 1) / C;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)n * dv, sizeof(double));
+        double *Z = calloc((size_t)n, sizeof(double));
+        double *PQ = calloc((size_t)C * n, sizeof(double));
+        double *PK = calloc((size_t)C * n, sizeof(double));
+        double *Vc = calloc((size_t)C * dv, sizeof(double));
+        double *P = calloc((size_t)C * C, sizeof(double));
+        double *N = calloc((size_t)C * dv, sizeof(double));
+        double *D = calloc((size_t)C, sizeof(double));
+        for (int c = 0; c < NC; ++c) {
+            /* load the chunk, zero-padding rows past T */
+            for (int r = 0; r < C; ++r) {
+                const int t = c * C + r;
+                if (t < T) {
+                    const int64_t row = (int64_t)bh * T + t;
+                    lift_one(q + row * d, d, PQ + (size_t)r * n);
+                    lift_one(k + row * d, d, PK + (size_t)r * n);
+                    memcpy(Vc + (size_t)r * dv, v + row * dv, sizeof(double) * dv);
+                } else {
+                    memset(PQ + (size_t)r * n, 0, sizeof(double) * n);
+                    memset(PK + (size_t)r * n, 0, sizeof(double) * n);
+                    memset(Vc + (size_t)r * dv, 0, sizeof(double) * dv);
+                }
+            }
+            /* P = (Psi(Q) Psi(K)^T) .* M */
+            for (int r = 0; r < C; ++r)
+                for (int s = 0; s < C; ++s) {
+                    double acc = 0.0;
+                    if (s <= r)
+                        for (int f = 0; f < n; ++f)
+                            acc += PQ[(size_t)r * n + f] * PK[(size_t)s * n + f];
+                    P[(size_t)r * C + s] = acc;
+                }
+            /* Eq. 18-19 */
+            for (int r = 0; r < C; ++r) {
+                double dacc = 0.0;
+                for (int f = 0; f < n; ++f) dacc += PQ[(size_t)r * n + f] * Z[f];
+                for (int s = 0; s < C; ++s) dacc += P[(size_t)r * C + s];
+                D[r] = dacc;
+                for (int j = 0; j < dv; ++j) {
+                    double nacc = 0.0;
+                    for (int f = 0; f < n; ++f)
+                        nacc += PQ[(size_t)r * n + f] * S[(size_t)f * dv + j];
+                    for (int s = 0; s < C; ++s)
+                        nacc += P[(size_t)r * C + s] * Vc[(size_t)s * dv + j];
+                    N[(size_t)r * dv + j] = nacc;
+                }
+            }
+            /* Eq. 20, truncated to T */
+            for (int r = 0; r < C; ++r) {
+                const int t = c * C + r;
+                if (t >= T) break;
+                double *o = out + ((int64_t)bh * T + t) * dv;
+                for (int j = 0; j < dv; ++j)
+                    o[j] = D[r] > 0.0 ? N[(size_t)r * dv + j] / D[r] : 0.0;
+            }
+            /* Eq. 17 */
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int s = 0; s < C; ++s)
+                        acc += PK[(size_t)s * n + f] * Vc[(size_t)s * dv + j];
+                    S[(size_t)f * dv + j] += acc;
+                }
+                double zacc = 0.0;
+                for (int s = 0; s < C; ++s) zacc += PK[(size_t)s * n + f];
+                Z[f] += zacc;
+            }
+        }
+        free(S);
+        free(Z);
+        free(PQ);
+        free(PK);
+        free(Vc);
+        free(P);
+        free(N);
+        free(D);
+    }
+}
+
+/* The state pair (S_T, Z_T) after T tokens, by the additive recurrence of
+ * Eq. 2 / App. D.1.  S is [BH][n][dv], z is [BH][n]. */
+void kata_oracle_prefix_state(const double *k, const double *v, double *S, double *z,
+                              int BH, int T, int d, int dv) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        memset(Sb, 0, sizeof(double) * n * dv);
+        memset(zb, 0, sizeof(double) * n);
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            lift_one(k + row * d, d, pk);
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j)
+                    Sb[(size_t)f * dv + j] += pk[f] * v[row * dv + j];
+                zb[f] += pk[f];
+            }
+        }
+        free(pk);
+    }
+}
+
+/* One recurrent decode step (App. D.1, Plain KATA), in place:
+ * S += psi(k) v^T, z += psi(k), then o = psi(q)^T S / psi(q)^T z
+ * (update, then read: the step's own key is included, as in Eq. 2).
+ * q, k are [BH][d], v and out are [BH][dv]. */
+void kata_oracle_decode_step(double *S, double *z, const double *q, const double *k,
+                             const double *v, double *out, int BH, int d, int dv) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        lift_one(k + (size_t)bh * d, d, pk);
+        lift_one(q + (size_t)bh * d, d, pq);
+        const double *vb = v + (size_t)bh * dv;
+        for (int f = 0; f < n; ++f) {
+            for (int j = 0; j < dv; ++j) Sb[(size_t)f * dv + j] += pk[f] * vb[j];
+            zb[f] += pk[f];
+        }
+        double den = 0.0;
+        for (int f = 0; f < n; ++f) den += pq[f] * zb[f];
+        for (int j = 0; j < dv; ++j) {
+            double num = 0.0;
+            for (int f = 0; f < n; ++f) num += pq[f] * Sb[(size_t)f * dv + j];
+            out[(size_t)bh * dv + j] = den > 0.0 ? num / den : 0.0;
+        }
+        free(pk);
+        free(pq);
+    }
+}
