@@ -1,0 +1,466 @@
+"""Benchmark of the KATA chunked forward on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one kata_fwd_chunked call over one batch of the workload (the
+feature lift, intra-chunk term, chunk state, inter-chunk prefix scan and the
+normalised output, all inside the call).  Inputs are resident in HBM before
+the timed region and are larger than L2 (129 MB) for the default workload, so
+no L2 flush is needed; the timed region is K back-to-back steps bracketed by a
+barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
+stream, max over ranks.  value = tokens (B*T per step, all heads) per second.
+
+Extra keys: "roofline" for the dominant kernel (its algorithmic work per
+launch over its mean CUDA-event launch time, from the library's tracing),
+"cpu_baseline" (the CPU oracle on sampled rows of the same workload),
+"e2e" (the host-buffer entry point with host<->device copies in the timed
+region), "decode" (the recurrent decode step at batch 256), "clocks"
+(nvidia-smi samples during the timed region) and "gpu_launches".
+
+--impl reference times the CPU oracle (the reference implementation of this
+repository; there is no installable upstream code) on bounded row samples of
+the same workload.  Multi-GPU runs are independent replicas (the path shards
+over (b, h) with no exchange), scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "long_ctx_bf16"
+L2_BYTES = 129 * 1024 * 1024
+SMS = 152
+FP32_FFMA_PEAK_TFLOPS = SMS * 128 * 2 * 2.070e9 / 1e12   # 152 SMs x 128 lanes x FMA x 2.07 GHz
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per launch of each kernel (stated in the design notes)
+
+
+def _intra_pairs(T, C):
+    """Causal (s <= t) pairs inside chunks, summed over the chunks of one head."""
+    full, tail = divmod(T, C)
+    return full * C * (C + 1) // 2 + tail * (tail + 1) // 2
+
+
+def stage_work(stage: str, w) -> tuple[float, str, str]:
+    """(work per launch, unit, bound) for a traced stage on workload w."""
+    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, w.n
+    NC = -(-T // C)
+    state_flops = 2.0 * n * (dv + 1) * T * BH          # Psi(K)^T [V|1]
+    out_inter = 2.0 * n * (dv + 1) * T * BH            # Psi(Q) [S|Z]
+    intra = 2.0 * (d + dv + 1) * _intra_pairs(T, C) * BH   # (q.k)^2 and P [V|1], causal
+    if stage == "simt_chunk_state":
+        return state_flops, "TFLOP/s", "alu"
+    if stage == "simt_output":
+        return out_inter + intra, "TFLOP/s", "alu"
+    if stage == "simt_scan":
+        return 2.0 * 4 * n * (dv + 1) * NC * BH, "GB/s", "hbm"
+    if stage == "tc_state":
+        return state_flops, "TFLOP/s", "tensor"
+    if stage == "tc_output":
+        return out_inter + intra + state_flops, "TFLOP/s", "tensor"
+    if stage == "tc_scan":
+        return None, "GB/s", "hbm"
+    return None, "", ""
+
+
+def _source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kernelized_causal_linear_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel_stage: str, workload: str):
+    """DRAM bytes per launch for a stage from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    digest = _source_digest()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#"):
+                stage, wl, sha, nbytes = parts
+                if stage == kernel_stage and wl == workload and sha == digest:
+                    return float(nbytes)
+    return None
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (rank 0 only)
+
+
+def _oracle_sample(w, q, k, v, seconds: float, rng):
+    """Time the oracle on sampled output rows (uniform over heads and positions)
+    for about `seconds`; returns (rows, elapsed seconds, threads).  Each row is
+    one head of one token."""
+    import oracle
+    BH = w.B * w.H
+    qf = q.reshape(BH, w.T, w.d)
+    kf = k.reshape(BH, w.T, w.d)
+    vf = v.reshape(BH, w.T, w.dv)
+
+    def run(nrows):
+        heads = rng.integers(0, BH, size=nrows)
+        ts = rng.integers(0, w.T, size=nrows)
+        t0 = time.perf_counter()
+        for h in np.unique(heads):
+            sel = ts[heads == h]
+            oracle.forward_rows(qf[h][None, None], kf[h][None, None], vf[h][None, None], sel)
+        return time.perf_counter() - t0
+
+    probe = 16
+    dt = run(probe)
+    while dt < min(1.0, seconds / 4):          # calibrate on at least ~1 s of work
+        probe *= 4
+        dt = run(probe)
+    nrows = max(probe, int(probe * seconds / dt))
+    dt = run(nrows)
+    return nrows, dt, oracle.get_threads()
+
+
+def _host_f64(t):
+    return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = workloads.WORKLOADS[args.workload]
+    q, k, v = workloads.make_qkv(w)
+    BH = w.B * w.H
+    # keep at most 4 heads on the host in fp64 (rows are sampled from them)
+    keep = min(BH, 4)
+    sub = w.scaled(B=1, H=keep)
+    qh = _host_f64(q.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
+    kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
+    vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
+    rng = np.random.default_rng(0)
+    per_step_s = float(os.environ.get("KATA_REF_STEP_SECONDS", "3"))
+    times, rows_total = [], 0
+    for i in range(args.warmup + args.steps):
+        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, per_step_s, rng)
+        if i >= args.warmup:
+            times.append(dt)
+            rows_total += nrows
+    # a token of the workload has H heads; each sampled row is one head
+    value = (rows_total / w.H) / sum(times)
+    line = {
+        "impl": "reference", "metric": _metric(), "value": value, "unit": "tokens/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total} output rows of heads 0..{keep - 1}, positions "
+                                   f"uniform in [0,T), direct O(T^2) fp64 definition; "
+                                   f"tokens = rows / H"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _metric():
+    return "fwd tokens/s for chunked PSD linear attention; % bf16 tensor peak (1 GB300)"
+
+
+def _config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "C": w.C,
+            "feature_dim": w.n, "global_batch": w.B, "seq_len": w.T,
+            "input_dtype": str(w.dtype).replace("torch.", ""),
+            "l2": "inputs larger than L2, no flush" if _input_bytes(w) > L2_BYTES
+            else "L2 flushed between steps",
+            "parallelism": "replicas"}
+
+
+def _input_bytes(w):
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    return w.B * w.H * w.T * (2 * w.d + w.dv) * es
+
+
+# ----------------------------------------------------------------------------
+
+
+def _dtype_name(w):
+    return "bf16" if w.dtype == torch.bfloat16 else "f32"
+
+
+def run_ours(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if rank == 0:
+            sys.stderr.write(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}\n")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from kernelized_causal_linear_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    import kernelized_causal_linear_gb300 as kg
+
+    w = workloads.WORKLOADS[args.workload]
+    peaks = _peaks()
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+    path = kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
+
+    for _ in range(args.warmup):
+        kg.kata_fwd_chunked(q, k, v, w.C, out=out)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.3)
+        kg.kata_trace_begin()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            kg.kata_fwd_chunked(q, k, v, w.C, out=out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        stages = kg.kata_trace_end()
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    tokens = w.B * w.T * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+
+    # dominant kernel roofline
+    launches = sum(n for n, _ in stages.values())
+    dom = max(stages.items(), key=lambda kv: kv[1][1])[0] if stages else None
+    roofline = None
+    if dom is not None:
+        nl, tot = stages[dom]
+        work, unit, bound = stage_work(dom, w)
+        mean_s = tot / nl / 1e3
+        if work is not None:
+            if unit == "TFLOP/s":
+                achieved = work / mean_s / 1e12
+                if bound == "tensor":
+                    peak, psrc = peaks["bf16_tflops"], f"bf16 dense burst, {peaks['source']}"
+                else:
+                    peak, psrc = FP32_FFMA_PEAK_TFLOPS, "fp32 FFMA: 152 SMs x 128 lanes x 2 x 2.07 GHz"
+            else:
+                achieved = work / mean_s / 1e9
+                peak, psrc = peaks["hbm_gbs"], f"HBM copy, {peaks['source']}"
+            traffic = _ncu_traffic(dom, w.name)
+            roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
+                        "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                        "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
+                        "work_per_launch": work}
+    # whole-call tensor fraction (algorithmic tensor flops over the step time)
+    step_s = elapsed_ms / 1e3 / args.steps
+    alg_flops = (stage_work("simt_chunk_state", w)[0] + stage_work("simt_output", w)[0])
+    whole = {"algorithmic_tflops": alg_flops / step_s / 1e12,
+             "frac_of_bf16_peak": alg_flops / step_s / 1e12 / peaks["bf16_tflops"]}
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
+        steps_e2e = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(steps_e2e):
+            kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
+        dt = time.perf_counter() - t0
+        es = qh.element_size()
+        e2e = {"value": w.B * w.T * steps_e2e * world / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": (qh.numel() + kh.numel() + vh.numel()) * es,
+               "d2h_bytes_per_step": oh.numel() * es, "steps": steps_e2e}
+        del qh, kh, vh, oh
+
+    decode = None if args.no_decode else _bench_decode(kg, peaks, args)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        keep = min(w.B * w.H, 4)
+        sub = w.scaled(B=1, H=keep)
+        BH = w.B * w.H
+        qh = _host_f64(q.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
+        kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
+        vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
+        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, args.cpu_seconds,
+                                            np.random.default_rng(1))
+        # each row is one head; a token of the workload has H heads
+        tps = (nrows / w.H) / dt
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} output rows from heads 0..{keep - 1}, positions uniform in "
+                         f"[0,T), direct O(T^2) fp64 definition, {dt:.1f} s; tokens = rows / H"}
+
+    if rank == 0:
+        line = {
+            "metric": _metric(), "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": _dtype_name(w), "data": "synthetic", "config": _config(w),
+            "path": {0: "none", 1: "simt", 2: "tcgen05"}.get(path, str(path)),
+            "roofline": roofline, "whole_call": whole, "cpu_baseline": cpu, "e2e": e2e,
+            "decode": decode, "clocks": clk.summary(), "gpu_launches": launches,
+            "stages": {k_: {"launches": n_, "total_ms": t_} for k_, (n_, t_) in stages.items()},
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def _bench_decode(kg, peaks, args):
+    w = workloads.DECODE
+    S, z = workloads.make_decode_state_fill(w, device="cuda")
+    q, k, v = workloads.make_decode_inputs(w, device="cuda")
+    o = torch.empty(w.B, w.H, w.dv, dtype=w.dtype, device="cuda")
+    for _ in range(3):
+        kg.kata_decode_step(S, z, q, k, v, out=o)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(5, args.steps)
+    a.record(stream)
+    for _ in range(steps):
+        kg.kata_decode_step(S, z, q, k, v, out=o)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    BH, n = w.B * w.H, w.n
+    nbytes = BH * (2 * 4 * n * w.dv + 2 * 4 * n) + BH * (2 * w.d + 2 * w.dv) * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "decode B=256 H=16 d=64 dv=64 fp32 state", "ms_per_step": ms,
+            "tokens_per_s": w.B / (ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "bytes_per_step": nbytes}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        sys.stderr.write("warning: fewer than 3 warm-up steps\n")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

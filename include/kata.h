@@ -1,0 +1,180 @@
+/*
+ * kata.h -- C ABI of libkata: causal kernelized linear attention with the
+ * rank-one PSD feature map (KATA) on NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Kernelized Linear Attention: Breaking the Capacity Wall with
+ * Symmetric Cones" (KATA, arXiv 2607.17419v1).
+ *
+ *   psi(x) = vech(x x^T) in R^n, n = d(d+1)/2            (Sec. 3.1, Sec. 4.1)
+ *            upper triangle, row-major, i <= j:
+ *              f(i,j) = i*d - i*(i-1)/2 + (j - i),
+ *              psi_f = x_i^2 (i == j),  sqrt(2) x_i x_j (i < j),
+ *            so that psi(q) . psi(k) = (q . k)^2 >= 0.
+ *   o_t    = psi(q_t)^T S_t / psi(q_t)^T Z_t,              (Sec. 2, Eq. 2)
+ *            S_t = sum_{s<=t} psi(k_s) v_s^T, Z_t = sum_{s<=t} psi(k_s)
+ *          = sum_{s<=t} (q_t.k_s)^2 v_s / sum_{s<=t} (q_t.k_s)^2.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense, row-major, contiguous, in the caller's memory.  The
+ *     library never frees or keeps a pointer it is given.
+ *   - q, k are [B][H][T][d]; v and out are [B][H][T][dv]; all of q, k, v and
+ *     out have the element type `dtype` (KATA_F32 or KATA_BF16).
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and is asynchronous unless stated otherwise.
+ *   - Accumulation is fp32.  A row whose denominator is exactly zero (its query
+ *     orthogonal to every key so far) is written as zeros.
+ *   - Return value: KATA_OK (0) or a negative kata_status.  Argument errors are
+ *     detected on the host before any work is enqueued, and leave every
+ *     output untouched.  KATA_ERR_CUDA reports a CUDA runtime error from a
+ *     launch or allocation (the CUDA error state is cleared first).
+ *   - There is no CPU fallback: unsupported shapes return
+ *     KATA_ERR_UNSUPPORTED.
+ */
+#ifndef KATA_H_
+#define KATA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum {
+    KATA_OK = 0,
+    KATA_ERR_ARG = -1,         /* null pointer, misaligned pointer, bad size */
+    KATA_ERR_UNSUPPORTED = -2, /* valid but unsupported shape or dtype       */
+    KATA_ERR_CUDA = -3,        /* CUDA runtime error                         */
+    KATA_ERR_ALLOC = -4,       /* device workspace allocation failed         */
+    KATA_ERR_TIMEOUT = -5      /* a bounded device-side wait expired         */
+} kata_status;
+
+/* Element types of q, k, v and out. */
+typedef enum { KATA_F32 = 0, KATA_BF16 = 1 } kata_dtype;
+
+/* Implementation a forward call runs on (see kata_fwd_path). */
+typedef enum {
+    KATA_PATH_NONE = 0, /* the shape is rejected                                 */
+    KATA_PATH_SIMT = 1, /* fp32 CUDA-core kernels (used for KATA_F32 inputs)     */
+    KATA_PATH_TC = 2    /* tcgen05 tensor-core kernels (bf16 inputs, sm_103a)    */
+} kata_path;
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *kata_stream_t;
+
+/* n = d(d+1)/2, the packed width of the lift (Sec. 4.1); -1 if d < 1. */
+int kata_feature_dim(int d);
+
+/* Static human-readable text for a status code. */
+const char *kata_status_str(int status);
+
+/*
+ * kata_fwd_chunked -- causal KATA forward in the exact O(T) chunked-state
+ * form (Sec. 4.1, Eq. 17-20; App. D.2, Algorithm 1; App. E.1 three-stage
+ * pipeline): per chunk of C tokens, the masked squared-score intra-chunk term
+ * (Psi(Q)Psi(K)^T .* M = (Q K^T)^2 .* M, M lower-triangular with the
+ * diagonal), the chunk state Psi(K)^T [V | 1], an exclusive prefix scan of the
+ * states over chunks, and the normalised output O = diag(D)^-1 N.
+ *
+ *   q, k  [B][H][T][d]   device, dtype, read only
+ *   v     [B][H][T][dv]  device, dtype, read only
+ *   out   [B][H][T][dv]  device, dtype, written (may not alias the inputs)
+ *   B, H, T >= 1; d in {16, 32, 64}; dv in {16, 32, 64, 128};
+ *   C in {32, 64, 128}: the chunk of Eq. 17-20.  T need not be a multiple of
+ *   C: the last chunk is zero-padded (Algorithm 1), padded rows are dropped.
+ *
+ * The output is the same function for every C (Eq. 17-20 regroup one sum);
+ * C changes only the rounding.  bf16 inputs run on the tensor-core path,
+ * which rounds the lifted features and the chunk-state prefix to bf16 as MMA
+ * operands (fp32 accumulation); fp32 inputs run on CUDA cores in fp32.
+ *
+ * Scratch: per-call device workspace (kata_fwd_workspace_size bytes) taken
+ * from the device's stream-ordered memory pool and released on `stream`.
+ * Returns KATA_ERR_ALLOC if that allocation fails.
+ */
+int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
+                     int T, int d, int dv, int C, int dtype, kata_stream_t stream);
+
+/* Bytes of device workspace kata_fwd_chunked allocates for this shape, written
+ * to *bytes.  Same argument checks as kata_fwd_chunked; no device work. */
+int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype,
+                            size_t *bytes);
+
+/* Which implementation kata_fwd_chunked selects for this shape on the current
+ * device (a kata_path value); KATA_PATH_NONE if it would reject the call.
+ * Queries the device's compute capability, nothing else. */
+int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype);
+
+/*
+ * kata_fwd_chunked_host -- the same forward with HOST buffers: allocates
+ * device buffers from the stream-ordered pool, copies q, k, v host->device,
+ * runs kata_fwd_chunked, copies out device->host and waits for `stream`.
+ * Pointers are host memory (pinned memory gives asynchronous copies).
+ * Synchronous: returns after out holds the result.
+ */
+int kata_fwd_chunked_host(const void *q, const void *k, const void *v, void *out, int B,
+                          int H, int T, int d, int dv, int C, int dtype,
+                          kata_stream_t stream);
+
+/*
+ * kata_decode_step -- one recurrent decode step per (b, h) (Sec. 2, Eq. 2
+ * additive recurrence; App. D.1 "Plain KATA"), updating the state in place and
+ * then reading it out, so the step's own key is included as in Eq. 2:
+ *   S += psi(k) v^T;  z += psi(k);  out = psi(q)^T S / psi(q)^T z.
+ *
+ *   state [B][H][n][dv] fp32 device, read and written (n = d(d+1)/2, packed in
+ *         the order of psi above; a prefill state in this layout continues it)
+ *   z     [B][H][n]     fp32 device, read and written
+ *   q, k  [B][H][d]     device, dtype
+ *   v     [B][H][dv]    device, dtype
+ *   out   [B][H][dv]    device, dtype, written
+ *   B, H >= 1; d in {16, 32, 64}; dv in {16, 32, 64, 128}.
+ * No workspace.
+ */
+int kata_decode_step(float *state, float *z, const void *q, const void *k, const void *v,
+                     void *out, int B, int H, int d, int dv, int dtype,
+                     kata_stream_t stream);
+
+/*
+ * kata_lift -- the feature lift alone (Sec. 3.1 rank-one PSD map, packed as
+ * in Sec. 4.1): phi[r][f] = psi(x_r)_f for rows r < rows.  The forward fuses
+ * this lift into its kernels and never writes phi to memory; this entry point
+ * exposes it for tests and for building states.
+ *
+ *   x   [rows][d]  device, dtype, read only
+ *   phi [rows][n]  fp32 device, written
+ *   rows >= 1; 1 <= d <= 64.
+ */
+int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype,
+              kata_stream_t stream);
+
+/*
+ * Tracing (no counterpart in the paper; measurement support).  Between
+ * kata_trace_begin and kata_trace_end, every kernel the library launches is
+ * bracketed by two CUDA events recorded on the stream it is launched on.
+ * kata_trace_end waits for those events, then reports per stage the number of
+ * launches and their summed device time, and switches tracing off.  Stages
+ * are named after the kernels ("chunk_state", "scan", "output", "decode",
+ * "lift", ...).  Tracing is process-wide and off by default.
+ */
+typedef struct {
+    char name[32];
+    int launches;
+    double total_ms;
+} kata_trace_stage;
+
+/* Start tracing (clears earlier records). */
+int kata_trace_begin(void);
+
+/* Stop tracing; writes up to max_stages entries to stages (may be NULL when
+ * max_stages is 0) and the number of distinct stages seen to *n_stages.
+ * Returns KATA_ERR_CUDA if an event could not be read. */
+int kata_trace_end(kata_trace_stage *stages, int max_stages, int *n_stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KATA_H_ */

@@ -1,0 +1,208 @@
+"""Python binding of libkata: KATA rank-one PSD causal linear attention on GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of libkata.so, reached through its C ABI (include/kata.h) with ctypes.
+PyTorch tensors supply device memory and the current CUDA stream; nothing here
+computes.  If libkata.so has not been built, every call raises -- there is no
+CPU fallback.
+
+Names follow the C ABI: kata_fwd_chunked, kata_decode_step, kata_lift,
+kata_fwd_chunked_host, kata_fwd_workspace_size, kata_fwd_path,
+kata_feature_dim, kata_status_str.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkata.so")
+
+KATA_OK = 0
+KATA_ERR_ARG = -1
+KATA_ERR_UNSUPPORTED = -2
+KATA_ERR_CUDA = -3
+KATA_ERR_ALLOC = -4
+KATA_ERR_TIMEOUT = -5
+
+KATA_F32 = 0
+KATA_BF16 = 1
+
+KATA_PATH_NONE = 0
+KATA_PATH_SIMT = 1
+KATA_PATH_TC = 2
+
+EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
+            "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
+            "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end")
+
+_lib = None
+
+
+class TraceStage(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
+
+
+class KataError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_str(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkata.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkata.so is not built ({LIB_PATH}); run "
+                               "kernelized_causal_linear_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        i, p, vp = ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+        L.kata_feature_dim.argtypes = [i]
+        L.kata_feature_dim.restype = i
+        L.kata_status_str.argtypes = [i]
+        L.kata_status_str.restype = ctypes.c_char_p
+        L.kata_fwd_chunked.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_chunked.restype = i
+        L.kata_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.kata_fwd_workspace_size.restype = i
+        L.kata_fwd_path.argtypes = [i, i, i, i, i, i, i]
+        L.kata_fwd_path.restype = i
+        L.kata_fwd_chunked_host.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_chunked_host.restype = i
+        L.kata_decode_step.argtypes = [p, p, p, p, p, p, i, i, i, i, i, vp]
+        L.kata_decode_step.restype = i
+        L.kata_lift.argtypes = [p, p, ctypes.c_int64, i, i, vp]
+        L.kata_lift.restype = i
+        L.kata_trace_begin.argtypes = []
+        L.kata_trace_begin.restype = i
+        L.kata_trace_end.argtypes = [ctypes.POINTER(TraceStage), i, ctypes.POINTER(i)]
+        L.kata_trace_end.restype = i
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return kata_status_str(status)
+
+
+def kata_status_str(status: int) -> str:
+    return lib().kata_status_str(int(status)).decode()
+
+
+def kata_feature_dim(d: int) -> int:
+    return int(lib().kata_feature_dim(int(d)))
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return KATA_F32
+    if t == torch.bfloat16:
+        return KATA_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != KATA_OK:
+        raise KataError(rc, where)
+
+
+def _contig(*ts):
+    for t in ts:
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def kata_fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal KATA forward (chunked O(T) form). q,k: [B,H,T,d]; v: [B,H,T,dv] on CUDA."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd_chunked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                B, H, T, d, dv, int(C), _dtype_code(q.dtype),
+                                _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked")
+    return out
+
+
+def kata_fwd_chunked_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Same forward on HOST tensors (pinned for async copies); synchronous."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, pin_memory=True)
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd_chunked_host(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     out.data_ptr(), B, H, T, d, dv, int(C),
+                                     _dtype_code(q.dtype), _stream_handle(stream, None))
+    _check(rc, "kata_fwd_chunked_host")
+    return out
+
+
+def kata_fwd_workspace_size(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().kata_fwd_workspace_size(B, H, T, d, dv, C, _dtype_code(dtype),
+                                         ctypes.byref(n)), "kata_fwd_workspace_size")
+    return int(n.value)
+
+
+def kata_fwd_path(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
+    return int(lib().kata_fwd_path(B, H, T, d, dv, C, _dtype_code(dtype)))
+
+
+def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+                     v: torch.Tensor, out: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """One recurrent decode step, state [B,H,n,dv] f32 and z [B,H,n] f32 updated in place."""
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=v.dtype, device=v.device)
+    _contig(state, z, q, k, v, out)
+    if state.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("state and z must be float32")
+    rc = lib().kata_decode_step(state.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                v.data_ptr(), out.data_ptr(), B, H, d, dv,
+                                _dtype_code(q.dtype), _stream_handle(stream, q.device))
+    _check(rc, "kata_decode_step")
+    return out
+
+
+def kata_lift(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """psi(x) for each row of x [..., d] -> fp32 [..., n]."""
+    d = x.shape[-1]
+    rows = x.numel() // d
+    n = d * (d + 1) // 2
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (n,), dtype=torch.float32, device=x.device)
+    _contig(x, out)
+    rc = lib().kata_lift(x.data_ptr(), out.data_ptr(), rows, d, _dtype_code(x.dtype),
+                         _stream_handle(stream, x.device))
+    _check(rc, "kata_lift")
+    return out
+
+
+def kata_trace_begin() -> None:
+    """Start per-stage device timing of every libkata launch."""
+    _check(lib().kata_trace_begin(), "kata_trace_begin")
+
+
+def kata_trace_end() -> dict:
+    """Stop tracing; {stage: (launches, total_ms)} since kata_trace_begin."""
+    buf = (TraceStage * 64)()
+    n = ctypes.c_int(0)
+    _check(lib().kata_trace_end(buf, 64, ctypes.byref(n)), "kata_trace_end")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(min(n.value, 64))}

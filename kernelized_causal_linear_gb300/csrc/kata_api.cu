@@ -1,0 +1,235 @@
+// C ABI of libkata (declared and documented in include/kata.h): argument
+// validation, path selection, workspace management and launches.
+#include <mutex>
+
+#include "../../include/kata.h"
+#include "kata_internal.cuh"
+
+using kata::FwdShape;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_d(int d) { return d == 16 || d == 32 || d == 64; }
+bool valid_dv(int dv) { return dv == 16 || dv == 32 || dv == 64 || dv == 128; }
+bool valid_C(int C) { return C == 32 || C == 64 || C == 128; }
+bool valid_dtype(int t) { return t == KATA_F32 || t == KATA_BF16; }
+size_t elem_size(int t) { return t == KATA_F32 ? 4 : 2; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_fwd_shape(int B, int H, int T, int d, int dv, int C, int dtype) {
+    if (B < 1 || H < 1 || T < 1) return KATA_ERR_ARG;
+    if (!valid_dtype(dtype)) return KATA_ERR_ARG;
+    if ((int64_t)B * H > 65535) return KATA_ERR_UNSUPPORTED;   // grid.y limit
+    if (!valid_d(d) || !valid_dv(dv) || !valid_C(C)) return KATA_ERR_UNSUPPORTED;
+    return KATA_OK;
+}
+
+// Device properties cached per device (queried once).
+struct DevInfo {
+    int major = 0, minor = 0, sms = 0;
+    bool ok = false;
+};
+
+int device_info(DevInfo &out) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    DevInfo &di = cache[dev];
+    if (!di.ok) {
+        if (cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return KATA_ERR_CUDA;
+        }
+        // Keep freed workspace in the stream-ordered pool between calls.
+        cudaMemPool_t pool;
+        if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+            uint64_t thr = UINT64_MAX;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+        }
+        cudaGetLastError();
+        di.ok = true;
+    }
+    out = di;
+    return KATA_OK;
+}
+
+int select_path(const FwdShape &s, const DevInfo &di) {
+    if (s.dtype == KATA_F32) return KATA_PATH_SIMT;
+    if (kata::tc_supported(s, di.major, di.minor)) return KATA_PATH_TC;
+    return KATA_PATH_SIMT;
+}
+
+size_t workspace_for(const FwdShape &s, int path, const DevInfo &di) {
+    return path == KATA_PATH_TC ? kata::tc_workspace_bytes(s, di.sms)
+                                : kata::simt_workspace_bytes(s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kata_feature_dim(int d) { return d < 1 ? -1 : d * (d + 1) / 2; }
+
+const char *kata_status_str(int status) {
+    switch (status) {
+        case KATA_OK: return "ok";
+        case KATA_ERR_ARG: return "invalid argument";
+        case KATA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case KATA_ERR_CUDA: return "CUDA runtime error";
+        case KATA_ERR_ALLOC: return "device workspace allocation failed";
+        case KATA_ERR_TIMEOUT: return "bounded device-side wait expired";
+        default: return "unknown status";
+    }
+}
+
+int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype,
+                            size_t *bytes) {
+    if (!bytes) return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    *bytes = workspace_for(s, select_path(s, di), di);
+    return KATA_OK;
+}
+
+int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype) {
+    if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_PATH_NONE;
+    DevInfo di;
+    if (device_info(di)) return KATA_PATH_NONE;
+    return select_path(FwdShape{B, H, T, d, dv, C, dtype}, di);
+}
+
+int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
+                     int T, int d, int dv, int C, int dtype, kata_stream_t stream) {
+    if (!q || !k || !v || !out) return KATA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    const size_t es = elem_size(dtype);
+    const size_t nqk = (size_t)B * H * T * d * es, nvo = (size_t)B * H * T * dv * es;
+    if (overlap(out, nvo, q, nqk) || overlap(out, nvo, k, nqk) || overlap(out, nvo, v, nvo))
+        return KATA_ERR_ARG;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    cudaGetLastError();
+
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    const int path = select_path(s, di);
+    const size_t wsb = workspace_for(s, path, di);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_ALLOC;
+    }
+    cudaError_t e = path == KATA_PATH_TC ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st)
+                                         : kata::simt_forward(s, q, k, v, out, ws, st);
+    if (ws) {
+        const cudaError_t ef = cudaFreeAsync(ws, st);
+        if (e == cudaSuccess) e = ef;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
+int kata_fwd_chunked_host(const void *q, const void *k, const void *v, void *out, int B,
+                          int H, int T, int d, int dv, int C, int dtype,
+                          kata_stream_t stream) {
+    if (!q || !k || !v || !out) return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    cudaGetLastError();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(dtype);
+    const size_t nqk = (size_t)B * H * T * d * es, nvo = (size_t)B * H * T * dv * es;
+    void *dq = nullptr, *dk = nullptr, *dvv = nullptr, *dout = nullptr;
+    rc = KATA_OK;
+    if (cudaMallocAsync(&dq, nqk, st) != cudaSuccess || cudaMallocAsync(&dk, nqk, st) != cudaSuccess ||
+        cudaMallocAsync(&dvv, nvo, st) != cudaSuccess ||
+        cudaMallocAsync(&dout, nvo, st) != cudaSuccess) {
+        cudaGetLastError();
+        rc = KATA_ERR_ALLOC;
+    }
+    if (rc == KATA_OK) {
+        if (cudaMemcpyAsync(dq, q, nqk, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(dk, k, nqk, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(dvv, v, nvo, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            rc = KATA_ERR_CUDA;
+    }
+    if (rc == KATA_OK) rc = kata_fwd_chunked(dq, dk, dvv, dout, B, H, T, d, dv, C, dtype, stream);
+    if (rc == KATA_OK &&
+        cudaMemcpyAsync(out, dout, nvo, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        rc = KATA_ERR_CUDA;
+    if (dq) cudaFreeAsync(dq, st);
+    if (dk) cudaFreeAsync(dk, st);
+    if (dvv) cudaFreeAsync(dvv, st);
+    if (dout) cudaFreeAsync(dout, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess && rc == KATA_OK) rc = KATA_ERR_CUDA;
+    cudaGetLastError();
+    return rc;
+}
+
+int kata_decode_step(float *state, float *z, const void *q, const void *k, const void *v,
+                     void *out, int B, int H, int d, int dv, int dtype,
+                     kata_stream_t stream) {
+    if (!state || !z || !q || !k || !v || !out) return KATA_ERR_ARG;
+    if (!aligned16(state) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+        !aligned16(v) || !aligned16(out))
+        return KATA_ERR_ARG;
+    if (B < 1 || H < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
+    if (!valid_d(d) || !valid_dv(dv)) return KATA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > INT32_MAX) return KATA_ERR_UNSUPPORTED;
+    const size_t n = (size_t)d * (d + 1) / 2;
+    const size_t BH = (size_t)B * H;
+    if (overlap(state, BH * n * dv * 4, z, BH * n * 4) ||
+        overlap(out, BH * dv * elem_size(dtype), state, BH * n * dv * 4))
+        return KATA_ERR_ARG;
+    cudaGetLastError();
+    const cudaError_t e = kata::decode_launch(state, z, q, k, v, out, (int)BH, d, dv, dtype,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
+int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype, kata_stream_t stream) {
+    if (!x || !phi || rows < 1 || d < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
+    if (d > 64) return KATA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(phi)) return KATA_ERR_ARG;
+    cudaGetLastError();
+    const cudaError_t e =
+        kata::lift_launch(x, phi, rows, d, dtype, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal declarations shared by the translation units of libkata.
+// Not part of the public ABI (include/kata.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kata {
+
+// Shape of one forward call, validated by the API layer.
+struct FwdShape {
+    int B, H, T, d, dv, C, dtype;
+    int BH() const { return B * H; }
+    int n() const { return d * (d + 1) / 2; }
+    int NC() const { return (T + C - 1) / C; }
+};
+
+// Element conversion for the two input types.
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Packed position f -> (i, j), i <= j, of the upper-triangle row-major order
+// f(i,j) = i*d - i*(i-1)/2 + (j - i) used by the rank-one PSD lift.
+__device__ __forceinline__ void vech_pair(int f, int d, int &i, int &j) {
+    int row = 0, start = 0;
+    while (start + (d - row) <= f) {
+        start += d - row;
+        ++row;
+    }
+    i = row;
+    j = row + (f - start);
+}
+
+constexpr float kSqrt2 = 1.41421356237309515f;
+
+// ---- tracing: kata_trace.cu ------------------------------------------------
+// Brackets one kernel launch with CUDA events on `stream` while tracing is on.
+class TraceScope {
+  public:
+    TraceScope(const char *stage, cudaStream_t stream);
+    ~TraceScope();
+    TraceScope(const TraceScope &) = delete;
+    TraceScope &operator=(const TraceScope &) = delete;
+
+  private:
+    const char *stage_;
+    cudaStream_t stream_;
+    cudaEvent_t start_ = nullptr;
+};
+
+// ---- CUDA-core (SIMT) path: kata_simt.cu ----------------------------------
+size_t simt_workspace_bytes(const FwdShape &s);
+cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                         void *out, void *workspace, cudaStream_t stream);
+cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
+                        cudaStream_t stream);
+
+// ---- decode: kata_decode.cu -----------------------------------------------
+cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
+                          void *out, int BH, int d, int dv, int dtype, cudaStream_t stream);
+
+// ---- tcgen05 path: kata_tc.cu ---------------------------------------------
+bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
+size_t tc_workspace_bytes(const FwdShape &s, int num_sms);
+cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                       void *out, void *workspace, int num_sms, cudaStream_t stream);
+
+}  // namespace kata

@@ -1,0 +1,296 @@
+// CUDA-core (fp32 FFMA) implementation of the KATA chunked forward.
+//
+// This is the path for fp32 inputs, where the 1e-4 accuracy target rules out
+// the tensor cores' reduced-precision operands.  It follows the three-stage
+// pipeline of the KATA paper (App. E.1 "Three-kernel pipeline"; Sec. 4.1
+// Eq. 17-20):
+//
+//   1. chunk state   S_loc[c] = Psi(K_c)^T [V_c | 1]            (Eq. 17 term)
+//   2. prefix scan   S_pre[c] = sum_{c' < c} S_loc[c']           (Sec. 4.2)
+//   3. chunk output  N = Psi(Q_c) S_pre[c] + P [V_c | 1],
+//                    P = (Q_c K_c^T)^2 .* M, O = N[:, :dv] / N[:, dv] (Eq. 18-20)
+//
+// The feature lift (Sec. 3.1) is fused: psi entries are formed in registers
+// from the q/k rows staged in shared memory and never written to memory.  The
+// intra-chunk weights use (q.k)^2 directly, which equals psi(q).psi(k).
+//
+// Workspace: per-chunk states [B*H][N_C][n][dv+1] fp32, scanned in place.
+#include "kata_internal.cuh"
+
+namespace kata {
+namespace {
+
+constexpr int kColGroup = 32;     // value columns per block (plus the ones column)
+constexpr int kStride = kColGroup + 1;
+constexpr int kFeatTile = 128;    // features per chunk-state block
+constexpr int kStageRows = 64;    // prefix rows staged per step in the output kernel
+
+// ---------------------------------------------------------------- stage 1
+template <typename T>
+__global__ void __launch_bounds__(kFeatTile)
+chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ st,
+                   int T_, int d, int dv, int C, int n, int NC, int nft) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x;
+    const int bh = blockIdx.y;
+    const int ft = blockIdx.z % nft;
+    const int cg = blockIdx.z / nft;
+    const int t0 = c * C;
+    const int tc = min(C, T_ - t0);
+    const int cols = min(kColGroup, dv - cg * kColGroup);
+    const int W = dv + 1;
+
+    float *ks = sm;                 // [C][d]
+    float *vs = ks + C * d;         // [C][33]
+    const T *kc = k + ((size_t)bh * T_ + t0) * d;
+    const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
+    for (int e = threadIdx.x; e < tc * d; e += blockDim.x) ks[e] = to_f(kc[e]);
+    for (int e = threadIdx.x; e < tc * kColGroup; e += blockDim.x) {
+        const int t = e / kColGroup, jj = e % kColGroup;
+        vs[t * kStride + jj] = jj < cols ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+    }
+    __syncthreads();
+
+    float acc[kStride];
+#pragma unroll
+    for (int jj = 0; jj < kStride; ++jj) acc[jj] = 0.f;
+    const int f = ft * kFeatTile + threadIdx.x;
+    if (f < n) {
+        int i, j;
+        vech_pair(f, d, i, j);
+        const float cf = (i == j) ? 1.f : kSqrt2;
+        for (int t = 0; t < tc; ++t) {
+            const float a = ks[t * d + i] * ks[t * d + j] * cf;   // psi(k_t)_f
+            const float *vr = vs + t * kStride;
+#pragma unroll
+            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(a, vr[jj], acc[jj]);
+            acc[kColGroup] += a;
+        }
+    }
+    __syncthreads();
+    // transpose through shared memory so each warp writes contiguous row segments
+    float *os = sm;                 // [128][33]
+#pragma unroll
+    for (int jj = 0; jj < kStride; ++jj) os[threadIdx.x * kStride + jj] = acc[jj];
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float *base = st + ((size_t)bh * NC + c) * (size_t)n * W;
+    for (int r = warp; r < kFeatTile; r += blockDim.x / 32) {
+        const int ff = ft * kFeatTile + r;
+        if (ff >= n) break;
+        float *row = base + (size_t)ff * W;
+        if (lane < cols) row[cg * kColGroup + lane] = os[r * kStride + lane];
+        if (cg == 0 && lane == 0) row[dv] = os[r * kStride + kColGroup];
+    }
+}
+
+// ---------------------------------------------------------------- stage 2
+// Exclusive prefix over chunks, independently per (b, h, element), in place.
+// Each thread walks the chunk axis for one element; consecutive threads touch
+// consecutive elements, so every step is a coalesced sweep.
+__global__ void __launch_bounds__(256)
+scan_kernel(float *__restrict__ st, int NC, int64_t E) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *p = st + (size_t)blockIdx.y * NC * E + e;
+    float run = 0.f;
+    int c = 0;
+    for (; c + 4 <= NC; c += 4) {
+        const float x0 = p[0], x1 = p[E], x2 = p[2 * E], x3 = p[3 * E];
+        p[0] = run;
+        run += x0;
+        p[E] = run;
+        run += x1;
+        p[2 * E] = run;
+        run += x2;
+        p[3 * E] = run;
+        run += x3;
+        p += 4 * E;
+    }
+    for (; c < NC; ++c) {
+        const float x = p[0];
+        p[0] = run;
+        run += x;
+        p += E;
+    }
+}
+
+// ---------------------------------------------------------------- stage 3
+// One block per (chunk, head, column group); thread r owns output row r.
+template <typename T>
+__global__ void __launch_bounds__(128)
+output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+              const float *__restrict__ st, T *__restrict__ out, int T_, int d, int dv,
+              int C, int n, int NC) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x;
+    const int bh = blockIdx.y;
+    const int cg = blockIdx.z;
+    const int r = threadIdx.x;
+    const int t0 = c * C;
+    const int tc = min(C, T_ - t0);
+    const int cols = min(kColGroup, dv - cg * kColGroup);
+    const int W = dv + 1;
+
+    float *qsT = sm;                // [d][C]  (transposed: conflict-free per-row reads)
+    float *ks = qsT + d * C;        // [C][d]
+    float *vs = ks + C * d;         // [C][33]
+    float *stg = vs + C * kStride;  // [kStageRows][33]
+    const T *qc = q + ((size_t)bh * T_ + t0) * d;
+    const T *kc = k + ((size_t)bh * T_ + t0) * d;
+    const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
+    for (int e = threadIdx.x; e < C * d; e += blockDim.x) {
+        const int t = e / d, i = e % d;
+        const bool ok = t < tc;
+        qsT[i * C + t] = ok ? to_f(qc[e]) : 0.f;
+        ks[e] = ok ? to_f(kc[e]) : 0.f;
+    }
+    for (int e = threadIdx.x; e < C * kColGroup; e += blockDim.x) {
+        const int t = e / kColGroup, jj = e % kColGroup;
+        vs[t * kStride + jj] = (t < tc && jj < cols) ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+    }
+
+    float acc[kStride];
+#pragma unroll
+    for (int jj = 0; jj < kStride; ++jj) acc[jj] = 0.f;
+
+    // inter-chunk term: psi(q_r) . [S_pre | Z_pre]
+    const float *sp = st + ((size_t)bh * NC + c) * (size_t)n * W;
+    int fi = 0, fj = 0;
+    for (int f0 = 0; f0 < n; f0 += kStageRows) {
+        const int nf = min(kStageRows, n - f0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nf * kStride; e += blockDim.x) {
+            const int fr = e / kStride, jj = e % kStride;
+            const float *row = sp + (size_t)(f0 + fr) * W;
+            float val = 0.f;
+            if (jj < cols) val = row[cg * kColGroup + jj];
+            else if (jj == kColGroup) val = row[dv];
+            stg[e] = val;
+        }
+        __syncthreads();
+        for (int fr = 0; fr < nf; ++fr) {
+            const float a = qsT[fi * C + r] * qsT[fj * C + r] * (fi == fj ? 1.f : kSqrt2);
+            const float *sr = stg + fr * kStride;
+#pragma unroll
+            for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
+            if (++fj == d) {
+                ++fi;
+                fj = fi;
+            }
+        }
+    }
+
+    // intra-chunk term: weights (q_r . k_s)^2 for s <= r (causal, diagonal kept)
+    if (r < tc) {
+        for (int s = 0; s <= r; ++s) {
+            float dot = 0.f;
+            for (int i = 0; i < d; ++i) dot = fmaf(qsT[i * C + r], ks[s * d + i], dot);
+            const float w = dot * dot;
+            const float *vr = vs + s * kStride;
+#pragma unroll
+            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(w, vr[jj], acc[jj]);
+            acc[kColGroup] += w;
+        }
+        // Eq. 20 normalisation; a zero denominator gives a zero row
+        const float den = acc[kColGroup];
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        T *orow = out + ((size_t)bh * T_ + t0 + r) * dv + cg * kColGroup;
+#pragma unroll
+        for (int jj = 0; jj < kColGroup; ++jj)
+            if (jj < cols) orow[jj] = from_f<T>(den > 0.f ? acc[jj] * inv : 0.f);
+    }
+}
+
+// ---------------------------------------------------------------- lift
+template <typename T>
+__global__ void __launch_bounds__(256)
+lift_kernel(const T *__restrict__ x, float *__restrict__ phi, int64_t rows, int d, int n) {
+    __shared__ unsigned char pi[2080], pj[2080];
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const int start = i * d - i * (i - 1) / 2;
+        for (int j = i; j < d; ++j) {
+            pi[start + j - i] = (unsigned char)i;
+            pj[start + j - i] = (unsigned char)j;
+        }
+    }
+    __syncthreads();
+    const int64_t total = rows * n;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = e / n;
+        const int f = (int)(e % n);
+        const int i = pi[f], j = pj[f];
+        const float xi = to_f(x[r * d + i]), xj = to_f(x[r * d + j]);
+        phi[e] = (i == j) ? xi * xi : kSqrt2 * xi * xj;
+    }
+}
+
+template <typename T>
+cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v, T *out,
+                           float *st, cudaStream_t stream) {
+    const int n = s.n(), NC = s.NC(), BH = s.BH();
+    const int nft = (n + kFeatTile - 1) / kFeatTile;
+    const int ncg = (s.dv + kColGroup - 1) / kColGroup;
+
+    size_t sm1 = sizeof(float) * (size_t)(s.C * s.d + s.C * kStride);
+    sm1 = sm1 > sizeof(float) * kFeatTile * kStride ? sm1 : sizeof(float) * kFeatTile * kStride;
+    cudaFuncSetAttribute(chunk_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm1);
+    {
+        TraceScope tr("simt_chunk_state", stream);
+        chunk_state_kernel<T><<<dim3(NC, BH, nft * ncg), kFeatTile, sm1, stream>>>(
+            k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft);
+    }
+    const int64_t E = (int64_t)n * (s.dv + 1);
+    {
+        TraceScope tr("simt_scan", stream);
+        scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(st, NC, E);
+    }
+
+    const size_t sm3 = sizeof(float) *
+                       (size_t)(2 * s.d * s.C + s.C * kStride + kStageRows * kStride);
+    cudaFuncSetAttribute(output_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm3);
+    {
+        TraceScope tr("simt_output", stream);
+        output_kernel<T><<<dim3(NC, BH, ncg), s.C, sm3, stream>>>(q, k, v, st, out, s.T, s.d,
+                                                                    s.dv, s.C, n, NC);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(const FwdShape &s) {
+    return sizeof(float) * (size_t)s.BH() * (size_t)s.NC() * (size_t)s.n() *
+           (size_t)(s.dv + 1);
+}
+
+cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                         void *out, void *workspace, cudaStream_t stream) {
+    float *st = static_cast<float *>(workspace);
+    if (s.dtype == 0)
+        return simt_forward_t<float>(s, (const float *)q, (const float *)k, (const float *)v,
+                                     (float *)out, st, stream);
+    return simt_forward_t<__nv_bfloat16>(s, (const __nv_bfloat16 *)q,
+                                         (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
+                                         (__nv_bfloat16 *)out, st, stream);
+}
+
+cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
+                        cudaStream_t stream) {
+    const int n = d * (d + 1) / 2;
+    const int64_t total = rows * n;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    TraceScope tr("lift", stream);
+    if (dtype == 0)
+        lift_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>((const float *)x, phi, rows, d, n);
+    else
+        lift_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
+            (const __nv_bfloat16 *)x, phi, rows, d, n);
+    return cudaGetLastError();
+}
+
+}  // namespace kata

@@ -1,0 +1,124 @@
+"""C ABI checks that need no GPU: the library builds, loads and exports every
+function include/kata.h declares, and host-side argument validation rejects
+bad calls before any device work (these calls return before the library
+touches the CUDA runtime)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kata.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kernelized_causal_linear_gb300 import build
+    build.build()
+    import kernelized_causal_linear_gb300 as kg
+    return kg.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kata_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("kata_fwd_chunked", "kata_decode_step", "kata_feature_dim", "kata_status_str",
+                 "kata_lift"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    import kernelized_causal_linear_gb300 as kg
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    assert set(_declared_functions()) <= set(kg.EXPORTED) | set()
+
+
+def test_feature_dim_and_status_text(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert kg.kata_feature_dim(16) == 136
+    assert kg.kata_feature_dim(32) == 528
+    assert kg.kata_feature_dim(64) == 2080
+    assert kg.kata_feature_dim(0) == -1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert kg.kata_status_str(code) != "unknown status"
+    assert kg.kata_status_str(7) == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def _fwd(L, q=FAKE, k=FAKE, v=FAKE, out=FAKE + 0x1000000, B=1, H=1, T=8, d=16, dv=16, C=32,
+         dtype=1):
+    return L.kata_fwd_chunked(q, k, v, out, B, H, T, d, dv, C, dtype, None)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert _fwd(L, q=0) == kg.KATA_ERR_ARG
+    assert _fwd(L, out=0) == kg.KATA_ERR_ARG
+    assert _fwd(L, v=FAKE + 8) == kg.KATA_ERR_ARG              # misaligned
+    assert _fwd(L, B=0) == kg.KATA_ERR_ARG
+    assert _fwd(L, T=0) == kg.KATA_ERR_ARG
+    assert _fwd(L, H=-3) == kg.KATA_ERR_ARG
+    assert _fwd(L, dtype=2) == kg.KATA_ERR_ARG
+    assert _fwd(L, d=24) == kg.KATA_ERR_UNSUPPORTED
+    assert _fwd(L, dv=48) == kg.KATA_ERR_UNSUPPORTED
+    assert _fwd(L, C=16) == kg.KATA_ERR_UNSUPPORTED
+    assert _fwd(L, B=300, H=300) == kg.KATA_ERR_UNSUPPORTED     # grid limit on B*H
+    # out overlapping an input
+    assert _fwd(L, out=FAKE + 16) == kg.KATA_ERR_ARG
+
+
+def test_workspace_and_path_queries_reject_bad_shapes(L):
+    import kernelized_causal_linear_gb300 as kg
+    n = ctypes.c_size_t(0)
+    assert L.kata_fwd_workspace_size(1, 1, 8, 16, 16, 32, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd_workspace_size(1, 1, 8, 20, 16, 32, 1, ctypes.byref(n)) == \
+        kg.KATA_ERR_UNSUPPORTED
+    assert L.kata_fwd_path(1, 1, 8, 20, 16, 32, 1) == kg.KATA_PATH_NONE
+    assert L.kata_fwd_path(0, 1, 8, 16, 16, 32, 1) == kg.KATA_PATH_NONE
+
+
+def test_host_variant_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert L.kata_fwd_chunked_host(0, FAKE, FAKE, FAKE, 1, 1, 8, 16, 16, 32, 1, None) == \
+        kg.KATA_ERR_ARG
+    assert L.kata_fwd_chunked_host(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 16, 17, 32, 1, None) == \
+        kg.KATA_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    S, z, q, k, v, o = (FAKE * (i + 1) * 256 for i in range(6))
+    assert L.kata_decode_step(0, z, q, k, v, o, 1, 1, 16, 16, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_decode_step(S, z, q, k, v + 4, o, 1, 1, 16, 16, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_decode_step(S, z, q, k, v, o, 0, 1, 16, 16, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_decode_step(S, z, q, k, v, o, 1, 1, 8, 16, 1, None) == kg.KATA_ERR_UNSUPPORTED
+    assert L.kata_decode_step(S, z, q, k, v, o, 1, 1, 16, 20, 1, None) == kg.KATA_ERR_UNSUPPORTED
+    # z overlapping the state
+    assert L.kata_decode_step(S, S + 64, q, k, v, o, 1, 1, 16, 16, 1, None) == kg.KATA_ERR_ARG
+
+
+def test_lift_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert L.kata_lift(0, FAKE, 4, 16, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_lift(FAKE, FAKE * 2, 0, 16, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_lift(FAKE, FAKE * 2, 4, 65, 1, None) == kg.KATA_ERR_UNSUPPORTED
+    assert L.kata_lift(FAKE + 2, FAKE * 2, 4, 16, 1, None) == kg.KATA_ERR_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import kernelized_causal_linear_gb300 as kg
+    monkeypatch.setattr(kg, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(kg, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        kg.lib()

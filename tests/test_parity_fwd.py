@@ -1,0 +1,142 @@
+"""GPU forward parity: libkata's kata_fwd_chunked against the CPU oracle.
+
+Element by element at sizes the oracle finishes in seconds (several chunks and a
+ragged tail), and on sampled rows at the workloads' full sizes in the same call
+configuration the benchmark times.  Inputs come from workloads.py; the oracle
+reads exactly the stored (bf16-rounded) values."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import TOL, require_gpu, slice_rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kg():
+    return require_gpu()
+
+
+def _run(kg, q, k, v, C):
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    out = kg.kata_fwd_chunked(qd, kd, vd, C)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check_full(kg, q, k, v, C, tol=None):
+    out = _run(kg, q, k, v, C)
+    ref = oracle.forward(to_f64(q), to_f64(k), to_f64(v))
+    err = slice_rel_err(to_f64(out), ref)
+    tol = TOL[q.dtype] if tol is None else tol
+    assert err <= tol, f"max relative error {err:.3e} > {tol:.1e}"
+    assert torch.isfinite(out).all()
+    return err
+
+
+def test_small_fp32_workload_full(kg):
+    w = workloads.WORKLOADS["small_fp32"]
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+
+
+@pytest.mark.parametrize("name,overrides", [
+    ("mid_bf16", dict(B=2, H=2, T=517)),
+    ("recall_bf16", dict(B=2, H=2, T=700)),
+    ("lm_layer_bf16", dict(B=1, H=3, T=333)),
+    ("long_ctx_bf16", dict(B=1, H=2, T=1100)),
+    ("small_fp32", dict(B=2, H=3, T=300)),
+])
+def test_workload_recipes_scaled(kg, name, overrides):
+    w = workloads.WORKLOADS[name].scaled(**overrides)
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_ragged_lengths(kg, dtype, C):
+    for T in (1, C - 1, C, C + 1, 3 * C + 5):
+        w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=T, dtype=dtype, C=C)
+        q, k, v = workloads.make_qkv(w)
+        _check_full(kg, q, k, v, C)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("dv", [16, 32, 64, 128])
+def test_head_dims(kg, dtype, d, dv):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=200, d=d, dv=dv, dtype=dtype, C=64)
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, 64)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_zero_denominator_rows_are_zero(kg, dtype):
+    # queries along e_0, the first 70 keys along e_1: rows t < 70 have D_t = 0
+    B, H, T, d, dv = 1, 1, 150, 32, 64
+    q = torch.zeros(B, H, T, d)
+    k = torch.zeros(B, H, T, d)
+    q[..., 0] = 1.0
+    k[..., :70, 1] = 1.0
+    k[..., 70:, 0] = 1.0
+    v = torch.randn(B, H, T, dv, generator=torch.Generator().manual_seed(5))
+    q, k, v = (t.to(dtype) for t in (q, k, v))
+    out = _run(kg, q, k, v, 64).float().cpu()
+    assert torch.all(out[..., :70, :] == 0)
+    ref = oracle.forward(to_f64(q), to_f64(k), to_f64(v))
+    assert slice_rel_err(out.numpy().astype(np.float64), ref) <= TOL[dtype]
+
+
+def test_deterministic(kg):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=2, H=2, T=1000)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked(q, k, v, w.C)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def _sample_rows(w, heads, rng, per_head=24):
+    T, C = w.T, w.C
+    fixed = [0, 1, C - 1, C, C + 1, 2 * C - 1, T // 2, T - 2, T - 1]
+    rows = []
+    for h in heads:
+        ts = sorted(set([t for t in fixed if 0 <= t < T] +
+                        rng.integers(0, T, size=per_head).tolist()))
+        rows.append(ts)
+    return rows
+
+
+@pytest.mark.parametrize("name", ["small_fp32", "mid_bf16", "recall_bf16", "lm_layer_bf16",
+                                  "long_ctx_bf16"])
+def test_full_size_sampled_rows(kg, name):
+    """Full workload size, the exact call the benchmark times, checked on
+    sampled rows computed one by one by the oracle."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    out = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    rng = np.random.default_rng(w.index)
+    BH = w.B * w.H
+    heads = sorted(set([0, BH - 1] + rng.integers(0, BH, size=2).tolist()))
+    # copy only the sampled heads to the host for the oracle
+    qf = q.reshape(BH, 1, w.T, w.d)[heads]
+    kf = k.reshape(BH, 1, w.T, w.d)[heads]
+    vf = v.reshape(BH, 1, w.T, w.dv)[heads]
+    of = out.reshape(BH, w.T, w.dv)[heads]
+    rows = _sample_rows(w, heads, rng)
+    worst = 0.0
+    for hi, ts in enumerate(rows):
+        flat = np.array(ts, dtype=np.int64)
+        ref = oracle.forward_rows(to_f64(qf[hi:hi + 1]), to_f64(kf[hi:hi + 1]),
+                                  to_f64(vf[hi:hi + 1]), flat)
+        got = to_f64(of[hi][flat])
+        worst = max(worst, slice_rel_err(got, ref))
+    assert worst <= TOL[w.dtype], f"{name}: {worst:.3e}"
