@@ -151,6 +151,14 @@ int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype,
               kata_stream_t stream);
 
 /*
+ * kata_sync_status -- waits for `stream`, then reports and clears the sticky
+ * device-side error word: KATA_ERR_TIMEOUT if a tensor-core kernel gave up a
+ * bounded wait (it records the error and exits instead of hanging; its output
+ * is then incomplete), KATA_OK otherwise.  No counterpart in the paper.
+ */
+int kata_sync_status(kata_stream_t stream);
+
+/*
  * Tracing (no counterpart in the paper; measurement support).  Between
  * kata_trace_begin and kata_trace_end, every kernel the library launches is
  * bracketed by two CUDA events recorded on the stream it is launched on.

@@ -35,7 +35,8 @@ KATA_PATH_TC = 2
 
 EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
-            "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end")
+            "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
+            "kata_sync_status")
 
 _lib = None
 
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.kata_decode_step.restype = i
         L.kata_lift.argtypes = [p, p, ctypes.c_int64, i, i, vp]
         L.kata_lift.restype = i
+        L.kata_sync_status.argtypes = [vp]
+        L.kata_sync_status.restype = i
         L.kata_trace_begin.argtypes = []
         L.kata_trace_begin.restype = i
         L.kata_trace_end.argtypes = [ctypes.POINTER(TraceStage), i, ctypes.POINTER(i)]
@@ -206,3 +209,8 @@ def kata_trace_end() -> dict:
     _check(lib().kata_trace_end(buf, 64, ctypes.byref(n)), "kata_trace_end")
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
             for i in range(min(n.value, 64))}
+
+
+def kata_sync_status(stream=None) -> int:
+    """Wait for the stream; KATA_ERR_TIMEOUT if a device-side bounded wait expired."""
+    return int(lib().kata_sync_status(_stream_handle(stream, None)))

@@ -218,6 +218,16 @@ int kata_decode_step(float *state, float *z, const void *q, const void *k, const
     return KATA_OK;
 }
 
+int kata_sync_status(kata_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    const int e = kata::tc_take_error();
+    if (e < 0) return KATA_ERR_CUDA;
+    return e ? KATA_ERR_TIMEOUT : KATA_OK;
+}
+
 int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype, kata_stream_t stream) {
     if (!x || !phi || rows < 1 || d < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
     if (d > 64) return KATA_ERR_UNSUPPORTED;

@@ -64,6 +64,9 @@ cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const 
                          void *out, void *workspace, cudaStream_t stream);
 cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
                         cudaStream_t stream);
+// Exclusive prefix in place along axis 1 of data[BH][n][E] (fp32).
+cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
+                                  cudaStream_t stream);
 
 // ---- decode: kata_decode.cu -----------------------------------------------
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
@@ -74,5 +77,8 @@ bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
 size_t tc_workspace_bytes(const FwdShape &s, int num_sms);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
                        void *out, void *workspace, int num_sms, cudaStream_t stream);
+// Reads and clears the sticky device error word of the tensor-core kernels
+// (nonzero: a bounded wait expired); -1 if it could not be read.
+int tc_take_error();
 
 }  // namespace kata

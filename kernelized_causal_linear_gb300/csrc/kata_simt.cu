@@ -243,10 +243,8 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
             k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft);
     }
     const int64_t E = (int64_t)n * (s.dv + 1);
-    {
-        TraceScope tr("simt_scan", stream);
-        scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(st, NC, E);
-    }
+    cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream);
+    if (e != cudaSuccess) return e;
 
     const size_t sm3 = sizeof(float) *
                        (size_t)(2 * s.d * s.C + s.C * kStride + kStageRows * kStride);
@@ -261,6 +259,13 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
 }
 
 }  // namespace
+
+cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
+                                  cudaStream_t stream) {
+    TraceScope tr(stage, stream);
+    scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(data, n, E);
+    return cudaGetLastError();
+}
 
 size_t simt_workspace_bytes(const FwdShape &s) {
     return sizeof(float) * (size_t)s.BH() * (size_t)s.NC() * (size_t)s.n() *

@@ -140,3 +140,19 @@ def test_full_size_sampled_rows(kg, name):
         got = to_f64(of[hi][flat])
         worst = max(worst, slice_rel_err(got, ref))
     assert worst <= TOL[w.dtype], f"{name}: {worst:.3e}"
+
+
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # many one-chunk segments (segment-state kernel + scan)
+    (16, 8, 700),    # 128 heads: a single segment of 6 chunks per head
+    (8, 8, 1000),    # 64 heads: 2 segments of 4 chunks, ragged tail
+    (4, 8, 4096),    # 32 heads: 4 segments of 8 chunks
+    (1, 1, 129),     # 1 head: 2 chunks, second has one token
+    (3, 1, 5),       # a single partial chunk
+])
+def test_tensor_path_segmentation(kg, B, H, T):
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+    assert kg.kata_sync_status() == kg.KATA_OK

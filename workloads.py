@@ -136,8 +136,10 @@ def make_decode_prefix(w: Workload = DECODE, length: int = 16, device="cpu"):
 
 
 def make_decode_state_fill(w: Workload = DECODE, device="cpu"):
-    """A seeded fp32 state (S [B,H,n,dv], z [B,H,n]) for timing the decode step:
-    S ~ N(0,1), z ~ |N(0,1)| + 1 (content does not change the cost)."""
+    """A seeded fp32 state (S [B,H,n,dv], z [B,H,n]) for timing the decode step
+    only: S ~ N(0,1), z ~ |N(0,1)| + 1.  It is not a state any token sequence
+    produces (its normaliser can be <= 0); the content does not change the
+    cost.  Parity tests build states from make_decode_prefix instead."""
     base = 1000 * w.index
     S = _randn((w.B, w.H, w.n, w.dv), device, base + 6)
     z = _randn((w.B, w.H, w.n), device, base + 7).abs_() + 1.0
