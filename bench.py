@@ -69,8 +69,18 @@ def _intra_pairs(T, C):
     return full * C * (C + 1) // 2 + tail * (tail + 1) // 2
 
 
-def stage_work(stage: str, w) -> tuple[float, str, str]:
-    """(work per launch, unit, bound) for a traced stage on workload w."""
+def tc_plan(w, num_sms: int):
+    """Segmentation the tensor path uses (mirrors plan() in csrc/kata_tc.cu):
+    128-token chunks, G segments of Lc chunks per head."""
+    nct = -(-w.T // 128)
+    G = max(1, min(num_sms // (w.B * w.H), nct))
+    Lc = -(-nct // G)
+    G = -(-nct // Lc)
+    return nct, G, Lc
+
+
+def stage_work(stage: str, w, num_sms: int = SMS):
+    """(algorithmic work per launch, unit, bound) for a traced stage on workload w."""
     BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, w.n
     NC = -(-T // C)
     state_flops = 2.0 * n * (dv + 1) * T * BH          # Psi(K)^T [V|1]
@@ -82,13 +92,26 @@ def stage_work(stage: str, w) -> tuple[float, str, str]:
         return out_inter + intra, "TFLOP/s", "alu"
     if stage == "simt_scan":
         return 2.0 * 4 * n * (dv + 1) * NC * BH, "GB/s", "hbm"
-    if stage == "tc_state":
-        return state_flops, "TFLOP/s", "tensor"
-    if stage == "tc_output":
-        return out_inter + intra + state_flops, "TFLOP/s", "tensor"
-    if stage == "tc_scan":
-        return None, "GB/s", "hbm"
+    if stage.startswith("tc_"):
+        nct, G, Lc = tc_plan(w, num_sms)
+        seg_tokens = min(T, (G - 1) * Lc * 128) * BH      # tokens in all but the last segments
+        if stage == "tc_segment_state":
+            return 2.0 * n * (dv + 1) * seg_tokens, "TFLOP/s", "tensor"
+        if stage == "tc_segment_output":
+            intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH
+            return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
+        if stage == "tc_segment_scan":
+            rec = 4.0 * (5 * 128 * dv + d * d)
+            return 2.0 * rec * G * BH, "GB/s", "hbm"
     return None, "", ""
+
+
+def call_flops(w) -> float:
+    """Algorithmic flops of one forward call at the workload's chunk size:
+    2n(dv+1) (state) + 2n(dv+1) (inter output) per token and head, plus the
+    causal intra-chunk term 2(d+dv+1) per (t, s<=t) pair inside chunks."""
+    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, w.n
+    return 4.0 * n * (dv + 1) * T * BH + 2.0 * (d + dv + 1) * _intra_pairs(T, C) * BH
 
 
 def _source_digest() -> str:
@@ -338,7 +361,7 @@ def run_ours(args):
     roofline = None
     if dom is not None:
         nl, tot = stages[dom]
-        work, unit, bound = stage_work(dom, w)
+        work, unit, bound = stage_work(dom, w, torch.cuda.get_device_properties(0).multi_processor_count)
         mean_s = tot / nl / 1e3
         if work is not None:
             if unit == "TFLOP/s":
@@ -357,7 +380,7 @@ def run_ours(args):
                         "work_per_launch": work}
     # whole-call tensor fraction (algorithmic tensor flops over the step time)
     step_s = elapsed_ms / 1e3 / args.steps
-    alg_flops = (stage_work("simt_chunk_state", w)[0] + stage_work("simt_output", w)[0])
+    alg_flops = call_flops(w)
     whole = {"algorithmic_tflops": alg_flops / step_s / 1e12,
              "frac_of_bf16_peak": alg_flops / step_s / 1e12 / peaks["bf16_tflops"]}
 

@@ -14,6 +14,7 @@ namespace kata {
 namespace sm100 {
 
 constexpr uint64_t kSpinLimitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kSpinLimitIters = 1u << 22;      // cap in case the timer does not advance
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -56,8 +57,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kSpinLimitNs) return false;
+    for (uint32_t it = 0; !mbar_try_wait(bar, parity); ++it) {
+        if (it >= kSpinLimitIters || globaltimer() - t0 > kSpinLimitNs) return false;
     }
     return true;
 }

@@ -161,6 +161,103 @@ __device__ __forceinline__ void lift_col_rt(int ac, const float (&x)[D], uint8_t
     }
 }
 
+// ---- packed bf16x2 lift: one mul.rn.bf16x2 per lifted pair.  A product of two
+// bf16 values is exact in fp32, so this rounds exactly like the fp32 lift above.
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// A row as bf16 pairs: w[m] = (x_2m, x_2m+1); so[m] = (x_2m+1, x_2m+2) with x_D = 0.
+template <int D>
+struct PackedRow {
+    uint32_t w[D / 2];
+    uint32_t so[D / 2];
+};
+
+template <int D>
+__device__ __forceinline__ void load_packed(const bf16 *__restrict__ p, int bh, int T, int tok,
+                                            PackedRow<D> &r) {
+    if (tok < T) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p + ((size_t)bh * T + tok) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 u = __ldg(src + c);
+            r.w[4 * c + 0] = u.x;
+            r.w[4 * c + 1] = u.y;
+            r.w[4 * c + 2] = u.z;
+            r.w[4 * c + 3] = u.w;
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < D / 2; ++m) r.w[m] = 0u;
+    }
+#pragma unroll
+    for (int m = 0; m < D / 2; ++m)
+        r.so[m] = __byte_perm(r.w[m], m + 1 < D / 2 ? r.w[m + 1] : 0u, 0x5432);
+}
+
+template <int D, bool KEY, int W>
+__device__ __forceinline__ uint32_t lift_word2(const PackedRow<D> &r) {
+    if constexpr (W >= Words<D>::count()) {
+        return 0u;
+    } else {
+        constexpr int I = Words<D>::row_of(W);
+        constexpr int J = Words<D>::col_of(W);
+        uint32_t pair;
+        if constexpr (J % 2 == 0) pair = r.w[J / 2];
+        else pair = r.so[(J - 1) / 2];
+        uint32_t bc = __byte_perm(r.w[I / 2], 0u, (I % 2 == 0) ? 0x1010 : 0x3232);   // (x_I, x_I)
+        if constexpr (KEY) {
+            const uint32_t bc2 = bmul2(bc, 0x40004000u);                             // (2x_I, 2x_I)
+            if constexpr (J == I) bc = __byte_perm(bc, bc2, 0x7610);                 // (x_I, 2x_I)
+            else bc = bc2;
+        }
+        return bmul2(bc, pair);
+    }
+}
+
+template <int D, bool KEY, int W0>
+__device__ __forceinline__ void lift_chunk2(const PackedRow<D> &r, uint8_t *dst) {
+    uint4 v;
+    v.x = lift_word2<D, KEY, W0 + 0>(r);
+    v.y = lift_word2<D, KEY, W0 + 1>(r);
+    v.z = lift_word2<D, KEY, W0 + 2>(r);
+    v.w = lift_word2<D, KEY, W0 + 3>(r);
+    *reinterpret_cast<uint4 *>(dst) = v;
+}
+
+template <int D, bool KEY, int AC, int... CH>
+__device__ __forceinline__ void lift_col2_impl(const PackedRow<D> &r, uint8_t *row, int t7,
+                                               std::integer_sequence<int, CH...>) {
+    (lift_chunk2<D, KEY, 32 * AC + 4 * CH>(r, row + ((CH ^ t7) << 4)), ...);
+}
+
+template <int D, bool KEY, int AC>
+__device__ __forceinline__ void lift_col2(const PackedRow<D> &r, uint8_t *tile_col, int t) {
+    lift_col2_impl<D, KEY, AC>(r, tile_col + (t >> 3) * 1024 + (t & 7) * 128, t & 7,
+                               std::make_integer_sequence<int, 8>{});
+}
+
+template <int D, bool KEY>
+__device__ __forceinline__ void lift_col2_rt(int ac, const PackedRow<D> &r, uint8_t *tile_col,
+                                             int t) {
+    switch (ac) {
+        case 0: lift_col2<D, KEY, 0>(r, tile_col, t); break;
+        case 1: lift_col2<D, KEY, 1>(r, tile_col, t); break;
+        case 2: lift_col2<D, KEY, 2>(r, tile_col, t); break;
+        case 3: lift_col2<D, KEY, 3>(r, tile_col, t); break;
+        case 4: lift_col2<D, KEY, 4>(r, tile_col, t); break;
+        case 5: lift_col2<D, KEY, 5>(r, tile_col, t); break;
+        case 6: lift_col2<D, KEY, 6>(r, tile_col, t); break;
+        case 7: lift_col2<D, KEY, 7>(r, tile_col, t); break;
+        case 8: lift_col2<D, KEY, 8>(r, tile_col, t); break;
+        case 9: lift_col2<D, KEY, 9>(r, tile_col, t); break;
+        default: break;
+    }
+}
+
 // Row `tok` of a [BH][T][D] bf16 tensor as fp32 (zeros past T).
 template <int D>
 __device__ __forceinline__ void load_row(const bf16 *__restrict__ p, int bh, int T, int tok,
@@ -604,21 +701,21 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         {
             const float den = dpart[0][row] + dpart[1][row];
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            if (t0 + row < T) {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV + half * 32);
+            // tcgen05.ld is warp-collective: every lane loads, only valid rows store
+            const bool valid = t0 + row < T;
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV + half * 32);
 #pragma unroll
-                for (int c16 = 0; c16 < 2; ++c16) {
-                    uint32_t r[16];
-                    tmem_ld16(tX + lrow + half * 32 + c16 * 16, r);
+            for (int c16 = 0; c16 < 2; ++c16) {
+                uint32_t r[16];
+                tmem_ld16(tX + lrow + half * 32 + c16 * 16, r);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * c + 0]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
-                        dst[2 * c16 + c] = v;
-                    }
+                for (int c = 0; c < 2; ++c) {
+                    uint4 v;
+                    v.x = pack_bf16(__uint_as_float(r[8 * c + 0]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
+                    v.y = pack_bf16(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
+                    v.z = pack_bf16(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
+                    v.w = pack_bf16(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
+                    if (valid) dst[2 * c16 + c] = v;
                 }
             }
             if (quarter == 0) {
