@@ -147,6 +147,9 @@ def _ncu_traffic(kernel_stage: str, workload: str):
 
 
 class ClockSampler:
+    """nvidia-smi clocks/throttle samples every 20 ms, each stamped with the
+    host time it arrived; summary() keeps the samples inside mark_start() ..
+    mark_stop() (the timed region)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -154,32 +157,48 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         self.idx = device_index
+        self.samples = []
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.samples.append((time.time(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.idx)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            self.thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for ts, l in self.samples:
+            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                continue
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -336,14 +355,16 @@ def run_ours(args):
 
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
-        time.sleep(0.3)
+        time.sleep(0.5)
         kg.kata_trace_begin()
         torch.cuda.synchronize()
+        clk.mark_start()
         start.record(stream)
         for _ in range(args.steps):
             kg.kata_fwd_chunked(q, k, v, w.C, out=out)
         stop.record(stream)
         torch.cuda.synchronize()
+        clk.mark_stop()
         stages = kg.kata_trace_end()
     if dist is not None:
         dist.barrier()
@@ -469,7 +490,7 @@ def _bench_decode(kg, peaks, args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
