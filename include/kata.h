@@ -48,8 +48,13 @@ typedef enum {
     KATA_ERR_UNSUPPORTED = -2, /* valid but unsupported shape or dtype       */
     KATA_ERR_CUDA = -3,        /* CUDA runtime error                         */
     KATA_ERR_ALLOC = -4,       /* device workspace allocation failed         */
-    KATA_ERR_TIMEOUT = -5      /* a bounded device-side wait expired         */
+    KATA_ERR_TIMEOUT = -5,     /* a bounded device-side wait expired         */
+    KATA_ERR_SCRATCH_LIMIT = -6 /* shape needs more scratch than the fixed
+                                   buffer of kata_fwd_chunked_noalloc holds    */
 } kata_status;
+
+/* Capacity of the fixed device scratch array of kata_fwd_chunked_noalloc. */
+#define KATA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /* Element types of q, k, v and out. */
 typedef enum { KATA_F32 = 0, KATA_BF16 = 1 } kata_dtype;
@@ -96,6 +101,33 @@ const char *kata_status_str(int status);
  */
 int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
                      int T, int d, int dv, int C, int dtype, kata_stream_t stream);
+
+/*
+ * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
+ * arguments, layouts, paths and results), for callers that cannot allocate
+ * device memory where they run it: code whose device memory is owned by a
+ * framework pool that forbids other allocators, hosts that must not allocate
+ * after start-up, and replays of pre-recorded GPU work that may not contain
+ * allocations.  The paper has no counterpart; this is an interface choice.
+ *
+ * It allocates nothing.  Its scratch is one fixed device array of
+ * KATA_NOALLOC_SCRATCH_BYTES (32 MiB) that is part of the library's device
+ * image; it occupies that much memory on every GPU where this entry point has
+ * run, until the process exits.  A shape whose scratch
+ * (kata_fwd_workspace_size) is larger returns KATA_ERR_SCRATCH_LIMIT before
+ * any device work: every bf16 shape of the tensor-core path fits on a 152-SM
+ * GPU; fp32 shapes fit while B*H*ceil(T/C)*n*(dv+1)*4 bytes stay under it.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address, which may load device code; make that first call
+ * before any stream capture starts.  All calls share the array and it keeps
+ * the last call's contents; no content has to start at zero, because each
+ * call writes every byte it later reads.  Calls whose work overlaps on the
+ * GPU (e.g. two streams without ordering) race on the array: order them.
+ */
+int kata_fwd_chunked_noalloc(const void *q, const void *k, const void *v, void *out, int B,
+                             int H, int T, int d, int dv, int C, int dtype,
+                             kata_stream_t stream);
 
 /* Bytes of device workspace kata_fwd_chunked allocates for this shape, written
  * to *bytes.  Same argument checks as kata_fwd_chunked; no device work. */

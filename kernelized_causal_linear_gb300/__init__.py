@@ -25,6 +25,8 @@ KATA_ERR_UNSUPPORTED = -2
 KATA_ERR_CUDA = -3
 KATA_ERR_ALLOC = -4
 KATA_ERR_TIMEOUT = -5
+KATA_ERR_SCRATCH_LIMIT = -6
+KATA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 KATA_F32 = 0
 KATA_BF16 = 1
@@ -36,7 +38,7 @@ KATA_PATH_TC = 2
 EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
-            "kata_sync_status")
+            "kata_sync_status", "kata_fwd_chunked_noalloc")
 
 _lib = None
 
@@ -77,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.kata_decode_step.restype = i
         L.kata_lift.argtypes = [p, p, ctypes.c_int64, i, i, vp]
         L.kata_lift.restype = i
+        L.kata_fwd_chunked_noalloc.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_chunked_noalloc.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
         L.kata_trace_begin.argtypes = []
@@ -136,6 +140,22 @@ def kata_fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
                                 B, H, T, d, dv, int(C), _dtype_code(q.dtype),
                                 _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_chunked")
+    return out
+
+
+def kata_fwd_chunked_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+                             out: torch.Tensor, stream=None) -> torch.Tensor:
+    """The forward without any device allocation, for callers that cannot
+    allocate where they run it: scratch comes from a fixed 32 MiB device array
+    inside the library, shared by all calls (order calls that could overlap).
+    `out` must be provided, so this function allocates nothing either."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd_chunked_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        out.data_ptr(), B, H, T, d, dv, int(C),
+                                        _dtype_code(q.dtype), _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked_noalloc")
     return out
 
 

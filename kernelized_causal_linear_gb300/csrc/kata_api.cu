@@ -94,6 +94,8 @@ const char *kata_status_str(int status) {
         case KATA_ERR_CUDA: return "CUDA runtime error";
         case KATA_ERR_ALLOC: return "device workspace allocation failed";
         case KATA_ERR_TIMEOUT: return "bounded device-side wait expired";
+        case KATA_ERR_SCRATCH_LIMIT:
+            return "shape needs more scratch than the fixed no-allocation buffer holds";
         default: return "unknown status";
     }
 }
