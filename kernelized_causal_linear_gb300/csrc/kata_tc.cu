@@ -6,10 +6,10 @@
 // segments of whole 128-token chunks, and the exclusive scan over chunks of
 // Eq. 17 (Sec. 4.2) is done at two levels:
 //
-//   1. seg_state_kernel   per (feature block, segment, head): the segment's
-//                         state sum Psi(K)^T V over all its chunks (tcgen05,
-//                         fp32 accumulator in TMEM) and its key Gram matrix
-//                         K^T K.                                       [Eq. 17]
+//   1. seg_state_kernel   per (segment, head): the segment's state sum
+//                         Psi(K)^T V over all its chunks (tcgen05, fp32
+//                         accumulators in TMEM) and its key Gram matrix K^T K.
+//                                                                      [Eq. 17]
 //   2. exclusive scan     of the segment states over segments (CUDA cores).
 //   3. seg_output_kernel  per (segment, head): starts from the segment's prefix
 //                         state, held in TMEM in fp32, and walks its chunks:
@@ -21,6 +21,11 @@
 //                         all contractions on tcgen05 with operands in shared
 //                         memory (TMA-fed for q, k, v tiles) and accumulators
 //                         in TMEM.
+//
+// Both tensor kernels are warp-specialised: one warp issues TMA copies, one
+// issues MMAs (one thread), and the other warps lift features, build P and
+// convert accumulators; they hand buffers to each other through mbarriers, so
+// the tensor pipe never waits on a __syncthreads.
 //
 // Normaliser.  Z = sum psi(k) is kept as the unpacked d x d matrix
 // G = sum k k^T: psi(q).Z = <q q^T, G>_F = q^T G q (Sec. 3.1 Frobenius
@@ -90,76 +95,12 @@ struct Cfg {
     static constexpr int NW = Words<D>::count();       // bf16 pairs per lifted row
     static constexpr int NF = 2 * NW;                  // padded feature count
     static constexpr int NBLK = (NF + 127) / 128;      // 128-feature state blocks
-    static constexpr int NAC = 2 * NBLK;               // 64-feature atom columns
     static constexpr int QK_ROW = D * 2;               // bytes per q/k row
     static constexpr int V_ROW = DV * 2;
     static constexpr int QK_TILE = kTile * QK_ROW;
     static constexpr int V_TILE = kTile * V_ROW;
     static constexpr int E = NBLK * 128 * DV + D * D;  // floats per segment record
-    static constexpr uint32_t QK_SW = QK_ROW == 128 ? kSw128 : QK_ROW == 64 ? kSw64 : kSw32;
 };
-
-// One lifted bf16 pair (features 2W, 2W+1) of one row x.
-template <int D, bool KEY, int W>
-__device__ __forceinline__ uint32_t lift_word(const float (&x)[D]) {
-    if constexpr (W >= Words<D>::count()) {
-        return 0u;
-    } else {
-        constexpr int I = Words<D>::row_of(W);
-        constexpr int J = Words<D>::col_of(W);
-        float lo = x[I] * x[J];
-        float hi = 0.f;
-        if constexpr (J + 1 < D) hi = x[I] * x[J + 1];
-        if constexpr (KEY) {
-            if constexpr (J != I) lo *= 2.f;
-            hi *= 2.f;
-        }
-        return pack_bf16(lo, hi);
-    }
-}
-
-template <int D, bool KEY, int W0>
-__device__ __forceinline__ void lift_chunk(const float (&x)[D], uint8_t *dst) {
-    uint4 v;
-    v.x = lift_word<D, KEY, W0 + 0>(x);
-    v.y = lift_word<D, KEY, W0 + 1>(x);
-    v.z = lift_word<D, KEY, W0 + 2>(x);
-    v.w = lift_word<D, KEY, W0 + 3>(x);
-    *reinterpret_cast<uint4 *>(dst) = v;
-}
-
-// Lift one token row into one 64-feature atom column AC of a [128 x 64] SW128
-// tile: row t, 8 chunks of 8 features, chunk c stored at chunk (c ^ (t % 8)).
-template <int D, bool KEY, int AC, int... CH>
-__device__ __forceinline__ void lift_col_impl(const float (&x)[D], uint8_t *row, int t7,
-                                              std::integer_sequence<int, CH...>) {
-    (lift_chunk<D, KEY, 32 * AC + 4 * CH>(x, row + ((CH ^ t7) << 4)), ...);
-}
-
-template <int D, bool KEY, int AC>
-__device__ __forceinline__ void lift_col(const float (&x)[D], uint8_t *tile_col, int t) {
-    lift_col_impl<D, KEY, AC>(x, tile_col + (t >> 3) * 1024 + (t & 7) * 128, t & 7,
-                              std::make_integer_sequence<int, 8>{});
-}
-
-// Runtime atom-column dispatch (ac < 2 * NBLK).
-template <int D, bool KEY>
-__device__ __forceinline__ void lift_col_rt(int ac, const float (&x)[D], uint8_t *tile_col,
-                                            int t) {
-    switch (ac) {
-        case 0: lift_col<D, KEY, 0>(x, tile_col, t); break;
-        case 1: lift_col<D, KEY, 1>(x, tile_col, t); break;
-        case 2: lift_col<D, KEY, 2>(x, tile_col, t); break;
-        case 3: lift_col<D, KEY, 3>(x, tile_col, t); break;
-        case 4: lift_col<D, KEY, 4>(x, tile_col, t); break;
-        case 5: lift_col<D, KEY, 5>(x, tile_col, t); break;
-        case 6: lift_col<D, KEY, 6>(x, tile_col, t); break;
-        case 7: lift_col<D, KEY, 7>(x, tile_col, t); break;
-        case 8: lift_col<D, KEY, 8>(x, tile_col, t); break;
-        case 9: lift_col<D, KEY, 9>(x, tile_col, t); break;
-        default: break;
-    }
-}
 
 // ---- packed bf16x2 lift: one mul.rn.bf16x2 per lifted pair.  A product of two
 // bf16 values is exact in fp32, so this rounds exactly like the fp32 lift above.
@@ -258,26 +199,25 @@ __device__ __forceinline__ void lift_col2_rt(int ac, const PackedRow<D> &r, uint
     }
 }
 
-// Row `tok` of a [BH][T][D] bf16 tensor as fp32 (zeros past T).
+// Row t of a [128 x D] bf16 tile written by TMA with the swizzle matching its
+// row width (32/64/128 bytes): the 16-byte chunk c of row t sits at chunk
+// c ^ ((t * row_bytes >> 7) & (chunks_per_row - 1)).
 template <int D>
-__device__ __forceinline__ void load_row(const bf16 *__restrict__ p, int bh, int T, int tok,
-                                         float (&x)[D]) {
-    if (tok < T) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p + ((size_t)bh * T + tok) * D);
+__device__ __forceinline__ void tile_row_packed(const uint8_t *tile, int t, PackedRow<D> &r) {
+    constexpr int RB = D * 2, CPR = RB / 16;
+    const uint8_t *row = tile + t * RB;
+    const int x = (t * RB >> 7) & (CPR - 1);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 u = __ldg(src + c);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[8 * c + 2 * e] = __uint_as_float(w[e] << 16);
-                x[8 * c + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < D; ++i) x[i] = 0.f;
+    for (int c = 0; c < CPR; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(row + ((c ^ x) << 4));
+        r.w[4 * c + 0] = u.x;
+        r.w[4 * c + 1] = u.y;
+        r.w[4 * c + 2] = u.z;
+        r.w[4 * c + 3] = u.w;
     }
+#pragma unroll
+    for (int m = 0; m < D / 2; ++m)
+        r.so[m] = __byte_perm(r.w[m], m + 1 < D / 2 ? r.w[m + 1] : 0u, 0x5432);
 }
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -287,463 +227,594 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 __device__ __forceinline__ void flag_error(int code) { atomicOr(&g_tc_error, code); }
 
+// Shared abort flag: any role whose bounded wait expires sets it; every later
+// wait then returns at once, so all roles drain to the final barrier.
+struct Sync {
+    volatile int *abort;
+    __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t n) const {
+        if (*abort) return false;
+        if (mbar_wait(bar, n & 1u)) return true;
+        *abort = 1;
+        return false;
+    }
+};
+
+__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
+
 // ================================================================= kernel 1
-// Segment state: S_seg[blk] = sum over the segment's tokens of psi_k(k)[blk] v^T
-// (128 features x DV, fp32 in TMEM), and for blk 0 also G_seg = K^T K.
+// Segment state of one (segment, head): S_seg = sum over the segment's tokens of
+// psi_k(k) v^T (all feature blocks, fp32 in TMEM) and G_seg = K^T K.
+//   warp 0: TMA (K and V tiles, 2 stages)      warp 1: MMA issue
+//   warps 2-5: key lift into a 3-stage ring, then the epilogue
 template <int D, int DV>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(192, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const bf16 *__restrict__ k, float *__restrict__ seg, int T, int NCt, int Lc,
-                 int G) {
+                 float *__restrict__ seg, int NCt, int Lc, int G) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32, "layouts below are written for d = 32, dv = 64");
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align1024(smem_raw);
     constexpr int kStage = C::QK_TILE + C::V_TILE;
-    uint8_t *phiK = sm + 2 * kStage;
-    __shared__ __align__(8) uint64_t bar_tile[2];
-    __shared__ __align__(8) uint64_t bar_mma;
-    __shared__ uint32_t tmem_base;
-
-    const int blk = blockIdx.x, g = blockIdx.y, bh = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c0 = g * Lc;
-    const int nch = min(NCt, c0 + Lc) - c0;
-
-    if (tid == 0) {
-        mbar_init(&bar_tile[0], 1);
-        mbar_init(&bar_tile[1], 1);
-        mbar_init(&bar_mma, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&tmem_base, 128);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tS = tmem_base, tG = tmem_base + 64;
-    constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
-    constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
-
-    auto issue_tile = [&](int i) {
-        const int st = i & 1;
-        uint8_t *tk = sm + st * kStage, *tv = tk + C::QK_TILE;
-        const int t0 = (c0 + i) * kTile;
-        mbar_arrive_expect_tx(&bar_tile[st], C::V_TILE + (blk == 0 ? C::QK_TILE : 0));
-        if (blk == 0) tma_load_3d(tk, &tm_k, 0, t0, bh, &bar_tile[st]);
-        tma_load_3d(tv, &tm_v, 0, t0, bh, &bar_tile[st]);
-    };
-    if (tid == 0) {
-        issue_tile(0);
-        if (nch > 1) issue_tile(1);
-    }
-
-    bool ok = true;
-    int issued = 0;
-#pragma unroll 1
-    for (int i = 0; i < nch; ++i) {
-        const int st = i & 1;
-        if (i >= 1) {
-            ok = ok && mbar_wait(&bar_mma, (i - 1) & 1);     // chunk i-1's MMAs done
-            if (tid == 0 && ok && i + 1 < nch) issue_tile(i + 1);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float x[D];
-            load_row<D>(k, bh, T, (c0 + i) * kTile + tid, x);
-            lift_col_rt<D, true>(2 * blk + h, x, phiK + h * 16384, tid);
-            asm volatile("" ::: "memory");
-        }
-        fence_proxy_async_smem();
-        ok = ok && mbar_wait(&bar_tile[st], (i >> 1) & 1);
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 0) {
-            const uint32_t tv = smem_u32(sm + st * kStage + C::QK_TILE);
-            const uint32_t pk = smem_u32(phiK);
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t a = smem_desc(pk + ks * 2048, 16384, 1024, kSw128);
-                const uint64_t b = smem_desc(tv + ks * 2048, 16384, 1024, kSw128);
-                mma_ss(tS, a, b, kIdState, (i > 0 || ks > 0) ? 1u : 0u);
-            }
-            if (blk == 0) {
-                const uint32_t tk = smem_u32(sm + st * kStage);
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t a = smem_desc(tk + ks * 1024, 8192, 512, kSw64);
-                    mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
-                }
-            }
-            mma_commit(&bar_mma);
-        }
-        ++issued;
-    }
-    if (issued > 0) ok = mbar_wait(&bar_mma, (issued - 1) & 1) && ok;
-    tc_fence_after();
-    ok = __syncthreads_and(ok);
-    if (!ok) {
-        if (tid == 0) flag_error(1);
-    } else {
-        // state rows: TMEM lane = feature (blk*128 + lane), 64 fp32 columns
-        float *dst = seg + ((size_t)bh * G + g) * C::E + (size_t)(blk * 128 + warp * 32 + lane) * DV;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-#pragma unroll
-        for (int c = 0; c < DV; c += 16) {
-            uint32_t r[16];
-            tmem_ld16(tS + lrow + c, r);
-            float4 *d4 = reinterpret_cast<float4 *>(dst + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                d4[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                    __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
-        }
-        if (blk == 0 && warp == 0) {   // Gram rows 0..D-1 live in lanes 0..D-1
-            float *gd = seg + ((size_t)bh * G + g) * C::E + (size_t)C::NBLK * 128 * DV +
-                        (size_t)lane * D;
-#pragma unroll
-            for (int c = 0; c < D; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tG + c, r);
-                float4 *d4 = reinterpret_cast<float4 *>(gd + c);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    d4[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                        __uint_as_float(r[4 * e + 2]),
-                                        __uint_as_float(r[4 * e + 3]));
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem_base, 128);
-}
-
-// ================================================================= kernel 3
-// Segment output: walk the segment's chunks with the running state in TMEM.
-template <int D, int DV>
-__global__ void __launch_bounds__(256, 1)
-seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const bf16 *__restrict__ q,
-                  const bf16 *__restrict__ k, bf16 *__restrict__ out,
-                  const float *__restrict__ seg, int T, int NCt, int Lc, int G) {
-    using C = Cfg<D, DV>;
-    static_assert(DV == 64 && D == 32, "layouts below are written for d = 32, dv = 64");
+    constexpr int kRing = 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
-    constexpr int kStage = 2 * C::QK_TILE + C::V_TILE;     // Q, K, V tiles of one chunk
-    uint8_t *phiQ = sm + 2 * kStage;                         // [2][32 KB]; phiQ[1] also holds P
-    uint8_t *phiK = phiQ + 2 * 32768;                        // [2][32 KB]
-    uint8_t *spre = phiK + 2 * 32768;                        // 16 KB: S_pre block, bf16
-    uint8_t *gram = spre + 16384;                            // 2 KB: G_pre, bf16, SW64
-    __shared__ __align__(8) uint64_t bar_tile[2];
-    __shared__ __align__(8) uint64_t bar_qk, bar_pv;
-    __shared__ __align__(8) uint64_t bar_blk[2];
+    uint8_t *ring = sm + 2 * kStage;                     // [kRing][32 KB]: psi_k block
+    __shared__ __align__(8) uint64_t tile_full[2], tile_empty[2], lift_full[kRing],
+        lift_empty[kRing], done_bar;
     __shared__ uint32_t tmem_base;
-    __shared__ float dpart[2][kTile];
+    __shared__ int abort_flag;
 
     const int g = blockIdx.x, bh = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;          // TMEM lane / tile row owned by this thread
-    const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
+    const Sync sy{&abort_flag};
 
-    if (tid == 0) {
-        mbar_init(&bar_tile[0], 1);
-        mbar_init(&bar_tile[1], 1);
-        mbar_init(&bar_qk, 1);
-        mbar_init(&bar_pv, 1);
-        mbar_init(&bar_blk[0], 1);
-        mbar_init(&bar_blk[1], 1);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tile_full[i], 1);
+            mbar_init(&tile_empty[i], 1 + 4);        // MMA commit + 4 lift warps
+        }
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&lift_full[i], 4);
+            mbar_init(&lift_empty[i], 1);
+        }
+        mbar_init(&done_bar, 1);
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base;          // [NBLK][DV] fp32 running state
-    const uint32_t tG = tmem_base + 320;    // D cols: running Gram (lanes 0..D-1)
-    const uint32_t tQG = tmem_base + 352;   // D cols: Q G_pre
-    const uint32_t tX = tmem_base + 384;    // 128 cols: Q K^T, then the output accumulator
+    const uint32_t tS = tmem_base, tG = tmem_base + C::NBLK * DV;
 
-    // ---- initial state: exclusive prefix of the segment states (zero for g == 0)
-    {
-        const float *pre = seg + ((size_t)bh * G + g) * C::E;
-        for (int blk = 0; blk < C::NBLK; ++blk) {
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (elect_lane0()) {
+            for (int i = 0; i < nch; ++i) {
+                const int st = i & 1, use = i >> 1;
+                if (use >= 1 && !sy.wait(&tile_empty[st], use - 1)) break;
+                uint8_t *tk = sm + st * kStage;
+                const int t0 = (c0 + i) * kTile;
+                mbar_arrive_expect_tx(&tile_full[st], kStage);
+                tma_load_3d(tk, &tm_k, 0, t0, bh, &tile_full[st]);
+                tma_load_3d(tk + C::QK_TILE, &tm_v, 0, t0, bh, &tile_full[st]);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issue
+        if (elect_lane0()) {
+            constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
+            constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i & 1;
+                ok = sy.wait(&tile_full[st], i >> 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tk = smem_u32(sm + st * kStage), tv = tk + C::QK_TILE;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-                uint32_t r[8];
-                if (g > 0) {
-                    const float4 *s4 = reinterpret_cast<const float4 *>(
-                        pre + (size_t)(blk * 128 + row) * DV + half * 32 + c);
-                    const float4 a = s4[0], b = s4[1];
-                    r[0] = __float_as_uint(a.x); r[1] = __float_as_uint(a.y);
-                    r[2] = __float_as_uint(a.z); r[3] = __float_as_uint(a.w);
-                    r[4] = __float_as_uint(b.x); r[5] = __float_as_uint(b.y);
-                    r[6] = __float_as_uint(b.z); r[7] = __float_as_uint(b.w);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) r[e] = 0u;
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                    const uint64_t a = smem_desc(tk + ks * 1024, 8192, 512, kSw64);
+                    mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
                 }
-                tmem_st8(tS + lrow + blk * DV + half * 32 + c, r);
+                for (int b = 0; b < C::NBLK && ok; ++b) {
+                    const int gb = i * C::NBLK + b, rs = gb % kRing;
+                    ok = sy.wait(&lift_full[rs], gb / kRing);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pk = smem_u32(ring + rs * 32768);
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ss(tS + b * DV, smem_desc(pk + ks * 2048, 16384, 1024, kSw128),
+                               smem_desc(tv + ks * 2048, 16384, 1024, kSw128), kIdState,
+                               (i > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&lift_empty[rs]);
+                }
+                mma_commit(&tile_empty[st]);
+            }
+            mma_commit(&done_bar);
+        }
+    } else {
+        // ---------------- lift warps (2..5): token t = 32*(warp-2) + lane
+        const int t = (warp - 2) * 32 + lane;
+        bool ok = true;
+        for (int i = 0; i < nch && ok; ++i) {
+            const int st = i & 1;
+            ok = __all_sync(0xffffffffu, sy.wait(&tile_full[st], i >> 1));
+            if (!ok) break;
+            PackedRow<D> r;
+            tile_row_packed<D>(sm + st * kStage, t, r);
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&tile_empty[st]);
+            for (int b = 0; b < C::NBLK && ok; ++b) {
+                const int gb = i * C::NBLK + b, rs = gb % kRing, use = gb / kRing;
+                if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[rs], use - 1));
+                if (!ok) break;
+                uint8_t *dst = ring + rs * 32768;
+                lift_col2_rt<D, true>(2 * b, r, dst, t);
+                lift_col2_rt<D, true>(2 * b + 1, r, dst + 16384, t);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (elect_lane0()) mbar_arrive(&lift_full[rs]);
             }
         }
-        if (quarter == 0) {   // Gram rows i = lane, columns 16*half .. 16*half+15
-            float gv[16];
+        // ---------------- epilogue: state rows and Gram rows to the segment record
+        ok = __all_sync(0xffffffffu, sy.wait(&done_bar, 0));
+        tc_fence_after();
+        if (ok) {
+            const int quarter = warp & 3;
+            const int lrow = quarter * 32 + lane;
+            const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+            float *rec = seg + ((size_t)bh * G + g) * C::E;
+            for (int b = 0; b < C::NBLK; ++b) {
+                float *dst = rec + (size_t)(b * 128 + lrow) * DV;
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                gv[e] = g > 0 ? pre[(size_t)C::NBLK * 128 * DV + lane * D + half * 16 + e] : 0.f;
+                for (int c = 0; c < DV; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tS + lsel + b * DV + c, v);
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
-            for (int c = 0; c < 16; c += 8) {
-                uint32_t r[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(gv[c + e]);
-                tmem_st8(tG + lrow + half * 16 + c, r);
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                }
             }
-            // bf16 copy for the Q G MMA: [D rows][D] K-major, 64-byte swizzle
+            if (quarter == 0) {   // Gram rows 0..D-1 are TMEM lanes 0..D-1
+                float *gd = rec + (size_t)C::NBLK * 128 * DV + (size_t)lane * D;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int chunk = 2 * half + cc;
-                uint4 v;
-                v.x = pack_bf16(gv[8 * cc + 0], gv[8 * cc + 1]);
-                v.y = pack_bf16(gv[8 * cc + 2], gv[8 * cc + 3]);
-                v.z = pack_bf16(gv[8 * cc + 4], gv[8 * cc + 5]);
-                v.w = pack_bf16(gv[8 * cc + 6], gv[8 * cc + 7]);
-                *reinterpret_cast<uint4 *>(gram + (lane >> 3) * 512 + (lane & 7) * 64 +
-                                           ((chunk ^ ((lane >> 1) & 3)) << 4)) = v;
+                for (int c = 0; c < D; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tG + lsel + c, v);
+                    float4 *d4 = reinterpret_cast<float4 *>(gd + c);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                }
             }
         }
-        tmem_st_wait();
-        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) flag_error(1);
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// ================================================================= kernel 3
+// Segment output: walk the segment's chunks with the running state in TMEM.
+//   warp 0: TMA (Q, K tiles: 1 stage; V tile: 2 stages)     warp 1: MMA issue
+//   warps 2-5 ("TMEM warps", lane quarter = warp % 4): P = (QK^T)^2 masked,
+//     denominators, S_run -> S_pre conversion, output epilogue, Gram -> bf16
+//   warps 6-9: query/key lift into a 2-stage ring
+// TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | QK^T half [384,448) |
+//       output accumulator [448,512)
+template <int D, int DV>
+__global__ void __launch_bounds__(320, 1)
+seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
+                  const float *__restrict__ seg, int T, int NCt, int Lc, int G) {
+    using C = Cfg<D, DV>;
+    static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
+    constexpr int NB = C::NBLK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *tq = sm;                                   // Q tile, 8 KB (64-byte swizzle)
+    uint8_t *tk = sm + C::QK_TILE;                      // K tile, 8 KB
+    uint8_t *tv = sm + 2 * C::QK_TILE;                  // V tiles [2][16 KB]
+    uint8_t *lring = tv + 2 * C::V_TILE;                // [2][psi_q 32 KB | psi_k 32 KB]
+    uint8_t *pbuf = lring + 2 * 65536;                  // P half, 16 KB
+    uint8_t *spre = pbuf + 16384;                       // S_pre block, 16 KB
+    uint8_t *gram = spre + 16384;                       // G_pre bf16, 2 KB
+    __shared__ __align__(8) uint64_t qk_full, qk_empty, v_full[2], v_empty[2], xs_full, xs_empty,
+        p_full, p_empty, lift_full[2], lift_empty[2], spre_full, spre_empty, state_done[NB],
+        o_full, o_empty, gram_done, gram_ready, fin_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int g = blockIdx.x, bh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = g * Lc;
+    const int nch = min(NCt, c0 + Lc) - c0;
+    const Sync sy{&abort_flag};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&qk_full, 1);
+        mbar_init(&qk_empty, 1 + 4 + 4);   // MMA commit, 4 lift warps, 4 TMEM warps
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&lift_full[i], 4);
+            mbar_init(&lift_empty[i], 1);
+        }
+        mbar_init(&xs_full, 1);
+        mbar_init(&xs_empty, 4);
+        mbar_init(&p_full, 4);
+        mbar_init(&p_empty, 1);
+        mbar_init(&spre_full, 4);
+        mbar_init(&spre_empty, 1);
+        for (int b = 0; b < NB; ++b) mbar_init(&state_done[b], 1);
+        mbar_init(&o_full, 1);
+        mbar_init(&o_empty, 4);
+        mbar_init(&gram_done, 1);
+        mbar_init(&gram_ready, 4);
+        mbar_init(&fin_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const uint32_t tS = tmem_base, tG = tmem_base + 320, tQG = tmem_base + 352;
+    const uint32_t tXs = tmem_base + 384, tXo = tmem_base + 448;
 
-    auto issue_tile = [&](int i) {
-        const int st = i & 1;
-        uint8_t *tq = sm + st * kStage;
-        const int t0 = (c0 + i) * kTile;
-        mbar_arrive_expect_tx(&bar_tile[st], kStage);
-        tma_load_3d(tq, &tm_q, 0, t0, bh, &bar_tile[st]);
-        tma_load_3d(tq + C::QK_TILE, &tm_k, 0, t0, bh, &bar_tile[st]);
-        tma_load_3d(tq + 2 * C::QK_TILE, &tm_v, 0, t0, bh, &bar_tile[st]);
-    };
-    if (tid == 0) {
-        issue_tile(0);
-        if (nch > 1) issue_tile(1);
-    }
-
-    constexpr int kEvenBlocks = (C::NBLK + 1) / 2, kOddBlocks = C::NBLK / 2;
-    constexpr uint32_t kIdQK = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t kIdQG = idesc_bf16(128, D, false, false);
-    constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
-    constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
-    constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
-
-    bool ok = true;
-#pragma unroll 1
-    for (int i = 0; i < nch && ok; ++i) {
-        const int st = i & 1;
-        const int t0 = (c0 + i) * kTile;
-        uint8_t *tq = sm + st * kStage;
-        uint8_t *tk = tq + C::QK_TILE;
-        uint8_t *tv = tk + C::QK_TILE;
-        ok = mbar_wait(&bar_tile[st], (i >> 1) & 1);
-        if (tid == 0 && ok) {
-            const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), ag = smem_u32(gram);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                mma_ss(tX, smem_desc(aq + ks * 32, 16, 512, kSw64),
-                       smem_desc(ak + ks * 32, 16, 512, kSw64), kIdQK, ks > 0);
-                mma_ss(tQG, smem_desc(aq + ks * 32, 16, 512, kSw64),
-                       smem_desc(ag + ks * 32, 16, 512, kSw64), kIdQG, ks > 0);
+    if (warp == 0) {
+        // ================= TMA producer
+        if (elect_lane0()) {
+            for (int i = 0; i < nch; ++i) {
+                const int t0 = (c0 + i) * kTile;
+                if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
+                mbar_arrive_expect_tx(&qk_full, 2 * C::QK_TILE);
+                tma_load_3d(tq, &tm_q, 0, t0, bh, &qk_full);
+                tma_load_3d(tk, &tm_k, 0, t0, bh, &qk_full);
+                const int st = i & 1, use = i >> 1;
+                if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
+                mbar_arrive_expect_tx(&v_full[st], C::V_TILE);
+                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, bh, &v_full[st]);
             }
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t a = smem_desc(ak + ks * 1024, 8192, 512, kSw64);
-                mma_ss(tG, a, a, kIdGram, 1u);
-            }
-            mma_commit(&bar_qk);
         }
-        ok = mbar_wait(&bar_qk, i & 1) && ok;
-        tc_fence_after();
-
-        // ---- intra-chunk weights: P = (Q K^T)^2 on s <= t, bf16, into phiQ[1]
-        float dacc = 0.f;
-        {
-            uint8_t *prow = phiQ + 32768 + half * 16384 + (row >> 3) * 1024 + (row & 7) * 128;
+    } else if (warp == 1) {
+        // ================= MMA issue
+        if (elect_lane0()) {
+            constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t kIdQG = idesc_bf16(128, D, false, false);
+            constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
+            constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
+            constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
+            const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), ag = smem_u32(gram);
+            const uint32_t ap = smem_u32(pbuf), as = smem_u32(spre);
+            auto qk_half = [&](int h) {   // Xs = Q K[64h .. 64h+63]^T
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tX + lrow + half * 64 + c, r);
-                float w[16];
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tXs, smem_desc(aq + ks * 32, 16, 512, kSw64),
+                           smem_desc(ak + h * 64 * 64 + ks * 32, 16, 512, kSw64), kIdQK, ks > 0);
+                mma_commit(&xs_full);
+            };
+            auto pv_half = [&](int h, uint32_t bv) {   // Xo += P[:, 64h..] V[64h..]
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int s = half * 64 + c + e;
-                    const float xv = __uint_as_float(r[e]);
-                    w[e] = (s <= row) ? xv * xv : 0.f;
-                    dacc += w[e];
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ss(tXo, smem_desc(ap + ks * 32, 16, 1024, kSw128),
+                           smem_desc(bv + (h * 4 + ks) * 2048, 16384, 1024, kSw128), kIdPV, 1u);
+                mma_commit(&p_empty);
+            };
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i & 1;
+                const uint32_t bv = smem_u32(tv + st * C::V_TILE);
+                // S/G pieces that need only the Q, K tiles
+                ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i) &&
+                     (i == 0 || sy.wait(&xs_empty, 2 * i - 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tQG, smem_desc(aq + ks * 32, 16, 512, kSw64),
+                           smem_desc(ag + ks * 32, 16, 512, kSw64), kIdQG, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                    const uint64_t a = smem_desc(ak + ks * 1024, 8192, 512, kSw64);
+                    mma_ss(tG, a, a, kIdGram, 1u);
                 }
+                mma_commit(&gram_done);
+                qk_half(0);
+                ok = sy.wait(&v_full[st], i >> 1);
+                for (int b = 0; b < NB && ok; ++b) {
+                    const int gb = i * NB + b, ls = gb & 1;
+                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full, gb) &&
+                         (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t lq = smem_u32(lring + ls * 65536), lk = lq + 32768;
+                    const int fleft = C::NF - b * 128;
+                    const int ksteps = fleft >= 128 ? 8 : (fleft + 15) / 16;
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        mma_ss(tXo, smem_desc(lq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128),
+                               smem_desc(as + ks * 2048, 16384, 1024, kSw128), kIdPV,
+                               (b > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&spre_empty);
+                    if (b == NB - 1) mma_commit(&o_full);
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ss(tS + b * DV, smem_desc(lk + ks * 2048, 16384, 1024, kSw128),
+                               smem_desc(bv + ks * 2048, 16384, 1024, kSw128), kIdState, 1u);
+                    mma_commit(&lift_empty[ls]);
+                    mma_commit(&state_done[b]);
+                    if (b == 0) {
+                        // second half of Q K^T once the first has been read, then P V for it
+                        ok = sy.wait(&xs_empty, 2 * i);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk_half(1);
+                        mma_commit(&qk_empty);
+                        ok = sy.wait(&p_full, 2 * i);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv_half(0, bv);
+                    }
+                    if (b == 2) {
+                        ok = sy.wait(&p_full, 2 * i + 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv_half(1, bv);
+                    }
+                }
+                mma_commit(&v_empty[st]);
+            }
+            mma_commit(&fin_bar);
+            sy.wait(&fin_bar, 0);
+        }
+    } else if (warp < 6) {
+        // ================= TMEM warps: lane quarter q owns rows / features 32q..32q+31
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        bool ok = true;
+        auto convert_spre = [&](int i, int b) -> bool {   // S_run block b -> spre (bf16)
+            const int gb = i * NB + b;
+            bool w = (gb == 0 || sy.wait(&spre_empty, gb - 1)) && (i == 0 || sy.wait(&state_done[b], i - 1));
+            w = __all_sync(0xffffffffu, w);
+            if (!w) return false;
+            tc_fence_after();
+            uint8_t *srow = spre + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < DV; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tS + lsel + b * DV + c, v);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int chunk = (c >> 3) + h2;
-                    uint4 v;
-                    v.x = pack_bf16(w[8 * h2 + 0], w[8 * h2 + 1]);
-                    v.y = pack_bf16(w[8 * h2 + 2], w[8 * h2 + 3]);
-                    v.z = pack_bf16(w[8 * h2 + 4], w[8 * h2 + 5]);
-                    v.w = pack_bf16(w[8 * h2 + 6], w[8 * h2 + 7]);
-                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ (row & 7)) << 4)) = v;
-                }
-            }
-            // inter-chunk denominator: q^T G_pre q, columns 16*half.. of Q G_pre
-            float xq[D];
-            load_row<D>(q, bh, T, t0 + row, xq);
-            uint32_t r[16];
-            tmem_ld16(tQG + lrow + half * 16, r);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) dacc = fmaf(__uint_as_float(r[e]), xq[half * 16 + e], dacc);
-            dpart[half][row] = dacc;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        if (tid == 0 && ok) {
-            const uint32_t ap = smem_u32(phiQ + 32768), bv = smem_u32(tv);
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ss(tX, smem_desc(ap + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128),
-                       smem_desc(bv + ks * 2048, 16384, 1024, kSw128), kIdPV, ks > 0);
-            mma_commit(&bar_pv);
-        }
-
-        // ---- feature blocks: O += Psi(Q)[blk] S_pre[blk];  S[blk] += Psi(K)[blk]^T V
-#pragma unroll 1
-        for (int blk = 0; blk < C::NBLK && ok; ++blk) {
-            const int sb = blk & 1;
-            // bar_blk[0] completes for even blocks, bar_blk[1] for odd ones
-            auto parity = [&](int b) {
-                return (uint32_t)(((b & 1) ? kOddBlocks * i + (b >> 1) : kEvenBlocks * i + (b >> 1)) & 1);
-            };
-            if (blk == 1) ok = mbar_wait(&bar_pv, i & 1) && ok;             // P consumed
-            if (blk >= 2) ok = mbar_wait(&bar_blk[sb], parity(blk - 2)) && ok;
-            {   // one row at a time; the barriers keep the two lifts from interleaving
-                float x[D];
-                load_row<D>(q, bh, T, t0 + row, x);
-                lift_col_rt<D, false>(2 * blk + half, x, phiQ + sb * 32768 + half * 16384, row);
-            }
-            asm volatile("" ::: "memory");
-            {
-                float x[D];
-                load_row<D>(k, bh, T, t0 + row, x);
-                lift_col_rt<D, true>(2 * blk + half, x, phiK + sb * 32768 + half * 16384, row);
-            }
-            asm volatile("" ::: "memory");
-            if (blk >= 1) ok = mbar_wait(&bar_blk[(blk - 1) & 1], parity(blk - 1)) && ok;
-            tc_fence_after();
-            {   // S_run[blk] -> S_pre (bf16, [128 features][DV], 128-byte swizzle)
-                uint8_t *srow = spre + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                for (int c = 0; c < 32; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tS + lrow + blk * DV + half * 32 + c, r);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int chunk = half * 4 + (c >> 3) + h2;
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * h2 + 0]), __uint_as_float(r[8 * h2 + 1]));
-                        v.y = pack_bf16(__uint_as_float(r[8 * h2 + 2]), __uint_as_float(r[8 * h2 + 3]));
-                        v.z = pack_bf16(__uint_as_float(r[8 * h2 + 4]), __uint_as_float(r[8 * h2 + 5]));
-                        v.w = pack_bf16(__uint_as_float(r[8 * h2 + 6]), __uint_as_float(r[8 * h2 + 7]));
-                        *reinterpret_cast<uint4 *>(srow + ((chunk ^ (row & 7)) << 4)) = v;
-                    }
+                    uint4 u;
+                    u.x = pack_bf16(__uint_as_float(v[8 * h2 + 0]), __uint_as_float(v[8 * h2 + 1]));
+                    u.y = pack_bf16(__uint_as_float(v[8 * h2 + 2]), __uint_as_float(v[8 * h2 + 3]));
+                    u.z = pack_bf16(__uint_as_float(v[8 * h2 + 4]), __uint_as_float(v[8 * h2 + 5]));
+                    u.w = pack_bf16(__uint_as_float(v[8 * h2 + 6]), __uint_as_float(v[8 * h2 + 7]));
+                    *reinterpret_cast<uint4 *>(srow + ((chunk ^ (row & 7)) << 4)) = u;
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            ok = __syncthreads_and(ok);
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&spre_full);
+            return true;
+        };
+        // P for key half h from the Xs accumulator; returns this row's sum of weights
+        auto build_p = [&](int i, int h, float &dsum) -> bool {
+            bool w = sy.wait(&xs_full, 2 * i + h) && (2 * i + h == 0 || sy.wait(&p_empty, 2 * i + h - 1));
+            w = __all_sync(0xffffffffu, w);
+            if (!w) return false;
             tc_fence_after();
-            if (tid == 0 && ok) {
-                const uint32_t aq = smem_u32(phiQ + sb * 32768), ak = smem_u32(phiK + sb * 32768);
-                const uint32_t bs = smem_u32(spre), bv = smem_u32(tv);
-                const int fleft = C::NF - blk * 128;
-                const int ksteps = fleft >= 128 ? 8 : (fleft + 15) / 16;
-                for (int ks = 0; ks < ksteps; ++ks)
-                    mma_ss(tX, smem_desc(aq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128),
-                           smem_desc(bs + ks * 2048, 16384, 1024, kSw128), kIdPV, 1u);
+            uint8_t *prow = pbuf + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                    mma_ss(tS + blk * DV, smem_desc(ak + ks * 2048, 16384, 1024, kSw128),
-                           smem_desc(bv + ks * 2048, 16384, 1024, kSw128), kIdState, 1u);
-                mma_commit(&bar_blk[sb]);
+            for (int c = 0; c < 64; c += 16) {
+                const int s0 = h * 64 + c;
+                float wv[16];
+                if (s0 > row) {                     // whole group above the diagonal
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) wv[e] = 0.f;
+                }
+                uint32_t v[16];
+                tmem_ld16(tXs + lsel + c, v);        // warp-collective: always executed
+                if (s0 <= row) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float x = __uint_as_float(v[e]);
+                        wv[e] = (s0 + e <= row) ? x * x : 0.f;
+                        dsum += wv[e];
+                    }
+                }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int chunk = (c >> 3) + h2;
+                    uint4 u;
+                    u.x = pack_bf16(wv[8 * h2 + 0], wv[8 * h2 + 1]);
+                    u.y = pack_bf16(wv[8 * h2 + 2], wv[8 * h2 + 3]);
+                    u.z = pack_bf16(wv[8 * h2 + 4], wv[8 * h2 + 5]);
+                    u.w = pack_bf16(wv[8 * h2 + 6], wv[8 * h2 + 7]);
+                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ (row & 7)) << 4)) = u;
+                }
             }
-        }
-        {
-            constexpr int kLast = C::NBLK - 1;
-            const uint32_t par = (uint32_t)((((kLast & 1) ? kOddBlocks : kEvenBlocks) * i + (kLast >> 1)) & 1);
-            ok = mbar_wait(&bar_blk[kLast & 1], par) && ok;
-        }
-        tc_fence_after();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-
-        // ---- epilogue: O = N / D for valid rows; refresh the bf16 Gram copy
-        {
-            const float den = dpart[0][row] + dpart[1][row];
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            // tcgen05.ld is warp-collective: every lane loads, only valid rows store
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) {
+                mbar_arrive(&xs_empty);
+                mbar_arrive(&p_full);
+            }
+            return true;
+        };
+        auto epilogue = [&](int i, float dsum) -> bool {   // O = N / D for chunk i
+            bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
+            if (!w) return false;
+            tc_fence_after();
+            const int t0 = (c0 + i) * kTile;
+            const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
             const bool valid = t0 + row < T;
-            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV + half * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV);
 #pragma unroll
-            for (int c16 = 0; c16 < 2; ++c16) {
-                uint32_t r[16];
-                tmem_ld16(tX + lrow + half * 32 + c16 * 16, r);
+            for (int c = 0; c < DV; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tXo + lsel + c, v);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint4 v;
-                    v.x = pack_bf16(__uint_as_float(r[8 * c + 0]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
-                    v.y = pack_bf16(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
-                    v.z = pack_bf16(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
-                    v.w = pack_bf16(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
-                    if (valid) dst[2 * c16 + c] = v;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint4 u;
+                    u.x = pack_bf16(__uint_as_float(v[8 * h2 + 0]) * inv, __uint_as_float(v[8 * h2 + 1]) * inv);
+                    u.y = pack_bf16(__uint_as_float(v[8 * h2 + 2]) * inv, __uint_as_float(v[8 * h2 + 3]) * inv);
+                    u.z = pack_bf16(__uint_as_float(v[8 * h2 + 4]) * inv, __uint_as_float(v[8 * h2 + 5]) * inv);
+                    u.w = pack_bf16(__uint_as_float(v[8 * h2 + 6]) * inv, __uint_as_float(v[8 * h2 + 7]) * inv);
+                    if (valid) dst[(c >> 3) + h2] = u;
                 }
             }
-            if (quarter == 0) {
-                uint32_t gr[16];
-                tmem_ld16(tG + lrow + half * 16, gr);
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&o_empty);
+            return true;
+        };
+        auto gram_to_smem = [&](bool from_tmem, const float *pre) {
+            // G rows i = lane (quarter 0 only): bf16 [D][D] K-major, 64-byte swizzle
+            if (quarter != 0) return;
+            float gv[D];
+            if (from_tmem) {
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int chunk = 2 * half + cc;
-                    uint4 v;
-                    v.x = pack_bf16(__uint_as_float(gr[8 * cc + 0]), __uint_as_float(gr[8 * cc + 1]));
-                    v.y = pack_bf16(__uint_as_float(gr[8 * cc + 2]), __uint_as_float(gr[8 * cc + 3]));
-                    v.z = pack_bf16(__uint_as_float(gr[8 * cc + 4]), __uint_as_float(gr[8 * cc + 5]));
-                    v.w = pack_bf16(__uint_as_float(gr[8 * cc + 6]), __uint_as_float(gr[8 * cc + 7]));
-                    *reinterpret_cast<uint4 *>(gram + (lane >> 3) * 512 + (lane & 7) * 64 +
-                                               ((chunk ^ ((lane >> 1) & 3)) << 4)) = v;
+                for (int c = 0; c < D; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tG + lsel + c, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) gv[c + e] = __uint_as_float(v[e]);
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < D; ++e) gv[e] = pre ? pre[lane * D + e] : 0.f;
+            }
+#pragma unroll
+            for (int chunk = 0; chunk < D / 8; ++chunk) {
+                uint4 u;
+                u.x = pack_bf16(gv[8 * chunk + 0], gv[8 * chunk + 1]);
+                u.y = pack_bf16(gv[8 * chunk + 2], gv[8 * chunk + 3]);
+                u.z = pack_bf16(gv[8 * chunk + 4], gv[8 * chunk + 5]);
+                u.w = pack_bf16(gv[8 * chunk + 6], gv[8 * chunk + 7]);
+                *reinterpret_cast<uint4 *>(gram + (lane >> 3) * 512 + (lane & 7) * 64 +
+                                           ((chunk ^ ((lane >> 1) & 3)) << 4)) = u;
+            }
+            if (!from_tmem) {
+#pragma unroll
+                for (int c = 0; c < D; c += 8) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(gv[c + e]);
+                    tmem_st8(tG + lsel + c, v);
+                }
+            }
+        };
+
+        // ---- initial state: the segment's exclusive prefix (zero for g == 0)
+        {
+            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
+            for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                for (int c = 0; c < DV; c += 8) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = pre ? __float_as_uint(pre[(size_t)(b * 128 + row) * DV + c + e]) : 0u;
+                    tmem_st8(tS + lsel + b * DV + c, v);
+                }
+            }
+            gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr);
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&gram_ready);
+        }
+        float dprev = 0.f;
+        for (int i = 0; i < nch && ok; ++i) {
+            ok = convert_spre(i, 0);
+            if (ok && i > 0) ok = epilogue(i - 1, dprev);
+            float dsum = 0.f;
+            if (ok) ok = build_p(i, 0, dsum);
+            if (ok) {   // inter-chunk denominator q^T G_pre q, with q from the Q tile
+                PackedRow<D> r;
+                tile_row_packed<D>(tq, row, r);
+                float qv[D];
+#pragma unroll
+                for (int m = 0; m < D / 2; ++m) {
+                    qv[2 * m] = __uint_as_float(r.w[m] << 16);
+                    qv[2 * m + 1] = __uint_as_float(r.w[m] & 0xFFFF0000u);
+                }
+#pragma unroll
+                for (int c = 0; c < D; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tQG + lsel + c, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dsum = fmaf(__uint_as_float(v[e]), qv[c + e], dsum);
+                }
+                // Gram of this chunk -> bf16 for the next chunk's Q G MMA
+                ok = __all_sync(0xffffffffu, sy.wait(&gram_done, i));
+                if (ok) {
+                    tc_fence_after();
+                    gram_to_smem(true, nullptr);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (elect_lane0()) {
+                        mbar_arrive(&gram_ready);
+                        mbar_arrive(&qk_empty);
+                    }
+                }
+            }
+            if (ok) ok = convert_spre(i, 1);
+            if (ok) ok = build_p(i, 1, dsum);
+            for (int b = 2; b < NB && ok; ++b) ok = convert_spre(i, b);
+            dprev = dsum;
+        }
+        if (ok && nch > 0) epilogue(nch - 1, dprev);
+    } else {
+        // ================= lift warps 6..9: token t = 32*(warp-6) + lane
+        const int t = (warp - 6) * 32 + lane;
+        bool ok = true;
+        for (int i = 0; i < nch && ok; ++i) {
+            ok = __all_sync(0xffffffffu, sy.wait(&qk_full, i));
+            if (!ok) break;
+            PackedRow<D> rq, rk;
+            tile_row_packed<D>(tq, t, rq);
+            tile_row_packed<D>(tk, t, rk);
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&qk_empty);
+            for (int b = 0; b < NB && ok; ++b) {
+                const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
+                if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[ls], use - 1));
+                if (!ok) break;
+                uint8_t *dq = lring + ls * 65536, *dk = dq + 32768;
+                lift_col2_rt<D, false>(2 * b, rq, dq, t);
+                lift_col2_rt<D, false>(2 * b + 1, rq, dq + 16384, t);
+                lift_col2_rt<D, true>(2 * b, rk, dk, t);
+                lift_col2_rt<D, true>(2 * b + 1, rk, dk + 16384, t);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (elect_lane0()) mbar_arrive(&lift_full[ls]);
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0 && i + 2 < nch) issue_tile(i + 2);
     }
-    if (!ok && tid == 0) flag_error(2);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem_base, 512);
+    if (threadIdx.x == 0 && abort_flag) flag_error(2);
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
 // ================================================================= host side
@@ -799,9 +870,9 @@ Plan plan(const FwdShape &s, int num_sms) {
     return p;
 }
 
-constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + 32768 + 1024;
-constexpr int kSmemOutput =
-    2 * (2 * Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + 4 * 32768 + 16384 + 2048 + 1024;
+constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + 3 * 32768 + 2048;
+constexpr int kSmemOutput = 2 * Cfg<32, 64>::QK_TILE + 2 * Cfg<32, 64>::V_TILE + 2 * 65536 +
+                            16384 + 16384 + 2048 + 2048;
 
 }  // namespace
 
@@ -830,8 +901,8 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(C::NBLK, p.G - 1, s.BH()), 128, kSmemState, stream>>>(
-                mk, mv, (const bf16 *)k, seg, s.T, p.NCt, p.Lc, p.G);
+            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 192, kSmemState, stream>>>(
+                mk, mv, seg, p.NCt, p.Lc, p.G);
         }
         cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream);
         if (e != cudaSuccess) return e;
@@ -840,8 +911,8 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                          kSmemOutput);
     {
         TraceScope tr("tc_segment_output", stream);
-        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 256, kSmemOutput, stream>>>(
-            mq, mk, mv, (const bf16 *)q, (const bf16 *)k, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G);
+        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 320, kSmemOutput, stream>>>(
+            mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G);
     }
     return cudaGetLastError();
 }
