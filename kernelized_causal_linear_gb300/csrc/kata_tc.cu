@@ -169,32 +169,125 @@ __device__ __forceinline__ void lift_chunk2(const PackedRow<D> &r, uint8_t *dst)
     *reinterpret_cast<uint4 *>(dst) = v;
 }
 
-template <int D, bool KEY, int AC, int... CH>
-__device__ __forceinline__ void lift_col2_impl(const PackedRow<D> &r, uint8_t *row, int t7,
-                                               std::integer_sequence<int, CH...>) {
-    (lift_chunk2<D, KEY, 32 * AC + 4 * CH>(r, row + ((CH ^ t7) << 4)), ...);
+// ---- lift with per-row broadcasts computed once per token: bc[i] holds
+// (x_i, x_i) for queries and (2 x_i, 2 x_i) for keys, so each lifted pair is a
+// single mul.bf16x2 (keys: the diagonal pair of row i uses (x_i, 2 x_i)).
+template <int D>
+struct LiftRow {
+    uint32_t w[D / 2];    // (x_2m, x_2m+1)
+    uint32_t so[D / 2];   // (x_2m+1, x_2m+2), x_D = 0
+    uint32_t bc[D];       // row broadcasts
+};
+
+template <int D, bool KEY>
+__device__ __forceinline__ void make_lift_row(const PackedRow<D> &p, LiftRow<D> &r) {
+#pragma unroll
+    for (int m = 0; m < D / 2; ++m) {
+        r.w[m] = p.w[m];
+        r.so[m] = p.so[m];
+    }
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        const uint32_t b = __byte_perm(p.w[i / 2], 0u, (i % 2 == 0) ? 0x1010 : 0x3232);
+        r.bc[i] = KEY ? bmul2(b, 0x40004000u) : b;
+    }
 }
 
-template <int D, bool KEY, int AC>
-__device__ __forceinline__ void lift_col2(const PackedRow<D> &r, uint8_t *tile_col, int t) {
-    lift_col2_impl<D, KEY, AC>(r, tile_col + (t >> 3) * 1024 + (t & 7) * 128, t & 7,
-                               std::make_integer_sequence<int, 8>{});
+template <int D, bool KEY, int W>
+__device__ __forceinline__ uint32_t lift_word3(const LiftRow<D> &r) {
+    if constexpr (W >= Words<D>::count()) {
+        return 0u;
+    } else {
+        constexpr int I = Words<D>::row_of(W);
+        constexpr int J = Words<D>::col_of(W);
+        uint32_t pair;
+        if constexpr (J % 2 == 0) pair = r.w[J / 2];
+        else pair = r.so[(J - 1) / 2];
+        uint32_t bc = r.bc[I];
+        if constexpr (KEY && J == I)   // (x_I, 2 x_I): low half from the raw row
+            bc = __byte_perm(r.w[I / 2], bc, (I % 2 == 0) ? 0x7610 : 0x7632);
+        return bmul2(bc, pair);
+    }
+}
+
+template <int D, bool KEY, int W0>
+__device__ __forceinline__ void lift_chunk3(const LiftRow<D> &r, uint8_t *dst) {
+    uint4 v;
+    v.x = lift_word3<D, KEY, W0 + 0>(r);
+    v.y = lift_word3<D, KEY, W0 + 1>(r);
+    v.z = lift_word3<D, KEY, W0 + 2>(r);
+    v.w = lift_word3<D, KEY, W0 + 3>(r);
+    *reinterpret_cast<uint4 *>(dst) = v;
+}
+
+// Destinations of the 8 16-byte chunks of token row t in a [128 x 64] atom
+// column with the 128-byte swizzle (chunk c stored at chunk c ^ (t % 8)).
+struct ChunkPtrs {
+    uint8_t *p[8];
+};
+__device__ __forceinline__ ChunkPtrs chunk_ptrs(uint8_t *tile_col, int t) {
+    ChunkPtrs c;
+    uint8_t *row = tile_col + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) c.p[ch] = row + ((ch ^ (t & 7)) << 4);
+    return c;
+}
+
+template <int D, bool KEY, int AC, int... CH>
+__device__ __forceinline__ void lift_col2_impl(const PackedRow<D> &r, const ChunkPtrs &cp,
+                                               std::integer_sequence<int, CH...>) {
+    (lift_chunk2<D, KEY, 32 * AC + 4 * CH>(r, cp.p[CH]), ...);
+}
+
+// Lift words 32*AC .. 32*AC + 4*NCH - 1 (NCH chunks) of one token row.
+template <int D, bool KEY, int AC, int NCH = 8>
+__device__ __forceinline__ void lift_col2(const PackedRow<D> &r, const ChunkPtrs &cp) {
+    lift_col2_impl<D, KEY, AC>(r, cp, std::make_integer_sequence<int, NCH>{});
+}
+
+// Runtime atom-column dispatch.  Atom columns holding only padding (every word
+// >= Words<D>::count()) are skipped, and a partly padded column stops at its
+// last real chunk: no MMA reads past the real features of a column's block.
+template <int D, bool KEY>
+__device__ __forceinline__ void lift_col2_rt(int ac, const PackedRow<D> &r, const ChunkPtrs &cp) {
+    constexpr int NW = Words<D>::count();
+    switch (ac) {
+#define KATA_LIFT_CASE(A)                                                                  \
+    case A:                                                                                \
+        if constexpr (32 * (A) < NW) {                                                     \
+            constexpr int nch = (NW - 32 * (A)) >= 32 ? 8 : ((NW - 32 * (A)) + 3) / 4;    \
+            lift_col2<D, KEY, A, nch>(r, cp);                                              \
+        }                                                                                  \
+        break;
+        KATA_LIFT_CASE(0) KATA_LIFT_CASE(1) KATA_LIFT_CASE(2) KATA_LIFT_CASE(3)
+        KATA_LIFT_CASE(4) KATA_LIFT_CASE(5) KATA_LIFT_CASE(6) KATA_LIFT_CASE(7)
+        KATA_LIFT_CASE(8) KATA_LIFT_CASE(9)
+#undef KATA_LIFT_CASE
+        default: break;
+    }
+}
+
+template <int D, bool KEY, int AC, int... CH>
+__device__ __forceinline__ void lift_col3_impl(const LiftRow<D> &r, const ChunkPtrs &cp,
+                                               std::integer_sequence<int, CH...>) {
+    (lift_chunk3<D, KEY, 32 * AC + 4 * CH>(r, cp.p[CH]), ...);
 }
 
 template <int D, bool KEY>
-__device__ __forceinline__ void lift_col2_rt(int ac, const PackedRow<D> &r, uint8_t *tile_col,
-                                             int t) {
+__device__ __forceinline__ void lift_col3_rt(int ac, const LiftRow<D> &r, const ChunkPtrs &cp) {
+    constexpr int NW = Words<D>::count();
     switch (ac) {
-        case 0: lift_col2<D, KEY, 0>(r, tile_col, t); break;
-        case 1: lift_col2<D, KEY, 1>(r, tile_col, t); break;
-        case 2: lift_col2<D, KEY, 2>(r, tile_col, t); break;
-        case 3: lift_col2<D, KEY, 3>(r, tile_col, t); break;
-        case 4: lift_col2<D, KEY, 4>(r, tile_col, t); break;
-        case 5: lift_col2<D, KEY, 5>(r, tile_col, t); break;
-        case 6: lift_col2<D, KEY, 6>(r, tile_col, t); break;
-        case 7: lift_col2<D, KEY, 7>(r, tile_col, t); break;
-        case 8: lift_col2<D, KEY, 8>(r, tile_col, t); break;
-        case 9: lift_col2<D, KEY, 9>(r, tile_col, t); break;
+#define KATA_LIFT3_CASE(A)                                                                     \
+    case A:                                                                                    \
+        if constexpr (32 * (A) < NW) {                                                         \
+            constexpr int nch = (NW - 32 * (A)) >= 32 ? 8 : ((NW - 32 * (A)) + 3) / 4;        \
+            lift_col3_impl<D, KEY, A>(r, cp, std::make_integer_sequence<int, nch>{});          \
+        }                                                                                      \
+        break;
+        KATA_LIFT3_CASE(0) KATA_LIFT3_CASE(1) KATA_LIFT3_CASE(2) KATA_LIFT3_CASE(3)
+        KATA_LIFT3_CASE(4) KATA_LIFT3_CASE(5) KATA_LIFT3_CASE(6) KATA_LIFT3_CASE(7)
+        KATA_LIFT3_CASE(8) KATA_LIFT3_CASE(9)
+#undef KATA_LIFT3_CASE
         default: break;
     }
 }
@@ -245,9 +338,10 @@ __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) ==
 // Segment state of one (segment, head): S_seg = sum over the segment's tokens of
 // psi_k(k) v^T (all feature blocks, fp32 in TMEM) and G_seg = K^T K.
 //   warp 0: TMA (K and V tiles, 2 stages)      warp 1: MMA issue
-//   warps 2-5: key lift into a 3-stage ring, then the epilogue
+//   warps 2-9: key lift into a 3-stage ring (two warps per 32 tokens, one
+//   64-feature atom column each), then the epilogue (warps 2-5)
 template <int D, int DV>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  float *__restrict__ seg, int NCt, int Lc, int G) {
     using C = Cfg<D, DV>;
@@ -272,10 +366,10 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         abort_flag = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tile_full[i], 1);
-            mbar_init(&tile_empty[i], 1 + 4);        // MMA commit + 4 lift warps
+            mbar_init(&tile_empty[i], 1 + 8);        // MMA commit + 8 lift warps
         }
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(&lift_full[i], 4);
+            mbar_init(&lift_full[i], 8);
             mbar_init(&lift_empty[i], 1);
         }
         mbar_init(&done_bar, 1);
@@ -308,16 +402,20 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (elect_lane0()) {
             constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
             constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
+            // base descriptors: K tile as MN-major A/B of the Gram, lifted keys as
+            // MN-major A and V as MN-major B of the state update
+            const uint64_t dK = smem_desc(smem_u32(sm), 8192, 512, kSw64);
+            const uint64_t dV = smem_desc(smem_u32(sm + C::QK_TILE), 16384, 1024, kSw128);
+            const uint64_t dR = smem_desc(smem_u32(ring), 16384, 1024, kSw128);
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
                 ok = sy.wait(&tile_full[st], i >> 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tk = smem_u32(sm + st * kStage), tv = tk + C::QK_TILE;
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t a = smem_desc(tk + ks * 1024, 8192, 512, kSw64);
+                    const uint64_t a = desc_add(dK, st * kStage + ks * 1024);
                     mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
                 }
                 for (int b = 0; b < C::NBLK && ok; ++b) {
@@ -325,12 +423,10 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     ok = sy.wait(&lift_full[rs], gb / kRing);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t pk = smem_u32(ring + rs * 32768);
 #pragma unroll
                     for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ss(tS + b * DV, smem_desc(pk + ks * 2048, 16384, 1024, kSw128),
-                               smem_desc(tv + ks * 2048, 16384, 1024, kSw128), kIdState,
-                               (i > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss(tS + b * DV, desc_add(dR, rs * 32768 + ks * 2048),
+                               desc_add(dV, st * kStage + ks * 2048), kIdState, (i > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&lift_empty[rs]);
                 }
                 mma_commit(&tile_empty[st]);
@@ -338,8 +434,8 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             mma_commit(&done_bar);
         }
     } else {
-        // ---------------- lift warps (2..5): token t = 32*(warp-2) + lane
-        const int t = (warp - 2) * 32 + lane;
+        // ---------------- lift warps (2..9): token t, atom column half h
+        const int t = ((warp - 2) & 3) * 32 + lane, h = (warp - 2) >> 2;
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
             const int st = i & 1;
@@ -353,34 +449,28 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int gb = i * C::NBLK + b, rs = gb % kRing, use = gb / kRing;
                 if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[rs], use - 1));
                 if (!ok) break;
-                uint8_t *dst = ring + rs * 32768;
-                lift_col2_rt<D, true>(2 * b, r, dst, t);
-                lift_col2_rt<D, true>(2 * b + 1, r, dst + 16384, t);
+                lift_col2_rt<D, true>(2 * b + h, r, chunk_ptrs(ring + rs * 32768 + h * 16384, t));
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_lane0()) mbar_arrive(&lift_full[rs]);
             }
         }
-        // ---------------- epilogue: state rows and Gram rows to the segment record
+        // ---------------- epilogue (warps 2-5): state and Gram rows to the segment record
         ok = __all_sync(0xffffffffu, sy.wait(&done_bar, 0));
         tc_fence_after();
-        if (ok) {
+        if (ok && h == 0) {
             const int quarter = warp & 3;
             const int lrow = quarter * 32 + lane;
             const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
             float *rec = seg + ((size_t)bh * G + g) * C::E;
             for (int b = 0; b < C::NBLK; ++b) {
-                float *dst = rec + (size_t)(b * 128 + lrow) * DV;
+                float4 *d4 = reinterpret_cast<float4 *>(rec + (size_t)(b * 128 + lrow) * DV);
+                uint32_t v[64];
+                tmem_ld64(tS + lsel + b * DV, v);
 #pragma unroll
-                for (int c = 0; c < DV; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tS + lsel + b * DV + c, v);
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-                }
+                for (int e = 0; e < DV / 4; ++e)
+                    d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                        __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
             }
             if (quarter == 0) {   // Gram rows 0..D-1 are TMEM lanes 0..D-1
                 float *gd = rec + (size_t)C::NBLK * 128 * DV + (size_t)lane * D;
@@ -408,11 +498,12 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 //   warp 0: TMA (Q, K tiles: 1 stage; V tile: 2 stages)     warp 1: MMA issue
 //   warps 2-5 ("TMEM warps", lane quarter = warp % 4): P = (QK^T)^2 masked,
 //     denominators, S_run -> S_pre conversion, output epilogue, Gram -> bf16
-//   warps 6-9: query/key lift into a 2-stage ring
+//   warps 6-13: query/key lift into a 2-stage ring; each thread lifts one
+//     token's row of one side (query or key) into both atom columns of a block
 // TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | QK^T half [384,448) |
 //       output accumulator [448,512)
 template <int D, int DV>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
                   const float *__restrict__ seg, int T, int NCt, int Lc, int G) {
@@ -443,11 +534,11 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&qk_full, 1);
-        mbar_init(&qk_empty, 1 + 4 + 4);   // MMA commit, 4 lift warps, 4 TMEM warps
+        mbar_init(&qk_empty, 1 + 8 + 4);   // MMA commit, 8 lift warps, 4 TMEM warps
         for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
-            mbar_init(&lift_full[i], 4);
+            mbar_init(&lift_full[i], 8);
             mbar_init(&lift_empty[i], 1);
         }
         mbar_init(&xs_full, 1);
@@ -497,26 +588,33 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
             constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
             constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
-            const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), ag = smem_u32(gram);
-            const uint32_t ap = smem_u32(pbuf), as = smem_u32(spre);
+            // base descriptors, built once; each MMA only offsets the start address
+            const uint64_t dQ = smem_desc(smem_u32(tq), 16, 512, kSw64);        // K-major A
+            const uint64_t dKb = smem_desc(smem_u32(tk), 16, 512, kSw64);       // K-major B
+            const uint64_t dKg = smem_desc(smem_u32(tk), 8192, 512, kSw64);     // MN-major (Gram)
+            const uint64_t dGr = smem_desc(smem_u32(gram), 16, 512, kSw64);     // K-major B
+            const uint64_t dP = smem_desc(smem_u32(pbuf), 16, 1024, kSw128);    // K-major A
+            const uint64_t dSp = smem_desc(smem_u32(spre), 16384, 1024, kSw128); // MN-major B
+            const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
+            const uint64_t dLq = smem_desc(smem_u32(lring), 16, 1024, kSw128);  // K-major A
+            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128); // MN-major A
             auto qk_half = [&](int h) {   // Xs = Q K[64h .. 64h+63]^T
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tXs, smem_desc(aq + ks * 32, 16, 512, kSw64),
-                           smem_desc(ak + h * 64 * 64 + ks * 32, 16, 512, kSw64), kIdQK, ks > 0);
+                    mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, h * 64 * 64 + ks * 32), kIdQK,
+                           ks > 0);
                 mma_commit(&xs_full);
             };
-            auto pv_half = [&](int h, uint32_t bv) {   // Xo += P[:, 64h..] V[64h..]
+            auto pv_half = [&](int h, uint32_t vo) {   // Xo += P[:, 64h..] V[64h..]
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tXo, smem_desc(ap + ks * 32, 16, 1024, kSw128),
-                           smem_desc(bv + (h * 4 + ks) * 2048, 16384, 1024, kSw128), kIdPV, 1u);
+                    mma_ss(tXo, desc_add(dP, ks * 32), desc_add(dV0, vo + (h * 4 + ks) * 2048), kIdPV, 1u);
                 mma_commit(&p_empty);
             };
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
-                const uint32_t bv = smem_u32(tv + st * C::V_TILE);
+                const uint32_t vo = st * C::V_TILE;     // byte offset of this chunk's V tile
                 // S/G pieces that need only the Q, K tiles
                 ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i) &&
                      (i == 0 || sy.wait(&xs_empty, 2 * i - 1));
@@ -524,11 +622,10 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tQG, smem_desc(aq + ks * 32, 16, 512, kSw64),
-                           smem_desc(ag + ks * 32, 16, 512, kSw64), kIdQG, ks > 0);
+                    mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t a = smem_desc(ak + ks * 1024, 8192, 512, kSw64);
+                    const uint64_t a = desc_add(dKg, ks * 1024);
                     mma_ss(tG, a, a, kIdGram, 1u);
                 }
                 mma_commit(&gram_done);
@@ -540,19 +637,18 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                          (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t lq = smem_u32(lring + ls * 65536), lk = lq + 32768;
+                    const uint32_t lo = ls * 65536;
                     const int fleft = C::NF - b * 128;
                     const int ksteps = fleft >= 128 ? 8 : (fleft + 15) / 16;
                     for (int ks = 0; ks < ksteps; ++ks)
-                        mma_ss(tXo, smem_desc(lq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128),
-                               smem_desc(as + ks * 2048, 16384, 1024, kSw128), kIdPV,
-                               (b > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss(tXo, desc_add(dLq, lo + (ks >> 2) * 16384 + (ks & 3) * 32),
+                               desc_add(dSp, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&spre_empty);
                     if (b == NB - 1) mma_commit(&o_full);
 #pragma unroll
                     for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ss(tS + b * DV, smem_desc(lk + ks * 2048, 16384, 1024, kSw128),
-                               smem_desc(bv + ks * 2048, 16384, 1024, kSw128), kIdState, 1u);
+                        mma_ss(tS + b * DV, desc_add(dLk, lo + ks * 2048), desc_add(dV0, vo + ks * 2048),
+                               kIdState, 1u);
                     mma_commit(&lift_empty[ls]);
                     mma_commit(&state_done[b]);
                     if (b == 0) {
@@ -565,13 +661,13 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         ok = sy.wait(&p_full, 2 * i);
                         if (!ok) break;
                         tc_fence_after();
-                        pv_half(0, bv);
+                        pv_half(0, vo);
                     }
                     if (b == 2) {
                         ok = sy.wait(&p_full, 2 * i + 1);
                         if (!ok) break;
                         tc_fence_after();
-                        pv_half(1, bv);
+                        pv_half(1, vo);
                     }
                 }
                 mma_commit(&v_empty[st]);
@@ -593,17 +689,17 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             uint8_t *srow = spre + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-            for (int c = 0; c < DV; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tS + lsel + b * DV + c, v);
+            for (int c32 = 0; c32 < DV; c32 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tS + lsel + b * DV + c32, v);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int chunk = (c >> 3) + h2;
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int chunk = (c32 >> 3) + cc;
                     uint4 u;
-                    u.x = pack_bf16(__uint_as_float(v[8 * h2 + 0]), __uint_as_float(v[8 * h2 + 1]));
-                    u.y = pack_bf16(__uint_as_float(v[8 * h2 + 2]), __uint_as_float(v[8 * h2 + 3]));
-                    u.z = pack_bf16(__uint_as_float(v[8 * h2 + 4]), __uint_as_float(v[8 * h2 + 5]));
-                    u.w = pack_bf16(__uint_as_float(v[8 * h2 + 6]), __uint_as_float(v[8 * h2 + 7]));
+                    u.x = pack_bf16(__uint_as_float(v[8 * cc + 0]), __uint_as_float(v[8 * cc + 1]));
+                    u.y = pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3]));
+                    u.z = pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5]));
+                    u.w = pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7]));
                     *reinterpret_cast<uint4 *>(srow + ((chunk ^ (row & 7)) << 4)) = u;
                 }
             }
@@ -621,33 +717,27 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             uint8_t *prow = pbuf + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-                const int s0 = h * 64 + c;
-                float wv[16];
-                if (s0 > row) {                     // whole group above the diagonal
+            for (int c32 = 0; c32 < 64; c32 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tXs + lsel + c32, v);           // warp-collective: always executed
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) wv[e] = 0.f;
-                }
-                uint32_t v[16];
-                tmem_ld16(tXs + lsel + c, v);        // warp-collective: always executed
-                if (s0 <= row) {
+            for (int cc = 0; cc < 4; ++cc) {
+                const int chunk = (c32 >> 3) + cc;
+                const int s0 = h * 64 + chunk * 8;
+                float wv[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float x = __uint_as_float(v[e]);
-                        wv[e] = (s0 + e <= row) ? x * x : 0.f;
-                        dsum += wv[e];
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    const float x = __uint_as_float(v[8 * cc + e]);
+                    wv[e] = (s0 + e <= row) ? x * x : 0.f;
+                    dsum += wv[e];
                 }
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int chunk = (c >> 3) + h2;
-                    uint4 u;
-                    u.x = pack_bf16(wv[8 * h2 + 0], wv[8 * h2 + 1]);
-                    u.y = pack_bf16(wv[8 * h2 + 2], wv[8 * h2 + 3]);
-                    u.z = pack_bf16(wv[8 * h2 + 4], wv[8 * h2 + 5]);
-                    u.w = pack_bf16(wv[8 * h2 + 6], wv[8 * h2 + 7]);
-                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ (row & 7)) << 4)) = u;
-                }
+                uint4 u;
+                u.x = pack_bf16(wv[0], wv[1]);
+                u.y = pack_bf16(wv[2], wv[3]);
+                u.z = pack_bf16(wv[4], wv[5]);
+                u.w = pack_bf16(wv[6], wv[7]);
+                *reinterpret_cast<uint4 *>(prow + ((chunk ^ (row & 7)) << 4)) = u;
+            }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -667,17 +757,17 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const bool valid = t0 + row < T;
             uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV);
 #pragma unroll
-            for (int c = 0; c < DV; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tXo + lsel + c, v);
+            for (int c32 = 0; c32 < DV; c32 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tXo + lsel + c32, v);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
+                for (int cc = 0; cc < 4; ++cc) {
                     uint4 u;
-                    u.x = pack_bf16(__uint_as_float(v[8 * h2 + 0]) * inv, __uint_as_float(v[8 * h2 + 1]) * inv);
-                    u.y = pack_bf16(__uint_as_float(v[8 * h2 + 2]) * inv, __uint_as_float(v[8 * h2 + 3]) * inv);
-                    u.z = pack_bf16(__uint_as_float(v[8 * h2 + 4]) * inv, __uint_as_float(v[8 * h2 + 5]) * inv);
-                    u.w = pack_bf16(__uint_as_float(v[8 * h2 + 6]) * inv, __uint_as_float(v[8 * h2 + 7]) * inv);
-                    if (valid) dst[(c >> 3) + h2] = u;
+                    u.x = pack_bf16(__uint_as_float(v[8 * cc + 0]) * inv, __uint_as_float(v[8 * cc + 1]) * inv);
+                    u.y = pack_bf16(__uint_as_float(v[8 * cc + 2]) * inv, __uint_as_float(v[8 * cc + 3]) * inv);
+                    u.z = pack_bf16(__uint_as_float(v[8 * cc + 4]) * inv, __uint_as_float(v[8 * cc + 5]) * inv);
+                    u.w = pack_bf16(__uint_as_float(v[8 * cc + 6]) * inv, __uint_as_float(v[8 * cc + 7]) * inv);
+                    if (valid) dst[(c32 >> 3) + cc] = u;
                 }
             }
             tc_fence_before();
@@ -757,12 +847,11 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     qv[2 * m] = __uint_as_float(r.w[m] << 16);
                     qv[2 * m + 1] = __uint_as_float(r.w[m] & 0xFFFF0000u);
                 }
+                {
+                    uint32_t v[32];
+                    tmem_ld32(tQG + lsel, v);
 #pragma unroll
-                for (int c = 0; c < D; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tQG + lsel + c, v);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) dsum = fmaf(__uint_as_float(v[e]), qv[c + e], dsum);
+                    for (int e = 0; e < D; ++e) dsum = fmaf(__uint_as_float(v[e]), qv[e], dsum);
                 }
                 // Gram of this chunk -> bf16 for the next chunk's Q G MMA
                 ok = __all_sync(0xffffffffu, sy.wait(&gram_done, i));
@@ -785,26 +874,28 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (ok && nch > 0) epilogue(nch - 1, dprev);
     } else {
-        // ================= lift warps 6..9: token t = 32*(warp-6) + lane
-        const int t = (warp - 6) * 32 + lane;
+        // ================= lift warps 6..13: token t, side (0 query, 1 key)
+        const int lw = warp - 6;
+        const int t = (lw & 3) * 32 + lane, side = lw >> 2;
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
             ok = __all_sync(0xffffffffu, sy.wait(&qk_full, i));
             if (!ok) break;
-            PackedRow<D> rq, rk;
-            tile_row_packed<D>(tq, t, rq);
-            tile_row_packed<D>(tk, t, rk);
+            PackedRow<D> r;
+            tile_row_packed<D>(side ? tk : tq, t, r);
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&qk_empty);
             for (int b = 0; b < NB && ok; ++b) {
                 const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
                 if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[ls], use - 1));
                 if (!ok) break;
-                uint8_t *dq = lring + ls * 65536, *dk = dq + 32768;
-                lift_col2_rt<D, false>(2 * b, rq, dq, t);
-                lift_col2_rt<D, false>(2 * b + 1, rq, dq + 16384, t);
-                lift_col2_rt<D, true>(2 * b, rk, dk, t);
-                lift_col2_rt<D, true>(2 * b + 1, rk, dk + 16384, t);
+                uint8_t *col = lring + ls * 65536 + side * 32768;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const ChunkPtrs cp = chunk_ptrs(col + h * 16384, t);
+                    if (side) lift_col2_rt<D, true>(2 * b + h, r, cp);
+                    else lift_col2_rt<D, false>(2 * b + h, r, cp);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_lane0()) mbar_arrive(&lift_full[ls]);
@@ -901,7 +992,7 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 192, kSmemState, stream>>>(
+            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 320, kSmemState, stream>>>(
                 mk, mv, seg, p.NCt, p.Lc, p.G);
         }
         cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream);
@@ -911,7 +1002,7 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                          kSmemOutput);
     {
         TraceScope tr("tc_segment_output", stream);
-        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 320, kSmemOutput, stream>>>(
+        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 448, kSmemOutput, stream>>>(
             mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G);
     }
     return cudaGetLastError();
