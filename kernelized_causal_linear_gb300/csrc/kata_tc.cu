@@ -34,12 +34,13 @@
 // accumulators inside the 512 TMEM columns of one SM.
 //
 // Feature order.  The forward never exports its state, so it uses its own
-// packing of psi: row i of the upper triangle (j = i..d-1) is padded to an even
-// length and consecutive (j, j+1) share one 32-bit bf16 pair; the sqrt(2) of
-// the off-diagonal entries is applied as a factor 2 on the key side only
-// (psi_q = q_i q_j, psi_k = 2 k_i k_j for i < j, k_i^2 on the diagonal), which
-// keeps psi(q).psi(k) = (q.k)^2 and makes every lifted entry an exactly
-// rounded bf16 product.  Padded entries are zero.
+// order of the features of psi (the grouped layout described at group8 below:
+// cross-group 8 x 8 rectangles, then within-group triangles), with two
+// features per 32-bit bf16 pair.  The sqrt(2) of the off-diagonal entries is
+// applied as a factor 2 on the key side only (psi_q = q_i q_j, psi_k =
+// 2 k_i k_j for i < j, k_i^2 on the diagonal), which keeps psi(q).psi(k) =
+// (q.k)^2 and makes every lifted entry an exactly rounded bf16 product.
+// Padded entries are zero.
 //
 // Chunk.  The tensor path uses 128-token chunks (the MMA tile height) for
 // every requested C; Eq. 17-20 give the same function for any chunk size, so
@@ -102,193 +103,128 @@ struct Cfg {
     static constexpr int E = NBLK * 128 * DV + D * D;  // floats per segment record
 };
 
-// ---- packed bf16x2 lift: one mul.rn.bf16x2 per lifted pair.  A product of two
-// bf16 values is exact in fp32, so this rounds exactly like the fp32 lift above.
+// ---- lift arithmetic: one mul.rn.bf16x2 per pair of features.  A product of
+// two bf16 values is exact in fp32, so every lifted entry is the correctly
+// rounded bf16 of x_i x_j (times the key factor 2, which is exact).
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
-// A row as bf16 pairs: w[m] = (x_2m, x_2m+1); so[m] = (x_2m+1, x_2m+2) with x_D = 0.
+constexpr uint32_t kOne2 = 0x3F803F80u;   // bf16 pair (1, 1): query factor
+constexpr uint32_t kTwo2 = 0x40004000u;   // bf16 pair (2, 2): key factor off the diagonal
+
+// A row as bf16 pairs: w[m] = (x_2m, x_2m+1).
 template <int D>
 struct PackedRow {
     uint32_t w[D / 2];
-    uint32_t so[D / 2];
 };
 
-template <int D>
-__device__ __forceinline__ void load_packed(const bf16 *__restrict__ p, int bh, int T, int tok,
-                                            PackedRow<D> &r) {
-    if (tok < T) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p + ((size_t)bh * T + tok) * D);
+// ---- grouped feature layout (d = 32, 544 slots = 5 blocks of 128, 528 real)
+// The coordinates form four groups of eight (group g = coordinates 8g..8g+7).
+// Blocks 0-2 hold the 384 cross-group products as six 8 x 8 rectangles, one
+// per 64-feature atom column: block 0 = (0,1) | (2,3), block 1 = (0,2) | (1,3),
+// block 2 = (0,3) | (1,2).  Row a of rectangle (X,Y) is one 16-byte chunk:
+// x_{8X+a} * (x_{8Y}, ..., x_{8Y+7}).  Blocks 3-4 hold the four within-group
+// triangles, each packed like the full upper triangle of an 8-vector (row a:
+// pairs (x_a x_J, x_a x_{J+1}) for J = a, a+2, ...; odd rows end with a zero
+// pad), 20 pairs = 5 chunks per group, groups back to back: block 3 = groups
+// 0, 1, 2 and chunk 0 of group 3, block 4 = chunks 1-4 of group 3.  Every
+// block is lifted by the same two short routines with the groups chosen at
+// run time, so the lift code stays resident in the instruction cache.
+
+struct Group8 {
+    uint32_t w[4];   // (x_{8g+2k}, x_{8g+2k+1}), k = 0..3
+};
+
+__device__ __forceinline__ Group8 group8(const PackedRow<32> &r, int g) {
+    Group8 o;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 u = __ldg(src + c);
-            r.w[4 * c + 0] = u.x;
-            r.w[4 * c + 1] = u.y;
-            r.w[4 * c + 2] = u.z;
-            r.w[4 * c + 3] = u.w;
+    for (int k = 0; k < 4; ++k)
+        o.w[k] = g == 0 ? r.w[k] : g == 1 ? r.w[4 + k] : g == 2 ? r.w[8 + k] : r.w[12 + k];
+    return o;
+}
+
+// Token t's row in one 128-feature block ([128 tokens x 128 features], two
+// 64-feature atom columns 16 KB apart, 128-byte swizzle): chunk position pos
+// (0..15) is atom column pos / 8, chunk pos % 8, stored at chunk (pos % 8) ^ (t % 8).
+struct BlockRow {
+    uint32_t row;   // shared address of the row in atom column 0
+    uint32_t x16;   // (t % 8) * 16
+    __device__ __forceinline__ uint32_t at(int pos) const {
+        return row + (pos >> 3) * 16384 + (((pos & 7) << 4) ^ x16);
+    }
+};
+__device__ __forceinline__ BlockRow block_row(uint8_t *block, int t) {
+    return BlockRow{smem_u32(block) + (t >> 3) * 1024 + (t & 7) * 128, (uint32_t)(t & 7) << 4};
+}
+
+// Rectangle (X,Y) into chunk positions pos0 .. pos0+7; f is the side factor.
+__device__ __forceinline__ void lift_rect(const Group8 &gx, const Group8 &gy, uint32_t f,
+                                          const BlockRow &br, int pos0) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const uint32_t bc = bmul2(__byte_perm(gx.w[a >> 1], 0u, (a & 1) ? 0x3232 : 0x1010), f);
+        st_shared_v4(br.at(pos0 + a), bmul2(bc, gy.w[0]), bmul2(bc, gy.w[1]), bmul2(bc, gy.w[2]),
+                     bmul2(bc, gy.w[3]));
+    }
+}
+
+// Pair W (0..19) of one group's triangle; so[k] = (x_{2k+1}, x_{2k+2}) within the group.
+template <int W>
+__device__ __forceinline__ uint32_t tri_word(const Group8 &g, const uint32_t (&so)[4], uint32_t f) {
+    constexpr int I = Words<8>::row_of(W), J = Words<8>::col_of(W);
+    const uint32_t pair = (J % 2 == 0) ? g.w[J / 2] : so[(J - 1) / 2];
+    const uint32_t bc = __byte_perm(g.w[I / 2], 0u, (I % 2 == 0) ? 0x1010 : 0x3232);
+    uint32_t bk = bmul2(bc, f);
+    if constexpr (J == I) bk = __byte_perm(bc, bk, 0x7610);   // the square keeps factor 1
+    return bmul2(bk, pair);
+}
+
+template <int C>
+__device__ __forceinline__ void tri_chunk(const Group8 &g, const uint32_t (&so)[4], uint32_t f,
+                                          const BlockRow &br, int c_lo, int c_hi, int pos0) {
+    if (C >= c_lo && C < c_hi)
+        st_shared_v4(br.at(pos0 + C), tri_word<4 * C + 0>(g, so, f), tri_word<4 * C + 1>(g, so, f),
+                     tri_word<4 * C + 2>(g, so, f), tri_word<4 * C + 3>(g, so, f));
+}
+
+// Chunks c_lo .. c_hi-1 of one group's triangle, chunk c at position pos0 + c.
+__device__ __forceinline__ void lift_tri(const Group8 &g, uint32_t f, const BlockRow &br, int c_lo,
+                                         int c_hi, int pos0) {
+    uint32_t so[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) so[k] = __byte_perm(g.w[k], k < 3 ? g.w[k + 1] : 0u, 0x5432);
+    tri_chunk<0>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk<1>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk<2>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk<3>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk<4>(g, so, f, br, c_lo, c_hi, pos0);
+}
+
+// Lift part `part` of `nparts` (1: the whole block; 2: one atom column's share)
+// of block b for one token.
+__device__ __forceinline__ void lift_block(int b, int part, int nparts, const PackedRow<32> &r,
+                                           uint32_t f, const BlockRow &br) {
+    if (b < 3) {
+        const int rr0 = nparts == 1 ? 0 : part, rr1 = nparts == 1 ? 2 : part + 1;
+#pragma unroll 1
+        for (int rr = rr0; rr < rr1; ++rr) {
+            const int X = rr == 0 ? 0 : (b == 0 ? 2 : 1);
+            const int Y = rr == 0 ? b + 1 : (b == 2 ? 2 : 3);
+            lift_rect(group8(r, X), group8(r, Y), f, br, 8 * rr);
         }
     } else {
-#pragma unroll
-        for (int m = 0; m < D / 2; ++m) r.w[m] = 0u;
-    }
-#pragma unroll
-    for (int m = 0; m < D / 2; ++m)
-        r.so[m] = __byte_perm(r.w[m], m + 1 < D / 2 ? r.w[m + 1] : 0u, 0x5432);
-}
-
-template <int D, bool KEY, int W>
-__device__ __forceinline__ uint32_t lift_word2(const PackedRow<D> &r) {
-    if constexpr (W >= Words<D>::count()) {
-        return 0u;
-    } else {
-        constexpr int I = Words<D>::row_of(W);
-        constexpr int J = Words<D>::col_of(W);
-        uint32_t pair;
-        if constexpr (J % 2 == 0) pair = r.w[J / 2];
-        else pair = r.so[(J - 1) / 2];
-        uint32_t bc = __byte_perm(r.w[I / 2], 0u, (I % 2 == 0) ? 0x1010 : 0x3232);   // (x_I, x_I)
-        if constexpr (KEY) {
-            const uint32_t bc2 = bmul2(bc, 0x40004000u);                             // (2x_I, 2x_I)
-            if constexpr (J == I) bc = __byte_perm(bc, bc2, 0x7610);                 // (x_I, 2x_I)
-            else bc = bc2;
+        int g0 = 3, g1 = (nparts == 1 || part == 0) ? 4 : 3;   // block 4: group 3, chunks 1-4
+        if (b == 3) {
+            g0 = nparts == 1 ? 0 : 2 * part;
+            g1 = nparts == 1 ? 4 : 2 * part + 2;
         }
-        return bmul2(bc, pair);
-    }
-}
-
-template <int D, bool KEY, int W0>
-__device__ __forceinline__ void lift_chunk2(const PackedRow<D> &r, uint8_t *dst) {
-    uint4 v;
-    v.x = lift_word2<D, KEY, W0 + 0>(r);
-    v.y = lift_word2<D, KEY, W0 + 1>(r);
-    v.z = lift_word2<D, KEY, W0 + 2>(r);
-    v.w = lift_word2<D, KEY, W0 + 3>(r);
-    *reinterpret_cast<uint4 *>(dst) = v;
-}
-
-// ---- lift with per-row broadcasts computed once per token: bc[i] holds
-// (x_i, x_i) for queries and (2 x_i, 2 x_i) for keys, so each lifted pair is a
-// single mul.bf16x2 (keys: the diagonal pair of row i uses (x_i, 2 x_i)).
-template <int D>
-struct LiftRow {
-    uint32_t w[D / 2];    // (x_2m, x_2m+1)
-    uint32_t so[D / 2];   // (x_2m+1, x_2m+2), x_D = 0
-    uint32_t bc[D];       // row broadcasts
-};
-
-template <int D, bool KEY>
-__device__ __forceinline__ void make_lift_row(const PackedRow<D> &p, LiftRow<D> &r) {
-#pragma unroll
-    for (int m = 0; m < D / 2; ++m) {
-        r.w[m] = p.w[m];
-        r.so[m] = p.so[m];
-    }
-#pragma unroll
-    for (int i = 0; i < D; ++i) {
-        const uint32_t b = __byte_perm(p.w[i / 2], 0u, (i % 2 == 0) ? 0x1010 : 0x3232);
-        r.bc[i] = KEY ? bmul2(b, 0x40004000u) : b;
-    }
-}
-
-template <int D, bool KEY, int W>
-__device__ __forceinline__ uint32_t lift_word3(const LiftRow<D> &r) {
-    if constexpr (W >= Words<D>::count()) {
-        return 0u;
-    } else {
-        constexpr int I = Words<D>::row_of(W);
-        constexpr int J = Words<D>::col_of(W);
-        uint32_t pair;
-        if constexpr (J % 2 == 0) pair = r.w[J / 2];
-        else pair = r.so[(J - 1) / 2];
-        uint32_t bc = r.bc[I];
-        if constexpr (KEY && J == I)   // (x_I, 2 x_I): low half from the raw row
-            bc = __byte_perm(r.w[I / 2], bc, (I % 2 == 0) ? 0x7610 : 0x7632);
-        return bmul2(bc, pair);
-    }
-}
-
-template <int D, bool KEY, int W0>
-__device__ __forceinline__ void lift_chunk3(const LiftRow<D> &r, uint8_t *dst) {
-    uint4 v;
-    v.x = lift_word3<D, KEY, W0 + 0>(r);
-    v.y = lift_word3<D, KEY, W0 + 1>(r);
-    v.z = lift_word3<D, KEY, W0 + 2>(r);
-    v.w = lift_word3<D, KEY, W0 + 3>(r);
-    *reinterpret_cast<uint4 *>(dst) = v;
-}
-
-// Destinations of the 8 16-byte chunks of token row t in a [128 x 64] atom
-// column with the 128-byte swizzle (chunk c stored at chunk c ^ (t % 8)).
-struct ChunkPtrs {
-    uint8_t *p[8];
-};
-__device__ __forceinline__ ChunkPtrs chunk_ptrs(uint8_t *tile_col, int t) {
-    ChunkPtrs c;
-    uint8_t *row = tile_col + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) c.p[ch] = row + ((ch ^ (t & 7)) << 4);
-    return c;
-}
-
-template <int D, bool KEY, int AC, int... CH>
-__device__ __forceinline__ void lift_col2_impl(const PackedRow<D> &r, const ChunkPtrs &cp,
-                                               std::integer_sequence<int, CH...>) {
-    (lift_chunk2<D, KEY, 32 * AC + 4 * CH>(r, cp.p[CH]), ...);
-}
-
-// Lift words 32*AC .. 32*AC + 4*NCH - 1 (NCH chunks) of one token row.
-template <int D, bool KEY, int AC, int NCH = 8>
-__device__ __forceinline__ void lift_col2(const PackedRow<D> &r, const ChunkPtrs &cp) {
-    lift_col2_impl<D, KEY, AC>(r, cp, std::make_integer_sequence<int, NCH>{});
-}
-
-// Runtime atom-column dispatch.  Atom columns holding only padding (every word
-// >= Words<D>::count()) are skipped, and a partly padded column stops at its
-// last real chunk: no MMA reads past the real features of a column's block.
-template <int D, bool KEY>
-__device__ __forceinline__ void lift_col2_rt(int ac, const PackedRow<D> &r, const ChunkPtrs &cp) {
-    constexpr int NW = Words<D>::count();
-    switch (ac) {
-#define KATA_LIFT_CASE(A)                                                                  \
-    case A:                                                                                \
-        if constexpr (32 * (A) < NW) {                                                     \
-            constexpr int nch = (NW - 32 * (A)) >= 32 ? 8 : ((NW - 32 * (A)) + 3) / 4;    \
-            lift_col2<D, KEY, A, nch>(r, cp);                                              \
-        }                                                                                  \
-        break;
-        KATA_LIFT_CASE(0) KATA_LIFT_CASE(1) KATA_LIFT_CASE(2) KATA_LIFT_CASE(3)
-        KATA_LIFT_CASE(4) KATA_LIFT_CASE(5) KATA_LIFT_CASE(6) KATA_LIFT_CASE(7)
-        KATA_LIFT_CASE(8) KATA_LIFT_CASE(9)
-#undef KATA_LIFT_CASE
-        default: break;
-    }
-}
-
-template <int D, bool KEY, int AC, int... CH>
-__device__ __forceinline__ void lift_col3_impl(const LiftRow<D> &r, const ChunkPtrs &cp,
-                                               std::integer_sequence<int, CH...>) {
-    (lift_chunk3<D, KEY, 32 * AC + 4 * CH>(r, cp.p[CH]), ...);
-}
-
-template <int D, bool KEY>
-__device__ __forceinline__ void lift_col3_rt(int ac, const LiftRow<D> &r, const ChunkPtrs &cp) {
-    constexpr int NW = Words<D>::count();
-    switch (ac) {
-#define KATA_LIFT3_CASE(A)                                                                     \
-    case A:                                                                                    \
-        if constexpr (32 * (A) < NW) {                                                         \
-            constexpr int nch = (NW - 32 * (A)) >= 32 ? 8 : ((NW - 32 * (A)) + 3) / 4;        \
-            lift_col3_impl<D, KEY, A>(r, cp, std::make_integer_sequence<int, nch>{});          \
-        }                                                                                      \
-        break;
-        KATA_LIFT3_CASE(0) KATA_LIFT3_CASE(1) KATA_LIFT3_CASE(2) KATA_LIFT3_CASE(3)
-        KATA_LIFT3_CASE(4) KATA_LIFT3_CASE(5) KATA_LIFT3_CASE(6) KATA_LIFT3_CASE(7)
-        KATA_LIFT3_CASE(8) KATA_LIFT3_CASE(9)
-#undef KATA_LIFT3_CASE
-        default: break;
+#pragma unroll 1
+        for (int g = g0; g < g1; ++g)
+            lift_tri(group8(r, g), f, br, b == 3 ? 0 : 1, (b == 3 && g == 3) ? 1 : 5,
+                     b == 3 ? 5 * g : -1);
     }
 }
 
@@ -308,9 +244,6 @@ __device__ __forceinline__ void tile_row_packed(const uint8_t *tile, int t, Pack
         r.w[4 * c + 2] = u.z;
         r.w[4 * c + 3] = u.w;
     }
-#pragma unroll
-    for (int m = 0; m < D / 2; ++m)
-        r.so[m] = __byte_perm(r.w[m], m + 1 < D / 2 ? r.w[m + 1] : 0u, 0x5432);
 }
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -338,8 +271,8 @@ __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) ==
 // Segment state of one (segment, head): S_seg = sum over the segment's tokens of
 // psi_k(k) v^T (all feature blocks, fp32 in TMEM) and G_seg = K^T K.
 //   warp 0: TMA (K and V tiles, 2 stages)      warp 1: MMA issue
-//   warps 2-9: key lift into a 3-stage ring (two warps per 32 tokens, one
-//   64-feature atom column each), then the epilogue (warps 2-5)
+//   warps 2-9: key lift into a 3-stage ring (two warps per 32 tokens, each
+//   lifting half of every block), then the epilogue (warps 2-5)
 template <int D, int DV>
 __global__ void __launch_bounds__(320, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -434,7 +367,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             mma_commit(&done_bar);
         }
     } else {
-        // ---------------- lift warps (2..9): token t, atom column half h
+        // ---------------- lift warps (2..9): token t, half h of every block
         const int t = ((warp - 2) & 3) * 32 + lane, h = (warp - 2) >> 2;
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
@@ -449,7 +382,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int gb = i * C::NBLK + b, rs = gb % kRing, use = gb / kRing;
                 if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[rs], use - 1));
                 if (!ok) break;
-                lift_col2_rt<D, true>(2 * b + h, r, chunk_ptrs(ring + rs * 32768 + h * 16384, t));
+                lift_block(b, h, 2, r, kTwo2, block_row(ring + rs * 32768, t));
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_lane0()) mbar_arrive(&lift_full[rs]);
@@ -493,35 +426,74 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
+// Lift role of the output kernel: the q (or k) row of token t into both
+// 64-feature atom columns of each block, through a 2-stage ring whose slots
+// are 64 KB apart.  Kept out of line so that its registers are allocated apart
+// from the other roles of the kernel.
+template <int D, int NB>
+__device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
+                                              int nch, uint64_t *qk_full, uint64_t *qk_empty,
+                                              uint64_t *lift_full, uint64_t *lift_empty,
+                                              volatile int *abort) {
+    const Sync sy{abort};
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+        ok = __all_sync(0xffffffffu, sy.wait(qk_full, i));
+        if (!ok) break;
+        PackedRow<D> r;
+        tile_row_packed<D>(tile, t, r);
+        __syncwarp();
+        if (elect_lane0()) mbar_arrive(qk_empty);
+        for (int b = 0; b < NB && ok; ++b) {
+            const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
+            if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[ls], use - 1));
+            if (!ok) break;
+            lift_block(b, 0, 1, r, key ? kTwo2 : kOne2, block_row(ring + ls * 65536, t));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&lift_full[ls]);
+        }
+    }
+}
+
 // ================================================================= kernel 3
 // Segment output: walk the segment's chunks with the running state in TMEM.
-//   warp 0: TMA (Q, K tiles: 1 stage; V tile: 2 stages)     warp 1: MMA issue
-//   warps 2-5 ("TMEM warps", lane quarter = warp % 4): P = (QK^T)^2 masked,
-//     denominators, S_run -> S_pre conversion, output epilogue, Gram -> bf16
-//   warps 6-13: query/key lift into a 2-stage ring; each thread lifts one
+//   warp 0: TMA (Q, K tiles: 1 stage; V tile: 2 stages; the next chunk's
+//     tiles are prefetched into L2)
+//   warp 1: output MMAs (Q G_pre, Q K^T quarters, psi_q S_pre, P V)
+//   warp 2: state MMAs (K^T K, psi_k^T V).  Two issuing threads keep the
+//     tensor pipe fed while either one waits on a barrier.
+//   warps 3-6 ("convert warps", lane quarter = warp % 4): S_run -> S_pre in
+//     bf16, one 128-feature block at a time, into a 2-slot shared-memory ring
+//   warps 7-10 ("P warps", lane quarter = warp % 4): P = (Q K^T)^2 masked, one
+//     32-key quarter at a time, written back to TMEM in bf16 as the A operand
+//     of P V; denominators; Gram -> bf16; output epilogue
+//   warps 11-18: query/key lift into a 2-stage ring; each thread lifts one
 //     token's row of one side (query or key) into both atom columns of a block
-// TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | QK^T half [384,448) |
-//       output accumulator [448,512)
+// TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | Q K^T quarter [384,416) |
+//       P slots [416,432) [432,448) | output accumulator [448,512)
 template <int D, int DV>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
                   const float *__restrict__ seg, int T, int NCt, int Lc, int G) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
+    constexpr int kLastK = (C::NF - (NB - 1) * 128 + 15) / 16;   // K steps of the last block
+    constexpr int kLiftWarps = 8, kTmemWarps = 4;
+    constexpr int kWarpConv = 3, kWarpP = 7, kWarpLift = 11;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *tq = sm;                                   // Q tile, 8 KB (64-byte swizzle)
     uint8_t *tk = sm + C::QK_TILE;                      // K tile, 8 KB
     uint8_t *tv = sm + 2 * C::QK_TILE;                  // V tiles [2][16 KB]
     uint8_t *lring = tv + 2 * C::V_TILE;                // [2][psi_q 32 KB | psi_k 32 KB]
-    uint8_t *pbuf = lring + 2 * 65536;                  // P half, 16 KB
-    uint8_t *spre = pbuf + 16384;                       // S_pre block, 16 KB
-    uint8_t *gram = spre + 16384;                       // G_pre bf16, 2 KB
+    uint8_t *spre = lring + 2 * 65536;                  // S_pre blocks [2][16 KB]
+    uint8_t *gram = spre + 2 * 16384;                   // G_pre bf16, 2 KB
     __shared__ __align__(8) uint64_t qk_full, qk_empty, v_full[2], v_empty[2], xs_full, xs_empty,
-        p_full, p_empty, lift_full[2], lift_empty[2], spre_full, spre_empty, state_done[NB],
-        o_full, o_empty, gram_done, gram_ready, fin_bar;
+        p_full[2], p_empty[2], lift_full[2], lift_empty[2], spre_full[2], spre_empty[2],
+        state_done[NB], o_full, o_empty, gram_done, qg_done, gram_ready, fin_bar[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -534,25 +506,26 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&qk_full, 1);
-        mbar_init(&qk_empty, 1 + 8 + 4);   // MMA commit, 8 lift warps, 4 TMEM warps
+        mbar_init(&qk_empty, 2 + kLiftWarps + kTmemWarps);   // 2 MMA commits, lift warps, P warps
         for (int i = 0; i < 2; ++i) {
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
-            mbar_init(&lift_full[i], 8);
-            mbar_init(&lift_empty[i], 1);
+            mbar_init(&v_empty[i], 2);
+            mbar_init(&lift_full[i], kLiftWarps);
+            mbar_init(&lift_empty[i], 2);
+            mbar_init(&spre_full[i], kTmemWarps);
+            mbar_init(&spre_empty[i], 2);
+            mbar_init(&p_full[i], kTmemWarps);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&fin_bar[i], 1);
         }
         mbar_init(&xs_full, 1);
-        mbar_init(&xs_empty, 4);
-        mbar_init(&p_full, 4);
-        mbar_init(&p_empty, 1);
-        mbar_init(&spre_full, 4);
-        mbar_init(&spre_empty, 1);
+        mbar_init(&xs_empty, kTmemWarps);
         for (int b = 0; b < NB; ++b) mbar_init(&state_done[b], 1);
         mbar_init(&o_full, 1);
-        mbar_init(&o_empty, 4);
+        mbar_init(&o_empty, kTmemWarps);
         mbar_init(&gram_done, 1);
-        mbar_init(&gram_ready, 4);
-        mbar_init(&fin_bar, 1);
+        mbar_init(&qg_done, 1);
+        mbar_init(&gram_ready, kTmemWarps);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -563,7 +536,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tS = tmem_base, tG = tmem_base + 320, tQG = tmem_base + 352;
-    const uint32_t tXs = tmem_base + 384, tXo = tmem_base + 448;
+    const uint32_t tXs = tmem_base + 384, tP = tmem_base + 416, tXo = tmem_base + 448;
 
     if (warp == 0) {
         // ================= TMA producer
@@ -578,201 +551,255 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
                 mbar_arrive_expect_tx(&v_full[st], C::V_TILE);
                 tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, bh, &v_full[st]);
+                if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
+                    tma_prefetch_3d(&tm_q, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, bh);
+                }
             }
         }
     } else if (warp == 1) {
-        // ================= MMA issue
+        // ================= output MMAs
         if (elect_lane0()) {
-            constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t kIdQK = idesc_bf16(128, 32, false, false);
             constexpr uint32_t kIdQG = idesc_bf16(128, D, false, false);
-            constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
             constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
-            constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
             // base descriptors, built once; each MMA only offsets the start address
             const uint64_t dQ = smem_desc(smem_u32(tq), 16, 512, kSw64);        // K-major A
             const uint64_t dKb = smem_desc(smem_u32(tk), 16, 512, kSw64);       // K-major B
-            const uint64_t dKg = smem_desc(smem_u32(tk), 8192, 512, kSw64);     // MN-major (Gram)
             const uint64_t dGr = smem_desc(smem_u32(gram), 16, 512, kSw64);     // K-major B
-            const uint64_t dP = smem_desc(smem_u32(pbuf), 16, 1024, kSw128);    // K-major A
             const uint64_t dSp = smem_desc(smem_u32(spre), 16384, 1024, kSw128); // MN-major B
             const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
             const uint64_t dLq = smem_desc(smem_u32(lring), 16, 1024, kSw128);  // K-major A
-            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128); // MN-major A
-            auto qk_half = [&](int h) {   // Xs = Q K[64h .. 64h+63]^T
+            auto qk_quarter = [&](int q) {   // Xs = Q K[32q .. 32q+31]^T
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, h * 64 * 64 + ks * 32), kIdQK,
+                    mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, q * 2048 + ks * 32), kIdQK,
                            ks > 0);
                 mma_commit(&xs_full);
             };
-            auto pv_half = [&](int h, uint32_t vo) {   // Xo += P[:, 64h..] V[64h..]
+            auto pv_quarter = [&](int n, uint32_t vo) {   // Xo += P_q V[32q .. 32q+31]
+                const int q = n & 3, slot = n & 1;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tXo, desc_add(dP, ks * 32), desc_add(dV0, vo + (h * 4 + ks) * 2048), kIdPV, 1u);
-                mma_commit(&p_empty);
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_ts(tXo, tP + slot * 16 + ks * 8, desc_add(dV0, vo + (2 * q + ks) * 2048),
+                           kIdPV, 1u);
+                mma_commit(&p_empty[slot]);
             };
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
                 const uint32_t vo = st * C::V_TILE;     // byte offset of this chunk's V tile
-                // S/G pieces that need only the Q, K tiles
                 ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i) &&
-                     (i == 0 || sy.wait(&xs_empty, 2 * i - 1));
+                     (i == 0 || sy.wait(&xs_empty, 4 * i - 1));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
+                mma_commit(&qg_done);
+                qk_quarter(0);
+                ok = sy.wait(&v_full[st], i >> 1);
+                for (int b = 0; b < NB && ok; ++b) {
+                    const int gb = i * NB + b, ls = gb & 1;
+                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full[ls], gb >> 1) &&
+                         (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    // Xo (+)= psi_q S_pre for this block
+                    const uint64_t a0 = desc_add(dLq, ls * 65536), b0 = desc_add(dSp, ls * 16384);
+                    if (b < NB - 1) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss(tXo, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                   desc_add(b0, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < kLastK; ++ks)
+                            mma_ss(tXo, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                   desc_add(b0, ks * 2048), kIdPV, 1u);
+                    }
+                    mma_commit(&spre_empty[ls]);
+                    mma_commit(&lift_empty[ls]);
+                    // Q K^T quarter b + 1 once the P warps have read quarter b, and P V
+                    // for quarter b - 1, whose P was built while block b ran
+                    if (b < 3) {
+                        ok = sy.wait(&xs_empty, 4 * i + b);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk_quarter(b + 1);
+                        if (b == 2) mma_commit(&qk_empty);
+                    }
+                    if (b >= 1) {
+                        const int n = 4 * i + b - 1;
+                        ok = sy.wait(&p_full[n & 1], n >> 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv_quarter(n, vo);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&o_full);
+                mma_commit(&v_empty[st]);
+            }
+            mma_commit(&fin_bar[0]);
+            sy.wait(&fin_bar[0], 0);
+        }
+    } else if (warp == 2) {
+        // ================= state MMAs
+        if (elect_lane0()) {
+            constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
+            constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
+            const uint64_t dKg = smem_desc(smem_u32(tk), 8192, 512, kSw64);     // MN-major (Gram)
+            const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
+            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128); // MN-major A
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i & 1;
+                const uint32_t vo = st * C::V_TILE;
+                // G += K^T K, after the P warps have read G_pre for this chunk
+                ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks) {
                     const uint64_t a = desc_add(dKg, ks * 1024);
                     mma_ss(tG, a, a, kIdGram, 1u);
                 }
                 mma_commit(&gram_done);
-                qk_half(0);
+                mma_commit(&qk_empty);
                 ok = sy.wait(&v_full[st], i >> 1);
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
-                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full, gb) &&
-                         (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
+                    // S_run block b += psi_k^T V once the convert warps have read it
+                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full[ls], gb >> 1);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t lo = ls * 65536;
-                    const int fleft = C::NF - b * 128;
-                    const int ksteps = fleft >= 128 ? 8 : (fleft + 15) / 16;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        mma_ss(tXo, desc_add(dLq, lo + (ks >> 2) * 16384 + (ks & 3) * 32),
-                               desc_add(dSp, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(&spre_empty);
-                    if (b == NB - 1) mma_commit(&o_full);
+                    const uint64_t a0 = desc_add(dLk, ls * 65536), b0 = desc_add(dV0, vo);
 #pragma unroll
                     for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ss(tS + b * DV, desc_add(dLk, lo + ks * 2048), desc_add(dV0, vo + ks * 2048),
-                               kIdState, 1u);
-                    mma_commit(&lift_empty[ls]);
+                        mma_ss(tS + b * DV, desc_add(a0, ks * 2048), desc_add(b0, ks * 2048), kIdState, 1u);
                     mma_commit(&state_done[b]);
-                    if (b == 0) {
-                        // second half of Q K^T once the first has been read, then P V for it
-                        ok = sy.wait(&xs_empty, 2 * i);
-                        if (!ok) break;
-                        tc_fence_after();
-                        qk_half(1);
-                        mma_commit(&qk_empty);
-                        ok = sy.wait(&p_full, 2 * i);
-                        if (!ok) break;
-                        tc_fence_after();
-                        pv_half(0, vo);
-                    }
-                    if (b == 2) {
-                        ok = sy.wait(&p_full, 2 * i + 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        pv_half(1, vo);
-                    }
+                    mma_commit(&spre_empty[ls]);
+                    mma_commit(&lift_empty[ls]);
                 }
+                if (!ok) break;
                 mma_commit(&v_empty[st]);
             }
-            mma_commit(&fin_bar);
-            sy.wait(&fin_bar, 0);
+            mma_commit(&fin_bar[1]);
+            sy.wait(&fin_bar[1], 0);
         }
-    } else if (warp < 6) {
-        // ================= TMEM warps: lane quarter q owns rows / features 32q..32q+31
+    } else if (warp < kWarpP) {
+        // ================= convert warps: S_run block -> bf16 S_pre slot
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        {   // initial state: the segment's exclusive prefix (zero for g == 0)
+            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
+            for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                for (int c = 0; c < DV; c += 8) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = pre ? __float_as_uint(pre[(size_t)(b * 128 + row) * DV + c + e]) : 0u;
+                    tmem_st8(tS + lsel + b * DV + c, v);
+                }
+            }
+            tmem_st_wait();
+        }
         bool ok = true;
-        auto convert_spre = [&](int i, int b) -> bool {   // S_run block b -> spre (bf16)
-            const int gb = i * NB + b;
-            bool w = (gb == 0 || sy.wait(&spre_empty, gb - 1)) && (i == 0 || sy.wait(&state_done[b], i - 1));
-            w = __all_sync(0xffffffffu, w);
-            if (!w) return false;
-            tc_fence_after();
-            uint8_t *srow = spre + (row >> 3) * 1024 + (row & 7) * 128;
+        for (int i = 0; i < nch && ok; ++i) {
+            for (int b = 0; b < NB && ok; ++b) {
+                const int gb = i * NB + b, ss = gb & 1, use = gb >> 1;
+                bool w = (use == 0 || sy.wait(&spre_empty[ss], use - 1)) &&
+                         (i == 0 || sy.wait(&state_done[b], i - 1));
+                ok = __all_sync(0xffffffffu, w);
+                if (!ok) break;
+                tc_fence_after();
+                if (quarter * 32 < C::NF - b * 128) {   // rows past the real features are never read
+                    const uint32_t srow = smem_u32(spre + ss * 16384 + (row >> 3) * 1024 + (row & 7) * 128);
 #pragma unroll
-            for (int c32 = 0; c32 < DV; c32 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tS + lsel + b * DV + c32, v);
+                    for (int c32 = 0; c32 < DV; c32 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tS + lsel + b * DV + c32, v);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int chunk = (c32 >> 3) + cc;
-                    uint4 u;
-                    u.x = pack_bf16(__uint_as_float(v[8 * cc + 0]), __uint_as_float(v[8 * cc + 1]));
-                    u.y = pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3]));
-                    u.z = pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5]));
-                    u.w = pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7]));
-                    *reinterpret_cast<uint4 *>(srow + ((chunk ^ (row & 7)) << 4)) = u;
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int chunk = (c32 >> 3) + cc;
+                            st_shared_v4(srow + ((chunk ^ (row & 7)) << 4),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 0]), __uint_as_float(v[8 * cc + 1])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                        }
+                    }
+                    fence_proxy_async_smem();
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (elect_lane0()) mbar_arrive(&spre_full[ss]);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (elect_lane0()) mbar_arrive(&spre_full);
-            return true;
-        };
-        // P for key half h from the Xs accumulator; returns this row's sum of weights
-        auto build_p = [&](int i, int h, float &dsum) -> bool {
-            bool w = sy.wait(&xs_full, 2 * i + h) && (2 * i + h == 0 || sy.wait(&p_empty, 2 * i + h - 1));
+        }
+    } else if (warp < kWarpLift) {
+        // ================= P warps: lane quarter q owns query rows 32q..32q+31
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        // P for key quarter n % 4 of chunk n / 4 into P slot n % 2; adds this row's weights to dsum
+        auto build_p = [&](int n, float &dsum) -> bool {
+            const int q = n & 3, slot = n & 1;
+            bool w = sy.wait(&xs_full, n) && (n < 2 || sy.wait(&p_empty[slot], (n >> 1) - 1));
             w = __all_sync(0xffffffffu, w);
             if (!w) return false;
             tc_fence_after();
-            uint8_t *prow = pbuf + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-            for (int c32 = 0; c32 < 64; c32 += 32) {
             uint32_t v[32];
-            tmem_ld32(tXs + lsel + c32, v);           // warp-collective: always executed
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int chunk = (c32 >> 3) + cc;
-                const int s0 = h * 64 + chunk * 8;
-                float wv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = __uint_as_float(v[8 * cc + e]);
-                    wv[e] = (s0 + e <= row) ? x * x : 0.f;
-                    dsum += wv[e];
-                }
-                uint4 u;
-                u.x = pack_bf16(wv[0], wv[1]);
-                u.y = pack_bf16(wv[2], wv[3]);
-                u.z = pack_bf16(wv[4], wv[5]);
-                u.w = pack_bf16(wv[6], wv[7]);
-                *reinterpret_cast<uint4 *>(prow + ((chunk ^ (row & 7)) << 4)) = u;
-            }
-            }
-            fence_proxy_async_smem();
+            tmem_ld32(tXs + lsel, v);                 // warp-collective: always executed
             tc_fence_before();
             __syncwarp();
-            if (elect_lane0()) {
-                mbar_arrive(&xs_empty);
-                mbar_arrive(&p_full);
+            if (elect_lane0()) mbar_arrive(&xs_empty);
+            uint32_t pw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int s = 32 * q + 2 * j;
+                const float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
+                const float w0 = s <= row ? x0 * x0 : 0.f;
+                const float w1 = s + 1 <= row ? x1 * x1 : 0.f;
+                dsum += w0;
+                dsum += w1;
+                pw[j] = pack_bf16(w0, w1);
             }
+            tmem_st16(tP + lsel + slot * 16, pw);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&p_full[slot]);
             return true;
         };
         auto epilogue = [&](int i, float dsum) -> bool {   // O = N / D for chunk i
             bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
             if (!w) return false;
             tc_fence_after();
-            const int t0 = (c0 + i) * kTile;
             const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
-            const bool valid = t0 + row < T;
-            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV);
+            uint32_t o[DV / 2];   // the row in bf16 pairs
 #pragma unroll
             for (int c32 = 0; c32 < DV; c32 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tXo + lsel + c32, v);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint4 u;
-                    u.x = pack_bf16(__uint_as_float(v[8 * cc + 0]) * inv, __uint_as_float(v[8 * cc + 1]) * inv);
-                    u.y = pack_bf16(__uint_as_float(v[8 * cc + 2]) * inv, __uint_as_float(v[8 * cc + 3]) * inv);
-                    u.z = pack_bf16(__uint_as_float(v[8 * cc + 4]) * inv, __uint_as_float(v[8 * cc + 5]) * inv);
-                    u.w = pack_bf16(__uint_as_float(v[8 * cc + 6]) * inv, __uint_as_float(v[8 * cc + 7]) * inv);
-                    if (valid) dst[(c32 >> 3) + cc] = u;
-                }
+                for (int e = 0; e < 16; ++e)
+                    o[c32 / 2 + e] = pack_bf16(__uint_as_float(v[2 * e]) * inv,
+                                               __uint_as_float(v[2 * e + 1]) * inv);
             }
             tc_fence_before();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&o_empty);
+            const int t0 = (c0 + i) * kTile;
+            if (t0 + row < T) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t0 + row) * DV);
+#pragma unroll
+                for (int c = 0; c < DV / 8; ++c)
+                    dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            }
             return true;
         };
         auto gram_to_smem = [&](bool from_tmem, const float *pre) {
@@ -811,20 +838,35 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
         };
-
-        // ---- initial state: the segment's exclusive prefix (zero for g == 0)
-        {
-            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
-            for (int b = 0; b < NB; ++b) {
+        // inter-chunk denominator q^T G_pre q (Q G_pre from TMEM, q from the Q
+        // tile), then this chunk's Gram -> bf16 for the next chunk
+        auto d_inter = [&](int i, float &dsum) -> bool {
+            bool w = __all_sync(0xffffffffu, sy.wait(&qk_full, i) && sy.wait(&qg_done, i) &&
+                                                 sy.wait(&gram_done, i));
+            if (!w) return false;
+            tc_fence_after();
+            PackedRow<D> r;
+            tile_row_packed<D>(tq, row, r);
+            uint32_t v[32];
+            tmem_ld32(tQG + lsel, v);
 #pragma unroll
-                for (int c = 0; c < DV; c += 8) {
-                    uint32_t v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        v[e] = pre ? __float_as_uint(pre[(size_t)(b * 128 + row) * DV + c + e]) : 0u;
-                    tmem_st8(tS + lsel + b * DV + c, v);
-                }
+            for (int m = 0; m < D / 2; ++m) {
+                dsum = fmaf(__uint_as_float(v[2 * m]), __uint_as_float(r.w[m] << 16), dsum);
+                dsum = fmaf(__uint_as_float(v[2 * m + 1]), __uint_as_float(r.w[m] & 0xFFFF0000u), dsum);
             }
+            gram_to_smem(true, nullptr);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) {
+                mbar_arrive(&gram_ready);
+                mbar_arrive(&qk_empty);
+            }
+            return true;
+        };
+
+        {   // initial Gram: the segment's exclusive prefix (zero for g == 0)
+            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
             gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr);
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -832,75 +874,24 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&gram_ready);
         }
+        bool ok = true;
         float dprev = 0.f;
-        for (int i = 0; i < nch && ok; ++i) {
-            ok = convert_spre(i, 0);
-            if (ok && i > 0) ok = epilogue(i - 1, dprev);
+        for (int i = 0; i <= nch && ok; ++i) {   // chunk i's P and denominators, chunk i-1's output
+            if (i > 0) ok = epilogue(i - 1, dprev);
+            if (i == nch) break;
             float dsum = 0.f;
-            if (ok) ok = build_p(i, 0, dsum);
-            if (ok) {   // inter-chunk denominator q^T G_pre q, with q from the Q tile
-                PackedRow<D> r;
-                tile_row_packed<D>(tq, row, r);
-                float qv[D];
-#pragma unroll
-                for (int m = 0; m < D / 2; ++m) {
-                    qv[2 * m] = __uint_as_float(r.w[m] << 16);
-                    qv[2 * m + 1] = __uint_as_float(r.w[m] & 0xFFFF0000u);
-                }
-                {
-                    uint32_t v[32];
-                    tmem_ld32(tQG + lsel, v);
-#pragma unroll
-                    for (int e = 0; e < D; ++e) dsum = fmaf(__uint_as_float(v[e]), qv[e], dsum);
-                }
-                // Gram of this chunk -> bf16 for the next chunk's Q G MMA
-                ok = __all_sync(0xffffffffu, sy.wait(&gram_done, i));
-                if (ok) {
-                    tc_fence_after();
-                    gram_to_smem(true, nullptr);
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (elect_lane0()) {
-                        mbar_arrive(&gram_ready);
-                        mbar_arrive(&qk_empty);
-                    }
-                }
+            for (int q = 0; q < 4 && ok; ++q) {
+                ok = build_p(4 * i + q, dsum);
+                if (ok && q == 0) ok = d_inter(i, dsum);
             }
-            if (ok) ok = convert_spre(i, 1);
-            if (ok) ok = build_p(i, 1, dsum);
-            for (int b = 2; b < NB && ok; ++b) ok = convert_spre(i, b);
             dprev = dsum;
         }
-        if (ok && nch > 0) epilogue(nch - 1, dprev);
     } else {
-        // ================= lift warps 6..13: token t, side (0 query, 1 key)
-        const int lw = warp - 6;
-        const int t = (lw & 3) * 32 + lane, side = lw >> 2;
-        bool ok = true;
-        for (int i = 0; i < nch && ok; ++i) {
-            ok = __all_sync(0xffffffffu, sy.wait(&qk_full, i));
-            if (!ok) break;
-            PackedRow<D> r;
-            tile_row_packed<D>(side ? tk : tq, t, r);
-            __syncwarp();
-            if (elect_lane0()) mbar_arrive(&qk_empty);
-            for (int b = 0; b < NB && ok; ++b) {
-                const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
-                if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[ls], use - 1));
-                if (!ok) break;
-                uint8_t *col = lring + ls * 65536 + side * 32768;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const ChunkPtrs cp = chunk_ptrs(col + h * 16384, t);
-                    if (side) lift_col2_rt<D, true>(2 * b + h, r, cp);
-                    else lift_col2_rt<D, false>(2 * b + h, r, cp);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (elect_lane0()) mbar_arrive(&lift_full[ls]);
-            }
-        }
+        // ================= lift warps: token t, side (0 query, 1 key)
+        const int lw = warp - kWarpLift;
+        const int side = lw >> 2;
+        output_lift_role<D, NB>(side ? tk : tq, lring + side * 32768, (lw & 3) * 32 + lane, side != 0, nch,
+                                &qk_full, &qk_empty, lift_full, lift_empty, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -963,7 +954,7 @@ Plan plan(const FwdShape &s, int num_sms) {
 
 constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + 3 * 32768 + 2048;
 constexpr int kSmemOutput = 2 * Cfg<32, 64>::QK_TILE + 2 * Cfg<32, 64>::V_TILE + 2 * 65536 +
-                            16384 + 16384 + 2048 + 2048;
+                            2 * 16384 + 2048 + 2048;
 
 }  // namespace
 
@@ -1002,7 +993,7 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                          kSmemOutput);
     {
         TraceScope tr("tc_segment_output", stream);
-        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 448, kSmemOutput, stream>>>(
+        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
             mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G);
     }
     return cudaGetLastError();
