@@ -258,8 +258,10 @@ __device__ __forceinline__ void flag_error(int code) { atomicOr(&g_tc_error, cod
 struct Sync {
     volatile int *abort;
     __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t n) const {
+        const uint32_t parity = n & 1u;
+        if (mbar_try_wait(bar, parity)) return true;   // fast path: a completed phase
         if (*abort) return false;
-        if (mbar_wait(bar, n & 1u)) return true;
+        if (mbar_wait(bar, parity)) return true;
         *abort = 1;
         return false;
     }
@@ -432,13 +434,13 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // from the other roles of the kernel.
 template <int D, int NB>
 __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
-                                              int nch, uint64_t *qk_full, uint64_t *qk_empty,
-                                              uint64_t *lift_full, uint64_t *lift_empty,
+                                              int nch, uint64_t *chunk_full, uint64_t *qk_empty,
+                                              uint64_t *block_ready, uint64_t *block_empty,
                                               volatile int *abort) {
     const Sync sy{abort};
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
-        ok = __all_sync(0xffffffffu, sy.wait(qk_full, i));
+        ok = __all_sync(0xffffffffu, sy.wait(&chunk_full[i & 1], i >> 1));
         if (!ok) break;
         PackedRow<D> r;
         tile_row_packed<D>(tile, t, r);
@@ -446,12 +448,12 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
         if (elect_lane0()) mbar_arrive(qk_empty);
         for (int b = 0; b < NB && ok; ++b) {
             const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
-            if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[ls], use - 1));
+            if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&block_empty[ls], use - 1));
             if (!ok) break;
             lift_block(b, 0, 1, r, key ? kTwo2 : kOne2, block_row(ring + ls * 65536, t));
             fence_proxy_async_smem();
             __syncwarp();
-            if (elect_lane0()) mbar_arrive(&lift_full[ls]);
+            if (elect_lane0()) mbar_arrive(&block_ready[ls]);
         }
     }
 }
@@ -491,9 +493,13 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t *lring = tv + 2 * C::V_TILE;                // [2][psi_q 32 KB | psi_k 32 KB]
     uint8_t *spre = lring + 2 * 65536;                  // S_pre blocks [2][16 KB]
     uint8_t *gram = spre + 2 * 16384;                   // G_pre bf16, 2 KB
-    __shared__ __align__(8) uint64_t qk_full, qk_empty, v_full[2], v_empty[2], xs_full, xs_empty,
-        p_full[2], p_empty[2], lift_full[2], lift_empty[2], spre_full[2], spre_empty[2],
-        state_done[NB], o_full, o_empty, gram_done, qg_done, gram_ready, fin_bar[2];
+    // chunk_full[s]: the Q, K, V tiles of a chunk in stage s have landed and G_pre
+    //   for it is in `gram` (TMA + P warps).
+    // block_ready[s] / block_empty[s]: ring slot s holds psi_q, psi_k and S_pre of
+    //   one block (lift + convert warps) / both MMA threads are done with it.
+    __shared__ __align__(8) uint64_t chunk_full[2], qk_empty, v_empty[2], xs_full, p_full[2],
+        p_empty[2], block_ready[2], block_empty[2], state_done[NB], o_full, o_empty, gram_done,
+        qg_done, fin_bar[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -505,27 +511,22 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&qk_full, 1);
         mbar_init(&qk_empty, 2 + kLiftWarps + kTmemWarps);   // 2 MMA commits, lift warps, P warps
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&v_full[i], 1);
+            mbar_init(&chunk_full[i], 1 + kTmemWarps);         // TMA arrive + P warps (G_pre)
             mbar_init(&v_empty[i], 2);
-            mbar_init(&lift_full[i], kLiftWarps);
-            mbar_init(&lift_empty[i], 2);
-            mbar_init(&spre_full[i], kTmemWarps);
-            mbar_init(&spre_empty[i], 2);
+            mbar_init(&block_ready[i], kLiftWarps + kTmemWarps);   // lift + convert warps
+            mbar_init(&block_empty[i], 2);
             mbar_init(&p_full[i], kTmemWarps);
             mbar_init(&p_empty[i], 1);
             mbar_init(&fin_bar[i], 1);
         }
         mbar_init(&xs_full, 1);
-        mbar_init(&xs_empty, kTmemWarps);
         for (int b = 0; b < NB; ++b) mbar_init(&state_done[b], 1);
         mbar_init(&o_full, 1);
         mbar_init(&o_empty, kTmemWarps);
         mbar_init(&gram_done, 1);
         mbar_init(&qg_done, 1);
-        mbar_init(&gram_ready, kTmemWarps);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -543,14 +544,13 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (elect_lane0()) {
             for (int i = 0; i < nch; ++i) {
                 const int t0 = (c0 + i) * kTile;
-                if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
-                mbar_arrive_expect_tx(&qk_full, 2 * C::QK_TILE);
-                tma_load_3d(tq, &tm_q, 0, t0, bh, &qk_full);
-                tma_load_3d(tk, &tm_k, 0, t0, bh, &qk_full);
                 const int st = i & 1, use = i >> 1;
+                if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
-                mbar_arrive_expect_tx(&v_full[st], C::V_TILE);
-                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, bh, &v_full[st]);
+                mbar_arrive_expect_tx(&chunk_full[st], 2 * C::QK_TILE + C::V_TILE);
+                tma_load_3d(tq, &tm_q, 0, t0, bh, &chunk_full[st]);
+                tma_load_3d(tk, &tm_k, 0, t0, bh, &chunk_full[st]);
+                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, bh, &chunk_full[st]);
                 if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
                     tma_prefetch_3d(&tm_q, 0, t0 + kTile, bh);
                     tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
@@ -590,8 +590,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
                 const uint32_t vo = st * C::V_TILE;     // byte offset of this chunk's V tile
-                ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i) &&
-                     (i == 0 || sy.wait(&xs_empty, 4 * i - 1));
+                // tiles and G_pre of this chunk (the P warps read quarter 3 of the
+                // previous chunk's Q K^T before building its P, waited for below)
+                ok = sy.wait(&chunk_full[st], i >> 1);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -599,10 +600,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
                 mma_commit(&qg_done);
                 qk_quarter(0);
-                ok = sy.wait(&v_full[st], i >> 1);
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
-                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full[ls], gb >> 1) &&
+                    ok = sy.wait(&block_ready[ls], gb >> 1) &&
                          (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
                     if (!ok) break;
                     tc_fence_after();
@@ -619,22 +619,18 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             mma_ss(tXo, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
                                    desc_add(b0, ks * 2048), kIdPV, 1u);
                     }
-                    mma_commit(&spre_empty[ls]);
-                    mma_commit(&lift_empty[ls]);
-                    // Q K^T quarter b + 1 once the P warps have read quarter b, and P V
-                    // for quarter b - 1, whose P was built while block b ran
-                    if (b < 3) {
-                        ok = sy.wait(&xs_empty, 4 * i + b);
-                        if (!ok) break;
-                        tc_fence_after();
-                        qk_quarter(b + 1);
-                        if (b == 2) mma_commit(&qk_empty);
-                    }
-                    if (b >= 1) {
-                        const int n = 4 * i + b - 1;
+                    mma_commit(&block_empty[ls]);
+                    // P of quarter b (built while block b ran; the P warps have read
+                    // Q K^T quarter b by then): Q K^T quarter b + 1, then P V quarter b
+                    if (b < 4) {
+                        const int n = 4 * i + b;
                         ok = sy.wait(&p_full[n & 1], n >> 1);
                         if (!ok) break;
                         tc_fence_after();
+                        if (b < 3) {
+                            qk_quarter(b + 1);
+                            if (b == 2) mma_commit(&qk_empty);
+                        }
                         pv_quarter(n, vo);
                     }
                 }
@@ -658,7 +654,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int st = i & 1;
                 const uint32_t vo = st * C::V_TILE;
                 // G += K^T K, after the P warps have read G_pre for this chunk
-                ok = sy.wait(&qk_full, i) && sy.wait(&gram_ready, i);
+                ok = sy.wait(&chunk_full[st], i >> 1);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -668,11 +664,10 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 mma_commit(&gram_done);
                 mma_commit(&qk_empty);
-                ok = sy.wait(&v_full[st], i >> 1);
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
                     // S_run block b += psi_k^T V once the convert warps have read it
-                    ok = sy.wait(&lift_full[ls], gb >> 1) && sy.wait(&spre_full[ls], gb >> 1);
+                    ok = sy.wait(&block_ready[ls], gb >> 1);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t a0 = desc_add(dLk, ls * 65536), b0 = desc_add(dV0, vo);
@@ -680,8 +675,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int ks = 0; ks < kTile / 16; ++ks)
                         mma_ss(tS + b * DV, desc_add(a0, ks * 2048), desc_add(b0, ks * 2048), kIdState, 1u);
                     mma_commit(&state_done[b]);
-                    mma_commit(&spre_empty[ls]);
-                    mma_commit(&lift_empty[ls]);
+                    mma_commit(&block_empty[ls]);
                 }
                 if (!ok) break;
                 mma_commit(&v_empty[st]);
@@ -712,7 +706,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int i = 0; i < nch && ok; ++i) {
             for (int b = 0; b < NB && ok; ++b) {
                 const int gb = i * NB + b, ss = gb & 1, use = gb >> 1;
-                bool w = (use == 0 || sy.wait(&spre_empty[ss], use - 1)) &&
+                bool w = (use == 0 || sy.wait(&block_empty[ss], use - 1)) &&
                          (i == 0 || sy.wait(&state_done[b], i - 1));
                 ok = __all_sync(0xffffffffu, w);
                 if (!ok) break;
@@ -737,7 +731,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (elect_lane0()) mbar_arrive(&spre_full[ss]);
+                if (elect_lane0()) mbar_arrive(&block_ready[ss]);
             }
         }
     } else if (warp < kWarpLift) {
@@ -754,9 +748,6 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             uint32_t v[32];
             tmem_ld32(tXs + lsel, v);                 // warp-collective: always executed
-            tc_fence_before();
-            __syncwarp();
-            if (elect_lane0()) mbar_arrive(&xs_empty);
             uint32_t pw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -841,8 +832,8 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // inter-chunk denominator q^T G_pre q (Q G_pre from TMEM, q from the Q
         // tile), then this chunk's Gram -> bf16 for the next chunk
         auto d_inter = [&](int i, float &dsum) -> bool {
-            bool w = __all_sync(0xffffffffu, sy.wait(&qk_full, i) && sy.wait(&qg_done, i) &&
-                                                 sy.wait(&gram_done, i));
+            bool w = __all_sync(0xffffffffu, sy.wait(&chunk_full[i & 1], i >> 1) &&
+                                                 sy.wait(&qg_done, i) && sy.wait(&gram_done, i));
             if (!w) return false;
             tc_fence_after();
             PackedRow<D> r;
@@ -859,7 +850,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             __syncwarp();
             if (elect_lane0()) {
-                mbar_arrive(&gram_ready);
+                mbar_arrive(&chunk_full[(i + 1) & 1]);   // G_pre of chunk i + 1
                 mbar_arrive(&qk_empty);
             }
             return true;
@@ -872,7 +863,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (elect_lane0()) mbar_arrive(&gram_ready);
+            if (elect_lane0()) mbar_arrive(&chunk_full[0]);
         }
         bool ok = true;
         float dprev = 0.f;
@@ -891,7 +882,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int lw = warp - kWarpLift;
         const int side = lw >> 2;
         output_lift_role<D, NB>(side ? tk : tq, lring + side * 32768, (lw & 3) * 32 + lane, side != 0, nch,
-                                &qk_full, &qk_empty, lift_full, lift_empty, &abort_flag);
+                                chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();
