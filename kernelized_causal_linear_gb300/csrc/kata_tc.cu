@@ -203,8 +203,9 @@ __device__ __forceinline__ void lift_tri(const Group8 &g, uint32_t f, const Bloc
     tri_chunk<4>(g, so, f, br, c_lo, c_hi, pos0);
 }
 
-// Lift part `part` of `nparts` (1: the whole block; 2: one atom column's share)
-// of block b for one token.
+// Lift part `part` of `nparts` of block b for one token: nparts = 1 lifts the
+// whole block; nparts = 2 splits each block so that, over the five blocks, the
+// two halves hold 34 of the 68 16-byte chunks of a token row each.
 __device__ __forceinline__ void lift_block(int b, int part, int nparts, const PackedRow<32> &r,
                                            uint32_t f, const BlockRow &br) {
     if (b < 3) {
@@ -216,7 +217,7 @@ __device__ __forceinline__ void lift_block(int b, int part, int nparts, const Pa
             lift_rect(group8(r, X), group8(r, Y), f, br, 8 * rr);
         }
     } else {
-        int g0 = 3, g1 = (nparts == 1 || part == 0) ? 4 : 3;   // block 4: group 3, chunks 1-4
+        int g0 = 3, g1 = (nparts == 1 || part == 1) ? 4 : 3;   // block 4: group 3, chunks 1-4
         if (b == 3) {
             g0 = nparts == 1 ? 0 : 2 * part;
             g1 = nparts == 1 ? 4 : 2 * part + 2;
@@ -272,17 +273,21 @@ __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) ==
 // ================================================================= kernel 1
 // Segment state of one (segment, head): S_seg = sum over the segment's tokens of
 // psi_k(k) v^T (all feature blocks, fp32 in TMEM) and G_seg = K^T K.
-//   warp 0: TMA (K and V tiles, 2 stages)      warp 1: MMA issue
-//   warps 2-9: key lift into a 3-stage ring (two warps per 32 tokens, each
-//   lifting half of every block), then the epilogue (warps 2-5)
+//   warp 0: TMA (K and V tiles, 2 stages)
+//   warps 1-2: MMA issue, split so that one thread's barrier waits never idle
+//     the tensor pipe: warp 1 the Gram and state blocks 0-1, warp 2 blocks 2-4
+//   warps 3-10: key lift into a 4-slot ring (two warps per 32 tokens, each
+//   lifting half of every block), then the epilogue (warps 3-6)
+constexpr int kStateRing = 4;
 template <int D, int DV>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  float *__restrict__ seg, int NCt, int Lc, int G) {
     using C = Cfg<D, DV>;
-    static_assert(DV == 64 && D == 32, "layouts below are written for d = 32, dv = 64");
+    static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int kStage = C::QK_TILE + C::V_TILE;
-    constexpr int kRing = 3;
+    constexpr int kRing = kStateRing;
+    constexpr int kLiftWarps = 8, kWarpLift = 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *ring = sm + 2 * kStage;                     // [kRing][32 KB]: psi_k block
@@ -301,13 +306,13 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         abort_flag = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tile_full[i], 1);
-            mbar_init(&tile_empty[i], 1 + 8);        // MMA commit + 8 lift warps
+            mbar_init(&tile_empty[i], 2 + kLiftWarps);   // 2 MMA commits + lift warps
         }
         for (int i = 0; i < kRing; ++i) {
-            mbar_init(&lift_full[i], 8);
-            mbar_init(&lift_empty[i], 1);
+            mbar_init(&lift_full[i], kLiftWarps);
+            mbar_init(&lift_empty[i], 1);                // the MMA thread of that block
         }
-        mbar_init(&done_bar, 1);
+        mbar_init(&done_bar, 2);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -330,10 +335,14 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 mbar_arrive_expect_tx(&tile_full[st], kStage);
                 tma_load_3d(tk, &tm_k, 0, t0, bh, &tile_full[st]);
                 tma_load_3d(tk + C::QK_TILE, &tm_v, 0, t0, bh, &tile_full[st]);
+                if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
+                    tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, bh);
+                }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issue
+    } else if (warp < kWarpLift) {
+        // ---------------- MMA issue: warp 1 = Gram + blocks 0-1, warp 2 = blocks 2-4
         if (elect_lane0()) {
             constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
             constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
@@ -342,26 +351,31 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint64_t dK = smem_desc(smem_u32(sm), 8192, 512, kSw64);
             const uint64_t dV = smem_desc(smem_u32(sm + C::QK_TILE), 16384, 1024, kSw128);
             const uint64_t dR = smem_desc(smem_u32(ring), 16384, 1024, kSw128);
+            const bool first = warp == 1;
+            const int b_lo = first ? 0 : 2, b_hi = first ? 2 : C::NBLK;
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
                 ok = sy.wait(&tile_full[st], i >> 1);
                 if (!ok) break;
                 tc_fence_after();
+                if (first) {
 #pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t a = desc_add(dK, st * kStage + ks * 1024);
-                    mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < kTile / 16; ++ks) {
+                        const uint64_t a = desc_add(dK, st * kStage + ks * 1024);
+                        mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
+                    }
                 }
-                for (int b = 0; b < C::NBLK && ok; ++b) {
+                for (int b = b_lo; b < b_hi && ok; ++b) {
                     const int gb = i * C::NBLK + b, rs = gb % kRing;
                     ok = sy.wait(&lift_full[rs], gb / kRing);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint64_t a0 = desc_add(dR, rs * 32768), b0 = desc_add(dV, st * kStage);
 #pragma unroll
                     for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ss(tS + b * DV, desc_add(dR, rs * 32768 + ks * 2048),
-                               desc_add(dV, st * kStage + ks * 2048), kIdState, (i > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss(tS + b * DV, desc_add(a0, ks * 2048), desc_add(b0, ks * 2048), kIdState,
+                               (i > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&lift_empty[rs]);
                 }
                 mma_commit(&tile_empty[st]);
@@ -369,8 +383,9 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             mma_commit(&done_bar);
         }
     } else {
-        // ---------------- lift warps (2..9): token t, half h of every block
-        const int t = ((warp - 2) & 3) * 32 + lane, h = (warp - 2) >> 2;
+        // ---------------- lift warps: token t, half h of every block
+        const int lw = warp - kWarpLift;
+        const int t = (lw & 3) * 32 + lane, h = lw >> 2;
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
             const int st = i & 1;
@@ -390,7 +405,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 if (elect_lane0()) mbar_arrive(&lift_full[rs]);
             }
         }
-        // ---------------- epilogue (warps 2-5): state and Gram rows to the segment record
+        // ---------------- epilogue (warps 3-6): state and Gram rows to the segment record
         ok = __all_sync(0xffffffffu, sy.wait(&done_bar, 0));
         tc_fence_after();
         if (ok && h == 0) {
@@ -943,7 +958,7 @@ Plan plan(const FwdShape &s, int num_sms) {
     return p;
 }
 
-constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + 3 * 32768 + 2048;
+constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + kStateRing * 32768 + 2048;
 constexpr int kSmemOutput = 2 * Cfg<32, 64>::QK_TILE + 2 * Cfg<32, 64>::V_TILE + 2 * 65536 +
                             2 * 16384 + 2048 + 2048;
 
@@ -974,7 +989,7 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 320, kSmemState, stream>>>(
+            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 352, kSmemState, stream>>>(
                 mk, mv, seg, p.NCt, p.Lc, p.G);
         }
         cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream);
