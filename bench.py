@@ -8,7 +8,8 @@ normalised output, all inside the call).  Inputs are resident in HBM before
 the timed region and are larger than L2 (129 MB) for the default workload, so
 no L2 flush is needed; the timed region is K back-to-back steps bracketed by a
 barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
-stream, max over ranks.  value = tokens (B*T per step, all heads) per second.
+stream, max over ranks.  Workloads whose inputs fit in L2 write a 258 MB buffer
+before every step and time each step with its own pair of events.  value = tokens (B*T per step, all heads) per second.
 
 Extra keys: "roofline" for the dominant kernel (its algorithmic work per
 launch over its mean CUDA-event launch time, from the library's tracing),
@@ -304,7 +305,7 @@ def _config(w):
             "feature_dim": w.n, "global_batch": w.B, "seq_len": w.T,
             "input_dtype": str(w.dtype).replace("torch.", ""),
             "l2": "inputs larger than L2, no flush" if _input_bytes(w) > L2_BYTES
-            else "L2 flushed between steps",
+            else "L2 flushed before every step (258 MB write, outside the per-step events)",
             "parallelism": "replicas"}
 
 
@@ -353,22 +354,37 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
 
+    # Inputs smaller than L2: flush L2 before every step by writing a buffer
+    # larger than it, and time each step alone (events around the call only).
+    flush = None
+    if _input_bytes(w) <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if flush is not None else [])
     with ClockSampler(torch.cuda.current_device()) as clk:
         time.sleep(0.5)
         kg.kata_trace_begin()
         torch.cuda.synchronize()
         clk.mark_start()
         start.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+                step_ev[i][0].record(stream)
             kg.kata_fwd_chunked(q, k, v, w.C, out=out)
+            if flush is not None:
+                step_ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
         clk.mark_stop()
         stages = kg.kata_trace_end()
     if dist is not None:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
+    if flush is not None:
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        elapsed_ms = start.elapsed_time(stop)
     if dist is not None:
         t = torch.tensor([elapsed_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
