@@ -34,7 +34,7 @@
 // accumulators inside the 512 TMEM columns of one SM.
 //
 // Feature order.  The forward never exports its state, so it uses its own
-// order of the features of psi (the grouped layout described at group8 below:
+// order of the features of psi (the grouped layout described above lift_rect:
 // cross-group 8 x 8 rectangles, then within-group triangles), with two
 // features per 32-bit bf16 pair.  The sqrt(2) of the off-diagonal entries is
 // applied as a factor 2 on the key side only (psi_q = q_i q_j, psi_k =
@@ -130,9 +130,120 @@ struct PackedRow {
 // triangles, each packed like the full upper triangle of an 8-vector (row a:
 // pairs (x_a x_J, x_a x_{J+1}) for J = a, a+2, ...; odd rows end with a zero
 // pad), 20 pairs = 5 chunks per group, groups back to back: block 3 = groups
-// 0, 1, 2 and chunk 0 of group 3, block 4 = chunks 1-4 of group 3.  Every
-// block is lifted by the same two short routines with the groups chosen at
-// run time, so the lift code stays resident in the instruction cache.
+// 0, 1, 2 and chunk 0 of group 3, block 4 = chunks 1-4 of group 3.  The state
+// kernel lifts every block with its own compile-time code (fewest instructions);
+// the output kernel lifts every block with one rectangle and one triangle
+// routine whose groups are chosen at run time (least code, since its other
+// roles already fill most of the instruction cache).
+
+// Token t's row in one 128-feature block ([128 tokens x 128 features], two
+// 64-feature atom columns 16 KB apart, 128-byte swizzle): chunk position pos
+// (0..15) is atom column pos / 8, chunk pos % 8, stored at chunk (pos % 8) ^ (t % 8).
+struct BlockRow {
+    uint32_t row;      // shared address of the row in atom column 0
+    uint32_t off[8];   // byte offset of chunk c within an atom-column row: (c ^ (t % 8)) * 16
+    template <int POS>
+    __device__ __forceinline__ uint32_t at() const {
+        return row + (POS >> 3) * 16384 + off[POS & 7];
+    }
+};
+__device__ __forceinline__ BlockRow block_row(uint8_t *block, int t) {
+    BlockRow br;
+    br.row = smem_u32(block) + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) br.off[c] = (uint32_t)((c ^ (t & 7)) << 4);
+    return br;
+}
+
+// Rectangle (X,Y) into chunk positions POS0 .. POS0+7; f is the side factor.
+template <int X, int Y, int POS0>
+__device__ __forceinline__ void lift_rect(const PackedRow<32> &r, uint32_t f, const BlockRow &br) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const uint32_t bc = bmul2(__byte_perm(r.w[4 * X + (a >> 1)], 0u, (a & 1) ? 0x3232 : 0x1010), f);
+        const uint32_t addr = br.row + (POS0 >> 3) * 16384 + br.off[a];
+        st_shared_v4(addr, bmul2(bc, r.w[4 * Y + 0]), bmul2(bc, r.w[4 * Y + 1]),
+                     bmul2(bc, r.w[4 * Y + 2]), bmul2(bc, r.w[4 * Y + 3]));
+    }
+}
+
+// Pair W (0..19) of group G's triangle; so[k] = (x_{2k+1}, x_{2k+2}) within the group.
+template <int G, int W>
+__device__ __forceinline__ uint32_t tri_word(const PackedRow<32> &r, const uint32_t (&so)[4],
+                                             uint32_t f) {
+    constexpr int I = Words<8>::row_of(W), J = Words<8>::col_of(W);
+    const uint32_t pair = (J % 2 == 0) ? r.w[4 * G + J / 2] : so[(J - 1) / 2];
+    const uint32_t bc = __byte_perm(r.w[4 * G + I / 2], 0u, (I % 2 == 0) ? 0x1010 : 0x3232);
+    uint32_t bk = bmul2(bc, f);
+    if constexpr (J == I) bk = __byte_perm(bc, bk, 0x7610);   // the square keeps factor 1
+    return bmul2(bk, pair);
+}
+
+// Chunks CLO .. CHI-1 of group G's triangle, chunk c at position POS0 + c.
+template <int G, int CLO, int CHI, int POS0, int... C>
+__device__ __forceinline__ void lift_tri_impl(const PackedRow<32> &r, uint32_t f, const BlockRow &br,
+                                              std::integer_sequence<int, C...>) {
+    uint32_t so[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        so[k] = __byte_perm(r.w[4 * G + k], k < 3 ? r.w[4 * G + k + 1] : 0u, 0x5432);
+    (st_shared_v4(br.at<POS0 + CLO + C>(), tri_word<G, 4 * (CLO + C) + 0>(r, so, f),
+                  tri_word<G, 4 * (CLO + C) + 1>(r, so, f), tri_word<G, 4 * (CLO + C) + 2>(r, so, f),
+                  tri_word<G, 4 * (CLO + C) + 3>(r, so, f)),
+     ...);
+}
+template <int G, int CLO, int CHI, int POS0>
+__device__ __forceinline__ void lift_tri(const PackedRow<32> &r, uint32_t f, const BlockRow &br) {
+    lift_tri_impl<G, CLO, CHI, POS0>(r, f, br, std::make_integer_sequence<int, CHI - CLO>{});
+}
+
+// Lift part PART of NPARTS of block B for one token: NPARTS = 1 lifts the whole
+// block; NPARTS = 2 splits the blocks so that, over the five blocks, each half
+// holds 34 of the 68 16-byte chunks of a token row.
+template <int B, int PART, int NPARTS>
+__device__ __forceinline__ void lift_block_ct(const PackedRow<32> &r, uint32_t f, const BlockRow &br) {
+    constexpr bool p0 = NPARTS == 1 || PART == 0, p1 = NPARTS == 1 || PART == 1;
+    if constexpr (B < 3) {
+        constexpr int X2 = B == 0 ? 2 : 1, Y2 = B == 2 ? 2 : 3;
+        if constexpr (p0) lift_rect<0, B + 1, 0>(r, f, br);
+        if constexpr (p1) lift_rect<X2, Y2, 8>(r, f, br);
+    } else if constexpr (B == 3) {
+        if constexpr (p0) {
+            lift_tri<0, 0, 5, 0>(r, f, br);
+            lift_tri<1, 0, 5, 5>(r, f, br);
+        }
+        if constexpr (p1) {
+            lift_tri<2, 0, 5, 10>(r, f, br);
+            lift_tri<3, 0, 1, 15>(r, f, br);
+        }
+    } else {
+        if constexpr (p1) lift_tri<3, 1, 5, -1>(r, f, br);
+    }
+}
+
+// Run-time block (and part) dispatch to the compile-time lifts above.
+template <int NPARTS>
+__device__ __forceinline__ void lift_block(int b, int part, const PackedRow<32> &r, uint32_t f,
+                                           const BlockRow &br) {
+    switch (b * 2 + (NPARTS == 1 ? 0 : part)) {
+        case 0: lift_block_ct<0, 0, NPARTS>(r, f, br); break;
+        case 1: lift_block_ct<0, 1, NPARTS>(r, f, br); break;
+        case 2: lift_block_ct<1, 0, NPARTS>(r, f, br); break;
+        case 3: lift_block_ct<1, 1, NPARTS>(r, f, br); break;
+        case 4: lift_block_ct<2, 0, NPARTS>(r, f, br); break;
+        case 5: lift_block_ct<2, 1, NPARTS>(r, f, br); break;
+        case 6: lift_block_ct<3, 0, NPARTS>(r, f, br); break;
+        case 7: lift_block_ct<3, 1, NPARTS>(r, f, br); break;
+        case 8: lift_block_ct<4, 0, NPARTS>(r, f, br); break;
+        case 9: lift_block_ct<4, 1, NPARTS>(r, f, br); break;
+        default: break;
+    }
+}
+
+// ---- the same layout lifted with the groups chosen at run time: one copy of
+// the rectangle and triangle code serves every block, which keeps the lift of
+// the output kernel (whose other roles already fill most of the instruction
+// cache) small.
 
 struct Group8 {
     uint32_t w[4];   // (x_{8g+2k}, x_{8g+2k+1}), k = 0..3
@@ -146,23 +257,21 @@ __device__ __forceinline__ Group8 group8(const PackedRow<32> &r, int g) {
     return o;
 }
 
-// Token t's row in one 128-feature block ([128 tokens x 128 features], two
-// 64-feature atom columns 16 KB apart, 128-byte swizzle): chunk position pos
-// (0..15) is atom column pos / 8, chunk pos % 8, stored at chunk (pos % 8) ^ (t % 8).
-struct BlockRow {
+// BlockRow with the chunk position known only at run time.
+struct BlockRowRt {
     uint32_t row;   // shared address of the row in atom column 0
     uint32_t x16;   // (t % 8) * 16
     __device__ __forceinline__ uint32_t at(int pos) const {
         return row + (pos >> 3) * 16384 + (((pos & 7) << 4) ^ x16);
     }
 };
-__device__ __forceinline__ BlockRow block_row(uint8_t *block, int t) {
-    return BlockRow{smem_u32(block) + (t >> 3) * 1024 + (t & 7) * 128, (uint32_t)(t & 7) << 4};
+__device__ __forceinline__ BlockRowRt block_row_rt(uint8_t *block, int t) {
+    return BlockRowRt{smem_u32(block) + (t >> 3) * 1024 + (t & 7) * 128, (uint32_t)(t & 7) << 4};
 }
 
 // Rectangle (X,Y) into chunk positions pos0 .. pos0+7; f is the side factor.
-__device__ __forceinline__ void lift_rect(const Group8 &gx, const Group8 &gy, uint32_t f,
-                                          const BlockRow &br, int pos0) {
+__device__ __forceinline__ void lift_rect_rt(const Group8 &gx, const Group8 &gy, uint32_t f,
+                                          const BlockRowRt &br, int pos0) {
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
         const uint32_t bc = bmul2(__byte_perm(gx.w[a >> 1], 0u, (a & 1) ? 0x3232 : 0x1010), f);
@@ -173,7 +282,7 @@ __device__ __forceinline__ void lift_rect(const Group8 &gx, const Group8 &gy, ui
 
 // Pair W (0..19) of one group's triangle; so[k] = (x_{2k+1}, x_{2k+2}) within the group.
 template <int W>
-__device__ __forceinline__ uint32_t tri_word(const Group8 &g, const uint32_t (&so)[4], uint32_t f) {
+__device__ __forceinline__ uint32_t tri_word_rt(const Group8 &g, const uint32_t (&so)[4], uint32_t f) {
     constexpr int I = Words<8>::row_of(W), J = Words<8>::col_of(W);
     const uint32_t pair = (J % 2 == 0) ? g.w[J / 2] : so[(J - 1) / 2];
     const uint32_t bc = __byte_perm(g.w[I / 2], 0u, (I % 2 == 0) ? 0x1010 : 0x3232);
@@ -183,49 +292,43 @@ __device__ __forceinline__ uint32_t tri_word(const Group8 &g, const uint32_t (&s
 }
 
 template <int C>
-__device__ __forceinline__ void tri_chunk(const Group8 &g, const uint32_t (&so)[4], uint32_t f,
-                                          const BlockRow &br, int c_lo, int c_hi, int pos0) {
+__device__ __forceinline__ void tri_chunk_rt(const Group8 &g, const uint32_t (&so)[4], uint32_t f,
+                                          const BlockRowRt &br, int c_lo, int c_hi, int pos0) {
     if (C >= c_lo && C < c_hi)
-        st_shared_v4(br.at(pos0 + C), tri_word<4 * C + 0>(g, so, f), tri_word<4 * C + 1>(g, so, f),
-                     tri_word<4 * C + 2>(g, so, f), tri_word<4 * C + 3>(g, so, f));
+        st_shared_v4(br.at(pos0 + C), tri_word_rt<4 * C + 0>(g, so, f), tri_word_rt<4 * C + 1>(g, so, f),
+                     tri_word_rt<4 * C + 2>(g, so, f), tri_word_rt<4 * C + 3>(g, so, f));
 }
 
 // Chunks c_lo .. c_hi-1 of one group's triangle, chunk c at position pos0 + c.
-__device__ __forceinline__ void lift_tri(const Group8 &g, uint32_t f, const BlockRow &br, int c_lo,
+__device__ __forceinline__ void lift_tri_rt(const Group8 &g, uint32_t f, const BlockRowRt &br, int c_lo,
                                          int c_hi, int pos0) {
     uint32_t so[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) so[k] = __byte_perm(g.w[k], k < 3 ? g.w[k + 1] : 0u, 0x5432);
-    tri_chunk<0>(g, so, f, br, c_lo, c_hi, pos0);
-    tri_chunk<1>(g, so, f, br, c_lo, c_hi, pos0);
-    tri_chunk<2>(g, so, f, br, c_lo, c_hi, pos0);
-    tri_chunk<3>(g, so, f, br, c_lo, c_hi, pos0);
-    tri_chunk<4>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk_rt<0>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk_rt<1>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk_rt<2>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk_rt<3>(g, so, f, br, c_lo, c_hi, pos0);
+    tri_chunk_rt<4>(g, so, f, br, c_lo, c_hi, pos0);
 }
 
-// Lift part `part` of `nparts` of block b for one token: nparts = 1 lifts the
-// whole block; nparts = 2 splits each block so that, over the five blocks, the
-// two halves hold 34 of the 68 16-byte chunks of a token row each.
-__device__ __forceinline__ void lift_block(int b, int part, int nparts, const PackedRow<32> &r,
-                                           uint32_t f, const BlockRow &br) {
+// Lift the whole of block b (run time) for one token.
+__device__ __forceinline__ void lift_block_rt(int b, const PackedRow<32> &r, uint32_t f,
+                                              const BlockRowRt &br) {
     if (b < 3) {
-        const int rr0 = nparts == 1 ? 0 : part, rr1 = nparts == 1 ? 2 : part + 1;
 #pragma unroll 1
-        for (int rr = rr0; rr < rr1; ++rr) {
+        for (int rr = 0; rr < 2; ++rr) {
             const int X = rr == 0 ? 0 : (b == 0 ? 2 : 1);
             const int Y = rr == 0 ? b + 1 : (b == 2 ? 2 : 3);
-            lift_rect(group8(r, X), group8(r, Y), f, br, 8 * rr);
+            lift_rect_rt(group8(r, X), group8(r, Y), f, br, 8 * rr);
         }
     } else {
-        int g0 = 3, g1 = (nparts == 1 || part == 1) ? 4 : 3;   // block 4: group 3, chunks 1-4
-        if (b == 3) {
-            g0 = nparts == 1 ? 0 : 2 * part;
-            g1 = nparts == 1 ? 4 : 2 * part + 2;
-        }
+        // block 3: groups 0..3 (group 3 only its chunk 0); block 4: group 3, chunks 1-4
+        const int g0 = b == 3 ? 0 : 3;
 #pragma unroll 1
-        for (int g = g0; g < g1; ++g)
-            lift_tri(group8(r, g), f, br, b == 3 ? 0 : 1, (b == 3 && g == 3) ? 1 : 5,
-                     b == 3 ? 5 * g : -1);
+        for (int g = g0; g < 4; ++g)
+            lift_tri_rt(group8(r, g), f, br, b == 3 ? 0 : 1, (b == 3 && g == 3) ? 1 : 5,
+                        b == 3 ? 5 * g : -1);
     }
 }
 
@@ -399,7 +502,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int gb = i * C::NBLK + b, rs = gb % kRing, use = gb / kRing;
                 if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&lift_empty[rs], use - 1));
                 if (!ok) break;
-                lift_block(b, h, 2, r, kTwo2, block_row(ring + rs * 32768, t));
+                lift_block<2>(b, h, r, kTwo2, block_row(ring + rs * 32768, t));
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_lane0()) mbar_arrive(&lift_full[rs]);
@@ -465,7 +568,7 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
             const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
             if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&block_empty[ls], use - 1));
             if (!ok) break;
-            lift_block(b, 0, 1, r, key ? kTwo2 : kOne2, block_row(ring + ls * 65536, t));
+            lift_block_rt(b, r, key ? kTwo2 : kOne2, block_row_rt(ring + ls * 65536, t));
             fence_proxy_async_smem();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&block_ready[ls]);
