@@ -718,6 +718,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
                 mma_commit(&qg_done);
                 qk_quarter(0);
+#pragma unroll 1
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
                     ok = sy.wait(&block_ready[ls], gb >> 1) &&
@@ -782,6 +783,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 mma_commit(&gram_done);
                 mma_commit(&qk_empty);
+#pragma unroll 1
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
                     // S_run block b += psi_k^T V once the convert warps have read it
@@ -822,6 +824,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
+#pragma unroll 1
             for (int b = 0; b < NB && ok; ++b) {
                 const int gb = i * NB + b, ss = gb & 1, use = gb >> 1;
                 bool w = (use == 0 || sy.wait(&block_empty[ss], use - 1)) &&
@@ -989,6 +992,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (i > 0) ok = epilogue(i - 1, dprev);
             if (i == nch) break;
             float dsum = 0.f;
+#pragma unroll 1
             for (int q = 0; q < 4 && ok; ++q) {
                 ok = build_p(4 * i + q, dsum);
                 if (ok && q == 0) ok = d_inter(i, dsum);
