@@ -103,6 +103,27 @@ int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int
                      int T, int d, int dv, int C, int dtype, kata_stream_t stream);
 
 /*
+ * kata_fwd_chunked_state -- kata_fwd_chunked plus the state after the last
+ * token, so that a prefill hands off to kata_decode_step: S_T = sum_{t<T}
+ * psi(k_t) v_t^T and z_T = sum_{t<T} psi(k_t) (Eq. 17 at the end of the last
+ * chunk; App. D.1 "Plain KATA" state), in the decode layout.
+ *
+ *   q, k, v, out, B, H, T, d, dv, C, dtype, stream: as kata_fwd_chunked
+ *   state  [B][H][n][dv]  device, fp32, written (n = d(d+1)/2)
+ *   z      [B][H][n]      device, fp32, written
+ *
+ * Features are in the row-major upper-triangle order of kata_lift with sqrt(2)
+ * on the off-diagonal entries (the layout kata_decode_step reads), whatever
+ * order the forward uses inside.  state and z must be 16-byte aligned and may
+ * not overlap each other or the other buffers (KATA_ERR_ARG).  The state is
+ * accumulated in fp32; on the tensor-core path its terms are products of the
+ * bf16-rounded lifted keys with v.  Other errors as kata_fwd_chunked.
+ */
+int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
+                           float *z, int B, int H, int T, int d, int dv, int C, int dtype,
+                           kata_stream_t stream);
+
+/*
  * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
  * arguments, layouts, paths and results), for callers that cannot allocate
  * device memory where they run it: code whose device memory is owned by a

@@ -38,7 +38,7 @@ KATA_PATH_TC = 2
 EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
-            "kata_sync_status", "kata_fwd_chunked_noalloc")
+            "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state")
 
 _lib = None
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.kata_lift.restype = i
         L.kata_fwd_chunked_noalloc.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
         L.kata_fwd_chunked_noalloc.restype = i
+        L.kata_fwd_chunked_state.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
         L.kata_trace_begin.argtypes = []
@@ -141,6 +143,29 @@ def kata_fwd_chunked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
                                 _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_chunked")
     return out
+
+
+def kata_fwd_chunked_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+                           out: torch.Tensor | None = None, state: torch.Tensor | None = None,
+                           z: torch.Tensor | None = None, stream=None):
+    """Forward plus the state after the last token in the decode layout:
+    returns (out, state [B,H,n,dv] fp32, z [B,H,n] fp32), ready for
+    kata_decode_step to continue the sequence."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    n = d * (d + 1) // 2
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    if state is None:
+        state = torch.empty((B, H, n, dv), dtype=torch.float32, device=v.device)
+    if z is None:
+        z = torch.empty((B, H, n), dtype=torch.float32, device=v.device)
+    _contig(q, k, v, out, state, z)
+    rc = lib().kata_fwd_chunked_state(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      state.data_ptr(), z.data_ptr(), B, H, T, d, dv, int(C),
+                                      _dtype_code(q.dtype), _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked_state")
+    return out, state, z
 
 
 def kata_fwd_chunked_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,

@@ -75,8 +75,8 @@ int select_path(const FwdShape &s, const DevInfo &di) {
     return KATA_PATH_SIMT;
 }
 
-size_t workspace_for(const FwdShape &s, int path, const DevInfo &di) {
-    return path == KATA_PATH_TC ? kata::tc_workspace_bytes(s, di.sms)
+size_t workspace_for(const FwdShape &s, int path, const DevInfo &di, bool with_state = false) {
+    return path == KATA_PATH_TC ? kata::tc_workspace_bytes(s, di.sms, with_state)
                                 : kata::simt_workspace_bytes(s);
 }
 
@@ -119,8 +119,13 @@ int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype) {
     return select_path(FwdShape{B, H, T, d, dv, C, dtype}, di);
 }
 
-int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
-                     int T, int d, int dv, int C, int dtype, kata_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Shared body of kata_fwd_chunked and kata_fwd_chunked_state.
+int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int B, int H, int T,
+                     int d, int dv, int C, int dtype, kata_stream_t stream,
+                     const kata::StateOut &so) {
     if (!q || !k || !v || !out) return KATA_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return KATA_ERR_ARG;
@@ -136,15 +141,15 @@ int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const int path = select_path(s, di);
-    const size_t wsb = workspace_for(s, path, di);
+    const size_t wsb = workspace_for(s, path, di, so.state != nullptr);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
-    cudaError_t e = path == KATA_PATH_TC ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st)
-                                         : kata::simt_forward(s, q, k, v, out, ws, st);
+    cudaError_t e = path == KATA_PATH_TC ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
+                                         : kata::simt_forward(s, q, k, v, out, ws, st, so);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -154,6 +159,34 @@ int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int
         return KATA_ERR_CUDA;
     }
     return KATA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
+                     int T, int d, int dv, int C, int dtype, kata_stream_t stream) {
+    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{});
+}
+
+int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
+                           float *z, int B, int H, int T, int d, int dv, int C, int dtype,
+                           kata_stream_t stream) {
+    if (!state || !z) return KATA_ERR_ARG;
+    if (!aligned16(state) || !aligned16(z)) return KATA_ERR_ARG;
+    const int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    const size_t es = elem_size(dtype), BH = (size_t)B * H, n = (size_t)d * (d + 1) / 2;
+    const size_t nqk = BH * T * d * es, nvo = BH * T * dv * es;
+    const size_t ns = BH * n * dv * 4, nz = BH * n * 4;
+    if (overlap(state, ns, z, nz) || overlap(state, ns, q, nqk) || overlap(state, ns, k, nqk) ||
+        overlap(state, ns, v, nvo) || overlap(state, ns, out, nvo) || overlap(z, nz, q, nqk) ||
+        overlap(z, nz, k, nqk) || overlap(z, nz, v, nvo) || overlap(z, nz, out, nvo))
+        return KATA_ERR_ARG;
+    kata::StateOut so;
+    so.state = state;
+    so.z = z;
+    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, so);
 }
 
 int kata_fwd_chunked_host(const void *q, const void *k, const void *v, void *out, int B,

@@ -58,15 +58,28 @@ class TraceScope {
     cudaEvent_t start_ = nullptr;
 };
 
+// Optional export of the state after the last token, in the decode layout:
+// state [BH][n][dv] and z [BH][n] fp32, row-major vech order with sqrt(2) on the
+// off-diagonal entries.  Both null: no export.
+struct StateOut {
+    float *state = nullptr;
+    float *z = nullptr;
+};
+
 // ---- CUDA-core (SIMT) path: kata_simt.cu ----------------------------------
 size_t simt_workspace_bytes(const FwdShape &s);
 cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                         void *out, void *workspace, cudaStream_t stream);
+                         void *out, void *workspace, cudaStream_t stream,
+                         const StateOut &so = StateOut{});
 cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
                         cudaStream_t stream);
-// Exclusive prefix in place along axis 1 of data[BH][n][E] (fp32).
+// Exclusive prefix in place along axis 1 of data[BH][n][E] (fp32).  With
+// so.state set, E = nf * W holds nf rows of W = dv + 1 values and the inclusive
+// totals go to so.state[BH][nf][dv] (columns 0..dv-1) and so.z[BH][nf] (column dv).
+// With totals set, the inclusive totals go to totals[BH][E] as they are.
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const StateOut &so = StateOut{},
+                                  int W = 0, float *totals = nullptr);
 
 // ---- decode: kata_decode.cu -----------------------------------------------
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
@@ -74,9 +87,10 @@ cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, cons
 
 // ---- tcgen05 path: kata_tc.cu ---------------------------------------------
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
-size_t tc_workspace_bytes(const FwdShape &s, int num_sms);
+size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                       void *out, void *workspace, int num_sms, cudaStream_t stream);
+                       void *out, void *workspace, int num_sms, cudaStream_t stream,
+                       const StateOut &so = StateOut{});
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();

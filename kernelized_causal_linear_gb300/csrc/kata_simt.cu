@@ -88,8 +88,12 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
 // Exclusive prefix over chunks, independently per (b, h, element), in place.
 // Each thread walks the chunk axis for one element; consecutive threads touch
 // consecutive elements, so every step is a coalesced sweep.
+// With state_out set, the inclusive total of element e = f * W + c is written to
+// state_out[bh][f][c] (c < W - 1) or z_out[bh][f] (c = W - 1); with totals set,
+// to totals[bh][e].
 __global__ void __launch_bounds__(256)
-scan_kernel(float *__restrict__ st, int NC, int64_t E) {
+scan_kernel(float *__restrict__ st, int NC, int64_t E, float *__restrict__ state_out,
+            float *__restrict__ z_out, int W, float *__restrict__ totals) {
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     float *p = st + (size_t)blockIdx.y * NC * E + e;
@@ -112,6 +116,14 @@ scan_kernel(float *__restrict__ st, int NC, int64_t E) {
         p[0] = run;
         run += x;
         p += E;
+    }
+    if (totals) totals[(size_t)blockIdx.y * E + e] = run;
+    if (state_out) {
+        const int64_t nf = E / W, f = e / W, col = e % W;
+        if (col < W - 1)
+            state_out[((size_t)blockIdx.y * nf + f) * (W - 1) + col] = run;
+        else
+            z_out[(size_t)blockIdx.y * nf + f] = run;
     }
 }
 
@@ -228,7 +240,7 @@ lift_kernel(const T *__restrict__ x, float *__restrict__ phi, int64_t rows, int 
 
 template <typename T>
 cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v, T *out,
-                           float *st, cudaStream_t stream) {
+                           float *st, cudaStream_t stream, const StateOut &so) {
     const int n = s.n(), NC = s.NC(), BH = s.BH();
     const int nft = (n + kFeatTile - 1) / kFeatTile;
     const int ncg = (s.dv + kColGroup - 1) / kColGroup;
@@ -243,7 +255,7 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
             k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft);
     }
     const int64_t E = (int64_t)n * (s.dv + 1);
-    cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream);
+    cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream, so, s.dv + 1);
     if (e != cudaSuccess) return e;
 
     const size_t sm3 = sizeof(float) *
@@ -261,9 +273,11 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
 }  // namespace
 
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const StateOut &so, int W, float *totals) {
+    if (so.state && (W < 2 || E % W != 0)) return cudaErrorInvalidValue;
     TraceScope tr(stage, stream);
-    scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(data, n, E);
+    scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(data, n, E, so.state,
+                                                                         so.z, W, totals);
     return cudaGetLastError();
 }
 
@@ -273,14 +287,14 @@ size_t simt_workspace_bytes(const FwdShape &s) {
 }
 
 cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                         void *out, void *workspace, cudaStream_t stream) {
+                         void *out, void *workspace, cudaStream_t stream, const StateOut &so) {
     float *st = static_cast<float *>(workspace);
     if (s.dtype == 0)
         return simt_forward_t<float>(s, (const float *)q, (const float *)k, (const float *)v,
-                                     (float *)out, st, stream);
+                                     (float *)out, st, stream, so);
     return simt_forward_t<__nv_bfloat16>(s, (const __nv_bfloat16 *)q,
                                          (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-                                         (__nv_bfloat16 *)out, st, stream);
+                                         (__nv_bfloat16 *)out, st, stream, so);
 }
 
 cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,

@@ -332,6 +332,41 @@ __device__ __forceinline__ void lift_block_rt(int b, const PackedRow<32> &r, uin
     }
 }
 
+// Coordinates (i, j), i <= j, of feature p (0..127) of block b in the grouped
+// layout; false for a pad slot.  Used to export the state in the decode
+// layout, whose features are in row-major upper-triangle order.
+__device__ __forceinline__ bool grouped_slot_pair(int b, int p, int &i, int &j) {
+    const int k = (p & 7) >> 1, hf = p & 1;
+    if (b < 3) {
+        const int h = p >> 6, a = (p & 63) >> 3;
+        const int X = h == 0 ? 0 : (b == 0 ? 2 : 1);
+        const int Y = h == 0 ? b + 1 : (b == 2 ? 2 : 3);
+        i = 8 * X + a;
+        j = 8 * Y + 2 * k + hf;
+        return true;
+    }
+    const int pos = p >> 3;
+    int g, c;
+    if (b == 3) {
+        g = pos < 15 ? pos / 5 : 3;
+        c = pos < 15 ? pos % 5 : 0;
+    } else {
+        if (pos >= 4) return false;
+        g = 3;
+        c = pos + 1;
+    }
+    int I = 0, w = 4 * c + k;   // pair w of the triangle: row I has (9 - I) / 2 pairs
+    while (w >= (9 - I) / 2) {
+        w -= (9 - I) / 2;
+        ++I;
+    }
+    const int J = I + 2 * w + hf;
+    if (J >= 8) return false;
+    i = 8 * g + I;
+    j = 8 * g + J;
+    return true;
+}
+
 // Row t of a [128 x D] bf16 tile written by TMA with the swizzle matching its
 // row width (32/64/128 bytes): the 16-byte chunk c of row t sits at chunk
 // c ^ ((t * row_bytes >> 7) & (chunks_per_row - 1)).
@@ -1012,6 +1047,45 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
+// ================================================================= state export
+// The inclusive state of a head (a segment record summed over all segments:
+// S in the grouped layout, 5 blocks x 128 features x DV, then the Gram
+// G = sum k k^T) in the decode layout: state[f][c] and z[f] for the row-major
+// upper-triangle feature f of (i, j), sqrt(2) on the off-diagonal entries.
+// The grouped layout carries a factor 2 on the key side off the diagonal, so
+// those rows are scaled by 1/sqrt(2); z_f is G_ij (sqrt(2) G_ij for i < j).
+// Grid: one CTA per head, 128 threads.
+template <int D, int DV>
+__global__ void __launch_bounds__(128)
+state_export_kernel(const float *__restrict__ total, float *__restrict__ state,
+                    float *__restrict__ z) {
+    using C = Cfg<D, DV>;
+    constexpr int kN = D * (D + 1) / 2;
+    const int bh = blockIdx.x, p = threadIdx.x;
+    const float *rec = total + (size_t)bh * C::E;
+    float *st = state + (size_t)bh * kN * DV;
+    for (int b = 0; b < C::NBLK; ++b) {
+        int i = 0, j = 0;
+        if (!grouped_slot_pair(b, p, i, j)) continue;
+        const int f = i * D - i * (i - 1) / 2 + (j - i);
+        const float sc = i == j ? 1.f : 0.70710678118654752f;
+        const float4 *src = reinterpret_cast<const float4 *>(rec + (size_t)(b * 128 + p) * DV);
+        float4 *dst = reinterpret_cast<float4 *>(st + (size_t)f * DV);
+#pragma unroll 4
+        for (int e = 0; e < DV / 4; ++e) {
+            const float4 x = src[e];
+            dst[e] = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
+        }
+    }
+    const float *gram = rec + (size_t)C::NBLK * 128 * DV;
+    for (int e = p; e < D * D; e += blockDim.x) {
+        const int i = e / D, j = e % D;
+        if (j < i) continue;
+        z[(size_t)bh * kN + i * D - i * (i - 1) / 2 + (j - i)] =
+            i == j ? gram[e] : kSqrt2 * gram[e];
+    }
+}
+
 // ================================================================= host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1076,14 +1150,16 @@ bool tc_supported(const FwdShape &s, int cc_major, int cc_minor) {
            encoder() != nullptr;
 }
 
-size_t tc_workspace_bytes(const FwdShape &s, int num_sms) {
+size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state) {
     const Plan p = plan(s, num_sms);
-    if (p.G <= 1) return 0;
-    return sizeof(float) * (size_t)s.BH() * p.G * Cfg<32, 64>::E;
+    // segment records (G of them), plus the inclusive totals when the state is exported
+    const size_t recs = with_state ? (size_t)p.G + 1 : (p.G <= 1 ? 0 : (size_t)p.G);
+    return sizeof(float) * (size_t)s.BH() * recs * Cfg<32, 64>::E;
 }
 
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                       void *out, void *workspace, int num_sms, cudaStream_t stream) {
+                       void *out, void *workspace, int num_sms, cudaStream_t stream,
+                       const StateOut &so) {
     using C = Cfg<32, 64>;
     const Plan p = plan(s, num_sms);
     CUtensorMap mq, mk, mv;
@@ -1091,16 +1167,26 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
         !make_map(mv, v, s.dv, s.T, s.BH()))
         return cudaErrorInvalidValue;
     float *seg = static_cast<float *>(workspace);
-    if (p.G > 1) {
+    const bool with_state = so.state != nullptr;
+    // Segment sums: of every segment but the last (the output kernel carries the
+    // last one on chip), and of the last one too when the final state is wanted.
+    const int nsum = with_state ? p.G : p.G - 1;
+    if (nsum > 0) {
         cudaFuncSetAttribute(seg_state_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(p.G - 1, s.BH()), 352, kSmemState, stream>>>(
+            seg_state_kernel<32, 64><<<dim3(nsum, s.BH()), 352, kSmemState, stream>>>(
                 mk, mv, seg, p.NCt, p.Lc, p.G);
         }
-        cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream);
+        float *totals = with_state ? seg + (size_t)s.BH() * p.G * C::E : nullptr;
+        cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream,
+                                              StateOut{}, 0, totals);
         if (e != cudaSuccess) return e;
+        if (with_state) {
+            TraceScope tr("tc_state_export", stream);
+            state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
+        }
     }
     cudaFuncSetAttribute(seg_output_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kSmemOutput);

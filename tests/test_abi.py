@@ -122,3 +122,26 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kg, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         kg.lib()
+
+
+def test_state_variant_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, o, S, z = (FAKE * (i + 1) * 4096 for i in range(6))
+
+    def st(**kw):
+        a = dict(q=q, k=k, v=v, out=o, S=S, z=z, B=1, H=1, T=8, d=16, dv=16, C=32, dtype=1)
+        a.update(kw)
+        return L.kata_fwd_chunked_state(a["q"], a["k"], a["v"], a["out"], a["S"], a["z"],
+                                        a["B"], a["H"], a["T"], a["d"], a["dv"], a["C"],
+                                        a["dtype"], None)
+
+    assert st(S=0) == kg.KATA_ERR_ARG
+    assert st(z=0) == kg.KATA_ERR_ARG
+    assert st(q=0) == kg.KATA_ERR_ARG
+    assert st(S=S + 8) == kg.KATA_ERR_ARG                      # misaligned state
+    assert st(z=z + 4) == kg.KATA_ERR_ARG                      # misaligned z
+    assert st(z=S + 64) == kg.KATA_ERR_ARG                     # z inside the state
+    assert st(S=q) == kg.KATA_ERR_ARG                          # state over an input
+    assert st(z=o + 16) == kg.KATA_ERR_ARG                     # z over the output
+    assert st(d=20) == kg.KATA_ERR_UNSUPPORTED
+    assert st(T=0) == kg.KATA_ERR_ARG

@@ -1,0 +1,113 @@
+"""GPU parity of kata_fwd_chunked_state: the state after the last token, in the
+decode layout, against the oracle's feature-state recurrence ([KATA] Eq. 2,
+App. D.1), and prefill -> decode consistency against the direct definition.
+
+Metric for a state: per (b, h), max |S - S_ref| / max |S_ref| (same for z).  The
+fp32 path accumulates fp32 products of the inputs (bar 1e-5).  The tensor-core
+path accumulates products of bf16-rounded lifted keys with v in fp32, so each
+term carries a relative rounding of at most 2^-9 (bar 1e-2)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import TOL, require_gpu, slice_rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+STATE_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
+
+
+@pytest.fixture(scope="module")
+def kg():
+    return require_gpu()
+
+
+def _state_err(got, ref):
+    """got, ref: [B, H, ...]; max over (b, h) of max|got - ref| / max|ref|."""
+    g = got.reshape(got.shape[0] * got.shape[1], -1)
+    r = ref.reshape(g.shape)
+    return max(float(np.max(np.abs(a - b)) / np.max(np.abs(b))) for a, b in zip(g, r))
+
+
+def _check_state(kg, w, expect_path=None):
+    q, k, v = workloads.make_qkv(w)
+    if expect_path is not None:
+        assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == expect_path
+    out, S, z = kg.kata_fwd_chunked_state(q.cuda(), k.cuda(), v.cuda(), w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    S_ref, z_ref = oracle.prefix_state(to_f64(k), to_f64(v))
+    tol = STATE_TOL[w.dtype]
+    es, ez = _state_err(to_f64(S), S_ref), _state_err(to_f64(z), z_ref)
+    assert es <= tol and ez <= tol, f"state {es:.2e}, z {ez:.2e} (bar {tol:.0e})"
+    # the output of the same call is the forward's
+    ref = oracle.forward(to_f64(q), to_f64(k), to_f64(v))
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # several segments per head, ragged last chunk
+    (16, 8, 700),    # one segment per head
+    (4, 8, 4096),    # 4 segments of 8 chunks
+    (1, 1, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+])
+def test_state_tensor_path(kg, B, H, T):
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
+    _check_state(kg, w, kg.KATA_PATH_TC)
+
+
+@pytest.mark.parametrize("name,overrides", [
+    ("small_fp32", dict(B=2, H=3, T=300)),
+    ("small_fp32", dict(B=1, H=2, T=97, d=32, dv=64, C=32)),
+    ("lm_layer_bf16", dict(B=1, H=2, T=333)),           # d = 64: CUDA-core path in bf16
+    ("mid_bf16", dict(B=1, H=2, T=200, dv=128, C=64)),  # dv = 128: CUDA-core path
+])
+def test_state_cuda_core_path(kg, name, overrides):
+    w = workloads.WORKLOADS[name].scaled(**overrides)
+    _check_state(kg, w, kg.KATA_PATH_SIMT)
+
+
+@pytest.mark.parametrize("name,overrides", [
+    ("long_ctx_bf16", dict(B=2, H=2, T=1000)),
+    ("small_fp32", dict(B=1, H=2, T=150)),
+])
+def test_prefill_then_decode(kg, name, overrides):
+    """Forward over T-1 tokens with state export, then one decode step with
+    token T-1: its output is the definition's output at row T-1."""
+    w = workloads.WORKLOADS[name].scaled(**overrides)
+    q, k, v = workloads.make_qkv(w)
+    Tp = w.T - 1
+    _, S, z = kg.kata_fwd_chunked_state(q[:, :, :Tp].contiguous().cuda(),
+                                        k[:, :, :Tp].contiguous().cuda(),
+                                        v[:, :, :Tp].contiguous().cuda(), w.C)
+    o = kg.kata_decode_step(S, z, q[:, :, Tp].contiguous().cuda(), k[:, :, Tp].contiguous().cuda(),
+                            v[:, :, Tp].contiguous().cuda())
+    torch.cuda.synchronize()
+    rows = np.arange(w.B * w.H, dtype=np.int64) * w.T + Tp
+    ref = oracle.forward_rows(to_f64(q), to_f64(k), to_f64(v), rows)
+    got = to_f64(o).reshape(w.B, w.H, 1, w.dv)
+    assert slice_rel_err(got, ref.reshape(got.shape)) <= TOL[w.dtype]
+
+
+def test_state_full_size_sampled_heads(kg):
+    """The long-context workload in the bench's call configuration: the exported
+    state of two heads against the oracle recurrence over all 131072 tokens."""
+    w = workloads.WORKLOADS["long_ctx_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    out, S, z = kg.kata_fwd_chunked_state(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    BH = w.B * w.H
+    for h in (0, BH - 1):
+        kh = k.reshape(BH, 1, 1, w.T, w.d)[h]
+        vh = v.reshape(BH, 1, 1, w.T, w.dv)[h]
+        S_ref, z_ref = oracle.prefix_state(to_f64(kh), to_f64(vh))
+        Sg = to_f64(S.reshape(BH, 1, -1, w.dv)[h:h + 1])
+        zg = to_f64(z.reshape(BH, 1, -1)[h:h + 1])
+        assert _state_err(Sg, S_ref) <= STATE_TOL[w.dtype]
+        assert _state_err(zg, z_ref) <= STATE_TOL[w.dtype]
