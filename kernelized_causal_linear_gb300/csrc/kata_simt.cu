@@ -86,44 +86,52 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
 
 // ---------------------------------------------------------------- stage 2
 // Exclusive prefix over chunks, independently per (b, h, element), in place.
-// Each thread walks the chunk axis for one element; consecutive threads touch
-// consecutive elements, so every step is a coalesced sweep.
+// Each thread walks the chunk axis for four consecutive elements (one float4);
+// consecutive threads touch consecutive elements, so every step is a coalesced
+// sweep, and each thread keeps up to eight loads in flight.
 // With state_out set, the inclusive total of element e = f * W + c is written to
 // state_out[bh][f][c] (c < W - 1) or z_out[bh][f] (c = W - 1); with totals set,
 // to totals[bh][e].
 __global__ void __launch_bounds__(256)
 scan_kernel(float *__restrict__ st, int NC, int64_t E, float *__restrict__ state_out,
             float *__restrict__ z_out, int W, float *__restrict__ totals) {
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    float *p = st + (size_t)blockIdx.y * NC * E + e;
-    float run = 0.f;
-    int c = 0;
-    for (; c + 4 <= NC; c += 4) {
-        const float x0 = p[0], x1 = p[E], x2 = p[2 * E], x3 = p[3 * E];
-        p[0] = run;
-        run += x0;
-        p[E] = run;
-        run += x1;
-        p[2 * E] = run;
-        run += x2;
-        p[3 * E] = run;
-        run += x3;
-        p += 4 * E;
+    // four consecutive elements per thread (E is a multiple of 4 for every
+    // supported shape); up to 8 records are loaded before any is written
+    const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t E4 = E >> 2;
+    if (e4 >= E4) return;
+    float4 *p = reinterpret_cast<float4 *>(st + (size_t)blockIdx.y * NC * E) + e4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < NC; c += 8) {
+        const int m = NC - c < 8 ? NC - c : 8;
+        float4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < m) x[j] = p[(size_t)j * E4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < m) {
+                p[(size_t)j * E4] = run;
+                run.x += x[j].x;
+                run.y += x[j].y;
+                run.z += x[j].z;
+                run.w += x[j].w;
+            }
+        }
+        p += (size_t)8 * E4;
     }
-    for (; c < NC; ++c) {
-        const float x = p[0];
-        p[0] = run;
-        run += x;
-        p += E;
-    }
-    if (totals) totals[(size_t)blockIdx.y * E + e] = run;
+    if (totals) reinterpret_cast<float4 *>(totals + (size_t)blockIdx.y * E)[e4] = run;
     if (state_out) {
-        const int64_t nf = E / W, f = e / W, col = e % W;
-        if (col < W - 1)
-            state_out[((size_t)blockIdx.y * nf + f) * (W - 1) + col] = run;
-        else
-            z_out[(size_t)blockIdx.y * nf + f] = run;
+        const int64_t nf = E / W;
+        const float rv[4] = {run.x, run.y, run.z, run.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t e = 4 * e4 + u, f = e / W, col = e % W;
+            if (col < W - 1)
+                state_out[((size_t)blockIdx.y * nf + f) * (W - 1) + col] = rv[u];
+            else
+                z_out[(size_t)blockIdx.y * nf + f] = rv[u];
+        }
     }
 }
 
@@ -275,9 +283,10 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
                                   cudaStream_t stream, const StateOut &so, int W, float *totals) {
     if (so.state && (W < 2 || E % W != 0)) return cudaErrorInvalidValue;
+    if (E % 4 != 0) return cudaErrorInvalidValue;
     TraceScope tr(stage, stream);
-    scan_kernel<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(data, n, E, so.state,
-                                                                         so.z, W, totals);
+    scan_kernel<<<dim3((unsigned)((E / 4 + 255) / 256), BH), 256, 0, stream>>>(data, n, E, so.state,
+                                                                             so.z, W, totals);
     return cudaGetLastError();
 }
 
