@@ -69,15 +69,28 @@ int device_info(DevInfo &out) {
     return KATA_OK;
 }
 
-int select_path(const FwdShape &s, const DevInfo &di) {
-    if (s.dtype == KATA_F32) return KATA_PATH_SIMT;
-    if (kata::tc_supported(s, di.major, di.minor)) return KATA_PATH_TC;
-    return KATA_PATH_SIMT;
+// Kernel families behind the public paths: KATA_PATH_TC covers both tensor-core
+// variants (d = 32 with segments, d = 64 with the state split over four CTAs).
+enum Kernels { kSimt, kTc32, kTc64 };
+
+Kernels select_kernels(const FwdShape &s, const DevInfo &di, bool with_state) {
+    if (s.dtype == KATA_F32) return kSimt;
+    if (kata::tc_supported(s, di.major, di.minor)) return kTc32;
+    // the d = 64 kernels keep no final state: the state export runs on CUDA cores
+    if (!with_state && kata::tc64_supported(s, di.major, di.minor, di.sms)) return kTc64;
+    return kSimt;
 }
 
-size_t workspace_for(const FwdShape &s, int path, const DevInfo &di, bool with_state = false) {
-    return path == KATA_PATH_TC ? kata::tc_workspace_bytes(s, di.sms, with_state)
-                                : kata::simt_workspace_bytes(s);
+int select_path(const FwdShape &s, const DevInfo &di) {
+    return select_kernels(s, di, false) == kSimt ? KATA_PATH_SIMT : KATA_PATH_TC;
+}
+
+size_t workspace_for(const FwdShape &s, Kernels kn, const DevInfo &di, bool with_state = false) {
+    switch (kn) {
+        case kTc32: return kata::tc_workspace_bytes(s, di.sms, with_state);
+        case kTc64: return kata::tc64_workspace_bytes(s);
+        default: return kata::simt_workspace_bytes(s);
+    }
 }
 
 }  // namespace
@@ -108,7 +121,7 @@ int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype
     DevInfo di;
     if ((rc = device_info(di))) return rc;
     const FwdShape s{B, H, T, d, dv, C, dtype};
-    *bytes = workspace_for(s, select_path(s, di), di);
+    *bytes = workspace_for(s, select_kernels(s, di, false), di);
     return KATA_OK;
 }
 
@@ -140,16 +153,18 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     cudaGetLastError();
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
-    const int path = select_path(s, di);
-    const size_t wsb = workspace_for(s, path, di, so.state != nullptr);
+    const bool with_state = so.state != nullptr;
+    const Kernels kn = select_kernels(s, di, with_state);
+    const size_t wsb = workspace_for(s, kn, di, with_state);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
-    cudaError_t e = path == KATA_PATH_TC ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
-                                         : kata::simt_forward(s, q, k, v, out, ws, st, so);
+    cudaError_t e = kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
+                    : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st)
+                                  : kata::simt_forward(s, q, k, v, out, ws, st, so);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -258,9 +273,9 @@ int kata_sync_status(kata_stream_t stream) {
         cudaGetLastError();
         return KATA_ERR_CUDA;
     }
-    const int e = kata::tc_take_error();
-    if (e < 0) return KATA_ERR_CUDA;
-    return e ? KATA_ERR_TIMEOUT : KATA_OK;
+    const int e = kata::tc_take_error(), e64 = kata::tc64_take_error();
+    if (e < 0 || e64 < 0) return KATA_ERR_CUDA;
+    return (e | e64) ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 
 int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype, kata_stream_t stream) {

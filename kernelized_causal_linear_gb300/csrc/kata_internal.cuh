@@ -95,4 +95,11 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();
 
+// ---- tcgen05 path at d = 64 (state split over four CTAs): kata_tc64.cu -----
+bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
+size_t tc64_workspace_bytes(const FwdShape &s);
+cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                         void *out, void *workspace, cudaStream_t stream);
+int tc64_take_error();
+
 }  // namespace kata

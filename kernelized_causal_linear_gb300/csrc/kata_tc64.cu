@@ -1,0 +1,591 @@
+// tcgen05 tensor-core path of the KATA chunked forward at d = 64 (bf16, sm_103a).
+//
+// At d = 64 the lift has n = 2080 coordinates: 17 blocks of 128 features in the
+// grouped layout below, whose fp32 state (17 x 64 TMEM columns) does not fit in
+// the 512 TMEM columns of one SM.  The state is therefore split by feature
+// blocks over four CTAs per head ("feature groups"):
+//   group 0: blocks 0-1, plus the intra-chunk term P = (Q K^T)^2 .* M, P V, and
+//            the normaliser (Gram G = K^T K; q^T G_pre q)      [Eq. 18, 19]
+//   groups 1-3: blocks 2-6, 7-11, 12-16
+// Every group walks all chunks of its head with its blocks' running state in
+// TMEM ([KATA] Sec. 4.1 Eq. 17), adds psi_q(Q) S_pre over its blocks into an
+// output accumulator (Eq. 18), and writes that partial numerator per token in
+// fp32; group 0 also writes the denominator.  finalize_kernel then forms
+// O = (N_0 + N_1 + N_2 + N_3) / D (Eq. 20), in that fixed order.
+//
+// The kernel keeps one segment per head: it is used when the four groups of all
+// heads fill the GPU (4 * B * H >= SM count).  Structure per CTA as in the d = 32
+// output kernel: warp 0 TMA, warps 1-2 MMA issue (output / state), warps 3-6
+// convert S_run -> bf16 S_pre (one shared-memory slot), warps 7-10 P and the
+// epilogue, warps 11-18 lift the group's blocks.
+#include "kata_tc_common.cuh"
+
+namespace kata {
+
+__device__ int g_tc64_error = 0;   // sticky: bounded waits that expired
+
+namespace {
+
+__device__ __forceinline__ void flag_error64(int code) { atomicOr(&g_tc64_error, code); }
+
+// ---- grouped feature layout at d = 64 (17 blocks of 128 slots, 2080 real)
+// Eight groups of eight coordinates.  Blocks 0-13 hold the 28 cross-group
+// 8 x 8 rectangles (X, Y), X < Y, in lexicographic order, one per 64-feature
+// atom column (rectangle 2b and 2b + 1 in block b); blocks 14-16 hold the eight
+// within-group triangles as one run of 40 chunks (5 per group): chunks 0-15,
+// 16-31 and 32-39, the last block using its first atom column only.  Rows,
+// triangles and the key factor 2 are as at d = 32.
+constexpr int kBlocks64 = 17;
+
+__device__ __forceinline__ Group8 group8_64(const PackedRow<64> &r, int g) {
+    Group8 o;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t a = (g & 1) ? r.w[4 + k] : r.w[k];
+        const uint32_t b = (g & 1) ? r.w[12 + k] : r.w[8 + k];
+        const uint32_t c = (g & 1) ? r.w[20 + k] : r.w[16 + k];
+        const uint32_t e = (g & 1) ? r.w[28 + k] : r.w[24 + k];
+        const uint32_t lo = (g & 2) ? b : a, hi = (g & 2) ? e : c;
+        o.w[k] = (g & 4) ? hi : lo;
+    }
+    return o;
+}
+
+// Rectangle r (0..27) -> groups (X, Y), X < Y, lexicographic.
+__device__ __forceinline__ void rect_pair64(int r, int &X, int &Y) {
+    X = 0;
+    int n = 7;   // rectangles whose first group is X: 7 - X
+    while (r >= n) {
+        r -= n;
+        ++X;
+        --n;
+    }
+    Y = X + 1 + r;
+}
+
+// Lift block b (0..16) of the d = 64 layout for one token.
+__device__ __forceinline__ void lift_block64(int b, const PackedRow<64> &r, uint32_t f,
+                                             const BlockRowRt &br) {
+    if (b < 14) {
+#pragma unroll 1
+        for (int rr = 0; rr < 2; ++rr) {
+            int X, Y;
+            rect_pair64(2 * b + rr, X, Y);
+            lift_rect_rt(group8_64(r, X), group8_64(r, Y), f, br, 8 * rr);
+        }
+    } else {
+        const int c0 = 16 * (b - 14), c1 = min(40, c0 + 16);
+#pragma unroll 1
+        for (int g = c0 / 5; g * 5 < c1; ++g)
+            lift_tri_rt(group8_64(r, g), f, br, max(0, c0 - 5 * g), min(5, c1 - 5 * g), 5 * g - c0);
+    }
+}
+
+// Blocks of feature group grp: [first, first + count).
+__device__ __forceinline__ int group_first(int grp) { return grp == 0 ? 0 : 2 + 5 * (grp - 1); }
+__device__ __forceinline__ int group_count(int grp) { return grp == 0 ? 2 : 5; }
+// Real features of block b (the last block holds 64).
+__device__ __forceinline__ int block_feats(int b) { return b == kBlocks64 - 1 ? 64 : 128; }
+
+// Lift role (out of line: its registers are allocated apart from the other roles).
+__device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
+                                            int b_first, int nb, int nch, uint64_t *chunk_full,
+                                            uint64_t *qk_empty, uint64_t *block_ready,
+                                            uint64_t *block_empty, volatile int *abort) {
+    const Sync sy{abort};
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+        ok = __all_sync(0xffffffffu, sy.wait(&chunk_full[i & 1], i >> 1));
+        if (!ok) break;
+        PackedRow<64> r;
+        tile_row_packed<64>(tile, t, r);
+        __syncwarp();
+        if (elect_lane0()) mbar_arrive(qk_empty);
+        for (int b = 0; b < nb && ok; ++b) {
+            const int gb = i * nb + b, ls = gb & 1, use = gb >> 1;
+            if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&block_empty[ls], use - 1));
+            if (!ok) break;
+            lift_block64(b_first + b, r, key ? kTwo2 : kOne2, block_row_rt(ring + ls * 65536, t));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&block_ready[ls]);
+        }
+    }
+}
+
+// ================================================================= output kernel
+// Grid (4 feature groups, B*H), 608 threads.  TMEM: S_run [0, 64 * nb) | (group 0:
+// G [128,192) | Q G_pre [192,256) | Q K^T quarter [256,288) | P slots [288,320)) |
+// output accumulator [320,384).  Shared memory: Q, K tiles (16 KB each, 128-byte
+// swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB | psi_k 32 KB], one
+// S_pre block (16 KB), G_pre bf16 [64][64] (8 KB).
+constexpr int kSmemWide = 2 * 16384 + 2 * 16384 + 2 * 65536 + 16384 + 8192 + 1024;
+
+__global__ void __launch_bounds__(608, 1)
+wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, float *__restrict__ part,
+                   float *__restrict__ dden, int T, int NCt) {
+    constexpr int D = 64, DV = 64;
+    constexpr int kQK = kTile * D * 2, kV = kTile * DV * 2;
+    constexpr int kLiftWarps = 8, kTmemWarps = 4;
+    constexpr int kWarpP = 7, kWarpLift = 11;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align1024(smem_raw);
+    uint8_t *tq = sm;
+    uint8_t *tk = sm + kQK;
+    uint8_t *tv = sm + 2 * kQK;                         // [2][16 KB]
+    uint8_t *lring = tv + 2 * kV;                       // [2][psi_q 32 KB | psi_k 32 KB]
+    uint8_t *spre = lring + 2 * 65536;                  // one S_pre block, 16 KB
+    uint8_t *gram = spre + 16384;                       // G_pre bf16, K-major, 8 KB
+    __shared__ __align__(8) uint64_t chunk_full[2], qk_empty, v_empty[2], xs_full, p_full[2],
+        p_empty[2], block_ready[2], block_empty[2], spre_empty, state_done[5], o_full, o_empty,
+        gram_done, qg_done, fin_bar[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int grp = blockIdx.x, bh = blockIdx.y;
+    const bool intra = grp == 0;
+    const int b_first = group_first(grp), nb = group_count(grp);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = NCt;
+    const Sync sy{&abort_flag};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        // Q/K tiles: read by the lift warps, and in group 0 by both MMA threads
+        // and the P warps
+        mbar_init(&qk_empty, kLiftWarps + (intra ? 2 + kTmemWarps : 0));
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&chunk_full[i], 1 + (intra ? kTmemWarps : 0));   // TMA (+ G_pre in group 0)
+            mbar_init(&v_empty[i], intra ? 2 : 1);
+            mbar_init(&block_ready[i], kLiftWarps + kTmemWarps);
+            mbar_init(&block_empty[i], 2);
+            mbar_init(&p_full[i], kTmemWarps);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&fin_bar[i], 1);
+        }
+        mbar_init(&xs_full, 1);
+        mbar_init(&spre_empty, 1);
+        for (int b = 0; b < 5; ++b) mbar_init(&state_done[b], 1);
+        mbar_init(&o_full, 1);
+        mbar_init(&o_empty, kTmemWarps);
+        mbar_init(&gram_done, 1);
+        mbar_init(&qg_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_base, tG = tmem_base + 128, tQG = tmem_base + 192;
+    const uint32_t tXs = tmem_base + 256, tP = tmem_base + 288, tXo = tmem_base + 320;
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (elect_lane0()) {
+            for (int i = 0; i < nch; ++i) {
+                const int t0 = i * kTile, st = i & 1, use = i >> 1;
+                if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
+                if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
+                mbar_arrive_expect_tx(&chunk_full[st], 2 * kQK + kV);
+                tma_load_3d(tq, &tm_q, 0, t0, bh, &chunk_full[st]);
+                tma_load_3d(tk, &tm_k, 0, t0, bh, &chunk_full[st]);
+                tma_load_3d(tv + st * kV, &tm_v, 0, t0, bh, &chunk_full[st]);
+                if (i + 1 < nch) {
+                    tma_prefetch_3d(&tm_q, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, bh);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================= output MMAs
+        if (elect_lane0()) {
+            constexpr uint32_t kIdQK = idesc_bf16(128, 32, false, false);
+            constexpr uint32_t kIdQG = idesc_bf16(128, D, false, false);
+            constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
+            const uint64_t dQ = smem_desc(smem_u32(tq), 16, 1024, kSw128);       // K-major A
+            const uint64_t dKb = smem_desc(smem_u32(tk), 16, 1024, kSw128);      // K-major B
+            const uint64_t dGr = smem_desc(smem_u32(gram), 16, 1024, kSw128);    // K-major B
+            const uint64_t dSp = smem_desc(smem_u32(spre), 16384, 1024, kSw128); // MN-major B
+            const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);   // MN-major B
+            const uint64_t dLq = smem_desc(smem_u32(lring), 16, 1024, kSw128);   // K-major A
+            auto qk_quarter = [&](int q) {   // Xs = Q K[32q .. 32q+31]^T
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, q * 4096 + ks * 32), kIdQK, ks > 0);
+                mma_commit(&xs_full);
+            };
+            // P of quarter q is ready: next quarter's Q K^T, then P V for quarter q
+            auto quarter_step = [&](int i, int q, uint32_t vo) -> bool {
+                const int n = 4 * i + q, slot = n & 1;
+                if (!sy.wait(&p_full[slot], n >> 1)) return false;
+                tc_fence_after();
+                if (q < 3) {
+                    qk_quarter(q + 1);
+                    if (q == 2) mma_commit(&qk_empty);
+                }
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_ts(tXo, tP + slot * 16 + ks * 8, desc_add(dV0, vo + (2 * q + ks) * 2048), kIdPV, 1u);
+                mma_commit(&p_empty[slot]);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i & 1;
+                const uint32_t vo = st * kV;
+                if (intra) {
+                    ok = sy.wait(&chunk_full[st], i >> 1);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
+                    mma_commit(&qg_done);
+                    qk_quarter(0);
+                }
+#pragma unroll 1
+                for (int b = 0; b < nb && ok; ++b) {
+                    const int gb = i * nb + b, ls = gb & 1;
+                    ok = sy.wait(&block_ready[ls], gb >> 1) &&
+                         (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t a0 = desc_add(dLq, ls * 65536);
+                    if (block_feats(b_first + b) == 128) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss(tXo, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                                   desc_add(dSp, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tXo, desc_add(a0, ks * 32), desc_add(dSp, ks * 2048), kIdPV,
+                                   (b > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&spre_empty);
+                    mma_commit(&block_empty[ls]);
+                    if (intra && b < 4) ok = quarter_step(i, b, vo);
+                }
+                for (int q = nb; intra && q < 4 && ok; ++q) ok = quarter_step(i, q, vo);
+                if (!ok) break;
+                mma_commit(&o_full);
+                if (intra) mma_commit(&v_empty[st]);
+            }
+            mma_commit(&fin_bar[0]);
+            sy.wait(&fin_bar[0], 0);
+        }
+    } else if (warp == 2) {
+        // ================= state MMAs
+        if (elect_lane0()) {
+            constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
+            constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
+            const uint64_t dKg = smem_desc(smem_u32(tk), 16384, 1024, kSw128);  // MN-major (Gram)
+            const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
+            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128);
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
+                const int st = i & 1;
+                const uint32_t vo = st * kV;
+                ok = sy.wait(&chunk_full[st], i >> 1);
+                if (!ok) break;
+                tc_fence_after();
+                if (intra) {   // G += K^T K, after the P warps have read G_pre for this chunk
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks) {
+                        const uint64_t a = desc_add(dKg, ks * 2048);
+                        mma_ss(tG, a, a, kIdGram, (i > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&gram_done);
+                    mma_commit(&qk_empty);
+                }
+#pragma unroll 1
+                for (int b = 0; b < nb && ok; ++b) {
+                    const int gb = i * nb + b, ls = gb & 1;
+                    ok = sy.wait(&block_ready[ls], gb >> 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t a0 = desc_add(dLk, ls * 65536), b0 = desc_add(dV0, vo);
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ss(tS + b * DV, desc_add(a0, ks * 2048), desc_add(b0, ks * 2048), kIdState,
+                               (i > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&state_done[b]);
+                    mma_commit(&block_empty[ls]);
+                }
+                if (!ok) break;
+                mma_commit(&v_empty[st]);
+            }
+            mma_commit(&fin_bar[1]);
+            sy.wait(&fin_bar[1], 0);
+        }
+    } else if (warp < kWarpP) {
+        // ================= convert warps: S_run block -> bf16 S_pre
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        bool ok = true;
+        for (int i = 0; i < nch && ok; ++i) {
+#pragma unroll 1
+            for (int b = 0; b < nb && ok; ++b) {
+                const int gb = i * nb + b, ss = gb & 1;
+                // S_pre of the first chunk is zero (one segment per head); the
+                // state MMAs start their accumulators from zero
+                bool w = (gb == 0 || sy.wait(&spre_empty, gb - 1)) &&
+                         (i == 0 || sy.wait(&state_done[b], i - 1));
+                ok = __all_sync(0xffffffffu, w);
+                if (!ok) break;
+                tc_fence_after();
+                if (quarter * 32 < block_feats(b_first + b)) {
+                    const uint32_t srow = smem_u32(spre + (row >> 3) * 1024 + (row & 7) * 128);
+#pragma unroll
+                    for (int c32 = 0; c32 < DV; c32 += 32) {
+                        uint32_t v[32];
+                        if (i > 0) tmem_ld32(tS + lsel + b * DV + c32, v);
+                        else
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = 0u;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int chunk = (c32 >> 3) + cc;
+                            st_shared_v4(srow + ((chunk ^ (row & 7)) << 4),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 0]), __uint_as_float(v[8 * cc + 1])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                         pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (elect_lane0()) mbar_arrive(&block_ready[ss]);
+            }
+        }
+    } else if (warp < kWarpLift) {
+        // ================= P warps: lane quarter q owns query rows 32q..32q+31
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        auto build_p = [&](int n, float &dsum) -> bool {
+            const int q = n & 3, slot = n & 1;
+            bool w = sy.wait(&xs_full, n) && (n < 2 || sy.wait(&p_empty[slot], (n >> 1) - 1));
+            w = __all_sync(0xffffffffu, w);
+            if (!w) return false;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(tXs + lsel, v);                 // warp-collective: always executed
+            uint32_t pw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int s = 32 * q + 2 * j;
+                const float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
+                const float w0 = s <= row ? x0 * x0 : 0.f;
+                const float w1 = s + 1 <= row ? x1 * x1 : 0.f;
+                dsum += w0;
+                dsum += w1;
+                pw[j] = pack_bf16(w0, w1);
+            }
+            tmem_st16(tP + lsel + slot * 16, pw);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&p_full[slot]);
+            return true;
+        };
+        // this group's numerator rows of chunk i (and the denominator in group 0)
+        auto epilogue = [&](int i, float dsum) -> bool {
+            bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
+            if (!w) return false;
+            tc_fence_after();
+            const int t = i * kTile + row;
+            float *dst = part + (((size_t)grp * gridDim.y + bh) * T + t) * DV;
+#pragma unroll
+            for (int c32 = 0; c32 < DV; c32 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tXo + lsel + c32, v);
+                if (t < T) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&o_empty);
+            if (intra && t < T) dden[(size_t)bh * T + t] = dsum;
+            return true;
+        };
+        // G rows r = 32 * quarter + lane (quarters 0-1) -> bf16 [64][64] K-major,
+        // 128-byte swizzle; from_tmem false: zero (G_pre of the first chunk; the
+        // first Gram MMA overwrites the accumulator)
+        auto gram_to_smem = [&](bool from_tmem) {
+            if (quarter >= 2) return;
+#pragma unroll
+            for (int c32 = 0; c32 < D; c32 += 32) {
+                uint32_t v[32];
+                if (from_tmem) tmem_ld32(tG + lsel + c32, v);
+                else
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int chunk = (c32 >> 3) + cc;
+                    *reinterpret_cast<uint4 *>(gram + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(pack_bf16(__uint_as_float(v[8 * cc + 0]), __uint_as_float(v[8 * cc + 1])),
+                                   pack_bf16(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                   pack_bf16(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                   pack_bf16(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                }
+            }
+        };
+        // q^T G_pre q (Q G_pre from TMEM, q from the Q tile), then G -> bf16 for chunk i + 1
+        auto d_inter = [&](int i, float &dsum) -> bool {
+            bool w = __all_sync(0xffffffffu, sy.wait(&chunk_full[i & 1], i >> 1) &&
+                                                 sy.wait(&qg_done, i) && sy.wait(&gram_done, i));
+            if (!w) return false;
+            tc_fence_after();
+            PackedRow<D> r;
+            tile_row_packed<D>(tq, row, r);
+#pragma unroll
+            for (int c32 = 0; c32 < D; c32 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tQG + lsel + c32, v);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const uint32_t pr = r.w[c32 / 2 + m];
+                    dsum = fmaf(__uint_as_float(v[2 * m]), __uint_as_float(pr << 16), dsum);
+                    dsum = fmaf(__uint_as_float(v[2 * m + 1]), __uint_as_float(pr & 0xFFFF0000u), dsum);
+                }
+            }
+            gram_to_smem(true);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) {
+                mbar_arrive(&chunk_full[(i + 1) & 1]);   // G_pre of chunk i + 1
+                mbar_arrive(&qk_empty);
+            }
+            return true;
+        };
+
+        bool ok = true;
+        if (intra) {
+            gram_to_smem(false);   // G_pre of the first chunk: zero
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&chunk_full[0]);
+        }
+        float dprev = 0.f;
+        for (int i = 0; i <= nch && ok; ++i) {   // chunk i's P and denominators, chunk i-1's output
+            if (i > 0) ok = epilogue(i - 1, dprev);
+            if (i == nch || !intra) continue;
+            float dsum = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < 4 && ok; ++q) {
+                ok = build_p(4 * i + q, dsum);
+                if (ok && q == 0) ok = d_inter(i, dsum);
+            }
+            dprev = dsum;
+        }
+    } else {
+        // ================= lift warps: token t, side (0 query, 1 key)
+        const int lw = warp - kWarpLift;
+        const int side = lw >> 2;
+        wide_lift_role(side ? tk : tq, lring + side * 32768, (lw & 3) * 32 + lane, side != 0,
+                       b_first, nb, nch, chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) flag_error64(4);
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// O = (N_0 + N_1 + N_2 + N_3) / D in bf16 (zero where D = 0); one thread per
+// four output values.
+__global__ void __launch_bounds__(256)
+wide_finalize_kernel(const float *__restrict__ part, const float *__restrict__ dden,
+                     __nv_bfloat16 *__restrict__ out, int64_t rows, int64_t stride) {
+    const int64_t n4 = rows * 16;   // 64 values per row
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = e >> 4;
+        const float4 *p = reinterpret_cast<const float4 *>(part) + e;
+        float4 s = p[0];
+#pragma unroll
+        for (int g = 1; g < 4; ++g) {
+            const float4 x = p[g * stride / 4];
+            s.x += x.x;
+            s.y += x.y;
+            s.z += x.z;
+            s.w += x.w;
+        }
+        const float dd = dden[row];
+        const float inv = dd > 0.f ? 1.f / dd : 0.f;
+        __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(out) + 2 * e;
+        o[0] = __floats2bfloat162_rn(s.x * inv, s.y * inv);
+        o[1] = __floats2bfloat162_rn(s.z * inv, s.w * inv);
+    }
+}
+
+}  // namespace
+
+// ================================================================= host side
+bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms) {
+    return s.dtype == 1 && cc_major == 10 && cc_minor == 3 && s.d == 64 && s.dv == 64 &&
+           (int64_t)4 * s.BH() >= num_sms && s.BH() <= 65535 && encoder() != nullptr;
+}
+
+size_t tc64_workspace_bytes(const FwdShape &s) {
+    const size_t rows = (size_t)s.BH() * s.T;
+    return sizeof(float) * (rows * 64 * 4 + rows);
+}
+
+cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
+                         void *workspace, cudaStream_t stream) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
+        !make_map(mv, v, s.dv, s.T, s.BH()))
+        return cudaErrorInvalidValue;
+    const int NCt = (s.T + kTile - 1) / kTile;
+    const size_t rows = (size_t)s.BH() * s.T;
+    if (rows == 0) return cudaSuccess;
+    float *part = static_cast<float *>(workspace);
+    float *dden = part + rows * 64 * 4;
+    cudaFuncSetAttribute(wide_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemWide);
+    {
+        TraceScope tr("tc64_output", stream);
+        wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, part, dden, s.T,
+                                                                        NCt);
+    }
+    {
+        TraceScope tr("tc64_finalize", stream);
+        const int64_t n4 = (int64_t)rows * 16;
+        const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+        wide_finalize_kernel<<<blocks, 256, 0, stream>>>(part, dden, (__nv_bfloat16 *)out,
+                                                          (int64_t)rows, (int64_t)rows * 64);
+    }
+    return cudaGetLastError();
+}
+
+int tc64_take_error() {
+    int h = 0;
+    if (cudaMemcpyFromSymbol(&h, g_tc64_error, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (h) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_tc64_error, &zero, sizeof(int));
+    }
+    return h;
+}
+
+}  // namespace kata

@@ -156,3 +156,36 @@ def test_tensor_path_segmentation(kg, B, H, T):
     q, k, v = workloads.make_qkv(w)
     _check_full(kg, q, k, v, w.C)
     assert kg.kata_sync_status() == kg.KATA_OK
+
+
+@pytest.mark.parametrize("B,H,T", [
+    (1, 38, 300),    # 38 heads: the fewest that fill 152 SMs with four CTAs each; ragged tail
+    (2, 19, 129),    # last chunk holds one token
+    (4, 10, 5),      # a single partial chunk
+    (8, 16, 640),    # the layer's 128 heads, five whole chunks
+])
+def test_d64_tensor_path(kg, B, H, T):
+    """d = 64: the state (17 feature blocks) split over four CTAs per head,
+    partial numerators summed in a separate pass."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+    assert kg.kata_sync_status() == kg.KATA_OK
+
+
+def test_d64_few_heads_use_cuda_cores(kg):
+    """Fewer than 38 heads at d = 64 would leave SMs idle on the split path."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=37, T=200)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_SIMT
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+
+
+def test_d64_tensor_path_deterministic(kg):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=19, T=700)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked(q, k, v, w.C)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

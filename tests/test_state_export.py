@@ -65,6 +65,8 @@ def test_state_tensor_path(kg, B, H, T):
     ("small_fp32", dict(B=2, H=3, T=300)),
     ("small_fp32", dict(B=1, H=2, T=97, d=32, dv=64, C=32)),
     ("lm_layer_bf16", dict(B=1, H=2, T=333)),           # d = 64: CUDA-core path in bf16
+    ("lm_layer_bf16", dict(B=2, H=19, T=300)),          # d = 64, 38 heads: the state
+                                                        # export stays on CUDA cores
     ("mid_bf16", dict(B=1, H=2, T=200, dv=128, C=64)),  # dv = 128: CUDA-core path
 ])
 def test_state_cuda_core_path(kg, name, overrides):
