@@ -16,8 +16,8 @@
 // The kernel keeps one segment per head: it is used when the four groups of all
 // heads fill the GPU (4 * B * H >= SM count).  Structure per CTA as in the d = 32
 // output kernel: warp 0 TMA, warps 1-2 MMA issue (output / state), warps 3-6
-// convert S_run -> bf16 S_pre (one shared-memory slot), warps 7-10 P and the
-// epilogue, warps 11-18 lift the group's blocks.
+// convert S_run -> bf16 S_pre, warps 7-10 P and the epilogue, warps 11-18 lift
+// the group's blocks.
 #include "kata_tc_common.cuh"
 
 namespace kata {
@@ -63,7 +63,9 @@ __device__ __forceinline__ void rect_pair64(int r, int &X, int &Y) {
     Y = X + 1 + r;
 }
 
-// Lift block b (0..16) of the d = 64 layout for one token.
+// Lift block b (0..16) of the d = 64 layout for one token.  Groups are chosen
+// at run time: one copy of the code serves every block and every feature group
+// (per-group compile-time copies were slower, through instruction fetch).
 __device__ __forceinline__ void lift_block64(int b, const PackedRow<64> &r, uint32_t f,
                                              const BlockRowRt &br) {
     if (b < 14) {
@@ -117,14 +119,24 @@ __device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, 
 // Grid (4 feature groups, B*H), 608 threads.  TMEM: S_run [0, 64 * nb) | (group 0:
 // G [128,192) | Q G_pre [192,256) | Q K^T quarter [256,288) | P slots [288,320)) |
 // output accumulator [320,384).  Shared memory: Q, K tiles (16 KB each, 128-byte
-// swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB | psi_k 32 KB], one
-// S_pre block (16 KB), G_pre bf16 [64][64] (8 KB).
-constexpr int kSmemWide = 2 * 16384 + 2 * 16384 + 2 * 65536 + 16384 + 8192 + 1024;
+// swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB | psi_k 32 KB], and
+// [2][16 KB] for S_pre: two blocks in groups 1-3 (the convert of block b + 1
+// overlaps the MMAs of block b), one block plus G_pre bf16 [64][64] in group 0.
+//
+// Epilogue.  In groups 1-3 only the lift warps read the Q and K tiles, once per
+// chunk into registers, so from then until the next chunk's TMA load the 32 KB
+// of the two tiles stage the partial numerators: fp32 [128][64] as four warp
+// quarters of two 128-byte-swizzled [32 x 32] boxes, written to memory by TMA
+// stores (whole lines, and no load/store-unit work while the lift runs).  The
+// TMA load of chunk i + 2 waits for the stores of chunk i to have read the
+// staging (stage_free).  Group 0, whose tiles feed its MMAs through the chunk,
+// writes its rows with 32-byte stores.
+constexpr int kSmemWide = 2 * 16384 + 2 * 16384 + 2 * 65536 + 2 * 16384 + 1024;
 
 __global__ void __launch_bounds__(608, 1)
 wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, float *__restrict__ part,
-                   float *__restrict__ dden, int T, int NCt) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_part,
+                   float *__restrict__ part, float *__restrict__ dden, int T, int NCt) {
     constexpr int D = 64, DV = 64;
     constexpr int kQK = kTile * D * 2, kV = kTile * DV * 2;
     constexpr int kLiftWarps = 8, kTmemWarps = 4;
@@ -135,11 +147,12 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t *tk = sm + kQK;
     uint8_t *tv = sm + 2 * kQK;                         // [2][16 KB]
     uint8_t *lring = tv + 2 * kV;                       // [2][psi_q 32 KB | psi_k 32 KB]
-    uint8_t *spre = lring + 2 * 65536;                  // one S_pre block, 16 KB
-    uint8_t *gram = spre + 16384;                       // G_pre bf16, K-major, 8 KB
+    uint8_t *spre = lring + 2 * 65536;                  // S_pre blocks [2][16 KB]
+    uint8_t *gram = spre + 16384;                       // group 0: G_pre bf16, K-major, 8 KB
+    uint8_t *stage = tq;                                // groups 1-3: epilogue staging (Q, K tiles)
     __shared__ __align__(8) uint64_t chunk_full[2], qk_empty, v_empty[2], xs_full, p_full[2],
-        p_empty[2], block_ready[2], block_empty[2], spre_empty, state_done[5], o_full, o_empty,
-        gram_done, qg_done, fin_bar[2];
+        p_empty[2], block_ready[2], block_empty[2], spre_empty[2], state_done[5], o_full,
+        o_empty, gram_done, qg_done, fin_bar[2], stage_free;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -163,9 +176,10 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&p_full[i], kTmemWarps);
             mbar_init(&p_empty[i], 1);
             mbar_init(&fin_bar[i], 1);
+            mbar_init(&spre_empty[i], 1);
         }
         mbar_init(&xs_full, 1);
-        mbar_init(&spre_empty, 1);
+        mbar_init(&stage_free, kTmemWarps);
         for (int b = 0; b < 5; ++b) mbar_init(&state_done[b], 1);
         mbar_init(&o_full, 1);
         mbar_init(&o_empty, kTmemWarps);
@@ -190,6 +204,8 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int t0 = i * kTile, st = i & 1, use = i >> 1;
                 if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
+                // groups 1-3: the staging (these tiles) of chunk i - 2 has been stored
+                if (!intra && i >= 2 && !sy.wait(&stage_free, i - 2)) break;
                 mbar_arrive_expect_tx(&chunk_full[st], 2 * kQK + kV);
                 tma_load_3d(tq, &tm_q, 0, t0, bh, &chunk_full[st]);
                 tma_load_3d(tk, &tm_k, 0, t0, bh, &chunk_full[st]);
@@ -255,19 +271,20 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                          (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t a0 = desc_add(dLq, ls * 65536);
+                    const int sp = intra ? 0 : ls;   // S_pre slot
+                    const uint64_t a0 = desc_add(dLq, ls * 65536), b0 = desc_add(dSp, sp * 16384);
                     if (block_feats(b_first + b) == 128) {
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
                             mma_ss(tXo, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
-                                   desc_add(dSp, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
+                                   desc_add(b0, ks * 2048), kIdPV, (b > 0 || ks > 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_ss(tXo, desc_add(a0, ks * 32), desc_add(dSp, ks * 2048), kIdPV,
+                            mma_ss(tXo, desc_add(a0, ks * 32), desc_add(b0, ks * 2048), kIdPV,
                                    (b > 0 || ks > 0) ? 1u : 0u);
                     }
-                    mma_commit(&spre_empty);
+                    mma_commit(&spre_empty[sp]);
                     mma_commit(&block_empty[ls]);
                     if (intra && b < 4) ok = quarter_step(i, b, vo);
                 }
@@ -286,7 +303,7 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
             const uint64_t dKg = smem_desc(smem_u32(tk), 16384, 1024, kSw128);  // MN-major (Gram)
             const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
-            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128);
+            const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128); // MN-major A
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
@@ -333,15 +350,17 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll 1
             for (int b = 0; b < nb && ok; ++b) {
                 const int gb = i * nb + b, ss = gb & 1;
+                const int sp = intra ? 0 : ss, suse = intra ? gb : gb >> 1;   // S_pre slot, use
                 // S_pre of the first chunk is zero (one segment per head); the
                 // state MMAs start their accumulators from zero
-                bool w = (gb == 0 || sy.wait(&spre_empty, gb - 1)) &&
+                bool w = (suse == 0 || sy.wait(&spre_empty[sp], suse - 1)) &&
                          (i == 0 || sy.wait(&state_done[b], i - 1));
                 ok = __all_sync(0xffffffffu, w);
                 if (!ok) break;
                 tc_fence_after();
                 if (quarter * 32 < block_feats(b_first + b)) {
-                    const uint32_t srow = smem_u32(spre + (row >> 3) * 1024 + (row & 7) * 128);
+                    const uint32_t srow =
+                        smem_u32(spre + sp * 16384 + (row >> 3) * 1024 + (row & 7) * 128);
 #pragma unroll
                     for (int c32 = 0; c32 < DV; c32 += 32) {
                         uint32_t v[32];
@@ -397,29 +416,50 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (elect_lane0()) mbar_arrive(&p_full[slot]);
             return true;
         };
-        // this group's numerator rows of chunk i (and the denominator in group 0)
+        // This group's numerator rows of chunk i (and the denominator in group
+        // 0).  The accumulator is read into registers and released at once.
+        uint8_t *sq = stage + quarter * 8192;
         auto epilogue = [&](int i, float dsum) -> bool {
             bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
             if (!w) return false;
             tc_fence_after();
-            const int t = i * kTile + row;
-            float *dst = part + (((size_t)grp * gridDim.y + bh) * T + t) * DV;
-#pragma unroll
-            for (int c32 = 0; c32 < DV; c32 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tXo + lsel + c32, v);
-                if (t < T) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c32);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-                }
-            }
+            const int t0 = i * kTile + quarter * 32, t = t0 + lane;
+            uint32_t v[DV];
+            tmem_ld64(tXo + lsel, v);
             tc_fence_before();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&o_empty);
-            if (intra && t < T) dden[(size_t)bh * T + t] = dsum;
+            if (intra) {
+                if (t < T) {
+                    dden[(size_t)bh * T + t] = dsum;
+                    float *dst = part + ((size_t)bh * T + t) * DV;   // group 0's partials
+#pragma unroll
+                    for (int e = 0; e < DV / 8; ++e) st_global_v8(dst + 8 * e, v + 8 * e);
+                }
+                return true;
+            }
+            // the tiles hold chunk i + 1 until the lift warps have read it
+            w = __all_sync(0xffffffffu, sy.wait(&qk_empty, min(i + 1, nch - 1)));
+            if (!w) return false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(smem_u32(sq + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                                 v[32 * h + 4 * c], v[32 * h + 4 * c + 1], v[32 * h + 4 * c + 2],
+                                 v[32 * h + 4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (elect_lane0()) {
+                if (t0 < T) {   // rows past T are clipped by the store
+                    const int z = grp * (int)gridDim.y + bh;
+                    tma_store_3d(&tm_part, 0, t0, z, sq);
+                    tma_store_3d(&tm_part, 32, t0, z, sq + 4096);
+                    bulk_commit();
+                }
+                bulk_wait_read_all();
+                mbar_arrive(&stage_free);
+            }
             return true;
         };
         // G rows r = 32 * quarter + lane (quarters 0-1) -> bf16 [64][64] K-major,
@@ -495,6 +535,7 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             dprev = dsum;
         }
+        if (elect_lane0()) bulk_wait_all();
     } else {
         // ================= lift warps: token t, side (0 query, 1 key)
         const int lw = warp - kWarpLift;
@@ -538,6 +579,20 @@ wide_finalize_kernel(const float *__restrict__ part, const float *__restrict__ d
 }  // namespace
 
 // ================================================================= host side
+// The partial numerators part[4 * BH][T][64] fp32 as a 3-D tensor for TMA
+// stores; box = [32 rows x 32 floats] (128 bytes, 128-byte swizzle).
+bool make_part_map(CUtensorMap &m, void *base, int T, int Z) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)Z};
+    const cuuint64_t strides[2] = {64 * 4, (cuuint64_t)T * 64 * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms) {
     return s.dtype == 1 && cc_major == 10 && cc_minor == 3 && s.d == 64 && s.dv == 64 &&
            (int64_t)4 * s.BH() >= num_sms && s.BH() <= 65535 && encoder() != nullptr;
@@ -550,20 +605,20 @@ size_t tc64_workspace_bytes(const FwdShape &s) {
 
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
                          void *workspace, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
-    if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
-        !make_map(mv, v, s.dv, s.T, s.BH()))
-        return cudaErrorInvalidValue;
     const int NCt = (s.T + kTile - 1) / kTile;
     const size_t rows = (size_t)s.BH() * s.T;
     if (rows == 0) return cudaSuccess;
     float *part = static_cast<float *>(workspace);
     float *dden = part + rows * 64 * 4;
+    CUtensorMap mq, mk, mv, mp;
+    if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
+        !make_map(mv, v, s.dv, s.T, s.BH()) || !make_part_map(mp, part, s.T, 4 * s.BH()))
+        return cudaErrorInvalidValue;
     cudaFuncSetAttribute(wide_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemWide);
     {
         TraceScope tr("tc64_output", stream);
-        wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, part, dden, s.T,
-                                                                        NCt);
+        wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, part, dden,
+                                                                        s.T, NCt);
     }
     {
         TraceScope tr("tc64_finalize", stream);
