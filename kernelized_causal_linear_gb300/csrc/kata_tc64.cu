@@ -37,20 +37,6 @@ __device__ __forceinline__ void flag_error64(int code) { atomicOr(&g_tc64_error,
 // triangles and the key factor 2 are as at d = 32.
 constexpr int kBlocks64 = 17;
 
-__device__ __forceinline__ Group8 group8_64(const PackedRow<64> &r, int g) {
-    Group8 o;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t a = (g & 1) ? r.w[4 + k] : r.w[k];
-        const uint32_t b = (g & 1) ? r.w[12 + k] : r.w[8 + k];
-        const uint32_t c = (g & 1) ? r.w[20 + k] : r.w[16 + k];
-        const uint32_t e = (g & 1) ? r.w[28 + k] : r.w[24 + k];
-        const uint32_t lo = (g & 2) ? b : a, hi = (g & 2) ? e : c;
-        o.w[k] = (g & 4) ? hi : lo;
-    }
-    return o;
-}
-
 // Rectangle r (0..27) -> groups (X, Y), X < Y, lexicographic.
 __device__ __forceinline__ void rect_pair64(int r, int &X, int &Y) {
     X = 0;
@@ -63,23 +49,30 @@ __device__ __forceinline__ void rect_pair64(int r, int &X, int &Y) {
     Y = X + 1 + r;
 }
 
-// Lift block b (0..16) of the d = 64 layout for one token.  Groups are chosen
-// at run time: one copy of the code serves every block and every feature group
-// (per-group compile-time copies were slower, through instruction fetch).
-__device__ __forceinline__ void lift_block64(int b, const PackedRow<64> &r, uint32_t f,
-                                             const BlockRowRt &br) {
+// Lift block b (0..16) of the d = 64 layout for one token whose row (bf16
+// pairs, group g = columns 4g .. 4g + 3) sits in TMEM at trow.  The groups a
+// block needs are chosen at run time, so one copy of the code serves every
+// block and every feature group (per-group compile-time copies were slower,
+// through instruction fetch); fetching a group from TMEM at a warp-uniform
+// column costs one load, where selecting it from registers took 28 ALU selects.
+__device__ __forceinline__ void lift_block64(int b, uint32_t trow, uint32_t f, const BlockRowRt &br) {
     if (b < 14) {
 #pragma unroll 1
         for (int rr = 0; rr < 2; ++rr) {
             int X, Y;
             rect_pair64(2 * b + rr, X, Y);
-            lift_rect_rt(group8_64(r, X), group8_64(r, Y), f, br, 8 * rr);
+            Group8 gx, gy;
+            tmem_ld4x2(trow + 4 * X, trow + 4 * Y, gx.w, gy.w);
+            lift_rect_rt(gx, gy, f, br, 8 * rr);
         }
     } else {
         const int c0 = 16 * (b - 14), c1 = min(40, c0 + 16);
 #pragma unroll 1
-        for (int g = c0 / 5; g * 5 < c1; ++g)
-            lift_tri_rt(group8_64(r, g), f, br, max(0, c0 - 5 * g), min(5, c1 - 5 * g), 5 * g - c0);
+        for (int g = c0 / 5; g * 5 < c1; ++g) {
+            Group8 gg;
+            tmem_ld4(trow + 4 * g, gg.w);
+            lift_tri_rt(gg, f, br, max(0, c0 - 5 * g), min(5, c1 - 5 * g), 5 * g - c0);
+        }
     }
 }
 
@@ -89,9 +82,12 @@ __device__ __forceinline__ int group_count(int grp) { return grp == 0 ? 2 : 5; }
 // Real features of block b (the last block holds 64).
 __device__ __forceinline__ int block_feats(int b) { return b == kBlocks64 - 1 ? 64 : 128; }
 
-// Lift role (out of line: its registers are allocated apart from the other roles).
+// Lift role (out of line: its registers are allocated apart from the other
+// roles).  Token t = 32 * (warp % 4) + lane: its row is parked in TMEM lane t
+// (the warp's lane quarter), columns trow .. trow + 31, once per chunk.
 __device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
-                                            int b_first, int nb, int nch, uint64_t *chunk_full,
+                                            uint32_t trow, int b_first, int nb, int nch,
+                                            uint64_t *chunk_full,
                                             uint64_t *qk_empty, uint64_t *block_ready,
                                             uint64_t *block_empty, volatile int *abort) {
     const Sync sy{abort};
@@ -99,15 +95,19 @@ __device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, 
     for (int i = 0; i < nch && ok; ++i) {
         ok = __all_sync(0xffffffffu, sy.wait(&chunk_full[i & 1], i >> 1));
         if (!ok) break;
-        PackedRow<64> r;
-        tile_row_packed<64>(tile, t, r);
+        {
+            PackedRow<64> r;
+            tile_row_packed<64>(tile, t, r);
+            tmem_st32(trow, r.w);   // the previous chunk's loads of these columns have completed
+            tmem_st_wait();
+        }
         __syncwarp();
         if (elect_lane0()) mbar_arrive(qk_empty);
         for (int b = 0; b < nb && ok; ++b) {
             const int gb = i * nb + b, ls = gb & 1, use = gb >> 1;
             if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&block_empty[ls], use - 1));
             if (!ok) break;
-            lift_block64(b_first + b, r, key ? kTwo2 : kOne2, block_row_rt(ring + ls * 65536, t));
+            lift_block64(b_first + b, trow, key ? kTwo2 : kOne2, block_row_rt(ring + ls * 65536, t));
             fence_proxy_async_smem();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&block_ready[ls]);
@@ -118,7 +118,7 @@ __device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, 
 // ================================================================= output kernel
 // Grid (4 feature groups, B*H), 608 threads.  TMEM: S_run [0, 64 * nb) | (group 0:
 // G [128,192) | Q G_pre [192,256) | Q K^T quarter [256,288) | P slots [288,320)) |
-// output accumulator [320,384).  Shared memory: Q, K tiles (16 KB each, 128-byte
+// output accumulator [320,384) | the lift warps' q and k rows [384,416) [416,448).  Shared memory: Q, K tiles (16 KB each, 128-byte
 // swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB | psi_k 32 KB], and
 // [2][16 KB] for S_pre: two blocks in groups 1-3 (the convert of block b + 1
 // overlaps the MMAs of block b), one block plus G_pre bf16 [64][64] in group 0.
@@ -538,10 +538,11 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (elect_lane0()) bulk_wait_all();
     } else {
         // ================= lift warps: token t, side (0 query, 1 key)
-        const int lw = warp - kWarpLift;
-        const int side = lw >> 2;
-        wide_lift_role(side ? tk : tq, lring + side * 32768, (lw & 3) * 32 + lane, side != 0,
-                       b_first, nb, nch, chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
+        const int side = (warp - kWarpLift) >> 2;
+        const int quarter = warp & 3;   // TMEM lane quarter of this warp
+        wide_lift_role(side ? tk : tq, lring + side * 32768, quarter * 32 + lane, side != 0,
+                       tmem_base + 384 + 32 * side + ((uint32_t)(quarter * 32) << 16), b_first, nb,
+                       nch, chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
     }
     tc_fence_before();
     __syncthreads();
