@@ -104,6 +104,12 @@ def stage_work(stage: str, w, num_sms: int = SMS):
         if stage == "tc_segment_scan":
             rec = 4.0 * (5 * 128 * dv + d * d)
             return 2.0 * rec * G * BH, "GB/s", "hbm"
+    if stage == "tc64_output":
+        intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH
+        return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
+    if stage == "tc64_finalize":
+        # reads four fp32 partial numerators and the denominator, writes bf16 out
+        return float(BH * T) * (4 * dv * 4 + 4 + dv * 2), "GB/s", "hbm"
     return None, "", ""
 
 

@@ -117,26 +117,34 @@ __device__ __noinline__ void wide_lift_role(const uint8_t *tile, uint8_t *ring, 
 
 // ================================================================= output kernel
 // Grid (4 feature groups, B*H), 608 threads.  TMEM: S_run [0, 64 * nb) | (group 0:
-// G [128,192) | Q G_pre [192,256) | Q K^T quarter [256,288) | P slots [288,320)) |
-// output accumulator [320,384) | the lift warps' q and k rows [384,416) [416,448).  Shared memory: Q, K tiles (16 KB each, 128-byte
-// swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB | psi_k 32 KB], and
-// [2][16 KB] for S_pre: two blocks in groups 1-3 (the convert of block b + 1
-// overlaps the MMAs of block b), one block plus G_pre bf16 [64][64] in group 0.
+// G [128,192) | Q G_pre [192,256) | Q K^T [256,384), P of key quarter q written
+// over the first 16 columns of its 32) | output accumulator [384,448) | the lift
+// warps' q and k rows [448,480) [480,512).  Shared memory: Q, K tiles (16 KB
+// each, 128-byte swizzle), V tiles [2][16 KB], lift ring [2][psi_q 32 KB |
+// psi_k 32 KB], and [2][16 KB] for S_pre: two blocks in groups 1-3 (the convert
+// of block b + 1 overlaps the MMAs of block b); in group 0 one block, G_pre bf16
+// [64][64] (8 KB) and the epilogue staging (8 KB).
+//
+// Group 0 computes Q K^T of a chunk with one N = 128 MMA; the P warps turn
+// each 32-key quarter into P in place and release it (p_full[q]) for its P V
+// MMA, so no quarter waits on a Q K^T round trip.
 //
 // Epilogue.  In groups 1-3 only the lift warps read the Q and K tiles, once per
-// chunk into registers, so from then until the next chunk's TMA load the 32 KB
-// of the two tiles stage the partial numerators: fp32 [128][64] as four warp
-// quarters of two 128-byte-swizzled [32 x 32] boxes, written to memory by TMA
-// stores (whole lines, and no load/store-unit work while the lift runs).  The
-// TMA load of chunk i + 2 waits for the stores of chunk i to have read the
-// staging (stage_free).  Group 0, whose tiles feed its MMAs through the chunk,
-// writes its rows with 32-byte stores.
+// chunk, so from then until the next chunk's TMA load the 32 KB of the two
+// tiles stage the partial numerators: fp32 [128][64] as four warp quarters of
+// two 128-byte-swizzled [32 x 32] boxes, written to memory by TMA stores (whole
+// lines, and no load/store-unit work while the lift runs).  The TMA load of
+// chunk i + 2 waits for the stores of chunk i to have read the staging
+// (stage_free).  In group 0, whose tiles feed its MMAs through the chunk, the
+// convert warps (two blocks a chunk leave them idle most of the time) store the
+// rows through an 8 KB staging area as [32 x 16] boxes, 64-byte swizzled.
 constexpr int kSmemWide = 2 * 16384 + 2 * 16384 + 2 * 65536 + 2 * 16384 + 1024;
 
 __global__ void __launch_bounds__(608, 1)
 wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_part,
-                   float *__restrict__ part, float *__restrict__ dden, int T, int NCt) {
+                   const __grid_constant__ CUtensorMap tm_part16, float *__restrict__ dden, int T,
+                   int NCt) {
     constexpr int D = 64, DV = 64;
     constexpr int kQK = kTile * D * 2, kV = kTile * DV * 2;
     constexpr int kLiftWarps = 8, kTmemWarps = 4;
@@ -150,9 +158,10 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t *spre = lring + 2 * 65536;                  // S_pre blocks [2][16 KB]
     uint8_t *gram = spre + 16384;                       // group 0: G_pre bf16, K-major, 8 KB
     uint8_t *stage = tq;                                // groups 1-3: epilogue staging (Q, K tiles)
-    __shared__ __align__(8) uint64_t chunk_full[2], qk_empty, v_empty[2], xs_full, p_full[2],
-        p_empty[2], block_ready[2], block_empty[2], spre_empty[2], state_done[5], o_full,
-        o_empty, gram_done, qg_done, fin_bar[2], stage_free;
+    uint8_t *gstage = gram + 8192;                      // group 0: epilogue staging, 4 x 2 KB
+    __shared__ __align__(8) uint64_t chunk_full[2], qk_empty, v_empty[2], xs_full, p_full[4],
+        pv_done, block_ready[2], block_empty[2], spre_empty[2], state_done[5], o_full, o_empty,
+        gram_done, qg_done, fin_bar[2], stage_free;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -173,12 +182,12 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&v_empty[i], intra ? 2 : 1);
             mbar_init(&block_ready[i], kLiftWarps + kTmemWarps);
             mbar_init(&block_empty[i], 2);
-            mbar_init(&p_full[i], kTmemWarps);
-            mbar_init(&p_empty[i], 1);
             mbar_init(&fin_bar[i], 1);
             mbar_init(&spre_empty[i], 1);
         }
         mbar_init(&xs_full, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&p_full[q], kTmemWarps);
+        mbar_init(&pv_done, 1);
         mbar_init(&stage_free, kTmemWarps);
         for (int b = 0; b < 5; ++b) mbar_init(&state_done[b], 1);
         mbar_init(&o_full, 1);
@@ -195,7 +204,7 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tS = tmem_base, tG = tmem_base + 128, tQG = tmem_base + 192;
-    const uint32_t tXs = tmem_base + 256, tP = tmem_base + 288, tXo = tmem_base + 320;
+    const uint32_t tXs = tmem_base + 256, tXo = tmem_base + 384;
 
     if (warp == 0) {
         // ================= TMA producer
@@ -220,7 +229,7 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     } else if (warp == 1) {
         // ================= output MMAs
         if (elect_lane0()) {
-            constexpr uint32_t kIdQK = idesc_bf16(128, 32, false, false);
+            constexpr uint32_t kIdQK = idesc_bf16(128, kTile, false, false);
             constexpr uint32_t kIdQG = idesc_bf16(128, D, false, false);
             constexpr uint32_t kIdPV = idesc_bf16(128, DV, false, true);
             const uint64_t dQ = smem_desc(smem_u32(tq), 16, 1024, kSw128);       // K-major A
@@ -229,25 +238,13 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint64_t dSp = smem_desc(smem_u32(spre), 16384, 1024, kSw128); // MN-major B
             const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);   // MN-major B
             const uint64_t dLq = smem_desc(smem_u32(lring), 16, 1024, kSw128);   // K-major A
-            auto qk_quarter = [&](int q) {   // Xs = Q K[32q .. 32q+31]^T
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, q * 4096 + ks * 32), kIdQK, ks > 0);
-                mma_commit(&xs_full);
-            };
-            // P of quarter q is ready: next quarter's Q K^T, then P V for quarter q
-            auto quarter_step = [&](int i, int q, uint32_t vo) -> bool {
-                const int n = 4 * i + q, slot = n & 1;
-                if (!sy.wait(&p_full[slot], n >> 1)) return false;
+            // P of key quarter q is ready: Xo += P_q V[32q .. 32q + 31]
+            auto pv_quarter = [&](int i, int q, uint32_t vo) -> bool {
+                if (!sy.wait(&p_full[q], i)) return false;
                 tc_fence_after();
-                if (q < 3) {
-                    qk_quarter(q + 1);
-                    if (q == 2) mma_commit(&qk_empty);
-                }
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    mma_ts(tXo, tP + slot * 16 + ks * 8, desc_add(dV0, vo + (2 * q + ks) * 2048), kIdPV, 1u);
-                mma_commit(&p_empty[slot]);
+                    mma_ts(tXo, tXs + 32 * q + ks * 8, desc_add(dV0, vo + (2 * q + ks) * 2048), kIdPV, 1u);
                 return true;
             };
             bool ok = true;
@@ -262,7 +259,18 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     for (int ks = 0; ks < D / 16; ++ks)
                         mma_ss(tQG, desc_add(dQ, ks * 32), desc_add(dGr, ks * 32), kIdQG, ks > 0);
                     mma_commit(&qg_done);
-                    qk_quarter(0);
+                    // Xs = Q K^T over the whole chunk, once the previous chunk's P V
+                    // MMAs (which read P from these columns) have completed
+                    if (i > 0 && !sy.wait(&pv_done, i - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_ss(tXs, desc_add(dQ, ks * 32), desc_add(dKb, ks * 32), kIdQK, ks > 0);
+                    mma_commit(&xs_full);
+                    mma_commit(&qk_empty);
                 }
 #pragma unroll 1
                 for (int b = 0; b < nb && ok; ++b) {
@@ -286,10 +294,11 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     mma_commit(&spre_empty[sp]);
                     mma_commit(&block_empty[ls]);
-                    if (intra && b < 4) ok = quarter_step(i, b, vo);
+                    if (intra) ok = pv_quarter(i, b, vo);
                 }
-                for (int q = nb; intra && q < 4 && ok; ++q) ok = quarter_step(i, q, vo);
+                for (int q = nb; intra && q < 4 && ok; ++q) ok = pv_quarter(i, q, vo);
                 if (!ok) break;
+                if (intra) mma_commit(&pv_done);
                 mma_commit(&o_full);
                 if (intra) mma_commit(&v_empty[st]);
             }
@@ -341,14 +350,49 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             sy.wait(&fin_bar[1], 0);
         }
     } else if (warp < kWarpP) {
-        // ================= convert warps: S_run block -> bf16 S_pre
+        // ================= convert warps: S_run block -> bf16 S_pre (and, in
+        // group 0, the epilogue)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
+        // Group 0: numerator rows of chunk i -> the warp's 2 KB staging slot, 16
+        // columns at a time -> TMA stores of [32 rows x 16 floats]
+        uint8_t *slot = gstage + quarter * 2048;
+        auto epilogue0 = [&](int i) -> bool {
+            bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
+            if (!w) return false;
+            tc_fence_after();
+            uint32_t v[DV];
+            tmem_ld64(tXo + lsel, v);
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&o_empty);
+            const int t0 = i * kTile + quarter * 32;
+#pragma unroll
+            for (int r = 0; r < DV / 16; ++r) {
+                if (elect_lane0()) bulk_wait_read_all();   // the slot's previous store has read it
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 4; ++c)   // 64-byte swizzle: chunk c of row l at c ^ ((l / 2) % 4)
+                    st_shared_v4(smem_u32(slot + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)),
+                                 v[16 * r + 4 * c], v[16 * r + 4 * c + 1], v[16 * r + 4 * c + 2],
+                                 v[16 * r + 4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (elect_lane0() && t0 < T) {   // rows past T are clipped by the store
+                    tma_store_3d(&tm_part16, 16 * r, t0, bh, slot);
+                    bulk_commit();
+                }
+            }
+            return true;
+        };
         bool ok = true;
         for (int i = 0; i < nch && ok; ++i) {
 #pragma unroll 1
             for (int b = 0; b < nb && ok; ++b) {
+                // group 0: the previous chunk's output goes out between this chunk's
+                // two blocks (its OUT MMAs of block 0 wait for the accumulator)
+                if (intra && b == 1 && i > 0 && !(ok = epilogue0(i - 1))) break;
                 const int gb = i * nb + b, ss = gb & 1;
                 const int sp = intra ? 0 : ss, suse = intra ? gb : gb >> 1;   // S_pre slot, use
                 // S_pre of the first chunk is zero (one segment per head); the
@@ -385,19 +429,18 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (elect_lane0()) mbar_arrive(&block_ready[ss]);
             }
         }
+        if (intra && ok && nch > 0) epilogue0(nch - 1);
+        if (elect_lane0()) bulk_wait_all();
     } else if (warp < kWarpLift) {
         // ================= P warps: lane quarter q owns query rows 32q..32q+31
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
-        auto build_p = [&](int n, float &dsum) -> bool {
-            const int q = n & 3, slot = n & 1;
-            bool w = sy.wait(&xs_full, n) && (n < 2 || sy.wait(&p_empty[slot], (n >> 1) - 1));
-            w = __all_sync(0xffffffffu, w);
-            if (!w) return false;
-            tc_fence_after();
+        // P of key quarter q of the chunk (Q K^T ready in TMEM), written over the
+        // first 16 columns of the quarter; adds this row's weights to dsum
+        auto build_p = [&](int q, float &dsum) {
             uint32_t v[32];
-            tmem_ld32(tXs + lsel, v);                 // warp-collective: always executed
+            tmem_ld32(tXs + lsel + 32 * q, v);
             uint32_t pw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -409,35 +452,25 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 dsum += w1;
                 pw[j] = pack_bf16(w0, w1);
             }
-            tmem_st16(tP + lsel + slot * 16, pw);
+            tmem_st16(tXs + lsel + 32 * q, pw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (elect_lane0()) mbar_arrive(&p_full[slot]);
-            return true;
+            if (elect_lane0()) mbar_arrive(&p_full[q]);
         };
-        // This group's numerator rows of chunk i (and the denominator in group
-        // 0).  The accumulator is read into registers and released at once.
+        // Groups 1-3: this group's numerator rows of chunk i.  The accumulator
+        // is read into registers and released at once.
         uint8_t *sq = stage + quarter * 8192;
-        auto epilogue = [&](int i, float dsum) -> bool {
+        auto epilogue = [&](int i) -> bool {
             bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
             if (!w) return false;
             tc_fence_after();
-            const int t0 = i * kTile + quarter * 32, t = t0 + lane;
+            const int t0 = i * kTile + quarter * 32;
             uint32_t v[DV];
             tmem_ld64(tXo + lsel, v);
             tc_fence_before();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&o_empty);
-            if (intra) {
-                if (t < T) {
-                    dden[(size_t)bh * T + t] = dsum;
-                    float *dst = part + ((size_t)bh * T + t) * DV;   // group 0's partials
-#pragma unroll
-                    for (int e = 0; e < DV / 8; ++e) st_global_v8(dst + 8 * e, v + 8 * e);
-                }
-                return true;
-            }
             // the tiles hold chunk i + 1 until the lift warps have read it
             w = __all_sync(0xffffffffu, sy.wait(&qk_empty, min(i + 1, nch - 1)));
             if (!w) return false;
@@ -523,17 +556,21 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&chunk_full[0]);
         }
-        float dprev = 0.f;
-        for (int i = 0; i <= nch && ok; ++i) {   // chunk i's P and denominators, chunk i-1's output
-            if (i > 0) ok = epilogue(i - 1, dprev);
-            if (i == nch || !intra) continue;
-            float dsum = 0.f;
+        if (intra) {   // chunk i's P quarters and denominators
+            for (int i = 0; i < nch && ok; ++i) {
+                ok = __all_sync(0xffffffffu, sy.wait(&xs_full, i));
+                if (!ok) break;
+                tc_fence_after();
+                float dsum = 0.f;
+                build_p(0, dsum);
+                if (!(ok = d_inter(i, dsum))) break;
 #pragma unroll 1
-            for (int q = 0; q < 4 && ok; ++q) {
-                ok = build_p(4 * i + q, dsum);
-                if (ok && q == 0) ok = d_inter(i, dsum);
+                for (int q = 1; q < 4; ++q) build_p(q, dsum);
+                const int t = i * kTile + row;
+                if (t < T) dden[(size_t)bh * T + t] = dsum;
             }
-            dprev = dsum;
+        } else {
+            for (int i = 0; i < nch && ok; ++i) ok = epilogue(i);
         }
         if (elect_lane0()) bulk_wait_all();
     } else {
@@ -541,7 +578,7 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int side = (warp - kWarpLift) >> 2;
         const int quarter = warp & 3;   // TMEM lane quarter of this warp
         wide_lift_role(side ? tk : tq, lring + side * 32768, quarter * 32 + lane, side != 0,
-                       tmem_base + 384 + 32 * side + ((uint32_t)(quarter * 32) << 16), b_first, nb,
+                       tmem_base + 448 + 32 * side + ((uint32_t)(quarter * 32) << 16), b_first, nb,
                        nch, chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
     }
     tc_fence_before();
@@ -581,16 +618,18 @@ wide_finalize_kernel(const float *__restrict__ part, const float *__restrict__ d
 
 // ================================================================= host side
 // The partial numerators part[4 * BH][T][64] fp32 as a 3-D tensor for TMA
-// stores; box = [32 rows x 32 floats] (128 bytes, 128-byte swizzle).
-bool make_part_map(CUtensorMap &m, void *base, int T, int Z) {
+// stores; box = [32 rows x `cols` floats], swizzled over its row of cols * 4
+// bytes (32 columns: 128-byte swizzle; 16 columns: 64-byte swizzle).
+bool make_part_map(CUtensorMap &m, void *base, int T, int Z, int cols) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)Z};
     const cuuint64_t strides[2] = {64 * 4, (cuuint64_t)T * 64 * 4};
-    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)cols, 32, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -611,14 +650,15 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
     if (rows == 0) return cudaSuccess;
     float *part = static_cast<float *>(workspace);
     float *dden = part + rows * 64 * 4;
-    CUtensorMap mq, mk, mv, mp;
+    CUtensorMap mq, mk, mv, mp, mp16;
     if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
-        !make_map(mv, v, s.dv, s.T, s.BH()) || !make_part_map(mp, part, s.T, 4 * s.BH()))
+        !make_map(mv, v, s.dv, s.T, s.BH()) || !make_part_map(mp, part, s.T, 4 * s.BH(), 32) ||
+        !make_part_map(mp16, part, s.T, 4 * s.BH(), 16))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(wide_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemWide);
     {
         TraceScope tr("tc64_output", stream);
-        wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, part, dden,
+        wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, mp16, dden,
                                                                         s.T, NCt);
     }
     {
