@@ -65,13 +65,20 @@ def test_state_tensor_path(kg, B, H, T):
     ("small_fp32", dict(B=2, H=3, T=300)),
     ("small_fp32", dict(B=1, H=2, T=97, d=32, dv=64, C=32)),
     ("lm_layer_bf16", dict(B=1, H=2, T=333)),           # d = 64: CUDA-core path in bf16
-    ("lm_layer_bf16", dict(B=2, H=19, T=300)),          # d = 64, 38 heads: the state
-                                                        # export stays on CUDA cores
     ("mid_bf16", dict(B=1, H=2, T=200, dv=128, C=64)),  # dv = 128: CUDA-core path
 ])
 def test_state_cuda_core_path(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)
     _check_state(kg, w, kg.KATA_PATH_SIMT)
+
+
+def test_state_d64_many_heads(kg):
+    """d = 64 with 38 heads: the plain forward takes the tensor-core path (the
+    state split over four CTAs keeps no final state), the state-exporting
+    forward runs on CUDA cores; both give the definition's output."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=19, T=300)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    _check_state(kg, w)
 
 
 @pytest.mark.parametrize("name,overrides", [
