@@ -91,9 +91,11 @@ const char *kata_status_str(int status);
  *   C: the last chunk is zero-padded (Algorithm 1), padded rows are dropped.
  *
  * The output is the same function for every C (Eq. 17-20 regroup one sum);
- * C changes only the rounding.  bf16 inputs run on the tensor-core path,
- * which rounds the lifted features and the chunk-state prefix to bf16 as MMA
- * operands (fp32 accumulation); fp32 inputs run on CUDA cores in fp32.
+ * C changes only the rounding.  bf16 inputs with dv = 64 and d = 32, or d = 64
+ * with at least 38 (b, h) heads, run on the tensor-core path, which rounds the
+ * lifted features and the chunk-state prefix to bf16 as MMA operands (fp32
+ * accumulation); fp32 inputs and the other shapes run on CUDA cores in fp32
+ * (kata_fwd_path tells which).
  *
  * Scratch: per-call device workspace (kata_fwd_workspace_size bytes) taken
  * from the device's stream-ordered memory pool and released on `stream`.
