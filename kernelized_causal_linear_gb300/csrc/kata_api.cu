@@ -73,22 +73,21 @@ int device_info(DevInfo &out) {
 // variants (d = 32 with segments, d = 64 with the state split over four CTAs).
 enum Kernels { kSimt, kTc32, kTc64 };
 
-Kernels select_kernels(const FwdShape &s, const DevInfo &di, bool with_state) {
+Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
     if (s.dtype == KATA_F32) return kSimt;
     if (kata::tc_supported(s, di.major, di.minor)) return kTc32;
-    // the d = 64 kernels keep no final state: the state export runs on CUDA cores
-    if (!with_state && kata::tc64_supported(s, di.major, di.minor, di.sms)) return kTc64;
+    if (kata::tc64_supported(s, di.major, di.minor, di.sms)) return kTc64;
     return kSimt;
 }
 
 int select_path(const FwdShape &s, const DevInfo &di) {
-    return select_kernels(s, di, false) == kSimt ? KATA_PATH_SIMT : KATA_PATH_TC;
+    return select_kernels(s, di) == kSimt ? KATA_PATH_SIMT : KATA_PATH_TC;
 }
 
 size_t workspace_for(const FwdShape &s, Kernels kn, const DevInfo &di, bool with_state = false) {
     switch (kn) {
         case kTc32: return kata::tc_workspace_bytes(s, di.sms, with_state);
-        case kTc64: return kata::tc64_workspace_bytes(s);
+        case kTc64: return kata::tc64_workspace_bytes(s, with_state);
         default: return kata::simt_workspace_bytes(s);
     }
 }
@@ -121,7 +120,7 @@ int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype
     DevInfo di;
     if ((rc = device_info(di))) return rc;
     const FwdShape s{B, H, T, d, dv, C, dtype};
-    *bytes = workspace_for(s, select_kernels(s, di, false), di);
+    *bytes = workspace_for(s, select_kernels(s, di), di);
     return KATA_OK;
 }
 
@@ -154,7 +153,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
-    const Kernels kn = select_kernels(s, di, with_state);
+    const Kernels kn = select_kernels(s, di);
     const size_t wsb = workspace_for(s, kn, di, with_state);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
@@ -163,7 +162,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
         return KATA_ERR_ALLOC;
     }
     cudaError_t e = kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
-                    : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st)
+                    : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st, so)
                                   : kata::simt_forward(s, q, k, v, out, ws, st, so);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);

@@ -97,9 +97,10 @@ int tc_take_error();
 
 // ---- tcgen05 path at d = 64 (state split over four CTAs): kata_tc64.cu -----
 bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
-size_t tc64_workspace_bytes(const FwdShape &s);
+size_t tc64_workspace_bytes(const FwdShape &s, bool with_state = false);
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                         void *out, void *workspace, cudaStream_t stream);
+                         void *out, void *workspace, cudaStream_t stream,
+                         const StateOut &so = StateOut{});
 int tc64_take_error();
 
 }  // namespace kata

@@ -100,6 +100,36 @@ __device__ __forceinline__ int group_count(int grp) { return grp == 0 ? 2 : 5; }
 // Real features of block b (the last block holds 64).
 __device__ __forceinline__ int block_feats(int b) { return b == kBlocks64 - 1 ? 64 : 128; }
 
+// Final-state record of one head (state export): S in the grouped layout
+// [17 blocks][128 features][64] fp32, then G = sum k k^T [64][64] fp32.
+constexpr int kRec64 = kBlocks64 * 128 * 64 + 64 * 64;
+
+// Coordinates (i, j), i <= j, of feature p (0..127) of block b of the d = 64
+// grouped layout; false for a pad slot.
+__device__ __forceinline__ bool grouped_slot_pair64(int b, int p, int &i, int &j) {
+    const int pos = p >> 3, k = (p & 7) >> 1, hf = p & 1;
+    if (b < 14) {   // rectangle 2b + pos / 8, row pos % 8
+        int X, Y;
+        rect_pair64(2 * b + (pos >> 3), X, Y);
+        i = 8 * X + (pos & 7);
+        j = 8 * Y + 2 * k + hf;
+        return true;
+    }
+    const int c = 16 * (b - 14) + pos;   // chunk of the run of 40 triangle chunks
+    if (c >= 40) return false;
+    const int g = c / 5;
+    int I = 0, w = 4 * (c % 5) + k;   // pair w of the triangle: row I has (9 - I) / 2 pairs
+    while (w >= (9 - I) / 2) {
+        w -= (9 - I) / 2;
+        ++I;
+    }
+    const int J = I + 2 * w + hf;
+    if (J >= 8) return false;
+    i = 8 * g + I;
+    j = 8 * g + J;
+    return true;
+}
+
 // Lift role (out of line: its registers are allocated apart from the other
 // roles).  Token t = 32 * (warp % 4) + lane: its row is parked in TMEM lane t
 // (the warp's lane quarter), columns trow .. trow + 31, once per chunk.
@@ -161,8 +191,8 @@ constexpr int kSmemWide = 2 * 16384 + 2 * 16384 + 2 * 65536 + 2 * 16384 + 1024;
 __global__ void __launch_bounds__(608, 1)
 wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_part,
-                   const __grid_constant__ CUtensorMap tm_part16, float *__restrict__ dden, int T,
-                   int NCt) {
+                   const __grid_constant__ CUtensorMap tm_part16, float *__restrict__ dden,
+                   float *__restrict__ srec, int T, int NCt) {
     constexpr int D = 64, DV = 64;
     constexpr int kQK = kTile * D * 2, kV = kTile * DV * 2;
     constexpr int kLiftWarps = 8, kTmemWarps = 4;
@@ -447,7 +477,25 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (elect_lane0()) mbar_arrive(&block_ready[ss]);
             }
         }
-        if (intra && ok && nch > 0) epilogue0(nch - 1);
+        if (intra && ok && nch > 0) ok = epilogue0(nch - 1);
+        if (srec != nullptr && ok && nch > 0) {   // state export: S after the last chunk
+#pragma unroll 1
+            for (int b = 0; b < nb && ok; ++b) {
+                ok = __all_sync(0xffffffffu, sy.wait(&state_done[b], nch - 1));
+                if (!ok) break;
+                tc_fence_after();
+                if (quarter * 32 < block_feats(b_first + b)) {
+                    float *dst = srec + (size_t)bh * kRec64 + ((size_t)(b_first + b) * 128 + row) * DV;
+#pragma unroll
+                    for (int c32 = 0; c32 < DV; c32 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tS + lsel + b * DV + c32, v);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) st_global_v8(dst + c32 + 8 * e, v + 8 * e);
+                    }
+                }
+            }
+        }
         if (elect_lane0()) bulk_wait_all();
     } else if (warp < kWarpLift) {
         // ================= P warps: lane quarter q owns query rows 32q..32q+31
@@ -587,6 +635,19 @@ wide_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int t = i * kTile + row;
                 if (t < T) dden[(size_t)bh * T + t] = dsum;
             }
+            // state export: G after the last chunk (its rows are TMEM lanes 0-63;
+            // the P warps waited for the last Gram MMA in d_inter)
+            if (srec != nullptr && ok && nch > 0 && quarter < 2) {
+                tc_fence_after();
+                float *dst = srec + (size_t)bh * kRec64 + (size_t)kBlocks64 * 128 * DV + (size_t)row * D;
+#pragma unroll
+                for (int c32 = 0; c32 < D; c32 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tG + lsel + c32, v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) st_global_v8(dst + c32 + 8 * e, v + 8 * e);
+                }
+            }
         } else {
             for (int i = 0; i < nch && ok; ++i) ok = epilogue(i);
         }
@@ -632,6 +693,39 @@ wide_finalize_kernel(const float *__restrict__ part, const float *__restrict__ d
     }
 }
 
+// The final state of a head in the decode layout (as the d = 32 export):
+// state[f][c] and z[f] for the row-major upper-triangle feature f of (i, j),
+// sqrt(2) on the off-diagonal entries.  The grouped layout carries a factor 2 on
+// the key side off the diagonal, so those rows are scaled by 1/sqrt(2); z_f is
+// G_ij (sqrt(2) G_ij for i < j).  One CTA per head, 128 threads.
+__global__ void __launch_bounds__(128)
+state_export64_kernel(const float *__restrict__ srec, float *__restrict__ state,
+                      float *__restrict__ z) {
+    constexpr int D = 64, DV = 64, kN = D * (D + 1) / 2;
+    const int bh = blockIdx.x, p = threadIdx.x;
+    const float *rec = srec + (size_t)bh * kRec64;
+    float *st = state + (size_t)bh * kN * DV;
+    for (int b = 0; b < kBlocks64; ++b) {
+        int i = 0, j = 0;
+        if (!grouped_slot_pair64(b, p, i, j)) continue;
+        const int f = i * D - i * (i - 1) / 2 + (j - i);
+        const float sc = i == j ? 1.f : 0.70710678118654752f;
+        const float4 *src = reinterpret_cast<const float4 *>(rec + ((size_t)b * 128 + p) * DV);
+        float4 *dst = reinterpret_cast<float4 *>(st + (size_t)f * DV);
+#pragma unroll 4
+        for (int e = 0; e < DV / 4; ++e) {
+            const float4 x = src[e];
+            dst[e] = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
+        }
+    }
+    const float *gram = rec + (size_t)kBlocks64 * 128 * DV;
+    for (int e = p; e < D * D; e += blockDim.x) {
+        const int i = e / D, j = e % D;
+        if (j < i) continue;
+        z[(size_t)bh * kN + i * D - i * (i - 1) / 2 + (j - i)] = i == j ? gram[e] : kSqrt2 * gram[e];
+    }
+}
+
 }  // namespace
 
 // ================================================================= host side
@@ -656,18 +750,25 @@ bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms) 
            (int64_t)4 * s.BH() >= num_sms && s.BH() <= 65535 && encoder() != nullptr;
 }
 
-size_t tc64_workspace_bytes(const FwdShape &s) {
+// Workspace: partial numerators [4][rows][64] fp32, D [rows] fp32, then (state
+// export) the final-state records [BH][kRec64] fp32 from a 256-byte boundary
+// (their 32-byte stores need it).
+size_t srec_offset_floats(size_t rows) { return (rows * 64 * 4 + rows + 63) & ~(size_t)63; }
+
+size_t tc64_workspace_bytes(const FwdShape &s, bool with_state) {
     const size_t rows = (size_t)s.BH() * s.T;
-    return sizeof(float) * (rows * 64 * 4 + rows);
+    return sizeof(float) * (with_state ? srec_offset_floats(rows) + (size_t)s.BH() * kRec64
+                                       : rows * 64 * 4 + rows);
 }
 
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                         void *workspace, cudaStream_t stream) {
+                         void *workspace, cudaStream_t stream, const StateOut &so) {
     const int NCt = (s.T + kTile - 1) / kTile;
     const size_t rows = (size_t)s.BH() * s.T;
     if (rows == 0) return cudaSuccess;
     float *part = static_cast<float *>(workspace);
     float *dden = part + rows * 64 * 4;
+    float *srec = so.state != nullptr ? part + srec_offset_floats(rows) : nullptr;   // final-state records
     CUtensorMap mq, mk, mv, mp, mp16;
     if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
         !make_map(mv, v, s.dv, s.T, s.BH()) || !make_part_map(mp, part, s.T, 4 * s.BH(), 32) ||
@@ -677,7 +778,7 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
     {
         TraceScope tr("tc64_output", stream);
         wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, mp16, dden,
-                                                                        s.T, NCt);
+                                                                        srec, s.T, NCt);
     }
     {
         TraceScope tr("tc64_finalize", stream);
@@ -685,6 +786,10 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
         const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
         wide_finalize_kernel<<<blocks, 256, 0, stream>>>(part, dden, (__nv_bfloat16 *)out,
                                                           (int64_t)rows, (int64_t)rows * 64);
+    }
+    if (srec != nullptr) {
+        TraceScope tr("tc64_state_export", stream);
+        state_export64_kernel<<<s.BH(), 128, 0, stream>>>(srec, so.state, so.z);
     }
     return cudaGetLastError();
 }

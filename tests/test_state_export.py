@@ -72,13 +72,17 @@ def test_state_cuda_core_path(kg, name, overrides):
     _check_state(kg, w, kg.KATA_PATH_SIMT)
 
 
-def test_state_d64_many_heads(kg):
-    """d = 64 with 38 heads: the plain forward takes the tensor-core path (the
-    state split over four CTAs keeps no final state), the state-exporting
-    forward runs on CUDA cores; both give the definition's output."""
-    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=19, T=300)
-    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
-    _check_state(kg, w)
+@pytest.mark.parametrize("B,H,T", [
+    (2, 19, 300),    # 38 heads, ragged tail
+    (2, 19, 129),    # last chunk holds one token (the state records follow an odd-sized workspace part)
+    (4, 10, 5),      # a single partial chunk
+])
+def test_state_d64_tensor_path(kg, B, H, T):
+    """d = 64 with the state split over four CTAs per head: each CTA writes the
+    running state of its feature blocks after the last chunk, group 0 also the
+    Gram matrix, and a reorder kernel maps them to the decode layout."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    _check_state(kg, w, kg.KATA_PATH_TC)
 
 
 @pytest.mark.parametrize("name,overrides", [
@@ -107,6 +111,25 @@ def test_state_full_size_sampled_heads(kg):
     """The long-context workload in the bench's call configuration: the exported
     state of two heads against the oracle recurrence over all 131072 tokens."""
     w = workloads.WORKLOADS["long_ctx_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    out, S, z = kg.kata_fwd_chunked_state(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    BH = w.B * w.H
+    for h in (0, BH - 1):
+        kh = k.reshape(BH, 1, 1, w.T, w.d)[h]
+        vh = v.reshape(BH, 1, 1, w.T, w.dv)[h]
+        S_ref, z_ref = oracle.prefix_state(to_f64(kh), to_f64(vh))
+        Sg = to_f64(S.reshape(BH, 1, -1, w.dv)[h:h + 1])
+        zg = to_f64(z.reshape(BH, 1, -1)[h:h + 1])
+        assert _state_err(Sg, S_ref) <= STATE_TOL[w.dtype]
+        assert _state_err(zg, z_ref) <= STATE_TOL[w.dtype]
+
+
+def test_state_d64_full_size_sampled_heads(kg):
+    """The LM-layer workload (d = 64) in the bench's call configuration: the
+    exported state of two heads against the oracle recurrence."""
+    w = workloads.WORKLOADS["lm_layer_bf16"]
     q, k, v = workloads.make_qkv(w, device="cuda")
     out, S, z = kg.kata_fwd_chunked_state(q, k, v, w.C)
     torch.cuda.synchronize()
