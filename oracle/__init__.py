@@ -70,6 +70,14 @@ def _load():
             lib.kata_oracle_chunked.argtypes = [_D, _D, _D, _D, i, i, i, i, i]
             lib.kata_oracle_prefix_state.argtypes = [_D, _D, _D, _D, i, i, i, i]
             lib.kata_oracle_decode_step.argtypes = [_D, _D, _D, _D, _D, _D, i, i, i]
+            dd = ctypes.c_double
+            lib.kata_oracle_map_dim.argtypes = [i, i, i]
+            lib.kata_oracle_map_dim.restype = i
+            lib.kata_oracle_lift_map.argtypes = [_D, ctypes.c_int64, i, i, i, dd, dd, _D]
+            lib.kata_oracle_forward_map.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, dd, dd]
+            lib.kata_oracle_forward_rows_map.argtypes = [_D, _D, _D, _I64, ctypes.c_int64, _D,
+                                                         i, i, i, i, i, i, dd, dd]
+            lib.kata_oracle_recurrent_map.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, dd, dd]
             _lib = lib
     return _lib
 
@@ -177,3 +185,63 @@ def decode_step(S, z, q, k, v):
     _load().kata_oracle_decode_step(_p(S), _p(z), _p(q), _p(k), _p(v), _p(out), B * H,
                                     d, dv)
     return S, z, out
+
+
+# ---------------------------------------------------------------------------
+# Reduced PSD families (Sec. 4.1, "two reduced PSD families"): u in R^d cut into
+# g blocks u_a of width m = d/g.  map "M": psi(u) = (u_1 u_1^T, ..., u_g u_g^T);
+# map "Sigma": psi(u) = eps I + s * sum_a u_a u_a^T (eps and s as the Sigma
+# configuration sets them: 1e-4, and 1/4 for Sigma_4); map "full": u u^T.
+MAPS = {"full": 0, "M": 1, "Sigma": 2}
+
+
+def map_dim(map_name: str, d: int, g: int) -> int:
+    """Packed width of the map: d(d+1)/2, g m(m+1)/2 (M_g) or m(m+1)/2 (Sigma_g)."""
+    return int(_load().kata_oracle_map_dim(MAPS[map_name], int(d), int(g)))
+
+
+def lift_map(x, map_name: str, g: int = 1, eps: float = 0.0, scale: float = 1.0) -> np.ndarray:
+    """Packed psi(x) under a map: each matrix vech'd with sqrt(2) off the diagonal."""
+    x = _f64(x)
+    d = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    n = map_dim(map_name, d, g)
+    out = np.empty(x.shape[:-1] + (n,), dtype=np.float64)
+    _load().kata_oracle_lift_map(_p(x), rows, d, MAPS[map_name], int(g), float(eps),
+                                 float(scale), _p(out))
+    return out
+
+
+def forward_map(q, k, v, map_name: str, g: int = 1, eps: float = 0.0,
+                scale: float = 1.0) -> np.ndarray:
+    """Direct O(T^2) definition (Eq. 2) with w_ts = <psi(q_t), psi(k_s)>_F of the map."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_forward_map(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv,
+                                    MAPS[map_name], int(g), float(eps), float(scale))
+    return out
+
+
+def forward_rows_map(q, k, v, rows, map_name: str, g: int = 1, eps: float = 0.0,
+                     scale: float = 1.0) -> np.ndarray:
+    """forward_map at sampled rows (flat (b*H + h)*T + t indices)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((rows.shape[0], dv), dtype=np.float64)
+    _load().kata_oracle_forward_rows_map(_p(q), _p(k), _p(v), rows.ctypes.data_as(_I64),
+                                         rows.shape[0], _p(out), B * H, T, d, dv,
+                                         MAPS[map_name], int(g), float(eps), float(scale))
+    return out
+
+
+def recurrent_map(q, k, v, map_name: str, g: int = 1, eps: float = 0.0,
+                  scale: float = 1.0) -> np.ndarray:
+    """Self-check form: the packed-feature recurrence of Eq. 2 under a map."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_recurrent_map(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv,
+                                      MAPS[map_name], int(g), float(eps), float(scale))
+    return out

@@ -311,3 +311,173 @@ void kata_oracle_decode_step(double *S, double *z, const double *q, const double
         free(pq);
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * Reduced PSD families (Sec. 4.1, "two reduced PSD families"; the
+ * configuration appendix for the Sigma maps' eps I term and scale).  The
+ * vector u in R^d is cut into g blocks u_a of width m = d / g:
+ *   map 1, KATA-M_g:     psi(u) = (u_1 u_1^T, ..., u_g u_g^T), g matrices m x m,
+ *                        <psi(q), psi(k)> = sum_a (q_a . k_a)^2;
+ *   map 2, KATA-Sigma_g: psi(u) = eps I + s * sum_a u_a u_a^T, one m x m matrix
+ *                        (eps: a numerical safeguard the Sigma configuration
+ *                        sets to 1e-4; s: 1/4 in its reported Sigma_4 setup);
+ *   map 0: the full rank-one map (g = 1).
+ * Both families give the full map at g = 1 (eps = 0, s = 1).  Inner products
+ * are Frobenius; each matrix is packed like the full map (upper triangle,
+ * row-major, sqrt(2) off the diagonal), the g matrices of M_g in block order.
+ * ------------------------------------------------------------------------- */
+
+/* Packed feature width of a map (the pages' dominant state size over d_v). */
+int kata_oracle_map_dim(int map, int d, int g) {
+    const int m = d / g;
+    if (map == 1) return g * m * (m + 1) / 2;
+    if (map == 2) return m * (m + 1) / 2;
+    return d * (d + 1) / 2;
+}
+
+/* The map's matrices for one vector u, written out from the definitions:
+ * A[a][i][j] for a < count, each w x w.  Returns count; *w_out = w. */
+static int map_matrices(const double *u, int d, int map, int g, double eps, double s,
+                        double *A, int *w_out) {
+    if (map == 1) {
+        const int m = d / g;
+        *w_out = m;
+        for (int a = 0; a < g; ++a)
+            for (int i = 0; i < m; ++i)
+                for (int j = 0; j < m; ++j)
+                    A[((size_t)a * m + i) * m + j] = u[a * m + i] * u[a * m + j];
+        return g;
+    }
+    if (map == 2) {
+        const int m = d / g;
+        *w_out = m;
+        for (int i = 0; i < m; ++i)
+            for (int j = 0; j < m; ++j) {
+                double acc = 0.0;
+                for (int a = 0; a < g; ++a) acc += u[a * m + i] * u[a * m + j];
+                A[(size_t)i * m + j] = (i == j ? eps : 0.0) + s * acc;
+            }
+        return 1;
+    }
+    *w_out = d;
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j) A[(size_t)i * d + j] = u[i] * u[j];
+    return 1;
+}
+
+/* Packed lift of one vector under a map; A is scratch of at least d*d. */
+static void lift_map_one(const double *x, int d, int map, int g, double eps, double s,
+                         double *phi, double *A) {
+    const double r2 = sqrt(2.0);
+    int w = 0;
+    const int count = map_matrices(x, d, map, g, eps, s, A, &w);
+    int f = 0;
+    for (int a = 0; a < count; ++a)
+        for (int i = 0; i < w; ++i)
+            for (int j = i; j < w; ++j) {
+                const double e = A[((size_t)a * w + i) * w + j];
+                phi[f++] = (i == j) ? e : r2 * e;
+            }
+}
+
+void kata_oracle_lift_map(const double *x, int64_t rows, int d, int map, int g, double eps,
+                          double s, double *phi) {
+    const int n = kata_oracle_map_dim(map, d, g);
+    double *A = malloc(sizeof(double) * (size_t)d * d);
+    for (int64_t r = 0; r < rows; ++r) lift_map_one(x + r * d, d, map, g, eps, s, phi + r * n, A);
+    free(A);
+}
+
+/* <psi(q), psi(k)>_F as the entrywise sum over the map's matrices. */
+static double map_weight(const double *q, const double *k, int d, int map, int g, double eps,
+                         double s, double *Aq, double *Ak) {
+    int w = 0;
+    const int count = map_matrices(q, d, map, g, eps, s, Aq, &w);
+    map_matrices(k, d, map, g, eps, s, Ak, &w);
+    double acc = 0.0;
+    for (size_t e = 0; e < (size_t)count * w * w; ++e) acc += Aq[e] * Ak[e];
+    return acc;
+}
+
+/* Eq. 2 with the map's psi, one output row t (direct O(T) sum over s <= t). */
+static void direct_row_map(const double *q, const double *k, const double *v, int t, int d,
+                           int dv, int map, int g, double eps, double s, double *o) {
+    double *Aq = malloc(sizeof(double) * (size_t)d * d);
+    double *Ak = malloc(sizeof(double) * (size_t)d * d);
+    const double *qt = q + (int64_t)t * d;
+    double den = 0.0;
+    for (int j = 0; j < dv; ++j) o[j] = 0.0;
+    for (int si = 0; si <= t; ++si) {
+        const double w = map_weight(qt, k + (int64_t)si * d, d, map, g, eps, s, Aq, Ak);
+        den += w;
+        const double *vs = v + (int64_t)si * dv;
+        for (int j = 0; j < dv; ++j) o[j] += w * vs[j];
+    }
+    for (int j = 0; j < dv; ++j) o[j] = den > 0.0 ? o[j] / den : 0.0;
+    free(Aq);
+    free(Ak);
+}
+
+void kata_oracle_forward_map(const double *q, const double *k, const double *v, double *out,
+                             int BH, int T, int d, int dv, int map, int g, double eps,
+                             double s) {
+    const int64_t total = (int64_t)BH * T;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(kata_oracle_get_threads())
+    for (int64_t r = 0; r < total; ++r) {
+        const int64_t bh = r / T;
+        const int t = (int)(r % T);
+        direct_row_map(q + bh * T * d, k + bh * T * d, v + bh * T * dv, t, d, dv, map, g, eps,
+                       s, out + r * dv);
+    }
+}
+
+void kata_oracle_forward_rows_map(const double *q, const double *k, const double *v,
+                                  const int64_t *rows, int64_t nrows, double *out, int BH,
+                                  int T, int d, int dv, int map, int g, double eps, double s) {
+    (void)BH;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t bh = rows[i] / T;
+        const int t = (int)(rows[i] % T);
+        direct_row_map(q + bh * T * d, k + bh * T * d, v + bh * T * dv, t, d, dv, map, g, eps,
+                       s, out + i * dv);
+    }
+}
+
+/* Self-check form: the packed-feature recurrence of Eq. 2 under the map. */
+void kata_oracle_recurrent_map(const double *q, const double *k, const double *v, double *out,
+                               int BH, int T, int d, int dv, int map, int g, double eps,
+                               double s) {
+    const int n = kata_oracle_map_dim(map, d, g);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)n * dv, sizeof(double));
+        double *Z = calloc((size_t)n, sizeof(double));
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        double *A = malloc(sizeof(double) * (size_t)d * d);
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            lift_map_one(k + row * d, d, map, g, eps, s, pk, A);
+            lift_map_one(q + row * d, d, map, g, eps, s, pq, A);
+            const double *vt = v + row * dv;
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j) S[(size_t)f * dv + j] += pk[f] * vt[j];
+                Z[f] += pk[f];
+            }
+            double den = 0.0;
+            for (int f = 0; f < n; ++f) den += pq[f] * Z[f];
+            double *o = out + row * dv;
+            for (int j = 0; j < dv; ++j) {
+                double num = 0.0;
+                for (int f = 0; f < n; ++f) num += pq[f] * S[(size_t)f * dv + j];
+                o[j] = den > 0.0 ? num / den : 0.0;
+            }
+        }
+        free(S);
+        free(Z);
+        free(pk);
+        free(pq);
+        free(A);
+    }
+}
