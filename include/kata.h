@@ -66,11 +66,24 @@ typedef enum {
     KATA_PATH_TC = 2    /* tcgen05 tensor-core kernels (bf16 inputs, sm_103a)    */
 } kata_path;
 
+/* Feature map of kata_fwd_chunked_map ([KATA] Sec. 4.1): the full rank-one map
+ * and the two reduced PSD families. */
+typedef enum {
+    KATA_MAP_FULL = 0,  /* psi(u) = u u^T                                        */
+    KATA_MAP_BLOCK = 1, /* KATA-M_g: psi(u) = (u_1 u_1^T, ..., u_g u_g^T)         */
+    KATA_MAP_SUM = 2    /* KATA-Sigma_g: psi(u) = eps I + scale sum_a u_a u_a^T    */
+} kata_map;
+
 /* A cudaStream_t, declared without the CUDA headers. */
 typedef struct CUstream_st *kata_stream_t;
 
 /* n = d(d+1)/2, the packed width of the lift (Sec. 4.1); -1 if d < 1. */
 int kata_feature_dim(int d);
+
+/* Packed feature width of a map with g blocks of width m = d/g: d(d+1)/2
+ * (full), g m(m+1)/2 (KATA-M_g) or m(m+1)/2 (KATA-Sigma_g) -- the pages' state
+ * sizes over d_v (Sec. 4.1); -1 for an invalid map, d or g. */
+int kata_map_feature_dim(int map, int d, int g);
 
 /* Static human-readable text for a status code. */
 const char *kata_status_str(int status);
@@ -124,6 +137,30 @@ int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int
 int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
                            float *z, int B, int H, int T, int d, int dv, int C, int dtype,
                            kata_stream_t stream);
+
+/*
+ * kata_fwd_chunked_map -- the chunked forward with a reduced PSD feature map
+ * ([KATA] Sec. 4.1, "two reduced PSD families"; the eps I term and scale of the
+ * Sigma configuration).  q and k are cut into g blocks u_a of width m = d/g:
+ *
+ *   KATA_MAP_BLOCK (KATA-M_g):     psi(u) = (u_1 u_1^T, ..., u_g u_g^T),
+ *                                  <psi(q), psi(k)> = sum_a (q_a . k_a)^2;
+ *   KATA_MAP_SUM   (KATA-Sigma_g): psi(u) = eps I + scale sum_a u_a u_a^T,
+ *                                  <psi(q), psi(k)> = eps^2 m + eps scale
+ *                                  (|q|^2 + |k|^2) + scale^2 sum_{a,b} (q_a . k_b)^2;
+ *   KATA_MAP_FULL with g = 1:      kata_fwd_chunked.
+ *
+ * Eq. 17-20 with this psi: states of kata_map_feature_dim(map, d, g) x (dv + 1).
+ *   map, g: g in {1, 2, 4} dividing d; KATA_MAP_FULL needs g = 1.
+ *   eps >= 0 and scale > 0, finite; KATA_MAP_FULL and KATA_MAP_BLOCK need
+ *   eps = 0 and scale = 1 (KATA_ERR_ARG otherwise).
+ * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  The
+ * reduced maps run on CUDA cores in fp32 (bf16 inputs are widened; the output
+ * is written in the input type).
+ */
+int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
+                         int T, int d, int dv, int C, int dtype, int map, int g, float eps,
+                         float scale, kata_stream_t stream);
 
 /*
  * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
@@ -204,6 +241,12 @@ int kata_decode_step(float *state, float *z, const void *q, const void *k, const
  */
 int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype,
               kata_stream_t stream);
+
+/* kata_lift_map -- the packed lift of a map (as kata_fwd_chunked_map defines
+ * it) for rows of x: phi [rows][kata_map_feature_dim(map, d, g)] fp32.  Map
+ * arguments as kata_fwd_chunked_map, other arguments as kata_lift. */
+int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int map, int g,
+                  float eps, float scale, kata_stream_t stream);
 
 /*
  * kata_sync_status -- waits for `stream`, then reports and clears the sticky

@@ -31,6 +31,10 @@ KATA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 KATA_F32 = 0
 KATA_BF16 = 1
 
+KATA_MAP_FULL = 0
+KATA_MAP_BLOCK = 1
+KATA_MAP_SUM = 2
+
 KATA_PATH_NONE = 0
 KATA_PATH_SIMT = 1
 KATA_PATH_TC = 2
@@ -38,7 +42,8 @@ KATA_PATH_TC = 2
 EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
-            "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state")
+            "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
+            "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim")
 
 _lib = None
 
@@ -82,6 +87,11 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_chunked_noalloc.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
         L.kata_fwd_chunked_noalloc.restype = i
         L.kata_fwd_chunked_state.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, vp]
+        f = ctypes.c_float
+        L.kata_fwd_chunked_map.argtypes = [p, p, p, p, i, i, i, i, i, i, i, i, i, f, f, vp]
+        L.kata_lift_map.argtypes = [p, p, ctypes.c_int64, i, i, i, i, f, f, vp]
+        L.kata_map_feature_dim.argtypes = [i, i, i]
+        L.kata_map_feature_dim.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -225,6 +235,46 @@ def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: t
                                 v.data_ptr(), out.data_ptr(), B, H, d, dv,
                                 _dtype_code(q.dtype), _stream_handle(stream, q.device))
     _check(rc, "kata_decode_step")
+    return out
+
+
+def kata_map_feature_dim(map: int, d: int, g: int) -> int:
+    """Packed width of a feature map (-1 if invalid)."""
+    return int(lib().kata_map_feature_dim(int(map), int(d), int(g)))
+
+
+def kata_fwd_chunked_map(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int, map: int,
+                         g: int, eps: float = 0.0, scale: float = 1.0,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal KATA forward with a reduced PSD map (KATA_MAP_BLOCK: M_g, KATA_MAP_SUM: Sigma_g)."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd_chunked_map(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    B, H, T, d, dv, int(C), _dtype_code(q.dtype), int(map),
+                                    int(g), float(eps), float(scale),
+                                    _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked_map")
+    return out
+
+
+def kata_lift_map(x: torch.Tensor, map: int, g: int, eps: float = 0.0, scale: float = 1.0,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Packed psi(x) of a map for each row of x [..., d] -> fp32 [..., n]."""
+    d = x.shape[-1]
+    rows = x.numel() // d
+    n = kata_map_feature_dim(map, d, g)
+    if n < 0:
+        raise KataError(KATA_ERR_ARG, "kata_lift_map")
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (n,), dtype=torch.float32, device=x.device)
+    _contig(x, out)
+    rc = lib().kata_lift_map(x.data_ptr(), out.data_ptr(), rows, d, _dtype_code(x.dtype),
+                             int(map), int(g), float(eps), float(scale),
+                             _stream_handle(stream, x.device))
+    _check(rc, "kata_lift_map")
     return out
 
 

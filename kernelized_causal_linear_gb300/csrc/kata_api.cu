@@ -1,5 +1,6 @@
 // C ABI of libkata (declared and documented in include/kata.h): argument
 // validation, path selection, workspace management and launches.
+#include <cmath>
 #include <mutex>
 
 #include "../../include/kata.h"
@@ -16,6 +17,16 @@ bool valid_dv(int dv) { return dv == 16 || dv == 32 || dv == 64 || dv == 128; }
 bool valid_C(int C) { return C == 32 || C == 64 || C == 128; }
 bool valid_dtype(int t) { return t == KATA_F32 || t == KATA_BF16; }
 size_t elem_size(int t) { return t == KATA_F32 ? 4 : 2; }
+
+// A map the reduced-PSD entry points accept (see kata_fwd_chunked_map).
+bool valid_map(int map, int d, int g, float eps, float scale) {
+    if (map < KATA_MAP_FULL || map > KATA_MAP_SUM) return false;
+    if (!(g == 1 || g == 2 || g == 4) || d < g || d % g != 0) return false;
+    if (!std::isfinite(eps) || !std::isfinite(scale) || eps < 0.f || scale <= 0.f) return false;
+    if (map == KATA_MAP_FULL && g != 1) return false;
+    if (map != KATA_MAP_SUM && (eps != 0.f || scale != 1.f)) return false;
+    return true;
+}
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -137,7 +148,7 @@ namespace {
 // Shared body of kata_fwd_chunked and kata_fwd_chunked_state.
 int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int B, int H, int T,
                      int d, int dv, int C, int dtype, kata_stream_t stream,
-                     const kata::StateOut &so) {
+                     const kata::StateOut &so, const kata::MapSpec &map = kata::MapSpec{}) {
     if (!q || !k || !v || !out) return KATA_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return KATA_ERR_ARG;
@@ -153,8 +164,9 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
-    const Kernels kn = select_kernels(s, di);
-    const size_t wsb = workspace_for(s, kn, di, with_state);
+    const Kernels kn = map.kind == 0 ? select_kernels(s, di) : kSimt;   // reduced maps: CUDA cores
+    const size_t wsb = map.kind == 0 ? workspace_for(s, kn, di, with_state)
+                                     : kata::simt_workspace_bytes(s, map);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
@@ -163,7 +175,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     }
     cudaError_t e = kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
                     : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st, so)
-                                  : kata::simt_forward(s, q, k, v, out, ws, st, so);
+                                  : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -181,6 +193,26 @@ extern "C" {
 int kata_fwd_chunked(const void *q, const void *k, const void *v, void *out, int B, int H,
                      int T, int d, int dv, int C, int dtype, kata_stream_t stream) {
     return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{});
+}
+
+int kata_map_feature_dim(int map, int d, int g) {
+    if (d < 1 || d > 64 || !valid_map(map, d, g, 0.f, 1.f)) return -1;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    return ms.n(d);
+}
+
+int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
+                         int T, int d, int dv, int C, int dtype, int map, int g, float eps,
+                         float scale, kata_stream_t stream) {
+    if (!valid_map(map, d, g, eps, scale)) return KATA_ERR_ARG;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    ms.eps = eps;
+    ms.scale = scale;
+    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{}, ms);
 }
 
 int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
@@ -275,6 +307,27 @@ int kata_sync_status(kata_stream_t stream) {
     const int e = kata::tc_take_error(), e64 = kata::tc64_take_error();
     if (e < 0 || e64 < 0) return KATA_ERR_CUDA;
     return (e | e64) ? KATA_ERR_TIMEOUT : KATA_OK;
+}
+
+int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int map, int g,
+                  float eps, float scale, kata_stream_t stream) {
+    if (!x || !phi || rows < 1 || d < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
+    if (d > 64) return KATA_ERR_UNSUPPORTED;
+    if (!valid_map(map, d, g, eps, scale)) return KATA_ERR_ARG;
+    if (!aligned16(x) || !aligned16(phi)) return KATA_ERR_ARG;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    ms.eps = eps;
+    ms.scale = scale;
+    cudaGetLastError();
+    const cudaError_t e =
+        kata::lift_launch(x, phi, rows, d, dtype, reinterpret_cast<cudaStream_t>(stream), ms);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
 }
 
 int kata_lift(const void *x, float *phi, int64_t rows, int d, int dtype, kata_stream_t stream) {

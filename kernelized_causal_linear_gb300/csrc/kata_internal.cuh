@@ -58,6 +58,22 @@ class TraceScope {
     cudaEvent_t start_ = nullptr;
 };
 
+// Feature map of the forward ([KATA] Sec. 4.1, the full rank-one map and the two
+// reduced PSD families): the vector is cut into g blocks of width m = d / g.
+//   kind 0: psi(u) = u u^T (g = 1);
+//   kind 1 (M_g): psi(u) = (u_1 u_1^T, ..., u_g u_g^T), g m(m+1)/2 features;
+//   kind 2 (Sigma_g): psi(u) = eps I + scale * sum_a u_a u_a^T, m(m+1)/2 features.
+// Packing per matrix: upper triangle row-major, sqrt(2) off the diagonal.
+struct MapSpec {
+    int kind = 0, g = 1;
+    float eps = 0.f, scale = 1.f;
+    __host__ __device__ int m(int d) const { return d / g; }
+    __host__ __device__ int n(int d) const {
+        const int w = d / g;
+        return kind == 1 ? g * w * (w + 1) / 2 : kind == 2 ? w * (w + 1) / 2 : d * (d + 1) / 2;
+    }
+};
+
 // Optional export of the state after the last token, in the decode layout:
 // state [BH][n][dv] and z [BH][n] fp32, row-major vech order with sqrt(2) on the
 // off-diagonal entries.  Both null: no export.
@@ -67,12 +83,12 @@ struct StateOut {
 };
 
 // ---- CUDA-core (SIMT) path: kata_simt.cu ----------------------------------
-size_t simt_workspace_bytes(const FwdShape &s);
+size_t simt_workspace_bytes(const FwdShape &s, const MapSpec &map = MapSpec{});
 cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
                          void *out, void *workspace, cudaStream_t stream,
-                         const StateOut &so = StateOut{});
+                         const StateOut &so = StateOut{}, const MapSpec &map = MapSpec{});
 cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const MapSpec &map = MapSpec{});
 // Exclusive prefix in place along axis 1 of data[BH][n][E] (fp32).  With
 // so.state set, E = nf * W holds nf rows of W = dv + 1 values and the inclusive
 // totals go to so.state[BH][nf][dv] (columns 0..dv-1) and so.z[BH][nf] (column dv).

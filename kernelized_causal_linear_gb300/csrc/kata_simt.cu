@@ -12,7 +12,9 @@
 //
 // The feature lift (Sec. 3.1) is fused: psi entries are formed in registers
 // from the q/k rows staged in shared memory and never written to memory.  The
-// intra-chunk weights use (q.k)^2 directly, which equals psi(q).psi(k).
+// intra-chunk weights use the closed form of psi(q).psi(k): (q.k)^2 for the full
+// map, sum_a (q_a.k_a)^2 for M_g, eps^2 m + eps s (|q|^2 + |k|^2) +
+// s^2 sum_{a,b} (q_a.k_b)^2 for Sigma_g (Sec. 4.1, reduced PSD families).
 //
 // Workspace: per-chunk states [B*H][N_C][n][dv+1] fp32, scanned in place.
 #include "kata_internal.cuh"
@@ -25,11 +27,80 @@ constexpr int kStride = kColGroup + 1;
 constexpr int kFeatTile = 128;    // features per chunk-state block
 constexpr int kStageRows = 64;    // prefix rows staged per step in the output kernel
 
+// Packed feature f of a map as entries of its matrix: psi_f = cf * (add + scl *
+// sum_{a < terms} x[i0 + a step] x[j0 + a step]) (one term except for Sigma_g,
+// whose matrix sums the g block outer products; add is eps on its diagonal).
+struct Feat {
+    int i0, j0, terms, step;
+    float cf, add, scl;
+    // x: coordinate c at x[c * xs]
+    template <typename X>
+    __device__ __forceinline__ float operator()(const X *x, int xs) const {
+        float e = 0.f;
+        for (int a = 0; a < terms; ++a)
+            e = fmaf(to_f(x[(i0 + a * step) * xs]), to_f(x[(j0 + a * step) * xs]), e);
+        return cf * fmaf(scl, e, add);
+    }
+};
+
+__device__ __forceinline__ Feat map_feature(int f, int d, const MapSpec &mp) {
+    Feat ft;
+    int i, j;
+    if (mp.kind == 0) {
+        vech_pair(f, d, i, j);
+        ft = Feat{i, j, 1, 0, 1.f, 0.f, 1.f};
+    } else {
+        const int m = d / mp.g, nb = m * (m + 1) / 2;
+        if (mp.kind == 1) {
+            const int a = f / nb;
+            vech_pair(f - a * nb, m, i, j);
+            ft = Feat{a * m + i, a * m + j, 1, 0, 1.f, 0.f, 1.f};
+        } else {
+            vech_pair(f, m, i, j);
+            ft = Feat{i, j, mp.g, m, 1.f, i == j ? mp.eps : 0.f, mp.scale};
+        }
+    }
+    ft.cf = ft.i0 == ft.j0 ? 1.f : kSqrt2;
+    return ft;
+}
+
+// <psi(q), psi(k)> of a map from the raw vectors; q at q[c * qs], k at k[c].
+__device__ __forceinline__ float map_weight(const float *q, int qs, const float *k, int d,
+                                            const MapSpec &mp) {
+    if (mp.kind == 0) {
+        float dot = 0.f;
+        for (int i = 0; i < d; ++i) dot = fmaf(q[i * qs], k[i], dot);
+        return dot * dot;
+    }
+    const int m = d / mp.g;
+    float w = 0.f;
+    if (mp.kind == 1) {
+        for (int a = 0; a < mp.g; ++a) {
+            float dot = 0.f;
+            for (int i = 0; i < m; ++i) dot = fmaf(q[(a * m + i) * qs], k[a * m + i], dot);
+            w = fmaf(dot, dot, w);
+        }
+        return w;
+    }
+    float qn = 0.f, kn = 0.f;
+    for (int i = 0; i < d; ++i) {
+        qn = fmaf(q[i * qs], q[i * qs], qn);
+        kn = fmaf(k[i], k[i], kn);
+    }
+    for (int a = 0; a < mp.g; ++a)
+        for (int b = 0; b < mp.g; ++b) {
+            float dot = 0.f;
+            for (int i = 0; i < m; ++i) dot = fmaf(q[(a * m + i) * qs], k[b * m + i], dot);
+            w = fmaf(dot, dot, w);
+        }
+    return mp.eps * mp.eps * m + mp.eps * mp.scale * (qn + kn) + mp.scale * mp.scale * w;
+}
+
 // ---------------------------------------------------------------- stage 1
 template <typename T>
 __global__ void __launch_bounds__(kFeatTile)
 chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ st,
-                   int T_, int d, int dv, int C, int n, int NC, int nft) {
+                   int T_, int d, int dv, int C, int n, int NC, int nft, MapSpec mp) {
     extern __shared__ float sm[];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
@@ -56,11 +127,9 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
     for (int jj = 0; jj < kStride; ++jj) acc[jj] = 0.f;
     const int f = ft * kFeatTile + threadIdx.x;
     if (f < n) {
-        int i, j;
-        vech_pair(f, d, i, j);
-        const float cf = (i == j) ? 1.f : kSqrt2;
+        const Feat ft = map_feature(f, d, mp);
         for (int t = 0; t < tc; ++t) {
-            const float a = ks[t * d + i] * ks[t * d + j] * cf;   // psi(k_t)_f
+            const float a = ft(ks + t * d, 1);   // psi(k_t)_f
             const float *vr = vs + t * kStride;
 #pragma unroll
             for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(a, vr[jj], acc[jj]);
@@ -95,8 +164,8 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
 __global__ void __launch_bounds__(256)
 scan_kernel(float *__restrict__ st, int NC, int64_t E, float *__restrict__ state_out,
             float *__restrict__ z_out, int W, float *__restrict__ totals) {
-    // four consecutive elements per thread (E is a multiple of 4 for every
-    // supported shape); up to 8 records are loaded before any is written
+    // four consecutive elements per thread (the launcher uses this kernel only
+    // when E is a multiple of 4); up to 8 records are loaded before any is written
     const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t E4 = E >> 2;
     if (e4 >= E4) return;
@@ -135,13 +204,37 @@ scan_kernel(float *__restrict__ st, int NC, int64_t E, float *__restrict__ state
     }
 }
 
+// The same scan one element per thread, for records whose length is not a
+// multiple of 4 (reduced maps with few features, e.g. Sigma_4 at d = 16).
+__global__ void __launch_bounds__(256)
+scan_kernel_scalar(float *__restrict__ st, int NC, int64_t E, float *__restrict__ state_out,
+                   float *__restrict__ z_out, int W, float *__restrict__ totals) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *p = st + (size_t)blockIdx.y * NC * E + e;
+    float run = 0.f;
+    for (int c = 0; c < NC; ++c) {
+        const float x = p[(size_t)c * E];
+        p[(size_t)c * E] = run;
+        run += x;
+    }
+    if (totals) totals[(size_t)blockIdx.y * E + e] = run;
+    if (state_out) {
+        const int64_t nf = E / W, f = e / W, col = e % W;
+        if (col < W - 1)
+            state_out[((size_t)blockIdx.y * nf + f) * (W - 1) + col] = run;
+        else
+            z_out[(size_t)blockIdx.y * nf + f] = run;
+    }
+}
+
 // ---------------------------------------------------------------- stage 3
 // One block per (chunk, head, column group); thread r owns output row r.
 template <typename T>
 __global__ void __launch_bounds__(128)
 output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ st, T *__restrict__ out, int T_, int d, int dv,
-              int C, int n, int NC) {
+              int C, int n, int NC, MapSpec mp) {
     extern __shared__ float sm[];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
@@ -174,9 +267,13 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 #pragma unroll
     for (int jj = 0; jj < kStride; ++jj) acc[jj] = 0.f;
 
-    // inter-chunk term: psi(q_r) . [S_pre | Z_pre]
+    // inter-chunk term: psi(q_r) . [S_pre | Z_pre]; features are walked in order:
+    // (fi, fj) within matrix blk of width w (M_g: blocks one after another)
     const float *sp = st + ((size_t)bh * NC + c) * (size_t)n * W;
-    int fi = 0, fj = 0;
+    const int w = mp.kind == 0 ? d : d / mp.g;
+    const int terms = mp.kind == 2 ? mp.g : 1;
+    const float scl = mp.kind == 2 ? mp.scale : 1.f;
+    int blk = 0, fi = 0, fj = 0;
     for (int f0 = 0; f0 < n; f0 += kStageRows) {
         const int nf = min(kStageRows, n - f0);
         __syncthreads();
@@ -190,12 +287,20 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         }
         __syncthreads();
         for (int fr = 0; fr < nf; ++fr) {
-            const float a = qsT[fi * C + r] * qsT[fj * C + r] * (fi == fj ? 1.f : kSqrt2);
+            float e = 0.f;
+            const int i0 = blk * w + fi, j0 = blk * w + fj;
+            for (int a = 0; a < terms; ++a)
+                e = fmaf(qsT[(i0 + a * w) * C + r], qsT[(j0 + a * w) * C + r], e);
+            const float add = (mp.kind == 2 && fi == fj) ? mp.eps : 0.f;
+            const float a = fmaf(scl, e, add) * (fi == fj ? 1.f : kSqrt2);
             const float *sr = stg + fr * kStride;
 #pragma unroll
             for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
-            if (++fj == d) {
-                ++fi;
+            if (++fj == w) {
+                if (++fi == w) {
+                    fi = 0;
+                    ++blk;
+                }
                 fj = fi;
             }
         }
@@ -204,9 +309,7 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     // intra-chunk term: weights (q_r . k_s)^2 for s <= r (causal, diagonal kept)
     if (r < tc) {
         for (int s = 0; s <= r; ++s) {
-            float dot = 0.f;
-            for (int i = 0; i < d; ++i) dot = fmaf(qsT[i * C + r], ks[s * d + i], dot);
-            const float w = dot * dot;
+            const float w = map_weight(qsT + r, C, ks + s * d, d, mp);
             const float *vr = vs + s * kStride;
 #pragma unroll
             for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(w, vr[jj], acc[jj]);
@@ -225,31 +328,22 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 // ---------------------------------------------------------------- lift
 template <typename T>
 __global__ void __launch_bounds__(256)
-lift_kernel(const T *__restrict__ x, float *__restrict__ phi, int64_t rows, int d, int n) {
-    __shared__ unsigned char pi[2080], pj[2080];
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        const int start = i * d - i * (i - 1) / 2;
-        for (int j = i; j < d; ++j) {
-            pi[start + j - i] = (unsigned char)i;
-            pj[start + j - i] = (unsigned char)j;
-        }
-    }
-    __syncthreads();
+lift_kernel(const T *__restrict__ x, float *__restrict__ phi, int64_t rows, int d, int n,
+            MapSpec mp) {
     const int64_t total = rows * n;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = e / n;
         const int f = (int)(e % n);
-        const int i = pi[f], j = pj[f];
-        const float xi = to_f(x[r * d + i]), xj = to_f(x[r * d + j]);
-        phi[e] = (i == j) ? xi * xi : kSqrt2 * xi * xj;
+        phi[e] = map_feature(f, d, mp)(x + r * d, 1);
     }
 }
 
 template <typename T>
 cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v, T *out,
-                           float *st, cudaStream_t stream, const StateOut &so) {
-    const int n = s.n(), NC = s.NC(), BH = s.BH();
+                           float *st, cudaStream_t stream, const StateOut &so,
+                           const MapSpec &mp) {
+    const int n = mp.n(s.d), NC = s.NC(), BH = s.BH();
     const int nft = (n + kFeatTile - 1) / kFeatTile;
     const int ncg = (s.dv + kColGroup - 1) / kColGroup;
 
@@ -260,7 +354,7 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
     {
         TraceScope tr("simt_chunk_state", stream);
         chunk_state_kernel<T><<<dim3(NC, BH, nft * ncg), kFeatTile, sm1, stream>>>(
-            k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft);
+            k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft, mp);
     }
     const int64_t E = (int64_t)n * (s.dv + 1);
     cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream, so, s.dv + 1);
@@ -273,7 +367,7 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
     {
         TraceScope tr("simt_output", stream);
         output_kernel<T><<<dim3(NC, BH, ncg), s.C, sm3, stream>>>(q, k, v, st, out, s.T, s.d,
-                                                                    s.dv, s.C, n, NC);
+                                                                    s.dv, s.C, n, NC, mp);
     }
     return cudaGetLastError();
 }
@@ -283,41 +377,46 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
                                   cudaStream_t stream, const StateOut &so, int W, float *totals) {
     if (so.state && (W < 2 || E % W != 0)) return cudaErrorInvalidValue;
-    if (E % 4 != 0) return cudaErrorInvalidValue;
     TraceScope tr(stage, stream);
-    scan_kernel<<<dim3((unsigned)((E / 4 + 255) / 256), BH), 256, 0, stream>>>(data, n, E, so.state,
-                                                                             so.z, W, totals);
+    if (E % 4 != 0)
+        scan_kernel_scalar<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(
+            data, n, E, so.state, so.z, W, totals);
+    else
+        scan_kernel<<<dim3((unsigned)((E / 4 + 255) / 256), BH), 256, 0, stream>>>(
+            data, n, E, so.state, so.z, W, totals);
     return cudaGetLastError();
 }
 
-size_t simt_workspace_bytes(const FwdShape &s) {
-    return sizeof(float) * (size_t)s.BH() * (size_t)s.NC() * (size_t)s.n() *
+size_t simt_workspace_bytes(const FwdShape &s, const MapSpec &map) {
+    return sizeof(float) * (size_t)s.BH() * (size_t)s.NC() * (size_t)map.n(s.d) *
            (size_t)(s.dv + 1);
 }
 
 cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                         void *out, void *workspace, cudaStream_t stream, const StateOut &so) {
+                         void *out, void *workspace, cudaStream_t stream, const StateOut &so,
+                         const MapSpec &map) {
     float *st = static_cast<float *>(workspace);
     if (s.dtype == 0)
         return simt_forward_t<float>(s, (const float *)q, (const float *)k, (const float *)v,
-                                     (float *)out, st, stream, so);
+                                     (float *)out, st, stream, so, map);
     return simt_forward_t<__nv_bfloat16>(s, (const __nv_bfloat16 *)q,
                                          (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-                                         (__nv_bfloat16 *)out, st, stream, so);
+                                         (__nv_bfloat16 *)out, st, stream, so, map);
 }
 
 cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtype,
-                        cudaStream_t stream) {
-    const int n = d * (d + 1) / 2;
+                        cudaStream_t stream, const MapSpec &map) {
+    const int n = map.n(d);
     const int64_t total = rows * n;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     TraceScope tr("lift", stream);
     if (dtype == 0)
-        lift_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>((const float *)x, phi, rows, d, n);
+        lift_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>((const float *)x, phi, rows, d, n,
+                                                                 map);
     else
         lift_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
-            (const __nv_bfloat16 *)x, phi, rows, d, n);
+            (const __nv_bfloat16 *)x, phi, rows, d, n, map);
     return cudaGetLastError();
 }
 

@@ -145,3 +145,36 @@ def test_state_variant_rejects_bad_arguments(L):
     assert st(z=o + 16) == kg.KATA_ERR_ARG                     # z over the output
     assert st(d=20) == kg.KATA_ERR_UNSUPPORTED
     assert st(T=0) == kg.KATA_ERR_ARG
+
+
+def test_map_feature_dims(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert L.kata_map_feature_dim(kg.KATA_MAP_FULL, 64, 1) == 2080
+    assert L.kata_map_feature_dim(kg.KATA_MAP_BLOCK, 64, 2) == 1056     # g m(m+1)/2
+    assert L.kata_map_feature_dim(kg.KATA_MAP_BLOCK, 64, 4) == 544
+    assert L.kata_map_feature_dim(kg.KATA_MAP_SUM, 64, 2) == 528        # m(m+1)/2
+    assert L.kata_map_feature_dim(kg.KATA_MAP_SUM, 32, 4) == 36
+    assert L.kata_map_feature_dim(kg.KATA_MAP_FULL, 64, 2) == -1        # full map is g = 1
+    assert L.kata_map_feature_dim(kg.KATA_MAP_BLOCK, 16, 3) == -1       # g must divide d, in {1,2,4}
+    assert L.kata_map_feature_dim(7, 16, 2) == -1
+
+
+def test_map_forward_rejects_bad_maps(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, o = (FAKE * (i + 1) * 4096 for i in range(4))
+
+    def fm(map_, g, eps=0.0, scale=1.0, **kw):
+        a = dict(B=1, H=1, T=8, d=16, dv=16, C=32, dtype=1)
+        a.update(kw)
+        return L.kata_fwd_chunked_map(q, k, v, o, a["B"], a["H"], a["T"], a["d"], a["dv"],
+                                      a["C"], a["dtype"], map_, g, eps, scale, None)
+
+    assert fm(3, 2) == kg.KATA_ERR_ARG                                   # unknown map
+    assert fm(kg.KATA_MAP_FULL, 2) == kg.KATA_ERR_ARG                    # full map needs g = 1
+    assert fm(kg.KATA_MAP_BLOCK, 3) == kg.KATA_ERR_ARG                   # g in {1, 2, 4}
+    assert fm(kg.KATA_MAP_BLOCK, 2, eps=1e-4) == kg.KATA_ERR_ARG         # eps only for Sigma
+    assert fm(kg.KATA_MAP_SUM, 2, eps=-1.0) == kg.KATA_ERR_ARG
+    assert fm(kg.KATA_MAP_SUM, 2, scale=0.0) == kg.KATA_ERR_ARG
+    assert fm(kg.KATA_MAP_SUM, 2, eps=float("nan")) == kg.KATA_ERR_ARG
+    assert fm(kg.KATA_MAP_SUM, 4, d=16, T=0) == kg.KATA_ERR_ARG          # shape rules as the forward
+    assert L.kata_lift_map(q, o, 4, 16, 1, kg.KATA_MAP_BLOCK, 3, 0.0, 1.0, None) == kg.KATA_ERR_ARG

@@ -1,0 +1,102 @@
+"""GPU parity of the reduced PSD families (KATA-M_g, KATA-Sigma_g; [KATA] Sec. 4.1)
+against the CPU oracle: kata_fwd_chunked_map element by element at sizes the
+oracle finishes in seconds (several chunks and a ragged tail), kata_lift_map,
+and sampled rows at the LM-layer size (B=8, H=16, T=2048, d=64)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import TOL, require_gpu, slice_rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+NAMES = {1: "M", 2: "Sigma"}
+
+
+@pytest.fixture(scope="module")
+def kg():
+    return require_gpu()
+
+
+def _params(kg, map_, g):
+    # the Sigma configuration: eps = 1e-4, scale 1 (Sigma_2) or 1/4 (Sigma_4)
+    if map_ == kg.KATA_MAP_SUM:
+        return 1e-4, (0.25 if g == 4 else 1.0)
+    return 0.0, 1.0
+
+
+@pytest.mark.parametrize("map_", [1, 2])
+@pytest.mark.parametrize("g", [2, 4])
+@pytest.mark.parametrize("d,dv,C", [(16, 16, 32), (32, 64, 64), (64, 64, 64)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_map_forward_parity(kg, map_, g, d, dv, C, dtype):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=2, T=3 * C + 7, d=d, dv=dv, C=C,
+                                                    dtype=dtype)
+    q, k, v = workloads.make_qkv(w)
+    eps, scale = _params(kg, map_, g)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), NAMES[map_], g, eps, scale)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[dtype], f"{NAMES[map_]}_{g} d={d}: {err:.3e}"
+
+
+@pytest.mark.parametrize("map_,g", [(1, 2), (1, 4), (2, 2), (2, 4)])
+def test_map_forward_ragged(kg, map_, g):
+    eps, scale = _params(kg, map_, g)
+    for T in (1, 31, 32, 33):
+        w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=1, T=T, C=32, dtype=torch.float32)
+        q, k, v = workloads.make_qkv(w)
+        out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), 32, map_, g, eps, scale)
+        torch.cuda.synchronize()
+        ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), NAMES[map_], g, eps, scale)
+        assert slice_rel_err(to_f64(out), ref) <= TOL[torch.float32]
+
+
+def test_full_map_is_the_plain_forward(kg):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=300)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked_map(q, k, v, w.C, kg.KATA_MAP_FULL, 1)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("map_,g,d", [(1, 2, 64), (1, 4, 32), (2, 2, 64), (2, 4, 16)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_map_lift_parity(kg, map_, g, d, dtype):
+    x = torch.randn(37, d, generator=torch.Generator().manual_seed(d + g)).to(dtype)
+    eps, scale = _params(kg, map_, g)
+    phi = kg.kata_lift_map(x.cuda(), map_, g, eps, scale)
+    torch.cuda.synchronize()
+    ref = oracle.lift_map(to_f64(x), NAMES[map_], g, eps, scale)
+    err = float(np.max(np.abs(to_f64(phi) - ref)) / np.max(np.abs(ref)))
+    assert err <= 1e-6
+
+
+@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2)])
+def test_map_full_size_sampled_rows(kg, map_, g):
+    """The LM-layer workload with M_2 / Sigma_2, sampled rows against the oracle."""
+    w = workloads.WORKLOADS["lm_layer_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    eps, scale = _params(kg, map_, g)
+    out = kg.kata_fwd_chunked_map(q, k, v, w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    BH = w.B * w.H
+    rng = np.random.default_rng(w.index + 10 * map_)
+    worst = 0.0
+    for h in sorted(set([0, BH - 1] + rng.integers(0, BH, size=1).tolist())):
+        ts = np.array(sorted(set([0, 1, w.C - 1, w.C, w.T // 2, w.T - 1] +
+                                 rng.integers(0, w.T, size=10).tolist())), dtype=np.int64)
+        ref = oracle.forward_rows_map(to_f64(q.reshape(BH, 1, w.T, w.d)[h:h + 1]),
+                                      to_f64(k.reshape(BH, 1, w.T, w.d)[h:h + 1]),
+                                      to_f64(v.reshape(BH, 1, w.T, w.dv)[h:h + 1]), ts,
+                                      NAMES[map_], g, eps, scale)
+        got = to_f64(out.reshape(BH, w.T, w.dv)[h][ts])
+        worst = max(worst, slice_rel_err(got, ref))
+    assert worst <= TOL[w.dtype], f"{NAMES[map_]}_{g}: {worst:.3e}"
