@@ -80,13 +80,40 @@ def tc_plan(w, num_sms: int):
     return nct, G, Lc
 
 
-def stage_work(stage: str, w, num_sms: int = SMS):
+class FeatureMap:
+    """The forward's feature map: the full rank-one map or a reduced PSD family
+    ([KATA] Sec. 4.1) with g blocks; the Sigma maps take the eps and scale of the
+    pages' Sigma configuration (eps = 1e-4; scale 1/4 for Sigma_4, else 1)."""
+    CODES = {"full": 0, "M": 1, "Sigma": 2}
+
+    def __init__(self, name: str = "full", g: int = 1):
+        self.name, self.g, self.code = name, int(g), self.CODES[name]
+        self.eps = 1e-4 if name == "Sigma" else 0.0
+        self.scale = (0.25 if self.g == 4 else 1.0) if name == "Sigma" else 1.0
+
+    def n(self, d: int) -> int:
+        m = d // self.g
+        return {0: d * (d + 1) // 2, 1: self.g * m * (m + 1) // 2, 2: m * (m + 1) // 2}[self.code]
+
+    def intra_d(self, d: int) -> int:
+        """Multiply-adds per (t, s) pair of the closed-form weight: all g x g block
+        products for Sigma_g, d otherwise."""
+        return self.g * d if self.code == 2 else d
+
+    def label(self) -> str:
+        return "full" if self.code == 0 else f"{self.name}_{self.g}"
+
+
+FULL_MAP = FeatureMap()
+
+
+def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     """(algorithmic work per launch, unit, bound) for a traced stage on workload w."""
-    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, w.n
+    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, fm.n(w.d)
     NC = -(-T // C)
     state_flops = 2.0 * n * (dv + 1) * T * BH          # Psi(K)^T [V|1]
     out_inter = 2.0 * n * (dv + 1) * T * BH            # Psi(Q) [S|Z]
-    intra = 2.0 * (d + dv + 1) * _intra_pairs(T, C) * BH   # (q.k)^2 and P [V|1], causal
+    intra = 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, C) * BH   # weights and P [V|1], causal
     if stage == "simt_chunk_state":
         return state_flops, "TFLOP/s", "alu"
     if stage == "simt_output":
@@ -113,12 +140,13 @@ def stage_work(stage: str, w, num_sms: int = SMS):
     return None, "", ""
 
 
-def call_flops(w) -> float:
+def call_flops(w, fm: FeatureMap = FULL_MAP) -> float:
     """Algorithmic flops of one forward call at the workload's chunk size:
     2n(dv+1) (state) + 2n(dv+1) (inter output) per token and head, plus the
-    causal intra-chunk term 2(d+dv+1) per (t, s<=t) pair inside chunks."""
-    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, w.n
-    return 4.0 * n * (dv + 1) * T * BH + 2.0 * (d + dv + 1) * _intra_pairs(T, C) * BH
+    causal intra-chunk term 2(d'+dv+1) per (t, s<=t) pair inside chunks (d' the
+    weight's multiply-adds: d, or g d for Sigma_g)."""
+    BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, fm.n(w.d)
+    return 4.0 * n * (dv + 1) * T * BH + 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, C) * BH
 
 
 def _source_digest() -> str:
@@ -227,7 +255,7 @@ class ClockSampler:
 # CPU oracle baseline (rank 0 only)
 
 
-def _oracle_sample(w, q, k, v, seconds: float, rng):
+def _oracle_sample(w, q, k, v, seconds: float, rng, fm: FeatureMap = FULL_MAP):
     """Time the oracle on sampled output rows (uniform over heads and positions)
     for about `seconds`; returns (rows, elapsed seconds, threads).  Each row is
     one head of one token."""
@@ -243,7 +271,11 @@ def _oracle_sample(w, q, k, v, seconds: float, rng):
         t0 = time.perf_counter()
         for h in np.unique(heads):
             sel = ts[heads == h]
-            oracle.forward_rows(qf[h][None, None], kf[h][None, None], vf[h][None, None], sel)
+            if fm.code == 0:
+                oracle.forward_rows(qf[h][None, None], kf[h][None, None], vf[h][None, None], sel)
+            else:
+                oracle.forward_rows_map(qf[h][None, None], kf[h][None, None], vf[h][None, None],
+                                        sel, fm.name, fm.g, fm.eps, fm.scale)
         return time.perf_counter() - t0
 
     probe = 16
@@ -267,6 +299,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     w = workloads.WORKLOADS[args.workload]
+    fm = FeatureMap(args.map, args.g)
     q, k, v = workloads.make_qkv(w)
     BH = w.B * w.H
     # keep at most 4 heads on the host in fp64 (rows are sampled from them)
@@ -279,7 +312,7 @@ def run_reference(args):
     per_step_s = float(os.environ.get("KATA_REF_STEP_SECONDS", "3"))
     times, rows_total = [], 0
     for i in range(args.warmup + args.steps):
-        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, per_step_s, rng)
+        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, per_step_s, rng, fm)
         if i >= args.warmup:
             times.append(dt)
             rows_total += nrows
@@ -290,7 +323,7 @@ def run_reference(args):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w),
+        "config": _config(w, fm),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_total} output rows of heads 0..{keep - 1}, positions "
                                    f"uniform in [0,T), direct O(T^2) fp64 definition; "
@@ -306,9 +339,10 @@ def _metric():
     return "fwd tokens/s for chunked PSD linear attention; % bf16 tensor peak (1 GB300)"
 
 
-def _config(w):
+def _config(w, fm: FeatureMap = FULL_MAP):
     return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "C": w.C,
-            "feature_dim": w.n, "global_batch": w.B, "seq_len": w.T,
+            "feature_map": fm.label(), "feature_dim": fm.n(w.d), "global_batch": w.B,
+            "seq_len": w.T,
             "input_dtype": str(w.dtype).replace("torch.", ""),
             "l2": "inputs larger than L2, no flush" if _input_bytes(w) > L2_BYTES
             else "L2 flushed before every step (258 MB write, outside the per-step events)",
@@ -348,14 +382,24 @@ def run_ours(args):
     import kernelized_causal_linear_gb300 as kg
 
     w = workloads.WORKLOADS[args.workload]
+    fm = FeatureMap(args.map, args.g)
     peaks = _peaks()
     q, k, v = workloads.make_qkv(w, device="cuda")
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
     stream = torch.cuda.current_stream()
-    path = kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
+    if fm.code == 0:
+        path = kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
+
+        def fwd(q_, k_, v_, out_):
+            kg.kata_fwd_chunked(q_, k_, v_, w.C, out=out_)
+    else:
+        path = kg.KATA_PATH_SIMT   # the reduced maps run on CUDA cores
+
+        def fwd(q_, k_, v_, out_):
+            kg.kata_fwd_chunked_map(q_, k_, v_, w.C, fm.code, fm.g, fm.eps, fm.scale, out=out_)
 
     for _ in range(args.warmup):
-        kg.kata_fwd_chunked(q, k, v, w.C, out=out)
+        fwd(q, k, v, out)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -378,7 +422,7 @@ def run_ours(args):
             if flush is not None:
                 flush.fill_(i & 0xFF)
                 step_ev[i][0].record(stream)
-            kg.kata_fwd_chunked(q, k, v, w.C, out=out)
+            fwd(q, k, v, out)
             if flush is not None:
                 step_ev[i][1].record(stream)
         stop.record(stream)
@@ -404,7 +448,8 @@ def run_ours(args):
     roofline = None
     if dom is not None:
         nl, tot = stages[dom]
-        work, unit, bound = stage_work(dom, w, torch.cuda.get_device_properties(0).multi_processor_count)
+        work, unit, bound = stage_work(dom, w, torch.cuda.get_device_properties(0).multi_processor_count,
+                                       fm)
         mean_s = tot / nl / 1e3
         if work is not None:
             if unit == "TFLOP/s":
@@ -416,14 +461,14 @@ def run_ours(args):
             else:
                 achieved = work / mean_s / 1e9
                 peak, psrc = peaks["hbm_gbs"], f"HBM copy, {peaks['source']}"
-            traffic = _ncu_traffic(dom, w.name)
+            traffic = _ncu_traffic(dom, w.name) if fm.code == 0 else None
             roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
                         "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
                         "work_per_launch": work}
     # whole-call tensor fraction (algorithmic tensor flops over the step time)
     step_s = elapsed_ms / 1e3 / args.steps
-    alg_flops = call_flops(w)
+    alg_flops = call_flops(w, fm)
     whole = {"algorithmic_tflops": alg_flops / step_s / 1e12,
              "frac_of_bf16_peak": alg_flops / step_s / 1e12 / peaks["bf16_tflops"]}
 
@@ -432,11 +477,23 @@ def run_ours(args):
     if not args.no_e2e:
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
         steps_e2e = max(3, min(args.steps, 10))
+        if fm.code == 0:   # the C ABI's host-buffer entry point
+            def e2e_step():
+                kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
+        else:              # reduced maps: pinned copies in, the map forward, copy out
+            qd, kd, vd, od = (torch.empty_like(t) for t in (q, k, v, out))
+
+            def e2e_step():
+                for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
+                    dst.copy_(src, non_blocking=True)
+                fwd(qd, kd, vd, od)
+                oh.copy_(od, non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+        e2e_step()
         t0 = time.perf_counter()
         for _ in range(steps_e2e):
-            kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
+            e2e_step()
         dt = time.perf_counter() - t0
         es = qh.element_size()
         e2e = {"value": w.B * w.T * steps_e2e * world / dt, "unit": "tokens/s",
@@ -457,7 +514,7 @@ def run_ours(args):
         kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
         vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
         nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, args.cpu_seconds,
-                                            np.random.default_rng(1))
+                                            np.random.default_rng(1), fm)
         # each row is one head; a token of the workload has H heads
         tps = (nrows / w.H) / dt
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -469,7 +526,7 @@ def run_ours(args):
             "metric": _metric(), "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": _dtype_name(w), "data": "synthetic", "config": _config(w),
+            "dtype": _dtype_name(w), "data": "synthetic", "config": _config(w, fm),
             "path": {0: "none", 1: "simt", 2: "tcgen05"}.get(path, str(path)),
             "roofline": roofline, "whole_call": whole, "cpu_baseline": cpu, "e2e": e2e,
             "decode": decode, "clocks": clk.summary(), "gpu_launches": launches,
@@ -516,11 +573,16 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--map", default="full", choices=["full", "M", "Sigma"],
+                    help="feature map: the full rank-one map or a reduced PSD family")
+    ap.add_argument("--g", type=int, default=1, help="blocks of the reduced map (1, 2 or 4)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args(argv)
+    if args.map == "full" and args.g != 1:
+        ap.error("--map full takes --g 1")
     if args.warmup < 3:
         sys.stderr.write("warning: fewer than 3 warm-up steps\n")
     if args.impl == "reference":
