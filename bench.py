@@ -126,11 +126,14 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         if stage == "tc_segment_state":
             return 2.0 * n * (dv + 1) * seg_tokens, "TFLOP/s", "tensor"
         if stage == "tc_segment_output":
-            intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH
+            intra128 = 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, 128) * BH
             return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
         if stage == "tc_segment_scan":
             rec = 4.0 * (5 * 128 * dv + d * d)
             return 2.0 * rec * G * BH, "GB/s", "hbm"
+    if stage == "tc_sub_finalize":
+        # M_2 sub-heads: reads two fp32 numerators and denominators, writes bf16 out
+        return float(BH * T) * (2 * (dv + 1) * 4 + dv * 2), "GB/s", "hbm"
     if stage == "tc64_output":
         intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH
         return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
@@ -393,7 +396,7 @@ def run_ours(args):
         def fwd(q_, k_, v_, out_):
             kg.kata_fwd_chunked(q_, k_, v_, w.C, out=out_)
     else:
-        path = kg.KATA_PATH_SIMT   # the reduced maps run on CUDA cores
+        path = kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, fm.code, fm.g)
 
         def fwd(q_, k_, v_, out_):
             kg.kata_fwd_chunked_map(q_, k_, v_, w.C, fm.code, fm.g, fm.eps, fm.scale, out=out_)

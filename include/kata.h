@@ -154,9 +154,11 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   map, g: g in {1, 2, 4} dividing d; KATA_MAP_FULL needs g = 1.
  *   eps >= 0 and scale > 0, finite; KATA_MAP_FULL and KATA_MAP_BLOCK need
  *   eps = 0 and scale = 1 (KATA_ERR_ARG otherwise).
- * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  The
- * reduced maps run on CUDA cores in fp32 (bf16 inputs are widened; the output
- * is written in the input type).
+ * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  KATA-M_2
+ * at d = 64 with bf16 inputs and dv = 64 runs on the tensor cores as two d = 32
+ * sub-heads whose numerators and denominators add; the other reduced maps run
+ * on CUDA cores in fp32 (bf16 inputs are widened; the output is written in the
+ * input type).  kata_fwd_path_map tells which.
  */
 int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
                          int T, int d, int dv, int C, int dtype, int map, int g, float eps,
@@ -193,6 +195,10 @@ int kata_fwd_chunked_noalloc(const void *q, const void *k, const void *v, void *
  * to *bytes.  Same argument checks as kata_fwd_chunked; no device work. */
 int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype,
                             size_t *bytes);
+
+/* Which implementation kata_fwd_chunked_map selects for this shape and map on
+ * the current device (a kata_path value); KATA_PATH_NONE if it would reject it. */
+int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int map, int g);
 
 /* Which implementation kata_fwd_chunked selects for this shape on the current
  * device (a kata_path value); KATA_PATH_NONE if it would reject the call.

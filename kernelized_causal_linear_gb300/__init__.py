@@ -43,7 +43,8 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_workspace_size", "kata_fwd_path", "kata_fwd_chunked_host",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
-            "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim")
+            "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
+            "kata_fwd_path_map")
 
 _lib = None
 
@@ -92,6 +93,8 @@ def lib() -> ctypes.CDLL:
         L.kata_lift_map.argtypes = [p, p, ctypes.c_int64, i, i, i, i, f, f, vp]
         L.kata_map_feature_dim.argtypes = [i, i, i]
         L.kata_map_feature_dim.restype = i
+        L.kata_fwd_path_map.argtypes = [i, i, i, i, i, i, i, i, i]
+        L.kata_fwd_path_map.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -236,6 +239,11 @@ def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: t
                                 _dtype_code(q.dtype), _stream_handle(stream, q.device))
     _check(rc, "kata_decode_step")
     return out
+
+
+def kata_fwd_path_map(B, H, T, d, dv, C, dtype, map: int, g: int) -> int:
+    """Path kata_fwd_chunked_map takes for a shape and map (a KATA_PATH_* value)."""
+    return int(lib().kata_fwd_path_map(B, H, T, d, dv, C, _dtype_code(dtype), int(map), int(g)))
 
 
 def kata_map_feature_dim(map: int, d: int, g: int) -> int:

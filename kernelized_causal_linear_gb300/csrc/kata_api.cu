@@ -82,12 +82,25 @@ int device_info(DevInfo &out) {
 
 // Kernel families behind the public paths: KATA_PATH_TC covers both tensor-core
 // variants (d = 32 with segments, d = 64 with the state split over four CTAs).
-enum Kernels { kSimt, kTc32, kTc64 };
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub };
 
 Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
     if (s.dtype == KATA_F32) return kSimt;
     if (kata::tc_supported(s, di.major, di.minor)) return kTc32;
     if (kata::tc64_supported(s, di.major, di.minor, di.sms)) return kTc64;
+    return kSimt;
+}
+
+// Kernels for a reduced map: KATA-M_2 at d = 64 is two d = 32 sub-heads on the
+// d = 32 tensor path (bf16, dv = 64); every other reduced map runs on CUDA cores.
+Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
+                           bool with_state) {
+    if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
+    if (map.kind == KATA_MAP_BLOCK && map.g == 2 && s.d == 64 && !with_state) {
+        FwdShape half = s;
+        half.d = 32;
+        if (kata::tc_supported(half, di.major, di.minor)) return kTc32Sub;
+    }
     return kSimt;
 }
 
@@ -164,16 +177,18 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
-    const Kernels kn = map.kind == 0 ? select_kernels(s, di) : kSimt;   // reduced maps: CUDA cores
-    const size_t wsb = map.kind == 0 ? workspace_for(s, kn, di, with_state)
-                                     : kata::simt_workspace_bytes(s, map);
+    const Kernels kn = select_map_kernels(s, di, map, with_state);
+    const size_t wsb = kn == kTc32Sub ? kata::tc_workspace_bytes(s, di.sms, false, 2)
+                       : map.kind == 0 ? workspace_for(s, kn, di, with_state)
+                                       : kata::simt_workspace_bytes(s, map);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
-    cudaError_t e = kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
+    cudaError_t e = kn == kTc32Sub ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
+                    : kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
                     : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st, so)
                                   : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
@@ -201,6 +216,19 @@ int kata_map_feature_dim(int map, int d, int g) {
     ms.kind = map;
     ms.g = g;
     return ms.n(d);
+}
+
+int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int map, int g) {
+    if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_PATH_NONE;
+    if (!valid_map(map, d, g, 0.f, 1.f)) return KATA_PATH_NONE;
+    DevInfo di;
+    if (device_info(di)) return KATA_PATH_NONE;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    return select_map_kernels(FwdShape{B, H, T, d, dv, C, dtype}, di, ms, false) == kSimt
+               ? KATA_PATH_SIMT
+               : KATA_PATH_TC;
 }
 
 int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,

@@ -103,10 +103,13 @@ cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, cons
 
 // ---- tcgen05 path: kata_tc.cu ---------------------------------------------
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
-size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false);
+// nsub > 1: the head's q/k columns are nsub sub-heads of width d / nsub, each run
+// as a d / nsub head (KATA-M_2 at d = 64); their numerators and denominators are
+// summed.  No state export then.
+size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false, int nsub = 1);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
-                       const StateOut &so = StateOut{});
+                       const StateOut &so = StateOut{}, int nsub = 1);
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();

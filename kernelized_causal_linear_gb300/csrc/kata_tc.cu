@@ -68,7 +68,7 @@ constexpr int kStateRing = 4;
 template <int D, int DV>
 __global__ void __launch_bounds__(352, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 float *__restrict__ seg, int NCt, int Lc, int G) {
+                 float *__restrict__ seg, int NCt, int Lc, int G, int nsub) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int kStage = C::QK_TILE + C::V_TILE;
@@ -83,6 +83,8 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     __shared__ int abort_flag;
 
     const int g = blockIdx.x, bh = blockIdx.y;
+    // sub-head bh of nsub per head: columns D * (bh % nsub) .. of head bh / nsub
+    const int hz = bh / nsub, hx = (bh % nsub) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
@@ -119,11 +121,11 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 uint8_t *tk = sm + st * kStage;
                 const int t0 = (c0 + i) * kTile;
                 mbar_arrive_expect_tx(&tile_full[st], kStage);
-                tma_load_3d(tk, &tm_k, 0, t0, bh, &tile_full[st]);
-                tma_load_3d(tk + C::QK_TILE, &tm_v, 0, t0, bh, &tile_full[st]);
+                tma_load_3d(tk, &tm_k, hx, t0, hz, &tile_full[st]);
+                tma_load_3d(tk + C::QK_TILE, &tm_v, 0, t0, hz, &tile_full[st]);
                 if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
-                    tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
-                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_k, hx, t0 + kTile, hz);
+                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, hz);
                 }
             }
         }
@@ -275,11 +277,14 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
 //     token's row of one side (query or key) into both atom columns of a block
 // TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | Q K^T quarter [384,416) |
 //       P slots [416,432) [432,448) | output accumulator [448,512)
-template <int D, int DV>
+// kSub: sub-head form (KATA-M_2): the epilogue writes the fp32 numerator and the
+// denominator for sub_finalize_kernel instead of O.
+template <int D, int DV, bool kSub>
 __global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
-                  const float *__restrict__ seg, int T, int NCt, int Lc, int G) {
+                  const float *__restrict__ seg, int T, int NCt, int Lc, int G, int nsub,
+                  float *__restrict__ part) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
@@ -305,6 +310,8 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __shared__ int abort_flag;
 
     const int g = blockIdx.x, bh = blockIdx.y;
+    // sub-head bh of nsub per head: q/k columns D * (bh % nsub) .. of head bh / nsub
+    const int hz = bh / nsub, hx = (bh % nsub) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
@@ -349,13 +356,13 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
                 mbar_arrive_expect_tx(&chunk_full[st], 2 * C::QK_TILE + C::V_TILE);
-                tma_load_3d(tq, &tm_q, 0, t0, bh, &chunk_full[st]);
-                tma_load_3d(tk, &tm_k, 0, t0, bh, &chunk_full[st]);
-                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, bh, &chunk_full[st]);
+                tma_load_3d(tq, &tm_q, hx, t0, hz, &chunk_full[st]);
+                tma_load_3d(tk, &tm_k, hx, t0, hz, &chunk_full[st]);
+                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, hz, &chunk_full[st]);
                 if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
-                    tma_prefetch_3d(&tm_q, 0, t0 + kTile, bh);
-                    tma_prefetch_3d(&tm_k, 0, t0 + kTile, bh);
-                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, bh);
+                    tma_prefetch_3d(&tm_q, hx, t0 + kTile, hz);
+                    tma_prefetch_3d(&tm_k, hx, t0 + kTile, hz);
+                    tma_prefetch_3d(&tm_v, 0, t0 + kTile, hz);
                 }
             }
         }
@@ -574,6 +581,23 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool w = __all_sync(0xffffffffu, sy.wait(&o_full, i));
             if (!w) return false;
             tc_fence_after();
+            if constexpr (kSub) {   // sub-heads: N (fp32) and D, summed over sub-heads later
+                const int t = (c0 + i) * kTile + row;
+                float *dst = part + ((size_t)bh * T + t) * DV;
+#pragma unroll
+                for (int c32 = 0; c32 < DV; c32 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tXo + lsel + c32, v);
+                    if (t < T)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) st_global_v8(dst + c32 + 8 * e, v + 8 * e);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (elect_lane0()) mbar_arrive(&o_empty);
+                if (t < T) part[(size_t)gridDim.y * T * DV + (size_t)bh * T + t] = dsum;
+                return true;
+            }
             const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
             uint32_t o[DV / 2];   // the row in bf16 pairs
 #pragma unroll
@@ -750,6 +774,36 @@ Plan plan(const FwdShape &s, int num_sms) {
     return p;
 }
 
+// Sub-heads (KATA-M_2 at d = 64): O = (N_0 + N_1) / (D_0 + D_1) in bf16 (zero
+// where the sum of denominators is not positive), summed in sub-head order.
+// part: N [BH * nsub][T][64] fp32, then D [BH * nsub][T].  One thread per four
+// output values.
+__global__ void __launch_bounds__(256)
+sub_finalize_kernel(const float *__restrict__ part, bf16 *__restrict__ out, int64_t rows, int T,
+                    int nsub) {
+    const int64_t n4 = rows * 16;   // 64 values per row
+    const float *dd = part + (size_t)rows * nsub * 64;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = e >> 4, bh = row / T, t = row % T;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
+        for (int a = 0; a < nsub; ++a) {
+            const int64_t r = (bh * nsub + a) * T + t;
+            const float4 x = reinterpret_cast<const float4 *>(part + r * 64)[e & 15];
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+            den += dd[r];
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(out) + 2 * e;
+        o[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        o[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+}
+
 constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + kStateRing * 32768 + 2048;
 constexpr int kSmemOutput = 2 * Cfg<32, 64>::QK_TILE + 2 * Cfg<32, 64>::V_TILE + 2 * 65536 +
                             2 * 16384 + 2048 + 2048;
@@ -761,23 +815,42 @@ bool tc_supported(const FwdShape &s, int cc_major, int cc_minor) {
            encoder() != nullptr;
 }
 
-size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state) {
+namespace {
+// The shape the kernels see: nsub sub-heads of width d / nsub per head.
+FwdShape sub_shape(const FwdShape &s, int nsub) {
+    FwdShape ss = s;
+    ss.B = s.B * nsub;
+    ss.d = s.d / nsub;
+    return ss;
+}
+// Sub-head partials (N and D, fp32) come first in the workspace, rounded to 256 bytes.
+size_t sub_part_floats(const FwdShape &ss, int nsub) {
+    return nsub > 1 ? (((size_t)ss.BH() * ss.T * 65 + 63) & ~(size_t)63) : 0;
+}
+}  // namespace
+
+size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int nsub) {
+    const FwdShape s = sub_shape(s0, nsub);
     const Plan p = plan(s, num_sms);
     // segment records (G of them), plus the inclusive totals when the state is exported
     const size_t recs = with_state ? (size_t)p.G + 1 : (p.G <= 1 ? 0 : (size_t)p.G);
-    return sizeof(float) * (size_t)s.BH() * recs * Cfg<32, 64>::E;
+    return sizeof(float) * (sub_part_floats(s, nsub) + (size_t)s.BH() * recs * Cfg<32, 64>::E);
 }
 
-cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const void *v,
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
-                       const StateOut &so) {
+                       const StateOut &so, int nsub) {
     using C = Cfg<32, 64>;
+    if (nsub > 1 && so.state != nullptr) return cudaErrorInvalidValue;   // no sub-head state export
+    const FwdShape s = sub_shape(s0, nsub);
     const Plan p = plan(s, num_sms);
     CUtensorMap mq, mk, mv;
-    if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
-        !make_map(mv, v, s.dv, s.T, s.BH()))
+    // q, k: rows of s0.d columns, read s.d at a time; v: one head's rows, shared by its sub-heads
+    if (!make_map(mq, q, s0.d, s.T, s0.BH(), s.d) || !make_map(mk, k, s0.d, s.T, s0.BH(), s.d) ||
+        !make_map(mv, v, s.dv, s.T, s0.BH()))
         return cudaErrorInvalidValue;
-    float *seg = static_cast<float *>(workspace);
+    float *part = nsub > 1 ? static_cast<float *>(workspace) : nullptr;
+    float *seg = static_cast<float *>(workspace) + sub_part_floats(s, nsub);
     const bool with_state = so.state != nullptr;
     // Segment sums: of every segment but the last (the output kernel carries the
     // last one on chip), and of the last one too when the final state is wanted.
@@ -788,7 +861,7 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
         {
             TraceScope tr("tc_segment_state", stream);
             seg_state_kernel<32, 64><<<dim3(nsum, s.BH()), 352, kSmemState, stream>>>(
-                mk, mv, seg, p.NCt, p.Lc, p.G);
+                mk, mv, seg, p.NCt, p.Lc, p.G, nsub);
         }
         float *totals = with_state ? seg + (size_t)s.BH() * p.G * C::E : nullptr;
         cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream,
@@ -799,12 +872,25 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
             state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
         }
     }
-    cudaFuncSetAttribute(seg_output_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemOutput);
     {
         TraceScope tr("tc_segment_output", stream);
-        seg_output_kernel<32, 64><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-            mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G);
+        if (part == nullptr) {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
+            seg_output_kernel<32, 64, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G, nsub, part);
+        } else {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
+            seg_output_kernel<32, 64, true><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G, nsub, part);
+        }
+    }
+    if (part != nullptr) {
+        TraceScope tr("tc_sub_finalize", stream);
+        const int64_t rows = (int64_t)s0.BH() * s0.T;
+        const int blocks = (int)std::min<int64_t>((rows * 16 + 255) / 256, 152 * 16);
+        sub_finalize_kernel<<<blocks, 256, 0, stream>>>(part, (bf16 *)out, rows, s0.T, nsub);
     }
     return cudaGetLastError();
 }

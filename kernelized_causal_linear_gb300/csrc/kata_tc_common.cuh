@@ -382,15 +382,18 @@ EncodeTiledFn encoder() {
     return fn;
 }
 
-// [BH][T][inner] bf16 viewed as a 3-D tensor; box = one 128-row tile of one head.
-bool make_map(CUtensorMap &m, const void *base, int inner, int T, int BH) {
+// [BH][T][inner] bf16 viewed as a 3-D tensor; box = one 128-row tile of one head,
+// box_inner columns wide (all of them by default; fewer to read one block of
+// the columns), swizzled over its row of box_inner * 2 bytes.
+bool make_map(CUtensorMap &m, const void *base, int inner, int T, int BH, int box_inner = 0) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
+    if (box_inner <= 0) box_inner = inner;
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)T, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)T * inner * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)kTile, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)kTile, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const int rb = inner * 2;
+    const int rb = box_inner * 2;
     const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                             : CU_TENSOR_MAP_SWIZZLE_32B;

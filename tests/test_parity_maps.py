@@ -100,3 +100,31 @@ def test_map_full_size_sampled_rows(kg, map_, g):
         got = to_f64(out.reshape(BH, w.T, w.dv)[h][ts])
         worst = max(worst, slice_rel_err(got, ref))
     assert worst <= TOL[w.dtype], f"{NAMES[map_]}_{g}: {worst:.3e}"
+
+
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # 4 sub-heads: many one-chunk segments (state kernel + scan per sub-head)
+    (8, 8, 700),     # 128 sub-heads, one segment each, ragged tail
+    (2, 3, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+])
+def test_m2_tensor_path(kg, B, H, T):
+    """KATA-M_2 at d = 64 (bf16, dv = 64): two d = 32 sub-heads on the tensor path,
+    numerators and denominators summed."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 1, 2) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 1, 2)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "M", 2)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+def test_other_maps_take_cuda_cores(kg):
+    w = workloads.WORKLOADS["lm_layer_bf16"]
+    for map_, g in ((1, 4), (2, 2), (2, 4)):
+        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
+            kg.KATA_PATH_SIMT
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, torch.float32, 1, 2) == \
+        kg.KATA_PATH_SIMT
