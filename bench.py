@@ -131,6 +131,9 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         if stage == "tc_segment_scan":
             rec = 4.0 * (5 * 128 * dv + d * d)
             return 2.0 * rec * G * BH, "GB/s", "hbm"
+    if stage == "tc_quadratic":
+        # every causal (t, s <= t) pair of the head: (q.k)^2 and P [V|1]
+        return 2.0 * (d + dv + 1) * _intra_pairs(T, T) * BH, "TFLOP/s", "tensor"
     if stage == "tc_sub_finalize":
         # M_2 sub-heads: reads two fp32 numerators and denominators, writes bf16 out
         return float(BH * T) * (2 * (dv + 1) * 4 + dv * 2), "GB/s", "hbm"
@@ -143,12 +146,14 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     return None, "", ""
 
 
-def call_flops(w, fm: FeatureMap = FULL_MAP) -> float:
+def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
     """Algorithmic flops of one forward call at the workload's chunk size:
     2n(dv+1) (state) + 2n(dv+1) (inter output) per token and head, plus the
     causal intra-chunk term 2(d'+dv+1) per (t, s<=t) pair inside chunks (d' the
     weight's multiply-adds: d, or g d for Sigma_g)."""
     BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, fm.n(w.d)
+    if algo == "quadratic":   # the O(T^2) form: every causal pair
+        return 2.0 * (d + dv + 1) * _intra_pairs(T, T) * BH
     return 4.0 * n * (dv + 1) * T * BH + 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, C) * BH
 
 
@@ -390,7 +395,12 @@ def run_ours(args):
     q, k, v = workloads.make_qkv(w, device="cuda")
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
     stream = torch.cuda.current_stream()
-    if fm.code == 0:
+    if args.algo == "quadratic":
+        path = kg.KATA_PATH_TC
+
+        def fwd(q_, k_, v_, out_):
+            kg.kata_fwd_quadratic(q_, k_, v_, out=out_)
+    elif fm.code == 0:
         path = kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
 
         def fwd(q_, k_, v_, out_):
@@ -471,7 +481,7 @@ def run_ours(args):
                         "work_per_launch": work}
     # whole-call tensor fraction (algorithmic tensor flops over the step time)
     step_s = elapsed_ms / 1e3 / args.steps
-    alg_flops = call_flops(w, fm)
+    alg_flops = call_flops(w, fm, args.algo)
     whole = {"algorithmic_tflops": alg_flops / step_s / 1e12,
              "frac_of_bf16_peak": alg_flops / step_s / 1e12 / peaks["bf16_tflops"]}
 
@@ -481,10 +491,10 @@ def run_ours(args):
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         steps_e2e = max(3, min(args.steps, 10))
-        if fm.code == 0:   # the C ABI's host-buffer entry point
+        if fm.code == 0 and args.algo == "chunked":   # the C ABI's host-buffer entry point
             def e2e_step():
                 kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
-        else:              # reduced maps: pinned copies in, the map forward, copy out
+        else:   # pinned copies in, the forward, copy out
             qd, kd, vd, od = (torch.empty_like(t) for t in (q, k, v, out))
 
             def e2e_step():
@@ -529,7 +539,8 @@ def run_ours(args):
             "metric": _metric(), "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": _dtype_name(w), "data": "synthetic", "config": _config(w, fm),
+            "dtype": _dtype_name(w), "data": "synthetic",
+            "config": dict(_config(w, fm), algorithm=args.algo),
             "path": {0: "none", 1: "simt", 2: "tcgen05"}.get(path, str(path)),
             "roofline": roofline, "whole_call": whole, "cpu_baseline": cpu, "e2e": e2e,
             "decode": decode, "clocks": clk.summary(), "gpu_launches": launches,
@@ -579,6 +590,8 @@ def main(argv=None):
     ap.add_argument("--map", default="full", choices=["full", "M", "Sigma"],
                     help="feature map: the full rank-one map or a reduced PSD family")
     ap.add_argument("--g", type=int, default=1, help="blocks of the reduced map (1, 2 or 4)")
+    ap.add_argument("--algo", default="chunked", choices=["chunked", "quadratic"],
+                    help="chunked O(T) form (the default) or the quadratic flash-style form")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -586,6 +599,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.map == "full" and args.g != 1:
         ap.error("--map full takes --g 1")
+    if args.algo == "quadratic" and args.map != "full":
+        ap.error("--algo quadratic runs the full map")
     if args.warmup < 3:
         sys.stderr.write("warning: fewer than 3 warm-up steps\n")
     if args.impl == "reference":

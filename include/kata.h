@@ -165,6 +165,21 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
                          float scale, kata_stream_t stream);
 
 /*
+ * kata_fwd_quadratic -- the quadratic (flash-style) form of the same forward:
+ * o_t = sum_{s<=t} (q_t . k_s)^2 v_s / sum_{s<=t} (q_t . k_s)^2 evaluated tile
+ * by tile, with no state ([KATA] Sec. 2 Eq. 2 directly; the pages' O(T^2)
+ * kernel).  O(T^2) work against the chunked form's O(T n dv): the faster form
+ * while T is short against n = d(d+1)/2.  The weights are non-negative, so no
+ * running maximum is kept.
+ *   q, k, v, out, B, H, T, d, dv, dtype, stream: as kata_fwd_chunked (no C).
+ *   Supported: bf16, d in {32, 64}, dv = 64, on sm_103a (KATA_ERR_UNSUPPORTED
+ *   otherwise).  Rounding as the tensor-core chunked path (P in bf16 as an MMA
+ *   operand, fp32 accumulation and denominators).  No workspace.
+ */
+int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, int B, int H,
+                       int T, int d, int dv, int dtype, kata_stream_t stream);
+
+/*
  * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
  * arguments, layouts, paths and results), for callers that cannot allocate
  * device memory where they run it: code whose device memory is owned by a

@@ -44,7 +44,7 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
-            "kata_fwd_path_map")
+            "kata_fwd_path_map", "kata_fwd_quadratic")
 
 _lib = None
 
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
         L.kata_map_feature_dim.restype = i
         L.kata_fwd_path_map.argtypes = [i, i, i, i, i, i, i, i, i]
         L.kata_fwd_path_map.restype = i
+        L.kata_fwd_quadratic.argtypes = [p, p, p, p, i, i, i, i, i, i, vp]
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -238,6 +239,21 @@ def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: t
                                 v.data_ptr(), out.data_ptr(), B, H, d, dv,
                                 _dtype_code(q.dtype), _stream_handle(stream, q.device))
     _check(rc, "kata_decode_step")
+    return out
+
+
+def kata_fwd_quadratic(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Quadratic (flash-style) KATA forward. q,k: [B,H,T,d]; v: [B,H,T,dv] on CUDA."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd_quadratic(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  B, H, T, d, dv, _dtype_code(q.dtype),
+                                  _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_quadratic")
     return out
 
 

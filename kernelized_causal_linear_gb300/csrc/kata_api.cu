@@ -243,6 +243,29 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
     return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{}, ms);
 }
 
+int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, int B, int H,
+                       int T, int d, int dv, int dtype, kata_stream_t stream) {
+    if (!q || !k || !v || !out) return KATA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, 64, dtype);
+    if (rc) return rc;
+    const size_t es = elem_size(dtype);
+    const size_t nqk = (size_t)B * H * T * d * es, nvo = (size_t)B * H * T * dv * es;
+    if (overlap(out, nvo, q, nqk) || overlap(out, nvo, k, nqk) || overlap(out, nvo, v, nvo))
+        return KATA_ERR_ARG;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    const FwdShape s{B, H, T, d, dv, 64, dtype};
+    if (!kata::quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
+    cudaGetLastError();
+    if (kata::quad_forward(s, q, k, v, out, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
 int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
                            float *z, int B, int H, int T, int d, int dv, int C, int dtype,
                            kata_stream_t stream) {
@@ -332,9 +355,9 @@ int kata_sync_status(kata_stream_t stream) {
         cudaGetLastError();
         return KATA_ERR_CUDA;
     }
-    const int e = kata::tc_take_error(), e64 = kata::tc64_take_error();
-    if (e < 0 || e64 < 0) return KATA_ERR_CUDA;
-    return (e | e64) ? KATA_ERR_TIMEOUT : KATA_OK;
+    const int e = kata::tc_take_error(), e64 = kata::tc64_take_error(), eq = kata::quad_take_error();
+    if (e < 0 || e64 < 0 || eq < 0) return KATA_ERR_CUDA;
+    return (e | e64 | eq) ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 
 int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int map, int g,

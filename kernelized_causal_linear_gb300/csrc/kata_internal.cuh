@@ -122,4 +122,10 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
                          const StateOut &so = StateOut{});
 int tc64_take_error();
 
+// ---- quadratic (flash-style) forward: kata_quad.cu ------------------------
+bool quad_supported(const FwdShape &s, int cc_major, int cc_minor);
+cudaError_t quad_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                         void *out, cudaStream_t stream);
+int quad_take_error();
+
 }  // namespace kata
