@@ -8,11 +8,13 @@
 // and the row sums of P in registers.  The weights are non-negative, so no
 // running maximum is needed (unlike softmax attention).
 //
-// Grid (query tiles, heads), tiles in decreasing order of work; 192 threads:
-//   warp 0: TMA (Q tile once; K and V tiles through a 3-stage ring),
+// Grid (heads, query tiles): CTAs launch in order of x fastest, so the heads'
+// longest tiles (most key tiles) go first and the short ones fill the tail; 320 threads:
+//   warp 0: TMA (Q tile once; K and V tiles through a ring of 2-3 stages),
 //   warp 1: MMA issue (one thread),
-//   warps 2-5 ("P warps", TMEM lane quarter = warp % 4): S row -> P row and
-//     row sums; the epilogue O / D.
+//   warps 2-9 ("P warps", TMEM lane quarter = warp % 4, key half = (warp - 2) / 4):
+//     64 keys of a query row: S -> P and a partial row sum; the epilogue O / D
+//     for 32 of the output columns (the two halves' sums meet in shared memory).
 // TMEM (256 columns, two CTAs per SM): S [0,128) | P [128,192) | O [192,256).
 #include "kata_tc_common.cuh"
 
@@ -22,40 +24,42 @@ __device__ int g_quad_error = 0;   // sticky: bounded waits that expired
 
 namespace {
 
-constexpr int kKvStages = 3;
-
+// K/V ring depth: as deep as lets two CTAs share an SM's shared memory (three
+// 32 KB stages at d = 64 overshoot half an SM by a few hundred bytes).
 template <int D>
 struct QuadCfg {
+    static constexpr int STAGES = D == 64 ? 2 : 3;
     static constexpr int QK_TILE = kTile * D * 2;   // 8 or 16 KB
     static constexpr int V_TILE = kTile * 64 * 2;   // 16 KB (dv = 64)
     static constexpr int SW = D == 64 ? kSw128 : kSw64;
     static constexpr int SBO = D * 2 * 8;            // 8 rows of the swizzled tile
-    static constexpr int SMEM = QK_TILE + kKvStages * (QK_TILE + V_TILE) + 1024;
+    static constexpr int SMEM = QK_TILE + STAGES * (QK_TILE + V_TILE) + 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(320, 2)
 quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out, int T, int NT) {
     using C = QuadCfg<D>;
     constexpr int DV = 64;
-    constexpr int kPWarps = 4;
+    constexpr int kPWarps = 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *tq = sm;
-    uint8_t *tk = sm + C::QK_TILE;                        // [kKvStages][QK_TILE]
-    uint8_t *tv = tk + kKvStages * C::QK_TILE;            // [kKvStages][V_TILE]
+    uint8_t *tk = sm + C::QK_TILE;                        // [C::STAGES][QK_TILE]
+    uint8_t *tv = tk + C::STAGES * C::QK_TILE;            // [C::STAGES][V_TILE]
     // q_full: the Q tile landed.  kv_full[s] / kv_empty[s]: stage s holds K_j, V_j
     //   (TMA bytes) / the MMAs that read them are done.  s_full: S = Q K_j^T is in
     //   TMEM; s_free: the P warps have read it.  p_full: P_j is in TMEM; p_free:
     //   the P V MMA that read it is done.  o_done: every MMA is done.
-    __shared__ __align__(8) uint64_t q_full, kv_full[kKvStages], kv_empty[kKvStages], s_full,
+    __shared__ __align__(8) uint64_t q_full, kv_full[C::STAGES], kv_empty[C::STAGES], s_full,
         s_free, p_full, p_free, o_done, fin_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    __shared__ float dpart[2][kTile];   // the two key halves' row sums
 
-    const int qi = NT - 1 - (int)blockIdx.x;   // longest tiles first
-    const int bh = blockIdx.y;
+    const int qi = NT - 1 - (int)blockIdx.y;   // longest tiles first
+    const int bh = blockIdx.x;
     const int nj = qi + 1;                      // key tiles 0 .. qi
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Sync sy{&abort_flag};
@@ -63,7 +67,7 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&q_full, 1);
-        for (int s = 0; s < kKvStages; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
@@ -90,7 +94,7 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_arrive_expect_tx(&q_full, C::QK_TILE);
             tma_load_3d(tq, &tm_q, 0, qi * kTile, bh, &q_full);
             for (int j = 0; j < nj; ++j) {
-                const int st = j % kKvStages, use = j / kKvStages;
+                const int st = j % C::STAGES, use = j / C::STAGES;
                 if (use >= 1 && !sy.wait(&kv_empty[st], use - 1)) break;
                 mbar_arrive_expect_tx(&kv_full[st], C::QK_TILE + C::V_TILE);
                 tma_load_3d(tk + st * C::QK_TILE, &tm_k, 0, j * kTile, bh, &kv_full[st]);
@@ -106,7 +110,7 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint64_t dK = smem_desc(smem_u32(tk), 16, C::SBO, C::SW);      // K-major B
             const uint64_t dV = smem_desc(smem_u32(tv), 16384, 1024, kSw128);    // MN-major B
             auto qk = [&](int j) {   // S = Q K_j^T
-                const uint64_t b0 = desc_add(dK, (j % kKvStages) * C::QK_TILE);
+                const uint64_t b0 = desc_add(dK, (j % C::STAGES) * C::QK_TILE);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     mma_ss(tS, desc_add(dQ, ks * 32), desc_add(b0, ks * 32), kIdQK, ks > 0);
@@ -120,8 +124,8 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int j = 0; j < nj && ok; ++j) {
                 // S_{j+1} once the P warps have read S_j (they may still be writing P_j)
                 if (j + 1 < nj) {
-                    const int st1 = (j + 1) % kKvStages;
-                    ok = sy.wait(&kv_full[st1], (j + 1) / kKvStages) && sy.wait(&s_free, j);
+                    const int st1 = (j + 1) % C::STAGES;
+                    ok = sy.wait(&kv_full[st1], (j + 1) / C::STAGES) && sy.wait(&s_free, j);
                     if (!ok) break;
                     tc_fence_after();
                     qk(j + 1);
@@ -130,20 +134,21 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 ok = sy.wait(&p_full, j);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t b0 = desc_add(dV, (j % kKvStages) * C::V_TILE);
+                const uint64_t b0 = desc_add(dV, (j % C::STAGES) * C::V_TILE);
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
                     mma_ts(tO, tP + ks * 8, desc_add(b0, ks * 2048), kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(&p_free);
-                mma_commit(&kv_empty[j % kKvStages]);
+                mma_commit(&kv_empty[j % C::STAGES]);
             }
             mma_commit(&o_done);
             mma_commit(&fin_bar);
             sy.wait(&fin_bar, 0);
         }
     } else {
-        // ================= P warps: query row r = 32 * (warp % 4) + lane
-        const int quarter = warp & 3;
+        // ================= P warps: query row r = 32 * (warp % 4) + lane, keys
+        // 64 h .. 64 h + 63 of each tile
+        const int quarter = warp & 3, h = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
         float dsum = 0.f;
@@ -153,14 +158,14 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (!ok) break;
             tc_fence_after();
             const bool diag = j == qi;   // keys past the query are masked on the diagonal tile
-            uint32_t pw[kTile / 2];
+            uint32_t pw[32];
 #pragma unroll
-            for (int c32 = 0; c32 < kTile; c32 += 32) {
+            for (int c32 = 0; c32 < 64; c32 += 32) {
                 uint32_t v[32];
-                tmem_ld32(tS + lsel + c32, v);
+                tmem_ld32(tS + lsel + 64 * h + c32, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int c = c32 + 2 * e;
+                    const int c = 64 * h + c32 + 2 * e;
                     const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
                     const float w0 = (!diag || c <= r) ? x0 * x0 : 0.f;
                     const float w1 = (!diag || c + 1 <= r) ? x1 * x1 : 0.f;
@@ -177,28 +182,32 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kTile / 2; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 uint32_t w16[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) w16[e] = pw[c + e];
-                tmem_st16(tP + lsel + c, w16);
+                tmem_st16(tP + lsel + 32 * h + c, w16);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&p_full);
         }
-        // epilogue: O = N / D (a zero denominator gives a zero row)
+        // epilogue: O = N / D (a zero denominator gives a zero row); every P warp
+        // reaches the named barrier once, also after a failed wait
+        dpart[h][r] = dsum;
+        asm volatile("bar.sync 1, %0;" ::"r"(kPWarps * 32) : "memory");
         if (ok && __all_sync(0xffffffffu, sy.wait(&o_done, 0))) {
             tc_fence_after();
-            const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
-            uint32_t v[DV];
-            tmem_ld64(tO + lsel, v);
+            const float den = dpart[0][r] + dpart[1][r];
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            uint32_t v[32];
+            tmem_ld32(tO + lsel + 32 * h, v);
             const int t = qi * kTile + r;
             if (t < T) {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t) * DV);
+                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t) * DV + 32 * h);
 #pragma unroll
-                for (int c = 0; c < DV / 8; ++c)
+                for (int c = 0; c < 4; ++c)
                     dst[c] = make_uint4(
                         pack_bf16(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv),
                         pack_bf16(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv),
@@ -224,7 +233,7 @@ cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const v
     const int NT = (s.T + kTile - 1) / kTile;
     cudaFuncSetAttribute(quad_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     TraceScope tr("tc_quadratic", stream);
-    quad_kernel<D><<<dim3(NT, s.BH()), 192, C::SMEM, stream>>>(mq, mk, mv, (bf16 *)out, s.T, NT);
+    quad_kernel<D><<<dim3(s.BH(), NT), 320, C::SMEM, stream>>>(mq, mk, mv, (bf16 *)out, s.T, NT);
     return cudaGetLastError();
 }
 
@@ -232,7 +241,7 @@ cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const v
 
 bool quad_supported(const FwdShape &s, int cc_major, int cc_minor) {
     return s.dtype == 1 && cc_major == 10 && cc_minor == 3 && (s.d == 32 || s.d == 64) &&
-           s.dv == 64 && encoder() != nullptr;
+           s.dv == 64 && (s.T + kTile - 1) / kTile <= 65535 && encoder() != nullptr;
 }
 
 cudaError_t quad_forward(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
