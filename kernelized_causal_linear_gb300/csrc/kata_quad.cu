@@ -10,7 +10,9 @@
 //
 // Grid (heads, query tiles): CTAs launch in order of x fastest, so the heads'
 // longest tiles (most key tiles) go first and the short ones fill the tail; 320 threads:
-//   warp 0: TMA (Q tile once; K and V tiles through a ring of 2-3 stages),
+//   warp 0: TMA (Q tile once; K tiles and V tiles through two rings: a K slot is
+//     free once its S MMA is done, a V slot once its P V MMA is, so the next K
+//     tile's L2 fetch starts a tile earlier than with shared K/V slots),
 //   warp 1: MMA issue (one thread),
 //   warps 2-9 ("P warps", TMEM lane quarter = warp % 4, key half = (warp - 2) / 4):
 //     64 keys of a query row: S -> P and a partial row sum; the epilogue O / D
@@ -24,17 +26,38 @@ __device__ int g_quad_error = 0;   // sticky: bounded waits that expired
 
 namespace {
 
-// K/V ring depth: as deep as lets two CTAs share an SM's shared memory (three
-// 32 KB stages at d = 64 overshoot half an SM by a few hundred bytes).
+// Ring depths: as deep as lets two CTAs share an SM's shared memory (97 KB at
+// d = 64, 81 KB at d = 32).
 template <int D>
 struct QuadCfg {
-    static constexpr int STAGES = D == 64 ? 2 : 3;
+    static constexpr int KST = 3;
+    static constexpr int VST = D == 64 ? 2 : 3;
     static constexpr int QK_TILE = kTile * D * 2;   // 8 or 16 KB
     static constexpr int V_TILE = kTile * 64 * 2;   // 16 KB (dv = 64)
     static constexpr int SW = D == 64 ? kSw128 : kSw64;
     static constexpr int SBO = D * 2 * 8;            // 8 rows of the swizzled tile
-    static constexpr int SMEM = QK_TILE + STAGES * (QK_TILE + V_TILE) + 1024;
+    static constexpr int SMEM = (1 + KST) * QK_TILE + VST * V_TILE + 1024;
 };
+
+// Packed fp32 pairs (two lanes of one 64-bit register; sm_100 family).
+__device__ __forceinline__ uint64_t f2_make(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sq(uint64_t x) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %1;" : "=l"(r) : "l"(x));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t x, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 2)
@@ -46,14 +69,15 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align1024(smem_raw);
     uint8_t *tq = sm;
-    uint8_t *tk = sm + C::QK_TILE;                        // [C::STAGES][QK_TILE]
-    uint8_t *tv = tk + C::STAGES * C::QK_TILE;            // [C::STAGES][V_TILE]
-    // q_full: the Q tile landed.  kv_full[s] / kv_empty[s]: stage s holds K_j, V_j
-    //   (TMA bytes) / the MMAs that read them are done.  s_full: S = Q K_j^T is in
-    //   TMEM; s_free: the P warps have read it.  p_full: P_j is in TMEM; p_free:
-    //   the P V MMA that read it is done.  o_done: every MMA is done.
-    __shared__ __align__(8) uint64_t q_full, kv_full[C::STAGES], kv_empty[C::STAGES], s_full,
-        s_free, p_full, p_free, o_done, fin_bar;
+    uint8_t *tk = sm + C::QK_TILE;                        // [KST][QK_TILE]
+    uint8_t *tv = tk + C::KST * C::QK_TILE;               // [VST][V_TILE]
+    // q_full: the Q tile landed.  k_full[s] / k_empty[s]: K slot s holds K_j (TMA
+    //   bytes) / the S MMA that read it is done; v_full / v_empty likewise for V_j
+    //   and the P V MMA.  s_full: S = Q K_j^T is in TMEM; s_free: the P warps have
+    //   read it.  p_full: P_j is in TMEM; p_free: the P V MMA that read it is
+    //   done.  o_done: every MMA is done.
+    __shared__ __align__(8) uint64_t q_full, k_full[C::KST], k_empty[C::KST], v_full[C::VST],
+        v_empty[C::VST], s_full, s_free, p_full, p_free, o_done, fin_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ float dpart[2][kTile];   // the two key halves' row sums
@@ -67,9 +91,13 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&q_full, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < C::KST; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         mbar_init(&s_full, 1);
         mbar_init(&s_free, kPWarps);
@@ -94,11 +122,14 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             mbar_arrive_expect_tx(&q_full, C::QK_TILE);
             tma_load_3d(tq, &tm_q, 0, qi * kTile, bh, &q_full);
             for (int j = 0; j < nj; ++j) {
-                const int st = j % C::STAGES, use = j / C::STAGES;
-                if (use >= 1 && !sy.wait(&kv_empty[st], use - 1)) break;
-                mbar_arrive_expect_tx(&kv_full[st], C::QK_TILE + C::V_TILE);
-                tma_load_3d(tk + st * C::QK_TILE, &tm_k, 0, j * kTile, bh, &kv_full[st]);
-                tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, j * kTile, bh, &kv_full[st]);
+                const int ks = j % C::KST, ku = j / C::KST;
+                if (ku >= 1 && !sy.wait(&k_empty[ks], ku - 1)) break;
+                mbar_arrive_expect_tx(&k_full[ks], C::QK_TILE);
+                tma_load_3d(tk + ks * C::QK_TILE, &tm_k, 0, j * kTile, bh, &k_full[ks]);
+                const int vs = j % C::VST, vu = j / C::VST;
+                if (vu >= 1 && !sy.wait(&v_empty[vs], vu - 1)) break;
+                mbar_arrive_expect_tx(&v_full[vs], C::V_TILE);
+                tma_load_3d(tv + vs * C::V_TILE, &tm_v, 0, j * kTile, bh, &v_full[vs]);
             }
         }
     } else if (warp == 1) {
@@ -110,13 +141,15 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint64_t dK = smem_desc(smem_u32(tk), 16, C::SBO, C::SW);      // K-major B
             const uint64_t dV = smem_desc(smem_u32(tv), 16384, 1024, kSw128);    // MN-major B
             auto qk = [&](int j) {   // S = Q K_j^T
-                const uint64_t b0 = desc_add(dK, (j % C::STAGES) * C::QK_TILE);
+                const int ks0 = j % C::KST;
+                const uint64_t b0 = desc_add(dK, ks0 * C::QK_TILE);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     mma_ss(tS, desc_add(dQ, ks * 32), desc_add(b0, ks * 32), kIdQK, ks > 0);
                 mma_commit(&s_full);
+                mma_commit(&k_empty[ks0]);
             };
-            bool ok = sy.wait(&q_full, 0) && sy.wait(&kv_full[0], 0);
+            bool ok = sy.wait(&q_full, 0) && sy.wait(&k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 qk(0);
@@ -124,22 +157,22 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int j = 0; j < nj && ok; ++j) {
                 // S_{j+1} once the P warps have read S_j (they may still be writing P_j)
                 if (j + 1 < nj) {
-                    const int st1 = (j + 1) % C::STAGES;
-                    ok = sy.wait(&kv_full[st1], (j + 1) / C::STAGES) && sy.wait(&s_free, j);
+                    ok = sy.wait(&k_full[(j + 1) % C::KST], (j + 1) / C::KST) && sy.wait(&s_free, j);
                     if (!ok) break;
                     tc_fence_after();
                     qk(j + 1);
                 }
                 // O += P_j V_j
-                ok = sy.wait(&p_full, j);
+                const int vs = j % C::VST;
+                ok = sy.wait(&v_full[vs], j / C::VST) && sy.wait(&p_full, j);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t b0 = desc_add(dV, (j % C::STAGES) * C::V_TILE);
+                const uint64_t b0 = desc_add(dV, vs * C::V_TILE);
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
                     mma_ts(tO, tP + ks * 8, desc_add(b0, ks * 2048), kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(&p_free);
-                mma_commit(&kv_empty[j % C::STAGES]);
+                mma_commit(&v_empty[vs]);
             }
             mma_commit(&o_done);
             mma_commit(&fin_bar);
@@ -158,21 +191,35 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (!ok) break;
             tc_fence_after();
             const bool diag = j == qi;   // keys past the query are masked on the diagonal tile
-            uint32_t pw[32];
+            uint32_t v[64], pw[32];
+            tmem_ld64(tS + lsel + 64 * h, v);
+            if (!diag) {
+                // packed pairs: one multiply, one add and one convert per two keys;
+                // four accumulator chains so the adds overlap
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c32 = 0; c32 < 64; c32 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tS + lsel + 64 * h + c32, v);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c = 64 * h + c32 + 2 * e;
-                    const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-                    const float w0 = (!diag || c <= r) ? x0 * x0 : 0.f;
-                    const float w1 = (!diag || c + 1 <= r) ? x1 * x1 : 0.f;
-                    dsum += w0;
-                    dsum += w1;
-                    pw[c32 / 2 + e] = pack_bf16(w0, w1);
+                for (int e = 0; e < 32; ++e) {
+                    const uint64_t w = f2_sq(f2_make(v[2 * e], v[2 * e + 1]));
+                    acc[e & 3] = f2_add(acc[e & 3], w);
+                    float w0, w1;
+                    f2_split(w, w0, w1);
+                    pw[e] = pack_bf16(w0, w1);
                 }
+                float a0, a1;
+                f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                dsum += a0 + a1;
+            } else {
+                float ds[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int c = 64 * h + 2 * e;
+                    const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
+                    const float w0 = c <= r ? x0 * x0 : 0.f;
+                    const float w1 = c + 1 <= r ? x1 * x1 : 0.f;
+                    ds[e & 3] += w0 + w1;
+                    pw[e] = pack_bf16(w0, w1);
+                }
+                dsum += (ds[0] + ds[1]) + (ds[2] + ds[3]);
             }
             tc_fence_before();
             __syncwarp();
@@ -181,13 +228,7 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             ok = __all_sync(0xffffffffu, j == 0 || sy.wait(&p_free, j - 1));
             if (!ok) break;
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 32; c += 16) {
-                uint32_t w16[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w16[e] = pw[c + e];
-                tmem_st16(tP + lsel + 32 * h + c, w16);
-            }
+            tmem_st32(tP + lsel + 32 * h, pw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
