@@ -10,9 +10,9 @@
 //
 // Grid (heads, query tiles): CTAs launch in order of x fastest, so the heads'
 // longest tiles (most key tiles) go first and the short ones fill the tail; 320 threads:
-//   warp 0: TMA (Q tile once; K tiles and V tiles through two rings: a K slot is
-//     free once its S MMA is done, a V slot once its P V MMA is, so the next K
-//     tile's L2 fetch starts a tile earlier than with shared K/V slots),
+//   warp 0: TMA (the Q tile once, then K and V tiles through two rings: a K slot
+//     is free once its S MMA is done, a V slot once its P V MMA is; one thread
+//     polls both rings, so a K fetch never queues behind a V slot),
 //   warp 1: MMA issue (one thread),
 //   warps 2-9 ("P warps", TMEM lane quarter = warp % 4, key half = (warp - 2) / 4):
 //     64 keys of a query row: S -> P and a partial row sum; the epilogue O / D
@@ -121,15 +121,40 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (elect_lane0()) {
             mbar_arrive_expect_tx(&q_full, C::QK_TILE);
             tma_load_3d(tq, &tm_q, 0, qi * kTile, bh, &q_full);
-            for (int j = 0; j < nj; ++j) {
-                const int ks = j % C::KST, ku = j / C::KST;
-                if (ku >= 1 && !sy.wait(&k_empty[ks], ku - 1)) break;
-                mbar_arrive_expect_tx(&k_full[ks], C::QK_TILE);
-                tma_load_3d(tk + ks * C::QK_TILE, &tm_k, 0, j * kTile, bh, &k_full[ks]);
-                const int vs = j % C::VST, vu = j / C::VST;
-                if (vu >= 1 && !sy.wait(&v_empty[vs], vu - 1)) break;
-                mbar_arrive_expect_tx(&v_full[vs], C::V_TILE);
-                tma_load_3d(tv + vs * C::V_TILE, &tm_v, 0, j * kTile, bh, &v_full[vs]);
+            // next K tile jk and next V tile jv, each as soon as its slot is free;
+            // the idle spins between two fetches are bounded like every other wait
+            int jk = 0, jv = 0;
+            uint32_t it = 0;
+            uint64_t t0 = globaltimer();
+            while (jk < nj || jv < nj) {
+                bool any = false;
+                if (jk < nj) {
+                    const int ks = jk % C::KST, ku = jk / C::KST;
+                    if (ku == 0 || mbar_test_wait(&k_empty[ks], (ku - 1) & 1)) {
+                        mbar_arrive_expect_tx(&k_full[ks], C::QK_TILE);
+                        tma_load_3d(tk + ks * C::QK_TILE, &tm_k, 0, jk * kTile, bh, &k_full[ks]);
+                        ++jk;
+                        any = true;
+                    }
+                }
+                if (jv < nj) {
+                    const int vs = jv % C::VST, vu = jv / C::VST;
+                    if (vu == 0 || mbar_test_wait(&v_empty[vs], (vu - 1) & 1)) {
+                        mbar_arrive_expect_tx(&v_full[vs], C::V_TILE);
+                        tma_load_3d(tv + vs * C::V_TILE, &tm_v, 0, jv * kTile, bh, &v_full[vs]);
+                        ++jv;
+                        any = true;
+                    }
+                }
+                if (any) {
+                    it = 0;
+                    t0 = globaltimer();
+                } else if (abort_flag) {
+                    break;
+                } else if (++it >= kSpinLimitIters || globaltimer() - t0 > kSpinLimitNs) {
+                    abort_flag = 1;
+                    break;
+                }
             }
         }
     } else if (warp == 1) {
