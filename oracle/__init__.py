@@ -78,6 +78,12 @@ def _load():
             lib.kata_oracle_forward_rows_map.argtypes = [_D, _D, _D, _I64, ctypes.c_int64, _D,
                                                          i, i, i, i, i, i, dd, dd]
             lib.kata_oracle_recurrent_map.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, dd, dd]
+            lib.kata_oracle_forward_gated.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i]
+            lib.kata_oracle_forward_rows_gated.argtypes = [_D, _D, _D, _D, _I64, ctypes.c_int64,
+                                                           _D, i, i, i, i, i]
+            lib.kata_oracle_recurrent_gated.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i]
+            lib.kata_oracle_prefix_state_gated.argtypes = [_D, _D, _D, _D, _D, i, i, i, i]
+            lib.kata_oracle_decode_step_gated.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i]
             _lib = lib
     return _lib
 
@@ -245,3 +251,80 @@ def recurrent_map(q, k, v, map_name: str, g: int = 1, eps: float = 0.0,
     _load().kata_oracle_recurrent_map(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv,
                                       MAPS[map_name], int(g), float(eps), float(scale))
     return out
+
+
+# ---------------------------------------------------------------------------
+# GatedKATA (the appendix on recurrent variants, "multiplicative scalar state
+# gate"; Sec. 5.2): S_t = gamma_t S_{t-1} + psi(k_t) v_t^T with gamma_t in [0, 1],
+# Z_t gated the same way; readout psi(q)^T S_t / psi(q)^T Z_t (normalize=True) or
+# psi(q)^T S_t (normalize=False, the MQAR appendix's no-denominator form).
+# gamma: [B, H, T] for the forward, [B, H] for one decode step.
+
+
+def _gate(gamma, shape) -> np.ndarray:
+    g = _f64(gamma)
+    if g.shape != tuple(shape):
+        raise ValueError(f"gamma must have shape {tuple(shape)}, got {g.shape}")
+    return g
+
+
+def forward_gated(q, k, v, gamma, normalize: bool = True) -> np.ndarray:
+    """Direct O(T^2) definition: weights prod_{r=s+1}^{t} gamma_r (q_t.k_s)^2."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    g = _gate(gamma, (B, H, T))
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_forward_gated(_p(q), _p(k), _p(v), _p(g), _p(out), B * H, T, d, dv,
+                                      int(bool(normalize)))
+    return out
+
+
+def forward_rows_gated(q, k, v, gamma, rows, normalize: bool = True) -> np.ndarray:
+    """The gated direct definition at flat rows (b*H + h)*T + t."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    g = _gate(gamma, (B, H, T))
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((rows.shape[0], dv), dtype=np.float64)
+    _load().kata_oracle_forward_rows_gated(_p(q), _p(k), _p(v), _p(g), rows.ctypes.data_as(_I64),
+                                           rows.shape[0], _p(out), B * H, T, d, dv,
+                                           int(bool(normalize)))
+    return out
+
+
+def recurrent_gated(q, k, v, gamma, normalize: bool = True) -> np.ndarray:
+    """Self-check form: the gated feature-state recurrence."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, d, dv = _dims(q, v)
+    g = _gate(gamma, (B, H, T))
+    out = np.empty((B, H, T, dv), dtype=np.float64)
+    _load().kata_oracle_recurrent_gated(_p(q), _p(k), _p(v), _p(g), _p(out), B * H, T, d, dv,
+                                        int(bool(normalize)))
+    return out
+
+
+def prefix_state_gated(k, v, gamma):
+    """(S_T, Z_T) after all T tokens under the gated recurrence."""
+    k, v = _f64(k), _f64(v)
+    B, H, T, d = k.shape
+    dv = v.shape[-1]
+    g = _gate(gamma, (B, H, T))
+    n = feature_dim(d)
+    S = np.empty((B, H, n, dv), dtype=np.float64)
+    z = np.empty((B, H, n), dtype=np.float64)
+    _load().kata_oracle_prefix_state_gated(_p(k), _p(v), _p(g), _p(S), _p(z), B * H, T, d, dv)
+    return S, z
+
+
+def decode_step_gated(S, z, q, k, v, gamma, normalize: bool = True):
+    """One gated step: returns (S', z', o) without modifying the inputs."""
+    S = _f64(S).copy()
+    z = _f64(z).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    g = _gate(gamma, (B, H))
+    out = np.empty((B, H, dv), dtype=np.float64)
+    _load().kata_oracle_decode_step_gated(_p(S), _p(z), _p(q), _p(k), _p(v), _p(g), _p(out),
+                                          B * H, d, dv, int(bool(normalize)))
+    return S, z, out

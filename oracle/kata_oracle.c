@@ -481,3 +481,165 @@ void kata_oracle_recurrent_map(const double *q, const double *k, const double *v
         free(A);
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * GatedKATA (the appendix on recurrent variants, "multiplicative scalar state
+ * gate", and Sec. 5.2): a scalar gate gamma_t in [0, 1] inside the recurrence,
+ *   S_t = gamma_t S_{t-1} + psi(k_t) v_t^T,
+ * which unrolls to S_t = sum_{s<=t} (prod_{r=s+1}^{t} gamma_r) psi(k_s) v_s^T:
+ * write s is weighted by the gates of the later tokens only.  Readings (each
+ * listed with its reason in the design notes of the repository):
+ *   - Z_t carries the same gate, Z_t = gamma_t Z_{t-1} + psi(k_t), so the
+ *     readout psi(q_t)^T S_t / psi(q_t)^T Z_t is the convex output gate of
+ *     Prop. 1 over the gated weights (normalize = 1);
+ *   - normalize = 0 gives the no-denominator readout o_t = psi(q_t)^T S_t of the
+ *     MQAR configuration appendix;
+ *   - gamma is given per (head, token) as a value in [0, 1]: gamma [BH][T] for
+ *     the forward, gamma [BH] for one decode step. */
+
+/* The direct definition for one output row: weights a_ts (q_t . k_s)^2 with
+ * a_tt = 1 and a_t,s-1 = a_ts gamma_s (the product over r = s .. t). */
+static void gated_row(const double *q, const double *k, const double *v, const double *gamma,
+                      int t, int d, int dv, int normalize, double *o) {
+    const double *qt = q + (int64_t)t * d;
+    double den = 0.0, a = 1.0;
+    for (int j = 0; j < dv; ++j) o[j] = 0.0;
+    for (int s = t; s >= 0; --s) {
+        const double *ks = k + (int64_t)s * d;
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i) dot += qt[i] * ks[i];
+        const double w = a * dot * dot;
+        den += w;
+        const double *vs = v + (int64_t)s * dv;
+        for (int j = 0; j < dv; ++j) o[j] += w * vs[j];
+        a *= gamma[s];
+    }
+    if (normalize)
+        for (int j = 0; j < dv; ++j) o[j] = den > 0.0 ? o[j] / den : 0.0;
+}
+
+/* Full causal gated forward by the direct O(T^2) definition. */
+void kata_oracle_forward_gated(const double *q, const double *k, const double *v,
+                               const double *gamma, double *out, int BH, int T, int d, int dv,
+                               int normalize) {
+    const int64_t total = (int64_t)BH * T;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(kata_oracle_get_threads())
+    for (int64_t r = 0; r < total; ++r) {
+        const int64_t bh = r / T;
+        const int t = (int)(r % T);
+        gated_row(q + bh * T * d, k + bh * T * d, v + bh * T * dv, gamma + bh * T, t, d, dv,
+                  normalize, out + r * dv);
+    }
+}
+
+/* The same at sampled rows: rows[i] = bh*T + t, out [nrows][dv]. */
+void kata_oracle_forward_rows_gated(const double *q, const double *k, const double *v,
+                                    const double *gamma, const int64_t *rows, int64_t nrows,
+                                    double *out, int BH, int T, int d, int dv, int normalize) {
+    (void)BH;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t bh = rows[i] / T;
+        const int t = (int)(rows[i] % T);
+        gated_row(q + bh * T * d, k + bh * T * d, v + bh * T * dv, gamma + bh * T, t, d, dv,
+                  normalize, out + i * dv);
+    }
+}
+
+/* Self-check form: the gated feature-state recurrence itself,
+ * S_t = gamma_t S_{t-1} + psi(k_t) v_t^T, Z_t = gamma_t Z_{t-1} + psi(k_t),
+ * read out as psi(q_t)^T S_t (/ psi(q_t)^T Z_t when normalize). */
+void kata_oracle_recurrent_gated(const double *q, const double *k, const double *v,
+                                 const double *gamma, double *out, int BH, int T, int d, int dv,
+                                 int normalize) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = calloc((size_t)n * dv, sizeof(double));
+        double *Z = calloc((size_t)n, sizeof(double));
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            const double g = gamma[row];
+            lift_one(k + row * d, d, pk);
+            lift_one(q + row * d, d, pq);
+            const double *vt = v + row * dv;
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)f * dv + j] = g * S[(size_t)f * dv + j] + pk[f] * vt[j];
+                Z[f] = g * Z[f] + pk[f];
+            }
+            double den = 0.0;
+            for (int f = 0; f < n; ++f) den += pq[f] * Z[f];
+            double *o = out + row * dv;
+            for (int j = 0; j < dv; ++j) {
+                double num = 0.0;
+                for (int f = 0; f < n; ++f) num += pq[f] * S[(size_t)f * dv + j];
+                o[j] = normalize ? (den > 0.0 ? num / den : 0.0) : num;
+            }
+        }
+        free(S);
+        free(Z);
+        free(pk);
+        free(pq);
+    }
+}
+
+/* (S_T, Z_T) after T tokens under the gated recurrence.  S [BH][n][dv], z [BH][n]. */
+void kata_oracle_prefix_state_gated(const double *k, const double *v, const double *gamma,
+                                    double *S, double *z, int BH, int T, int d, int dv) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        memset(Sb, 0, sizeof(double) * n * dv);
+        memset(zb, 0, sizeof(double) * n);
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            const double g = gamma[row];
+            lift_one(k + row * d, d, pk);
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j)
+                    Sb[(size_t)f * dv + j] = g * Sb[(size_t)f * dv + j] + pk[f] * v[row * dv + j];
+                zb[f] = g * zb[f] + pk[f];
+            }
+        }
+        free(pk);
+    }
+}
+
+/* One gated decode step, in place: S = gamma S + psi(k) v^T, z = gamma z + psi(k),
+ * then the readout (update, then read).  gamma is [BH]. */
+void kata_oracle_decode_step_gated(double *S, double *z, const double *q, const double *k,
+                                   const double *v, const double *gamma, double *out, int BH,
+                                   int d, int dv, int normalize) {
+    const int n = kata_oracle_feature_dim(d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        const double g = gamma[bh];
+        lift_one(k + (size_t)bh * d, d, pk);
+        lift_one(q + (size_t)bh * d, d, pq);
+        const double *vb = v + (size_t)bh * dv;
+        for (int f = 0; f < n; ++f) {
+            for (int j = 0; j < dv; ++j)
+                Sb[(size_t)f * dv + j] = g * Sb[(size_t)f * dv + j] + pk[f] * vb[j];
+            zb[f] = g * zb[f] + pk[f];
+        }
+        double den = 0.0;
+        for (int f = 0; f < n; ++f) den += pq[f] * zb[f];
+        for (int j = 0; j < dv; ++j) {
+            double num = 0.0;
+            for (int f = 0; f < n; ++f) num += pq[f] * Sb[(size_t)f * dv + j];
+            out[(size_t)bh * dv + j] = normalize ? (den > 0.0 ? num / den : 0.0) : num;
+        }
+        free(pk);
+        free(pq);
+    }
+}
