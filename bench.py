@@ -120,6 +120,14 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         return out_inter + intra, "TFLOP/s", "alu"
     if stage == "simt_scan":
         return 2.0 * 4 * n * (dv + 1) * NC * BH, "GB/s", "hbm"
+    # GatedKATA on CUDA cores: the same contractions (the gate products add O(C)
+    # multiplies per chunk); the gated scan also reads one gate product per chunk
+    if stage == "gated_chunk_state":
+        return state_flops, "TFLOP/s", "alu"
+    if stage == "gated_output":
+        return out_inter + intra, "TFLOP/s", "alu"
+    if stage == "gated_scan":
+        return (2.0 * 4 * n * (dv + 1) + 4) * NC * BH, "GB/s", "hbm"
     if stage.startswith("tc_"):
         nct, G, Lc = tc_plan(w, num_sms)
         seg_tokens = min(T, (G - 1) * Lc * 128) * BH      # tokens in all but the last segments
@@ -263,15 +271,16 @@ class ClockSampler:
 # CPU oracle baseline (rank 0 only)
 
 
-def _oracle_sample(w, q, k, v, seconds: float, rng, fm: FeatureMap = FULL_MAP):
+def _oracle_sample(w, q, k, v, seconds: float, rng, fm: FeatureMap = FULL_MAP, gate=None):
     """Time the oracle on sampled output rows (uniform over heads and positions)
     for about `seconds`; returns (rows, elapsed seconds, threads).  Each row is
-    one head of one token."""
+    one head of one token.  With `gate` ([1, heads, T] fp64) the gated definition."""
     import oracle
     BH = w.B * w.H
     qf = q.reshape(BH, w.T, w.d)
     kf = k.reshape(BH, w.T, w.d)
     vf = v.reshape(BH, w.T, w.dv)
+    gf = gate.reshape(BH, w.T) if gate is not None else None
 
     def run(nrows):
         heads = rng.integers(0, BH, size=nrows)
@@ -279,7 +288,10 @@ def _oracle_sample(w, q, k, v, seconds: float, rng, fm: FeatureMap = FULL_MAP):
         t0 = time.perf_counter()
         for h in np.unique(heads):
             sel = ts[heads == h]
-            if fm.code == 0:
+            if gf is not None:
+                oracle.forward_rows_gated(qf[h][None, None], kf[h][None, None], vf[h][None, None],
+                                          gf[h][None, None], sel)
+            elif fm.code == 0:
                 oracle.forward_rows(qf[h][None, None], kf[h][None, None], vf[h][None, None], sel)
             else:
                 oracle.forward_rows_map(qf[h][None, None], kf[h][None, None], vf[h][None, None],
@@ -316,11 +328,14 @@ def run_reference(args):
     qh = _host_f64(q.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
     kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
     vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
+    gh = None
+    if args.algo == "gated":
+        gh = _host_f64(workloads.make_gate(w).reshape(BH, w.T)[:keep]).reshape(1, keep, w.T)
     rng = np.random.default_rng(0)
     per_step_s = float(os.environ.get("KATA_REF_STEP_SECONDS", "3"))
     times, rows_total = [], 0
     for i in range(args.warmup + args.steps):
-        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, per_step_s, rng, fm)
+        nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, per_step_s, rng, fm, gh)
         if i >= args.warmup:
             times.append(dt)
             rows_total += nrows
@@ -331,11 +346,11 @@ def run_reference(args):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w, fm),
+        "config": dict(_config(w, fm), algorithm=args.algo),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_total} output rows of heads 0..{keep - 1}, positions "
-                                   f"uniform in [0,T), direct O(T^2) fp64 definition; "
-                                   f"tokens = rows / H"},
+                                   f"uniform in [0,T), direct O(T^2) fp64 definition"
+                                   f"{' (gated)' if gh is not None else ''}; tokens = rows / H"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -393,9 +408,15 @@ def run_ours(args):
     fm = FeatureMap(args.map, args.g)
     peaks = _peaks()
     q, k, v = workloads.make_qkv(w, device="cuda")
+    gate = workloads.make_gate(w, device="cuda") if args.algo == "gated" else None
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
     stream = torch.cuda.current_stream()
-    if args.algo == "quadratic":
+    if args.algo == "gated":
+        path = kg.KATA_PATH_SIMT
+
+        def fwd(q_, k_, v_, out_, g_=gate):
+            kg.kata_fwd_chunked_gated(q_, k_, v_, g_, w.C, out=out_)
+    elif args.algo == "quadratic":
         path = kg.KATA_PATH_TC
 
         def fwd(q_, k_, v_, out_):
@@ -494,13 +515,21 @@ def run_ours(args):
         if fm.code == 0 and args.algo == "chunked":   # the C ABI's host-buffer entry point
             def e2e_step():
                 kg.kata_fwd_chunked_host(qh, kh, vh, w.C, out=oh)
-        else:   # pinned copies in, the forward, copy out
+        else:   # pinned copies in (the gates too), the forward, copy out
             qd, kd, vd, od = (torch.empty_like(t) for t in (q, k, v, out))
+            pairs = [(qd, qh), (kd, kh), (vd, vh)]
+            if gate is not None:
+                gh = gate.cpu().pin_memory()
+                gd = torch.empty_like(gate)
+                pairs.append((gd, gh))
 
             def e2e_step():
-                for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
+                for dst, src in pairs:
                     dst.copy_(src, non_blocking=True)
-                fwd(qd, kd, vd, od)
+                if gate is not None:
+                    fwd(qd, kd, vd, od, gd)
+                else:
+                    fwd(qd, kd, vd, od)
                 oh.copy_(od, non_blocking=True)
                 torch.cuda.current_stream().synchronize()
         e2e_step()
@@ -509,8 +538,9 @@ def run_ours(args):
             e2e_step()
         dt = time.perf_counter() - t0
         es = qh.element_size()
+        gate_bytes = gate.numel() * 4 if gate is not None else 0
         e2e = {"value": w.B * w.T * steps_e2e * world / dt, "unit": "tokens/s",
-               "h2d_bytes_per_step": (qh.numel() + kh.numel() + vh.numel()) * es,
+               "h2d_bytes_per_step": (qh.numel() + kh.numel() + vh.numel()) * es + gate_bytes,
                "d2h_bytes_per_step": oh.numel() * es, "steps": steps_e2e}
         del qh, kh, vh, oh
 
@@ -526,13 +556,17 @@ def run_ours(args):
         qh = _host_f64(q.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
         kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
         vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
+        gh64 = None
+        if gate is not None:
+            gh64 = _host_f64(gate.reshape(BH, w.T)[:keep]).reshape(1, keep, w.T)
         nrows, dt, threads = _oracle_sample(sub, qh, kh, vh, args.cpu_seconds,
-                                            np.random.default_rng(1), fm)
+                                            np.random.default_rng(1), fm, gh64)
         # each row is one head; a token of the workload has H heads
         tps = (nrows / w.H) / dt
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{nrows} output rows from heads 0..{keep - 1}, positions uniform in "
-                         f"[0,T), direct O(T^2) fp64 definition, {dt:.1f} s; tokens = rows / H"}
+                         f"[0,T), direct O(T^2) fp64 definition"
+                         f"{' (gated)' if gh64 is not None else ''}, {dt:.1f} s; tokens = rows / H"}
 
     if rank == 0:
         line = {
@@ -590,8 +624,9 @@ def main(argv=None):
     ap.add_argument("--map", default="full", choices=["full", "M", "Sigma"],
                     help="feature map: the full rank-one map or a reduced PSD family")
     ap.add_argument("--g", type=int, default=1, help="blocks of the reduced map (1, 2 or 4)")
-    ap.add_argument("--algo", default="chunked", choices=["chunked", "quadratic"],
-                    help="chunked O(T) form (the default) or the quadratic flash-style form")
+    ap.add_argument("--algo", default="chunked", choices=["chunked", "quadratic", "gated"],
+                    help="chunked O(T) form (the default), the quadratic flash-style form, or "
+                         "GatedKATA (chunked, seeded gates)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -599,8 +634,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.map == "full" and args.g != 1:
         ap.error("--map full takes --g 1")
-    if args.algo == "quadratic" and args.map != "full":
-        ap.error("--algo quadratic runs the full map")
+    if args.algo != "chunked" and args.map != "full":
+        ap.error(f"--algo {args.algo} runs the full map")
     if args.warmup < 3:
         sys.stderr.write("warning: fewer than 3 warm-up steps\n")
     if args.impl == "reference":

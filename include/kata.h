@@ -180,6 +180,34 @@ int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, i
                        int T, int d, int dv, int dtype, kata_stream_t stream);
 
 /*
+ * kata_fwd_chunked_gated -- GatedKATA, the pages' "multiplicative scalar state
+ * gate" variant ([KATA] appendix on recurrent variants; Sec. 5.2): a gate
+ * gamma_t in [0, 1] inside the recurrence,
+ *   S_t = gamma_t S_{t-1} + psi(k_t) v_t^T,  Z_t = gamma_t Z_{t-1} + psi(k_t),
+ * so write s reaches token t with the weight prod_{r=s+1}^{t} gamma_r (q_t . k_s)^2;
+ *   normalize = 1: out_t = psi(q_t)^T S_t / psi(q_t)^T Z_t (the convex readout of
+ *                  Prop. 1 over the gated weights; a zero denominator gives 0);
+ *   normalize = 0: out_t = psi(q_t)^T S_t (the no-denominator readout of the
+ *                  pages' MQAR configuration).
+ * Computed in the chunked form of Eq. 17-20 with the chunk's gate products
+ * folded into the state, the scan and the output (CUDA cores, fp32 FFMA, for
+ * fp32 and bf16 inputs).
+ *
+ *   gamma    [B][H][T] fp32 device, read only, 16-byte aligned; values in [0, 1]
+ *            (not checked on the device: other values give the recurrence's
+ *            arithmetic as written; gamma = 0 resets the state exactly).
+ *   state, z both null, or both set: [B][H][n][dv] and [B][H][n] fp32 device,
+ *            written with the gated state after the last token, in the layout
+ *            kata_decode_step_gated reads.
+ *   normalize 0 or 1 (KATA_ERR_ARG otherwise).
+ * q, k, v, out, B, H, T, d, dv, C, dtype, stream: as kata_fwd_chunked.
+ * Workspace: allocated and freed stream-ordered inside the call.
+ */
+int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const float *gamma,
+                           void *out, float *state, float *z, int B, int H, int T, int d, int dv,
+                           int C, int dtype, int normalize, kata_stream_t stream);
+
+/*
  * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
  * arguments, layouts, paths and results), for callers that cannot allocate
  * device memory where they run it: code whose device memory is owned by a
@@ -249,6 +277,18 @@ int kata_fwd_chunked_host(const void *q, const void *k, const void *v, void *out
 int kata_decode_step(float *state, float *z, const void *q, const void *k, const void *v,
                      void *out, int B, int H, int d, int dv, int dtype,
                      kata_stream_t stream);
+
+/*
+ * kata_decode_step_gated -- one GatedKATA step per (b, h), in place (the
+ * recurrence of kata_fwd_chunked_gated at one token):
+ *   S = gamma S + psi(k) v^T;  z = gamma z + psi(k);
+ *   out = psi(q)^T S / psi(q)^T z (normalize = 1) or psi(q)^T S (normalize = 0).
+ *   gamma [B][H] fp32 device, read only, 16-byte aligned, values in [0, 1].
+ * Other arguments as kata_decode_step.
+ */
+int kata_decode_step_gated(float *state, float *z, const void *q, const void *k, const void *v,
+                           const float *gamma, void *out, int B, int H, int d, int dv,
+                           int dtype, int normalize, kata_stream_t stream);
 
 /*
  * kata_lift -- the feature lift alone (Sec. 3.1 rank-one PSD map, packed as

@@ -44,7 +44,8 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_decode_step", "kata_lift", "kata_trace_begin", "kata_trace_end",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
-            "kata_fwd_path_map", "kata_fwd_quadratic")
+            "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
+            "kata_decode_step_gated")
 
 _lib = None
 
@@ -96,6 +97,11 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_path_map.argtypes = [i, i, i, i, i, i, i, i, i]
         L.kata_fwd_path_map.restype = i
         L.kata_fwd_quadratic.argtypes = [p, p, p, p, i, i, i, i, i, i, vp]
+        L.kata_fwd_quadratic.restype = i
+        L.kata_fwd_chunked_gated.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_chunked_gated.restype = i
+        L.kata_decode_step_gated.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, vp]
+        L.kata_decode_step_gated.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -254,6 +260,59 @@ def kata_fwd_quadratic(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                   B, H, T, d, dv, _dtype_code(q.dtype),
                                   _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_quadratic")
+    return out
+
+
+def kata_fwd_chunked_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           gamma: torch.Tensor, C: int, normalize: bool = True,
+                           out: torch.Tensor | None = None, with_state: bool = False,
+                           stream=None):
+    """GatedKATA forward: S_t = gamma_t S_{t-1} + psi(k_t) v_t^T (Z_t alike),
+    read out as psi(q)^T S / psi(q)^T Z (normalize) or psi(q)^T S.
+    gamma: [B,H,T] float32 in [0, 1] on the same device.  Returns out, or
+    (out, state [B,H,n,dv], z [B,H,n]) with with_state."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (B, H, T):
+        raise TypeError("gamma must be float32 of shape [B, H, T]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    state = z = None
+    if with_state:
+        n = d * (d + 1) // 2
+        state = torch.empty((B, H, n, dv), dtype=torch.float32, device=v.device)
+        z = torch.empty((B, H, n), dtype=torch.float32, device=v.device)
+        _contig(state, z)
+    _contig(q, k, v, gamma, out)
+    rc = lib().kata_fwd_chunked_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(), gamma.data_ptr(),
+                                      out.data_ptr(), state.data_ptr() if with_state else None,
+                                      z.data_ptr() if with_state else None, B, H, T, d, dv,
+                                      int(C), _dtype_code(q.dtype), int(bool(normalize)),
+                                      _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked_gated")
+    return (out, state, z) if with_state else out
+
+
+def kata_decode_step_gated(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor,
+                           k: torch.Tensor, v: torch.Tensor, gamma: torch.Tensor,
+                           normalize: bool = True, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """One GatedKATA step (S = gamma S + psi(k) v^T, z = gamma z + psi(k)) in place;
+    gamma: [B,H] float32."""
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (B, H):
+        raise TypeError("gamma must be float32 of shape [B, H]")
+    if state.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("state and z must be float32")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=v.dtype, device=v.device)
+    _contig(state, z, q, k, v, gamma, out)
+    rc = lib().kata_decode_step_gated(state.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                      v.data_ptr(), gamma.data_ptr(), out.data_ptr(), B, H, d, dv,
+                                      _dtype_code(q.dtype), int(bool(normalize)),
+                                      _stream_handle(stream, q.device))
+    _check(rc, "kata_decode_step_gated")
     return out
 
 

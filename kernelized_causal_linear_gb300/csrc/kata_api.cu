@@ -350,6 +350,82 @@ int kata_decode_step(float *state, float *z, const void *q, const void *k, const
     return KATA_OK;
 }
 
+int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const float *gamma,
+                           void *out, float *state, float *z, int B, int H, int T, int d, int dv,
+                           int C, int dtype, int normalize, kata_stream_t stream) {
+    if (!q || !k || !v || !gamma || !out) return KATA_ERR_ARG;
+    if (!state != !z) return KATA_ERR_ARG;
+    if (normalize != 0 && normalize != 1) return KATA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma))
+        return KATA_ERR_ARG;
+    if (state && (!aligned16(state) || !aligned16(z))) return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    const size_t es = elem_size(dtype), BH = (size_t)B * H, n = (size_t)d * (d + 1) / 2;
+    const size_t nqk = BH * T * d * es, nvo = BH * T * dv * es, ng = BH * T * 4;
+    if (overlap(out, nvo, q, nqk) || overlap(out, nvo, k, nqk) || overlap(out, nvo, v, nvo) ||
+        overlap(out, nvo, gamma, ng))
+        return KATA_ERR_ARG;
+    if (state) {
+        const size_t ns = BH * n * dv * 4, nz = BH * n * 4;
+        const void *ins[5] = {q, k, v, gamma, out};
+        const size_t lens[5] = {nqk, nqk, nvo, ng, nvo};
+        if (overlap(state, ns, z, nz)) return KATA_ERR_ARG;
+        for (int i = 0; i < 5; ++i)
+            if (overlap(state, ns, ins[i], lens[i]) || overlap(z, nz, ins[i], lens[i]))
+                return KATA_ERR_ARG;
+    }
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    cudaGetLastError();
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, kata::gated_workspace_bytes(s), st) != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_ALLOC;
+    }
+    kata::StateOut so;
+    so.state = state;
+    so.z = z;
+    cudaError_t e = kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
+int kata_decode_step_gated(float *state, float *z, const void *q, const void *k, const void *v,
+                           const float *gamma, void *out, int B, int H, int d, int dv,
+                           int dtype, int normalize, kata_stream_t stream) {
+    if (!state || !z || !q || !k || !v || !gamma || !out) return KATA_ERR_ARG;
+    if (normalize != 0 && normalize != 1) return KATA_ERR_ARG;
+    if (!aligned16(state) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+        !aligned16(v) || !aligned16(out) || !aligned16(gamma))
+        return KATA_ERR_ARG;
+    if (B < 1 || H < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
+    if (!valid_d(d) || !valid_dv(dv)) return KATA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > INT32_MAX) return KATA_ERR_UNSUPPORTED;
+    const size_t n = (size_t)d * (d + 1) / 2;
+    const size_t BH = (size_t)B * H;
+    if (overlap(state, BH * n * dv * 4, z, BH * n * 4) ||
+        overlap(out, BH * dv * elem_size(dtype), state, BH * n * dv * 4) ||
+        overlap(gamma, BH * 4, state, BH * n * dv * 4) || overlap(gamma, BH * 4, z, BH * n * 4))
+        return KATA_ERR_ARG;
+    cudaGetLastError();
+    const cudaError_t e = kata::decode_launch(state, z, q, k, v, out, (int)BH, d, dv, dtype,
+                                              reinterpret_cast<cudaStream_t>(stream), gamma,
+                                              normalize);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
 int kata_sync_status(kata_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();

@@ -7,6 +7,11 @@
 // write of S and z), so it is bound by HBM bandwidth: one block per (b, h),
 // 256 threads, 16-byte vector accesses, and the psi(q)^T S reduction folded
 // into the same sweep so S is touched exactly once.
+//
+// The GatedKATA step (the pages' multiplicative scalar state gate) is the same
+// sweep with S = gamma S + psi(k) v^T, z = gamma z + psi(k) (gamma per head; a
+// null gate is gamma = 1, for which the products are exact), read out with or
+// without the denominator.
 #include "kata_internal.cuh"
 
 namespace kata {
@@ -18,7 +23,7 @@ template <typename T, int DV4>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
               const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ out, int d,
-              int n) {
+              int n, const float *__restrict__ gamma, int normalize) {
     extern __shared__ float sm[];
     float *pk = sm;                 // psi(k) [n]
     float *pq = pk + n;             // psi(q) [n]
@@ -30,6 +35,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     const int bh = blockIdx.x;
     const int tid = threadIdx.x;
     constexpr int dv = 4 * DV4;
+    const float g = gamma ? gamma[bh] : 1.f;
     if (tid < d) {
         qs[tid] = to_f(q[(size_t)bh * d + tid]);
         ks[tid] = to_f(k[(size_t)bh * d + tid]);
@@ -48,7 +54,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         const float b = qs[i] * qs[j] * cf;
         pk[f] = a;
         pq[f] = b;
-        const float zn = zb[f] + a;
+        const float zn = fmaf(g, zb[f], a);
         zb[f] = zn;
         den = fmaf(b, zn, den);
     }
@@ -69,10 +75,10 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         for (int u = 0; u < 4; ++u) {
             const float a = pk[f + u * kRowStep];
             const float b = pq[f + u * kRowStep];
-            s[u].x = fmaf(a, vv.x, s[u].x);
-            s[u].y = fmaf(a, vv.y, s[u].y);
-            s[u].z = fmaf(a, vv.z, s[u].z);
-            s[u].w = fmaf(a, vv.w, s[u].w);
+            s[u].x = fmaf(a, vv.x, g * s[u].x);
+            s[u].y = fmaf(a, vv.y, g * s[u].y);
+            s[u].z = fmaf(a, vv.z, g * s[u].z);
+            s[u].w = fmaf(a, vv.w, g * s[u].w);
             Sb[(size_t)(f + u * kRowStep) * DV4 + c4] = s[u];
             acc.x = fmaf(b, s[u].x, acc.x);
             acc.y = fmaf(b, s[u].y, acc.y);
@@ -83,10 +89,10 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     for (; f < n; f += kRowStep) {
         float4 s = Sb[(size_t)f * DV4 + c4];
         const float a = pk[f], b = pq[f];
-        s.x = fmaf(a, vv.x, s.x);
-        s.y = fmaf(a, vv.y, s.y);
-        s.z = fmaf(a, vv.z, s.z);
-        s.w = fmaf(a, vv.w, s.w);
+        s.x = fmaf(a, vv.x, g * s.x);
+        s.y = fmaf(a, vv.y, g * s.y);
+        s.z = fmaf(a, vv.z, g * s.z);
+        s.w = fmaf(a, vv.w, g * s.w);
         Sb[(size_t)f * DV4 + c4] = s;
         acc.x = fmaf(b, s.x, acc.x);
         acc.y = fmaf(b, s.y, acc.y);
@@ -106,28 +112,33 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         const int cq = tid / 4, lane4 = tid % 4;
         float num = 0.f;
         for (int r = 0; r < kRowStep; ++r) num += part[(r * DV4 + cq) * 4 + lane4];
-        out[(size_t)bh * dv + tid] = from_f<T>(dsum > 0.f ? num / dsum : 0.f);
+        out[(size_t)bh * dv + tid] =
+            from_f<T>(normalize ? (dsum > 0.f ? num / dsum : 0.f) : num);
     }
 }
 
 template <typename T>
 cudaError_t decode_t(float *S, float *z, const T *q, const T *k, const T *v, T *out, int BH,
-                     int d, int dv, cudaStream_t stream) {
+                     int d, int dv, cudaStream_t stream, const float *gamma, int normalize) {
     const int n = d * (d + 1) / 2;
     const size_t sm = sizeof(float) * 2 * (size_t)n;
     TraceScope tr("decode", stream);
     switch (dv) {
         case 16:
-            decode_kernel<T, 4><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n);
+            decode_kernel<T, 4><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
+                                                                normalize);
             break;
         case 32:
-            decode_kernel<T, 8><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n);
+            decode_kernel<T, 8><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
+                                                                normalize);
             break;
         case 64:
-            decode_kernel<T, 16><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n);
+            decode_kernel<T, 16><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
+                                                                normalize);
             break;
         case 128:
-            decode_kernel<T, 32><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n);
+            decode_kernel<T, 32><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
+                                                                normalize);
             break;
         default:
             return cudaErrorInvalidValue;
@@ -138,13 +149,14 @@ cudaError_t decode_t(float *S, float *z, const T *q, const T *k, const T *v, T *
 }  // namespace
 
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
-                          void *out, int BH, int d, int dv, int dtype, cudaStream_t stream) {
+                          void *out, int BH, int d, int dv, int dtype, cudaStream_t stream,
+                          const float *gamma, int normalize) {
     if (dtype == 0)
         return decode_t<float>(S, z, (const float *)q, (const float *)k, (const float *)v,
-                               (float *)out, BH, d, dv, stream);
+                               (float *)out, BH, d, dv, stream, gamma, normalize);
     return decode_t<__nv_bfloat16>(S, z, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                                    (const __nv_bfloat16 *)v, (__nv_bfloat16 *)out, BH, d, dv,
-                                   stream);
+                                   stream, gamma, normalize);
 }
 
 }  // namespace kata

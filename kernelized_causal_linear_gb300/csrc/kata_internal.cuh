@@ -99,7 +99,14 @@ cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const c
 
 // ---- decode: kata_decode.cu -----------------------------------------------
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
-                          void *out, int BH, int d, int dv, int dtype, cudaStream_t stream);
+                          void *out, int BH, int d, int dv, int dtype, cudaStream_t stream,
+                          const float *gamma = nullptr, int normalize = 1);
+
+// ---- GatedKATA chunked forward on CUDA cores: kata_gated.cu ----------------
+size_t gated_workspace_bytes(const FwdShape &s);
+cudaError_t gated_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                          const float *gamma, void *out, void *workspace, cudaStream_t stream,
+                          const StateOut &so, int normalize);
 
 // ---- tcgen05 path: kata_tc.cu ---------------------------------------------
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);

@@ -178,3 +178,48 @@ def test_map_forward_rejects_bad_maps(L):
     assert fm(kg.KATA_MAP_SUM, 2, eps=float("nan")) == kg.KATA_ERR_ARG
     assert fm(kg.KATA_MAP_SUM, 4, d=16, T=0) == kg.KATA_ERR_ARG          # shape rules as the forward
     assert L.kata_lift_map(q, o, 4, 16, 1, kg.KATA_MAP_BLOCK, 3, 0.0, 1.0, None) == kg.KATA_ERR_ARG
+
+
+def test_gated_forward_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, g, o, S, z = (FAKE * (i + 1) * 4096 for i in range(7))
+
+    def fw(**kw):
+        a = dict(q=q, k=k, v=v, g=g, out=o, S=0, z=0, B=1, H=1, T=8, d=16, dv=16, C=32,
+                 dtype=1, norm=1)
+        a.update(kw)
+        return L.kata_fwd_chunked_gated(a["q"], a["k"], a["v"], a["g"], a["out"], a["S"] or None,
+                                        a["z"] or None, a["B"], a["H"], a["T"], a["d"], a["dv"],
+                                        a["C"], a["dtype"], a["norm"], None)
+
+    assert fw(g=0) == kg.KATA_ERR_ARG                          # no gate
+    assert fw(q=0) == kg.KATA_ERR_ARG
+    assert fw(g=g + 4) == kg.KATA_ERR_ARG                      # misaligned gate
+    assert fw(norm=2) == kg.KATA_ERR_ARG
+    assert fw(S=S) == kg.KATA_ERR_ARG                          # state without z
+    assert fw(z=z) == kg.KATA_ERR_ARG                          # z without state
+    assert fw(S=S, z=S + 64) == kg.KATA_ERR_ARG                # z inside the state
+    assert fw(S=g, z=z) == kg.KATA_ERR_ARG                     # state over the gate
+    assert fw(out=g) == kg.KATA_ERR_ARG                        # output over the gate
+    assert fw(d=20) == kg.KATA_ERR_UNSUPPORTED
+    assert fw(C=16) == kg.KATA_ERR_UNSUPPORTED
+    assert fw(T=0) == kg.KATA_ERR_ARG
+
+
+def test_gated_decode_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    S, z, q, k, v, g, o = (FAKE * (i + 1) * 256 for i in range(7))
+
+    def dc(**kw):
+        a = dict(S=S, z=z, q=q, k=k, v=v, g=g, out=o, B=1, H=1, d=16, dv=16, dtype=1, norm=1)
+        a.update(kw)
+        return L.kata_decode_step_gated(a["S"], a["z"], a["q"], a["k"], a["v"], a["g"], a["out"],
+                                        a["B"], a["H"], a["d"], a["dv"], a["dtype"], a["norm"],
+                                        None)
+
+    assert dc(g=0) == kg.KATA_ERR_ARG
+    assert dc(g=g + 8) == kg.KATA_ERR_ARG
+    assert dc(norm=-1) == kg.KATA_ERR_ARG
+    assert dc(g=S + 16) == kg.KATA_ERR_ARG                     # gate inside the state
+    assert dc(d=8) == kg.KATA_ERR_UNSUPPORTED
+    assert dc(B=0) == kg.KATA_ERR_ARG

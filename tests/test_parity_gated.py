@@ -1,0 +1,165 @@
+"""GPU parity of GatedKATA (the pages' multiplicative scalar state gate:
+S_t = gamma_t S_{t-1} + psi(k_t) v_t^T, Z_t alike) against the CPU oracle:
+kata_fwd_chunked_gated element by element at sizes the oracle finishes in
+seconds (several chunks and a ragged tail, resets and unit gates at chunk
+edges, both readouts), the exported final state, the gated decode step, and
+sampled rows at the mid-size workload."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import TOL, require_gpu, slice_rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kg():
+    return require_gpu()
+
+
+def _gates(w, edges=True):
+    g = workloads.make_gate(w)
+    if edges:   # exact resets and unit gates, on and next to chunk boundaries
+        T, C = w.T, w.C
+        for t in (0, C - 1, C, 2 * C + 1, T - 1):
+            if t < T:
+                g[..., t] = 0.0
+        for t in (1, C + 1, 2 * C):
+            if t < T:
+                g[..., t] = 1.0
+        g[..., 3::17] = 0.5
+    return g.contiguous()
+
+
+def _check(kg, w, g, normalize):
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize)
+    torch.cuda.synchronize()
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[w.dtype], f"{w.name} normalize={normalize}: {err:.3e}"
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dv,C,dtype", [
+    (16, 16, 32, torch.float32), (32, 64, 64, torch.bfloat16), (64, 64, 64, torch.bfloat16),
+    (32, 128, 128, torch.float32), (16, 32, 32, torch.bfloat16), (64, 16, 128, torch.float32)])
+def test_gated_forward_parity(kg, normalize, d, dv, C, dtype):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=2, H=2, T=3 * C + 7, d=d, dv=dv, C=C,
+                                               dtype=dtype)
+    _check(kg, w, _gates(w), normalize)
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 95])
+def test_gated_forward_ragged(kg, T):
+    w = workloads.WORKLOADS["small_fp32"].scaled(B=1, H=3, T=T)
+    for normalize in (True, False):
+        _check(kg, w, _gates(w, edges=T > 40), normalize)
+
+
+def test_gated_unit_and_zero_gates(kg):
+    """gamma = 1 everywhere is plain KATA; gamma = 0 everywhere keeps only the
+    token's own write (o_t = v_t where (q_t . k_t) != 0)."""
+    w = workloads.WORKLOADS["small_fp32"].scaled(B=1, H=2, T=100)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    one = torch.ones((w.B, w.H, w.T), device="cuda")
+    a = kg.kata_fwd_chunked_gated(q, k, v, one, w.C)
+    torch.cuda.synchronize()
+    ref = oracle.forward(to_f64(q), to_f64(k), to_f64(v))
+    assert slice_rel_err(to_f64(a), ref) <= TOL[torch.float32]
+    zero = torch.zeros_like(one)
+    b = kg.kata_fwd_chunked_gated(q, k, v, zero, w.C)
+    torch.cuda.synchronize()
+    assert slice_rel_err(to_f64(b), to_f64(v)) <= TOL[torch.float32]
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dv,C,dtype", [(16, 16, 32, torch.float32),
+                                          (32, 64, 64, torch.bfloat16),
+                                          (64, 32, 64, torch.float32)])
+def test_gated_state_export_and_decode(kg, normalize, d, dv, C, dtype):
+    """The state after the last token equals the oracle's gated recurrence, and a
+    gated decode step from it continues the forward."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=2, H=2, T=2 * C + 5, d=d, dv=dv, C=C,
+                                               dtype=dtype)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    T = w.T - 1   # the forward covers tokens 0 .. T-1; the decode step takes token T
+    sl = (slice(None), slice(None), slice(0, T))
+    out, S, z = kg.kata_fwd_chunked_gated(q[sl].contiguous().cuda(), k[sl].contiguous().cuda(),
+                                          v[sl].contiguous().cuda(), g[sl].contiguous().cuda(),
+                                          C, normalize, with_state=True)
+    torch.cuda.synchronize()
+    S_ref, z_ref = oracle.prefix_state_gated(to_f64(k[sl]), to_f64(v[sl]), to_f64(g[sl]))
+    assert slice_rel_err(to_f64(S), S_ref) <= TOL[torch.float32]
+    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= TOL[torch.float32]
+    o = kg.kata_decode_step_gated(S, z, q[..., T, :].contiguous().cuda(),
+                                  k[..., T, :].contiguous().cuda(),
+                                  v[..., T, :].contiguous().cuda(),
+                                  g[..., T].contiguous().cuda(), normalize)
+    torch.cuda.synchronize()
+    full = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(o)[:, :, None, :], full[:, :, T:T + 1, :])
+    assert err <= TOL[dtype], f"{err:.3e}"
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gated_decode_parity(kg, normalize, dtype):
+    w = workloads.DECODE.scaled(B=4, H=4, dtype=dtype)
+    kp, vp = workloads.make_decode_prefix(w, length=12)
+    gp = torch.sigmoid(torch.randn(w.B, w.H, 12, generator=torch.Generator().manual_seed(5)) + 2)
+    S0, z0 = oracle.prefix_state_gated(to_f64(kp), to_f64(vp), to_f64(gp))
+    q, k, v = workloads.make_decode_inputs(w)
+    g = workloads.make_decode_gate(w)
+    S = torch.from_numpy(S0).float().cuda()
+    z = torch.from_numpy(z0).float().cuda()
+    o = kg.kata_decode_step_gated(S, z, q.cuda(), k.cuda(), v.cuda(), g.cuda(), normalize)
+    torch.cuda.synchronize()
+    S1, z1, o_ref = oracle.decode_step_gated(S0, z0, to_f64(q), to_f64(k), to_f64(v), to_f64(g),
+                                             normalize)
+    assert slice_rel_err(to_f64(o)[:, :, None, :], o_ref[:, :, None, :]) <= TOL[dtype]
+    assert slice_rel_err(to_f64(S), S1) <= 1e-5
+    assert slice_rel_err(to_f64(z)[..., None], z1[..., None]) <= 1e-5
+
+
+def test_plain_decode_unchanged_by_a_unit_gate(kg):
+    w = workloads.DECODE.scaled(B=2, H=3)
+    q, k, v = (t.cuda() for t in workloads.make_decode_inputs(w))
+    S, z = (t.cuda() for t in workloads.make_decode_state_fill(w))
+    S2, z2 = S.clone(), z.clone()
+    a = kg.kata_decode_step(S, z, q, k, v)
+    b = kg.kata_decode_step_gated(S2, z2, q, k, v, torch.ones((w.B, w.H), device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(S, S2) and torch.equal(z, z2)
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_gated_full_size_sampled_rows(kg, normalize):
+    """The mid-size workload (B=4, H=8, T=4096, d=32, dv=64, C=64, bf16) with its
+    seeded gates, sampled rows against the oracle."""
+    w = workloads.WORKLOADS["mid_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    g = workloads.make_gate(w, device="cuda")
+    out = kg.kata_fwd_chunked_gated(q, k, v, g, w.C, normalize)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    BH = w.B * w.H
+    rng = np.random.default_rng(77)
+    worst = 0.0
+    qf, kf, vf, gf = to_f64(q), to_f64(k), to_f64(v), to_f64(g)
+    for h in sorted(set([0, BH - 1] + rng.integers(0, BH, size=2).tolist())):
+        b, hh = divmod(h, w.H)
+        ts = np.array(sorted(set([0, 1, w.C - 1, w.C, w.T // 2, w.T - 1] +
+                                 rng.integers(0, w.T, size=10).tolist())), dtype=np.int64)
+        ref = oracle.forward_rows_gated(qf[b:b + 1, hh:hh + 1], kf[b:b + 1, hh:hh + 1],
+                                        vf[b:b + 1, hh:hh + 1], gf[b:b + 1, hh:hh + 1], ts,
+                                        normalize)
+        got = to_f64(out[b, hh])[ts]
+        worst = max(worst, slice_rel_err(got, ref))
+    assert worst <= TOL[w.dtype], f"{worst:.3e}"

@@ -24,6 +24,11 @@ dictionary.
 
 Seeds: tensor i of workload j (j in table order, 0..5) comes from a
 torch.Generator seeded with 1000*j + i on the device the tensor is made on.
+
+GatedKATA gates (the pages parameterise log gamma_t as the log-sigmoid of a
+per-token projection): gamma = sigmoid(x), x ~ N(4, 1) per (b, h, t) (seed
+1000*j + 8; per (b, h) for one decode step, seed 1000*j + 9), so most gates lie
+in 0.95 .. 0.995 and writes fade over some tens of tokens.
 """
 from __future__ import annotations
 
@@ -144,3 +149,15 @@ def make_decode_state_fill(w: Workload = DECODE, device="cpu"):
     S = _randn((w.B, w.H, w.n, w.dv), device, base + 6)
     z = _randn((w.B, w.H, w.n), device, base + 7).abs_() + 1.0
     return S.contiguous(), z.contiguous()
+
+
+def make_gate(w: Workload, device="cpu"):
+    """GatedKATA gates gamma [B,H,T] float32 in (0, 1): sigmoid of N(4, 1)."""
+    x = _randn((w.B, w.H, w.T), device, 1000 * w.index + 8) + 4.0
+    return torch.sigmoid(x).contiguous()
+
+
+def make_decode_gate(w: Workload = DECODE, device="cpu"):
+    """Gates for one decode step, gamma [B,H] float32: sigmoid of N(4, 1)."""
+    x = _randn((w.B, w.H), device, 1000 * w.index + 9) + 4.0
+    return torch.sigmoid(x).contiguous()
