@@ -139,7 +139,10 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         if stage == "tc_segment_scan":
             rec = 4.0 * (5 * 128 * dv + d * d)
             return 2.0 * rec * G * BH, "GB/s", "hbm"
-    if stage == "tc_quadratic":
+    if stage == "tc_gate_prep":
+        # reads k and the gates, writes the scaled keys and the cumulative log2 gates
+        return float(BH * T) * (2 * d * 2 + 2 * 4), "GB/s", "hbm"
+    if stage in ("tc_quadratic", "tc_quadratic_gated"):
         # every causal (t, s <= t) pair of the head: (q.k)^2 and P [V|1]
         return 2.0 * (d + dv + 1) * _intra_pairs(T, T) * BH, "TFLOP/s", "tensor"
     if stage == "tc_sub_finalize":
@@ -160,7 +163,7 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
     causal intra-chunk term 2(d'+dv+1) per (t, s<=t) pair inside chunks (d' the
     weight's multiply-adds: d, or g d for Sigma_g)."""
     BH, T, d, dv, C, n = w.B * w.H, w.T, w.d, w.dv, w.C, fm.n(w.d)
-    if algo == "quadratic":   # the O(T^2) form: every causal pair
+    if algo in ("quadratic", "gated_quadratic"):   # the O(T^2) form: every causal pair
         return 2.0 * (d + dv + 1) * _intra_pairs(T, T) * BH
     return 4.0 * n * (dv + 1) * T * BH + 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, C) * BH
 
@@ -329,7 +332,7 @@ def run_reference(args):
     kh = _host_f64(k.reshape(BH, w.T, w.d)[:keep]).reshape(1, keep, w.T, w.d)
     vh = _host_f64(v.reshape(BH, w.T, w.dv)[:keep]).reshape(1, keep, w.T, w.dv)
     gh = None
-    if args.algo == "gated":
+    if args.algo.startswith("gated"):
         gh = _host_f64(workloads.make_gate(w).reshape(BH, w.T)[:keep]).reshape(1, keep, w.T)
     rng = np.random.default_rng(0)
     per_step_s = float(os.environ.get("KATA_REF_STEP_SECONDS", "3"))
@@ -408,10 +411,15 @@ def run_ours(args):
     fm = FeatureMap(args.map, args.g)
     peaks = _peaks()
     q, k, v = workloads.make_qkv(w, device="cuda")
-    gate = workloads.make_gate(w, device="cuda") if args.algo == "gated" else None
+    gate = workloads.make_gate(w, device="cuda") if args.algo.startswith("gated") else None
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
     stream = torch.cuda.current_stream()
-    if args.algo == "gated":
+    if args.algo == "gated_quadratic":
+        path = kg.KATA_PATH_TC
+
+        def fwd(q_, k_, v_, out_, g_=gate):
+            kg.kata_fwd_quadratic_gated(q_, k_, v_, g_, out=out_)
+    elif args.algo == "gated":
         path = kg.KATA_PATH_SIMT
 
         def fwd(q_, k_, v_, out_, g_=gate):
@@ -624,9 +632,11 @@ def main(argv=None):
     ap.add_argument("--map", default="full", choices=["full", "M", "Sigma"],
                     help="feature map: the full rank-one map or a reduced PSD family")
     ap.add_argument("--g", type=int, default=1, help="blocks of the reduced map (1, 2 or 4)")
-    ap.add_argument("--algo", default="chunked", choices=["chunked", "quadratic", "gated"],
-                    help="chunked O(T) form (the default), the quadratic flash-style form, or "
-                         "GatedKATA (chunked, seeded gates)")
+    ap.add_argument("--algo", default="chunked",
+                    choices=["chunked", "quadratic", "gated", "gated_quadratic"],
+                    help="chunked O(T) form (the default), the quadratic flash-style form, "
+                         "GatedKATA chunked (CUDA cores) or GatedKATA quadratic (tensor cores); "
+                         "the gated forms draw seeded gates")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

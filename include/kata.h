@@ -180,6 +180,27 @@ int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, i
                        int T, int d, int dv, int dtype, kata_stream_t stream);
 
 /*
+ * kata_fwd_quadratic_gated -- GatedKATA (see kata_fwd_chunked_gated for the
+ * recurrence and the two readouts) in the quadratic form on the tensor cores:
+ * every causal pair weighted by prod_{r=s+1}^{t} gamma_r (q_t . k_s)^2, tile by
+ * tile with no state.  The gate products are folded into the keys of the tiles
+ * below the diagonal (K'_s = sqrt(c_s) k_s, c_s <= 1 the gates after s to the
+ * end of its 128-token tile), a per-row and a per-tile factor, and on the
+ * diagonal tile into 2^(l_t - l_s) from the tile-local cumulative log2 of the
+ * gates (a gate below 2^-126 counts as 2^-126 there: a zero gate leaves a
+ * weight of at most 2^-126 on the writes before it within the tile).
+ *   gamma [B][H][T] fp32 device, 16-byte aligned, values in [0, 1].
+ *   normalize 0 or 1 as kata_fwd_chunked_gated.
+ * Supported shapes, rounding and other arguments as kata_fwd_quadratic.
+ * Workspace (scaled keys, cumulative log2 gates, tile gate products;
+ * B H T (2 d + 4) bytes and a little more) is allocated and freed
+ * stream-ordered inside the call.
+ */
+int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const float *gamma,
+                             void *out, int B, int H, int T, int d, int dv, int dtype,
+                             int normalize, kata_stream_t stream);
+
+/*
  * kata_fwd_chunked_gated -- GatedKATA, the pages' "multiplicative scalar state
  * gate" variant ([KATA] appendix on recurrent variants; Sec. 5.2): a gate
  * gamma_t in [0, 1] inside the recurrence,

@@ -45,7 +45,7 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
-            "kata_decode_step_gated")
+            "kata_decode_step_gated", "kata_fwd_quadratic_gated")
 
 _lib = None
 
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_chunked_gated.restype = i
         L.kata_decode_step_gated.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, vp]
         L.kata_decode_step_gated.restype = i
+        L.kata_fwd_quadratic_gated.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_quadratic_gated.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -291,6 +293,26 @@ def kata_fwd_chunked_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                       _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_chunked_gated")
     return (out, state, z) if with_state else out
+
+
+def kata_fwd_quadratic_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                             gamma: torch.Tensor, normalize: bool = True,
+                             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """GatedKATA in the quadratic form on the tensor cores (bf16, d in {32, 64},
+    dv = 64): weights prod_{r=s+1}^{t} gamma_r (q_t.k_s)^2; gamma [B,H,T] float32."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (B, H, T):
+        raise TypeError("gamma must be float32 of shape [B, H, T]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, gamma, out)
+    rc = lib().kata_fwd_quadratic_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        gamma.data_ptr(), out.data_ptr(), B, H, T, d, dv,
+                                        _dtype_code(q.dtype), int(bool(normalize)),
+                                        _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_quadratic_gated")
+    return out
 
 
 def kata_decode_step_gated(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor,

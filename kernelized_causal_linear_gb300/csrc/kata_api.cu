@@ -266,6 +266,42 @@ int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, i
     return KATA_OK;
 }
 
+int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const float *gamma,
+                             void *out, int B, int H, int T, int d, int dv, int dtype,
+                             int normalize, kata_stream_t stream) {
+    if (!q || !k || !v || !gamma || !out) return KATA_ERR_ARG;
+    if (normalize != 0 && normalize != 1) return KATA_ERR_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma))
+        return KATA_ERR_ARG;
+    int rc = check_fwd_shape(B, H, T, d, dv, 64, dtype);
+    if (rc) return rc;
+    const size_t es = elem_size(dtype);
+    const size_t nqk = (size_t)B * H * T * d * es, nvo = (size_t)B * H * T * dv * es;
+    const size_t ng = (size_t)B * H * T * 4;
+    if (overlap(out, nvo, q, nqk) || overlap(out, nvo, k, nqk) || overlap(out, nvo, v, nvo) ||
+        overlap(out, nvo, gamma, ng))
+        return KATA_ERR_ARG;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    const FwdShape s{B, H, T, d, dv, 64, dtype};
+    if (!kata::quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
+    cudaGetLastError();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, kata::quad_gated_workspace_bytes(s), st) != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_ALLOC;
+    }
+    cudaError_t e = kata::quad_forward(s, q, k, v, out, st, gamma, normalize, ws);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
 int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *out, float *state,
                            float *z, int B, int H, int T, int d, int dv, int C, int dtype,
                            kata_stream_t stream) {

@@ -131,8 +131,12 @@ int tc64_take_error();
 
 // ---- quadratic (flash-style) forward: kata_quad.cu ------------------------
 bool quad_supported(const FwdShape &s, int cc_major, int cc_minor);
+// gamma non-null: the GatedKATA weights (gamma [BH][T]; ws of
+// quad_gated_workspace_bytes; normalize 0 drops the denominator).
 cudaError_t quad_forward(const FwdShape &s, const void *q, const void *k, const void *v,
-                         void *out, cudaStream_t stream);
+                         void *out, cudaStream_t stream, const float *gamma = nullptr,
+                         int normalize = 1, void *ws = nullptr);
+size_t quad_gated_workspace_bytes(const FwdShape &s);
 int quad_take_error();
 
 }  // namespace kata

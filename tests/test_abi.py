@@ -223,3 +223,22 @@ def test_gated_decode_rejects_bad_arguments(L):
     assert dc(g=S + 16) == kg.KATA_ERR_ARG                     # gate inside the state
     assert dc(d=8) == kg.KATA_ERR_UNSUPPORTED
     assert dc(B=0) == kg.KATA_ERR_ARG
+
+
+def test_gated_quadratic_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, g, o = (FAKE * (i + 1) * 4096 for i in range(5))
+
+    def fq(**kw):
+        a = dict(q=q, k=k, v=v, g=g, out=o, B=1, H=1, T=8, d=32, dv=64, dtype=1, norm=1)
+        a.update(kw)
+        return L.kata_fwd_quadratic_gated(a["q"], a["k"], a["v"], a["g"], a["out"], a["B"],
+                                          a["H"], a["T"], a["d"], a["dv"], a["dtype"], a["norm"],
+                                          None)
+
+    assert fq(g=0) == kg.KATA_ERR_ARG
+    assert fq(g=g + 4) == kg.KATA_ERR_ARG
+    assert fq(norm=3) == kg.KATA_ERR_ARG
+    assert fq(out=g) == kg.KATA_ERR_ARG                        # output over the gate
+    assert fq(T=0) == kg.KATA_ERR_ARG
+    assert fq(d=24) == kg.KATA_ERR_UNSUPPORTED

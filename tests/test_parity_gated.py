@@ -163,3 +163,68 @@ def test_gated_full_size_sampled_rows(kg, normalize):
         got = to_f64(out[b, hh])[ts]
         worst = max(worst, slice_rel_err(got, ref))
     assert worst <= TOL[w.dtype], f"{worst:.3e}"
+
+
+# ---- GatedKATA in the quadratic form on the tensor cores (bf16, d in {32, 64}, dv = 64)
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,T", [(32, 129), (32, 300), (64, 257), (64, 1000)])
+def test_gated_quadratic_parity(kg, normalize, d, T):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=2, T=T, d=d, C=128)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out = kg.kata_fwd_quadratic_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[torch.bfloat16], f"d={d} T={T} normalize={normalize}: {err:.3e}"
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129])
+def test_gated_quadratic_ragged(kg, T):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=T, C=128)
+    q, k, v = workloads.make_qkv(w)
+    g = workloads.make_gate(w)
+    g[..., T // 2] = 0.0
+    out = kg.kata_fwd_quadratic_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(out), ref) <= TOL[torch.bfloat16]
+
+
+def test_gated_quadratic_unit_gate_is_the_plain_kernel(kg):
+    """gamma = 1: scaled keys equal the keys, every factor is 1, so the gated
+    kernel produces the plain quadratic kernel's output bit for bit."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=3, T=700)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    one = torch.ones((w.B, w.H, w.T), device="cuda")
+    a = kg.kata_fwd_quadratic_gated(q, k, v, one)
+    b = kg.kata_fwd_quadratic(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_gated_quadratic_full_size_sampled_rows(kg, normalize):
+    """The LM-layer workload (B=8, H=16, T=2048, d=64, dv=64, bf16) with its seeded
+    gates, sampled rows against the oracle."""
+    w = workloads.WORKLOADS["lm_layer_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    g = workloads.make_gate(w, device="cuda")
+    out = kg.kata_fwd_quadratic_gated(q, k, v, g, normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    assert torch.isfinite(out).all()
+    BH = w.B * w.H
+    rng = np.random.default_rng(78)
+    worst = 0.0
+    qf, kf, vf, gf = to_f64(q), to_f64(k), to_f64(v), to_f64(g)
+    for h in sorted(set([0, BH - 1] + rng.integers(0, BH, size=2).tolist())):
+        b, hh = divmod(h, w.H)
+        ts = np.array(sorted(set([0, 1, 127, 128, w.T // 2, w.T - 1] +
+                                 rng.integers(0, w.T, size=10).tolist())), dtype=np.int64)
+        ref = oracle.forward_rows_gated(qf[b:b + 1, hh:hh + 1], kf[b:b + 1, hh:hh + 1],
+                                        vf[b:b + 1, hh:hh + 1], gf[b:b + 1, hh:hh + 1], ts,
+                                        normalize)
+        worst = max(worst, slice_rel_err(to_f64(out[b, hh])[ts], ref))
+    assert worst <= TOL[w.dtype], f"{worst:.3e}"
