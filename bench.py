@@ -168,11 +168,24 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
     return 4.0 * n * (dv + 1) * T * BH + 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, C) * BH
 
 
-def _source_digest() -> str:
+# the translation unit of each traced stage's kernel (its launch configuration
+# lives there too); every stage also depends on all the shared headers
+_STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
+                 ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
+                 ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
+                 ("gated", "kata_gated.cu"), ("decode", "kata_decode.cu"))
+
+
+def _source_digest(stage: str | None = None) -> str:
+    """Digest of the CUDA sources a stage's kernel is built from: its own .cu and
+    every .cuh header (all of csrc without a stage)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kernelized_causal_linear_gb300", "csrc")
+    own = None
+    if stage is not None:
+        own = next((f for prefix, f in _STAGE_SOURCE if stage.startswith(prefix)), None)
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith(".cuh") or (name.endswith(".cu") and own in (None, name)):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
@@ -181,11 +194,11 @@ def _source_digest() -> str:
 
 def _ncu_traffic(kernel_stage: str, workload: str):
     """DRAM bytes per launch for a stage from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+    was taken on the current sources of that stage's kernel; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    digest = _source_digest()
+    digest = _source_digest(kernel_stage)
     with open(p) as f:
         for line in f:
             parts = line.split()
