@@ -9,9 +9,9 @@
 // into the same sweep so S is touched exactly once.
 //
 // The GatedKATA step (the pages' multiplicative scalar state gate) is the same
-// sweep with S = gamma S + psi(k) v^T, z = gamma z + psi(k) (gamma per head; a
-// null gate is gamma = 1, for which the products are exact), read out with or
-// without the denominator.
+// sweep with S = gamma S + psi(k) v^T, z = gamma z + psi(k) (gamma per head), read
+// out with or without the denominator: a compile-time variant, so the plain step
+// carries no gate multiply.
 #include "kata_internal.cuh"
 
 namespace kata {
@@ -19,7 +19,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <typename T, int DV4>
+template <typename T, int DV4, bool kGated>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
               const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ out, int d,
@@ -35,7 +35,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     const int bh = blockIdx.x;
     const int tid = threadIdx.x;
     constexpr int dv = 4 * DV4;
-    const float g = gamma ? gamma[bh] : 1.f;
+    const float g = kGated ? gamma[bh] : 1.f;
     if (tid < d) {
         qs[tid] = to_f(q[(size_t)bh * d + tid]);
         ks[tid] = to_f(k[(size_t)bh * d + tid]);
@@ -54,7 +54,7 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         const float b = qs[i] * qs[j] * cf;
         pk[f] = a;
         pq[f] = b;
-        const float zn = fmaf(g, zb[f], a);
+        const float zn = kGated ? fmaf(g, zb[f], a) : zb[f] + a;
         zb[f] = zn;
         den = fmaf(b, zn, den);
     }
@@ -75,10 +75,10 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         for (int u = 0; u < 4; ++u) {
             const float a = pk[f + u * kRowStep];
             const float b = pq[f + u * kRowStep];
-            s[u].x = fmaf(a, vv.x, g * s[u].x);
-            s[u].y = fmaf(a, vv.y, g * s[u].y);
-            s[u].z = fmaf(a, vv.z, g * s[u].z);
-            s[u].w = fmaf(a, vv.w, g * s[u].w);
+            s[u].x = fmaf(a, vv.x, kGated ? g * s[u].x : s[u].x);
+            s[u].y = fmaf(a, vv.y, kGated ? g * s[u].y : s[u].y);
+            s[u].z = fmaf(a, vv.z, kGated ? g * s[u].z : s[u].z);
+            s[u].w = fmaf(a, vv.w, kGated ? g * s[u].w : s[u].w);
             Sb[(size_t)(f + u * kRowStep) * DV4 + c4] = s[u];
             acc.x = fmaf(b, s[u].x, acc.x);
             acc.y = fmaf(b, s[u].y, acc.y);
@@ -89,10 +89,10 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     for (; f < n; f += kRowStep) {
         float4 s = Sb[(size_t)f * DV4 + c4];
         const float a = pk[f], b = pq[f];
-        s.x = fmaf(a, vv.x, g * s.x);
-        s.y = fmaf(a, vv.y, g * s.y);
-        s.z = fmaf(a, vv.z, g * s.z);
-        s.w = fmaf(a, vv.w, g * s.w);
+        s.x = fmaf(a, vv.x, kGated ? g * s.x : s.x);
+        s.y = fmaf(a, vv.y, kGated ? g * s.y : s.y);
+        s.z = fmaf(a, vv.z, kGated ? g * s.z : s.z);
+        s.w = fmaf(a, vv.w, kGated ? g * s.w : s.w);
         Sb[(size_t)f * DV4 + c4] = s;
         acc.x = fmaf(b, s.x, acc.x);
         acc.y = fmaf(b, s.y, acc.y);
@@ -113,8 +113,19 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
         float num = 0.f;
         for (int r = 0; r < kRowStep; ++r) num += part[(r * DV4 + cq) * 4 + lane4];
         out[(size_t)bh * dv + tid] =
-            from_f<T>(normalize ? (dsum > 0.f ? num / dsum : 0.f) : num);
+            from_f<T>((!kGated || normalize) ? (dsum > 0.f ? num / dsum : 0.f) : num);
     }
+}
+
+template <typename T, int DV4>
+void decode_go(float *S, float *z, const T *q, const T *k, const T *v, T *out, int BH, int d,
+               int n, size_t sm, cudaStream_t stream, const float *gamma, int normalize) {
+    if (gamma)
+        decode_kernel<T, DV4, true><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
+                                                                 normalize);
+    else
+        decode_kernel<T, DV4, false><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n,
+                                                                  nullptr, 1);
 }
 
 template <typename T>
@@ -122,26 +133,13 @@ cudaError_t decode_t(float *S, float *z, const T *q, const T *k, const T *v, T *
                      int d, int dv, cudaStream_t stream, const float *gamma, int normalize) {
     const int n = d * (d + 1) / 2;
     const size_t sm = sizeof(float) * 2 * (size_t)n;
-    TraceScope tr("decode", stream);
+    TraceScope tr(gamma ? "decode_gated" : "decode", stream);
     switch (dv) {
-        case 16:
-            decode_kernel<T, 4><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
-                                                                normalize);
-            break;
-        case 32:
-            decode_kernel<T, 8><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
-                                                                normalize);
-            break;
-        case 64:
-            decode_kernel<T, 16><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
-                                                                normalize);
-            break;
-        case 128:
-            decode_kernel<T, 32><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
-                                                                normalize);
-            break;
-        default:
-            return cudaErrorInvalidValue;
+        case 16: decode_go<T, 4>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
+        case 32: decode_go<T, 8>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
+        case 64: decode_go<T, 16>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
+        case 128: decode_go<T, 32>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
+        default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
