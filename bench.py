@@ -329,7 +329,7 @@ def _host_f64(t):
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    rank = rank_env()[0]
     if rank != 0:
         return 0
     import oracle
@@ -400,10 +400,34 @@ def _dtype_name(w):
     return "bf16" if w.dtype == torch.bfloat16 else "f32"
 
 
+# ----------------------------------------------------------------------------
+# one process per GPU (replicas): rank layout and the whole-job aggregate
+
+
+def rank_env():
+    """(rank, world size, local rank) from the launcher's environment (torchrun
+    sets RANK / WORLD_SIZE / LOCAL_RANK; a plain run is rank 0 of 1)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(elapsed_ms: float, dist=None, device="cuda") -> float:
+    """The slowest rank's timed region (every rank gets it); no-op on one rank."""
+    if dist is None:
+        return elapsed_ms
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job tokens/s: every replica's tokens over the slowest rank's time
+    (weak scaling: the per-GPU work stays fixed as ranks are added)."""
+    return tokens_per_rank * world / (elapsed_ms / 1e3)
+
+
 def run_ours(args):
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     if world != args.gpus:
         if rank == 0:
             sys.stderr.write(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}\n")
@@ -490,12 +514,8 @@ def run_ours(args):
         elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     else:
         elapsed_ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    tokens = w.B * w.T * args.steps * world
-    value = tokens / (elapsed_ms / 1e3)
+    elapsed_ms = max_over_ranks(elapsed_ms, dist)
+    value = job_throughput(w.B * w.T * args.steps, world, elapsed_ms)
 
     # dominant kernel roofline
     launches = sum(n for n, _ in stages.values())
@@ -554,10 +574,12 @@ def run_ours(args):
                 oh.copy_(od, non_blocking=True)
                 torch.cuda.current_stream().synchronize()
         e2e_step()
+        if dist is not None:
+            dist.barrier()
         t0 = time.perf_counter()
         for _ in range(steps_e2e):
             e2e_step()
-        dt = time.perf_counter() - t0
+        dt = max_over_ranks((time.perf_counter() - t0) * 1e3, dist) / 1e3
         es = qh.element_size()
         gate_bytes = gate.numel() * 4 if gate is not None else 0
         e2e = {"value": w.B * w.T * steps_e2e * world / dt, "unit": "tokens/s",
