@@ -142,7 +142,7 @@ template <int D, bool kGated>
 __global__ void __launch_bounds__(320, 2)
 quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kp,
-            bf16 *__restrict__ out, int T, int NT, GateArgs ga) {
+            const __grid_constant__ CUtensorMap tm_o, int T, int NT, GateArgs ga) {
     using C = QuadCfg<D>;
     constexpr int DV = 64;
     constexpr int kPWarps = 8;
@@ -385,8 +385,10 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             __syncwarp();
             if (elect_lane0()) mbar_arrive(&p_full);
         }
-        // epilogue: O = N / D (a zero denominator gives a zero row); every P warp
-        // reaches the named barrier once, also after a failed wait
+        // epilogue: O = N / D (a zero denominator gives a zero row), staged
+        // 128B-swizzled in V slot 0 (every P V MMA is done by then) and written by
+        // one TMA store, which also clips the rows past T; every P warp reaches the
+        // named barriers, also after a failed wait
         dpart[h][r] = dsum;
         asm volatile("bar.sync 1, %0;" ::"r"(kPWarps * 32) : "memory");
         if (ok && __all_sync(0xffffffffu, sy.wait(&o_done, 0))) {
@@ -395,17 +397,23 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const float inv = (kGated && !ga.normalize) ? 1.f : den > 0.f ? 1.f / den : 0.f;
             uint32_t v[32];
             tmem_ld32(tO + lsel + 32 * h, v);
-            const int t = qi * kTile + r;
-            if (t < T) {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)bh * T + t) * DV + 32 * h);
+            const uint32_t row = smem_u32(tv) + (uint32_t)r * 128u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dst[c] = make_uint4(
-                        pack_bf16(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv),
-                        pack_bf16(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv),
-                        pack_bf16(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv),
-                        pack_bf16(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv));
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t chunk = (uint32_t)(4 * h + c) ^ (uint32_t)(r & 7);
+                st_shared_v4(row + (chunk << 4),
+                             pack_bf16(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv),
+                             pack_bf16(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv),
+                             pack_bf16(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv),
+                             pack_bf16(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv));
             }
+            fence_proxy_async_smem();
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kPWarps * 32) : "memory");
+        if (warp == 2 && lane == 0 && !abort_flag) {
+            tma_store_3d(&tm_o, 0, qi * kTile, bh, tv);
+            bulk_commit();
+            bulk_wait_read_all();
         }
     }
     tc_fence_before();
@@ -418,9 +426,9 @@ template <int D>
 cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
                         cudaStream_t stream, const float *gamma, int normalize, void *ws) {
     using C = QuadCfg<D>;
-    CUtensorMap mq, mk, mv, mkp;
+    CUtensorMap mq, mk, mv, mkp, mo;
     if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
-        !make_map(mv, v, s.dv, s.T, s.BH()))
+        !make_map(mv, v, s.dv, s.T, s.BH()) || !make_map(mo, out, s.dv, s.T, s.BH()))
         return cudaErrorInvalidValue;
     const int NT = (s.T + kTile - 1) / kTile;
     if (!gamma) {
@@ -428,7 +436,7 @@ cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const v
                              C::SMEM);
         TraceScope tr("tc_quadratic", stream);
         quad_kernel<D, false><<<dim3(s.BH(), NT), 320, C::SMEM, stream>>>(
-            mq, mk, mv, mk, (bf16 *)out, s.T, NT, GateArgs{nullptr, nullptr, 1});
+            mq, mk, mv, mk, mo, s.T, NT, GateArgs{nullptr, nullptr, 1});
         return cudaGetLastError();
     }
     // workspace: K' [BH][T][d] bf16 | lam2 [BH][T] fp32 | tile gate products [BH][NT] fp32
@@ -446,7 +454,7 @@ cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const v
                          C::SMEM);
     TraceScope tr("tc_quadratic_gated", stream);
     quad_kernel<D, true><<<dim3(s.BH(), NT), 320, C::SMEM, stream>>>(
-        mq, mk, mv, mkp, (bf16 *)out, s.T, NT, GateArgs{lam2, gtile, normalize});
+        mq, mk, mv, mkp, mo, s.T, NT, GateArgs{lam2, gtile, normalize});
     return cudaGetLastError();
 }
 
