@@ -29,6 +29,8 @@
 //   warps 2-9 ("P warps", TMEM lane quarter = warp % 4, key half = (warp - 2) / 4):
 //     64 keys of a query row: S -> P and a partial row sum; the epilogue O / D
 //     for 32 of the output columns (the two halves' sums meet in shared memory).
+//     S is released as soon as it is in registers, so the next S MMA runs while
+//     P is formed.
 // TMEM (256 columns, two CTAs per SM): S [0,128) | P [128,192) | O [192,256).
 #include "kata_tc_common.cuh"
 
@@ -313,6 +315,11 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const bool diag = j == 0;   // keys past the query are masked on the diagonal tile
             uint32_t v[64], pw[32];
             tmem_ld64(tS + lsel + 64 * h, v);
+            // S_j is in registers (the load has completed): the next S MMA may
+            // overwrite it while P_j is formed
+            tc_fence_before();
+            __syncwarp();
+            if (elect_lane0()) mbar_arrive(&s_free);
             if (kGated && !diag) {
                 // w = S'^2 r_t M_ij: packed square, packed scale, packed sum, convert
                 const float f = rt * M;
@@ -372,9 +379,6 @@ quad_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 dsum += (ds[0] + ds[1]) + (ds[2] + ds[3]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (elect_lane0()) mbar_arrive(&s_free);
             // the P V MMA of the previous tile has read P
             ok = __all_sync(0xffffffffu, j == 0 || sy.wait(&p_free, j - 1));
             if (!ok) break;
