@@ -96,3 +96,30 @@ def test_quadratic_full_size_sampled_rows(kg, name):
         got = to_f64(out.reshape(BH, w.T, w.dv)[h][ts])
         worst = max(worst, slice_rel_err(got, ref))
     assert worst <= TOL[w.dtype], f"{name}: {worst:.3e}"
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_long_context_sampled_rows(kg, gated):
+    """The long-context shape (B=1, H=16, T=131072, d=32: 1024 query tiles per head,
+    the longest walking 1024 key tiles) in the quadratic form, plain and gated,
+    sampled rows against the oracle (first, last, tile edges, random)."""
+    w = workloads.WORKLOADS["long_ctx_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    g = workloads.make_gate(w, device="cuda") if gated else None
+    out = kg.kata_fwd_quadratic_gated(q, k, v, g) if gated else kg.kata_fwd_quadratic(q, k, v)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    assert torch.isfinite(out).all()
+    rng = np.random.default_rng(91)
+    worst = 0.0
+    for h in (0, 7, w.H - 1):
+        ts = np.array(sorted(set([0, 127, 128, w.T // 2, w.T - 1] +
+                                 rng.integers(0, w.T, size=6).tolist())), dtype=np.int64)
+        sl = (slice(0, 1), slice(h, h + 1))
+        qf, kf, vf = to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl])
+        if gated:
+            ref = oracle.forward_rows_gated(qf, kf, vf, to_f64(g[sl]), ts)
+        else:
+            ref = oracle.forward_rows(qf, kf, vf, ts)
+        worst = max(worst, slice_rel_err(to_f64(out[0, h])[ts], ref))
+    assert worst <= TOL[torch.bfloat16], f"{worst:.3e}"
