@@ -333,30 +333,98 @@ int kata_fwd_chunked_host(const void *q, const void *k, const void *v, void *out
     cudaGetLastError();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t es = elem_size(dtype);
-    const size_t nqk = (size_t)B * H * T * d * es, nvo = (size_t)B * H * T * dv * es;
-    void *dq = nullptr, *dk = nullptr, *dvv = nullptr, *dout = nullptr;
+    const int BH = B * H;
+    const size_t hqk = (size_t)T * d * es, hvo = (size_t)T * dv * es;   // bytes per head
+    const size_t nqk = BH * hqk, nvo = BH * hvo;
+    // Heads are independent: for large transfers the heads are cut into groups so
+    // that later groups are copied in while group g runs and group g - 1 is copied
+    // out (two streams in, alternating groups; one out; the forward on the
+    // caller's stream).  A group keeps the whole call's kernel path and still
+    // fills the GPU.
+    const FwdShape whole{1, BH, T, d, dv, C, dtype};
+    const int path = select_path(whole, di);
+    int ng = 1;
+    if (2 * nqk + 2 * nvo >= ((size_t)64 << 20)) {
+        for (int cand : {8, 4, 2}) {
+            const int hg = BH / cand;
+            if (BH % cand != 0 || hg < 1) continue;
+            const FwdShape part{1, hg, T, d, dv, C, dtype};
+            const bool fills = path == KATA_PATH_SIMT || hg * (int64_t)((T + 127) / 128) >= di.sms;
+            if (select_path(part, di) == path && fills) {
+                ng = cand;
+                break;
+            }
+        }
+    }
+    const int hg = BH / ng;
+    char *dq = nullptr, *dk = nullptr, *dvv = nullptr, *dout = nullptr;
     rc = KATA_OK;
-    if (cudaMallocAsync(&dq, nqk, st) != cudaSuccess || cudaMallocAsync(&dk, nqk, st) != cudaSuccess ||
-        cudaMallocAsync(&dvv, nvo, st) != cudaSuccess ||
-        cudaMallocAsync(&dout, nvo, st) != cudaSuccess) {
+    if (cudaMallocAsync((void **)&dq, nqk, st) != cudaSuccess ||
+        cudaMallocAsync((void **)&dk, nqk, st) != cudaSuccess ||
+        cudaMallocAsync((void **)&dvv, nvo, st) != cudaSuccess ||
+        cudaMallocAsync((void **)&dout, nvo, st) != cudaSuccess) {
         cudaGetLastError();
         rc = KATA_ERR_ALLOC;
     }
+    cudaStream_t sin2[2] = {nullptr, nullptr}, sout = nullptr;
+    cudaEvent_t ready = nullptr, done = nullptr, ev_in[8] = {}, ev_run[8] = {};
+    bool ev_ok = rc == KATA_OK &&
+                 cudaStreamCreateWithFlags(&sin2[0], cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&sin2[1], cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&sout, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess;
+    for (int g = 0; g < ng && ev_ok; ++g)
+        ev_ok = cudaEventCreateWithFlags(&ev_in[g], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&ev_run[g], cudaEventDisableTiming) == cudaSuccess;
+    if (rc == KATA_OK && !ev_ok) rc = KATA_ERR_CUDA;
     if (rc == KATA_OK) {
-        if (cudaMemcpyAsync(dq, q, nqk, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyAsync(dk, k, nqk, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyAsync(dvv, v, nvo, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        // the buffers were allocated on the caller's stream: order the copy streams after it
+        if (cudaEventRecord(ready, st) != cudaSuccess ||
+            cudaStreamWaitEvent(sin2[0], ready, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(sin2[1], ready, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(sout, ready, 0) != cudaSuccess)
             rc = KATA_ERR_CUDA;
     }
-    if (rc == KATA_OK) rc = kata_fwd_chunked(dq, dk, dvv, dout, B, H, T, d, dv, C, dtype, stream);
-    if (rc == KATA_OK &&
-        cudaMemcpyAsync(out, dout, nvo, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        rc = KATA_ERR_CUDA;
+    for (int g = 0; g < ng && rc == KATA_OK; ++g) {
+        const size_t oq = (size_t)g * hg * hqk, ov = (size_t)g * hg * hvo;
+        cudaStream_t sin = sin2[g & 1];
+        if (cudaMemcpyAsync(dq + oq, (const char *)q + oq, hg * hqk, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+            cudaMemcpyAsync(dk + oq, (const char *)k + oq, hg * hqk, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+            cudaMemcpyAsync(dvv + ov, (const char *)v + ov, hg * hvo, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+            cudaEventRecord(ev_in[g], sin) != cudaSuccess)
+            rc = KATA_ERR_CUDA;
+    }
+    for (int g = 0; g < ng && rc == KATA_OK; ++g) {
+        const size_t oq = (size_t)g * hg * hqk, ov = (size_t)g * hg * hvo;
+        if (cudaStreamWaitEvent(st, ev_in[g], 0) != cudaSuccess) {
+            rc = KATA_ERR_CUDA;
+            break;
+        }
+        rc = kata_fwd_chunked(dq + oq, dk + oq, dvv + ov, dout + ov, 1, hg, T, d, dv, C, dtype, stream);
+        if (rc != KATA_OK) break;
+        if (cudaEventRecord(ev_run[g], st) != cudaSuccess || cudaStreamWaitEvent(sout, ev_run[g], 0) != cudaSuccess ||
+            cudaMemcpyAsync((char *)out + ov, dout + ov, hg * hvo, cudaMemcpyDeviceToHost, sout) != cudaSuccess)
+            rc = KATA_ERR_CUDA;
+    }
+    // the buffers are freed on the caller's stream after both copy streams are done
+    for (cudaStream_t x : {sin2[0], sin2[1], sout})
+        if (x && done && cudaEventRecord(done, x) == cudaSuccess) cudaStreamWaitEvent(st, done, 0);
     if (dq) cudaFreeAsync(dq, st);
     if (dk) cudaFreeAsync(dk, st);
     if (dvv) cudaFreeAsync(dvv, st);
     if (dout) cudaFreeAsync(dout, st);
     if (cudaStreamSynchronize(st) != cudaSuccess && rc == KATA_OK) rc = KATA_ERR_CUDA;
+    for (cudaStream_t x : {sin2[0], sin2[1], sout})
+        if (x && cudaStreamSynchronize(x) != cudaSuccess && rc == KATA_OK) rc = KATA_ERR_CUDA;
+    for (int g = 0; g < 8; ++g) {
+        if (ev_in[g]) cudaEventDestroy(ev_in[g]);
+        if (ev_run[g]) cudaEventDestroy(ev_run[g]);
+    }
+    if (ready) cudaEventDestroy(ready);
+    if (done) cudaEventDestroy(done);
+    for (cudaStream_t x : {sin2[0], sin2[1], sout})
+        if (x) cudaStreamDestroy(x);
     cudaGetLastError();
     return rc;
 }

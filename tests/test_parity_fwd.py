@@ -189,3 +189,31 @@ def test_d64_tensor_path_deterministic(kg):
     b = kg.kata_fwd_chunked(q, k, v, w.C)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["long_ctx_bf16", "lm_layer_bf16", "small_fp32"])
+def test_host_entry_point(kg, name):
+    """kata_fwd_chunked_host (host buffers; large transfers pipelined over groups of
+    heads): sampled rows against the oracle and the whole output against the
+    device entry point within the tolerance (a head group may be segmented
+    differently from the whole call, which changes only the rounding)."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_qkv(w)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    out = kg.kata_fwd_chunked_host(qh, kh, vh, w.C)
+    dev = kg.kata_fwd_chunked(q.cuda(), k.cuda(), v.cuda(), w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    assert torch.isfinite(out).all()
+    assert slice_rel_err(to_f64(out), to_f64(dev)) <= TOL[w.dtype]
+    BH = w.B * w.H
+    rng = np.random.default_rng(5)
+    worst = 0.0
+    for h in sorted(set([0, BH - 1])):
+        b, hh = divmod(h, w.H)
+        ts = np.array(sorted(set([0, w.T // 2, w.T - 1] + rng.integers(0, w.T, size=5).tolist())),
+                      dtype=np.int64)
+        sl = (slice(b, b + 1), slice(hh, hh + 1))
+        ref = oracle.forward_rows(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), ts)
+        worst = max(worst, slice_rel_err(to_f64(out[b, hh])[ts], ref))
+    assert worst <= TOL[w.dtype], f"{worst:.3e}"
