@@ -127,16 +127,25 @@ gate_prep_kernel(const bf16 *__restrict__ k, const float *__restrict__ gamma,
     const size_t base = ((size_t)bh * T + (size_t)j * kTile) * D;
     const uint4 *src = reinterpret_cast<const uint4 *>(k + base);
     uint4 *dst = reinterpret_cast<uint4 *>(kp + base);
-    for (int e = i; e < rows * (D / 8); e += kTile) {
-        const float sc = scale[e / (D / 8)];
-        uint4 u = src[e];
-        uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+    constexpr int kPer = D / 8;   // 16-byte pieces per thread (one tile has kTile * D / 8)
+    uint4 u[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {   // every load in flight before the first store
+        const int e = i + m * kTile;
+        if (e < rows * kPer) u[m] = src[e];
+    }
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+        const int e = i + m * kTile;
+        if (e >= rows * kPer) continue;
+        const float sc = scale[e / kPer];
+        uint32_t *w = reinterpret_cast<uint32_t *>(&u[m]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[c]);
             w[c] = pack_bf16(__low2float(b) * sc, __high2float(b) * sc);
         }
-        dst[e] = u;
+        dst[e] = u[m];
     }
 }
 
