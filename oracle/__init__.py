@@ -197,8 +197,10 @@ def decode_step(S, z, q, k, v):
 # Reduced PSD families (Sec. 4.1, "two reduced PSD families"): u in R^d cut into
 # g blocks u_a of width m = d/g.  map "M": psi(u) = (u_1 u_1^T, ..., u_g u_g^T);
 # map "Sigma": psi(u) = eps I + s * sum_a u_a u_a^T (eps and s as the Sigma
-# configuration sets them: 1e-4, and 1/4 for Sigma_4); map "full": u u^T.
-MAPS = {"full": 0, "M": 1, "Sigma": 2}
+# configuration sets them: 1e-4, and 1/4 for Sigma_4); map "full": u u^T; map
+# "orthant": psi(u)_i = max(u_i, 0) + eps, one feature per coordinate (the pages'
+# linear-state family, eps = 1e-6 in their configuration).
+MAPS = {"full": 0, "M": 1, "Sigma": 2, "orthant": 3}
 
 
 def map_dim(map_name: str, d: int, g: int) -> int:

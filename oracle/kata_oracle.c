@@ -321,7 +321,10 @@ void kata_oracle_decode_step(double *S, double *z, const double *q, const double
  *   map 2, KATA-Sigma_g: psi(u) = eps I + s * sum_a u_a u_a^T, one m x m matrix
  *                        (eps: a numerical safeguard the Sigma configuration
  *                        sets to 1e-4; s: 1/4 in its reported Sigma_4 setup);
- *   map 0: the full rank-one map (g = 1).
+ *   map 0: the full rank-one map (g = 1);
+ *   map 3, orthant (the linear-state family of the pages' kernel appendix, one
+ *                        feature per coordinate): psi(u)_i = max(u_i, 0) + eps,
+ *                        n = d (eps: 1e-6 in the pages' configuration).
  * Both families give the full map at g = 1 (eps = 0, s = 1).  Inner products
  * are Frobenius; each matrix is packed like the full map (upper triangle,
  * row-major, sqrt(2) off the diagonal), the g matrices of M_g in block order.
@@ -330,6 +333,7 @@ void kata_oracle_decode_step(double *S, double *z, const double *q, const double
 /* Packed feature width of a map (the pages' dominant state size over d_v). */
 int kata_oracle_map_dim(int map, int d, int g) {
     const int m = d / g;
+    if (map == 3) return d;
     if (map == 1) return g * m * (m + 1) / 2;
     if (map == 2) return m * (m + 1) / 2;
     return d * (d + 1) / 2;
@@ -368,6 +372,10 @@ static int map_matrices(const double *u, int d, int map, int g, double eps, doub
 /* Packed lift of one vector under a map; A is scratch of at least d*d. */
 static void lift_map_one(const double *x, int d, int map, int g, double eps, double s,
                          double *phi, double *A) {
+    if (map == 3) {   /* orthant: coordinatewise */
+        for (int i = 0; i < d; ++i) phi[i] = (x[i] > 0.0 ? x[i] : 0.0) + eps;
+        return;
+    }
     const double r2 = sqrt(2.0);
     int w = 0;
     const int count = map_matrices(x, d, map, g, eps, s, A, &w);
@@ -391,6 +399,12 @@ void kata_oracle_lift_map(const double *x, int64_t rows, int d, int map, int g, 
 /* <psi(q), psi(k)>_F as the entrywise sum over the map's matrices. */
 static double map_weight(const double *q, const double *k, int d, int map, int g, double eps,
                          double s, double *Aq, double *Ak) {
+    if (map == 3) {   /* orthant: the dot product of the two feature vectors */
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i)
+            acc += ((q[i] > 0.0 ? q[i] : 0.0) + eps) * ((k[i] > 0.0 ? k[i] : 0.0) + eps);
+        return acc;
+    }
     int w = 0;
     const int count = map_matrices(q, d, map, g, eps, s, Aq, &w);
     map_matrices(k, d, map, g, eps, s, Ak, &w);

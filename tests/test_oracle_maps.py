@@ -210,3 +210,68 @@ def test_planted_weight_mistakes_fail(map_name, mistake):
     bad = _weight_numpy(q, k, map_name, g, e, s, mistake)
     want = _closed_form(q, k, map_name, g, e, s)
     assert abs(bad - want) > 1e-6 * abs(want)
+
+
+# ---- orthant map (the pages' linear-state family): psi(u)_i = max(u_i, 0) + eps, n = d
+def _orthant_identity(q, k, eps):
+    """Expanded inner product: sum q+ k+ + eps (sum q+ + sum k+) + d eps^2."""
+    qp, kp = np.maximum(q, 0.0), np.maximum(k, 0.0)
+    return float(qp @ kp) + eps * (float(qp.sum()) + float(kp.sum())) + q.shape[-1] * eps * eps
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("eps", [0.0, 1e-6, 0.25])
+def test_orthant_width_and_inner_product(d, eps):
+    assert oracle.map_dim("orthant", d, 1) == d
+    rng = np.random.default_rng(d + int(eps * 100))
+    for _ in range(20):
+        q, k = rng.standard_normal(d), rng.standard_normal(d)
+        pq, pk = oracle.lift_map(q, "orthant", 1, eps), oracle.lift_map(k, "orthant", 1, eps)
+        assert pq.shape == (d,) and np.all(pq >= eps)
+        want = _orthant_identity(q, k, eps)
+        assert abs(float(pq @ pk) - want) <= 1e-12 * max(1.0, abs(want))
+
+
+def test_orthant_one_hot_lookup():
+    """eps = 0, one-hot keys and queries: the weight is 1 exactly when the indices
+    match, so o_t is the mean of the values stored under the query's index so far
+    (a zero row when there are none)."""
+    rng = np.random.default_rng(2)
+    d, T, dv = 8, 40, 3
+    ki, qi = rng.integers(0, d, T), rng.integers(0, d, T)
+    k = np.eye(d)[ki][None, None]
+    q = np.eye(d)[qi][None, None]
+    v = rng.standard_normal((1, 1, T, dv))
+    got = oracle.forward_map(q, k, v, "orthant", 1, 0.0)
+    want = np.zeros((T, dv))
+    for t in range(T):
+        hits = [s for s in range(t + 1) if ki[s] == qi[t]]
+        if hits:
+            want[t] = v[0, 0, hits].mean(axis=0)
+    assert _rel(got[0, 0], want) <= 1e-13
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.1])
+def test_orthant_equal_keys_convex_hull_and_recurrence(eps):
+    rng = np.random.default_rng(17)
+    q, k, v = _rand_qkv(rng, T=33, d=16)
+    keq = np.broadcast_to(np.abs(rng.standard_normal(16)), q.shape).copy()
+    got = oracle.forward_map(q, keq, v, "orthant", 1, eps)
+    want = np.cumsum(v, axis=2) / np.arange(1, v.shape[2] + 1)[None, None, :, None]
+    assert _rel(got, want) <= 1e-12
+    o = oracle.forward_map(q, k, v, "orthant", 1, eps)
+    lo, hi = np.minimum.accumulate(v, axis=2), np.maximum.accumulate(v, axis=2)
+    assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)
+    assert _rel(o, oracle.recurrent_map(q, k, v, "orthant", 1, eps)) <= 1e-11
+
+
+@pytest.mark.parametrize("mistake", ["no_relu", "eps_on_query_only"])
+def test_orthant_planted_mistakes_fail(mistake):
+    rng = np.random.default_rng(23)
+    q, k = rng.standard_normal(16), rng.standard_normal(16)
+    eps = 0.2
+    if mistake == "no_relu":
+        bad = float((q + eps) @ (k + eps))
+    else:
+        bad = float((np.maximum(q, 0) + eps) @ np.maximum(k, 0))
+    assert abs(bad - _orthant_identity(q, k, eps)) > 1e-6
