@@ -84,16 +84,17 @@ class FeatureMap:
     """The forward's feature map: the full rank-one map or a reduced PSD family
     ([KATA] Sec. 4.1) with g blocks; the Sigma maps take the eps and scale of the
     pages' Sigma configuration (eps = 1e-4; scale 1/4 for Sigma_4, else 1)."""
-    CODES = {"full": 0, "M": 1, "Sigma": 2}
+    CODES = {"full": 0, "M": 1, "Sigma": 2, "orthant": 3}
 
     def __init__(self, name: str = "full", g: int = 1):
         self.name, self.g, self.code = name, int(g), self.CODES[name]
-        self.eps = 1e-4 if name == "Sigma" else 0.0
+        self.eps = 1e-4 if name == "Sigma" else 1e-6 if name == "orthant" else 0.0
         self.scale = (0.25 if self.g == 4 else 1.0) if name == "Sigma" else 1.0
 
     def n(self, d: int) -> int:
         m = d // self.g
-        return {0: d * (d + 1) // 2, 1: self.g * m * (m + 1) // 2, 2: m * (m + 1) // 2}[self.code]
+        return {0: d * (d + 1) // 2, 1: self.g * m * (m + 1) // 2, 2: m * (m + 1) // 2,
+                3: d}[self.code]
 
     def intra_d(self, d: int) -> int:
         """Multiply-adds per (t, s) pair of the closed-form weight: all g x g block
@@ -101,7 +102,7 @@ class FeatureMap:
         return self.g * d if self.code == 2 else d
 
     def label(self) -> str:
-        return "full" if self.code == 0 else f"{self.name}_{self.g}"
+        return {0: "full", 3: "orthant"}.get(self.code, f"{self.name}_{self.g}")
 
 
 FULL_MAP = FeatureMap()
@@ -120,6 +121,8 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         return out_inter + intra, "TFLOP/s", "alu"
     if stage == "simt_scan":
         return 2.0 * 4 * n * (dv + 1) * NC * BH, "GB/s", "hbm"
+    if stage == "simt_scan_blocked":   # the records are read twice, written once
+        return 3.0 * 4 * n * (dv + 1) * NC * BH, "GB/s", "hbm"
     # GatedKATA on CUDA cores: the same contractions (the gate products add O(C)
     # multiplies per chunk); the gated scan also reads one gate product per chunk
     if stage == "gated_chunk_state":
@@ -657,6 +660,42 @@ def _bench_decode(kg, peaks, args):
                          "bytes_per_step": nbytes}}
 
 
+def run_scan_ubench(args):
+    """Chunk-scan micro-benchmark at the pages' small-batch linear-state shape
+    (B=1, H=16, d=64, dv=64, C=128, orthant map, bf16 inputs, T from 2k to 64k):
+    the forward with the one-pass chunk scan and with the two-level scan
+    (KATA_CHUNK_SCAN), one JSON line per (T, scan); inputs resident, no flush."""
+    from kernelized_causal_linear_gb300 import build
+    build.build()
+    import kernelized_causal_linear_gb300 as kg
+    fm = FeatureMap("orthant")
+    stream = torch.cuda.current_stream()
+    for T in (2048, 8192, 32768, 65536):
+        w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=1, H=16, T=T, d=64, dv=64, C=128)
+        q, k, v = workloads.make_qkv(w, device="cuda")
+        out = torch.empty(w.B, w.H, w.T, w.dv, dtype=w.dtype, device="cuda")
+        for mode in ("sequential", "blocked"):
+            os.environ["KATA_CHUNK_SCAN"] = mode
+            for _ in range(max(3, args.warmup)):
+                kg.kata_fwd_chunked_map(q, k, v, w.C, fm.code, 1, fm.eps, out=out)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            kg.kata_trace_begin()
+            a.record(stream)
+            for _ in range(args.steps):
+                kg.kata_fwd_chunked_map(q, k, v, w.C, fm.code, 1, fm.eps, out=out)
+            b.record(stream)
+            torch.cuda.synchronize()
+            stages = kg.kata_trace_end()
+            ms = a.elapsed_time(b) / args.steps
+            scan = {k_: t_ / n_ for k_, (n_, t_) in stages.items() if "scan" in k_}
+            print(json.dumps({"ubench": "chunk_scan", "T": T, "scan": mode, "ms_per_call": ms,
+                              "Mtok_s": w.B * w.T / ms / 1e3, "scan_ms": scan,
+                              "config": _config(w, fm)}), flush=True)
+        os.environ.pop("KATA_CHUNK_SCAN", None)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -664,7 +703,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--map", default="full", choices=["full", "M", "Sigma"],
+    ap.add_argument("--map", default="full", choices=["full", "M", "Sigma", "orthant"],
                     help="feature map: the full rank-one map or a reduced PSD family")
     ap.add_argument("--g", type=int, default=1, help="blocks of the reduced map (1, 2 or 4)")
     ap.add_argument("--algo", default="chunked",
@@ -676,7 +715,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--ubench", choices=["scan"], default=None,
+                    help="micro-benchmark instead of the bench line: 'scan' compares the "
+                         "one-pass and the two-level chunk scan at small-batch shapes")
     args = ap.parse_args(argv)
+    if args.ubench == "scan":
+        return run_scan_ubench(args)
     if args.map == "full" and args.g != 1:
         ap.error("--map full takes --g 1")
     if args.algo != "chunked" and args.map != "full":

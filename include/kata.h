@@ -66,12 +66,14 @@ typedef enum {
     KATA_PATH_TC = 2    /* tcgen05 tensor-core kernels (bf16 inputs, sm_103a)    */
 } kata_path;
 
-/* Feature map of kata_fwd_chunked_map ([KATA] Sec. 4.1): the full rank-one map
- * and the two reduced PSD families. */
+/* Feature map of kata_fwd_chunked_map ([KATA] Sec. 4.1): the full rank-one map,
+ * the two reduced PSD families, and the orthant map of the pages' linear-state
+ * baselines (kernel appendix; one feature per coordinate). */
 typedef enum {
-    KATA_MAP_FULL = 0,  /* psi(u) = u u^T                                        */
-    KATA_MAP_BLOCK = 1, /* KATA-M_g: psi(u) = (u_1 u_1^T, ..., u_g u_g^T)         */
-    KATA_MAP_SUM = 2    /* KATA-Sigma_g: psi(u) = eps I + scale sum_a u_a u_a^T    */
+    KATA_MAP_FULL = 0,   /* psi(u) = u u^T                                        */
+    KATA_MAP_BLOCK = 1,  /* KATA-M_g: psi(u) = (u_1 u_1^T, ..., u_g u_g^T)         */
+    KATA_MAP_SUM = 2,    /* KATA-Sigma_g: psi(u) = eps I + scale sum_a u_a u_a^T    */
+    KATA_MAP_ORTHANT = 3 /* psi(u)_i = max(u_i, 0) + eps, n = d (g = 1, scale 1)   */
 } kata_map;
 
 /* A cudaStream_t, declared without the CUDA headers. */
@@ -81,8 +83,8 @@ typedef struct CUstream_st *kata_stream_t;
 int kata_feature_dim(int d);
 
 /* Packed feature width of a map with g blocks of width m = d/g: d(d+1)/2
- * (full), g m(m+1)/2 (KATA-M_g) or m(m+1)/2 (KATA-Sigma_g) -- the pages' state
- * sizes over d_v (Sec. 4.1); -1 for an invalid map, d or g. */
+ * (full), g m(m+1)/2 (KATA-M_g), m(m+1)/2 (KATA-Sigma_g) or d (orthant) -- the
+ * pages' state sizes over d_v (Sec. 4.1); -1 for an invalid map, d or g. */
 int kata_map_feature_dim(int map, int d, int g);
 
 /* Static human-readable text for a status code. */
@@ -148,10 +150,14 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   KATA_MAP_SUM   (KATA-Sigma_g): psi(u) = eps I + scale sum_a u_a u_a^T,
  *                                  <psi(q), psi(k)> = eps^2 m + eps scale
  *                                  (|q|^2 + |k|^2) + scale^2 sum_{a,b} (q_a . k_b)^2;
- *   KATA_MAP_FULL with g = 1:      kata_fwd_chunked.
+ *   KATA_MAP_FULL with g = 1:      kata_fwd_chunked;
+ *   KATA_MAP_ORTHANT with g = 1:   psi(u)_i = max(u_i, 0) + eps, n = d,
+ *                                  <psi(q), psi(k)> = sum_i (q_i^+ + eps)(k_i^+ + eps)
+ *                                  (the pages' linear-state family; eps = 1e-6 in
+ *                                  their configuration; scale must be 1).
  *
  * Eq. 17-20 with this psi: states of kata_map_feature_dim(map, d, g) x (dv + 1).
- *   map, g: g in {1, 2, 4} dividing d; KATA_MAP_FULL needs g = 1.
+ *   map, g: g in {1, 2, 4} dividing d; KATA_MAP_FULL and KATA_MAP_ORTHANT need g = 1.
  *   eps >= 0 and scale > 0, finite; KATA_MAP_FULL and KATA_MAP_BLOCK need
  *   eps = 0 and scale = 1 (KATA_ERR_ARG otherwise).
  * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  KATA-M_2

@@ -34,6 +34,7 @@ KATA_BF16 = 1
 KATA_MAP_FULL = 0
 KATA_MAP_BLOCK = 1
 KATA_MAP_SUM = 2
+KATA_MAP_ORTHANT = 3
 
 KATA_PATH_NONE = 0
 KATA_PATH_SIMT = 1

@@ -20,6 +20,8 @@ size_t elem_size(int t) { return t == KATA_F32 ? 4 : 2; }
 
 // A map the reduced-PSD entry points accept (see kata_fwd_chunked_map).
 bool valid_map(int map, int d, int g, float eps, float scale) {
+    if (map == KATA_MAP_ORTHANT)   // one feature per coordinate: g = 1, scale 1, eps >= 0
+        return g == 1 && std::isfinite(eps) && eps >= 0.f && scale == 1.f;
     if (map < KATA_MAP_FULL || map > KATA_MAP_SUM) return false;
     if (!(g == 1 || g == 2 || g == 4) || d < g || d % g != 0) return false;
     if (!std::isfinite(eps) || !std::isfinite(scale) || eps < 0.f || scale <= 0.f) return false;

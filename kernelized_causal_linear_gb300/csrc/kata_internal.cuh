@@ -70,7 +70,8 @@ struct MapSpec {
     __host__ __device__ int m(int d) const { return d / g; }
     __host__ __device__ int n(int d) const {
         const int w = d / g;
-        return kind == 1 ? g * w * (w + 1) / 2 : kind == 2 ? w * (w + 1) / 2 : d * (d + 1) / 2;
+        return kind == 1 ? g * w * (w + 1) / 2 : kind == 2 ? w * (w + 1) / 2 : kind == 3 ? d
+                                                                                 : d * (d + 1) / 2;
     }
 };
 
@@ -93,9 +94,10 @@ cudaError_t lift_launch(const void *x, float *phi, int64_t rows, int d, int dtyp
 // so.state set, E = nf * W holds nf rows of W = dv + 1 values and the inclusive
 // totals go to so.state[BH][nf][dv] (columns 0..dv-1) and so.z[BH][nf] (column dv).
 // With totals set, the inclusive totals go to totals[BH][E] as they are.
+// part_ws (BH * (n / 16 + 1) * E floats) allows the two-level form of the scan.
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
                                   cudaStream_t stream, const StateOut &so = StateOut{},
-                                  int W = 0, float *totals = nullptr);
+                                  int W = 0, float *totals = nullptr, float *part_ws = nullptr);
 
 // ---- decode: kata_decode.cu -----------------------------------------------
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,

@@ -14,9 +14,14 @@
 // from the q/k rows staged in shared memory and never written to memory.  The
 // intra-chunk weights use the closed form of psi(q).psi(k): (q.k)^2 for the full
 // map, sum_a (q_a.k_a)^2 for M_g, eps^2 m + eps s (|q|^2 + |k|^2) +
-// s^2 sum_{a,b} (q_a.k_b)^2 for Sigma_g (Sec. 4.1, reduced PSD families).
+// s^2 sum_{a,b} (q_a.k_b)^2 for Sigma_g (Sec. 4.1, reduced PSD families), and
+// sum_i (q_i^+ + eps)(k_i^+ + eps) for the orthant map (one feature per
+// coordinate, the pages' linear-state family).
 //
 // Workspace: per-chunk states [B*H][N_C][n][dv+1] fp32, scanned in place.
+#include <cstdlib>
+#include <cstring>
+
 #include "kata_internal.cuh"
 
 namespace kata {
@@ -33,9 +38,11 @@ constexpr int kStageRows = 64;    // prefix rows staged per step in the output k
 struct Feat {
     int i0, j0, terms, step;
     float cf, add, scl;
+    bool orthant = false;   // psi_f = max(x[i0], 0) + add instead
     // x: coordinate c at x[c * xs]
     template <typename X>
     __device__ __forceinline__ float operator()(const X *x, int xs) const {
+        if (orthant) return fmaxf(to_f(x[i0 * xs]), 0.f) + add;
         float e = 0.f;
         for (int a = 0; a < terms; ++a)
             e = fmaf(to_f(x[(i0 + a * step) * xs]), to_f(x[(j0 + a * step) * xs]), e);
@@ -46,6 +53,11 @@ struct Feat {
 __device__ __forceinline__ Feat map_feature(int f, int d, const MapSpec &mp) {
     Feat ft;
     int i, j;
+    if (mp.kind == 3) {
+        ft = Feat{f, f, 0, 0, 1.f, mp.eps, 1.f};
+        ft.orthant = true;
+        return ft;
+    }
     if (mp.kind == 0) {
         vech_pair(f, d, i, j);
         ft = Feat{i, j, 1, 0, 1.f, 0.f, 1.f};
@@ -71,6 +83,12 @@ __device__ __forceinline__ float map_weight(const float *q, int qs, const float 
         float dot = 0.f;
         for (int i = 0; i < d; ++i) dot = fmaf(q[i * qs], k[i], dot);
         return dot * dot;
+    }
+    if (mp.kind == 3) {
+        float w = 0.f;
+        for (int i = 0; i < d; ++i)
+            w = fmaf(fmaxf(q[i * qs], 0.f) + mp.eps, fmaxf(k[i], 0.f) + mp.eps, w);
+        return w;
     }
     const int m = d / mp.g;
     float w = 0.f;
@@ -228,6 +246,94 @@ scan_kernel_scalar(float *__restrict__ st, int NC, int64_t E, float *__restrict_
     }
 }
 
+// Two-level form of the same exclusive scan, for records that leave the GPU idle
+// with one thread per four elements (few heads, small states, many chunks): the
+// chunk axis is cut into P parts of L chunks; (1) each part's total, (2) an
+// exclusive scan of the totals over the parts (its last value is the inclusive
+// total), (3) each part rescans from its offset.  Like the pages' tree scan it
+// exposes parallelism along the chunk axis; it reads the records twice.
+__global__ void __launch_bounds__(256)
+scan_part_totals(const float *__restrict__ st, float *__restrict__ tot, int NC, int64_t E, int L,
+                 int P) {
+    const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, E4 = E >> 2;
+    if (e4 >= E4) return;
+    const int p = blockIdx.z, c0 = p * L, c1 = min(NC, c0 + L);
+    const float4 *src = reinterpret_cast<const float4 *>(st + (size_t)blockIdx.y * NC * E) + e4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c < c1; c += 8) {   // up to 8 loads in flight
+        const int m = c1 - c < 8 ? c1 - c : 8;
+        float4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < m) x[j] = src[(size_t)(c + j) * E4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < m) {
+                run.x += x[j].x;
+                run.y += x[j].y;
+                run.z += x[j].z;
+                run.w += x[j].w;
+            }
+    }
+    reinterpret_cast<float4 *>(tot)[((size_t)blockIdx.y * P + p) * E4 + e4] = run;
+}
+
+__global__ void __launch_bounds__(256)
+scan_part_offsets(float *__restrict__ tot, int P, int64_t E, float *__restrict__ state_out,
+                  float *__restrict__ z_out, int W, float *__restrict__ totals) {
+    const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, E4 = E >> 2;
+    if (e4 >= E4) return;
+    float4 *t = reinterpret_cast<float4 *>(tot) + (size_t)blockIdx.y * P * E4 + e4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < P; ++p) {
+        const float4 x = t[(size_t)p * E4];
+        t[(size_t)p * E4] = run;
+        run.x += x.x;
+        run.y += x.y;
+        run.z += x.z;
+        run.w += x.w;
+    }
+    if (totals) reinterpret_cast<float4 *>(totals + (size_t)blockIdx.y * E)[e4] = run;
+    if (state_out) {
+        const int64_t nf = E / W;
+        const float rv[4] = {run.x, run.y, run.z, run.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t e = 4 * e4 + u, f = e / W, col = e % W;
+            if (col < W - 1)
+                state_out[((size_t)blockIdx.y * nf + f) * (W - 1) + col] = rv[u];
+            else
+                z_out[(size_t)blockIdx.y * nf + f] = rv[u];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256)
+scan_part_apply(float *__restrict__ st, const float *__restrict__ tot, int NC, int64_t E, int L,
+                int P) {
+    const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, E4 = E >> 2;
+    if (e4 >= E4) return;
+    const int p = blockIdx.z, c0 = p * L, c1 = min(NC, c0 + L);
+    float4 *dst = reinterpret_cast<float4 *>(st + (size_t)blockIdx.y * NC * E) + e4;
+    float4 run = reinterpret_cast<const float4 *>(tot)[((size_t)blockIdx.y * P + p) * E4 + e4];
+    for (int c = c0; c < c1; c += 8) {   // up to 8 loads in flight
+        const int m = c1 - c < 8 ? c1 - c : 8;
+        float4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < m) x[j] = dst[(size_t)(c + j) * E4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < m) {
+                dst[(size_t)(c + j) * E4] = run;
+                run.x += x[j].x;
+                run.y += x[j].y;
+                run.z += x[j].z;
+                run.w += x[j].w;
+            }
+    }
+}
+
 // ---------------------------------------------------------------- stage 3
 // One block per (chunk, head, column group); thread r owns output row r.
 template <typename T>
@@ -287,6 +393,13 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         }
         __syncthreads();
         for (int fr = 0; fr < nf; ++fr) {
+            if (mp.kind == 3) {   // orthant: feature f0 + fr is coordinate f0 + fr
+                const float a = fmaxf(qsT[(f0 + fr) * C + r], 0.f) + mp.eps;
+                const float *sr = stg + fr * kStride;
+#pragma unroll
+                for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
+                continue;
+            }
             float e = 0.f;
             const int i0 = blk * w + fi, j0 = blk * w + fj;
             for (int a = 0; a < terms; ++a)
@@ -357,7 +470,9 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
             k, v, st, s.T, s.d, s.dv, s.C, n, NC, nft, mp);
     }
     const int64_t E = (int64_t)n * (s.dv + 1);
-    cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream, so, s.dv + 1);
+    float *part_ws = st + (size_t)BH * NC * E;   // part totals of the two-level scan
+    cudaError_t e = scan_exclusive_launch(st, BH, NC, E, "simt_scan", stream, so, s.dv + 1,
+                                          nullptr, part_ws);
     if (e != cudaSuccess) return e;
 
     const size_t sm3 = sizeof(float) *
@@ -374,9 +489,51 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
 
 }  // namespace
 
+// Parts of the two-level scan for a record set (1: the one-pass scan).  The
+// one-pass scan is used while one thread per four elements fills the GPU; the
+// environment variable KATA_CHUNK_SCAN=sequential or =blocked forces either
+// form (both give the same exclusive prefix; for measuring them).
+int scan_parts(int BH, int NC, int64_t E, bool have_ws) {
+    if (!have_ws || E % 4 != 0 || NC < 32) return 1;
+    const char *env0 = getenv("KATA_CHUNK_SCAN");
+    if (NC < 128 && !(env0 && strcmp(env0, "blocked") == 0)) return 1;   // too few parts to pay
+    const int cap = NC / 16;   // the workspace holds NC / 16 + 1 parts per head
+    const char *env = getenv("KATA_CHUNK_SCAN");
+    const bool force_seq = env && strcmp(env, "sequential") == 0;
+    const bool force_blk = env && strcmp(env, "blocked") == 0;
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            sms = v;
+        else
+            sms = 148;
+        cudaGetLastError();
+    }
+    const int64_t threads = (E / 4) * BH, want = (int64_t)sms * 2048;
+    if (force_seq || (!force_blk && threads >= want / 2)) return 1;
+    int64_t P = (want + threads - 1) / threads;
+    P = P < 2 ? 2 : P > cap ? cap : P;
+    const int L = (int)((NC + P - 1) / P);
+    return (NC + L - 1) / L;
+}
+
 cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const char *stage,
-                                  cudaStream_t stream, const StateOut &so, int W, float *totals) {
+                                  cudaStream_t stream, const StateOut &so, int W, float *totals,
+                                  float *part_ws) {
     if (so.state && (W < 2 || E % W != 0)) return cudaErrorInvalidValue;
+    const int P = scan_parts(BH, n, E, part_ws != nullptr);
+    if (P > 1) {
+        const int L = (n + P - 1) / P;
+        const unsigned gx = (unsigned)((E / 4 + 255) / 256);
+        TraceScope tr("simt_scan_blocked", stream);
+        scan_part_totals<<<dim3(gx, BH, P), 256, 0, stream>>>(data, part_ws, n, E, L, P);
+        scan_part_offsets<<<dim3(gx, BH), 256, 0, stream>>>(part_ws, P, E, so.state, so.z, W,
+                                                             totals);
+        scan_part_apply<<<dim3(gx, BH, P), 256, 0, stream>>>(data, part_ws, n, E, L, P);
+        return cudaGetLastError();
+    }
     TraceScope tr(stage, stream);
     if (E % 4 != 0)
         scan_kernel_scalar<<<dim3((unsigned)((E + 255) / 256), BH), 256, 0, stream>>>(
@@ -388,8 +545,9 @@ cudaError_t scan_exclusive_launch(float *data, int BH, int n, int64_t E, const c
 }
 
 size_t simt_workspace_bytes(const FwdShape &s, const MapSpec &map) {
-    return sizeof(float) * (size_t)s.BH() * (size_t)s.NC() * (size_t)map.n(s.d) *
-           (size_t)(s.dv + 1);
+    // per-chunk states, then the part totals of the two-level scan (NC / 16 + 1 parts)
+    return sizeof(float) * (size_t)s.BH() * ((size_t)s.NC() + (size_t)(s.NC() / 16 + 1)) *
+           (size_t)map.n(s.d) * (size_t)(s.dv + 1);
 }
 
 cudaError_t simt_forward(const FwdShape &s, const void *q, const void *k, const void *v,

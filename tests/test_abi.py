@@ -242,3 +242,15 @@ def test_gated_quadratic_rejects_bad_arguments(L):
     assert fq(out=g) == kg.KATA_ERR_ARG                        # output over the gate
     assert fq(T=0) == kg.KATA_ERR_ARG
     assert fq(d=24) == kg.KATA_ERR_UNSUPPORTED
+
+
+def test_orthant_map_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    assert kg.kata_map_feature_dim(kg.KATA_MAP_ORTHANT, 64, 1) == 64
+    assert kg.kata_map_feature_dim(kg.KATA_MAP_ORTHANT, 64, 2) == -1     # one feature per coordinate
+    q, k, v, o = (FAKE * (i + 1) * 4096 for i in range(4))
+    bad_scale = L.kata_fwd_chunked_map(q, k, v, o, 1, 1, 8, 16, 16, 32, 0, 3, 1,
+                                       ctypes.c_float(1e-6), ctypes.c_float(2.0), None)
+    bad_eps = L.kata_fwd_chunked_map(q, k, v, o, 1, 1, 8, 16, 16, 32, 0, 3, 1,
+                                     ctypes.c_float(-1.0), ctypes.c_float(1.0), None)
+    assert bad_scale == kg.KATA_ERR_ARG and bad_eps == kg.KATA_ERR_ARG

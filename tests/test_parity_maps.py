@@ -128,3 +128,48 @@ def test_other_maps_take_cuda_cores(kg):
             kg.KATA_PATH_SIMT
     assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, torch.float32, 1, 2) == \
         kg.KATA_PATH_SIMT
+
+
+# ---- orthant map (psi_i = max(u_i, 0) + eps, n = d) and the two-level chunk scan
+@pytest.mark.parametrize("d,dv,C,dtype", [(16, 16, 32, torch.float32), (32, 64, 64, torch.bfloat16),
+                                          (64, 64, 128, torch.bfloat16), (64, 32, 64, torch.float32)])
+def test_orthant_forward_parity(kg, d, dv, C, dtype):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=3 * C + 5, d=d, dv=dv, C=C, dtype=dtype)
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), C, kg.KATA_MAP_ORTHANT, 1, 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "orthant", 1, 1e-6)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[dtype]
+    x = q.reshape(-1, d)[:50].cuda()
+    phi = kg.kata_lift_map(x, kg.KATA_MAP_ORTHANT, 1, 1e-6)
+    torch.cuda.synchronize()
+    refl = oracle.lift_map(to_f64(x.cpu()), "orthant", 1, 1e-6)
+    assert float(np.max(np.abs(to_f64(phi) - refl))) <= 1e-6 * float(np.max(np.abs(refl)))
+
+
+@pytest.mark.parametrize("mapname,d,dv", [("orthant", 64, 64), ("full", 16, 16)])
+def test_two_level_scan(kg, monkeypatch, mapname, d, dv):
+    """Few heads, small states, many chunks: the two-level chunk scan (forced) and
+    the one-pass scan (forced) both match the oracle and each other; the state
+    exported through the two-level scan matches the oracle's recurrence."""
+    w = workloads.WORKLOADS["small_fp32"].scaled(B=1, H=2, T=64 * 32 + 9, d=d, dv=dv, C=32)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    code = kg.KATA_MAP_ORTHANT if mapname == "orthant" else kg.KATA_MAP_FULL
+    eps = 1e-6 if mapname == "orthant" else 0.0
+    outs = {}
+    for mode in ("sequential", "blocked"):
+        monkeypatch.setenv("KATA_CHUNK_SCAN", mode)
+        outs[mode] = kg.kata_fwd_chunked_map(q, k, v, w.C, code, 1, eps)
+        torch.cuda.synchronize()
+    monkeypatch.delenv("KATA_CHUNK_SCAN")
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), mapname, 1, eps)
+    for mode, o in outs.items():
+        assert slice_rel_err(to_f64(o), ref) <= TOL[torch.float32], mode
+    assert slice_rel_err(to_f64(outs["blocked"]), to_f64(outs["sequential"])) <= 1e-5
+    if mapname == "full":
+        monkeypatch.setenv("KATA_CHUNK_SCAN", "blocked")
+        _, S, z = kg.kata_fwd_chunked_state(q, k, v, w.C)
+        torch.cuda.synchronize()
+        S_ref, z_ref = oracle.prefix_state(to_f64(k), to_f64(v))
+        assert slice_rel_err(to_f64(S), S_ref) <= 1e-5
+        assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= 1e-5
