@@ -24,9 +24,24 @@ namespace {
 
 constexpr int kColGroup = 32;     // value columns per block (plus the ones column)
 constexpr int kStride = kColGroup + 1;
+constexpr int kRow = 36;         // staged state rows: 33 values, 16-byte aligned
 constexpr int kFeatTile = 128;    // features per chunk-state block
 constexpr int kStageRows = 64;    // prefix rows staged per step in the output kernel
 constexpr int kMaxC = 128;
+
+// acc[0..31] += a * row[0..31] for a 16-byte aligned shared-memory row: eight
+// 16-byte loads per 32 FMAs (the rows are read by every thread at once).
+__device__ __forceinline__ void fma_row32(float a, const float *row, float (&acc)[kColGroup + 1]) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+    for (int u = 0; u < kColGroup / 4; ++u) {
+        const float4 x = r4[u];
+        acc[4 * u + 0] = fmaf(a, x.x, acc[4 * u + 0]);
+        acc[4 * u + 1] = fmaf(a, x.y, acc[4 * u + 1]);
+        acc[4 * u + 2] = fmaf(a, x.z, acc[4 * u + 2]);
+        acc[4 * u + 3] = fmaf(a, x.w, acc[4 * u + 3]);
+    }
+}
 
 // Gate products of the chunk starting at t0 with tc tokens, into shared memory:
 // gam[t] = gamma, pre[t] = prod_{r<=t} gamma_r (from the chunk start),
@@ -56,7 +71,7 @@ gated_state_kernel(const T *__restrict__ k, const T *__restrict__ v,
                    const float *__restrict__ gamma, float *__restrict__ st,
                    float *__restrict__ cgate, int T_, int d, int dv, int C, int n, int NC,
                    int nft) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     __shared__ float gam[kMaxC], pre[kMaxC], suf[kMaxC];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
@@ -68,13 +83,13 @@ gated_state_kernel(const T *__restrict__ k, const T *__restrict__ v,
     const int W = dv + 1;
 
     float *ks = sm;                 // [C][d]
-    float *vs = ks + C * d;         // [C][33]
+    float *vs = ks + C * d;         // [C][32]
     const T *kc = k + ((size_t)bh * T_ + t0) * d;
     const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
     for (int e = threadIdx.x; e < tc * d; e += blockDim.x) ks[e] = to_f(kc[e]);
     for (int e = threadIdx.x; e < tc * kColGroup; e += blockDim.x) {
         const int t = e / kColGroup, jj = e % kColGroup;
-        vs[t * kStride + jj] = jj < cols ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+        vs[t * kColGroup + jj] = jj < cols ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
     }
     chunk_gates(gamma + (size_t)bh * T_ + t0, tc, gam, pre, suf);
     if (ft == 0 && cg == 0 && threadIdx.x == 0) cgate[(size_t)bh * NC + c] = pre[tc - 1];
@@ -89,9 +104,7 @@ gated_state_kernel(const T *__restrict__ k, const T *__restrict__ v,
         const float cf = i == j ? 1.f : kSqrt2;
         for (int t = 0; t < tc; ++t) {
             const float a = ks[t * d + i] * ks[t * d + j] * cf * suf[t];   // decayed psi(k_t)_f
-            const float *vr = vs + t * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(a, vr[jj], acc[jj]);
+            fma_row32(a, vs + t * kColGroup, acc);
             acc[kColGroup] += a;
         }
     }
@@ -168,7 +181,7 @@ gated_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
                     const float *__restrict__ gamma, const float *__restrict__ st,
                     T *__restrict__ out, int T_, int d, int dv, int C, int n, int NC,
                     int normalize) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     __shared__ float gam[kMaxC], pre[kMaxC], suf[kMaxC];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
@@ -181,8 +194,8 @@ gated_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
 
     float *qsT = sm;                // [d][C]  (transposed: conflict-free per-row reads)
     float *ks = qsT + d * C;        // [C][d]
-    float *vs = ks + C * d;         // [C][33]
-    float *stg = vs + C * kStride;  // [kStageRows][33]
+    float *vs = ks + C * d;         // [C][32]
+    float *stg = vs + C * kColGroup;  // [kStageRows][kRow]
     const T *qc = q + ((size_t)bh * T_ + t0) * d;
     const T *kc = k + ((size_t)bh * T_ + t0) * d;
     const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
@@ -194,7 +207,7 @@ gated_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     }
     for (int e = threadIdx.x; e < C * kColGroup; e += blockDim.x) {
         const int t = e / kColGroup, jj = e % kColGroup;
-        vs[t * kStride + jj] = (t < tc && jj < cols) ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+        vs[t * kColGroup + jj] = (t < tc && jj < cols) ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
     }
     chunk_gates(gamma + (size_t)bh * T_ + t0, tc, gam, pre, suf);
 
@@ -214,14 +227,14 @@ gated_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             float val = 0.f;
             if (jj < cols) val = row[cg * kColGroup + jj];
             else if (jj == kColGroup) val = row[dv];
-            stg[e] = val;
+            stg[fr * kRow + jj] = val;
         }
         __syncthreads();
         for (int fr = 0; fr < nf; ++fr) {
             const float a = qsT[fi * C + r] * qsT[fj * C + r] * (fi == fj ? 1.f : kSqrt2);
-            const float *sr = stg + fr * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
+            const float *sr = stg + fr * kRow;
+            fma_row32(a, sr, acc);
+            acc[kColGroup] = fmaf(a, sr[kColGroup], acc[kColGroup]);
             if (++fj == d) fj = ++fi;
         }
     }
@@ -237,9 +250,7 @@ gated_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             float dot = 0.f;
             for (int i = 0; i < d; ++i) dot = fmaf(qsT[i * C + r], ks[s * d + i], dot);
             const float w = a * dot * dot;
-            const float *vr = vs + s * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(w, vr[jj], acc[jj]);
+            fma_row32(w, vs + s * kColGroup, acc);
             acc[kColGroup] += w;
             a *= gam[s];
         }
@@ -262,7 +273,7 @@ cudaError_t gated_forward_t(const FwdShape &s, const T *q, const T *k, const T *
     const int ncg = (s.dv + kColGroup - 1) / kColGroup;
     float *cgate = st + (size_t)BH * NC * n * (s.dv + 1);
 
-    size_t sm1 = sizeof(float) * (size_t)(s.C * s.d + s.C * kStride);
+    size_t sm1 = sizeof(float) * (size_t)(s.C * s.d + s.C * kColGroup);
     sm1 = sm1 > sizeof(float) * kFeatTile * kStride ? sm1 : sizeof(float) * kFeatTile * kStride;
     cudaFuncSetAttribute(gated_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sm1);
@@ -279,7 +290,7 @@ cudaError_t gated_forward_t(const FwdShape &s, const T *q, const T *k, const T *
             st, cgate, NC, E, so.state, so.z, s.dv + 1);
     }
     const size_t sm3 = sizeof(float) *
-                       (size_t)(2 * s.d * s.C + s.C * kStride + kStageRows * kStride);
+                       (size_t)(2 * s.d * s.C + s.C * kColGroup + kStageRows * kRow);
     cudaFuncSetAttribute(gated_output_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sm3);
     {

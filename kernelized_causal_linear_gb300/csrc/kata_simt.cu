@@ -29,8 +29,23 @@ namespace {
 
 constexpr int kColGroup = 32;     // value columns per block (plus the ones column)
 constexpr int kStride = kColGroup + 1;
+constexpr int kRow = 36;         // staged state rows: 33 values, 16-byte aligned
 constexpr int kFeatTile = 128;    // features per chunk-state block
 constexpr int kStageRows = 64;    // prefix rows staged per step in the output kernel
+
+// acc[0..31] += a * row[0..31] for a 16-byte aligned shared-memory row: eight
+// 16-byte loads per 32 FMAs (the rows are read by every thread at once).
+__device__ __forceinline__ void fma_row32(float a, const float *row, float (&acc)[kColGroup + 1]) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+    for (int u = 0; u < kColGroup / 4; ++u) {
+        const float4 x = r4[u];
+        acc[4 * u + 0] = fmaf(a, x.x, acc[4 * u + 0]);
+        acc[4 * u + 1] = fmaf(a, x.y, acc[4 * u + 1]);
+        acc[4 * u + 2] = fmaf(a, x.z, acc[4 * u + 2]);
+        acc[4 * u + 3] = fmaf(a, x.w, acc[4 * u + 3]);
+    }
+}
 
 // Packed feature f of a map as entries of its matrix: psi_f = cf * (add + scl *
 // sum_{a < terms} x[i0 + a step] x[j0 + a step]) (one term except for Sigma_g,
@@ -119,7 +134,7 @@ template <typename T>
 __global__ void __launch_bounds__(kFeatTile)
 chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ st,
                    int T_, int d, int dv, int C, int n, int NC, int nft, MapSpec mp) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
     const int ft = blockIdx.z % nft;
@@ -130,13 +145,13 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
     const int W = dv + 1;
 
     float *ks = sm;                 // [C][d]
-    float *vs = ks + C * d;         // [C][33]
+    float *vs = ks + C * d;         // [C][32]
     const T *kc = k + ((size_t)bh * T_ + t0) * d;
     const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
     for (int e = threadIdx.x; e < tc * d; e += blockDim.x) ks[e] = to_f(kc[e]);
     for (int e = threadIdx.x; e < tc * kColGroup; e += blockDim.x) {
         const int t = e / kColGroup, jj = e % kColGroup;
-        vs[t * kStride + jj] = jj < cols ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+        vs[t * kColGroup + jj] = jj < cols ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
     }
     __syncthreads();
 
@@ -148,9 +163,7 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
         const Feat ft = map_feature(f, d, mp);
         for (int t = 0; t < tc; ++t) {
             const float a = ft(ks + t * d, 1);   // psi(k_t)_f
-            const float *vr = vs + t * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(a, vr[jj], acc[jj]);
+            fma_row32(a, vs + t * kColGroup, acc);
             acc[kColGroup] += a;
         }
     }
@@ -341,7 +354,7 @@ __global__ void __launch_bounds__(128)
 output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ st, T *__restrict__ out, int T_, int d, int dv,
               int C, int n, int NC, MapSpec mp) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int c = blockIdx.x;
     const int bh = blockIdx.y;
     const int cg = blockIdx.z;
@@ -353,8 +366,8 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
     float *qsT = sm;                // [d][C]  (transposed: conflict-free per-row reads)
     float *ks = qsT + d * C;        // [C][d]
-    float *vs = ks + C * d;         // [C][33]
-    float *stg = vs + C * kStride;  // [kStageRows][33]
+    float *vs = ks + C * d;         // [C][32]
+    float *stg = vs + C * kColGroup;  // [kStageRows][kRow]
     const T *qc = q + ((size_t)bh * T_ + t0) * d;
     const T *kc = k + ((size_t)bh * T_ + t0) * d;
     const T *vc = v + ((size_t)bh * T_ + t0) * dv + cg * kColGroup;
@@ -366,7 +379,7 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     }
     for (int e = threadIdx.x; e < C * kColGroup; e += blockDim.x) {
         const int t = e / kColGroup, jj = e % kColGroup;
-        vs[t * kStride + jj] = (t < tc && jj < cols) ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
+        vs[t * kColGroup + jj] = (t < tc && jj < cols) ? to_f(vc[(size_t)t * dv + jj]) : 0.f;
     }
 
     float acc[kStride];
@@ -389,15 +402,15 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             float val = 0.f;
             if (jj < cols) val = row[cg * kColGroup + jj];
             else if (jj == kColGroup) val = row[dv];
-            stg[e] = val;
+            stg[fr * kRow + jj] = val;
         }
         __syncthreads();
         for (int fr = 0; fr < nf; ++fr) {
             if (mp.kind == 3) {   // orthant: feature f0 + fr is coordinate f0 + fr
                 const float a = fmaxf(qsT[(f0 + fr) * C + r], 0.f) + mp.eps;
-                const float *sr = stg + fr * kStride;
-#pragma unroll
-                for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
+                const float *sr = stg + fr * kRow;
+                fma_row32(a, sr, acc);
+                acc[kColGroup] = fmaf(a, sr[kColGroup], acc[kColGroup]);
                 continue;
             }
             float e = 0.f;
@@ -406,9 +419,9 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
                 e = fmaf(qsT[(i0 + a * w) * C + r], qsT[(j0 + a * w) * C + r], e);
             const float add = (mp.kind == 2 && fi == fj) ? mp.eps : 0.f;
             const float a = fmaf(scl, e, add) * (fi == fj ? 1.f : kSqrt2);
-            const float *sr = stg + fr * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kStride; ++jj) acc[jj] = fmaf(a, sr[jj], acc[jj]);
+            const float *sr = stg + fr * kRow;
+            fma_row32(a, sr, acc);
+            acc[kColGroup] = fmaf(a, sr[kColGroup], acc[kColGroup]);
             if (++fj == w) {
                 if (++fi == w) {
                     fi = 0;
@@ -423,9 +436,7 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     if (r < tc) {
         for (int s = 0; s <= r; ++s) {
             const float w = map_weight(qsT + r, C, ks + s * d, d, mp);
-            const float *vr = vs + s * kStride;
-#pragma unroll
-            for (int jj = 0; jj < kColGroup; ++jj) acc[jj] = fmaf(w, vr[jj], acc[jj]);
+            fma_row32(w, vs + s * kColGroup, acc);
             acc[kColGroup] += w;
         }
         // Eq. 20 normalisation; a zero denominator gives a zero row
@@ -460,7 +471,7 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
     const int nft = (n + kFeatTile - 1) / kFeatTile;
     const int ncg = (s.dv + kColGroup - 1) / kColGroup;
 
-    size_t sm1 = sizeof(float) * (size_t)(s.C * s.d + s.C * kStride);
+    size_t sm1 = sizeof(float) * (size_t)(s.C * s.d + s.C * kColGroup);
     sm1 = sm1 > sizeof(float) * kFeatTile * kStride ? sm1 : sizeof(float) * kFeatTile * kStride;
     cudaFuncSetAttribute(chunk_state_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sm1);
@@ -476,7 +487,7 @@ cudaError_t simt_forward_t(const FwdShape &s, const T *q, const T *k, const T *v
     if (e != cudaSuccess) return e;
 
     const size_t sm3 = sizeof(float) *
-                       (size_t)(2 * s.d * s.C + s.C * kStride + kStageRows * kStride);
+                       (size_t)(2 * s.d * s.C + s.C * kColGroup + kStageRows * kRow);
     cudaFuncSetAttribute(output_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sm3);
     {
