@@ -217,3 +217,33 @@ def test_host_entry_point(kg, name):
         ref = oracle.forward_rows(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), ts)
         worst = max(worst, slice_rel_err(to_f64(out[b, hh])[ts], ref))
     assert worst <= TOL[w.dtype], f"{worst:.3e}"
+
+
+@pytest.mark.parametrize("form", ["simt_fp32", "tc_bf16", "quadratic", "gated"])
+def test_maximum_head_count(kg, form):
+    """B * H = 65535 (the grid limit every path checks) at T = 3: one partial chunk
+    per head.  Sampled heads against the oracle."""
+    if form == "simt_fp32":
+        w = workloads.WORKLOADS["small_fp32"].scaled(B=3, H=21845, T=3)
+    else:
+        w = workloads.WORKLOADS["mid_bf16"].scaled(B=3, H=21845, T=3)
+    q, k, v = workloads.make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    g = None
+    if form == "quadratic":
+        out = kg.kata_fwd_quadratic(qd, kd, vd)
+    elif form == "gated":
+        g = workloads.make_gate(w)
+        out = kg.kata_fwd_chunked_gated(qd, kd, vd, g.cuda(), w.C)
+    else:
+        out = kg.kata_fwd_chunked(qd, kd, vd, w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    heads = [(0, 0), (1, 12345), (2, w.H - 1)]
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        if g is None:
+            ref = oracle.forward(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]))
+        else:
+            ref = oracle.forward_gated(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(g[sl]))
+        assert slice_rel_err(to_f64(out[sl]), ref) <= TOL[w.dtype], (form, b, h)
