@@ -327,6 +327,61 @@ def _oracle_sample(w, q, k, v, seconds: float, rng, fm: FeatureMap = FULL_MAP, g
     return nrows, dt, oracle.get_threads()
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        for key in ("Model name", "Vendor ID"):
+            name = fields.get(key, "").strip()
+            if name and name != "-":
+                return name
+    except (OSError, subprocess.SubprocessError, ValueError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _cpu_extras(w, qh, kh, vh, seconds: float, fm: FeatureMap, gate):
+    """More CPU reference points: the same sampled direct oracle on one core, and
+    the O(T n dv) feature-state recurrence (the fairer CPU algorithm) on a prefix of
+    each kept head (its cost per token is the same at every position)."""
+    import oracle
+    extras = {"cpu_model": _cpu_model(), "nproc": os.cpu_count()}
+    prev = oracle.get_threads()
+    oracle.set_threads(1)
+    try:
+        nrows, dt, _ = _oracle_sample(w, qh, kh, vh, max(1.0, seconds / 3),
+                                      np.random.default_rng(2), fm, gate)
+        extras["single_core"] = {"value": (nrows / w.H) / dt, "unit": "tokens/s", "cores": 1,
+                                 "sample": f"{nrows} output rows, direct O(T^2) fp64, {dt:.1f} s"}
+    finally:
+        oracle.set_threads(prev)
+    if fm.code == 0 and gate is None:
+        heads = qh.shape[1]
+        L = min(w.T, 256)
+        while True:   # a prefix of L tokens on every kept head, about seconds / 3 of work
+            t0 = time.perf_counter()
+            oracle.recurrent(qh[:, :, :L], kh[:, :, :L], vh[:, :, :L])
+            dt = time.perf_counter() - t0
+            if dt >= max(0.5, seconds / 6) or L >= w.T:
+                break
+            L = min(w.T, L * 4)
+        extras["recurrent_form"] = {
+            "value": (heads * L / w.H) / dt, "unit": "tokens/s",
+            "cores": min(heads, oracle.get_threads()), "kind": "oracle recurrence",
+            "sample": f"first {L} tokens of heads 0..{heads - 1}, explicit vech-state "
+                      f"recurrence (O(T n dv)) in fp64, {dt:.2f} s; tokens = head-tokens / H"}
+    return extras
+
+
 def _host_f64(t):
     return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
 
@@ -613,6 +668,7 @@ def run_ours(args):
                "sample": f"{nrows} output rows from heads 0..{keep - 1}, positions uniform in "
                          f"[0,T), direct O(T^2) fp64 definition"
                          f"{' (gated)' if gh64 is not None else ''}, {dt:.1f} s; tokens = rows / H"}
+        cpu.update(_cpu_extras(sub, qh, kh, vh, args.cpu_seconds, fm, gh64))
 
     if rank == 0:
         line = {
