@@ -160,6 +160,31 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     return None, "", ""
 
 
+def stage_dense_flops(stage: str, w, num_sms: int = SMS):
+    """Tile-level flops a tensor-core launch executes (padding and masked halves
+    included), for the kernels whose MMA tiles are fixed: per 128-token chunk the
+    d = 32 output kernel runs 5 state blocks (M128 N64 K128), psi_q S_pre over 4
+    full blocks and one 16-feature block, 4 Q K^T quarters (M128 N32 K32), 4 P V
+    quarters (M128 N64 K32), the Gram (M128 N32 K128) and Q G_pre (M128 N32 K32);
+    the state kernel the 5 state blocks and the Gram.  The quadratic kernels run
+    every (query tile, key tile <= it) pair as full 128 x 128 tiles."""
+    BH, T, d, dv = w.B * w.H, w.T, w.d, w.dv
+    mma = lambda m, n, k: 2.0 * m * n * k
+    nct, G, Lc = tc_plan(w, num_sms)
+    state = 5 * mma(128, 64, 128)
+    gram = mma(128, 32, 128)
+    if stage == "tc_segment_output":
+        per = (state + 4 * mma(128, 64, 128) + mma(128, 64, 16) + 4 * mma(128, 32, 32)
+               + 4 * mma(128, 64, 32) + gram + mma(128, 32, 32))
+        return per * nct * BH
+    if stage == "tc_segment_state":
+        return (state + gram) * min(nct, (G - 1) * Lc) * BH
+    if stage in ("tc_quadratic", "tc_quadratic_gated"):
+        nt = -(-T // 128)
+        return (nt * (nt + 1) // 2) * BH * (mma(128, 128, d) + mma(128, dv, 128))
+    return None
+
+
 def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
     """Algorithmic flops of one forward call at the workload's chunk size:
     2n(dv+1) (state) + 2n(dv+1) (inter output) per token and head, plus the
@@ -599,6 +624,10 @@ def run_ours(args):
                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
                         "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
                         "work_per_launch": work}
+            dense = stage_dense_flops(dom, w, torch.cuda.get_device_properties(0).multi_processor_count)
+            if dense is not None:   # what the tensor cores execute, beside the algorithmic work
+                roofline["dense_tflops"] = dense / mean_s / 1e12
+                roofline["dense_frac"] = dense / mean_s / 1e12 / peaks["bf16_tflops"]
     # whole-call tensor fraction (algorithmic tensor flops over the step time)
     step_s = elapsed_ms / 1e3 / args.steps
     alg_flops = call_flops(w, fm, args.algo)
