@@ -738,11 +738,25 @@ def _bench_decode(kg, peaks, args):
     BH, n = w.B * w.H, w.n
     nbytes = BH * (2 * 4 * n * w.dv + 2 * 4 * n) + BH * (2 * w.d + 2 * w.dv) * 2
     gbs = nbytes / (ms / 1e3) / 1e9
+    # the GatedKATA step: the same sweep with a per-head gate (4 more bytes per head)
+    g = workloads.make_decode_gate(w, device="cuda")
+    for _ in range(3):
+        kg.kata_decode_step_gated(S, z, q, k, v, g, out=o)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        kg.kata_decode_step_gated(S, z, q, k, v, g, out=o)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_g = a.elapsed_time(b) / steps
+    gbs_g = (nbytes + 4 * BH) / (ms_g / 1e3) / 1e9
     return {"workload": "decode B=256 H=16 d=64 dv=64 fp32 state", "ms_per_step": ms,
             "tokens_per_s": w.B / (ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                         "bytes_per_step": nbytes}}
+                         "bytes_per_step": nbytes},
+            "gated": {"ms_per_step": ms_g, "achieved_gbs": gbs_g,
+                      "frac": gbs_g / peaks["hbm_gbs"]}}
 
 
 def run_scan_ubench(args):
