@@ -275,6 +275,26 @@ int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int 
  * Queries the device's compute capability, nothing else. */
 int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype);
 
+/* Which form kata_fwd runs for a shape on the current device. */
+typedef enum {
+    KATA_FORM_NONE = 0,       /* the shape is rejected                           */
+    KATA_FORM_CHUNKED = 1,    /* kata_fwd_chunked                                */
+    KATA_FORM_QUADRATIC = 2   /* kata_fwd_quadratic                              */
+} kata_form;
+
+/*
+ * kata_fwd -- the forward in whichever exact form is faster for the shape:
+ * the quadratic form (kata_fwd_quadratic) where it is supported and T is at
+ * most a head-dimension-dependent crossover (6144 tokens at d = 32, 8192 at
+ * d = 64, from measurements of both forms on GB300), else the chunked form
+ * (kata_fwd_chunked).  Both compute the same o_t; they differ in rounding
+ * only.  Arguments, layouts and errors as kata_fwd_chunked (C is used by the
+ * chunked form).  kata_fwd_form tells which form a shape takes.
+ */
+int kata_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int T, int d,
+             int dv, int C, int dtype, kata_stream_t stream);
+int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype);
+
 /*
  * kata_fwd_chunked_host -- the same forward with HOST buffers: allocates
  * device buffers from the stream-ordered pool, copies q, k, v host->device,

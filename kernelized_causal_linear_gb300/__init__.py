@@ -35,6 +35,9 @@ KATA_MAP_FULL = 0
 KATA_MAP_BLOCK = 1
 KATA_MAP_SUM = 2
 KATA_MAP_ORTHANT = 3
+KATA_FORM_NONE = 0
+KATA_FORM_CHUNKED = 1
+KATA_FORM_QUADRATIC = 2
 
 KATA_PATH_NONE = 0
 KATA_PATH_SIMT = 1
@@ -46,7 +49,7 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
-            "kata_decode_step_gated", "kata_fwd_quadratic_gated")
+            "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form")
 
 _lib = None
 
@@ -105,6 +108,10 @@ def lib() -> ctypes.CDLL:
         L.kata_decode_step_gated.restype = i
         L.kata_fwd_quadratic_gated.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, vp]
         L.kata_fwd_quadratic_gated.restype = i
+        L.kata_fwd.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
+        L.kata_fwd.restype = i
+        L.kata_fwd_form.argtypes = [i, i, i, i, i, i, i]
+        L.kata_fwd_form.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -249,6 +256,25 @@ def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: t
                                 _dtype_code(q.dtype), _stream_handle(stream, q.device))
     _check(rc, "kata_decode_step")
     return out
+
+
+def kata_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The forward in whichever exact form is faster for the shape (quadratic for
+    short sequences on the tensor cores, else chunked); kata_fwd_form tells which."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, out)
+    rc = lib().kata_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, d, dv,
+                        int(C), _dtype_code(q.dtype), _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd")
+    return out
+
+
+def kata_fwd_form(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
+    return int(lib().kata_fwd_form(B, H, T, d, dv, C, _dtype_code(dtype)))
 
 
 def kata_fwd_quadratic(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

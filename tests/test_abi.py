@@ -254,3 +254,13 @@ def test_orthant_map_arguments(L):
     bad_eps = L.kata_fwd_chunked_map(q, k, v, o, 1, 1, 8, 16, 16, 32, 0, 3, 1,
                                      ctypes.c_float(-1.0), ctypes.c_float(1.0), None)
     assert bad_scale == kg.KATA_ERR_ARG and bad_eps == kg.KATA_ERR_ARG
+
+
+def test_fwd_auto_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, o = (FAKE * (i + 1) * 4096 for i in range(4))
+    assert L.kata_fwd(0, k, v, o, 1, 1, 8, 32, 64, 64, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd(q, k, v, 0, 1, 1, 8, 32, 64, 64, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd(q, k, v, o, 1, 1, 0, 32, 64, 64, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd(q, k, v, o, 1, 1, 8, 24, 64, 64, 1, None) == kg.KATA_ERR_UNSUPPORTED
+    assert L.kata_fwd_form(1, 1, 8, 24, 64, 64, 1) == kg.KATA_FORM_NONE

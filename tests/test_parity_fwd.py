@@ -247,3 +247,23 @@ def test_maximum_head_count(kg, form):
         else:
             ref = oracle.forward_gated(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(g[sl]))
         assert slice_rel_err(to_f64(out[sl]), ref) <= TOL[w.dtype], (form, b, h)
+
+
+@pytest.mark.parametrize("name,T,form", [("lm_layer_bf16", 700, "quadratic"),
+                                         ("mid_bf16", 4096, "quadratic"),
+                                         ("recall_bf16", 8192, "chunked"),
+                                         ("small_fp32", 256, "chunked")])
+def test_fwd_picks_the_faster_form(kg, name, T, form):
+    """kata_fwd: the quadratic form up to the crossover on the tensor cores, the
+    chunked form beyond it and for fp32; sampled rows against the oracle."""
+    w = workloads.WORKLOADS[name].scaled(B=1, H=2, T=T)
+    want = kg.KATA_FORM_QUADRATIC if form == "quadratic" else kg.KATA_FORM_CHUNKED
+    assert kg.kata_fwd_form(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == want
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd(q.cuda(), k.cuda(), v.cuda(), w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    rows = np.array(sorted(set([0, 1, T // 3, T // 2, T - 1, T + 5, 2 * T - 1])), dtype=np.int64)
+    ref = oracle.forward_rows(to_f64(q), to_f64(k), to_f64(v), rows)
+    got = to_f64(out).reshape(-1, w.dv)[rows]
+    assert slice_rel_err(got, ref) <= TOL[w.dtype]
