@@ -88,19 +88,6 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // ---------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-// 2-D tiled load of a box into shared memory; completes `bytes` on `bar`.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // 3-D tiled load (x innermost); out-of-range rows are zero-filled.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
                                             uint64_t *bar) {
@@ -274,9 +261,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "r"(taddr)
         : "memory");
 }
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 // Two 32 lanes x 4 columns loads (columns a .. a+3 and b .. b+3), one wait.
 __device__ __forceinline__ void tmem_ld4x2(uint32_t ta, uint32_t tb, uint32_t (&x)[4],
                                            uint32_t (&y)[4]) {
@@ -348,17 +332,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-
-// Byte offset of element (row, k) of a K-major tile in the 128-byte swizzle
-// layout: 64 bf16 per 128-byte row, 8-row atoms of 1024 bytes stacked along
-// the row axis, atom columns (64 k each) `col_stride` bytes apart; the 16-byte
-// chunk index is XORed with (row % 8).
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t k,
-                                                          uint32_t col_stride) {
-    const uint32_t kc = k >> 6, kk = k & 63;
-    const uint32_t chunk = (kk >> 3) ^ (row & 7);
-    return kc * col_stride + (row >> 3) * 1024u + (row & 7) * 128u + chunk * 16u + (kk & 7) * 2u;
 }
 
 }  // namespace sm100
