@@ -22,30 +22,12 @@
 #include <cstdlib>
 #include <cstring>
 
-#include "kata_internal.cuh"
+#include "kata_simt_common.cuh"
 
 namespace kata {
 namespace {
 
-constexpr int kColGroup = 32;     // value columns per block (plus the ones column)
-constexpr int kStride = kColGroup + 1;
-constexpr int kRow = 36;         // staged state rows: 33 values, 16-byte aligned
-constexpr int kFeatTile = 128;    // features per chunk-state block
-constexpr int kStageRows = 64;    // prefix rows staged per step in the output kernel
-
-// acc[0..31] += a * row[0..31] for a 16-byte aligned shared-memory row: eight
-// 16-byte loads per 32 FMAs (the rows are read by every thread at once).
-__device__ __forceinline__ void fma_row32(float a, const float *row, float (&acc)[kColGroup + 1]) {
-    const float4 *r4 = reinterpret_cast<const float4 *>(row);
-#pragma unroll
-    for (int u = 0; u < kColGroup / 4; ++u) {
-        const float4 x = r4[u];
-        acc[4 * u + 0] = fmaf(a, x.x, acc[4 * u + 0]);
-        acc[4 * u + 1] = fmaf(a, x.y, acc[4 * u + 1]);
-        acc[4 * u + 2] = fmaf(a, x.z, acc[4 * u + 2]);
-        acc[4 * u + 3] = fmaf(a, x.w, acc[4 * u + 3]);
-    }
-}
+using namespace simt;
 
 // Packed feature f of a map as entries of its matrix: psi_f = cf * (add + scl *
 // sum_{a < terms} x[i0 + a step] x[j0 + a step]) (one term except for Sigma_g,
@@ -167,21 +149,8 @@ chunk_state_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__re
             acc[kColGroup] += a;
         }
     }
-    __syncthreads();
-    // transpose through shared memory so each warp writes contiguous row segments
-    float *os = sm;                 // [128][33]
-#pragma unroll
-    for (int jj = 0; jj < kStride; ++jj) os[threadIdx.x * kStride + jj] = acc[jj];
-    __syncthreads();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    float *base = st + ((size_t)bh * NC + c) * (size_t)n * W;
-    for (int r = warp; r < kFeatTile; r += blockDim.x / 32) {
-        const int ff = ft * kFeatTile + r;
-        if (ff >= n) break;
-        float *row = base + (size_t)ff * W;
-        if (lane < cols) row[cg * kColGroup + lane] = os[r * kStride + lane];
-        if (cg == 0 && lane == 0) row[dv] = os[r * kStride + kColGroup];
-    }
+    // through shared memory so that each warp writes contiguous row segments
+    store_state_rows(acc, sm, st + ((size_t)bh * NC + c) * (size_t)n * W, ft, cg, cols, n, dv);
 }
 
 // ---------------------------------------------------------------- stage 2
@@ -396,14 +365,7 @@ output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     for (int f0 = 0; f0 < n; f0 += kStageRows) {
         const int nf = min(kStageRows, n - f0);
         __syncthreads();
-        for (int e = threadIdx.x; e < nf * kStride; e += blockDim.x) {
-            const int fr = e / kStride, jj = e % kStride;
-            const float *row = sp + (size_t)(f0 + fr) * W;
-            float val = 0.f;
-            if (jj < cols) val = row[cg * kColGroup + jj];
-            else if (jj == kColGroup) val = row[dv];
-            stg[fr * kRow + jj] = val;
-        }
+        stage_state_rows(sp, stg, f0, nf, cg, cols, dv);
         __syncthreads();
         for (int fr = 0; fr < nf; ++fr) {
             if (mp.kind == 3) {   // orthant: feature f0 + fr is coordinate f0 + fr
