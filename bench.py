@@ -29,6 +29,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -204,19 +205,37 @@ _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu")
                  ("gated", "kata_gated.cu"), ("decode", "kata_decode.cu"))
 
 
+def _local_includes(path: str, seen: set) -> None:
+    """path and, transitively, the quoted local headers it includes."""
+    path = os.path.normpath(path)
+    if path in seen or not os.path.exists(path):
+        return
+    seen.add(path)
+    with open(path) as f:
+        for line in f:
+            m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+            if m:
+                _local_includes(os.path.join(os.path.dirname(path), m.group(1)), seen)
+
+
 def _source_digest(stage: str | None = None) -> str:
     """Digest of the CUDA sources a stage's kernel is built from: its own .cu and
-    every .cuh header (all of csrc without a stage)."""
+    the local headers it includes, transitively (all of csrc without a stage)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kernelized_causal_linear_gb300", "csrc")
     own = None
     if stage is not None:
         own = next((f for prefix, f in _STAGE_SOURCE if stage.startswith(prefix)), None)
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith(".cuh") or (name.endswith(".cu") and own in (None, name)):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    if own is None:
+        files = [os.path.join(csrc, n) for n in os.listdir(csrc) if n.endswith((".cu", ".cuh"))]
+    else:
+        seen: set = set()
+        _local_includes(os.path.join(csrc, own), seen)
+        files = list(seen)
+    for path in sorted(files, key=lambda x: os.path.relpath(x, ROOT)):
+        with open(path, "rb") as f:
+            h.update(os.path.relpath(path, ROOT).encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
