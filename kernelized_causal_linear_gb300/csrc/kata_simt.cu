@@ -172,11 +172,13 @@ __device__ __forceinline__ void feature_table(int f0, int cnt, int n, int d, con
 }
 
 // psi_f of the vector x (coordinate c at x[c * xs]) from its table entry.
-template <bool kFull>
+// KIND: the map fixed at compile time (0 full, 3 orthant) or -1 (read at run time).
+template <int KIND>
 __device__ __forceinline__ float psi_at(const float *x, int xs, int ij, float A, float B,
                                         int terms, int step, bool orth) {
     const int i0 = ij & 0xffff, j0 = ij >> 16;
-    if constexpr (kFull) return fmaf(A, x[i0 * xs] * x[j0 * xs], B);   // one term, no eps
+    if constexpr (KIND == 0) return fmaf(A, x[i0 * xs] * x[j0 * xs], B);   // one term, no eps
+    if constexpr (KIND == 3) return x[i0 * xs];
     if (orth) return x[i0 * xs];
     float e = 0.f;
     for (int a = 0; a < terms; ++a)
@@ -254,7 +256,7 @@ __device__ __forceinline__ void stage_values(const T *vc, int dv, int tc, int C,
 // value columns over the chunk's tokens in 32-token slabs.  The key rows, the
 // value rows and the feature table are staged once for all tiles.  Gated: v_s
 // and the ones column scaled by suf_s.
-template <typename T, bool kGated, bool kFull>
+template <typename T, bool kGated, int KIND>
 __global__ void __maxnreg__(112)
 tiled_state_kernel(const T *__restrict__ k, const T *__restrict__ v,
                    const float *__restrict__ gamma, float *__restrict__ st,
@@ -312,7 +314,7 @@ tiled_state_kernel(const T *__restrict__ k, const T *__restrict__ v,
                 for (int kk = u / FT; kk < kKS; kk += nsplit) {
                     const int t = s0 + kk;
                     A[kk * FT + fl] = (t < tc && f < n)
-                                          ? psi_at<kFull>(ks + t * d, 1, ij, fa, fb, terms, step, orth)
+                                          ? psi_at<KIND>(ks + t * d, 1, ij, fa, fb, terms, step, orth)
                                           : 0.f;
                 }
             }
@@ -518,16 +520,16 @@ scan_part_apply(float *__restrict__ st, const float *__restrict__ tot, int NC, i
 // sum_a (q_a.k_a)^2 for M_g, eps^2 m + eps s (|q|^2 + |k|^2) + s^2 sum_{a,b}
 // (q_a.k_b)^2 for Sigma_g (Sec. 4.1, reduced PSD families; qn, kn the squared
 // norms), the plain dot of the transformed vectors for the orthant map.
-template <bool kFull>
+template <int KIND>
 __device__ __forceinline__ void weight_tile(const float *qsT, const float *ksT, const float *qn,
                                             const float *kn, int C, int d, const MapSpec &mp,
                                             int r0, int s, float (&p)[kTM][2]) {
-    const int g = kFull ? 1 : (mp.kind == 1 || mp.kind == 2) ? mp.g : 1, m = d / g;
-    const bool sq = kFull || mp.kind != 3;
+    const int g = KIND >= 0 ? 1 : (mp.kind == 1 || mp.kind == 2) ? mp.g : 1, m = d / g;
+    const bool sq = KIND == 0 || (KIND < 0 && mp.kind != 3);
 #pragma unroll
     for (int i = 0; i < kTM; ++i) p[i][0] = p[i][1] = 0.f;
     for (int a = 0; a < g; ++a) {
-        const int blo = (!kFull && mp.kind == 2) ? 0 : a, bhi = (!kFull && mp.kind == 2) ? g : a + 1;
+        const int blo = (KIND < 0 && mp.kind == 2) ? 0 : a, bhi = (KIND < 0 && mp.kind == 2) ? g : a + 1;
         for (int b = blo; b < bhi; ++b) {
             float pa[kTM][2] = {};
             const float *qp = qsT + (size_t)(a * m) * C + r0;
@@ -550,7 +552,7 @@ __device__ __forceinline__ void weight_tile(const float *qsT, const float *ksT, 
                 for (int u = 0; u < 2; ++u) p[r][u] += sq ? pa[r][u] * pa[r][u] : pa[r][u];
         }
     }
-    if (!kFull && mp.kind == 2) {
+    if (KIND < 0 && mp.kind == 2) {
 #pragma unroll
         for (int r = 0; r < kTM; ++r)
 #pragma unroll
@@ -565,7 +567,7 @@ __device__ __forceinline__ void weight_tile(const float *qsT, const float *ksT, 
 // keys in 32-key slabs from the last to the first.  Gated: psi(q_r) scaled by
 // pre_r and the weight of key s <= r by prod_{u=s+1}^{r} gamma_u, a running
 // product per row walked from s = r down (carried across the key slabs).
-template <typename T, bool kGated, int TM, bool kFull>
+template <typename T, bool kGated, int TM, int KIND>
 __global__ void __maxnreg__(112)
 tiled_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     const float *__restrict__ gamma, const float *__restrict__ st,
@@ -664,7 +666,7 @@ tiled_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
                     const int ij = fij[f];
                     const float fa = fA[f], fb = fB[f];
                     for (int r = lane; r < C; r += 32) {
-                        float x = psi_at<kFull>(qsT + r, C, ij, fa, fb, terms, step, orth);
+                        float x = psi_at<KIND>(qsT + r, C, ij, fa, fb, terms, step, orth);
                         if (kGated) x *= pre[r];
                         arow[r] = x;
                     }
@@ -676,7 +678,7 @@ tiled_output_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             for (int tile = threadIdx.x; tile < (C / kTM) * (kKS / 2); tile += blockDim.x) {
                 const int r0 = (tile / (kKS / 2)) * kTM, kp = tile % (kKS / 2), s = s0 + 2 * kp;
                 float p[kTM][2];
-                weight_tile<kFull>(qsT, ksT, qn, kn, C, d, mp, r0, s, p);
+                weight_tile<KIND>(qsT, ksT, qn, kn, C, d, mp, r0, s, p);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     float m8[kTM];
@@ -758,11 +760,12 @@ cudaError_t state_launch(const FwdShape &s, const T *k, const T *v, const float 
     const size_t smem = sizeof(float) * ((size_t)s.C * s.d + 2 * kKS * FT + 2 * kKS * kSlabCols +
                                          2 * kKS + 3 * s.C + 3 * (size_t)n) +
                         sizeof(T) * (size_t)s.C * kSlabCols;
-    // the full map (and every gated call) with its feature and weight forms fixed at
-    // compile time; the reduced and orthant maps read the map at run time
-    auto kern = gamma          ? tiled_state_kernel<T, true, true>
-                : mp.kind == 0 ? tiled_state_kernel<T, false, true>
-                               : tiled_state_kernel<T, false, false>;
+    // the full map (and every gated call) and the orthant map with their feature and
+    // weight forms fixed at compile time; the reduced maps read the map at run time
+    auto kern = gamma          ? tiled_state_kernel<T, true, 0>
+                : mp.kind == 0 ? tiled_state_kernel<T, false, 0>
+                : mp.kind == 3 ? tiled_state_kernel<T, false, 3>
+                               : tiled_state_kernel<T, false, -1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     TraceScope tr(stage, stream);
     kern<<<dim3(NC, BH, ncs), block_threads(ng, ncg), smem, stream>>>(
@@ -782,9 +785,10 @@ cudaError_t output_launch(const FwdShape &s, const T *q, const T *k, const T *v,
                         sizeof(T) * (size_t)s.C * kSlabCols;
     // 8-row thread tiles for every chunk length: 4 x 4 tiles (twice the threads
     // at C = 64) measured slower, bound by the shared-memory loads
-    auto kern = gamma          ? tiled_output_kernel<T, true, kTM, true>
-                : mp.kind == 0 ? tiled_output_kernel<T, false, kTM, true>
-                               : tiled_output_kernel<T, false, kTM, false>;
+    auto kern = gamma          ? tiled_output_kernel<T, true, kTM, 0>
+                : mp.kind == 0 ? tiled_output_kernel<T, false, kTM, 0>
+                : mp.kind == 3 ? tiled_output_kernel<T, false, kTM, 3>
+                               : tiled_output_kernel<T, false, kTM, -1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     TraceScope tr(stage, stream);
     kern<<<dim3(NC, BH, ncs), block_threads(s.C / kTM, ncg), smem, stream>>>(
