@@ -757,6 +757,8 @@ cudaError_t state_launch(const FwdShape &s, const T *k, const T *v, const float 
     const int ncs = (s.dv + kSlabCols - 1) / kSlabCols;
     const int ncg = (s.dv < kSlabCols ? s.dv : kSlabCols) / kTN;
     const int FT = ng * kTM;
+    const int threads = block_threads(ng, ncg);
+    if (threads > kMaxThreads) return cudaErrorInvalidConfiguration;   // the 112-register budget
     const size_t smem = sizeof(float) * ((size_t)s.C * s.d + 2 * kKS * FT + 2 * kKS * kSlabCols +
                                          2 * kKS + 3 * s.C + 3 * (size_t)n) +
                         sizeof(T) * (size_t)s.C * kSlabCols;
@@ -768,7 +770,7 @@ cudaError_t state_launch(const FwdShape &s, const T *k, const T *v, const float 
                                : tiled_state_kernel<T, false, -1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     TraceScope tr(stage, stream);
-    kern<<<dim3(NC, BH, ncs), block_threads(ng, ncg), smem, stream>>>(
+    kern<<<dim3(NC, BH, ncs), threads, smem, stream>>>(
         k, v, gamma, st, cgate, s.T, s.d, s.dv, s.C, n, NC, ntile, ng, mp);
     return cudaGetLastError();
 }
@@ -780,6 +782,8 @@ cudaError_t output_launch(const FwdShape &s, const T *q, const T *k, const T *v,
     const int n = mp.n(s.d), NC = s.NC(), BH = s.BH();
     const int ncs = (s.dv + kSlabCols - 1) / kSlabCols;
     const int ncg = (s.dv < kSlabCols ? s.dv : kSlabCols) / kTN;
+    const int threads = block_threads(s.C / kTM, ncg);
+    if (threads > kMaxThreads) return cudaErrorInvalidConfiguration;   // the 112-register budget
     const size_t smem = sizeof(float) * (2 * (size_t)s.d * s.C + 2 * kKS * s.C +
                                          2 * kKS * kSlabCols + 2 * kKS + 7 * s.C + 3 * (size_t)n) +
                         sizeof(T) * (size_t)s.C * kSlabCols;
@@ -791,7 +795,7 @@ cudaError_t output_launch(const FwdShape &s, const T *q, const T *k, const T *v,
                                : tiled_output_kernel<T, false, kTM, -1>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     TraceScope tr(stage, stream);
-    kern<<<dim3(NC, BH, ncs), block_threads(s.C / kTM, ncg), smem, stream>>>(
+    kern<<<dim3(NC, BH, ncs), threads, smem, stream>>>(
         q, k, v, gamma, st, out, s.T, s.d, s.dv, s.C, n, NC, mp, normalize);
     return cudaGetLastError();
 }
