@@ -296,6 +296,22 @@ int kata_fwd(const void *q, const void *k, const void *v, void *out, int B, int 
 int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype);
 
 /*
+ * kata_fwd_gated -- GatedKATA in whichever exact form is faster for the shape:
+ * the gated quadratic form (kata_fwd_quadratic_gated) where it is supported and
+ * T <= 32768, else the gated chunked form (kata_fwd_chunked_gated, no state
+ * export).  The bound comes from the measured per-token costs of both forms on
+ * GB300: the quadratic form's grows with T, the chunked form's does not, and
+ * at T = 32768 the quadratic form is still at least ~2x faster.  Arguments,
+ * layouts, ownership and errors as kata_fwd_chunked_gated with state = z = NULL
+ * (gamma [B][H][T] fp32 device; normalize 0 or 1).  kata_fwd_gated_form tells
+ * which form a shape takes (a kata_form value).
+ */
+int kata_fwd_gated(const void *q, const void *k, const void *v, const float *gamma, void *out,
+                   int B, int H, int T, int d, int dv, int C, int dtype, int normalize,
+                   kata_stream_t stream);
+int kata_fwd_gated_form(int B, int H, int T, int d, int dv, int C, int dtype);
+
+/*
  * kata_fwd_chunked_host -- the same forward with HOST buffers: allocates
  * device buffers from the stream-ordered pool, copies q, k, v host->device,
  * runs kata_fwd_chunked, copies out device->host and waits for `stream`.

@@ -49,7 +49,8 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_sync_status", "kata_fwd_chunked_noalloc", "kata_fwd_chunked_state",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
-            "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form")
+            "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form",
+            "kata_fwd_gated", "kata_fwd_gated_form")
 
 _lib = None
 
@@ -112,6 +113,10 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd.restype = i
         L.kata_fwd_form.argtypes = [i, i, i, i, i, i, i]
         L.kata_fwd_form.restype = i
+        L.kata_fwd_gated.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, i, vp]
+        L.kata_fwd_gated.restype = i
+        L.kata_fwd_gated_form.argtypes = [i, i, i, i, i, i, i]
+        L.kata_fwd_gated_form.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -320,6 +325,30 @@ def kata_fwd_chunked_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                       _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_chunked_gated")
     return (out, state, z) if with_state else out
+
+
+def kata_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, gamma: torch.Tensor,
+                   C: int, normalize: bool = True, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """GatedKATA in whichever exact form is faster for the shape (the quadratic form
+    on the tensor cores up to T = 32768 where supported, else chunked);
+    kata_fwd_gated_form tells which.  gamma: [B,H,T] float32."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (B, H, T):
+        raise TypeError("gamma must be float32 of shape [B, H, T]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    _contig(q, k, v, gamma, out)
+    rc = lib().kata_fwd_gated(q.data_ptr(), k.data_ptr(), v.data_ptr(), gamma.data_ptr(),
+                              out.data_ptr(), B, H, T, d, dv, int(C), _dtype_code(q.dtype),
+                              int(bool(normalize)), _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_gated")
+    return out
+
+
+def kata_fwd_gated_form(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
+    return int(lib().kata_fwd_gated_form(B, H, T, d, dv, C, _dtype_code(dtype)))
 
 
 def kata_fwd_quadratic_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -529,6 +529,36 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     return KATA_OK;
 }
 
+// GatedKATA in whichever exact form is faster for the shape.  Per token the
+// gated quadratic form costs work in proportion to T and the gated chunked form
+// (CUDA cores) a constant.  Measured per-token costs put them level near
+// T = 64k at d = 32 (8 ns chunked; the quadratic form 1 ns at T = 8192), higher at
+// d = 64.  Up to T = 32768 the quadratic form is at least ~2x faster.
+static constexpr int kGatedQuadraticMaxT = 32768;
+
+int kata_fwd_gated_form(int B, int H, int T, int d, int dv, int C, int dtype) {
+    if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_FORM_NONE;
+    DevInfo di;
+    if (device_info(di)) return KATA_FORM_NONE;
+    const FwdShape s{B, H, T, d, dv, 64, dtype};
+    return (kata::quad_supported(s, di.major, di.minor) && T <= kGatedQuadraticMaxT)
+               ? KATA_FORM_QUADRATIC
+               : KATA_FORM_CHUNKED;
+}
+
+int kata_fwd_gated(const void *q, const void *k, const void *v, const float *gamma, void *out,
+                   int B, int H, int T, int d, int dv, int C, int dtype, int normalize,
+                   kata_stream_t stream) {
+    if (!q || !k || !v || !gamma || !out) return KATA_ERR_ARG;
+    const int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    if (kata_fwd_gated_form(B, H, T, d, dv, C, dtype) == KATA_FORM_QUADRATIC)
+        return kata_fwd_quadratic_gated(q, k, v, gamma, out, B, H, T, d, dv, dtype, normalize,
+                                        stream);
+    return kata_fwd_chunked_gated(q, k, v, gamma, out, nullptr, nullptr, B, H, T, d, dv, C, dtype,
+                                  normalize, stream);
+}
+
 int kata_decode_step_gated(float *state, float *z, const void *q, const void *k, const void *v,
                            const float *gamma, void *out, int B, int H, int d, int dv,
                            int dtype, int normalize, kata_stream_t stream) {

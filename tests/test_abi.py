@@ -264,3 +264,14 @@ def test_fwd_auto_rejects_bad_arguments(L):
     assert L.kata_fwd(q, k, v, o, 1, 1, 0, 32, 64, 64, 1, None) == kg.KATA_ERR_ARG
     assert L.kata_fwd(q, k, v, o, 1, 1, 8, 24, 64, 64, 1, None) == kg.KATA_ERR_UNSUPPORTED
     assert L.kata_fwd_form(1, 1, 8, 24, 64, 64, 1) == kg.KATA_FORM_NONE
+
+
+def test_fwd_gated_auto_rejects_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, o, g = (FAKE * (i + 1) * 4096 for i in range(5))
+    assert L.kata_fwd_gated(0, k, v, g, o, 1, 1, 8, 32, 64, 64, 1, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd_gated(q, k, v, 0, o, 1, 1, 8, 32, 64, 64, 1, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd_gated(q, k, v, g, 0, 1, 1, 8, 32, 64, 64, 1, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd_gated(q, k, v, g, o, 1, 1, 0, 32, 64, 64, 1, 1, None) == kg.KATA_ERR_ARG
+    assert L.kata_fwd_gated(q, k, v, g, o, 1, 1, 8, 24, 64, 64, 1, 1, None) == kg.KATA_ERR_UNSUPPORTED
+    assert L.kata_fwd_gated_form(1, 1, 8, 24, 64, 64, 1) == kg.KATA_FORM_NONE

@@ -228,3 +228,25 @@ def test_gated_quadratic_full_size_sampled_rows(kg, normalize):
                                         normalize)
         worst = max(worst, slice_rel_err(to_f64(out[b, hh])[ts], ref))
     assert worst <= TOL[w.dtype], f"{worst:.3e}"
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dtype,form", [
+    (32, torch.bfloat16, "quadratic"),   # tensor-core quadratic form
+    (64, torch.bfloat16, "quadratic"),
+    (32, torch.float32, "chunked"),      # fp32: the chunked CUDA-core form
+])
+def test_gated_auto_form(kg, normalize, d, dtype, form):
+    """kata_fwd_gated takes the form kata_fwd_gated_form names, and either form
+    matches the oracle's gated forward."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=300, d=d, C=64, dtype=dtype)
+    want = {"quadratic": kg.KATA_FORM_QUADRATIC, "chunked": kg.KATA_FORM_CHUNKED}[form]
+    assert kg.kata_fwd_gated_form(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == want
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out = kg.kata_fwd_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[w.dtype], f"{form} normalize={normalize}: {err:.3e}"
