@@ -72,13 +72,13 @@ def _intra_pairs(T, C):
 
 
 def tc_plan(w, num_sms: int):
-    """Segmentation the tensor path uses (mirrors plan() in csrc/kata_tc.cu):
-    128-token chunks, G segments of Lc chunks per head."""
+    """Segmentation of the d = 32 tensor path for workload w, as the library
+    reports it (kata_fwd_segments): 128-token chunks, G segments of Lc chunks per
+    head.  num_sms is the device's, which the library reads itself."""
     nct = -(-w.T // 128)
-    G = max(1, min(num_sms // (w.B * w.H), nct))
-    Lc = -(-nct // G)
-    G = -(-nct // Lc)
-    return nct, G, Lc
+    import kernelized_causal_linear_gb300 as kg
+    G, seg_tokens = kg.kata_fwd_segments(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
+    return nct, G, max(1, seg_tokens // 128)
 
 
 class FeatureMap:
@@ -137,7 +137,7 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         seg_tokens = min(T, (G - 1) * Lc * 128) * BH      # tokens in all but the last segments
         if stage == "tc_segment_state":
             return 2.0 * n * (dv + 1) * seg_tokens, "TFLOP/s", "tensor"
-        if stage == "tc_segment_output":
+        if stage in ("tc_segment_output", "tc_pair_output"):
             intra128 = 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, 128) * BH
             return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
         if stage == "tc_segment_scan":
@@ -178,6 +178,13 @@ def stage_dense_flops(stage: str, w, num_sms: int = SMS):
         per = (state + 4 * mma(128, 64, 128) + mma(128, 64, 16) + 4 * mma(128, 32, 32)
                + 4 * mma(128, 64, 32) + gram + mma(128, 32, 32))
         return per * nct * BH
+    if stage == "tc_pair_output":
+        # over the CTA pair: the 5 state blocks, psi_q S_pre over 4 full blocks and
+        # the 32-feature block, one Q K^T (M128 N128 K32), P V (M128 N64 K128), the
+        # Gram and Q G_pre
+        per = (state + 4 * mma(128, 64, 128) + mma(128, 64, 32) + mma(128, 128, 32)
+               + mma(128, 64, 128) + gram + mma(128, 32, 32))
+        return per * nct * BH
     if stage == "tc_segment_state":
         return (state + gram) * min(nct, (G - 1) * Lc) * BH
     if stage in ("tc_quadratic", "tc_quadratic_gated"):
@@ -199,7 +206,8 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 
 # the translation unit of each traced stage's kernel (its launch configuration
 # lives there too); every stage also depends on all the shared headers
-_STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
+_STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
+                 ("tc_sub_finalize", "kata_tc.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
                  ("gated", "kata_gated.cu"), ("decode", "kata_decode.cu"))

@@ -244,11 +244,18 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
  *
  * It allocates nothing.  Its scratch is one fixed device array of
  * KATA_NOALLOC_SCRATCH_BYTES (32 MiB) that is part of the library's device
- * image; it occupies that much memory on every GPU where this entry point has
- * run, until the process exits.  A shape whose scratch
- * (kata_fwd_workspace_size) is larger returns KATA_ERR_SCRATCH_LIMIT before
- * any device work: every bf16 shape of the tensor-core path fits on a 152-SM
- * GPU; fp32 shapes fit while B*H*ceil(T/C)*n*(dv+1)*4 bytes stay under it.
+ * image.  It is reserved when that device code is loaded: with the default
+ * lazy loading, at this entry point's first call on a device; with eager
+ * module loading (CUDA_MODULE_LOADING=EAGER), on every device context of the
+ * process.  It stays reserved until the process exits.
+ *
+ * It takes the kernel family kata_fwd_chunked takes for the shape (see
+ * kata_fwd_path) and needs the scratch kata_fwd_workspace_size reports; a
+ * shape that needs more than the array returns KATA_ERR_SCRATCH_LIMIT before
+ * any device work.  Every bf16 shape of the d = 32 tensor path fits on a
+ * 152-SM GPU.  The d = 64 tensor path needs about 1 KB per token and head
+ * (B*H*T up to roughly 32 K); the CUDA-core path needs
+ * B*H*(NC + NC/16 + 1)*n*(dv+1)*4 bytes with NC = ceil(T/C).
  *
  * The first call on each device (with that device current) looks up the
  * array's device address, which may load device code; make that first call
@@ -269,6 +276,16 @@ int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype
 /* Which implementation kata_fwd_chunked_map selects for this shape and map on
  * the current device (a kata_path value); KATA_PATH_NONE if it would reject it. */
 int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int map, int g);
+
+/* How kata_fwd_chunked cuts each head along the sequence on the current device:
+ * returns the number of segments (>= 1) and writes the tokens of every segment
+ * but the last to *seg_tokens (may be NULL); a negative kata_status for a shape
+ * it would reject.  Segments are processed in parallel, each starting from the
+ * exclusive prefix state of the segments before it ([KATA] Sec. 4.2, the scan
+ * over chunks); the CUDA-core and d = 64 paths use one segment of T tokens.
+ * For diagnostics and tests (the first rows after a segment start take the
+ * scanned state); no device work. */
+int kata_fwd_segments(int B, int H, int T, int d, int dv, int C, int dtype, int *seg_tokens);
 
 /* Which implementation kata_fwd_chunked selects for this shape on the current
  * device (a kata_path value); KATA_PATH_NONE if it would reject the call.

@@ -7,7 +7,7 @@ computes.  If libkata.so has not been built, every call raises -- there is no
 CPU fallback.
 
 Names follow the C ABI: kata_fwd_chunked, kata_decode_step, kata_lift,
-kata_fwd_chunked_host, kata_fwd_workspace_size, kata_fwd_path,
+kata_fwd_chunked_host, kata_fwd_workspace_size, kata_fwd_path, kata_fwd_segments,
 kata_feature_dim, kata_status_str.
 """
 from __future__ import annotations
@@ -50,7 +50,7 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
             "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form",
-            "kata_fwd_gated", "kata_fwd_gated_form")
+            "kata_fwd_gated", "kata_fwd_gated_form", "kata_fwd_segments")
 
 _lib = None
 
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_workspace_size.restype = i
         L.kata_fwd_path.argtypes = [i, i, i, i, i, i, i]
         L.kata_fwd_path.restype = i
+        L.kata_fwd_segments.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        L.kata_fwd_segments.restype = i
         L.kata_fwd_chunked_host.argtypes = [p, p, p, p, i, i, i, i, i, i, i, vp]
         L.kata_fwd_chunked_host.restype = i
         L.kata_decode_step.argtypes = [p, p, p, p, p, p, i, i, i, i, i, vp]
@@ -243,6 +245,15 @@ def kata_fwd_workspace_size(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
 
 def kata_fwd_path(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
     return int(lib().kata_fwd_path(B, H, T, d, dv, C, _dtype_code(dtype)))
+
+
+def kata_fwd_segments(B, H, T, d, dv, C, dtype: torch.dtype) -> tuple[int, int]:
+    """(segments per head, tokens per segment but the last) of kata_fwd_chunked."""
+    tok = ctypes.c_int(0)
+    n = int(lib().kata_fwd_segments(B, H, T, d, dv, C, _dtype_code(dtype), ctypes.byref(tok)))
+    if n < 0:
+        _check(n, "kata_fwd_segments")
+    return n, int(tok.value)
 
 
 def kata_decode_step(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.Tensor,

@@ -83,14 +83,16 @@ int device_info(DevInfo &out) {
 }
 
 // Kernel families behind the public paths: KATA_PATH_TC covers both tensor-core
-// variants (d = 32 with segments, d = 64 with the state split over four CTAs).
+// variants (d = 32 with segments, d = 64 with the state split over four CTAs);
+// kTc32Sub is KATA-M_2 at d = 64 as two d = 32 sub-heads.
 enum Kernels { kSimt, kTc32, kTc64, kTc32Sub };
 
+Kernels from_fwd(kata::FwdKernels k) {
+    return k == kata::FwdKernels::Tc32 ? kTc32 : k == kata::FwdKernels::Tc64 ? kTc64 : kSimt;
+}
+
 Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
-    if (s.dtype == KATA_F32) return kSimt;
-    if (kata::tc_supported(s, di.major, di.minor)) return kTc32;
-    if (kata::tc64_supported(s, di.major, di.minor, di.sms)) return kTc64;
-    return kSimt;
+    return from_fwd(kata::select_fwd_kernels(s, di.major, di.minor, di.sms));
 }
 
 // Kernels for a reduced map: KATA-M_2 at d = 64 is two d = 32 sub-heads on the
@@ -110,15 +112,46 @@ int select_path(const FwdShape &s, const DevInfo &di) {
     return select_kernels(s, di) == kSimt ? KATA_PATH_SIMT : KATA_PATH_TC;
 }
 
+kata::FwdKernels to_fwd(Kernels kn) {
+    return kn == kTc32 ? kata::FwdKernels::Tc32
+           : kn == kTc64 ? kata::FwdKernels::Tc64
+                         : kata::FwdKernels::Simt;
+}
+
 size_t workspace_for(const FwdShape &s, Kernels kn, const DevInfo &di, bool with_state = false) {
-    switch (kn) {
-        case kTc32: return kata::tc_workspace_bytes(s, di.sms, with_state);
-        case kTc64: return kata::tc64_workspace_bytes(s, with_state);
-        default: return kata::simt_workspace_bytes(s);
-    }
+    return kata::fwd_workspace_bytes(s, to_fwd(kn), di.sms, with_state);
 }
 
 }  // namespace
+
+namespace kata {
+
+FwdKernels select_fwd_kernels(const FwdShape &s, int cc_major, int cc_minor, int num_sms) {
+    if (s.dtype == KATA_F32) return FwdKernels::Simt;
+    if (tc_supported(s, cc_major, cc_minor)) return FwdKernels::Tc32;
+    if (tc64_supported(s, cc_major, cc_minor, num_sms)) return FwdKernels::Tc64;
+    return FwdKernels::Simt;
+}
+
+size_t fwd_workspace_bytes(const FwdShape &s, FwdKernels kn, int num_sms, bool with_state) {
+    switch (kn) {
+        case FwdKernels::Tc32: return tc_workspace_bytes(s, num_sms, with_state);
+        case FwdKernels::Tc64: return tc64_workspace_bytes(s, with_state);
+        default: return simt_workspace_bytes(s);
+    }
+}
+
+cudaError_t fwd_launch(const FwdShape &s, FwdKernels kn, const void *q, const void *k,
+                       const void *v, void *out, void *workspace, int num_sms,
+                       cudaStream_t stream, const StateOut &so) {
+    switch (kn) {
+        case FwdKernels::Tc32: return tc_forward(s, q, k, v, out, workspace, num_sms, stream, so);
+        case FwdKernels::Tc64: return tc64_forward(s, q, k, v, out, workspace, stream, so);
+        default: return simt_forward(s, q, k, v, out, workspace, stream, so);
+    }
+}
+
+}  // namespace kata
 
 extern "C" {
 
@@ -148,6 +181,17 @@ int kata_fwd_workspace_size(int B, int H, int T, int d, int dv, int C, int dtype
     const FwdShape s{B, H, T, d, dv, C, dtype};
     *bytes = workspace_for(s, select_kernels(s, di), di);
     return KATA_OK;
+}
+
+int kata_fwd_segments(int B, int H, int T, int d, int dv, int C, int dtype, int *seg_tokens) {
+    int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    DevInfo di;
+    if ((rc = device_info(di))) return rc;
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    if (select_kernels(s, di) == kTc32) return kata::tc_segments(s, di.sms, seg_tokens);
+    if (seg_tokens) *seg_tokens = T;
+    return 1;
 }
 
 int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype) {
@@ -190,9 +234,8 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
         return KATA_ERR_ALLOC;
     }
     cudaError_t e = kn == kTc32Sub ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
-                    : kn == kTc32   ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so)
-                    : kn == kTc64 ? kata::tc64_forward(s, q, k, v, out, ws, st, so)
-                                  : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
+                    : map.kind == 0 ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
+                                    : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -592,9 +635,10 @@ int kata_sync_status(kata_stream_t stream) {
         cudaGetLastError();
         return KATA_ERR_CUDA;
     }
-    const int e = kata::tc_take_error(), e64 = kata::tc64_take_error(), eq = kata::quad_take_error();
-    if (e < 0 || e64 < 0 || eq < 0) return KATA_ERR_CUDA;
-    return (e | e64 | eq) ? KATA_ERR_TIMEOUT : KATA_OK;
+    const int e = kata::tc_take_error(), e64 = kata::tc64_take_error(), eq = kata::quad_take_error(),
+              ep = kata::pair_take_error();
+    if (e < 0 || e64 < 0 || eq < 0 || ep < 0) return KATA_ERR_CUDA;
+    return (e | e64 | eq | ep) ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 
 int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int map, int g,

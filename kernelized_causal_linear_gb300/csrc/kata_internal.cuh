@@ -122,6 +122,10 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();
+int pair_take_error();
+// Segments per head of the d = 32 tensor path and the tokens in each (all but
+// the last); the output of a segment starts from the scan's prefix state.
+int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens);
 
 // ---- tcgen05 path at d = 64 (state split over four CTAs): kata_tc64.cu -----
 bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
@@ -130,6 +134,17 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
                          void *out, void *workspace, cudaStream_t stream,
                          const StateOut &so = StateOut{});
 int tc64_take_error();
+
+// ---- plain forward dispatch: kata_api.cu ------------------------------------
+// The kernel family a plain (full-map) chunked forward runs on, its workspace
+// size and its launch; shared by kata_fwd_chunked and kata_fwd_chunked_noalloc
+// so that both take the same path for the same shape.
+enum class FwdKernels { Simt, Tc32, Tc64 };
+FwdKernels select_fwd_kernels(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
+size_t fwd_workspace_bytes(const FwdShape &s, FwdKernels kn, int num_sms, bool with_state = false);
+cudaError_t fwd_launch(const FwdShape &s, FwdKernels kn, const void *q, const void *k,
+                       const void *v, void *out, void *workspace, int num_sms,
+                       cudaStream_t stream, const StateOut &so = StateOut{});
 
 // ---- quadratic (flash-style) forward: kata_quad.cu ------------------------
 bool quad_supported(const FwdShape &s, int cc_major, int cc_minor);

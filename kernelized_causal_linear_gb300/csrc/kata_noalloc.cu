@@ -10,13 +10,21 @@
 // stream-ordered pool.
 //
 // Properties a user must know:
-//   * Capacity: KATA_NOALLOC_SCRATCH_BYTES (32 MiB).  A shape whose scratch
-//     (kata_fwd_workspace_size) exceeds it is rejected with
-//     KATA_ERR_SCRATCH_LIMIT before any device work.  Every bf16 shape of the
-//     tensor-core path fits on a 152-SM GPU; fp32 shapes fit only while
-//     B*H*ceil(T/C)*n*(dv+1)*4 bytes stay under the limit.
-//   * The array occupies 32 MiB on every GPU where this entry point has run,
-//     until the process exits.
+//   * Path and capacity: the call takes the kernel family kata_fwd_chunked
+//     takes for the shape, and needs the scratch kata_fwd_workspace_size
+//     reports for it.  Capacity is KATA_NOALLOC_SCRATCH_BYTES (32 MiB); a
+//     shape that needs more is rejected with KATA_ERR_SCRATCH_LIMIT before any
+//     device work.  Every bf16 shape of the d = 32 tensor path fits on a
+//     152-SM GPU (its scratch is a few segment records per head).  The d = 64
+//     tensor path keeps fp32 partial numerators of every token (about 1 KB per
+//     token and head), so it fits up to roughly 32 K tokens x heads; the CUDA-
+//     core path keeps every chunk's state, B*H*(NC + NC/16 + 1)*n*(dv+1)*4
+//     bytes with NC = ceil(T/C).
+//   * Memory: the array is part of this library's device code.  It is
+//     reserved when that code is loaded on a device: under the default lazy
+//     loading, at this entry point's first call there; with eager module
+//     loading (CUDA_MODULE_LOADING=EAGER), on every device context the
+//     process creates.  It stays reserved until the process exits.
 //   * Set-up: the first call on each device (with that device current) looks
 //     up the array's device address with cudaGetSymbolAddress, which may load
 //     this part of the library's device code.  Make that first call before
@@ -109,14 +117,14 @@ extern "C" int kata_fwd_chunked_noalloc(const void *q, const void *k, const void
     if (rc) return rc;
     cudaGetLastError();
 
+    // the kernel family, and so the scratch size, kata_fwd_chunked takes for this shape
     const kata::FwdShape s{B, H, T, d, dv, C, dtype};
-    const bool tc = dtype == KATA_BF16 && kata::tc_supported(s, dev.major, dev.minor);
-    const size_t need = tc ? kata::tc_workspace_bytes(s, dev.sms) : kata::simt_workspace_bytes(s);
-    if (need > (size_t)KATA_NOALLOC_SCRATCH_BYTES) return KATA_ERR_SCRATCH_LIMIT;
+    const kata::FwdKernels kn = kata::select_fwd_kernels(s, dev.major, dev.minor, dev.sms);
+    if (kata::fwd_workspace_bytes(s, kn, dev.sms) > (size_t)KATA_NOALLOC_SCRATCH_BYTES)
+        return KATA_ERR_SCRATCH_LIMIT;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = tc ? kata::tc_forward(s, q, k, v, out, dev.scratch, dev.sms, st)
-                             : kata::simt_forward(s, q, k, v, out, dev.scratch, st);
+    const cudaError_t e = kata::fwd_launch(s, kn, q, k, v, out, dev.scratch, dev.sms, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_CUDA;

@@ -45,6 +45,9 @@
 // Chunk.  The tensor path uses 128-token chunks (the MMA tile height) for
 // every requested C; Eq. 17-20 give the same function for any chunk size, so
 // C only changes rounding.
+#include <cstdlib>
+#include <cstring>
+
 #include "kata_tc_common.cuh"
 
 namespace kata {
@@ -68,7 +71,7 @@ constexpr int kStateRing = 4;
 template <int D, int DV>
 __global__ void __launch_bounds__(352, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 float *__restrict__ seg, int NCt, int Lc, int G, int nsub) {
+                 float *__restrict__ seg, int NCt, int Lc, int m_pieces, int NR, int nsub) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int kStage = C::QK_TILE + C::V_TILE;
@@ -82,13 +85,20 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
-    const int g = blockIdx.x, bh = blockIdx.y;
+    // piece p of segment g: chunks g Lc + [p Lc / m, (p + 1) Lc / m) of the head
+    const int piece = blockIdx.x, bh = blockIdx.y;
+    const int g = piece / m_pieces, p = piece % m_pieces;
     // sub-head bh of nsub per head: columns D * (bh % nsub) .. of head bh / nsub
     const int hz = bh / nsub, hx = (bh % nsub) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c0 = g * Lc;
-    const int nch = min(NCt, c0 + Lc) - c0;
+    const int c0 = g * Lc + (p * Lc) / m_pieces;
+    const int nch = max(0, min(NCt, g * Lc + ((p + 1) * Lc) / m_pieces) - c0);
     const Sync sy{&abort_flag};
+    float *rec = seg + ((size_t)bh * NR + piece) * C::E;
+    if (nch == 0) {   // an empty piece (a short last segment) sums to zero
+        for (int e = threadIdx.x; e < C::E; e += blockDim.x) rec[e] = 0.f;
+        return;
+    }
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -200,7 +210,6 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const int quarter = warp & 3;
             const int lrow = quarter * 32 + lane;
             const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
-            float *rec = seg + ((size_t)bh * G + g) * C::E;
             for (int b = 0; b < C::NBLK; ++b) {
                 float4 *d4 = reinterpret_cast<float4 *>(rec + (size_t)(b * 128 + lrow) * DV);
                 uint32_t v[64];
@@ -283,8 +292,8 @@ template <int D, int DV, bool kSub>
 __global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
-                  const float *__restrict__ seg, int T, int NCt, int Lc, int G, int nsub,
-                  float *__restrict__ part) {
+                  const float *__restrict__ seg, int T, int NCt, int Lc, int m_pieces, int NR,
+                  int nsub, float *__restrict__ part) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
@@ -499,7 +508,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int row = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
         {   // initial state: the segment's exclusive prefix (zero for g == 0)
-            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
+            const float *pre = g > 0 ? seg + ((size_t)bh * NR + (size_t)g * m_pieces) * C::E : nullptr;
             for (int b = 0; b < NB; ++b) {
 #pragma unroll
                 for (int c = 0; c < DV; c += 8) {
@@ -685,7 +694,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         };
 
         {   // initial Gram: the segment's exclusive prefix (zero for g == 0)
-            const float *pre = g > 0 ? seg + ((size_t)bh * G + g) * C::E : nullptr;
+            const float *pre = g > 0 ? seg + ((size_t)bh * NR + (size_t)g * m_pieces) * C::E : nullptr;
             gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr);
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -759,21 +768,6 @@ state_export_kernel(const float *__restrict__ total, float *__restrict__ state,
 }
 
 // ================================================================= host side
-struct Plan {
-    int NCt, G, Lc;
-};
-
-Plan plan(const FwdShape &s, int num_sms) {
-    Plan p;
-    p.NCt = (s.T + kTile - 1) / kTile;
-    int G = num_sms / s.BH();
-    if (G < 1) G = 1;
-    if (G > p.NCt) G = p.NCt;
-    p.Lc = (p.NCt + G - 1) / G;
-    p.G = (p.NCt + p.Lc - 1) / p.Lc;
-    return p;
-}
-
 // Sub-heads (KATA-M_2 at d = 64): O = (N_0 + N_1) / (D_0 + D_1) in bf16 (zero
 // where the sum of denominators is not positive), summed in sub-head order.
 // part: N [BH * nsub][T][64] fp32, then D [BH * nsub][T].  One thread per four
@@ -829,12 +823,56 @@ size_t sub_part_floats(const FwdShape &ss, int nsub) {
 }
 }  // namespace
 
+namespace {
+// Segmentation: G segments of Lc chunks per head, each taken by `span` CTAs of
+// the output kernel (one, or a CTA pair) so that span G BH CTAs fill the SMs
+// once when BH is small.  The segment sums come from m pieces of each segment,
+// one state-kernel CTA per piece, so that the state kernel fills the SMs as
+// well.  Records: [BH][NR][E]: nsum m piece sums, plus (without the final
+// state) one record past them that receives the last segment's prefix; the
+// exclusive scan over them leaves segment g's prefix at record g m.
+struct Plan {
+    int NCt, G, Lc, m, nsum, NR;
+};
+
+Plan plan(const FwdShape &s, int num_sms, bool with_state, int span) {
+    Plan p;
+    p.NCt = (s.T + kTile - 1) / kTile;
+    int G = num_sms / (span * s.BH());
+    if (G < 1) G = 1;
+    if (G > p.NCt) G = p.NCt;
+    p.Lc = (p.NCt + G - 1) / G;
+    p.G = (p.NCt + p.Lc - 1) / p.Lc;
+    p.nsum = with_state ? p.G : p.G - 1;
+    p.m = p.nsum > 0 ? num_sms / (p.nsum * s.BH()) : 1;
+    if (p.m < 1) p.m = 1;
+    if (p.m > p.Lc) p.m = p.Lc;
+    p.NR = p.nsum > 0 ? p.nsum * p.m + (with_state ? 0 : 1) : 0;
+    return p;
+}
+
+// The CTA-pair output kernel (kata_tc_pair.cu) splits the feature blocks of a
+// segment over two SMs.  It is exact, but slower than the one-CTA kernel on
+// every measured shape, so it runs only when KATA_TC_OUTPUT=pair is set.
+bool use_pair(int nsub) {
+    if (nsub != 1) return false;
+    const char *e = getenv("KATA_TC_OUTPUT");
+    return e != nullptr && strcmp(e, "pair") == 0;
+}
+}  // namespace
+
 size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int nsub) {
     const FwdShape s = sub_shape(s0, nsub);
-    const Plan p = plan(s, num_sms);
-    // segment records (G of them), plus the inclusive totals when the state is exported
-    const size_t recs = with_state ? (size_t)p.G + 1 : (p.G <= 1 ? 0 : (size_t)p.G);
+    // piece records, plus the inclusive totals when the state is exported
+    const Plan p = plan(s, num_sms, with_state, use_pair(nsub) ? 2 : 1);
+    const size_t recs = (size_t)p.NR + (with_state ? 1 : 0);
     return sizeof(float) * (sub_part_floats(s, nsub) + (size_t)s.BH() * recs * Cfg<32, 64>::E);
+}
+
+int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens) {
+    const Plan p = plan(s, num_sms, false, use_pair(1) ? 2 : 1);
+    if (seg_tokens) *seg_tokens = p.Lc * kTile;
+    return p.G;
 }
 
 cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const void *v,
@@ -843,7 +881,8 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     using C = Cfg<32, 64>;
     if (nsub > 1 && so.state != nullptr) return cudaErrorInvalidValue;   // no sub-head state export
     const FwdShape s = sub_shape(s0, nsub);
-    const Plan p = plan(s, num_sms);
+    const bool with_state = so.state != nullptr, pair = use_pair(nsub);
+    const Plan p = plan(s, num_sms, with_state, pair ? 2 : 1);
     CUtensorMap mq, mk, mv;
     // q, k: rows of s0.d columns, read s.d at a time; v: one head's rows, shared by its sub-heads
     if (!make_map(mq, q, s0.d, s.T, s0.BH(), s.d) || !make_map(mk, k, s0.d, s.T, s0.BH(), s.d) ||
@@ -851,20 +890,18 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
         return cudaErrorInvalidValue;
     float *part = nsub > 1 ? static_cast<float *>(workspace) : nullptr;
     float *seg = static_cast<float *>(workspace) + sub_part_floats(s, nsub);
-    const bool with_state = so.state != nullptr;
     // Segment sums: of every segment but the last (the output kernel carries the
     // last one on chip), and of the last one too when the final state is wanted.
-    const int nsum = with_state ? p.G : p.G - 1;
-    if (nsum > 0) {
+    if (p.nsum > 0) {
         cudaFuncSetAttribute(seg_state_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(nsum, s.BH()), 352, kSmemState, stream>>>(
-                mk, mv, seg, p.NCt, p.Lc, p.G, nsub);
+            seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, s.BH()), 352, kSmemState, stream>>>(
+                mk, mv, seg, p.NCt, p.Lc, p.m, p.NR, nsub);
         }
-        float *totals = with_state ? seg + (size_t)s.BH() * p.G * C::E : nullptr;
-        cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.G, C::E, "tc_segment_scan", stream,
+        float *totals = with_state ? seg + (size_t)s.BH() * p.NR * C::E : nullptr;
+        cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.NR, C::E, "tc_segment_scan", stream,
                                               StateOut{}, 0, totals);
         if (e != cudaSuccess) return e;
         if (with_state) {
@@ -872,18 +909,24 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
             state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
         }
     }
+    if (pair) {
+        cudaError_t e = pair_output_launch(mq, mk, mv, out, seg, s.BH(), s.T, p.NCt, p.Lc, p.G, p.m,
+                                           p.NR, stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     {
         TraceScope tr("tc_segment_output", stream);
         if (part == nullptr) {
             cudaFuncSetAttribute(seg_output_kernel<32, 64, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
             seg_output_kernel<32, 64, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G, nsub, part);
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, part);
         } else {
             cudaFuncSetAttribute(seg_output_kernel<32, 64, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
             seg_output_kernel<32, 64, true><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.G, nsub, part);
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, part);
         }
     }
     if (part != nullptr) {

@@ -196,6 +196,96 @@ __device__ __forceinline__ void lift_block(int b, int part, const PackedRow<32> 
     }
 }
 
+// ---- the same layout lifted into registers, half a block (one 64-feature atom
+// column, 32 bf16 pairs) at a time: word 4p + m of half h is the pair m of chunk
+// position 8h + p.  The pair kernel stores these words in TMEM as the A operand
+// of its output MMAs (token t = TMEM lane t).
+
+// Rectangle (X,Y) into words 0..31 (chunk positions 0..7 of the half).
+template <int X, int Y>
+__device__ __forceinline__ void rect_regs(const PackedRow<32> &r, uint32_t f, uint32_t (&w)[32]) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const uint32_t bc = bmul2(__byte_perm(r.w[4 * X + (a >> 1)], 0u, (a & 1) ? 0x3232 : 0x1010), f);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) w[4 * a + m] = bmul2(bc, r.w[4 * Y + m]);
+    }
+}
+
+// Chunks CLO .. CHI-1 of group G's triangle at half positions P0 .. P0+CHI-CLO-1.
+template <int G, int CLO, int CHI, int P0, int... C>
+__device__ __forceinline__ void tri_regs_impl(const PackedRow<32> &r, uint32_t f, uint32_t (&w)[32],
+                                              std::integer_sequence<int, C...>) {
+    uint32_t so[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        so[k] = __byte_perm(r.w[4 * G + k], k < 3 ? r.w[4 * G + k + 1] : 0u, 0x5432);
+    ((w[4 * (P0 + C) + 0] = tri_word<G, 4 * (CLO + C) + 0>(r, so, f),
+      w[4 * (P0 + C) + 1] = tri_word<G, 4 * (CLO + C) + 1>(r, so, f),
+      w[4 * (P0 + C) + 2] = tri_word<G, 4 * (CLO + C) + 2>(r, so, f),
+      w[4 * (P0 + C) + 3] = tri_word<G, 4 * (CLO + C) + 3>(r, so, f)),
+     ...);
+}
+template <int G, int CLO, int CHI, int P0>
+__device__ __forceinline__ void tri_regs(const PackedRow<32> &r, uint32_t f, uint32_t (&w)[32]) {
+    tri_regs_impl<G, CLO, CHI, P0>(r, f, w, std::make_integer_sequence<int, CHI - CLO>{});
+}
+
+// Half HALF of block B (positions 8 HALF .. 8 HALF + 7); block 4 has only
+// positions 0..3 (words 0..15 of half 0; the rest are left unset).
+template <int B, int HALF>
+__device__ __forceinline__ void lift_half_regs(const PackedRow<32> &r, uint32_t f, uint32_t (&w)[32]) {
+    if constexpr (B < 3) {
+        constexpr int X2 = B == 0 ? 2 : 1, Y2 = B == 2 ? 2 : 3;
+        if constexpr (HALF == 0) rect_regs<0, B + 1>(r, f, w);
+        else rect_regs<X2, Y2>(r, f, w);
+    } else if constexpr (B == 3) {
+        if constexpr (HALF == 0) {
+            tri_regs<0, 0, 5, 0>(r, f, w);   // positions 0-4
+            tri_regs<1, 0, 3, 5>(r, f, w);   // positions 5-7
+        } else {
+            tri_regs<1, 3, 5, 0>(r, f, w);   // positions 8-9
+            tri_regs<2, 0, 5, 2>(r, f, w);   // positions 10-14
+            tri_regs<3, 0, 1, 7>(r, f, w);   // position 15
+        }
+    } else {
+        if constexpr (HALF == 0) tri_regs<3, 1, 5, 0>(r, f, w);   // positions 0-3
+    }
+}
+
+// The 4 words (8 features) of chunk position POS of block B, f the side factor.
+template <int B, int POS>
+__device__ __forceinline__ void chunk_words(const PackedRow<32> &r, uint32_t f, uint32_t *w4) {
+    if constexpr (B < 3) {
+        constexpr int X = POS < 8 ? 0 : (B == 0 ? 2 : 1);
+        constexpr int Y = POS < 8 ? B + 1 : (B == 2 ? 2 : 3);
+        constexpr int a = POS & 7;
+        const uint32_t bc = bmul2(__byte_perm(r.w[4 * X + (a >> 1)], 0u, (a & 1) ? 0x3232 : 0x1010), f);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) w4[m] = bmul2(bc, r.w[4 * Y + m]);
+    } else {
+        constexpr int G = B == 4 ? 3 : (POS < 15 ? POS / 5 : 3);
+        constexpr int c = B == 4 ? POS + 1 : (POS < 15 ? POS % 5 : 0);
+        uint32_t so[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            so[k] = __byte_perm(r.w[4 * G + k], k < 3 ? r.w[4 * G + k + 1] : 0u, 0x5432);
+        w4[0] = tri_word<G, 4 * c + 0>(r, so, f);
+        w4[1] = tri_word<G, 4 * c + 1>(r, so, f);
+        w4[2] = tri_word<G, 4 * c + 2>(r, so, f);
+        w4[3] = tri_word<G, 4 * c + 3>(r, so, f);
+    }
+}
+
+// Words of chunk positions 4Q .. 4Q+3 of block B (16 words).
+template <int B, int Q>
+__device__ __forceinline__ void lift_quarter_regs(const PackedRow<32> &r, uint32_t f, uint32_t (&w)[16]) {
+    chunk_words<B, 4 * Q + 0>(r, f, w + 0);
+    chunk_words<B, 4 * Q + 1>(r, f, w + 4);
+    chunk_words<B, 4 * Q + 2>(r, f, w + 8);
+    chunk_words<B, 4 * Q + 3>(r, f, w + 12);
+}
+
 // ---- the same layout lifted with the groups chosen at run time: one copy of
 // the rectangle and triangle code serves every block, which keeps the lift of
 // the output kernel (whose other roles already fill most of the instruction
@@ -288,6 +378,40 @@ __device__ __forceinline__ void lift_block_rt(int b, const PackedRow<32> &r, uin
     }
 }
 
+// The 4 words (8 features) of chunk position pos of block b, both chosen at run
+// time: called from a rolled loop it is one small copy of code for every block,
+// so that a kernel whose roles run many different loops keeps its lift code in
+// the instruction cache.
+__device__ __forceinline__ uint4 chunk_words_rt(int b, int pos, const PackedRow<32> &r, uint32_t f) {
+    uint4 o;
+    if (b < 3) {
+        const int h = pos >> 3, a = pos & 7;
+        const int X = h == 0 ? 0 : (b == 0 ? 2 : 1);
+        const int Y = h == 0 ? b + 1 : (b == 2 ? 2 : 3);
+        const Group8 gx = group8(r, X), gy = group8(r, Y);
+        const uint32_t bc = bmul2(__byte_perm(gx.w[a >> 1], 0u, (a & 1) ? 0x3232 : 0x1010), f);
+        o.x = bmul2(bc, gy.w[0]);
+        o.y = bmul2(bc, gy.w[1]);
+        o.z = bmul2(bc, gy.w[2]);
+        o.w = bmul2(bc, gy.w[3]);
+        return o;
+    }
+    const int g = b == 4 ? 3 : (pos < 15 ? pos / 5 : 3);
+    const int c = b == 4 ? pos + 1 : (pos < 15 ? pos % 5 : 0);
+    const Group8 gg = group8(r, g);
+    uint32_t so[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) so[k] = __byte_perm(gg.w[k], k < 3 ? gg.w[k + 1] : 0u, 0x5432);
+    switch (c) {
+        case 0: o = make_uint4(tri_word_rt<0>(gg, so, f), tri_word_rt<1>(gg, so, f), tri_word_rt<2>(gg, so, f), tri_word_rt<3>(gg, so, f)); break;
+        case 1: o = make_uint4(tri_word_rt<4>(gg, so, f), tri_word_rt<5>(gg, so, f), tri_word_rt<6>(gg, so, f), tri_word_rt<7>(gg, so, f)); break;
+        case 2: o = make_uint4(tri_word_rt<8>(gg, so, f), tri_word_rt<9>(gg, so, f), tri_word_rt<10>(gg, so, f), tri_word_rt<11>(gg, so, f)); break;
+        case 3: o = make_uint4(tri_word_rt<12>(gg, so, f), tri_word_rt<13>(gg, so, f), tri_word_rt<14>(gg, so, f), tri_word_rt<15>(gg, so, f)); break;
+        default: o = make_uint4(tri_word_rt<16>(gg, so, f), tri_word_rt<17>(gg, so, f), tri_word_rt<18>(gg, so, f), tri_word_rt<19>(gg, so, f)); break;
+    }
+    return o;
+}
+
 // Coordinates (i, j), i <= j, of feature p (0..127) of block b in the grouped
 // layout; false for a pad slot.  Used to export the state in the decode
 // layout, whose features are in row-major upper-triangle order.
@@ -326,19 +450,20 @@ __device__ __forceinline__ bool grouped_slot_pair(int b, int p, int &i, int &j) 
 // Row t of a [128 x D] bf16 tile written by TMA with the swizzle matching its
 // row width (32/64/128 bytes): the 16-byte chunk c of row t sits at chunk
 // c ^ ((t * row_bytes >> 7) & (chunks_per_row - 1)).
+// The loads are volatile: a caller releases the tile (an mbarrier arrive) right
+// after reading its row, and the TMA may then overwrite it; a non-volatile load
+// could legally be issued again later, where it would read the next tile.
 template <int D>
 __device__ __forceinline__ void tile_row_packed(const uint8_t *tile, int t, PackedRow<D> &r) {
     constexpr int RB = D * 2, CPR = RB / 16;
-    const uint8_t *row = tile + t * RB;
+    const uint32_t row = smem_u32(tile + t * RB);
     const int x = (t * RB >> 7) & (CPR - 1);
 #pragma unroll
-    for (int c = 0; c < CPR; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(row + ((c ^ x) << 4));
-        r.w[4 * c + 0] = u.x;
-        r.w[4 * c + 1] = u.y;
-        r.w[4 * c + 2] = u.z;
-        r.w[4 * c + 3] = u.w;
-    }
+    for (int c = 0; c < CPR; ++c)
+        asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r.w[4 * c + 0]), "=r"(r.w[4 * c + 1]), "=r"(r.w[4 * c + 2]), "=r"(r.w[4 * c + 3])
+                     : "r"(row + ((c ^ x) << 4))
+                     : "memory");
 }
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -403,4 +528,10 @@ bool make_map(CUtensorMap &m, const void *base, int inner, int T, int BH, int bo
 }
 
 }  // namespace
+
+// ---- the pair output kernel (kata_tc_pair.cu)
+cudaError_t pair_output_launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                               void *out, const float *seg, int BH, int T, int NCt, int Lc, int G,
+                               int m_pieces, int NR, cudaStream_t stream);
+
 }  // namespace kata

@@ -52,7 +52,8 @@ def _check_state(kg, w, expect_path=None):
 @pytest.mark.parametrize("B,H,T", [
     (1, 2, 1100),    # several segments per head, ragged last chunk
     (16, 8, 700),    # one segment per head
-    (4, 8, 4096),    # 4 segments of 8 chunks
+    (4, 8, 4096),    # 2 segments of 16 chunks, 4 pieces each
+    (1, 4, 5000),    # 14 segments of 3 chunks; the last has 1, so one of its pieces is empty
     (1, 1, 129),     # last chunk holds one token
     (3, 1, 5),       # a single partial chunk
 ])

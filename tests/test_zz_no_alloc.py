@@ -40,12 +40,16 @@ def _noalloc_raw(kg, q, k, v, out, C):
 @pytest.mark.parametrize("name,overrides", [
     ("long_ctx_bf16", dict(B=1, H=4, T=2000)),     # tensor-core path, 16 segments
     ("mid_bf16", dict(B=2, H=8, T=1500)),          # tensor-core path, C = 64
+    ("lm_layer_bf16", dict(B=1, H=38, T=300)),     # d = 64 tensor path (state over 4 CTAs)
+    ("lm_layer_bf16", dict(B=1, H=64, T=256)),     # d = 64 tensor path, ~17 MB of scratch
     ("small_fp32", dict()),                        # CUDA-core fp32 path
 ])
 def test_noalloc_matches_allocating_forward_twice(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)
     assert kg.kata_fwd_workspace_size(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) <= \
         kg.KATA_NOALLOC_SCRATCH_BYTES
+    if w.dtype == torch.bfloat16:   # the same kernel family as the allocating call
+        assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
     q1, k1, v1 = (t.cuda() for t in workloads.make_qkv(w))
     # a second, different batch: its call must not depend on what the first left behind
     q2, k2, v2 = (t.cuda() for t in workloads.make_qkv(w.scaled(index=w.index + 10)))
@@ -69,5 +73,19 @@ def test_noalloc_rejects_oversized_scratch(kg):
     out = torch.zeros(w.B, w.H, w.T, w.dv, device="cuda")
     assert _noalloc_raw(kg, q, k, v, out, w.C) == kg.KATA_ERR_SCRATCH_LIMIT
     assert "scratch" in kg.kata_status_str(kg.KATA_ERR_SCRATCH_LIMIT)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+def test_noalloc_rejects_oversized_d64_tensor_path(kg):
+    # the d = 64 tensor path keeps ~1 KB of fp32 partials per token and head:
+    # 64 heads x 1024 tokens need ~67 MB, more than the 32 MiB array
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=64, T=1024)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    assert kg.kata_fwd_workspace_size(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) > \
+        kg.KATA_NOALLOC_SCRATCH_BYTES
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    out = torch.zeros(w.B, w.H, w.T, w.dv, device="cuda", dtype=torch.bfloat16)
+    assert _noalloc_raw(kg, q, k, v, out, w.C) == kg.KATA_ERR_SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert torch.all(out == 0)
