@@ -152,6 +152,17 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     if stage == "tc_sub_finalize":
         # M_2 sub-heads: reads two fp32 numerators and denominators, writes bf16 out
         return float(BH * T) * (2 * (dv + 1) * 4 + dv * 2), "GB/s", "hbm"
+    # Sigma_2 finalize: 128-token chunk sums of v, |k|^2 v, |k|^2 (reads k, v, writes
+    # one record per chunk), their exclusive scan, and the pass that reads the four
+    # sub-heads' fp32 numerators and denominators with q, k, v and writes bf16 out
+    rec_sigma = 4.0 * (2 * dv + 4)
+    if stage == "tc_sigma_sums":
+        return float(BH * T) * (d + dv) * 2 + rec_sigma * -(-T // 128) * BH, "GB/s", "hbm"
+    if stage == "tc_sigma_scan":
+        return 2.0 * rec_sigma * -(-T // 128) * BH, "GB/s", "hbm"
+    if stage == "tc_sigma_finalize":
+        return (float(BH * T) * (4 * (dv + 1) * 4 + (2 * d + dv) * 2 + dv * 2)
+                + rec_sigma * -(-T // 128) * BH), "GB/s", "hbm"
     if stage == "tc64_output":
         intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH
         return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
@@ -161,15 +172,22 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     return None, "", ""
 
 
-def stage_dense_flops(stage: str, w, num_sms: int = SMS):
+def stage_dense_flops(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     """Tile-level flops a tensor-core launch executes (padding and masked halves
     included), for the kernels whose MMA tiles are fixed: per 128-token chunk the
     d = 32 output kernel runs 5 state blocks (M128 N64 K128), psi_q S_pre over 4
     full blocks and one 16-feature block, 4 Q K^T quarters (M128 N32 K32), 4 P V
     quarters (M128 N64 K32), the Gram (M128 N32 K128) and Q G_pre (M128 N32 K32);
     the state kernel the 5 state blocks and the Gram.  The quadratic kernels run
-    every (query tile, key tile <= it) pair as full 128 x 128 tiles."""
+    every (query tile, key tile <= it) pair as full 128 x 128 tiles.  The reduced
+    maps on the tensor path run d = 32 sub-heads: 2 per head for M_2, 4 for
+    Sigma_2 (whose segment sums need only the 2 key halves)."""
     BH, T, d, dv = w.B * w.H, w.T, w.d, w.dv
+    if fm.code in (1, 2) and fm.g == 2 and d == 64:
+        sub_w = w.scaled(B=w.B * (2 if fm.code == 1 else 4), d=32)
+        if stage == "tc_segment_state" and fm.code == 2:
+            sub_w = w.scaled(B=w.B * 2, d=32)
+        return stage_dense_flops(stage, sub_w, num_sms)
     mma = lambda m, n, k: 2.0 * m * n * k
     nct, G, Lc = tc_plan(w, num_sms)
     state = 5 * mma(128, 64, 128)
@@ -207,7 +225,7 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 # the translation unit of each traced stage's kernel (its launch configuration
 # lives there too); every stage also depends on all the shared headers
 _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
-                 ("tc_sub_finalize", "kata_tc.cu"),
+                 ("tc_sub_finalize", "kata_tc.cu"), ("tc_sigma", "kata_sigma.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
                  ("gated", "kata_gated.cu"), ("decode", "kata_decode.cu"))
@@ -651,7 +669,8 @@ def run_ours(args):
                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
                         "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
                         "work_per_launch": work}
-            dense = stage_dense_flops(dom, w, torch.cuda.get_device_properties(0).multi_processor_count)
+            dense = stage_dense_flops(dom, w, torch.cuda.get_device_properties(0).multi_processor_count,
+                                      fm)
             if dense is not None:   # what the tensor cores execute, beside the algorithmic work
                 roofline["dense_tflops"] = dense / mean_s / 1e12
                 roofline["dense_frac"] = dense / mean_s / 1e12 / peaks["bf16_tflops"]

@@ -160,11 +160,16 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   map, g: g in {1, 2, 4} dividing d; KATA_MAP_FULL and KATA_MAP_ORTHANT need g = 1.
  *   eps >= 0 and scale > 0, finite; KATA_MAP_FULL and KATA_MAP_BLOCK need
  *   eps = 0 and scale = 1 (KATA_ERR_ARG otherwise).
- * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  KATA-M_2
- * at d = 64 with bf16 inputs and dv = 64 runs on the tensor cores as two d = 32
- * sub-heads whose numerators and denominators add; the other reduced maps run
- * on CUDA cores in fp32 (bf16 inputs are widened; the output is written in the
- * input type).  kata_fwd_path_map tells which.
+ * Other arguments, layouts, scratch and errors as kata_fwd_chunked.  With bf16
+ * inputs, d = 64 and dv = 64, two maps run on the tensor cores as d = 32
+ * sub-heads whose fp32 numerators and denominators add:
+ *   KATA-M_2: two sub-heads, (q_a . k_a)^2 for a = 1, 2;
+ *   KATA-Sigma_2: four sub-heads, (q_a . k_b)^2 for every (a, b), scaled by
+ *   scale^2, plus the eps terms as a linear attention with the query features
+ *   (eps^2 m + eps scale |q|^2, eps scale) and the key features (1, |k|^2),
+ *   summed in fp32 in 128-token chunks.
+ * The other reduced maps run on CUDA cores in fp32 (bf16 inputs are widened;
+ * the output is written in the input type).  kata_fwd_path_map tells which.
  */
 int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
                          int T, int d, int dv, int C, int dtype, int map, int g, float eps,
@@ -396,6 +401,19 @@ int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int
  * is then incomplete), KATA_OK otherwise.  No counterpart in the paper.
  */
 int kata_sync_status(kata_stream_t stream);
+
+/*
+ * kata_test_arm_stall -- test hook for the failure path that kata_sync_status
+ * reports.  It arms a host-side flag that the next launch of the tensor path's
+ * segment-state kernel (a bf16 d = 32, dv = 64 call of kata_fwd_chunked that
+ * cuts its heads into two or more segments) consumes: that launch issues no
+ * tile loads, so every wait on the tiles runs out its bounded limit (about
+ * 2 s per wave of CTAs), the kernel leaves through its abort path with no
+ * copy or MMA in flight and its TMEM released, and the next kata_sync_status
+ * returns KATA_ERR_TIMEOUT.  That call's output is undefined; later calls are
+ * unaffected.  Returns KATA_OK.  No counterpart in the paper.
+ */
+int kata_test_arm_stall(void);
 
 /*
  * Tracing (no counterpart in the paper; measurement support).  Between

@@ -50,7 +50,8 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_chunked_map", "kata_lift_map", "kata_map_feature_dim",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
             "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form",
-            "kata_fwd_gated", "kata_fwd_gated_form", "kata_fwd_segments")
+            "kata_fwd_gated", "kata_fwd_gated_form", "kata_fwd_segments",
+            "kata_test_arm_stall")
 
 _lib = None
 
@@ -122,6 +123,8 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
+        L.kata_test_arm_stall.argtypes = []
+        L.kata_test_arm_stall.restype = i
         L.kata_trace_begin.argtypes = []
         L.kata_trace_begin.restype = i
         L.kata_trace_end.argtypes = [ctypes.POINTER(TraceStage), i, ctypes.POINTER(i)]
@@ -481,3 +484,10 @@ def kata_trace_end() -> dict:
 def kata_sync_status(stream=None) -> int:
     """Wait for the stream; KATA_ERR_TIMEOUT if a device-side bounded wait expired."""
     return int(lib().kata_sync_status(_stream_handle(stream, None)))
+
+
+def kata_test_arm_stall() -> None:
+    """Test hook: the next segment-state launch of the d = 32 tensor path issues
+    no tile loads, so its bounded waits expire and kata_sync_status reports
+    KATA_ERR_TIMEOUT for that call."""
+    _check(lib().kata_test_arm_stall(), "kata_test_arm_stall")

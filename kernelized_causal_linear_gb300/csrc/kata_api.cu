@@ -84,8 +84,9 @@ int device_info(DevInfo &out) {
 
 // Kernel families behind the public paths: KATA_PATH_TC covers both tensor-core
 // variants (d = 32 with segments, d = 64 with the state split over four CTAs);
-// kTc32Sub is KATA-M_2 at d = 64 as two d = 32 sub-heads.
-enum Kernels { kSimt, kTc32, kTc64, kTc32Sub };
+// kTc32Sub is KATA-M_2 at d = 64 as two d = 32 sub-heads, kTc32Sigma is
+// KATA-Sigma_2 at d = 64 as four crosswise d = 32 sub-heads plus its eps terms.
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma };
 
 Kernels from_fwd(kata::FwdKernels k) {
     return k == kata::FwdKernels::Tc32 ? kTc32 : k == kata::FwdKernels::Tc64 ? kTc64 : kSimt;
@@ -95,15 +96,18 @@ Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
     return from_fwd(kata::select_fwd_kernels(s, di.major, di.minor, di.sms));
 }
 
-// Kernels for a reduced map: KATA-M_2 at d = 64 is two d = 32 sub-heads on the
-// d = 32 tensor path (bf16, dv = 64); every other reduced map runs on CUDA cores.
+// Kernels for a reduced map: KATA-M_2 and KATA-Sigma_2 at d = 64 are d = 32
+// sub-heads on the d = 32 tensor path (bf16, dv = 64); every other reduced map
+// runs on CUDA cores.
 Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
                            bool with_state) {
     if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
-    if (map.kind == KATA_MAP_BLOCK && map.g == 2 && s.d == 64 && !with_state) {
+    if ((map.kind == KATA_MAP_BLOCK || map.kind == KATA_MAP_SUM) && map.g == 2 && s.d == 64 &&
+        !with_state) {
         FwdShape half = s;
         half.d = 32;
-        if (kata::tc_supported(half, di.major, di.minor)) return kTc32Sub;
+        if (kata::tc_supported(half, di.major, di.minor))
+            return map.kind == KATA_MAP_BLOCK ? kTc32Sub : kTc32Sigma;
     }
     return kSimt;
 }
@@ -224,18 +228,21 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
     const Kernels kn = select_map_kernels(s, di, map, with_state);
-    const size_t wsb = kn == kTc32Sub ? kata::tc_workspace_bytes(s, di.sms, false, 2)
-                       : map.kind == 0 ? workspace_for(s, kn, di, with_state)
-                                       : kata::simt_workspace_bytes(s, map);
+    const size_t wsb = kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
+                       : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
+                       : map.kind == 0    ? workspace_for(s, kn, di, with_state)
+                                          : kata::simt_workspace_bytes(s, map);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
-    cudaError_t e = kn == kTc32Sub ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
-                    : map.kind == 0 ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
-                                    : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
+    cudaError_t e =
+        kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
+        : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
+        : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
+                           : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -639,6 +646,11 @@ int kata_sync_status(kata_stream_t stream) {
               ep = kata::pair_take_error();
     if (e < 0 || e64 < 0 || eq < 0 || ep < 0) return KATA_ERR_CUDA;
     return (e | e64 | eq | ep) ? KATA_ERR_TIMEOUT : KATA_OK;
+}
+
+int kata_test_arm_stall(void) {
+    kata::tc_arm_stall();
+    return KATA_OK;
 }
 
 int kata_lift_map(const void *x, float *phi, int64_t rows, int d, int dtype, int map, int g,

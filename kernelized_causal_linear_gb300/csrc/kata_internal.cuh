@@ -114,14 +114,25 @@ cudaError_t gated_forward(const FwdShape &s, const void *q, const void *k, const
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
 // nsub > 1: the head's q/k columns are nsub sub-heads of width d / nsub, each run
 // as a d / nsub head (KATA-M_2 at d = 64); their numerators and denominators are
-// summed.  No state export then.
-size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false, int nsub = 1);
+// summed.  No state export then.  sigma (KATA-Sigma_2 at d = 64, nsub = 4): the
+// four sub-heads pair query half a with key half b, and the map's eps terms are
+// added in the finalize pass (kata_sigma.cu).
+size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false, int nsub = 1,
+                          const MapSpec *sigma = nullptr);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
-                       const StateOut &so = StateOut{}, int nsub = 1);
+                       const StateOut &so = StateOut{}, int nsub = 1,
+                       const MapSpec *sigma = nullptr);
+// KATA-Sigma_2 finalize (kata_sigma.cu): the scratch it needs after the
+// sub-head partials, and the pass that sums them with the eps terms.
+size_t sigma_workspace_bytes(const FwdShape &s);
+cudaError_t sigma_finalize_launch(const FwdShape &s, const float *part, float *ws, const void *q,
+                                  const void *k, const void *v, void *out, const MapSpec &map,
+                                  cudaStream_t stream);
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();
+void tc_arm_stall();   // test hook: the next segment-state launch issues no loads
 int pair_take_error();
 // Segments per head of the d = 32 tensor path and the tokens in each (all but
 // the last); the output of a segment starts from the scan's prefix state.

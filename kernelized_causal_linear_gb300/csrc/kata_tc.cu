@@ -45,6 +45,7 @@
 // Chunk.  The tensor path uses 128-token chunks (the MMA tile height) for
 // every requested C; Eq. 17-20 give the same function for any chunk size, so
 // C only changes rounding.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -67,11 +68,15 @@ __device__ __forceinline__ void flag_error(int code) { atomicOr(&g_tc_error, cod
 //     the tensor pipe: warp 1 the Gram and state blocks 0-1, warp 2 blocks 2-4
 //   warps 3-10: key lift into a 4-slot ring (two warps per 32 tokens, each
 //   lifting half of every block), then the epilogue (warps 3-6)
+// stall (a test hook): the producer issues no tile loads, so every wait on the
+// tiles expires and the kernel leaves through its abort path with no copy or
+// MMA in flight.
 constexpr int kStateRing = 4;
 template <int D, int DV>
 __global__ void __launch_bounds__(352, 1)
 seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 float *__restrict__ seg, int NCt, int Lc, int m_pieces, int NR, int nsub) {
+                 float *__restrict__ seg, int NCt, int Lc, int m_pieces, int NR, int nsub,
+                 int stall) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int kStage = C::QK_TILE + C::V_TILE;
@@ -125,7 +130,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (warp == 0) {
         // ---------------- TMA producer
         if (elect_lane0()) {
-            for (int i = 0; i < nch; ++i) {
+            for (int i = 0; i < (stall ? 0 : nch); ++i) {
                 const int st = i & 1, use = i >> 1;
                 if (use >= 1 && !sy.wait(&tile_empty[st], use - 1)) break;
                 uint8_t *tk = sm + st * kStage;
@@ -286,14 +291,17 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
 //     token's row of one side (query or key) into both atom columns of a block
 // TMEM: S_run [0,320) | G [320,352) | Q G_pre [352,384) | Q K^T quarter [384,416) |
 //       P slots [416,432) [432,448) | output accumulator [448,512)
-// kSub: sub-head form (KATA-M_2): the epilogue writes the fp32 numerator and the
-// denominator for sub_finalize_kernel instead of O.
+// kSub: sub-head form (KATA-M_2, KATA-Sigma_2): the epilogue writes the fp32
+// numerator and the denominator of the sub-head for a finalize pass instead of O.
+// cross: the nsub = 4 sub-heads of a head pair query half j / 2 with key half
+// j % 2 (KATA-Sigma_2); otherwise sub-head j takes half j of both.  The segment
+// prefixes then come from the key half's records (2 per head).
 template <int D, int DV, bool kSub>
 __global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
                   const float *__restrict__ seg, int T, int NCt, int Lc, int m_pieces, int NR,
-                  int nsub, float *__restrict__ part) {
+                  int nsub, int cross, float *__restrict__ part) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
@@ -320,7 +328,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     const int g = blockIdx.x, bh = blockIdx.y;
     // sub-head bh of nsub per head: q/k columns D * (bh % nsub) .. of head bh / nsub
-    const int hz = bh / nsub, hx = (bh % nsub) * D;
+    const int hz = bh / nsub, j = bh % nsub;
+    const int qx = (cross ? j >> 1 : j) * D, kx = (cross ? j & 1 : j) * D;
+    const int sbh = cross ? hz * 2 + (j & 1) : bh;   // records of this sub-head's keys
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
@@ -365,12 +375,12 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
                 mbar_arrive_expect_tx(&chunk_full[st], 2 * C::QK_TILE + C::V_TILE);
-                tma_load_3d(tq, &tm_q, hx, t0, hz, &chunk_full[st]);
-                tma_load_3d(tk, &tm_k, hx, t0, hz, &chunk_full[st]);
+                tma_load_3d(tq, &tm_q, qx, t0, hz, &chunk_full[st]);
+                tma_load_3d(tk, &tm_k, kx, t0, hz, &chunk_full[st]);
                 tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, hz, &chunk_full[st]);
                 if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
-                    tma_prefetch_3d(&tm_q, hx, t0 + kTile, hz);
-                    tma_prefetch_3d(&tm_k, hx, t0 + kTile, hz);
+                    tma_prefetch_3d(&tm_q, qx, t0 + kTile, hz);
+                    tma_prefetch_3d(&tm_k, kx, t0 + kTile, hz);
                     tma_prefetch_3d(&tm_v, 0, t0 + kTile, hz);
                 }
             }
@@ -508,7 +518,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int row = quarter * 32 + lane;
         const uint32_t lsel = (uint32_t)(quarter * 32) << 16;
         {   // initial state: the segment's exclusive prefix (zero for g == 0)
-            const float *pre = g > 0 ? seg + ((size_t)bh * NR + (size_t)g * m_pieces) * C::E : nullptr;
+            const float *pre = g > 0 ? seg + ((size_t)sbh * NR + (size_t)g * m_pieces) * C::E : nullptr;
             for (int b = 0; b < NB; ++b) {
 #pragma unroll
                 for (int c = 0; c < DV; c += 8) {
@@ -694,7 +704,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         };
 
         {   // initial Gram: the segment's exclusive prefix (zero for g == 0)
-            const float *pre = g > 0 ? seg + ((size_t)bh * NR + (size_t)g * m_pieces) * C::E : nullptr;
+            const float *pre = g > 0 ? seg + ((size_t)sbh * NR + (size_t)g * m_pieces) * C::E : nullptr;
             gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr);
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -809,12 +819,15 @@ bool tc_supported(const FwdShape &s, int cc_major, int cc_minor) {
            encoder() != nullptr;
 }
 
+std::atomic<int> g_stall_next{0};   // test hook: stall the next segment-state launch
+
 namespace {
-// The shape the kernels see: nsub sub-heads of width d / nsub per head.
-FwdShape sub_shape(const FwdShape &s, int nsub) {
+// The shape the output kernel sees: nsub sub-heads per head, of width d / nsub,
+// or d / 2 when they pair the two halves crosswise (KATA-Sigma_2, nsub = 4).
+FwdShape sub_shape(const FwdShape &s, int nsub, bool cross = false) {
     FwdShape ss = s;
     ss.B = s.B * nsub;
-    ss.d = s.d / nsub;
+    ss.d = cross ? s.d / 2 : s.d / nsub;
     return ss;
 }
 // Sub-head partials (N and D, fp32) come first in the workspace, rounded to 256 bytes.
@@ -861,12 +874,17 @@ bool use_pair(int nsub) {
 }
 }  // namespace
 
-size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int nsub) {
-    const FwdShape s = sub_shape(s0, nsub);
-    // piece records, plus the inclusive totals when the state is exported
+size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int nsub,
+                          const MapSpec *sigma) {
+    const bool cross = sigma != nullptr;
+    const FwdShape s = sub_shape(s0, nsub, cross);
+    // piece records (of the key sub-heads: 2 per head when crosswise), plus the
+    // inclusive totals when the state is exported
     const Plan p = plan(s, num_sms, with_state, use_pair(nsub) ? 2 : 1);
     const size_t recs = (size_t)p.NR + (with_state ? 1 : 0);
-    return sizeof(float) * (sub_part_floats(s, nsub) + (size_t)s.BH() * recs * Cfg<32, 64>::E);
+    const size_t heads = cross ? (size_t)s0.BH() * 2 : (size_t)s.BH();
+    return sizeof(float) * (sub_part_floats(s, nsub) + heads * recs * Cfg<32, 64>::E) +
+           (cross ? sigma_workspace_bytes(s0) : 0);
 }
 
 int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens) {
@@ -877,10 +895,12 @@ int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens) {
 
 cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const void *v,
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
-                       const StateOut &so, int nsub) {
+                       const StateOut &so, int nsub, const MapSpec *sigma) {
     using C = Cfg<32, 64>;
     if (nsub > 1 && so.state != nullptr) return cudaErrorInvalidValue;   // no sub-head state export
-    const FwdShape s = sub_shape(s0, nsub);
+    const bool cross = sigma != nullptr;
+    if (cross && (nsub != 4 || s0.d != 64)) return cudaErrorInvalidValue;
+    const FwdShape s = sub_shape(s0, nsub, cross);
     const bool with_state = so.state != nullptr, pair = use_pair(nsub);
     const Plan p = plan(s, num_sms, with_state, pair ? 2 : 1);
     CUtensorMap mq, mk, mv;
@@ -890,6 +910,8 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
         return cudaErrorInvalidValue;
     float *part = nsub > 1 ? static_cast<float *>(workspace) : nullptr;
     float *seg = static_cast<float *>(workspace) + sub_part_floats(s, nsub);
+    // crosswise, the segment sums depend on the key half only: 2 per head
+    const int state_heads = cross ? s0.BH() * 2 : s.BH(), state_nsub = cross ? 2 : nsub;
     // Segment sums: of every segment but the last (the output kernel carries the
     // last one on chip), and of the last one too when the final state is wanted.
     if (p.nsum > 0) {
@@ -897,11 +919,11 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
                              kSmemState);
         {
             TraceScope tr("tc_segment_state", stream);
-            seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, s.BH()), 352, kSmemState, stream>>>(
-                mk, mv, seg, p.NCt, p.Lc, p.m, p.NR, nsub);
+            seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, state_heads), 352, kSmemState, stream>>>(
+                mk, mv, seg, p.NCt, p.Lc, p.m, p.NR, state_nsub, g_stall_next.exchange(0));
         }
         float *totals = with_state ? seg + (size_t)s.BH() * p.NR * C::E : nullptr;
-        cudaError_t e = scan_exclusive_launch(seg, s.BH(), p.NR, C::E, "tc_segment_scan", stream,
+        cudaError_t e = scan_exclusive_launch(seg, state_heads, p.NR, C::E, "tc_segment_scan", stream,
                                               StateOut{}, 0, totals);
         if (e != cudaSuccess) return e;
         if (with_state) {
@@ -921,13 +943,18 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
             cudaFuncSetAttribute(seg_output_kernel<32, 64, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
             seg_output_kernel<32, 64, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, part);
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part);
         } else {
             cudaFuncSetAttribute(seg_output_kernel<32, 64, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
             seg_output_kernel<32, 64, true><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, part);
+                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part);
         }
+    }
+    if (cross) {
+        const size_t off = sub_part_floats(s, nsub) + (size_t)state_heads * p.NR * C::E;
+        return sigma_finalize_launch(s0, part, static_cast<float *>(workspace) + off, q, k, v, out,
+                                     *sigma, stream);
     }
     if (part != nullptr) {
         TraceScope tr("tc_sub_finalize", stream);
@@ -937,6 +964,8 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     }
     return cudaGetLastError();
 }
+
+void tc_arm_stall() { g_stall_next.store(1); }
 
 int tc_take_error() {
     int h = 0;

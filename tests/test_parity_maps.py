@@ -121,13 +121,69 @@ def test_m2_tensor_path(kg, B, H, T):
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
 
 
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # 8 sub-heads: 9 one-chunk segments (state kernel on the key halves + scan)
+    (8, 8, 700),     # 256 sub-heads, one segment each, ragged tail
+    (2, 3, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+])
+@pytest.mark.parametrize("eps,scale", [
+    (1e-4, 1.0),     # the Sigma_2 configuration
+    (0.5, 0.25),     # eps terms of the size of the (q_a . k_b)^2 terms
+    (3.0, 1.0),      # eps terms dominant
+])
+def test_sigma2_tensor_path(kg, B, H, T, eps, scale):
+    """KATA-Sigma_2 at d = 64 (bf16, dv = 64): four crosswise d = 32 sub-heads on
+    the tensor path plus the eps terms as a linear attention."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 2) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 2, 2, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 2, eps, scale)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+def test_sigma2_tensor_path_eps_only_rows(kg):
+    """Zero queries: <psi(0), psi(k)> = eps^2 m + eps s |k|^2, so those rows come
+    from the eps terms alone; zero keys in one half leave only the other half's
+    cross terms."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=2, T=300)
+    q, k, v = workloads.make_qkv(w)
+    q[:, :, ::3] = 0
+    k[:, :, 100:200, 32:] = 0
+    for eps, scale in ((1e-4, 1.0), (0.5, 0.25)):
+        out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 2, 2, eps, scale)
+        torch.cuda.synchronize()
+        ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 2, eps, scale)
+        assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype], (eps, scale)
+
+
+def test_sigma2_eps_zero_is_four_cross_terms(kg):
+    """eps = 0: the weight is scale^2 sum_{a,b} (q_a . k_b)^2, and the scale cancels."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=400)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked_map(q, k, v, w.C, 2, 2, 0.0, 1.0)
+    b = kg.kata_fwd_chunked_map(q, k, v, w.C, 2, 2, 0.0, 0.5)
+    torch.cuda.synchronize()
+    ref = oracle.forward_map(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), "Sigma", 2, 0.0, 1.0)
+    assert slice_rel_err(to_f64(a), ref) <= TOL[w.dtype]
+    assert slice_rel_err(to_f64(b), to_f64(a)) <= 1e-2
+
+
 def test_other_maps_take_cuda_cores(kg):
     w = workloads.WORKLOADS["lm_layer_bf16"]
-    for map_, g in ((1, 4), (2, 2), (2, 4)):
+    for map_, g in ((1, 4), (2, 4)):
         assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
             kg.KATA_PATH_SIMT
-    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, torch.float32, 1, 2) == \
-        kg.KATA_PATH_SIMT
+    for map_ in (1, 2):
+        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, 2) == \
+            kg.KATA_PATH_TC
+        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, torch.float32, map_, 2) == \
+            kg.KATA_PATH_SIMT
+        assert kg.kata_fwd_path_map(w.B, w.H, w.T, 32, w.dv, w.C, w.dtype, map_, 2) == \
+            kg.KATA_PATH_SIMT
 
 
 # ---- orthant map (psi_i = max(u_i, 0) + eps, n = d) and the two-level chunk scan
