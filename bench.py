@@ -137,7 +137,15 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         seg_tokens = min(T, (G - 1) * Lc * 128) * BH      # tokens in all but the last segments
         if stage == "tc_segment_state":
             return 2.0 * n * (dv + 1) * seg_tokens, "TFLOP/s", "tensor"
-        if stage in ("tc_segment_output", "tc_pair_output"):
+        # GatedKATA on the tensor path: the same contractions as the plain kernels;
+        # the piece prep reads and writes the scaled keys of the summed segments,
+        # the gated scan reads and writes the records with one multiplier each
+        if stage == "tc_gated_piece_prep":
+            return 2.0 * 2 * d * seg_tokens + 4.0 * nct * BH, "GB/s", "hbm"
+        if stage == "tc_gated_scan":
+            rec = 4.0 * (5 * 128 * dv + d * d)
+            return 2.0 * rec * G * BH, "GB/s", "hbm"
+        if stage in ("tc_segment_output", "tc_pair_output", "tc_segment_output_gated"):
             intra128 = 2.0 * (fm.intra_d(d) + dv + 1) * _intra_pairs(T, 128) * BH
             return state_flops + out_inter + intra128, "TFLOP/s", "tensor"
         if stage == "tc_segment_scan":
@@ -192,7 +200,7 @@ def stage_dense_flops(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_M
     nct, G, Lc = tc_plan(w, num_sms)
     state = 5 * mma(128, 64, 128)
     gram = mma(128, 32, 128)
-    if stage == "tc_segment_output":
+    if stage in ("tc_segment_output", "tc_segment_output_gated"):
         per = (state + 4 * mma(128, 64, 128) + mma(128, 64, 16) + 4 * mma(128, 32, 32)
                + 4 * mma(128, 64, 32) + gram + mma(128, 32, 32))
         return per * nct * BH
@@ -225,7 +233,8 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 # the translation unit of each traced stage's kernel (its launch configuration
 # lives there too); every stage also depends on all the shared headers
 _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
-                 ("tc_sub_finalize", "kata_tc.cu"), ("tc_sigma", "kata_sigma.cu"),
+                 ("tc_gated", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
+                 ("tc_sigma", "kata_sigma.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
                  ("gated", "kata_gated.cu"), ("decode", "kata_decode.cu"))
@@ -585,7 +594,7 @@ def run_ours(args):
         def fwd(q_, k_, v_, out_, g_=gate):
             kg.kata_fwd_quadratic_gated(q_, k_, v_, g_, out=out_)
     elif args.algo == "gated":
-        path = kg.KATA_PATH_SIMT
+        path = kg.kata_fwd_path_gated(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
 
         def fwd(q_, k_, v_, out_, g_=gate):
             kg.kata_fwd_chunked_gated(q_, k_, v_, g_, w.C, out=out_)

@@ -222,8 +222,17 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
  *   normalize = 0: out_t = psi(q_t)^T S_t (the no-denominator readout of the
  *                  pages' MQAR configuration).
  * Computed in the chunked form of Eq. 17-20 with the chunk's gate products
- * folded into the state, the scan and the output (CUDA cores, fp32 FFMA, for
- * fp32 and bf16 inputs).
+ * folded into the state, the scan and the output.  bf16 inputs with d = 32 and
+ * dv = 64 take the tensor cores (kata_fwd_path_gated reports which path a
+ * shape takes): the d = 32 segments of kata_fwd_chunked, with the keys scaled by
+ * the square root of the gates after them (to the end of their 128-token chunk
+ * for the running state, to the end of their piece for the segment sums, as
+ * bf16), the queries by the square root of the gates from their chunk's start,
+ * a gated segment scan, the running state and Gram decayed by each chunk's gate
+ * product in TMEM, and the intra-chunk weights multiplied by 2^(l_t - l_s) from
+ * the chunk-local cumulative log2 of the gates (a gate below 2^-126 counts as
+ * 2^-126 there: a zero gate leaves a weight of at most 2^-126 on the writes
+ * before it within the chunk).  Other shapes run on CUDA cores in fp32 FFMA.
  *
  *   gamma    [B][H][T] fp32 device, read only, 16-byte aligned; values in [0, 1]
  *            (not checked on the device: other values give the recurrence's
@@ -238,6 +247,11 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
 int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const float *gamma,
                            void *out, float *state, float *z, int B, int H, int T, int d, int dv,
                            int C, int dtype, int normalize, kata_stream_t stream);
+
+/* kata_fwd_path_gated -- the path kata_fwd_chunked_gated takes for a shape:
+ * KATA_PATH_TC (tensor cores), KATA_PATH_SIMT (CUDA cores) or KATA_PATH_NONE
+ * (invalid shape or no device). */
+int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype);
 
 /*
  * kata_fwd_chunked_noalloc -- the same forward as kata_fwd_chunked (same
@@ -320,10 +334,13 @@ int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype);
 /*
  * kata_fwd_gated -- GatedKATA in whichever exact form is faster for the shape:
  * the gated quadratic form (kata_fwd_quadratic_gated) where it is supported and
- * T <= 32768, else the gated chunked form (kata_fwd_chunked_gated, no state
- * export).  The bound comes from the measured per-token costs of both forms on
- * GB300: the quadratic form's grows with T, the chunked form's does not, and
- * at T = 32768 the quadratic form is still at least ~2x faster.  Arguments,
+ * T <= 10240 (d = 32) or T <= 65536 (d = 64), else the gated chunked form
+ * (kata_fwd_chunked_gated, no state export).  The bounds come from the
+ * measured per-token costs of both forms on GB300 (bf16, dv = 64): the
+ * quadratic form's grows with T (1.1 ns per token and head at T = 8192, 1.9 at
+ * 16384, d = 32); the chunked form's does not (1.3 ns at d = 32 on the tensor
+ * cores, ~35 ns at d = 64 on CUDA cores, where the quadratic form is faster up
+ * to the largest measured T = 65536).  Arguments,
  * layouts, ownership and errors as kata_fwd_chunked_gated with state = z = NULL
  * (gamma [B][H][T] fp32 device; normalize 0 or 1).  kata_fwd_gated_form tells
  * which form a shape takes (a kata_form value).

@@ -51,7 +51,7 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
             "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form",
             "kata_fwd_gated", "kata_fwd_gated_form", "kata_fwd_segments",
-            "kata_test_arm_stall")
+            "kata_test_arm_stall", "kata_fwd_path_gated")
 
 _lib = None
 
@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_gated.restype = i
         L.kata_fwd_gated_form.argtypes = [i, i, i, i, i, i, i]
         L.kata_fwd_gated_form.restype = i
+        L.kata_fwd_path_gated.argtypes = [i, i, i, i, i, i, i]
+        L.kata_fwd_path_gated.restype = i
         L.kata_fwd_chunked_state.restype = i
         L.kata_sync_status.argtypes = [vp]
         L.kata_sync_status.restype = i
@@ -363,6 +365,11 @@ def kata_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, gamma: tor
 
 def kata_fwd_gated_form(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
     return int(lib().kata_fwd_gated_form(B, H, T, d, dv, C, _dtype_code(dtype)))
+
+
+def kata_fwd_path_gated(B, H, T, d, dv, C, dtype: torch.dtype) -> int:
+    """Path kata_fwd_chunked_gated takes for a shape (a KATA_PATH_* value)."""
+    return int(lib().kata_fwd_path_gated(B, H, T, d, dv, C, _dtype_code(dtype)))
 
 
 def kata_fwd_quadratic_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -560,16 +560,20 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     if ((rc = device_info(di))) return rc;
     cudaGetLastError();
     const FwdShape s{B, H, T, d, dv, C, dtype};
+    const bool tc = kata::tc_supported(s, di.major, di.minor);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    if (cudaMallocAsync(&ws, kata::gated_workspace_bytes(s), st) != cudaSuccess) {
+    const size_t wsb = tc ? kata::tc_gated_workspace_bytes(s, di.sms, state != nullptr)
+                          : kata::gated_workspace_bytes(s);
+    if (cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
     kata::StateOut so;
     so.state = state;
     so.z = z;
-    cudaError_t e = kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
+    cudaError_t e = tc ? kata::tc_forward_gated(s, q, k, v, gamma, out, ws, di.sms, st, so, normalize)
+                       : kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
     const cudaError_t ef = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {
@@ -580,18 +584,28 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
 }
 
 // GatedKATA in whichever exact form is faster for the shape.  Per token the
-// gated quadratic form costs work in proportion to T and the gated chunked form
-// (CUDA cores) a constant.  Measured per-token costs put them level near
-// T = 64k at d = 32 (8 ns chunked; the quadratic form 1 ns at T = 8192), higher at
-// d = 64.  Up to T = 32768 the quadratic form is at least ~2x faster.
-static constexpr int kGatedQuadraticMaxT = 32768;
+// gated quadratic form costs work in proportion to T, the gated chunked form a
+// constant.  Measured on GB300 (bf16, dv = 64, per token and head): at d = 32
+// the chunked form runs on the tensor cores at 1.3 ns for every T, the
+// quadratic form at 1.10 ns at T = 8192 and 1.90 ns at T = 16384, so they level
+// near T = 10k; at d = 64 the chunked form runs on CUDA cores at ~35 ns and the
+// quadratic form is faster at every measured T (7.1 ns at T = 65536).
+static int gated_quadratic_max_t(int d) { return d == 32 ? 10240 : 65536; }
+
+int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype) {
+    if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_PATH_NONE;
+    DevInfo di;
+    if (device_info(di)) return KATA_PATH_NONE;
+    return kata::tc_supported(FwdShape{B, H, T, d, dv, C, dtype}, di.major, di.minor) ? KATA_PATH_TC
+                                                                                     : KATA_PATH_SIMT;
+}
 
 int kata_fwd_gated_form(int B, int H, int T, int d, int dv, int C, int dtype) {
     if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_FORM_NONE;
     DevInfo di;
     if (device_info(di)) return KATA_FORM_NONE;
     const FwdShape s{B, H, T, d, dv, 64, dtype};
-    return (kata::quad_supported(s, di.major, di.minor) && T <= kGatedQuadraticMaxT)
+    return (kata::quad_supported(s, di.major, di.minor) && T <= gated_quadratic_max_t(d))
                ? KATA_FORM_QUADRATIC
                : KATA_FORM_CHUNKED;
 }

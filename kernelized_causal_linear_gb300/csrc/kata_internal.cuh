@@ -123,6 +123,13 @@ cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const vo
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
                        const StateOut &so = StateOut{}, int nsub = 1,
                        const MapSpec *sigma = nullptr);
+// GatedKATA on the d = 32 tensor path (bf16, dv = 64): the same segments, with
+// the gates folded into the keys, a gated segment scan and the running state
+// decayed by each chunk's gate product.  normalize 0 drops the denominator.
+size_t tc_gated_workspace_bytes(const FwdShape &s, int num_sms, bool with_state);
+cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, const void *v,
+                             const float *gamma, void *out, void *workspace, int num_sms,
+                             cudaStream_t stream, const StateOut &so, int normalize);
 // KATA-Sigma_2 finalize (kata_sigma.cu): the scratch it needs after the
 // sub-head partials, and the pass that sums them with the eps terms.
 size_t sigma_workspace_bytes(const FwdShape &s);
@@ -165,6 +172,12 @@ cudaError_t quad_forward(const FwdShape &s, const void *q, const void *k, const 
                          void *out, cudaStream_t stream, const float *gamma = nullptr,
                          int normalize = 1, void *ws = nullptr);
 size_t quad_gated_workspace_bytes(const FwdShape &s);
+// Per 128-token chunk of every head: the keys scaled by the square root of the
+// gates after them to the end of their chunk (kp, bf16 [BH][T][d]), the
+// chunk-local inclusive cumulative log2 of the gates (lam2 [BH][T], a gate below
+// 2^-126 counted as 2^-126) and each chunk's gate product (gtile [BH][NC]).
+cudaError_t gate_prep_launch(const void *k, const float *gamma, void *kp, float *lam2, float *gtile,
+                             int BH, int T, int d, cudaStream_t stream);
 int quad_take_error();
 
 }  // namespace kata

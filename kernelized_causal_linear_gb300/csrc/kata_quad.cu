@@ -473,6 +473,20 @@ cudaError_t quad_launch(const FwdShape &s, const void *q, const void *k, const v
 
 }  // namespace
 
+cudaError_t gate_prep_launch(const void *k, const float *gamma, void *kp, float *lam2, float *gtile,
+                             int BH, int T, int d, cudaStream_t stream) {
+    if (d != 32 && d != 64) return cudaErrorInvalidValue;
+    const int NT = (T + kTile - 1) / kTile;
+    TraceScope tr("tc_gate_prep", stream);
+    if (d == 32)
+        gate_prep_kernel<32><<<dim3(NT, BH), kTile, 0, stream>>>((const bf16 *)k, gamma, (bf16 *)kp,
+                                                                  lam2, gtile, T, NT);
+    else
+        gate_prep_kernel<64><<<dim3(NT, BH), kTile, 0, stream>>>((const bf16 *)k, gamma, (bf16 *)kp,
+                                                                  lam2, gtile, T, NT);
+    return cudaGetLastError();
+}
+
 bool quad_supported(const FwdShape &s, int cc_major, int cc_minor) {
     return s.dtype == 1 && cc_major == 10 && cc_minor == 3 && (s.d == 32 || s.d == 64) &&
            s.dv == 64 && (s.T + kTile - 1) / kTile <= 65535 && encoder() != nullptr;

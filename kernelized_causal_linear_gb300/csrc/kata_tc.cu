@@ -249,11 +249,14 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // 64-feature atom columns of each block, through a 2-stage ring whose slots
 // are 64 KB apart.  Kept out of line so that its registers are allocated apart
 // from the other roles of the kernel.
+// lam2 (gated queries): the chunk-local cumulative log2 of the gates of this
+// head's tokens from chunk c0 on; the query row of token t is scaled by the
+// square root of the gates from its chunk's start to t before it is lifted.
 template <int D, int NB>
 __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
                                               int nch, uint64_t *chunk_full, uint64_t *qk_empty,
                                               uint64_t *block_ready, uint64_t *block_empty,
-                                              volatile int *abort) {
+                                              volatile int *abort, const float *lam2, int nvalid) {
     const Sync sy{abort};
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
@@ -263,6 +266,14 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
         tile_row_packed<D>(tile, t, r);
         __syncwarp();
         if (elect_lane0()) mbar_arrive(qk_empty);
+        if (lam2 != nullptr) {
+            const int ta = min(i * kTile + t, nvalid - 1);
+            const float sc = exp2f(0.5f * lam2[ta]);
+#pragma unroll
+            for (int m = 0; m < D / 2; ++m)
+                r.w[m] = pack_bf16(__uint_as_float(r.w[m] << 16) * sc,
+                                   __uint_as_float(r.w[m] & 0xFFFF0000u) * sc);
+        }
         for (int b = 0; b < NB && ok; ++b) {
             const int gb = i * NB + b, ls = gb & 1, use = gb >> 1;
             if (use >= 1) ok = __all_sync(0xffffffffu, sy.wait(&block_empty[ls], use - 1));
@@ -296,12 +307,26 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
 // cross: the nsub = 4 sub-heads of a head pair query half j / 2 with key half
 // j % 2 (KATA-Sigma_2); otherwise sub-head j takes half j of both.  The segment
 // prefixes then come from the key half's records (2 per head).
-template <int D, int DV, bool kSub>
+// kGated (GatedKATA, S_t = gamma_t S_{t-1} + psi(k_t) v_t^T): in chunk c with
+// gate product g_c, cumulative log2 gates l_t from the chunk's start, and a_s the
+// gates after s to the chunk's end,
+//   S_run <- g_c S_run + sum_s psi(sqrt(a_s) k_s) v_s^T   (keys from tm_kg),
+//   G     <- g_c G     + sum_s a_s k_s k_s^T,
+//   N_t = psi(sqrt(b_t) q_t) . S_pre + sum_{s<=t} 2^(l_t - l_s) (q_t . k_s)^2 v_s,
+//   D_t = b_t q_t^T G_pre q_t      + sum_{s<=t} 2^(l_t - l_s) (q_t . k_s)^2,
+// b_t = 2^l_t.  The convert warps decay S_run block by block as they read it,
+// the P warps decay G as they read it; O = N / D, or N when !normalize.
+struct OutGate {
+    const float *lam2;     // [BH][T] chunk-local cumulative log2 of the gates
+    const float *gchunk;   // [BH][NC] gate product of each 128-token chunk
+    int normalize;
+};
+template <int D, int DV, bool kSub, bool kGated>
 __global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, bf16 *__restrict__ out,
-                  const float *__restrict__ seg, int T, int NCt, int Lc, int m_pieces, int NR,
-                  int nsub, int cross, float *__restrict__ part) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kg,
+                  bf16 *__restrict__ out, const float *__restrict__ seg, int T, int NCt, int Lc,
+                  int m_pieces, int NR, int nsub, int cross, float *__restrict__ part, OutGate ga) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
@@ -312,7 +337,11 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t *sm = align1024(smem_raw);
     uint8_t *tq = sm;                                   // Q tile, 8 KB (64-byte swizzle)
     uint8_t *tk = sm + C::QK_TILE;                      // K tile, 8 KB
-    uint8_t *tv = sm + 2 * C::QK_TILE;                  // V tiles [2][16 KB]
+    // gated: the scaled K tile follows K.  The Gram MMA (M = 128, MN-major) reads
+    // its operand as four 8 KB atoms 8 KB apart, i.e. 24 KB past the tile it
+    // names, which here are the V tiles (the real rows are the first 32).
+    uint8_t *tkg = sm + 2 * C::QK_TILE;
+    uint8_t *tv = sm + (kGated ? 3 : 2) * C::QK_TILE;   // V tiles [2][16 KB]
     uint8_t *lring = tv + 2 * C::V_TILE;                // [2][psi_q 32 KB | psi_k 32 KB]
     uint8_t *spre = lring + 2 * 65536;                  // S_pre blocks [2][16 KB]
     uint8_t *gram = spre + 2 * 16384;                   // G_pre bf16, 2 KB
@@ -335,6 +364,10 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
     const Sync sy{&abort_flag};
+    // gated: this segment's cumulative log2 gates (valid for nvalid tokens) and chunk gate products
+    const float *lam2 = kGated ? ga.lam2 + (size_t)bh * T + (size_t)c0 * kTile : nullptr;
+    const float *gch = kGated ? ga.gchunk + (size_t)bh * NCt + c0 : nullptr;
+    const int nvalid = T - c0 * kTile;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -374,9 +407,11 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int st = i & 1, use = i >> 1;
                 if (i >= 1 && !sy.wait(&qk_empty, i - 1)) break;
                 if (use >= 1 && !sy.wait(&v_empty[st], use - 1)) break;
-                mbar_arrive_expect_tx(&chunk_full[st], 2 * C::QK_TILE + C::V_TILE);
+                mbar_arrive_expect_tx(&chunk_full[st],
+                                      (kGated ? 3 : 2) * C::QK_TILE + C::V_TILE);
                 tma_load_3d(tq, &tm_q, qx, t0, hz, &chunk_full[st]);
                 tma_load_3d(tk, &tm_k, kx, t0, hz, &chunk_full[st]);
+                if constexpr (kGated) tma_load_3d(tkg, &tm_kg, 0, t0, hz, &chunk_full[st]);
                 tma_load_3d(tv + st * C::V_TILE, &tm_v, 0, t0, hz, &chunk_full[st]);
                 if (i + 1 < nch) {   // warm L2 with the next chunk's tiles
                     tma_prefetch_3d(&tm_q, qx, t0 + kTile, hz);
@@ -474,7 +509,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (elect_lane0()) {
             constexpr uint32_t kIdGram = idesc_bf16(128, D, true, true);
             constexpr uint32_t kIdState = idesc_bf16(128, DV, true, true);
-            const uint64_t dKg = smem_desc(smem_u32(tk), 8192, 512, kSw64);     // MN-major (Gram)
+            const uint64_t dKg = smem_desc(smem_u32(kGated ? tkg : tk), 8192, 512, kSw64); // MN-major (Gram)
             const uint64_t dV0 = smem_desc(smem_u32(tv), 16384, 1024, kSw128);  // MN-major B
             const uint64_t dLk = smem_desc(smem_u32(lring + 32768), 16384, 1024, kSw128); // MN-major A
             bool ok = true;
@@ -543,10 +578,17 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 if (quarter * 32 < C::NF - b * 128) {   // rows past the real features are never read
                     const uint32_t srow = smem_u32(spre + ss * 16384 + (row >> 3) * 1024 + (row & 7) * 128);
+                    const float gc = kGated ? gch[i] : 1.f;
 #pragma unroll
                     for (int c32 = 0; c32 < DV; c32 += 32) {
                         uint32_t v[32];
                         tmem_ld32(tS + lsel + b * DV + c32, v);
+                        if constexpr (kGated) {   // S_run <- g_c S_run before this chunk's update
+                            uint32_t dv32[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) dv32[e] = __float_as_uint(__uint_as_float(v[e]) * gc);
+                            tmem_st32(tS + lsel + b * DV + c32, dv32);
+                        }
 #pragma unroll
                         for (int cc = 0; cc < 4; ++cc) {
                             const int chunk = (c32 >> 3) + cc;
@@ -558,6 +600,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         }
                     }
                     fence_proxy_async_smem();
+                    if constexpr (kGated) tmem_st_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -578,13 +621,26 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             uint32_t v[32];
             tmem_ld32(tXs + lsel, v);                 // warp-collective: always executed
+            // gated: key s weighs 2^(l_t - l_s) for query t (lane s % 32 holds l_s)
+            float lt = 0.f, lk = 0.f;
+            if constexpr (kGated) {
+                const int cb = (n >> 2) * kTile;
+                lt = lam2[min(cb + row, nvalid - 1)];
+                lk = lam2[min(cb + 32 * q + lane, nvalid - 1)];
+            }
             uint32_t pw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int s = 32 * q + 2 * j;
-                const float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
-                const float w0 = s <= row ? x0 * x0 : 0.f;
-                const float w1 = s + 1 <= row ? x1 * x1 : 0.f;
+                float x0 = __uint_as_float(v[2 * j]), x1 = __uint_as_float(v[2 * j + 1]);
+                x0 *= x0;
+                x1 *= x1;
+                if constexpr (kGated) {
+                    x0 *= exp2f(lt - __shfl_sync(0xffffffffu, lk, 2 * j));
+                    x1 *= exp2f(lt - __shfl_sync(0xffffffffu, lk, 2 * j + 1));
+                }
+                const float w0 = s <= row ? x0 : 0.f;
+                const float w1 = s + 1 <= row ? x1 : 0.f;
                 dsum += w0;
                 dsum += w1;
                 pw[j] = pack_bf16(w0, w1);
@@ -617,7 +673,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (t < T) part[(size_t)gridDim.y * T * DV + (size_t)bh * T + t] = dsum;
                 return true;
             }
-            const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+            const float inv = (kGated && !ga.normalize) ? 1.f : dsum > 0.f ? 1.f / dsum : 0.f;
             uint32_t o[DV / 2];   // the row in bf16 pairs
 #pragma unroll
             for (int c32 = 0; c32 < DV; c32 += 32) {
@@ -640,7 +696,8 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             return true;
         };
-        auto gram_to_smem = [&](bool from_tmem, const float *pre) {
+        // gscale (gated): the factor G is left with in TMEM for the next Gram update
+        auto gram_to_smem = [&](bool from_tmem, const float *pre, float gscale) {
             // G rows i = lane (quarter 0 only): bf16 [D][D] K-major, 64-byte swizzle
             if (quarter != 0) return;
             float gv[D];
@@ -666,14 +723,15 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<uint4 *>(gram + (lane >> 3) * 512 + (lane & 7) * 64 +
                                            ((chunk ^ ((lane >> 1) & 3)) << 4)) = u;
             }
-            if (!from_tmem) {
+            if (!from_tmem || (kGated && gscale != 1.f)) {
 #pragma unroll
                 for (int c = 0; c < D; c += 8) {
                     uint32_t v[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(gv[c + e]);
+                    for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(gv[c + e] * gscale);
                     tmem_st8(tG + lsel + c, v);
                 }
+                tmem_st_wait();
             }
         };
         // inter-chunk denominator q^T G_pre q (Q G_pre from TMEM, q from the Q
@@ -687,12 +745,15 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tile_row_packed<D>(tq, row, r);
             uint32_t v[32];
             tmem_ld32(tQG + lsel, v);
+            float di = 0.f;
 #pragma unroll
             for (int m = 0; m < D / 2; ++m) {
-                dsum = fmaf(__uint_as_float(v[2 * m]), __uint_as_float(r.w[m] << 16), dsum);
-                dsum = fmaf(__uint_as_float(v[2 * m + 1]), __uint_as_float(r.w[m] & 0xFFFF0000u), dsum);
+                di = fmaf(__uint_as_float(v[2 * m]), __uint_as_float(r.w[m] << 16), di);
+                di = fmaf(__uint_as_float(v[2 * m + 1]), __uint_as_float(r.w[m] & 0xFFFF0000u), di);
             }
-            gram_to_smem(true, nullptr);
+            if constexpr (kGated) di *= exp2f(lam2[min(i * kTile + row, nvalid - 1)]);   // b_t
+            dsum += di;
+            gram_to_smem(true, nullptr, (kGated && i + 1 < nch) ? gch[i + 1] : 1.f);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -705,7 +766,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
         {   // initial Gram: the segment's exclusive prefix (zero for g == 0)
             const float *pre = g > 0 ? seg + ((size_t)sbh * NR + (size_t)g * m_pieces) * C::E : nullptr;
-            gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr);
+            gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr, kGated ? gch[0] : 1.f);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -729,8 +790,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ================= lift warps: token t, side (0 query, 1 key)
         const int lw = warp - kWarpLift;
         const int side = lw >> 2;
-        output_lift_role<D, NB>(side ? tk : tq, lring + side * 32768, (lw & 3) * 32 + lane, side != 0, nch,
-                                chunk_full, &qk_empty, block_ready, block_empty, &abort_flag);
+        output_lift_role<D, NB>(side ? (kGated ? tkg : tk) : tq, lring + side * 32768, (lw & 3) * 32 + lane,
+                                side != 0, nch, chunk_full, &qk_empty, block_ready, block_empty,
+                                &abort_flag, side ? nullptr : lam2, nvalid);
     }
     tc_fence_before();
     __syncthreads();
@@ -811,6 +873,77 @@ sub_finalize_kernel(const float *__restrict__ part, bf16 *__restrict__ out, int6
 constexpr int kSmemState = 2 * (Cfg<32, 64>::QK_TILE + Cfg<32, 64>::V_TILE) + kStateRing * 32768 + 2048;
 constexpr int kSmemOutput = 2 * Cfg<32, 64>::QK_TILE + 2 * Cfg<32, 64>::V_TILE + 2 * 65536 +
                             2 * 16384 + 2048 + 2048;
+constexpr int kSmemOutputGated = kSmemOutput + Cfg<32, 64>::QK_TILE;   // + the scaled K tile
+
+// GatedKATA segment sums come from the keys scaled to the end of their piece:
+// per chunk c of a summed piece, k''_s = sqrt(P_c) k'_s, where k'_s carries the
+// gates after s to the end of chunk c and P_c is the product of the gates of the
+// piece's later chunks.  The first chunk of each segment also writes the gate
+// products of the segment's m pieces (the gated scan's multipliers; an empty
+// piece has product 1).  Grid (summed chunks, heads), 128 threads.
+__global__ void __launch_bounds__(128)
+gated_piece_prep_kernel(const bf16 *__restrict__ kc, const float *__restrict__ gch,
+                        bf16 *__restrict__ kpc, float *__restrict__ pgate, int T, int NCt, int Lc,
+                        int m_pieces, int npieces, int NR) {
+    __shared__ float wprod[4];
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int g = c / Lc, cs = g * Lc;
+    const float *gc = gch + (size_t)bh * NCt;
+    auto piece_lo = [&](int p) { return min(NCt, cs + (p * Lc) / m_pieces); };
+    int p = 0;
+    while (p + 1 < m_pieces && piece_lo(p + 1) <= c) ++p;
+    const int lo = piece_lo(p), hi = piece_lo(p + 1);   // the piece's chunks
+    // product of the gates of the piece's chunks after c, over the block
+    float after = 1.f;
+    for (int cc = c + 1 + threadIdx.x; cc < hi; cc += blockDim.x) after *= gc[cc];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) after *= __shfl_xor_sync(0xffffffffu, after, o);
+    if ((threadIdx.x & 31) == 0) wprod[threadIdx.x >> 5] = after;
+    __syncthreads();
+    after = wprod[0] * wprod[1] * wprod[2] * wprod[3];
+    if (c == lo && threadIdx.x == 0)   // the piece's gate product
+        pgate[(size_t)bh * NR + g * m_pieces + p] = gc[c] * after;
+    if (c == cs)   // empty pieces of the segment multiply by 1
+        for (int pp = threadIdx.x; pp < m_pieces; pp += blockDim.x)
+            if (piece_lo(pp) == piece_lo(pp + 1)) pgate[(size_t)bh * NR + g * m_pieces + pp] = 1.f;
+    if (c == 0)   // the record past the pieces (the last segment's prefix) multiplies nothing
+        for (int r = npieces + threadIdx.x; r < NR; r += blockDim.x) pgate[(size_t)bh * NR + r] = 1.f;
+    const float sc = sqrtf(after);
+    const int rows = min(kTile, T - c * kTile);
+    const size_t base = ((size_t)bh * T + (size_t)c * kTile) * 32;
+    const uint4 *src = reinterpret_cast<const uint4 *>(kc + base);
+    uint4 *dst = reinterpret_cast<uint4 *>(kpc + base);
+    for (int e = threadIdx.x; e < rows * 4; e += blockDim.x) {
+        uint4 u = src[e];
+        uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = pack_bf16(__uint_as_float(w[k] << 16) * sc, __uint_as_float(w[k] & 0xFFFF0000u) * sc);
+        dst[e] = u;
+    }
+}
+
+// Exclusive gated prefix of the piece records in place: run = 0; per record r,
+// store run, then run = pg_r run + rec_r (the affine maps (g, S) compose as
+// (g, S) o (g', S') = (g g', g' S + S')).  Inclusive totals to totals[BH][E].
+__global__ void __launch_bounds__(256)
+gated_record_scan_kernel(float *__restrict__ rec, const float *__restrict__ pgate, int NR, int64_t E,
+                         float *__restrict__ totals) {
+    const int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e4 >= E / 4) return;
+    const int bh = blockIdx.y;
+    float4 *p = reinterpret_cast<float4 *>(rec + (size_t)bh * NR * E) + e4;
+    const float *pg = pgate + (size_t)bh * NR;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < NR; ++r) {
+        const float4 x = p[(size_t)r * (E / 4)];
+        const float gr = pg[r];
+        p[(size_t)r * (E / 4)] = run;
+        run = make_float4(fmaf(gr, run.x, x.x), fmaf(gr, run.y, x.y), fmaf(gr, run.z, x.z),
+                          fmaf(gr, run.w, x.w));
+    }
+    if (totals) reinterpret_cast<float4 *>(totals + (size_t)bh * E)[e4] = run;
+}
 
 }  // namespace
 
@@ -940,15 +1073,17 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     {
         TraceScope tr("tc_segment_output", stream);
         if (part == nullptr) {
-            cudaFuncSetAttribute(seg_output_kernel<32, 64, false>,
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, false, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
-            seg_output_kernel<32, 64, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part);
+            seg_output_kernel<32, 64, false, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part,
+                OutGate{nullptr, nullptr, 1});
         } else {
-            cudaFuncSetAttribute(seg_output_kernel<32, 64, true>,
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
-            seg_output_kernel<32, 64, true><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part);
+            seg_output_kernel<32, 64, true, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part,
+                OutGate{nullptr, nullptr, 1});
         }
     }
     if (cross) {
@@ -961,6 +1096,86 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
         const int64_t rows = (int64_t)s0.BH() * s0.T;
         const int blocks = (int)std::min<int64_t>((rows * 16 + 255) / 256, 152 * 16);
         sub_finalize_kernel<<<blocks, 256, 0, stream>>>(part, (bf16 *)out, rows, s0.T, nsub);
+    }
+    return cudaGetLastError();
+}
+
+namespace {
+// GatedKATA workspace: K' and K'' (bf16 [BH][T][32]), then the piece records
+// (plus the totals with a state), the cumulative log2 gates [BH][T], the chunk
+// gate products [BH][NC] and the piece gate products [BH][NR].
+struct GatedWs {
+    bf16 *kc, *kpc;
+    float *rec, *lam2, *gch, *pgate;
+    size_t bytes;
+};
+GatedWs gated_ws(const FwdShape &s, const Plan &p, bool with_state, void *base) {
+    GatedWs w;
+    uint8_t *b = static_cast<uint8_t *>(base);
+    const size_t nk = (size_t)s.BH() * s.T * 32 * sizeof(bf16);
+    const size_t nrec = (size_t)s.BH() * ((size_t)p.NR + (with_state ? 1 : 0)) * Cfg<32, 64>::E;
+    w.kc = reinterpret_cast<bf16 *>(b);
+    w.kpc = reinterpret_cast<bf16 *>(b + nk);
+    w.rec = reinterpret_cast<float *>(b + 2 * nk);
+    w.lam2 = w.rec + nrec;
+    w.gch = w.lam2 + (size_t)s.BH() * s.T;
+    w.pgate = w.gch + (size_t)s.BH() * p.NCt;
+    w.bytes = 2 * nk + sizeof(float) * (nrec + (size_t)s.BH() * s.T + (size_t)s.BH() * p.NCt +
+                                        (size_t)s.BH() * p.NR);
+    return w;
+}
+}  // namespace
+
+size_t tc_gated_workspace_bytes(const FwdShape &s, int num_sms, bool with_state) {
+    return gated_ws(s, plan(s, num_sms, with_state, 1), with_state, nullptr).bytes;
+}
+
+cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, const void *v,
+                             const float *gamma, void *out, void *workspace, int num_sms,
+                             cudaStream_t stream, const StateOut &so, int normalize) {
+    using C = Cfg<32, 64>;
+    const bool with_state = so.state != nullptr;
+    const Plan p = plan(s, num_sms, with_state, 1);
+    const GatedWs w = gated_ws(s, p, with_state, workspace);
+    CUtensorMap mq, mk, mv, mkc, mkpc;
+    if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
+        !make_map(mv, v, s.dv, s.T, s.BH()) || !make_map(mkc, w.kc, s.d, s.T, s.BH()) ||
+        !make_map(mkpc, w.kpc, s.d, s.T, s.BH()))
+        return cudaErrorInvalidValue;
+    cudaError_t e = gate_prep_launch(k, gamma, w.kc, w.lam2, w.gch, s.BH(), s.T, s.d, stream);
+    if (e != cudaSuccess) return e;
+    if (p.nsum > 0) {
+        const int summed = std::min(p.NCt, p.nsum * p.Lc);
+        {
+            TraceScope tr("tc_gated_piece_prep", stream);
+            gated_piece_prep_kernel<<<dim3(summed, s.BH()), 128, 0, stream>>>(
+                w.kc, w.gch, w.kpc, w.pgate, s.T, p.NCt, p.Lc, p.m, p.nsum * p.m, p.NR);
+        }
+        cudaFuncSetAttribute(seg_state_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemState);
+        {
+            TraceScope tr("tc_segment_state", stream);
+            seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, s.BH()), 352, kSmemState, stream>>>(
+                mkpc, mv, w.rec, p.NCt, p.Lc, p.m, p.NR, 1, g_stall_next.exchange(0));
+        }
+        float *totals = with_state ? w.rec + (size_t)s.BH() * p.NR * C::E : nullptr;
+        {
+            TraceScope tr("tc_gated_scan", stream);
+            gated_record_scan_kernel<<<dim3((unsigned)((C::E / 4 + 255) / 256), s.BH()), 256, 0, stream>>>(
+                w.rec, w.pgate, p.NR, C::E, totals);
+        }
+        if (with_state) {
+            TraceScope tr("tc_state_export", stream);
+            state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
+        }
+    }
+    {
+        TraceScope tr("tc_segment_output_gated", stream);
+        cudaFuncSetAttribute(seg_output_kernel<32, 64, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutputGated);
+        seg_output_kernel<32, 64, false, true><<<dim3(p.G, s.BH()), 608, kSmemOutputGated, stream>>>(
+            mq, mk, mv, mkc, (bf16 *)out, w.rec, s.T, p.NCt, p.Lc, p.m, p.NR, 1, 0, nullptr,
+            OutGate{w.lam2, w.gch, normalize});
     }
     return cudaGetLastError();
 }

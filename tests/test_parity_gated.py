@@ -96,8 +96,11 @@ def test_gated_state_export_and_decode(kg, normalize, d, dv, C, dtype):
                                           C, normalize, with_state=True)
     torch.cuda.synchronize()
     S_ref, z_ref = oracle.prefix_state_gated(to_f64(k[sl]), to_f64(v[sl]), to_f64(g[sl]))
-    assert slice_rel_err(to_f64(S), S_ref) <= TOL[torch.float32]
-    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= TOL[torch.float32]
+    # the tensor path sums products of bf16 lifted keys (scaled by the gates) with v
+    tc = kg.kata_fwd_path_gated(w.B, w.H, T, d, dv, C, dtype) == kg.KATA_PATH_TC
+    stol = 1e-2 if tc else TOL[torch.float32]
+    assert slice_rel_err(to_f64(S), S_ref) <= stol
+    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= stol
     o = kg.kata_decode_step_gated(S, z, q[..., T, :].contiguous().cuda(),
                                   k[..., T, :].contiguous().cuda(),
                                   v[..., T, :].contiguous().cuda(),
@@ -250,3 +253,162 @@ def test_gated_auto_form(kg, normalize, d, dtype, form):
     ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
     err = slice_rel_err(to_f64(out), ref)
     assert err <= TOL[w.dtype], f"{form} normalize={normalize}: {err:.3e}"
+
+
+# ---- GatedKATA chunked on the tensor cores (bf16, d = 32, dv = 64): the d = 32
+# segments with gated keys, a gated segment scan and decayed running state
+def _seam_rows(kg, w):
+    nseg, seg_tokens = kg.kata_fwd_segments(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype)
+    rows = []
+    for g in range(1, nseg):
+        s0 = g * seg_tokens
+        rows += [s0 - 2, s0 - 1, s0, s0 + 1, s0 + 127, s0 + 128]
+    return [t for t in rows if 0 <= t < w.T]
+
+
+_TC_SHAPES = [
+    (1, 2, 1100),    # nine one-chunk segments per head: state kernel, gated scan
+    (4, 15, 1000),   # 60 heads: 2 segments of 4 chunks, sums from 2 pieces of 2 chunks
+    (1, 4, 5000),    # 20 segments of 2 chunks, one-chunk pieces
+    (8, 8, 1000),    # 2 segments of 4 chunks, ragged tail
+    (1, 1, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+]
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("B,H,T", _TC_SHAPES)
+def test_gated_tensor_path(kg, normalize, B, H, T):
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_gated(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)   # resets and unit gates at 128-token chunk edges, runs of 0.5
+    out = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[w.dtype], f"normalize={normalize}: {err:.3e}"
+
+
+@pytest.mark.parametrize("B,H,T", [(1, 2, 1100), (4, 15, 1000), (1, 1, 129)])
+def test_gated_tensor_path_unit_gates_are_the_plain_path(kg, B, H, T):
+    """gamma = 1: every scale is exactly 1 and every decay exactly 1, so the
+    gated tensor path reproduces the plain one bit for bit."""
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    one = torch.ones((w.B, w.H, w.T), device="cuda")
+    a = kg.kata_fwd_chunked_gated(q, k, v, one, w.C)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_gated_tensor_path_zero_gates(kg):
+    """gamma = 0 everywhere keeps only each token's own write: o_t = v_t."""
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=1, H=2, T=1100)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    zero = torch.zeros((w.B, w.H, w.T), device="cuda")
+    for normalize in (True, False):
+        out = kg.kata_fwd_chunked_gated(q, k, v, zero, w.C, normalize)
+        torch.cuda.synchronize()
+        ref = oracle.forward_gated(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()),
+                                   to_f64(zero.cpu()), normalize)
+        assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+    out = kg.kata_fwd_chunked_gated(q, k, v, zero, w.C, True)
+    torch.cuda.synchronize()
+    assert slice_rel_err(to_f64(out), to_f64(v)) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("B,H,T", [(1, 2, 1100), (4, 15, 1000), (1, 4, 5000)])
+def test_gated_tensor_path_state(kg, normalize, B, H, T):
+    """The state after the last token (every segment summed, gated scan totals)."""
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out, S, z = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize,
+                                          with_state=True)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    S_ref, z_ref = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(S), S_ref) <= 1e-2
+    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= 1e-2
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_gated_tensor_path_long_context_sampled_rows(kg, normalize):
+    """The long-context workload (B=1, H=16, T=131072) with its seeded gates plus
+    resets and unit gates at chunk edges, sampled rows (the rows on both sides of
+    every segment seam among them) against the oracle."""
+    w = workloads.WORKLOADS["long_ctx_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    g = workloads.make_gate(w, device="cuda")
+    g[..., 128 * 300] = 0.0          # a reset at a chunk start
+    g[..., 128 * 301 - 1] = 0.0      # and at a chunk end
+    g[..., 5000:5300] = 1.0          # a run of unit gates
+    g[..., 70000:70100] = 0.5        # a run of halving gates
+    out = kg.kata_fwd_chunked_gated(q, k, v, g, w.C, normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    assert torch.isfinite(out).all()
+    BH = w.B * w.H
+    rng = np.random.default_rng(131)
+    seams = _seam_rows(kg, w)
+    fixed = [0, 1, 127, 128, 128 * 300 - 1, 128 * 300, 128 * 300 + 1, 128 * 301 - 1,
+             128 * 301, 5299, 70050, 70100, w.T - 1]
+    worst = 0.0
+    for h in sorted(set([0, BH - 1] + rng.integers(0, BH, size=2).tolist())):
+        ts = np.array(sorted(set(fixed + seams + rng.integers(0, w.T, size=16).tolist())),
+                      dtype=np.int64)
+        qh, kh, vh = (to_f64(t.reshape(BH, 1, w.T, -1)[h:h + 1]) for t in (q, k, v))
+        gh = to_f64(g.reshape(BH, 1, w.T)[h:h + 1])
+        ref = oracle.forward_rows_gated(qh, kh, vh, gh, ts, normalize)
+        got = to_f64(out.reshape(BH, w.T, w.dv)[h])[ts]
+        worst = max(worst, slice_rel_err(got, ref))
+    print(f"long-context gated: {len(seams)} seam rows, worst slice metric {worst:.3e}")
+    assert worst <= TOL[w.dtype], f"{worst:.3e}"
+
+
+@pytest.mark.parametrize("d,T,form", [
+    (32, 10240, "quadratic"), (32, 10241, "chunked"), (32, 32768, "chunked"),
+    (64, 32768, "quadratic"), (64, 65536, "quadratic"), (64, 65537, "chunked"),
+])
+def test_gated_form_bounds(kg, d, T, form):
+    """kata_fwd_gated's form at and past its measured bounds (bf16, dv = 64)."""
+    want = {"quadratic": kg.KATA_FORM_QUADRATIC, "chunked": kg.KATA_FORM_CHUNKED}[form]
+    assert kg.kata_fwd_gated_form(1, 1, T, d, 64, 64, torch.bfloat16) == want
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d", [32, 64])
+def test_gated_auto_form_32k_sampled_rows(kg, normalize, d):
+    """kata_fwd_gated at T = 32768 (d = 32: the chunked tensor form; d = 64: the
+    quadratic form) with the seeded gates plus resets, unit gates and runs of
+    0.5 gates, sampled rows against the oracle."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=32768, d=d, C=64)
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    g = workloads.make_gate(w, device="cuda")
+    for t in (0, 127, 128, 4095, 4096, 20000):
+        g[..., t] = 0.0
+    g[..., 1000:1400] = 1.0
+    g[..., 9000:9300] = 0.5
+    g[..., 30000:30040] = 0.5
+    out = kg.kata_fwd_gated(q, k, v, g, w.C, normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    assert torch.isfinite(out).all()
+    BH = w.B * w.H
+    rng = np.random.default_rng(32768 + d)
+    fixed = [0, 1, 127, 128, 129, 1399, 4095, 4096, 4097, 9299, 19999, 20000, 20001, 30039,
+             w.T - 1]
+    worst = 0.0
+    for h in range(BH):
+        ts = np.array(sorted(set(fixed + rng.integers(0, w.T, size=12).tolist())), dtype=np.int64)
+        qh, kh, vh = (to_f64(t.reshape(BH, 1, w.T, -1)[h:h + 1]) for t in (q, k, v))
+        gh = to_f64(g.reshape(BH, 1, w.T)[h:h + 1])
+        ref = oracle.forward_rows_gated(qh, kh, vh, gh, ts, normalize)
+        worst = max(worst, slice_rel_err(to_f64(out.reshape(BH, w.T, w.dv)[h])[ts], ref))
+    assert worst <= TOL[w.dtype], f"d={d}: {worst:.3e}"
