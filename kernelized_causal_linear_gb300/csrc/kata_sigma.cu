@@ -93,23 +93,36 @@ sigma_finalize_kernel(const float *__restrict__ part, const float *__restrict__ 
     const float *r = rec + ((size_t)bh * NC + c) * kRec;
     float sv = r[col], skv = r[kDim + col], sk = r[2 * kDim];
     const float *pd = part + (size_t)BH * 4 * T * kDim;
-#pragma unroll 4
-    for (int t = 0; t < n; ++t) {
-        const float x = __bfloat162float(v[(base + t) * kDim + col]);
-        sv += x;
-        skv = fmaf(kk[t], x, skv);
-        sk += kk[t];
-        float num = 0.f, den = 0.f;
+    // 8 tokens at a time: every load of the group is issued before the running
+    // sums use the first, so the walk is not paced by one load latency per token
+    constexpr int kGroup = 8;
+    for (int t8 = 0; t8 < n; t8 += kGroup) {
+        float xs[kGroup], ns[kGroup], ds[kGroup];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const size_t row = ((size_t)bh * 4 + j) * T + t0 + t;
-            num += part[row * kDim + col];
-            den += pd[row];
+        for (int u = 0; u < kGroup; ++u) {
+            const int t = min(t8 + u, n - 1);
+            xs[u] = __bfloat162float(v[(base + t) * kDim + col]);
+            ns[u] = 0.f;
+            ds[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const size_t row = ((size_t)bh * 4 + j) * T + t0 + t;
+                ns[u] += part[row * kDim + col];
+                ds[u] += pd[row];
+            }
         }
-        const float ct = fmaf(es, qq[t], e2m);
-        num = fmaf(s2, num, fmaf(ct, sv, es * skv));
-        den = fmaf(s2, den, fmaf(ct, (float)(t0 + t + 1), es * sk));
-        out[(base + t) * kDim + col] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int t = t8 + u;
+            if (t >= n) break;
+            sv += xs[u];
+            skv = fmaf(kk[t], xs[u], skv);
+            sk += kk[t];
+            const float ct = fmaf(es, qq[t], e2m);
+            const float num = fmaf(s2, ns[u], fmaf(ct, sv, es * skv));
+            const float den = fmaf(s2, ds[u], fmaf(ct, (float)(t0 + t + 1), es * sk));
+            out[(base + t) * kDim + col] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+        }
     }
 }
 

@@ -252,7 +252,7 @@ seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // lam2 (gated queries): the chunk-local cumulative log2 of the gates of this
 // head's tokens from chunk c0 on; the query row of token t is scaled by the
 // square root of the gates from its chunk's start to t before it is lifted.
-template <int D, int NB>
+template <int D, int NB, bool kScaleQ>
 __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring, int t, bool key,
                                               int nch, uint64_t *chunk_full, uint64_t *qk_empty,
                                               uint64_t *block_ready, uint64_t *block_empty,
@@ -266,7 +266,7 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
         tile_row_packed<D>(tile, t, r);
         __syncwarp();
         if (elect_lane0()) mbar_arrive(qk_empty);
-        if (lam2 != nullptr) {
+        if (kScaleQ && lam2 != nullptr) {
             const int ta = min(i * kTile + t, nvalid - 1);
             const float sc = exp2f(0.5f * lam2[ta]);
 #pragma unroll
@@ -357,9 +357,11 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     const int g = blockIdx.x, bh = blockIdx.y;
     // sub-head bh of nsub per head: q/k columns D * (bh % nsub) .. of head bh / nsub
-    const int hz = bh / nsub, j = bh % nsub;
-    const int qx = (cross ? j >> 1 : j) * D, kx = (cross ? j & 1 : j) * D;
-    const int sbh = cross ? hz * 2 + (j & 1) : bh;   // records of this sub-head's keys
+    // (one sub-head per head, nsub = 1, unless kSub)
+    const int hz = kSub ? bh / nsub : bh, j = kSub ? bh % nsub : 0;
+    const bool xc = kSub && cross;
+    const int qx = (xc ? j >> 1 : j) * D, kx = (xc ? j & 1 : j) * D;
+    const int sbh = xc ? hz * 2 + (j & 1) : bh;   // records of this sub-head's keys
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
@@ -790,7 +792,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ================= lift warps: token t, side (0 query, 1 key)
         const int lw = warp - kWarpLift;
         const int side = lw >> 2;
-        output_lift_role<D, NB>(side ? (kGated ? tkg : tk) : tq, lring + side * 32768, (lw & 3) * 32 + lane,
+        output_lift_role<D, NB, kGated>(side ? (kGated ? tkg : tk) : tq, lring + side * 32768, (lw & 3) * 32 + lane,
                                 side != 0, nch, chunk_full, &qk_empty, block_ready, block_empty,
                                 &abort_flag, side ? nullptr : lam2, nvalid);
     }

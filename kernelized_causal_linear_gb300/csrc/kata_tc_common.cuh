@@ -450,9 +450,11 @@ __device__ __forceinline__ bool grouped_slot_pair(int b, int p, int &i, int &j) 
 // Row t of a [128 x D] bf16 tile written by TMA with the swizzle matching its
 // row width (32/64/128 bytes): the 16-byte chunk c of row t sits at chunk
 // c ^ ((t * row_bytes >> 7) & (chunks_per_row - 1)).
-// The loads are volatile: a caller releases the tile (an mbarrier arrive) right
-// after reading its row, and the TMA may then overwrite it; a non-volatile load
-// could legally be issued again later, where it would read the next tile.
+// The loads are volatile: a caller releases the tile (one lane's mbarrier arrive
+// after __syncwarp) right after reading its row, and the TMA may then overwrite
+// it.  With plain loads, even behind a compiler memory barrier, the CTA-pair
+// kernel read rows of the next tile in some runs; volatile loads keep every
+// lane's reads ahead of the release.
 template <int D>
 __device__ __forceinline__ void tile_row_packed(const uint8_t *tile, int t, PackedRow<D> &r) {
     constexpr int RB = D * 2, CPR = RB / 16;
