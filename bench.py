@@ -471,7 +471,7 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
     fm = FeatureMap(args.map, args.g)
     q, k, v = workloads.make_qkv(w)
     BH = w.B * w.H
@@ -509,6 +509,15 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _workload(args):
+    """The named workload, at --shape B,H,T when given."""
+    w = workloads.WORKLOADS[args.workload]
+    if args.shape is not None:
+        b_, h_, t_ = args.shape
+        w = w.scaled(B=b_, H=h_, T=t_)
+    return w
 
 
 def _metric():
@@ -581,7 +590,7 @@ def run_ours(args):
         dist.barrier()
     import kernelized_causal_linear_gb300 as kg
 
-    w = workloads.WORKLOADS[args.workload]
+    w = _workload(args)
     fm = FeatureMap(args.map, args.g)
     peaks = _peaks()
     q, k, v = workloads.make_qkv(w, device="cuda")
@@ -673,7 +682,7 @@ def run_ours(args):
             else:
                 achieved = work / mean_s / 1e9
                 peak, psrc = peaks["hbm_gbs"], f"HBM copy, {peaks['source']}"
-            traffic = _ncu_traffic(dom, w.name) if fm.code == 0 else None
+            traffic = _ncu_traffic(dom, w.name) if fm.code == 0 and args.shape is None else None
             roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
                         "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
@@ -863,8 +872,12 @@ def main(argv=None):
     ap.add_argument("--algo", default="chunked",
                     choices=["chunked", "quadratic", "gated", "gated_quadratic"],
                     help="chunked O(T) form (the default), the quadratic flash-style form, "
-                         "GatedKATA chunked (CUDA cores) or GatedKATA quadratic (tensor cores); "
-                         "the gated forms draw seeded gates")
+                         "GatedKATA chunked (tensor cores for bf16 d=32 dv=64, else CUDA "
+                         "cores) or GatedKATA quadratic (tensor cores); the gated forms draw "
+                         "seeded gates")
+    ap.add_argument("--shape", default=None, metavar="B,H,T",
+                    help="the workload's recipe at another batch, head count and length "
+                         "(for profiles of other shapes; the bench line uses the named sizes)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -873,6 +886,12 @@ def main(argv=None):
                     help="micro-benchmark instead of the bench line: 'scan' compares the "
                          "one-pass and the two-level chunk scan at small-batch shapes")
     args = ap.parse_args(argv)
+    if args.shape is not None:
+        try:
+            b_, h_, t_ = (int(x) for x in args.shape.split(","))
+        except ValueError:
+            ap.error("--shape takes B,H,T")
+        args.shape = (b_, h_, t_)
     if args.ubench == "scan":
         return run_scan_ubench(args)
     if args.map == "full" and args.g != 1:
