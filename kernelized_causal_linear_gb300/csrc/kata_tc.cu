@@ -467,6 +467,20 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll 1
                 for (int b = 0; b < NB && ok; ++b) {
                     const int gb = i * NB + b, ls = gb & 1;
+                    if (b > 0) {
+                        // P of quarter b - 1 was built while block b - 1 ran: queue
+                        // Q K^T quarter b and P V of quarter b - 1 ahead of this
+                        // block's MMAs, so that quarter b's P is built while they run
+                        const int n = 4 * i + b - 1;
+                        ok = sy.wait(&p_full[n & 1], n >> 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (b < 4) {
+                            qk_quarter(b);
+                            if (b == 3) mma_commit(&qk_empty);
+                        }
+                        pv_quarter(n, vo);
+                    }
                     ok = sy.wait(&block_ready[ls], gb >> 1) &&
                          (b != 0 || i == 0 || sy.wait(&o_empty, i - 1));
                     if (!ok) break;
@@ -485,19 +499,6 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                    desc_add(b0, ks * 2048), kIdPV, 1u);
                     }
                     mma_commit(&block_empty[ls]);
-                    // P of quarter b (built while block b ran; the P warps have read
-                    // Q K^T quarter b by then): Q K^T quarter b + 1, then P V quarter b
-                    if (b < 4) {
-                        const int n = 4 * i + b;
-                        ok = sy.wait(&p_full[n & 1], n >> 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        if (b < 3) {
-                            qk_quarter(b + 1);
-                            if (b == 2) mma_commit(&qk_empty);
-                        }
-                        pv_quarter(n, vo);
-                    }
                 }
                 if (!ok) break;
                 mma_commit(&o_full);

@@ -49,11 +49,13 @@ def _check_state(kg, w, expect_path=None):
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
 
 
+# With the state exported every segment is summed (the last one too) and the
+# scan's inclusive totals are the state.
 @pytest.mark.parametrize("B,H,T", [
-    (1, 2, 1100),    # several segments per head, ragged last chunk
+    (1, 2, 1100),    # 9 one-chunk segments per head, ragged last chunk
     (16, 8, 700),    # one segment per head
-    (4, 8, 4096),    # 2 segments of 16 chunks, 4 pieces each
-    (1, 4, 5000),    # 14 segments of 3 chunks; the last has 1, so one of its pieces is empty
+    (4, 8, 4096),    # 4 segments of 8 chunks
+    (1, 4, 5000),    # 20 segments of 2 chunks
     (1, 1, 129),     # last chunk holds one token
     (3, 1, 5),       # a single partial chunk
 ])
