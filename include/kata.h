@@ -168,6 +168,8 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   scale^2, plus the eps terms as a linear attention with the query features
  *   (eps^2 m + eps scale |q|^2, eps scale) and the key features (1, |k|^2),
  *   summed in fp32 in 128-token chunks.
+ *   KATA-M_4: four sub-heads on the 16-wide blocks, each zero-padded to 32
+ *   columns in scratch (the zero coordinates add nothing to (q_a . k_a)^2).
  * The other reduced maps run on CUDA cores in fp32 (bf16 inputs are widened;
  * the output is written in the input type).  kata_fwd_path_map tells which.
  */

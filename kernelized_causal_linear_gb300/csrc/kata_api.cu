@@ -85,8 +85,9 @@ int device_info(DevInfo &out) {
 // Kernel families behind the public paths: KATA_PATH_TC covers both tensor-core
 // variants (d = 32 with segments, d = 64 with the state split over four CTAs);
 // kTc32Sub is KATA-M_2 at d = 64 as two d = 32 sub-heads, kTc32Sigma is
-// KATA-Sigma_2 at d = 64 as four crosswise d = 32 sub-heads plus its eps terms.
-enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma };
+// KATA-Sigma_2 at d = 64 as four crosswise d = 32 sub-heads plus its eps terms,
+// kTc32M4 is KATA-M_4 at d = 64 as four zero-padded d = 32 sub-heads.
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4 };
 
 Kernels from_fwd(kata::FwdKernels k) {
     return k == kata::FwdKernels::Tc32 ? kTc32 : k == kata::FwdKernels::Tc64 ? kTc64 : kSimt;
@@ -96,18 +97,20 @@ Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
     return from_fwd(kata::select_fwd_kernels(s, di.major, di.minor, di.sms));
 }
 
-// Kernels for a reduced map: KATA-M_2 and KATA-Sigma_2 at d = 64 are d = 32
-// sub-heads on the d = 32 tensor path (bf16, dv = 64); every other reduced map
-// runs on CUDA cores.
+// Kernels for a reduced map: KATA-M_2, KATA-Sigma_2 and KATA-M_4 at d = 64 are
+// d = 32 sub-heads on the d = 32 tensor path (bf16, dv = 64); every other
+// reduced map runs on CUDA cores.
 Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
                            bool with_state) {
     if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
-    if ((map.kind == KATA_MAP_BLOCK || map.kind == KATA_MAP_SUM) && map.g == 2 && s.d == 64 &&
-        !with_state) {
+    if (s.d == 64 && !with_state) {
         FwdShape half = s;
         half.d = 32;
-        if (kata::tc_supported(half, di.major, di.minor))
-            return map.kind == KATA_MAP_BLOCK ? kTc32Sub : kTc32Sigma;
+        if (kata::tc_supported(half, di.major, di.minor)) {
+            if (map.kind == KATA_MAP_BLOCK && map.g == 2) return kTc32Sub;
+            if (map.kind == KATA_MAP_SUM && map.g == 2) return kTc32Sigma;
+            if (map.kind == KATA_MAP_BLOCK && map.g == 4) return kTc32M4;
+        }
     }
     return kSimt;
 }
@@ -230,6 +233,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     const Kernels kn = select_map_kernels(s, di, map, with_state);
     const size_t wsb = kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
                        : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
+                       : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
                        : map.kind == 0    ? workspace_for(s, kn, di, with_state)
                                           : kata::simt_workspace_bytes(s, map);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -241,6 +245,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     cudaError_t e =
         kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
         : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
+        : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
         : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
                            : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {

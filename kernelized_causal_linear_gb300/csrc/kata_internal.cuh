@@ -130,6 +130,11 @@ size_t tc_gated_workspace_bytes(const FwdShape &s, int num_sms, bool with_state)
 cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, const void *v,
                              const float *gamma, void *out, void *workspace, int num_sms,
                              cudaStream_t stream, const StateOut &so, int normalize);
+// KATA-M_4 at d = 64: q and k rows padded to four 32-wide blocks [u_a | 0], run
+// as four d = 32 sub-heads (nsub = 4) whose numerators and denominators add.
+size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms);
+cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
+                          void *workspace, int num_sms, cudaStream_t stream);
 // KATA-Sigma_2 finalize (kata_sigma.cu): the scratch it needs after the
 // sub-head partials, and the pass that sums them with the eps terms.
 size_t sigma_workspace_bytes(const FwdShape &s);

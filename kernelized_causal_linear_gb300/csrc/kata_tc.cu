@@ -1183,6 +1183,50 @@ cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, co
     return cudaGetLastError();
 }
 
+namespace {
+// KATA-M_4 at d = 64: each 16-wide block u_a of a q or k row becomes a 32-wide
+// row [u_a | 0]; psi of the padded row holds psi(u_a) and zeros, so the four
+// padded blocks run as full-map d = 32 sub-heads whose N and D add (Sec. 4.1,
+// KATA-M_g: <psi(q), psi(k)> = sum_a (q_a . k_a)^2).  One thread per 16-wide block.
+__global__ void __launch_bounds__(256)
+pad_blocks16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int64_t rows) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (row, block)
+    if (e >= rows * 4) return;
+    const uint4 *src = x + e * 2;   // 16 bf16 = 2 x 16 bytes
+    uint4 *dst = xp + e * 4;        // 32 bf16 = 4 x 16 bytes
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    dst[0] = src[0];
+    dst[1] = src[1];
+    dst[2] = z;
+    dst[3] = z;
+}
+FwdShape padded_m4(const FwdShape &s) {
+    FwdShape sp = s;
+    sp.d = 128;   // four 32-wide padded blocks per row
+    return sp;
+}
+}  // namespace
+
+size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms) {
+    const size_t np = (size_t)s.BH() * s.T * 128 * sizeof(bf16);
+    return 2 * np + tc_workspace_bytes(padded_m4(s), num_sms, false, 4);
+}
+
+cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
+                          void *workspace, int num_sms, cudaStream_t stream) {
+    if (s.d != 64) return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)s.BH() * s.T;
+    const size_t np = (size_t)rows * 128;
+    bf16 *qp = static_cast<bf16 *>(workspace), *kp = qp + np;
+    {
+        TraceScope tr("tc_m4_pad", stream);
+        const unsigned blocks = (unsigned)((rows * 4 + 255) / 256);
+        pad_blocks16_kernel<<<blocks, 256, 0, stream>>>((const uint4 *)q, (uint4 *)qp, rows);
+        pad_blocks16_kernel<<<blocks, 256, 0, stream>>>((const uint4 *)k, (uint4 *)kp, rows);
+    }
+    return tc_forward(padded_m4(s), qp, kp, v, out, kp + np, num_sms, stream, StateOut{}, 4);
+}
+
 void tc_arm_stall() { g_stall_next.store(1); }
 
 int tc_take_error() {

@@ -78,9 +78,9 @@ def test_map_lift_parity(kg, map_, g, d, dtype):
     assert err <= 1e-6
 
 
-@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2)])
+@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4)])
 def test_map_full_size_sampled_rows(kg, map_, g):
-    """The LM-layer workload with M_2 / Sigma_2, sampled rows against the oracle."""
+    """The LM-layer workload with M_2 / Sigma_2 / M_4, sampled rows against the oracle."""
     w = workloads.WORKLOADS["lm_layer_bf16"]
     q, k, v = workloads.make_qkv(w, device="cuda")
     eps, scale = _params(kg, map_, g)
@@ -172,11 +172,43 @@ def test_sigma2_eps_zero_is_four_cross_terms(kg):
     assert slice_rel_err(to_f64(b), to_f64(a)) <= 1e-2
 
 
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # 8 sub-heads: 9 one-chunk segments
+    (8, 8, 700),     # 256 sub-heads, one segment each, ragged tail
+    (2, 3, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+])
+def test_m4_tensor_path(kg, B, H, T):
+    """KATA-M_4 at d = 64 (bf16, dv = 64): each 16-wide block zero-padded to 32
+    and run as a d = 32 sub-head; the zero coordinates contribute nothing."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 1, 4) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 1, 4)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "M", 4)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+def test_m4_tensor_path_zero_block(kg):
+    """A query block that is zero in every row leaves only the other blocks'
+    weights; a key block that is zero everywhere does the same."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=2, T=300)
+    q, k, v = workloads.make_qkv(w)
+    q[..., 16:32] = 0
+    k[..., 48:64] = 0
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 1, 4)
+    torch.cuda.synchronize()
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "M", 4)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
 def test_other_maps_take_cuda_cores(kg):
     w = workloads.WORKLOADS["lm_layer_bf16"]
-    for map_, g in ((1, 4), (2, 4)):
-        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
-            kg.KATA_PATH_SIMT
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 4) == \
+        kg.KATA_PATH_SIMT
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 1, 4) == kg.KATA_PATH_TC
     for map_ in (1, 2):
         assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, 2) == \
             kg.KATA_PATH_TC
