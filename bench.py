@@ -158,8 +158,12 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
         # every causal (t, s <= t) pair of the head: (q.k)^2 and P [V|1]
         return 2.0 * (d + dv + 1) * _intra_pairs(T, T) * BH, "TFLOP/s", "tensor"
     if stage == "tc_sub_finalize":
-        # M_2 sub-heads: reads two fp32 numerators and denominators, writes bf16 out
-        return float(BH * T) * (2 * (dv + 1) * 4 + dv * 2), "GB/s", "hbm"
+        # M_2 / M_4 sub-heads: reads their fp32 numerators and denominators, writes bf16 out
+        nsub = 4 if (fm.code, fm.g) == (1, 4) else 2
+        return float(BH * T) * (nsub * (dv + 1) * 4 + dv * 2), "GB/s", "hbm"
+    if stage == "tc_m4_pad":
+        # q and k rows in, zero-padded to four 32-wide blocks out
+        return float(BH * T) * 2 * (d * 2 + 4 * 32 * 2), "GB/s", "hbm"
     # Sigma_2 finalize: 128-token chunk sums of v, |k|^2 v, |k|^2 (reads k, v, writes
     # one record per chunk), their exclusive scan, and the pass that reads the four
     # sub-heads' fp32 numerators and denominators with q, k, v and writes bf16 out
@@ -189,10 +193,11 @@ def stage_dense_flops(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_M
     the state kernel the 5 state blocks and the Gram.  The quadratic kernels run
     every (query tile, key tile <= it) pair as full 128 x 128 tiles.  The reduced
     maps on the tensor path run d = 32 sub-heads: 2 per head for M_2, 4 for
-    Sigma_2 (whose segment sums need only the 2 key halves)."""
+    M_4 (zero-padded blocks) and Sigma_2 (whose segment sums need only the 2 key
+    halves)."""
     BH, T, d, dv = w.B * w.H, w.T, w.d, w.dv
-    if fm.code in (1, 2) and fm.g == 2 and d == 64:
-        sub_w = w.scaled(B=w.B * (2 if fm.code == 1 else 4), d=32)
+    if d == 64 and (fm.code, fm.g) in ((1, 2), (2, 2), (1, 4)):
+        sub_w = w.scaled(B=w.B * (2 if (fm.code, fm.g) == (1, 2) else 4), d=32)
         if stage == "tc_segment_state" and fm.code == 2:
             sub_w = w.scaled(B=w.B * 2, d=32)
         return stage_dense_flops(stage, sub_w, num_sms)
@@ -234,6 +239,7 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 # lives there too); every stage also depends on all the shared headers
 _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
                  ("tc_gated", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
+                 ("tc_m4", "kata_tc.cu"),
                  ("tc_sigma", "kata_sigma.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
