@@ -234,7 +234,14 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
  * product in TMEM, and the intra-chunk weights multiplied by 2^(l_t - l_s) from
  * the chunk-local cumulative log2 of the gates (a gate below 2^-126 counts as
  * 2^-126 there: a zero gate leaves a weight of at most 2^-126 on the writes
- * before it within the chunk).  Other shapes run on CUDA cores in fp32 FFMA.
+ * before it within the chunk).  bf16 inputs with d = 64, dv = 64 and T <= 262144
+ * take the tensor cores as well.  The output comes from the gated quadratic form
+ * (kata_fwd_quadratic_gated), which evaluates the same weights tile by tile.
+ * The state is sum_s A_s psi(k_s) v_s^T, A_s the product of the gates after s,
+ * and psi is quadratic, so the state comes from the chunked d = 64 tensor path
+ * run on the keys sqrt(A_s) k_s (rounded to bf16).  That part needs 4 B H >=
+ * the SM count; with fewer heads a call that exports the state runs on CUDA
+ * cores.  Other shapes run on CUDA cores in fp32 FFMA.
  *
  *   gamma    [B][H][T] fp32 device, read only, 16-byte aligned; values in [0, 1]
  *            (not checked on the device: other values give the recurrence's
@@ -250,9 +257,10 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
                            void *out, float *state, float *z, int B, int H, int T, int d, int dv,
                            int C, int dtype, int normalize, kata_stream_t stream);
 
-/* kata_fwd_path_gated -- the path kata_fwd_chunked_gated takes for a shape:
- * KATA_PATH_TC (tensor cores), KATA_PATH_SIMT (CUDA cores) or KATA_PATH_NONE
- * (invalid shape or no device). */
+/* kata_fwd_path_gated -- the path kata_fwd_chunked_gated takes for a shape
+ * without the state export: KATA_PATH_TC (tensor cores), KATA_PATH_SIMT (CUDA
+ * cores) or KATA_PATH_NONE (invalid shape or no device).  With the state
+ * exported at d = 64, the tensor path also needs 4 B H >= the SM count. */
 int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype);
 
 /*

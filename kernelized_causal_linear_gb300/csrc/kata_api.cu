@@ -566,10 +566,12 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     cudaGetLastError();
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool tc = kata::tc_supported(s, di.major, di.minor);
+    const bool wide = !tc && kata::gated_wide_supported(s, di.major, di.minor, di.sms, state != nullptr);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    const size_t wsb = tc ? kata::tc_gated_workspace_bytes(s, di.sms, state != nullptr)
-                          : kata::gated_workspace_bytes(s);
+    const size_t wsb = tc     ? kata::tc_gated_workspace_bytes(s, di.sms, state != nullptr)
+                       : wide ? kata::gated_wide_workspace_bytes(s, state != nullptr)
+                              : kata::gated_workspace_bytes(s);
     if (cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
@@ -577,8 +579,10 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     kata::StateOut so;
     so.state = state;
     so.z = z;
-    cudaError_t e = tc ? kata::tc_forward_gated(s, q, k, v, gamma, out, ws, di.sms, st, so, normalize)
-                       : kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
+    cudaError_t e =
+        tc     ? kata::tc_forward_gated(s, q, k, v, gamma, out, ws, di.sms, st, so, normalize)
+        : wide ? kata::gated_wide_forward(s, q, k, v, gamma, out, ws, st, so, normalize)
+               : kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
     const cudaError_t ef = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {
@@ -601,8 +605,11 @@ int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype) {
     if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_PATH_NONE;
     DevInfo di;
     if (device_info(di)) return KATA_PATH_NONE;
-    return kata::tc_supported(FwdShape{B, H, T, d, dv, C, dtype}, di.major, di.minor) ? KATA_PATH_TC
-                                                                                     : KATA_PATH_SIMT;
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    return kata::tc_supported(s, di.major, di.minor) ||
+                   kata::gated_wide_supported(s, di.major, di.minor, di.sms, false)
+               ? KATA_PATH_TC
+               : KATA_PATH_SIMT;
 }
 
 int kata_fwd_gated_form(int B, int H, int T, int d, int dv, int C, int dtype) {

@@ -130,6 +130,18 @@ size_t tc_gated_workspace_bytes(const FwdShape &s, int num_sms, bool with_state)
 cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, const void *v,
                              const float *gamma, void *out, void *workspace, int num_sms,
                              cudaStream_t stream, const StateOut &so, int normalize);
+// GatedKATA at d = 64 on the tensor cores (kata_gated_wide.cu): the output from
+// the gated quadratic form, the state after the last token (when asked) from
+// the plain d = 64 chunked tensor path on the keys scaled by the square root of
+// the gates after them.  Up to kGatedWideMaxT tokens (the quadratic form's cost
+// per token grows with T; ~13 ns per token and head at that bound).
+constexpr int kGatedWideMaxT = 262144;
+bool gated_wide_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms,
+                          bool with_state);
+size_t gated_wide_workspace_bytes(const FwdShape &s, bool with_state);
+cudaError_t gated_wide_forward(const FwdShape &s, const void *q, const void *k, const void *v,
+                               const float *gamma, void *out, void *workspace, cudaStream_t stream,
+                               const StateOut &so, int normalize);
 // KATA-M_4 at d = 64: q and k rows padded to four 32-wide blocks [u_a | 0], run
 // as four d = 32 sub-heads (nsub = 4) whose numerators and denominators add.
 size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms);

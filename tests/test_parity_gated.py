@@ -90,6 +90,7 @@ def test_gated_state_export_and_decode(kg, normalize, d, dv, C, dtype):
     q, k, v = workloads.make_qkv(w)
     g = _gates(w)
     T = w.T - 1   # the forward covers tokens 0 .. T-1; the decode step takes token T
+    g[..., T] = 0.9   # a reset here would make the step's output independent of the state
     sl = (slice(None), slice(None), slice(0, T))
     out, S, z = kg.kata_fwd_chunked_gated(q[sl].contiguous().cuda(), k[sl].contiguous().cuda(),
                                           v[sl].contiguous().cuda(), g[sl].contiguous().cuda(),
@@ -412,3 +413,63 @@ def test_gated_auto_form_32k_sampled_rows(kg, normalize, d):
         ref = oracle.forward_rows_gated(qh, kh, vh, gh, ts, normalize)
         worst = max(worst, slice_rel_err(to_f64(out.reshape(BH, w.T, w.dv)[h])[ts], ref))
     assert worst <= TOL[w.dtype], f"d={d}: {worst:.3e}"
+
+
+# ---- GatedKATA at d = 64 on the tensor cores (bf16, dv = 64): the output from the
+# gated quadratic form, the state from the chunked d = 64 path on sqrt(A_s) k_s
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("B,H,T", [
+    (1, 38, 300),    # 38 heads: the fewest with the d = 64 chunked path for the state
+    (2, 19, 129),    # last tile holds one token
+    (4, 10, 5),      # a single partial tile
+])
+def test_gated_d64_tensor_path_state(kg, normalize, B, H, T):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_gated(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out, S, z = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize,
+                                          with_state=True)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+    S_ref, z_ref = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(S), S_ref) <= 1e-2
+    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= 1e-2
+
+
+def test_gated_d64_prefill_then_decode(kg):
+    """Gated prefill of T-1 tokens at the decode shape's head size (d = 64) with the
+    state exported on the tensor path, then one gated decode step: the step's
+    output is the definition's output at row T-1."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=19, T=257)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    Tp = w.T - 1
+    g[..., Tp] = 0.9   # a reset here would make the step's output independent of the state
+    sl = (slice(None), slice(None), slice(0, Tp))
+    _, S, z = kg.kata_fwd_chunked_gated(q[sl].contiguous().cuda(), k[sl].contiguous().cuda(),
+                                        v[sl].contiguous().cuda(), g[sl].contiguous().cuda(),
+                                        w.C, True, with_state=True)
+    o = kg.kata_decode_step_gated(S, z, q[..., Tp, :].contiguous().cuda(),
+                                  k[..., Tp, :].contiguous().cuda(),
+                                  v[..., Tp, :].contiguous().cuda(), g[..., Tp].contiguous().cuda())
+    torch.cuda.synchronize()
+    full = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(o)[:, :, None, :], full[:, :, Tp:Tp + 1, :]) <= TOL[w.dtype]
+
+
+def test_gated_d64_few_heads_state_on_cuda_cores(kg):
+    """Fewer than 38 heads with the state exported: the call runs on CUDA cores
+    and still matches the oracle."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=200)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out, S, z = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, True,
+                                          with_state=True)
+    torch.cuda.synchronize()
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+    S_ref, _ = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(S), S_ref) <= 1e-4
