@@ -6,11 +6,13 @@
 // segments of whole 128-token chunks, and the exclusive scan over chunks of
 // Eq. 17 (Sec. 4.2) is done at two levels:
 //
-//   1. seg_state_kernel   per (segment, head): the segment's state sum
-//                         Psi(K)^T V over all its chunks (tcgen05, fp32
-//                         accumulators in TMEM) and its key Gram matrix K^T K.
-//                                                                      [Eq. 17]
-//   2. exclusive scan     of the segment states over segments (CUDA cores).
+//   1. seg_state_kernel   per (piece of a segment, head): the state sum
+//                         Psi(K)^T V over the piece's chunks (tcgen05, fp32
+//                         accumulators in TMEM) and its key Gram matrix K^T K;
+//                         a segment is cut into m pieces when that fills more
+//                         SMs.                                         [Eq. 17]
+//   2. exclusive scan     of the piece records (CUDA cores); segment g's
+//                         prefix is the record of its first piece.
 //   3. seg_output_kernel  per (segment, head): starts from the segment's prefix
 //                         state, held in TMEM in fp32, and walks its chunks:
 //                           P   = (Q K^T)^2 .* M            (intra, Eq. 18)
@@ -45,6 +47,11 @@
 // Chunk.  The tensor path uses 128-token chunks (the MMA tile height) for
 // every requested C; Eq. 17-20 give the same function for any chunk size, so
 // C only changes rounding.
+//
+// Variants of the output kernel: the sub-head form (M_2, M_4, Sigma_2 at d = 64
+// as d = 32 sub-heads whose fp32 N and D are summed afterwards) and the gated
+// form (GatedKATA: keys scaled by the gates, the running state decayed per
+// chunk); both are described at the kernel.
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
