@@ -181,7 +181,29 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     if stage == "tc64_finalize":
         # reads four fp32 partial numerators and the denominator, writes bf16 out
         return float(BH * T) * (4 * dv * 4 + 4 + dv * 2), "GB/s", "hbm"
+    # other bf16 head sizes on the tensor kernels: q or k padded to 32 columns
+    # (one launch each), v cut into 64-column parts, each part's output columns
+    # copied out, each part's state gathered (w: the v columns of one part)
+    wp = min(dv, 64)
+    if stage == "tc_adapt_pad":
+        return float(BH * T) * (d * 2 + 32 * 2), "GB/s", "hbm"
+    if stage == "tc_adapt_v_part":
+        return float(BH * T) * (wp * 2 + 64 * 2), "GB/s", "hbm"
+    if stage == "tc_adapt_out_part":
+        return float(BH * T) * (wp * 2 + wp * 2), "GB/s", "hbm"
+    if stage == "tc_adapt_state_part":
+        return float(BH) * n * (wp + 1) * 4 * 2, "GB/s", "hbm"
     return None, "", ""
+
+
+def kernel_workload(w, path):
+    """The shape the tensor-core kernels run for w: a bf16 head with d = 16 or
+    dv != 64 runs on them with q, k padded to d = 32 and v cut into 64-column
+    parts (one launch of each kernel per part), so their per-launch work is that
+    of the padded shape with dv = 64."""
+    if path != 2 or w.dtype != torch.bfloat16 or (w.d != 16 and w.dv == 64):
+        return w
+    return w.scaled(d=max(w.d, 32), dv=64)
 
 
 def stage_dense_flops(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
@@ -239,7 +261,7 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 # lives there too); every stage also depends on all the shared headers
 _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
                  ("tc_gated", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
-                 ("tc_m4", "kata_tc.cu"),
+                 ("tc_m4", "kata_tc.cu"), ("tc_adapt", "kata_adapt.cu"),
                  ("tc_sigma", "kata_sigma.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),
@@ -523,6 +545,9 @@ def _workload(args):
     if args.shape is not None:
         b_, h_, t_ = args.shape
         w = w.scaled(B=b_, H=h_, T=t_)
+    if args.head_dims is not None:
+        d_, dv_ = args.head_dims
+        w = w.scaled(d=d_, dv=dv_)
     return w
 
 
@@ -675,7 +700,9 @@ def run_ours(args):
     roofline = None
     if dom is not None:
         nl, tot = stages[dom]
-        work, unit, bound = stage_work(dom, w, torch.cuda.get_device_properties(0).multi_processor_count,
+        wk = w if dom.startswith("tc_adapt") or fm.code != 0 or args.algo != "chunked" \
+            else kernel_workload(w, path)
+        work, unit, bound = stage_work(dom, wk, torch.cuda.get_device_properties(0).multi_processor_count,
                                        fm)
         mean_s = tot / nl / 1e3
         if work is not None:
@@ -688,12 +715,13 @@ def run_ours(args):
             else:
                 achieved = work / mean_s / 1e9
                 peak, psrc = peaks["hbm_gbs"], f"HBM copy, {peaks['source']}"
-            traffic = _ncu_traffic(dom, w.name) if fm.code == 0 and args.shape is None else None
+            traffic = (_ncu_traffic(dom, w.name)
+                       if fm.code == 0 and args.shape is None and args.head_dims is None else None)
             roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
                         "peak_source": psrc, "mean_launch_ms": mean_s * 1e3,
                         "work_per_launch": work}
-            dense = stage_dense_flops(dom, w, torch.cuda.get_device_properties(0).multi_processor_count,
+            dense = stage_dense_flops(dom, wk, torch.cuda.get_device_properties(0).multi_processor_count,
                                       fm)
             if dense is not None:   # what the tensor cores execute, beside the algorithmic work
                 roofline["dense_tflops"] = dense / mean_s / 1e12
@@ -884,6 +912,9 @@ def main(argv=None):
     ap.add_argument("--shape", default=None, metavar="B,H,T",
                     help="the workload's recipe at another batch, head count and length "
                          "(for profiles of other shapes; the bench line uses the named sizes)")
+    ap.add_argument("--head-dims", default=None, metavar="d,dv",
+                    help="the workload's recipe at another head size (d in 16, 32, 64; dv in "
+                         "16, 32, 64, 128), for timings of the other shapes the library takes")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -898,6 +929,12 @@ def main(argv=None):
         except ValueError:
             ap.error("--shape takes B,H,T")
         args.shape = (b_, h_, t_)
+    if args.head_dims is not None:
+        try:
+            d_, dv_ = (int(x) for x in args.head_dims.split(","))
+        except ValueError:
+            ap.error("--head-dims takes d,dv")
+        args.head_dims = (d_, dv_)
     if args.ubench == "scan":
         return run_scan_ubench(args)
     if args.map == "full" and args.g != 1:

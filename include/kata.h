@@ -106,11 +106,15 @@ const char *kata_status_str(int status);
  *   C: the last chunk is zero-padded (Algorithm 1), padded rows are dropped.
  *
  * The output is the same function for every C (Eq. 17-20 regroup one sum);
- * C changes only the rounding.  bf16 inputs with dv = 64 and d = 32, or d = 64
- * with at least 38 (b, h) heads, run on the tensor-core path, which rounds the
- * lifted features and the chunk-state prefix to bf16 as MMA operands (fp32
- * accumulation); fp32 inputs and the other shapes run on CUDA cores in fp32
- * (kata_fwd_path tells which).
+ * C changes only the rounding.  bf16 inputs run on the tensor-core path, which
+ * rounds the lifted features and the chunk-state prefix to bf16 as MMA
+ * operands (fp32 accumulation), for every d and dv except d = 64 with fewer
+ * than 38 (b, h) heads.  Its kernels take d = 32 or 64 with dv = 64; other head
+ * sizes run on them through scratch copies: q and k padded with zero columns
+ * to d = 32 (d = 16), v cut into 64-column parts (dv = 16, 32 zero-padded; dv =
+ * 128 as two parts, each a full pass of the kernels).  Both are exact
+ * rewritings of Eq. 17-20.  fp32 inputs, and d = 64 with fewer heads, run on
+ * CUDA cores in fp32 (kata_fwd_path tells which).
  *
  * Scratch: per-call device workspace (kata_fwd_workspace_size bytes) taken
  * from the device's stream-ordered memory pool and released on `stream`.
@@ -281,9 +285,13 @@ int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype);
  * It takes the kernel family kata_fwd_chunked takes for the shape (see
  * kata_fwd_path) and needs the scratch kata_fwd_workspace_size reports; a
  * shape that needs more than the array returns KATA_ERR_SCRATCH_LIMIT before
- * any device work.  Every bf16 shape of the d = 32 tensor path fits on a
+ * any device work.  Every bf16 shape with d = 32 and dv = 64 fits on a
  * 152-SM GPU.  The d = 64 tensor path needs about 1 KB per token and head
- * (B*H*T up to roughly 32 K); the CUDA-core path needs
+ * (B*H*T up to roughly 32 K).  The scratch copies of the other head sizes add,
+ * per token and head, 128 bytes for q and k padded to d = 32 (d = 16) and 256
+ * bytes for one 64-column part of v and its output (dv != 64): B*H*T up to
+ * about 256 K for d = 16 with dv = 64, 128 K for d = 32 with dv != 64 and 85 K
+ * for d = 16 with dv != 64.  The CUDA-core path needs
  * B*H*(NC + NC/16 + 1)*n*(dv+1)*4 bytes with NC = ceil(T/C).
  *
  * The first call on each device (with that device current) looks up the

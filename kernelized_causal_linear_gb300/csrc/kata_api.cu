@@ -86,11 +86,19 @@ int device_info(DevInfo &out) {
 // variants (d = 32 with segments, d = 64 with the state split over four CTAs);
 // kTc32Sub is KATA-M_2 at d = 64 as two d = 32 sub-heads, kTc32Sigma is
 // KATA-Sigma_2 at d = 64 as four crosswise d = 32 sub-heads plus its eps terms,
-// kTc32M4 is KATA-M_4 at d = 64 as four zero-padded d = 32 sub-heads.
-enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4 };
+// kTc32M4 is KATA-M_4 at d = 64 as four zero-padded d = 32 sub-heads;
+// kTc32Adapt / kTc64Adapt run the other bf16 shapes (d = 16, dv != 64) on the
+// two tensor-core paths through padded copies and 64-column parts of v.
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt };
 
 Kernels from_fwd(kata::FwdKernels k) {
-    return k == kata::FwdKernels::Tc32 ? kTc32 : k == kata::FwdKernels::Tc64 ? kTc64 : kSimt;
+    switch (k) {
+        case kata::FwdKernels::Tc32: return kTc32;
+        case kata::FwdKernels::Tc64: return kTc64;
+        case kata::FwdKernels::Tc32Adapt: return kTc32Adapt;
+        case kata::FwdKernels::Tc64Adapt: return kTc64Adapt;
+        default: return kSimt;
+    }
 }
 
 Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
@@ -120,9 +128,13 @@ int select_path(const FwdShape &s, const DevInfo &di) {
 }
 
 kata::FwdKernels to_fwd(Kernels kn) {
-    return kn == kTc32 ? kata::FwdKernels::Tc32
-           : kn == kTc64 ? kata::FwdKernels::Tc64
-                         : kata::FwdKernels::Simt;
+    switch (kn) {
+        case kTc32: return kata::FwdKernels::Tc32;
+        case kTc64: return kata::FwdKernels::Tc64;
+        case kTc32Adapt: return kata::FwdKernels::Tc32Adapt;
+        case kTc64Adapt: return kata::FwdKernels::Tc64Adapt;
+        default: return kata::FwdKernels::Simt;
+    }
 }
 
 size_t workspace_for(const FwdShape &s, Kernels kn, const DevInfo &di, bool with_state = false) {
@@ -137,13 +149,15 @@ FwdKernels select_fwd_kernels(const FwdShape &s, int cc_major, int cc_minor, int
     if (s.dtype == KATA_F32) return FwdKernels::Simt;
     if (tc_supported(s, cc_major, cc_minor)) return FwdKernels::Tc32;
     if (tc64_supported(s, cc_major, cc_minor, num_sms)) return FwdKernels::Tc64;
-    return FwdKernels::Simt;
+    return adapt_kernels(s, cc_major, cc_minor, num_sms);
 }
 
 size_t fwd_workspace_bytes(const FwdShape &s, FwdKernels kn, int num_sms, bool with_state) {
     switch (kn) {
         case FwdKernels::Tc32: return tc_workspace_bytes(s, num_sms, with_state);
         case FwdKernels::Tc64: return tc64_workspace_bytes(s, with_state);
+        case FwdKernels::Tc32Adapt:
+        case FwdKernels::Tc64Adapt: return adapt_workspace_bytes(s, kn, num_sms, with_state);
         default: return simt_workspace_bytes(s);
     }
 }
@@ -154,6 +168,9 @@ cudaError_t fwd_launch(const FwdShape &s, FwdKernels kn, const void *q, const vo
     switch (kn) {
         case FwdKernels::Tc32: return tc_forward(s, q, k, v, out, workspace, num_sms, stream, so);
         case FwdKernels::Tc64: return tc64_forward(s, q, k, v, out, workspace, stream, so);
+        case FwdKernels::Tc32Adapt:
+        case FwdKernels::Tc64Adapt:
+            return adapt_forward(s, kn, q, k, v, out, workspace, num_sms, stream, so);
         default: return simt_forward(s, q, k, v, out, workspace, stream, so);
     }
 }
@@ -196,7 +213,8 @@ int kata_fwd_segments(int B, int H, int T, int d, int dv, int C, int dtype, int 
     DevInfo di;
     if ((rc = device_info(di))) return rc;
     const FwdShape s{B, H, T, d, dv, C, dtype};
-    if (select_kernels(s, di) == kTc32) return kata::tc_segments(s, di.sms, seg_tokens);
+    const Kernels kn = select_kernels(s, di);
+    if (kn == kTc32 || kn == kTc32Adapt) return kata::tc_segments(s, di.sms, seg_tokens);
     if (seg_tokens) *seg_tokens = T;
     return 1;
 }

@@ -174,12 +174,25 @@ int tc64_take_error();
 // The kernel family a plain (full-map) chunked forward runs on, its workspace
 // size and its launch; shared by kata_fwd_chunked and kata_fwd_chunked_noalloc
 // so that both take the same path for the same shape.
-enum class FwdKernels { Simt, Tc32, Tc64 };
+// Tc32Adapt / Tc64Adapt: a bf16 shape the tensor-core kernels do not take
+// directly (d = 16, or dv != 64) run on them through scratch copies
+// (kata_adapt.cu).
+enum class FwdKernels { Simt, Tc32, Tc64, Tc32Adapt, Tc64Adapt };
 FwdKernels select_fwd_kernels(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
 size_t fwd_workspace_bytes(const FwdShape &s, FwdKernels kn, int num_sms, bool with_state = false);
 cudaError_t fwd_launch(const FwdShape &s, FwdKernels kn, const void *q, const void *k,
                        const void *v, void *out, void *workspace, int num_sms,
                        cudaStream_t stream, const StateOut &so = StateOut{});
+
+// ---- other bf16 shapes on the tensor-core kernels: kata_adapt.cu -----------
+// Tc32Adapt or Tc64Adapt when q, k padded to d = 32 (d = 16) and v cut into
+// 64-column parts fit one of the two tensor-core paths; Simt otherwise (also
+// for the shapes those paths take directly).
+FwdKernels adapt_kernels(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
+size_t adapt_workspace_bytes(const FwdShape &s, FwdKernels core, int num_sms, bool with_state);
+cudaError_t adapt_forward(const FwdShape &s, FwdKernels core, const void *q, const void *k,
+                          const void *v, void *out, void *workspace, int num_sms,
+                          cudaStream_t stream, const StateOut &so);
 
 // ---- quadratic (flash-style) forward: kata_quad.cu ------------------------
 bool quad_supported(const FwdShape &s, int cc_major, int cc_minor);

@@ -56,7 +56,10 @@ def _fwd_case(kg, w, call):
     ("long_ctx_bf16", dict(B=2, H=3, T=129)),    # one-token last chunk
     ("lm_layer_bf16", dict(B=2, H=19, T=300)),   # d = 64 tensor path
     ("small_fp32", dict(B=2, H=3, T=97)),        # CUDA cores
-    ("mid_bf16", dict(B=1, H=2, T=77, dv=128)),  # CUDA cores, dv = 128
+    ("mid_bf16", dict(B=1, H=2, T=77, dv=128)),  # tensor path, two v parts
+    ("mid_bf16", dict(B=1, H=3, T=130, d=16, dv=16)),   # q, k padded to d = 32
+    ("lm_layer_bf16", dict(B=1, H=38, T=129, dv=32)),   # d = 64 kernels, one v part
+    ("lm_layer_bf16", dict(B=1, H=37, T=100, dv=128)),  # CUDA cores, dv = 128
 ])
 def test_chunked_forward_stays_in_bounds(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)

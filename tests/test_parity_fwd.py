@@ -133,7 +133,10 @@ def _sample_rows(w, heads, rng, per_head=24, extra=()):
 def test_full_size_sampled_rows(kg, name):
     """Full workload size, the exact call the benchmark times, checked on
     sampled rows computed one by one by the oracle."""
-    w = workloads.WORKLOADS[name]
+    _sampled_check(kg, workloads.WORKLOADS[name], name)
+
+
+def _sampled_check(kg, w, name):
     q, k, v = workloads.make_qkv(w, device="cuda")
     out = kg.kata_fwd_chunked(q, k, v, w.C)
     torch.cuda.synchronize()
@@ -222,9 +225,57 @@ def test_d64_tensor_path(kg, B, H, T):
     assert kg.kata_sync_status() == kg.KATA_OK
 
 
-def test_d64_few_heads_use_cuda_cores(kg):
+# bf16 shapes outside the tensor kernels' own (d = 16, or dv != 64): q and k
+# padded with zero columns to d = 32, v cut into 64-column parts, each part one
+# forward on the kernels (exact: the padding adds zero features, and output
+# columns depend on their own v column only).
+_ADAPTED = [
+    (16, 16, 1, 2, 1100),    # nine one-chunk segments per head
+    (16, 64, 2, 3, 129),     # last chunk holds one token
+    (16, 128, 1, 2, 700),    # two v parts
+    (16, 32, 3, 1, 5),       # a single partial chunk
+    (32, 16, 1, 2, 1100),
+    (32, 32, 2, 2, 517),
+    (32, 128, 1, 3, 1100),
+    (64, 16, 1, 38, 300),    # the d = 64 kernels (38 heads or more)
+    (64, 32, 2, 19, 129),
+    (64, 128, 1, 38, 300),
+]
+
+
+@pytest.mark.parametrize("d,dv,B,H,T", _ADAPTED)
+def test_adapted_shapes_take_the_tensor_path(kg, d, dv, B, H, T):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=B, H=H, T=T, d=d, dv=dv, C=64)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    _check_full(kg, q, k, v, w.C)
+    assert kg.kata_sync_status() == kg.KATA_OK
+    if d < 64 and torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert kg.kata_fwd_segments(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == _segments(B * H, T, 1)
+
+
+@pytest.mark.parametrize("d,dv", [(16, 128), (32, 16)])
+def test_adapted_shapes_long_context_sampled_rows(kg, d, dv):
+    """The long-context shape (B=1, H=16, T=131072) at the other head sizes,
+    on sampled rows (segment seams included)."""
+    w = workloads.WORKLOADS["long_ctx_bf16"].scaled(d=d, dv=dv)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    _sampled_check(kg, w, f"long_ctx d={d} dv={dv}")
+
+
+def test_adapted_shapes_deterministic(kg):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=1100, d=16, dv=128)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked(q, k, v, w.C)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+def test_d64_few_heads_use_cuda_cores(kg, dv):
     """Fewer than 38 heads at d = 64 would leave SMs idle on the split path."""
-    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=37, T=200)
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=37, T=200, dv=dv)
     assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_SIMT
     q, k, v = workloads.make_qkv(w)
     _check_full(kg, q, k, v, w.C)

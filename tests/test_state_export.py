@@ -67,12 +67,27 @@ def test_state_tensor_path(kg, B, H, T):
 @pytest.mark.parametrize("name,overrides", [
     ("small_fp32", dict(B=2, H=3, T=300)),
     ("small_fp32", dict(B=1, H=2, T=97, d=32, dv=64, C=32)),
-    ("lm_layer_bf16", dict(B=1, H=2, T=333)),           # d = 64: CUDA-core path in bf16
-    ("mid_bf16", dict(B=1, H=2, T=200, dv=128, C=64)),  # dv = 128: CUDA-core path
+    ("lm_layer_bf16", dict(B=1, H=2, T=333)),           # d = 64, 2 heads: CUDA-core path in bf16
+    ("lm_layer_bf16", dict(B=1, H=2, T=333, dv=128)),
 ])
 def test_state_cuda_core_path(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)
     _check_state(kg, w, kg.KATA_PATH_SIMT)
+
+
+@pytest.mark.parametrize("d,dv,B,H,T", [
+    (32, 128, 1, 2, 200),    # two v parts, one column block of the state each
+    (16, 16, 1, 2, 1100),    # q, k padded to d = 32: 136 of the 528 features kept
+    (16, 128, 3, 1, 129),
+    (32, 32, 2, 2, 5),
+    (64, 128, 2, 19, 300),   # the d = 64 kernels, two v parts
+])
+def test_state_adapted_shapes(kg, d, dv, B, H, T):
+    """bf16 shapes the tensor kernels take through padded q, k and 64-column
+    parts of v: each part's state is a column block of the state, and the
+    padded features that mix in a zero column are dropped."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=B, H=H, T=T, d=d, dv=dv, C=64)
+    _check_state(kg, w, kg.KATA_PATH_TC)
 
 
 @pytest.mark.parametrize("B,H,T", [
@@ -91,6 +106,7 @@ def test_state_d64_tensor_path(kg, B, H, T):
 @pytest.mark.parametrize("name,overrides", [
     ("long_ctx_bf16", dict(B=2, H=2, T=1000)),
     ("small_fp32", dict(B=1, H=2, T=150)),
+    ("long_ctx_bf16", dict(B=1, H=3, T=700, d=16, dv=128)),   # padded q, k; two v parts
 ])
 def test_prefill_then_decode(kg, name, overrides):
     """Forward over T-1 tokens with state export, then one decode step with

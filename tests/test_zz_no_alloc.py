@@ -43,6 +43,7 @@ def _noalloc_raw(kg, q, k, v, out, C):
     ("lm_layer_bf16", dict(B=1, H=38, T=300)),     # d = 64 tensor path (state over 4 CTAs)
     ("lm_layer_bf16", dict(B=1, H=64, T=256)),     # d = 64 tensor path, ~17 MB of scratch
     ("small_fp32", dict()),                        # CUDA-core fp32 path
+    ("mid_bf16", dict(B=1, H=4, T=1000, d=16, dv=128)),   # padded q, k; two v parts
 ])
 def test_noalloc_matches_allocating_forward_twice(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)
