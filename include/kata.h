@@ -189,9 +189,13 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
  * while T is short against n = d(d+1)/2.  The weights are non-negative, so no
  * running maximum is kept.
  *   q, k, v, out, B, H, T, d, dv, dtype, stream: as kata_fwd_chunked (no C).
- *   Supported: bf16, d in {32, 64}, dv = 64, on sm_103a (KATA_ERR_UNSUPPORTED
- *   otherwise).  Rounding as the tensor-core chunked path (P in bf16 as an MMA
- *   operand, fp32 accumulation and denominators).  No workspace.
+ *   Supported: bf16 on sm_103a (KATA_ERR_UNSUPPORTED otherwise).  The kernel
+ *   takes d in {32, 64} with dv = 64 and needs no workspace; the other head
+ *   sizes (d = 16, dv in {16, 32, 128}) run on it as kata_fwd_chunked runs them
+ *   (q, k padded to d = 32, v in 64-column parts, one pass per part), with a
+ *   workspace for those copies allocated and freed stream-ordered inside the
+ *   call (KATA_ERR_ALLOC if that fails).  Rounding as the tensor-core chunked
+ *   path (P in bf16 as an MMA operand, fp32 accumulation and denominators).
  */
 int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, int B, int H,
                        int T, int d, int dv, int dtype, kata_stream_t stream);
@@ -239,7 +243,10 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
  * the chunk-local cumulative log2 of the gates (a gate below 2^-126 counts as
  * 2^-126 there: a zero gate leaves a weight of at most 2^-126 on the writes
  * before it within the chunk).  bf16 inputs with d = 64, dv = 64 and T <= 262144
- * take the tensor cores as well.  The output comes from the gated quadratic form
+ * take the tensor cores as well.  The other bf16 head sizes (d = 16, dv in {16,
+ * 32, 128}) run on these two routes as kata_fwd_chunked runs them (q, k padded
+ * to d = 32, v in 64-column parts; gates act on the weights only, so each part
+ * is one gated forward), under the same bounds.  The output comes from the gated quadratic form
  * (kata_fwd_quadratic_gated), which evaluates the same weights tile by tile.
  * The state is sum_s A_s psi(k_s) v_s^T, A_s the product of the gates after s,
  * and psi is quadratic, so the state comes from the chunked d = 64 tensor path
@@ -339,8 +346,9 @@ typedef enum {
 /*
  * kata_fwd -- the forward in whichever exact form is faster for the shape:
  * the quadratic form (kata_fwd_quadratic) where it is supported and T is at
- * most a head-dimension-dependent crossover (6144 tokens at d = 32, 8192 at
- * d = 64, from measurements of both forms on GB300), else the chunked form
+ * most a head-dimension-dependent crossover (6144 tokens at d = 32 and d = 16,
+ * which runs the d = 32 kernels; 8192 at d = 64; from measurements of both
+ * forms on GB300), else the chunked form
  * (kata_fwd_chunked).  Both compute the same o_t; they differ in rounding
  * only.  Arguments, layouts and errors as kata_fwd_chunked (C is used by the
  * chunked form).  kata_fwd_form tells which form a shape takes.
@@ -352,7 +360,7 @@ int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype);
 /*
  * kata_fwd_gated -- GatedKATA in whichever exact form is faster for the shape:
  * the gated quadratic form (kata_fwd_quadratic_gated) where it is supported and
- * T <= 10240 (d = 32) or T <= 65536 (d = 64), else the gated chunked form
+ * T <= 10240 (d = 16 or 32) or T <= 65536 (d = 64), else the gated chunked form
  * (kata_fwd_chunked_gated, no state export).  The bounds come from the
  * measured per-token costs of both forms on GB300 (bf16, dv = 64): the
  * quadratic form's grows with T (1.1 ns per token and head at T = 8192, 1.9 at

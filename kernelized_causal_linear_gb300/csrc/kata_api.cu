@@ -318,6 +318,27 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
     return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{}, ms);
 }
 
+// The quadratic form of a shape its kernels take through the rewritings of
+// kata_adapt.cu (d = 16, dv != 64), with a stream-ordered workspace.
+static int adapted_quadratic(const FwdShape &s, const void *q, const void *k, const void *v,
+                             void *out, cudaStream_t st, const float *gamma, int normalize) {
+    cudaGetLastError();
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, kata::adapt_quad_workspace_bytes(s, gamma != nullptr), st) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_ALLOC;
+    }
+    cudaError_t e = kata::adapt_quad_forward(s, q, k, v, out, ws, st, gamma, normalize);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
 int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, int B, int H,
                        int T, int d, int dv, int dtype, kata_stream_t stream) {
     if (!q || !k || !v || !out) return KATA_ERR_ARG;
@@ -331,14 +352,17 @@ int kata_fwd_quadratic(const void *q, const void *k, const void *v, void *out, i
     DevInfo di;
     if ((rc = device_info(di))) return rc;
     const FwdShape s{B, H, T, d, dv, 64, dtype};
-    if (!kata::quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
-    cudaGetLastError();
-    if (kata::quad_forward(s, q, k, v, out, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (kata::quad_supported(s, di.major, di.minor)) {
         cudaGetLastError();
-        return KATA_ERR_CUDA;
+        if (kata::quad_forward(s, q, k, v, out, st) != cudaSuccess) {
+            cudaGetLastError();
+            return KATA_ERR_CUDA;
+        }
+        return KATA_OK;
     }
-    return KATA_OK;
+    if (!kata::adapt_quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
+    return adapted_quadratic(s, q, k, v, out, st, nullptr, 1);
 }
 
 int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const float *gamma,
@@ -359,9 +383,12 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
     DevInfo di;
     if ((rc = device_info(di))) return rc;
     const FwdShape s{B, H, T, d, dv, 64, dtype};
-    if (!kata::quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
-    cudaGetLastError();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!kata::quad_supported(s, di.major, di.minor)) {
+        if (!kata::adapt_quad_supported(s, di.major, di.minor)) return KATA_ERR_UNSUPPORTED;
+        return adapted_quadratic(s, q, k, v, out, st, gamma, normalize);
+    }
+    cudaGetLastError();
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, kata::quad_gated_workspace_bytes(s), st) != cudaSuccess) {
         cudaGetLastError();
@@ -387,9 +414,11 @@ int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype) {
     DevInfo di;
     if (device_info(di)) return KATA_FORM_NONE;
     const FwdShape s{B, H, T, d, dv, 64, dtype};
-    return (kata::quad_supported(s, di.major, di.minor) && T <= quadratic_crossover(d))
-               ? KATA_FORM_QUADRATIC
-               : KATA_FORM_CHUNKED;
+    const bool quad = kata::quad_supported(s, di.major, di.minor) ||
+                      kata::adapt_quad_supported(s, di.major, di.minor);
+    // d = 16 runs the kernels of d = 32
+    return (quad && T <= quadratic_crossover(d < 32 ? 32 : d)) ? KATA_FORM_QUADRATIC
+                                                               : KATA_FORM_CHUNKED;
 }
 
 int kata_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int T, int d,
@@ -583,13 +612,19 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     if ((rc = device_info(di))) return rc;
     cudaGetLastError();
     const FwdShape s{B, H, T, d, dv, C, dtype};
+    const bool with_state = state != nullptr;
     const bool tc = kata::tc_supported(s, di.major, di.minor);
-    const bool wide = !tc && kata::gated_wide_supported(s, di.major, di.minor, di.sms, state != nullptr);
+    const bool wide = !tc && kata::gated_wide_supported(s, di.major, di.minor, di.sms, with_state);
+    const kata::GatedCore ad = tc || wide ? kata::GatedCore::None
+                                          : kata::adapt_gated_core(s, di.major, di.minor, di.sms,
+                                                                   with_state);
+    const bool adapt = ad != kata::GatedCore::None;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    const size_t wsb = tc     ? kata::tc_gated_workspace_bytes(s, di.sms, state != nullptr)
-                       : wide ? kata::gated_wide_workspace_bytes(s, state != nullptr)
-                              : kata::gated_workspace_bytes(s);
+    const size_t wsb = tc      ? kata::tc_gated_workspace_bytes(s, di.sms, with_state)
+                       : wide  ? kata::gated_wide_workspace_bytes(s, with_state)
+                       : adapt ? kata::adapt_gated_workspace_bytes(s, ad, di.sms, with_state)
+                               : kata::gated_workspace_bytes(s);
     if (cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
@@ -598,9 +633,11 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
     so.state = state;
     so.z = z;
     cudaError_t e =
-        tc     ? kata::tc_forward_gated(s, q, k, v, gamma, out, ws, di.sms, st, so, normalize)
-        : wide ? kata::gated_wide_forward(s, q, k, v, gamma, out, ws, st, so, normalize)
-               : kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
+        tc      ? kata::tc_forward_gated(s, q, k, v, gamma, out, ws, di.sms, st, so, normalize)
+        : wide  ? kata::gated_wide_forward(s, q, k, v, gamma, out, ws, st, so, normalize)
+        : adapt ? kata::adapt_gated_forward(s, ad, q, k, v, gamma, out, ws, di.sms, st, so,
+                                            normalize)
+                : kata::gated_forward(s, q, k, v, gamma, out, ws, st, so, normalize);
     const cudaError_t ef = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = ef;
     if (e != cudaSuccess) {
@@ -625,7 +662,9 @@ int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype) {
     if (device_info(di)) return KATA_PATH_NONE;
     const FwdShape s{B, H, T, d, dv, C, dtype};
     return kata::tc_supported(s, di.major, di.minor) ||
-                   kata::gated_wide_supported(s, di.major, di.minor, di.sms, false)
+                   kata::gated_wide_supported(s, di.major, di.minor, di.sms, false) ||
+                   kata::adapt_gated_core(s, di.major, di.minor, di.sms, false) !=
+                       kata::GatedCore::None
                ? KATA_PATH_TC
                : KATA_PATH_SIMT;
 }
@@ -635,9 +674,10 @@ int kata_fwd_gated_form(int B, int H, int T, int d, int dv, int C, int dtype) {
     DevInfo di;
     if (device_info(di)) return KATA_FORM_NONE;
     const FwdShape s{B, H, T, d, dv, 64, dtype};
-    return (kata::quad_supported(s, di.major, di.minor) && T <= gated_quadratic_max_t(d))
-               ? KATA_FORM_QUADRATIC
-               : KATA_FORM_CHUNKED;
+    const bool quad = kata::quad_supported(s, di.major, di.minor) ||
+                      kata::adapt_quad_supported(s, di.major, di.minor);
+    return (quad && T <= gated_quadratic_max_t(d < 32 ? 32 : d)) ? KATA_FORM_QUADRATIC
+                                                                 : KATA_FORM_CHUNKED;
 }
 
 int kata_fwd_gated(const void *q, const void *k, const void *v, const float *gamma, void *out,

@@ -85,6 +85,19 @@ def test_gated_and_quadratic_stay_in_bounds(kg, d, T):
     assert torch.equal(gate, g_before)
 
 
+@pytest.mark.parametrize("d,dv,T", [(16, 128, 300), (32, 16, 1100), (64, 32, 129)])
+def test_adapted_gated_and_quadratic_stay_in_bounds(kg, d, dv, T):
+    """Other bf16 head sizes (padded q, k; 64-column parts of v) in the gated
+    chunked and both quadratic forms."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=T, d=d, dv=dv, C=64)
+    gate = workloads.make_gate(w, device="cuda")
+    g_before = gate.clone()
+    _fwd_case(kg, w, lambda q, k, v, out: kg.kata_fwd_chunked_gated(q, k, v, gate, w.C, out=out))
+    _fwd_case(kg, w, lambda q, k, v, out: kg.kata_fwd_quadratic(q, k, v, out=out))
+    _fwd_case(kg, w, lambda q, k, v, out: kg.kata_fwd_quadratic_gated(q, k, v, gate, out=out))
+    assert torch.equal(gate, g_before)
+
+
 def test_decode_stays_in_bounds(kg):
     w = workloads.DECODE.scaled(B=4, H=3)
     q, k, v = (t.cuda() for t in workloads.make_decode_inputs(w))

@@ -348,14 +348,19 @@ def test_maximum_head_count(kg, form):
         assert slice_rel_err(to_f64(out[sl]), ref) <= TOL[w.dtype], (form, b, h)
 
 
-@pytest.mark.parametrize("name,T,form", [("lm_layer_bf16", 700, "quadratic"),
-                                         ("mid_bf16", 4096, "quadratic"),
-                                         ("recall_bf16", 8192, "chunked"),
-                                         ("small_fp32", 256, "chunked")])
-def test_fwd_picks_the_faster_form(kg, name, T, form):
+@pytest.mark.parametrize("name,T,form,dims", [("lm_layer_bf16", 700, "quadratic", None),
+                                              ("mid_bf16", 4096, "quadratic", None),
+                                              ("recall_bf16", 8192, "chunked", None),
+                                              ("small_fp32", 256, "chunked", None),
+                                              ("mid_bf16", 2000, "quadratic", (16, 128)),
+                                              ("lm_layer_bf16", 700, "quadratic", (64, 32)),
+                                              ("mid_bf16", 7000, "chunked", (16, 32))])
+def test_fwd_picks_the_faster_form(kg, name, T, form, dims):
     """kata_fwd: the quadratic form up to the crossover on the tensor cores, the
     chunked form beyond it and for fp32; sampled rows against the oracle."""
     w = workloads.WORKLOADS[name].scaled(B=1, H=2, T=T)
+    if dims is not None:
+        w = w.scaled(d=dims[0], dv=dims[1])
     want = kg.KATA_FORM_QUADRATIC if form == "quadratic" else kg.KATA_FORM_CHUNKED
     assert kg.kata_fwd_form(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == want
     q, k, v = workloads.make_qkv(w)

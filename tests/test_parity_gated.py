@@ -184,6 +184,22 @@ def test_gated_quadratic_parity(kg, normalize, d, T):
     assert err <= TOL[torch.bfloat16], f"d={d} T={T} normalize={normalize}: {err:.3e}"
 
 
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dv", [(16, 64), (16, 128), (32, 16), (64, 32), (64, 128)])
+def test_gated_quadratic_adapted_shapes(kg, normalize, d, dv):
+    """Other bf16 head sizes in the gated quadratic form: q, k padded to d = 32,
+    v in 64-column parts, each part one pass of the kernel."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=2, H=2, T=300, d=d, dv=dv, C=128)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out = kg.kata_fwd_quadratic_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), normalize)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[torch.bfloat16], f"d={d} dv={dv} normalize={normalize}: {err:.3e}"
+
+
 @pytest.mark.parametrize("T", [1, 127, 128, 129])
 def test_gated_quadratic_ragged(kg, T):
     w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=T, C=128)
@@ -473,3 +489,82 @@ def test_gated_d64_few_heads_state_on_cuda_cores(kg):
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
     S_ref, _ = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
     assert slice_rel_err(to_f64(S), S_ref) <= 1e-4
+
+
+# ---- other bf16 head sizes (d = 16, dv != 64) on the gated tensor routes: q, k
+# padded to d = 32, v in 64-column parts, each part one gated forward
+_ADAPTED_GATED = [
+    (16, 64, 1, 2, 1100),    # the d = 32 gated segments, q and k padded
+    (16, 128, 2, 2, 300),
+    (32, 16, 1, 3, 700),
+    (32, 128, 1, 2, 1100),
+    (64, 32, 1, 2, 300),     # d = 64: output from the gated quadratic form
+    (64, 128, 2, 2, 129),
+]
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dv,B,H,T", _ADAPTED_GATED)
+def test_gated_adapted_shapes(kg, normalize, d, dv, B, H, T):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=B, H=H, T=T, d=d, dv=dv, C=128)
+    assert kg.kata_fwd_path_gated(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    _check(kg, w, _gates(w), normalize)
+    assert kg.kata_sync_status() == kg.KATA_OK
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("d,dv,B,H,T", [
+    (16, 128, 1, 2, 1100),   # padded features gathered, two column blocks
+    (32, 32, 2, 2, 300),
+    (64, 128, 2, 19, 300),   # d = 64: the state from the chunked d = 64 kernels
+])
+def test_gated_adapted_shapes_state(kg, normalize, d, dv, B, H, T):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=B, H=H, T=T, d=d, dv=dv, C=128)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out, S, z = kg.kata_fwd_chunked_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C, normalize,
+                                          with_state=True)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), normalize)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+    S_ref, z_ref = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(S), S_ref) <= 1e-2
+    assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= 1e-2
+
+
+def test_gated_adapted_prefill_then_decode(kg):
+    """Gated prefill at d = 16, dv = 128 on the tensor route, then a gated decode
+    step from the exported state: the definition's output at the last row."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=500, d=16, dv=128, C=128)
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    Tp = w.T - 1
+    g[..., Tp] = 0.9   # a reset here would make the step's output independent of the state
+    sl = (slice(None), slice(None), slice(0, Tp))
+    _, S, z = kg.kata_fwd_chunked_gated(q[sl].contiguous().cuda(), k[sl].contiguous().cuda(),
+                                        v[sl].contiguous().cuda(), g[sl].contiguous().cuda(),
+                                        w.C, True, with_state=True)
+    o = kg.kata_decode_step_gated(S, z, q[..., Tp, :].contiguous().cuda(),
+                                  k[..., Tp, :].contiguous().cuda(),
+                                  v[..., Tp, :].contiguous().cuda(), g[..., Tp].contiguous().cuda())
+    torch.cuda.synchronize()
+    full = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g))
+    assert slice_rel_err(to_f64(o)[:, :, None, :], full[:, :, Tp:Tp + 1, :]) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("d,dv,T,form", [(16, 128, 300, "quadratic"), (32, 16, 20000, "chunked")])
+def test_gated_auto_form_adapted_shapes(kg, d, dv, T, form):
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=2, T=T, d=d, dv=dv, C=128)
+    want = {"quadratic": kg.KATA_FORM_QUADRATIC, "chunked": kg.KATA_FORM_CHUNKED}[form]
+    assert kg.kata_fwd_gated_form(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == want
+    q, k, v = workloads.make_qkv(w)
+    g = _gates(w)
+    out = kg.kata_fwd_gated(q.cuda(), k.cuda(), v.cuda(), g.cuda(), w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    rows = np.array(sorted(set([0, 1, 127, 128, T // 2, T - 1, T + 3, 2 * T - 1])),
+                    dtype=np.int64)
+    ref = oracle.forward_rows_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g), rows)
+    got = to_f64(out).reshape(-1, w.dv)[rows]
+    assert slice_rel_err(got, ref) <= TOL[w.dtype]

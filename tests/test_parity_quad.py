@@ -68,6 +68,16 @@ def test_quadratic_deterministic(kg):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("d,dv", [(16, 16), (16, 64), (16, 128), (32, 32), (32, 128), (64, 16),
+                                  (64, 128)])
+@pytest.mark.parametrize("T", [129, 300])
+def test_quadratic_adapted_shapes(kg, d, dv, T):
+    """Other bf16 head sizes: q, k padded to d = 32 and v in 64-column parts, each
+    part one pass of the quadratic kernel."""
+    w = workloads.WORKLOADS["mid_bf16"].scaled(B=1, H=3, T=T, d=d, dv=dv)
+    _check(kg, *workloads.make_qkv(w))
+
+
 def test_quadratic_unsupported_shapes(kg):
     w = workloads.WORKLOADS["small_fp32"]
     q, k, v = (t.cuda() for t in workloads.make_qkv(w))
