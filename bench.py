@@ -181,6 +181,20 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     if stage == "tc64_finalize":
         # reads four fp32 partial numerators and the denominator, writes bf16 out
         return float(BH * T) * (4 * dv * 4 + 4 + dv * 2), "GB/s", "hbm"
+    # explicit-feature tensor path (reduced maps with few features): the lift reads
+    # q or k and writes its features (n rounded up to 8, bf16), the state kernel
+    # forms Phi_K^T V per chunk (tensor) and writes an fp32 record [n][65], the scan
+    # reads and writes the records, the output kernel forms Phi_Q Phi_K^T, Phi_Q
+    # S_pre and P V (tensor; algorithmic: the inter term and the causal pairs)
+    if stage == "tc_feat_lift":
+        return float(BH * T) * (d * 2 + ((n + 7) // 8 * 8) * 2), "GB/s", "hbm"
+    if stage == "tc_feat_state":
+        return 2.0 * n * dv * T * BH, "TFLOP/s", "tensor"
+    if stage == "tc_feat_scan":
+        return 2.0 * 4 * n * (dv + 1) * -(-T // 128) * BH, "GB/s", "hbm"
+    if stage == "tc_feat_output":
+        return (2.0 * n * (dv + 1) * T * BH +
+                2.0 * (n + dv + 1) * _intra_pairs(T, 128) * BH), "TFLOP/s", "tensor"
     # other bf16 head sizes on the tensor kernels: q or k padded to 32 columns
     # (one launch each), v cut into 64-column parts, each part's output columns
     # copied out, each part's state gathered (w: the v columns of one part)
@@ -262,6 +276,7 @@ def call_flops(w, fm: FeatureMap = FULL_MAP, algo: str = "chunked") -> float:
 _STAGE_SOURCE = (("tc_segment", "kata_tc.cu"), ("tc_pair", "kata_tc_pair.cu"),
                  ("tc_gated", "kata_tc.cu"), ("tc_sub_finalize", "kata_tc.cu"),
                  ("tc_m4", "kata_tc.cu"), ("tc_adapt", "kata_adapt.cu"),
+                 ("tc_feat", "kata_feat.cu"),
                  ("tc_sigma", "kata_sigma.cu"),
                  ("tc64", "kata_tc64.cu"), ("tc_quadratic", "kata_quad.cu"),
                  ("tc_gate_prep", "kata_quad.cu"), ("simt", "kata_simt.cu"),

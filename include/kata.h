@@ -174,8 +174,19 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   summed in fp32 in 128-token chunks.
  *   KATA-M_4: four sub-heads on the 16-wide blocks, each zero-padded to 32
  *   columns in scratch (the zero coordinates add nothing to (q_a . k_a)^2).
- * The other reduced maps run on CUDA cores in fp32 (bf16 inputs are widened;
- * the output is written in the input type).  kata_fwd_path_map tells which.
+ * With bf16 inputs and dv = 64, the other maps with at most 192 packed features
+ * (KATA-Sigma_4 at d = 64; Sigma_2, Sigma_4 and M_4 at d = 32; every map at
+ * d = 16; the orthant map) run on the tensor cores with their features written
+ * out: psi of every q and k row in two bf16 parts (psi = hi + lo to ~2^-16),
+ * per 128-token chunk the state Psi(K)^T V from the hi part and an fp32 record
+ * [n][dv + 1], the chunk scan, and per chunk the output with the intra-chunk
+ * weights Psi(Q) Psi(K)^T from the hi and lo parts (the weights are signed sums
+ * that can be much smaller than the features; bf16 parts alone would leave
+ * them ~2^-9 |psi(q)| |psi(k)| off) and Psi(Q) S_pre from the hi part.  Scratch
+ * per token and head: 8 n bytes of features plus the records, about 260 n
+ * bytes per 128-token chunk.  The other reduced maps run on CUDA cores in fp32
+ * (bf16 inputs are widened; the output is written in the input type).
+ * kata_fwd_path_map tells which.
  */
 int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
                          int T, int d, int dv, int C, int dtype, int map, int g, float eps,

@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "../../include/kata.h"
+#include "kata_feat.cuh"
 #include "kata_internal.cuh"
 
 using kata::FwdShape;
@@ -89,7 +90,9 @@ int device_info(DevInfo &out) {
 // kTc32M4 is KATA-M_4 at d = 64 as four zero-padded d = 32 sub-heads;
 // kTc32Adapt / kTc64Adapt run the other bf16 shapes (d = 16, dv != 64) on the
 // two tensor-core paths through padded copies and 64-column parts of v.
-enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt };
+// kFeat: a reduced map with at most kFeatMax packed features on the explicit-
+// feature tensor path (kata_feat.cu).
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt, kFeat };
 
 Kernels from_fwd(kata::FwdKernels k) {
     switch (k) {
@@ -106,8 +109,10 @@ Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
 }
 
 // Kernels for a reduced map: KATA-M_2, KATA-Sigma_2 and KATA-M_4 at d = 64 are
-// d = 32 sub-heads on the d = 32 tensor path (bf16, dv = 64); every other
-// reduced map runs on CUDA cores.
+// d = 32 sub-heads on the d = 32 tensor path (bf16, dv = 64); the other maps
+// with at most kFeatMax packed features (KATA-Sigma_4 at d = 64; Sigma_2,
+// Sigma_4 and M_4 at d = 32; every map at d = 16; the orthant map) take the
+// explicit-feature tensor path (bf16, dv = 64); the rest runs on CUDA cores.
 Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
                            bool with_state) {
     if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
@@ -120,6 +125,7 @@ Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::Map
             if (map.kind == KATA_MAP_BLOCK && map.g == 4) return kTc32M4;
         }
     }
+    if (!with_state && kata::feat_supported(s, map, di.major, di.minor)) return kFeat;
     return kSimt;
 }
 
@@ -252,6 +258,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     const size_t wsb = kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
                        : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
                        : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
+                       : kn == kFeat      ? kata::feat_workspace_bytes(s, map)
                        : map.kind == 0    ? workspace_for(s, kn, di, with_state)
                                           : kata::simt_workspace_bytes(s, map);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -264,6 +271,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
         kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
         : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
         : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
+        : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map)
         : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
                            : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
@@ -727,9 +735,9 @@ int kata_sync_status(kata_stream_t stream) {
         return KATA_ERR_CUDA;
     }
     const int e = kata::tc_take_error(), e64 = kata::tc64_take_error(), eq = kata::quad_take_error(),
-              ep = kata::pair_take_error();
-    if (e < 0 || e64 < 0 || eq < 0 || ep < 0) return KATA_ERR_CUDA;
-    return (e | e64 | eq | ep) ? KATA_ERR_TIMEOUT : KATA_OK;
+              ep = kata::pair_take_error(), ef = kata::feat_take_error();
+    if (e < 0 || e64 < 0 || eq < 0 || ep < 0 || ef < 0) return KATA_ERR_CUDA;
+    return (e | e64 | eq | ep | ef) ? KATA_ERR_TIMEOUT : KATA_OK;
 }
 
 int kata_test_arm_stall(void) {

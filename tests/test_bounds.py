@@ -66,10 +66,14 @@ def test_chunked_forward_stays_in_bounds(kg, name, overrides):
     _fwd_case(kg, w, lambda q, k, v, out: kg.kata_fwd_chunked(q, k, v, w.C, out=out))
 
 
-@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4)])
-def test_map_sub_heads_stay_in_bounds(kg, map_, g):
-    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=333)
-    eps, scale = (1e-4, 1.0) if map_ == kg.KATA_MAP_SUM else (0.0, 1.0)
+@pytest.mark.parametrize("map_,g,d", [(1, 2, 64), (2, 2, 64), (1, 4, 64), (2, 4, 64), (1, 4, 32),
+                                      (3, 1, 16)])
+def test_map_sub_heads_stay_in_bounds(kg, map_, g, d):
+    """Sub-head routes at d = 64 and the explicit-feature path (Sigma_4, M_4 at
+    d = 32, the orthant map)."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=333, d=d)
+    eps, scale = ((1e-4, 1.0) if map_ == kg.KATA_MAP_SUM else (1e-6, 1.0) if map_ == 3
+                  else (0.0, 1.0))
     _fwd_case(kg, w, lambda q, k, v, out: kg.kata_fwd_chunked_map(q, k, v, w.C, map_, g, eps,
                                                                   scale, out=out))
 

@@ -78,9 +78,10 @@ def test_map_lift_parity(kg, map_, g, d, dtype):
     assert err <= 1e-6
 
 
-@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4)])
+@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4), (2, 4)])
 def test_map_full_size_sampled_rows(kg, map_, g):
-    """The LM-layer workload with M_2 / Sigma_2 / M_4, sampled rows against the oracle."""
+    """The LM-layer workload with M_2 / Sigma_2 / M_4 / Sigma_4, sampled rows
+    against the oracle."""
     w = workloads.WORKLOADS["lm_layer_bf16"]
     q, k, v = workloads.make_qkv(w, device="cuda")
     eps, scale = _params(kg, map_, g)
@@ -204,18 +205,104 @@ def test_m4_tensor_path_zero_block(kg):
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
 
 
-def test_other_maps_take_cuda_cores(kg):
+def test_map_paths(kg):
+    """bf16, dv = 64: M_2, Sigma_2, M_4 at d = 64 as d = 32 sub-heads; Sigma_4 at
+    d = 64, every map at d = 16 and all but M_2 / M_1 / Sigma_1 at d = 32 (more
+    than 192 features) on the explicit-feature path; fp32, other dv and the
+    larger maps on CUDA cores."""
     w = workloads.WORKLOADS["lm_layer_bf16"]
-    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 4) == \
-        kg.KATA_PATH_SIMT
-    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 1, 4) == kg.KATA_PATH_TC
-    for map_ in (1, 2):
-        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, 2) == \
-            kg.KATA_PATH_TC
-        assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, torch.float32, map_, 2) == \
-            kg.KATA_PATH_SIMT
-        assert kg.kata_fwd_path_map(w.B, w.H, w.T, 32, w.dv, w.C, w.dtype, map_, 2) == \
-            kg.KATA_PATH_SIMT
+
+    def path(d=w.d, dv=w.dv, dtype=w.dtype, map_=1, g=2):
+        return kg.kata_fwd_path_map(w.B, w.H, w.T, d, dv, w.C, dtype, map_, g)
+
+    for map_, g in ((1, 2), (2, 2), (1, 4), (2, 4)):
+        assert path(map_=map_, g=g) == kg.KATA_PATH_TC
+        assert path(d=16, map_=map_, g=g) == kg.KATA_PATH_TC
+        assert path(dtype=torch.float32, map_=map_, g=g) == kg.KATA_PATH_SIMT
+    for map_, g in ((2, 2), (1, 4), (2, 4)):
+        assert path(d=32, map_=map_, g=g) == kg.KATA_PATH_TC
+    assert path(d=32, map_=1, g=2) == kg.KATA_PATH_SIMT     # 272 features
+    assert path(d=32, map_=2, g=1) == kg.KATA_PATH_SIMT     # 528 features
+    assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_SIMT
+    for d in (16, 32, 64):
+        assert path(d=d, map_=kg.KATA_MAP_ORTHANT, g=1) == kg.KATA_PATH_TC
+
+
+# ---- explicit-feature tensor path (kata_feat.cu): the map's features written
+# out, chunk states and outputs on tcgen05 around the chunk scan
+_FEAT_MAPS = [
+    (2, 4, 64),   # Sigma_4 at the LM-layer head size: 136 features, 3 boxes, 2 blocks
+    (2, 2, 32),   # 136
+    (2, 4, 32),   # 36: one box, one block
+    (1, 4, 32),   # 144
+    (1, 2, 16),
+    (2, 2, 16),
+    (1, 4, 16),
+    (2, 4, 16),   # 10 features
+    (1, 1, 16),   # M_1 = the rank-one lift at d = 16: 136 features, weights
+                  # (q.k)^2 near zero for near-orthogonal pairs (the hi/lo X)
+    (2, 1, 16),   # Sigma_1: eps I + s x x^T
+    (3, 1, 64),   # orthant: n = d
+    (3, 1, 32),
+    (3, 1, 16),
+]
+
+
+def _feat_params(kg, map_, g):
+    return (1e-6, 1.0) if map_ == kg.KATA_MAP_ORTHANT else _params(kg, map_, g)
+
+
+def _feat_name(map_):
+    return "orthant" if map_ == 3 else NAMES[map_]
+
+
+@pytest.mark.parametrize("map_,g,d", _FEAT_MAPS)
+@pytest.mark.parametrize("B,H,T", [(1, 3, 300), (2, 2, 129), (1, 1, 5)])
+def test_feature_path_parity(kg, map_, g, d, B, H, T):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, d=d)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
+        kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    eps, scale = _feat_params(kg, map_, g)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), _feat_name(map_), g, eps, scale)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[w.dtype], f"{_feat_name(map_)}_{g} d={d}: {err:.3e}"
+
+
+def test_feature_path_deterministic(kg):
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=3, T=700)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked_map(q, k, v, w.C, 2, 4, 1e-4, 0.25)
+    b = kg.kata_fwd_chunked_map(q, k, v, w.C, 2, 4, 1e-4, 0.25)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("map_,g,d", [(2, 4, 64), (3, 1, 64)])
+def test_feature_path_long_sequence_sampled_rows(kg, map_, g, d):
+    """256 chunks per head (the two-level chunk scan), sampled rows."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=4, T=32768, d=d)
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    eps, scale = _feat_params(kg, map_, g)
+    out = kg.kata_fwd_chunked_map(q, k, v, w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    BH = w.B * w.H
+    rng = np.random.default_rng(7)
+    worst = 0.0
+    for h in range(BH):
+        ts = np.array(sorted(set([0, 1, 127, 128, 129, w.T // 2, w.T - 1] +
+                                 rng.integers(0, w.T, size=12).tolist())), dtype=np.int64)
+        ref = oracle.forward_rows_map(to_f64(q.reshape(BH, 1, w.T, w.d)[h:h + 1]),
+                                      to_f64(k.reshape(BH, 1, w.T, w.d)[h:h + 1]),
+                                      to_f64(v.reshape(BH, 1, w.T, w.dv)[h:h + 1]), ts,
+                                      _feat_name(map_), g, eps, scale)
+        got = to_f64(out.reshape(BH, w.T, w.dv)[h][ts])
+        worst = max(worst, slice_rel_err(got, ref))
+    assert worst <= TOL[w.dtype], f"{worst:.3e}"
 
 
 # ---- orthant map (psi_i = max(u_i, 0) + eps, n = d) and the two-level chunk scan
