@@ -16,7 +16,7 @@
 // A part's output and state go to scratch; their real columns and features are
 // copied to the caller's buffers.  With dv = 64 (d = 16) the one part is v
 // itself and its output is out.
-#include "kata_internal.cuh"
+#include "kata_dispatch.cuh"
 
 #include <cuda_bf16.h>
 

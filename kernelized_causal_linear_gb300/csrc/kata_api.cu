@@ -5,7 +5,7 @@
 
 #include "../../include/kata.h"
 #include "kata_feat.cuh"
-#include "kata_internal.cuh"
+#include "kata_dispatch.cuh"
 
 using kata::FwdShape;
 

@@ -39,7 +39,7 @@
 #include <mutex>
 
 #include "../../include/kata.h"
-#include "kata_internal.cuh"
+#include "kata_dispatch.cuh"
 
 namespace {
 
