@@ -78,6 +78,9 @@ def _load():
             lib.kata_oracle_forward_rows_map.argtypes = [_D, _D, _D, _I64, ctypes.c_int64, _D,
                                                          i, i, i, i, i, i, dd, dd]
             lib.kata_oracle_recurrent_map.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, dd, dd]
+            lib.kata_oracle_prefix_state_map.argtypes = [_D, _D, _D, _D, i, i, i, i, i, i, dd, dd]
+            lib.kata_oracle_decode_step_map.argtypes = [_D, _D, _D, _D, _D, _D, i, i, i, i, i, dd,
+                                                        dd]
             lib.kata_oracle_forward_gated.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i]
             lib.kata_oracle_forward_rows_gated.argtypes = [_D, _D, _D, _D, _I64, ctypes.c_int64,
                                                            _D, i, i, i, i, i]
@@ -253,6 +256,34 @@ def recurrent_map(q, k, v, map_name: str, g: int = 1, eps: float = 0.0,
     _load().kata_oracle_recurrent_map(_p(q), _p(k), _p(v), _p(out), B * H, T, d, dv,
                                       MAPS[map_name], int(g), float(eps), float(scale))
     return out
+
+
+def prefix_state_map(k, v, map_name: str, g: int = 1, eps: float = 0.0, scale: float = 1.0):
+    """(S_T, Z_T) after all T tokens under a map (Eq. 2's recurrence with the
+    map's psi), features in lift_map's packed order."""
+    k, v = _f64(k), _f64(v)
+    B, H, T, d = k.shape
+    dv = v.shape[-1]
+    n = map_dim(map_name, d, g)
+    S = np.empty((B, H, n, dv), dtype=np.float64)
+    z = np.empty((B, H, n), dtype=np.float64)
+    _load().kata_oracle_prefix_state_map(_p(k), _p(v), _p(S), _p(z), B * H, T, d, dv,
+                                         MAPS[map_name], int(g), float(eps), float(scale))
+    return S, z
+
+
+def decode_step_map(S, z, q, k, v, map_name: str, g: int = 1, eps: float = 0.0,
+                    scale: float = 1.0):
+    """One decode step under a map: returns (S', z', o) without modifying inputs."""
+    S = _f64(S).copy()
+    z = _f64(z).copy()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    out = np.empty((B, H, dv), dtype=np.float64)
+    _load().kata_oracle_decode_step_map(_p(S), _p(z), _p(q), _p(k), _p(v), _p(out), B * H, d,
+                                        dv, MAPS[map_name], int(g), float(eps), float(scale))
+    return S, z, out
 
 
 # ---------------------------------------------------------------------------

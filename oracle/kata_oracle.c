@@ -496,6 +496,67 @@ void kata_oracle_recurrent_map(const double *q, const double *k, const double *v
     }
 }
 
+/* The state pair after T tokens under a map (Eq. 2's additive recurrence with
+ * the map's psi): S = sum_t psi(k_t) v_t^T [BH][n][dv], z = sum_t psi(k_t)
+ * [BH][n], features in the packed order of kata_oracle_lift_map. */
+void kata_oracle_prefix_state_map(const double *k, const double *v, double *S, double *z,
+                                  int BH, int T, int d, int dv, int map, int g, double eps,
+                                  double s) {
+    const int n = kata_oracle_map_dim(map, d, g);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *A = malloc(sizeof(double) * (size_t)d * d);
+        memset(Sb, 0, sizeof(double) * n * dv);
+        memset(zb, 0, sizeof(double) * n);
+        for (int t = 0; t < T; ++t) {
+            const int64_t row = (int64_t)bh * T + t;
+            lift_map_one(k + row * d, d, map, g, eps, s, pk, A);
+            for (int f = 0; f < n; ++f) {
+                for (int j = 0; j < dv; ++j) Sb[(size_t)f * dv + j] += pk[f] * v[row * dv + j];
+                zb[f] += pk[f];
+            }
+        }
+        free(pk);
+        free(A);
+    }
+}
+
+/* One decode step under a map, in place: S += psi(k) v^T, z += psi(k), then
+ * o = psi(q)^T S / psi(q)^T z (0 where the denominator is not positive). */
+void kata_oracle_decode_step_map(double *S, double *z, const double *q, const double *k,
+                                 const double *v, double *out, int BH, int d, int dv, int map,
+                                 int g, double eps, double s) {
+    const int n = kata_oracle_map_dim(map, d, g);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(kata_oracle_get_threads())
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Sb = S + (size_t)bh * n * dv;
+        double *zb = z + (size_t)bh * n;
+        double *pk = malloc((size_t)n * sizeof(double));
+        double *pq = malloc((size_t)n * sizeof(double));
+        double *A = malloc(sizeof(double) * (size_t)d * d);
+        lift_map_one(k + (size_t)bh * d, d, map, g, eps, s, pk, A);
+        lift_map_one(q + (size_t)bh * d, d, map, g, eps, s, pq, A);
+        const double *vb = v + (size_t)bh * dv;
+        for (int f = 0; f < n; ++f) {
+            for (int j = 0; j < dv; ++j) Sb[(size_t)f * dv + j] += pk[f] * vb[j];
+            zb[f] += pk[f];
+        }
+        double den = 0.0;
+        for (int f = 0; f < n; ++f) den += pq[f] * zb[f];
+        for (int j = 0; j < dv; ++j) {
+            double num = 0.0;
+            for (int f = 0; f < n; ++f) num += pq[f] * Sb[(size_t)f * dv + j];
+            out[(size_t)bh * dv + j] = den > 0.0 ? num / den : 0.0;
+        }
+        free(pk);
+        free(pq);
+        free(A);
+    }
+}
+
 /* ---------------------------------------------------------------------------
  * GatedKATA (the appendix on recurrent variants, "multiplicative scalar state
  * gate", and Sec. 5.2): a scalar gate gamma_t in [0, 1] inside the recurrence,

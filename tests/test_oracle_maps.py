@@ -275,3 +275,56 @@ def test_orthant_planted_mistakes_fail(mistake):
     else:
         bad = float((np.maximum(q, 0) + eps) @ np.maximum(k, 0))
     assert abs(bad - _orthant_identity(q, k, eps)) > 1e-6
+
+
+# ---- the map's state after a prefix and one decode step (Eq. 2's recurrence
+# with the map's psi): pinned to the direct definition and the printed identities
+STATE_CASES = [("M", 16, 2, 0.0, 1.0), ("M", 32, 4, 0.0, 1.0), ("Sigma", 16, 2, 1e-4, 1.0),
+               ("Sigma", 64, 4, 1e-4, 0.25), ("Sigma", 32, 2, 0.3, 2.0), ("orthant", 16, 1, 1e-6, 1.0)]
+
+
+@pytest.mark.parametrize("map_name,d,g,eps,s", STATE_CASES)
+def test_prefix_then_decode_is_the_direct_row(map_name, d, g, eps, s):
+    """State of tokens 0..T-1, then one step with token T: its output is row T
+    of the direct O(T^2) definition."""
+    q, k, v = _rand_qkv(np.random.default_rng(d + g), B=2, H=1, T=23, d=d, dv=6)
+    T = q.shape[2] - 1
+    S, z = oracle.prefix_state_map(k[:, :, :T], v[:, :, :T], map_name, g, eps, s)
+    S2, z2, o = oracle.decode_step_map(S, z, q[:, :, T], k[:, :, T], v[:, :, T], map_name, g,
+                                       eps, s)
+    ref = oracle.forward_map(q, k, v, map_name, g, eps, s)[:, :, T]
+    assert _rel(o, ref) < 1e-12
+    # the step's state is the prefix state of all T + 1 tokens
+    S_all, z_all = oracle.prefix_state_map(k, v, map_name, g, eps, s)
+    assert _rel(S2, S_all) < 1e-12 and _rel(z2, z_all) < 1e-12
+
+
+@pytest.mark.parametrize("map_name,d,g,eps,s", STATE_CASES[:5])
+def test_state_contracts_to_the_printed_weights(map_name, d, g, eps, s):
+    """psi(q)^T S = sum_s w(q, k_s) v_s and psi(q)^T z = sum_s w(q, k_s), with w
+    the printed inner-product identity (computed here in numpy)."""
+    q, k, v = _rand_qkv(np.random.default_rng(3 * d + g), B=1, H=1, T=17, d=d, dv=4)
+    S, z = oracle.prefix_state_map(k, v, map_name, g, eps, s)
+    pq = oracle.lift_map(q[0, 0, 5], map_name, g, eps, s)
+    w = np.array([_closed_form(q[0, 0, 5], k[0, 0, t], map_name, g, eps, s) for t in range(17)])
+    assert _rel(pq @ S[0, 0], w @ v[0, 0]) < 1e-12
+    assert abs(float(pq @ z[0, 0]) - float(w.sum())) < 1e-12 * float(w.sum())
+
+
+def test_full_map_state_is_the_pinned_prefix_state():
+    q, k, v = _rand_qkv(np.random.default_rng(5), B=1, H=2, T=19, d=16, dv=5)
+    S, z = oracle.prefix_state_map(k, v, "M", 1)
+    S0, z0 = oracle.prefix_state(k, v)
+    assert _rel(S, S0) < 1e-12 and _rel(z, z0) < 1e-12
+
+
+def test_decode_read_before_update_fails_the_pin():
+    """A step that reads the state before adding its own key misses the token's
+    own weight: it differs from the direct row."""
+    q, k, v = _rand_qkv(np.random.default_rng(9), B=1, H=1, T=12, d=16, dv=3)
+    T = 11
+    S, z = oracle.prefix_state_map(k[:, :, :T], v[:, :, :T], "Sigma", 2, 1e-4, 1.0)
+    pq = oracle.lift_map(q[0, 0, T], "Sigma", 2, 1e-4, 1.0)
+    wrong = (pq @ S[0, 0]) / (pq @ z[0, 0])
+    ref = oracle.forward_map(q, k, v, "Sigma", 2, 1e-4, 1.0)[0, 0, T]
+    assert _rel(wrong, ref) > 1e-6
