@@ -193,6 +193,37 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
                          float scale, kata_stream_t stream);
 
 /*
+ * kata_fwd_chunked_map_state -- kata_fwd_chunked_map plus the state after the
+ * last token under the map (Eq. 2's recurrence with the map's psi, at the end of
+ * the last chunk), for kata_decode_step_map to continue:
+ *   state [B][H][n][dv] fp32 = sum_t psi(k_t) v_t^T, z [B][H][n] fp32 =
+ *   sum_t psi(k_t), n = kata_map_feature_dim(map, d, g), features in the packed
+ *   order of kata_lift_map (each matrix row-major over its upper triangle,
+ *   sqrt(2) off the diagonal, M_g's matrices block by block).
+ * state and z 16-byte aligned, not overlapping each other or the other buffers
+ * (KATA_ERR_ARG).  The d = 64 sub-head routes of M_2, Sigma_2 and M_4 keep no
+ * state of the map, so with the state exported those maps take the CUDA cores;
+ * the explicit-feature path exports its scanned records (products of the bf16
+ * hi feature parts with v, accumulated in fp32).  Other arguments and errors as
+ * kata_fwd_chunked_map.
+ */
+int kata_fwd_chunked_map_state(const void *q, const void *k, const void *v, void *out,
+                               float *state, float *z, int B, int H, int T, int d, int dv, int C,
+                               int dtype, int map, int g, float eps, float scale,
+                               kata_stream_t stream);
+
+/*
+ * kata_decode_step_map -- one decode step under a map, in place:
+ *   S += psi(k) v^T, z += psi(k), o = psi(q)^T S / psi(q)^T z (0 where the
+ *   denominator is not positive), psi the map's packed features.
+ * Layouts, alignment, ownership and errors as kata_decode_step with
+ * n = kata_map_feature_dim(map, d, g); map, g, eps, scale as kata_fwd_chunked_map.
+ */
+int kata_decode_step_map(float *state, float *z, const void *q, const void *k, const void *v,
+                         void *out, int B, int H, int d, int dv, int dtype, int map, int g,
+                         float eps, float scale, kata_stream_t stream);
+
+/*
  * kata_fwd_quadratic -- the quadratic (flash-style) form of the same forward:
  * o_t = sum_{s<=t} (q_t . k_s)^2 v_s / sum_{s<=t} (q_t . k_s)^2 evaluated tile
  * by tile, with no state ([KATA] Sec. 2 Eq. 2 directly; the pages' O(T^2)

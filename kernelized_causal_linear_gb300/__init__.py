@@ -51,7 +51,8 @@ EXPORTED = ("kata_feature_dim", "kata_status_str", "kata_fwd_chunked",
             "kata_fwd_path_map", "kata_fwd_quadratic", "kata_fwd_chunked_gated",
             "kata_decode_step_gated", "kata_fwd_quadratic_gated", "kata_fwd", "kata_fwd_form",
             "kata_fwd_gated", "kata_fwd_gated_form", "kata_fwd_segments",
-            "kata_test_arm_stall", "kata_fwd_path_gated")
+            "kata_test_arm_stall", "kata_fwd_path_gated", "kata_fwd_chunked_map_state",
+            "kata_decode_step_map")
 
 _lib = None
 
@@ -99,6 +100,9 @@ def lib() -> ctypes.CDLL:
         L.kata_fwd_chunked_state.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, vp]
         f = ctypes.c_float
         L.kata_fwd_chunked_map.argtypes = [p, p, p, p, i, i, i, i, i, i, i, i, i, f, f, vp]
+        L.kata_fwd_chunked_map_state.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, i, i, f, f,
+                                                 vp]
+        L.kata_decode_step_map.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, f, f, vp]
         L.kata_lift_map.argtypes = [p, p, ctypes.c_int64, i, i, i, i, f, f, vp]
         L.kata_map_feature_dim.argtypes = [i, i, i]
         L.kata_map_feature_dim.restype = i
@@ -439,6 +443,52 @@ def kata_fwd_chunked_map(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: i
                                     int(g), float(eps), float(scale),
                                     _stream_handle(stream, q.device))
     _check(rc, "kata_fwd_chunked_map")
+    return out
+
+
+def kata_fwd_chunked_map_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, C: int,
+                               map: int, g: int, eps: float = 0.0, scale: float = 1.0,
+                               out: torch.Tensor | None = None, state: torch.Tensor | None = None,
+                               z: torch.Tensor | None = None, stream=None):
+    """kata_fwd_chunked_map plus the map's state after the last token: returns
+    (out, state [B,H,n,dv] fp32, z [B,H,n] fp32) for kata_decode_step_map."""
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    n = kata_map_feature_dim(map, d, g)
+    if n < 0:
+        raise KataError(KATA_ERR_ARG, "kata_fwd_chunked_map_state")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=v.dtype, device=v.device)
+    if state is None:
+        state = torch.empty((B, H, n, dv), dtype=torch.float32, device=v.device)
+    if z is None:
+        z = torch.empty((B, H, n), dtype=torch.float32, device=v.device)
+    _contig(q, k, v, out, state, z)
+    rc = lib().kata_fwd_chunked_map_state(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          out.data_ptr(), state.data_ptr(), z.data_ptr(), B, H, T,
+                                          d, dv, int(C), _dtype_code(q.dtype), int(map), int(g),
+                                          float(eps), float(scale),
+                                          _stream_handle(stream, q.device))
+    _check(rc, "kata_fwd_chunked_map_state")
+    return out, state, z
+
+
+def kata_decode_step_map(state: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+                         v: torch.Tensor, map: int, g: int, eps: float = 0.0, scale: float = 1.0,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step under a map; state [B,H,n,dv] and z [B,H,n] (fp32) in place."""
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=v.dtype, device=v.device)
+    _contig(state, z, q, k, v, out)
+    if state.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("state and z must be float32")
+    rc = lib().kata_decode_step_map(state.data_ptr(), z.data_ptr(), q.data_ptr(), k.data_ptr(),
+                                    v.data_ptr(), out.data_ptr(), B, H, d, dv,
+                                    _dtype_code(q.dtype), int(map), int(g), float(eps),
+                                    float(scale), _stream_handle(stream, q.device))
+    _check(rc, "kata_decode_step_map")
     return out
 
 

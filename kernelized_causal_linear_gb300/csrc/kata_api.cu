@@ -125,7 +125,7 @@ Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::Map
             if (map.kind == KATA_MAP_BLOCK && map.g == 4) return kTc32M4;
         }
     }
-    if (!with_state && kata::feat_supported(s, map, di.major, di.minor)) return kFeat;
+    if (kata::feat_supported(s, map, di.major, di.minor)) return kFeat;
     return kSimt;
 }
 
@@ -271,7 +271,7 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
         kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
         : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
         : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
-        : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map)
+        : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map, so)
         : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
                            : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
     if (ws) {
@@ -340,6 +340,63 @@ static int adapted_quadratic(const FwdShape &s, const void *q, const void *k, co
     cudaError_t e = kata::adapt_quad_forward(s, q, k, v, out, ws, st, gamma, normalize);
     const cudaError_t ef = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = ef;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KATA_ERR_CUDA;
+    }
+    return KATA_OK;
+}
+
+int kata_fwd_chunked_map_state(const void *q, const void *k, const void *v, void *out,
+                               float *state, float *z, int B, int H, int T, int d, int dv, int C,
+                               int dtype, int map, int g, float eps, float scale,
+                               kata_stream_t stream) {
+    if (!valid_map(map, d, g, eps, scale)) return KATA_ERR_ARG;
+    if (!state || !z) return KATA_ERR_ARG;
+    if (!aligned16(state) || !aligned16(z)) return KATA_ERR_ARG;
+    const int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
+    if (rc) return rc;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    ms.eps = eps;
+    ms.scale = scale;
+    const size_t es = elem_size(dtype), BH = (size_t)B * H, n = (size_t)ms.n(d);
+    const size_t nqk = BH * T * d * es, nvo = BH * T * dv * es;
+    const size_t ns = BH * n * dv * 4, nz = BH * n * 4;
+    if (overlap(state, ns, z, nz) || overlap(state, ns, q, nqk) || overlap(state, ns, k, nqk) ||
+        overlap(state, ns, v, nvo) || overlap(state, ns, out, nvo) || overlap(z, nz, q, nqk) ||
+        overlap(z, nz, k, nqk) || overlap(z, nz, v, nvo) || overlap(z, nz, out, nvo))
+        return KATA_ERR_ARG;
+    kata::StateOut so;
+    so.state = state;
+    so.z = z;
+    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, so, ms);
+}
+
+int kata_decode_step_map(float *state, float *z, const void *q, const void *k, const void *v,
+                         void *out, int B, int H, int d, int dv, int dtype, int map, int g,
+                         float eps, float scale, kata_stream_t stream) {
+    if (!state || !z || !q || !k || !v || !out) return KATA_ERR_ARG;
+    if (!aligned16(state) || !aligned16(z) || !aligned16(q) || !aligned16(k) ||
+        !aligned16(v) || !aligned16(out))
+        return KATA_ERR_ARG;
+    if (B < 1 || H < 1 || !valid_dtype(dtype)) return KATA_ERR_ARG;
+    if (!valid_d(d) || !valid_dv(dv)) return KATA_ERR_UNSUPPORTED;
+    if (!valid_map(map, d, g, eps, scale)) return KATA_ERR_ARG;
+    if ((int64_t)B * H > INT32_MAX) return KATA_ERR_UNSUPPORTED;
+    kata::MapSpec ms;
+    ms.kind = map;
+    ms.g = g;
+    ms.eps = eps;
+    ms.scale = scale;
+    const size_t n = (size_t)ms.n(d), BH = (size_t)B * H;
+    if (overlap(state, BH * n * dv * 4, z, BH * n * 4) ||
+        overlap(out, BH * dv * elem_size(dtype), state, BH * n * dv * 4))
+        return KATA_ERR_ARG;
+    cudaGetLastError();
+    const cudaError_t e = kata::decode_map_launch(state, z, q, k, v, out, (int)BH, d, dv, dtype, ms,
+                                                  reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_CUDA;

@@ -11,8 +11,11 @@
 // The GatedKATA step (the pages' multiplicative scalar state gate) is the same
 // sweep with S = gamma S + psi(k) v^T, z = gamma z + psi(k) (gamma per head), read
 // out with or without the denominator: a compile-time variant, so the plain step
-// carries no gate multiply.
-#include "kata_internal.cuh"
+// carries no gate multiply.  A reduced map (KATA-M_g, KATA-Sigma_g, the orthant
+// map) changes only the lift: its packed features from kata_map.cuh, its state
+// width n.
+#include "kata_dispatch.cuh"
+#include "kata_map.cuh"
 
 namespace kata {
 namespace {
@@ -23,7 +26,7 @@ template <typename T, int DV4, bool kGated>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict__ q,
               const T *__restrict__ k, const T *__restrict__ v, T *__restrict__ out, int d,
-              int n, const float *__restrict__ gamma, int normalize) {
+              int n, const float *__restrict__ gamma, int normalize, MapSpec mp) {
     extern __shared__ float sm[];
     float *pk = sm;                 // psi(k) [n]
     float *pq = pk + n;             // psi(q) [n]
@@ -47,11 +50,18 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
     float den = 0.f;
     float *zb = z + (size_t)bh * n;
     for (int f = tid; f < n; f += kThreads) {
-        int i, j;
-        vech_pair(f, d, i, j);
-        const float cf = (i == j) ? 1.f : kSqrt2;
-        const float a = ks[i] * ks[j] * cf;
-        const float b = qs[i] * qs[j] * cf;
+        float a, b;
+        if (mp.kind == 0) {   // the rank-one lift
+            int i, j;
+            vech_pair(f, d, i, j);
+            const float cf = (i == j) ? 1.f : kSqrt2;
+            a = ks[i] * ks[j] * cf;
+            b = qs[i] * qs[j] * cf;
+        } else {              // a reduced map's packed feature f
+            const Feat ft = map_feature(f, d, mp);
+            a = ft(ks, 1);
+            b = ft(qs, 1);
+        }
         pk[f] = a;
         pq[f] = b;
         const float zn = kGated ? fmaf(g, zb[f], a) : zb[f] + a;
@@ -119,29 +129,42 @@ decode_kernel(float *__restrict__ S, float *__restrict__ z, const T *__restrict_
 
 template <typename T, int DV4>
 void decode_go(float *S, float *z, const T *q, const T *k, const T *v, T *out, int BH, int d,
-               int n, size_t sm, cudaStream_t stream, const float *gamma, int normalize) {
+               int n, size_t sm, cudaStream_t stream, const float *gamma, int normalize,
+               const MapSpec &mp) {
     if (gamma)
         decode_kernel<T, DV4, true><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n, gamma,
-                                                                 normalize);
+                                                                 normalize, mp);
     else
         decode_kernel<T, DV4, false><<<BH, kThreads, sm, stream>>>(S, z, q, k, v, out, d, n,
-                                                                  nullptr, 1);
+                                                                  nullptr, 1, mp);
 }
 
 template <typename T>
 cudaError_t decode_t(float *S, float *z, const T *q, const T *k, const T *v, T *out, int BH,
-                     int d, int dv, cudaStream_t stream, const float *gamma, int normalize) {
-    const int n = d * (d + 1) / 2;
+                     int d, int dv, cudaStream_t stream, const float *gamma, int normalize,
+                     const MapSpec &mp) {
+    const int n = mp.n(d);
     const size_t sm = sizeof(float) * 2 * (size_t)n;
-    TraceScope tr(gamma ? "decode_gated" : "decode", stream);
+    TraceScope tr(gamma ? "decode_gated" : mp.kind ? "decode_map" : "decode", stream);
     switch (dv) {
-        case 16: decode_go<T, 4>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
-        case 32: decode_go<T, 8>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
-        case 64: decode_go<T, 16>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
-        case 128: decode_go<T, 32>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize); break;
+        case 16: decode_go<T, 4>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize, mp); break;
+        case 32: decode_go<T, 8>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize, mp); break;
+        case 64: decode_go<T, 16>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize, mp); break;
+        case 128: decode_go<T, 32>(S, z, q, k, v, out, BH, d, n, sm, stream, gamma, normalize, mp); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+cudaError_t decode_any(float *S, float *z, const void *q, const void *k, const void *v, void *out,
+                       int BH, int d, int dv, int dtype, cudaStream_t stream, const float *gamma,
+                       int normalize, const MapSpec &mp) {
+    if (dtype == 0)
+        return decode_t<float>(S, z, (const float *)q, (const float *)k, (const float *)v,
+                               (float *)out, BH, d, dv, stream, gamma, normalize, mp);
+    return decode_t<__nv_bfloat16>(S, z, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                                   (const __nv_bfloat16 *)v, (__nv_bfloat16 *)out, BH, d, dv,
+                                   stream, gamma, normalize, mp);
 }
 
 }  // namespace
@@ -149,12 +172,13 @@ cudaError_t decode_t(float *S, float *z, const T *q, const T *k, const T *v, T *
 cudaError_t decode_launch(float *S, float *z, const void *q, const void *k, const void *v,
                           void *out, int BH, int d, int dv, int dtype, cudaStream_t stream,
                           const float *gamma, int normalize) {
-    if (dtype == 0)
-        return decode_t<float>(S, z, (const float *)q, (const float *)k, (const float *)v,
-                               (float *)out, BH, d, dv, stream, gamma, normalize);
-    return decode_t<__nv_bfloat16>(S, z, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
-                                   (const __nv_bfloat16 *)v, (__nv_bfloat16 *)out, BH, d, dv,
-                                   stream, gamma, normalize);
+    return decode_any(S, z, q, k, v, out, BH, d, dv, dtype, stream, gamma, normalize, MapSpec{});
+}
+
+cudaError_t decode_map_launch(float *S, float *z, const void *q, const void *k, const void *v,
+                              void *out, int BH, int d, int dv, int dtype, const MapSpec &map,
+                              cudaStream_t stream) {
+    return decode_any(S, z, q, k, v, out, BH, d, dv, dtype, stream, nullptr, 1, map);
 }
 
 }  // namespace kata

@@ -47,4 +47,10 @@ cudaError_t adapt_quad_forward(const FwdShape &s, const void *q, const void *k, 
                                void *out, void *workspace, cudaStream_t stream, const float *gamma,
                                int normalize);
 
+// ---- decode step under a reduced map: kata_decode.cu -------------------------
+// S [BH][n][dv], z [BH][n] with n = map.n(d), features in map_feature's order.
+cudaError_t decode_map_launch(float *S, float *z, const void *q, const void *k, const void *v,
+                              void *out, int BH, int d, int dv, int dtype, const MapSpec &map,
+                              cudaStream_t stream);
+
 }  // namespace kata

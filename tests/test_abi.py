@@ -275,3 +275,42 @@ def test_fwd_gated_auto_rejects_bad_arguments(L):
     assert L.kata_fwd_gated(q, k, v, g, o, 1, 1, 0, 32, 64, 64, 1, 1, None) == kg.KATA_ERR_ARG
     assert L.kata_fwd_gated(q, k, v, g, o, 1, 1, 8, 24, 64, 64, 1, 1, None) == kg.KATA_ERR_UNSUPPORTED
     assert L.kata_fwd_gated_form(1, 1, 8, 24, 64, 64, 1) == kg.KATA_FORM_NONE
+
+
+def test_map_state_and_decode_reject_bad_arguments(L):
+    import kernelized_causal_linear_gb300 as kg
+    q, k, v, o, S, z = (FAKE * (i + 1) * 4096 for i in range(6))
+
+    def fs(**kw):
+        a = dict(q=q, S=S, z=z, B=1, H=1, T=8, d=16, dv=16, C=32, dtype=1,
+                 map_=kg.KATA_MAP_SUM, g=2, eps=1e-4, scale=1.0)
+        a.update(kw)
+        return L.kata_fwd_chunked_map_state(a["q"], k, v, o, a["S"] or None, a["z"] or None,
+                                            a["B"], a["H"], a["T"], a["d"], a["dv"], a["C"],
+                                            a["dtype"], a["map_"], a["g"], a["eps"], a["scale"],
+                                            None)
+
+    assert fs(map_=kg.KATA_MAP_ORTHANT, g=2) == kg.KATA_ERR_ARG   # the orthant map needs g = 1
+    assert fs(map_=kg.KATA_MAP_BLOCK, eps=1e-4) == kg.KATA_ERR_ARG
+    assert fs(S=0) == kg.KATA_ERR_ARG                              # no state
+    assert fs(z=0) == kg.KATA_ERR_ARG
+    assert fs(S=S + 4) == kg.KATA_ERR_ARG                          # misaligned state
+    assert fs(T=0) == kg.KATA_ERR_ARG                              # shape rules as the forward
+    assert fs(d=24, g=4) == kg.KATA_ERR_UNSUPPORTED
+    assert fs(z=S + 64) == kg.KATA_ERR_ARG                         # z inside the state
+
+    def dm(**kw):
+        a = dict(S=S, q=q, B=1, H=1, d=16, dv=16, dtype=1, map_=kg.KATA_MAP_BLOCK, g=2, eps=0.0,
+                 scale=1.0)
+        a.update(kw)
+        return L.kata_decode_step_map(a["S"] or None, z, a["q"] or None, k, v, o, a["B"], a["H"],
+                                      a["d"], a["dv"], a["dtype"], a["map_"], a["g"], a["eps"],
+                                      a["scale"], None)
+
+    assert dm(S=0) == kg.KATA_ERR_ARG
+    assert dm(q=0) == kg.KATA_ERR_ARG
+    assert dm(g=3) == kg.KATA_ERR_ARG
+    assert dm(map_=kg.KATA_MAP_SUM, eps=-1.0) == kg.KATA_ERR_ARG
+    assert dm(d=20) == kg.KATA_ERR_UNSUPPORTED
+    assert dm(dv=48) == kg.KATA_ERR_UNSUPPORTED
+    assert dm(B=0) == kg.KATA_ERR_ARG

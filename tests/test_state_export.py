@@ -162,3 +162,79 @@ def test_state_d64_full_size_sampled_heads(kg):
         zg = to_f64(z.reshape(BH, 1, -1)[h:h + 1])
         assert _state_err(Sg, S_ref) <= STATE_TOL[w.dtype]
         assert _state_err(zg, z_ref) <= STATE_TOL[w.dtype]
+
+
+# ---- reduced maps: the map's state after a prefill, and a decode step from it
+_MAP_NAMES = {1: "M", 2: "Sigma", 3: "orthant"}
+
+
+def _map_params(map_, g):
+    if map_ == 2:
+        return 1e-4, (0.25 if g == 4 else 1.0)
+    if map_ == 3:
+        return 1e-6, 1.0
+    return 0.0, 1.0
+
+
+@pytest.mark.parametrize("map_,g,d,dtype", [
+    (2, 4, 64, torch.bfloat16),   # Sigma_4: the explicit-feature path exports its scanned records
+    (2, 2, 32, torch.bfloat16),
+    (3, 1, 64, torch.bfloat16),   # orthant
+    (1, 4, 16, torch.bfloat16),
+    (1, 2, 64, torch.bfloat16),   # M_2 at d = 64: the sub-heads keep no map state -> CUDA cores
+    (2, 2, 16, torch.float32),    # fp32: CUDA cores
+])
+def test_map_prefill_then_decode(kg, map_, g, d, dtype):
+    """kata_fwd_chunked_map_state over T-1 tokens: its state against the oracle's
+    map recurrence, its output against the direct definition; then
+    kata_decode_step_map with token T-1: the direct definition's row T-1."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=2, T=301, d=d, dtype=dtype)
+    name = _MAP_NAMES[map_]
+    eps, scale = _map_params(map_, g)
+    q, k, v = workloads.make_qkv(w)
+    Tp = w.T - 1
+    sl = (slice(None), slice(None), slice(0, Tp))
+    out, S, z = kg.kata_fwd_chunked_map_state(q[sl].contiguous().cuda(), k[sl].contiguous().cuda(),
+                                              v[sl].contiguous().cuda(), w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    S_ref, z_ref = oracle.prefix_state_map(to_f64(k[sl]), to_f64(v[sl]), name, g, eps, scale)
+    tol = STATE_TOL[dtype]
+    es, ez = _state_err(to_f64(S), S_ref), _state_err(to_f64(z), z_ref)
+    assert es <= tol and ez <= tol, f"state {es:.2e}, z {ez:.2e} (bar {tol:.0e})"
+    ref = oracle.forward_map(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), name, g, eps, scale)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[dtype]
+    o = kg.kata_decode_step_map(S, z, q[:, :, Tp].contiguous().cuda(), k[:, :, Tp].contiguous().cuda(),
+                                v[:, :, Tp].contiguous().cuda(), map_, g, eps, scale)
+    torch.cuda.synchronize()
+    rows = np.arange(w.B * w.H, dtype=np.int64) * w.T + Tp
+    refo = oracle.forward_rows_map(to_f64(q), to_f64(k), to_f64(v), rows, name, g, eps, scale)
+    got = to_f64(o).reshape(w.B, w.H, 1, w.dv)
+    assert slice_rel_err(got, refo.reshape(got.shape)) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("map_,g,d,dv", [(2, 4, 64, 64), (1, 2, 32, 16), (3, 1, 16, 128),
+                                         (2, 2, 64, 32)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_map_decode_step_parity(kg, map_, g, d, dv, dtype):
+    """One decode step from an oracle state (a 16-token prefix) against the
+    oracle's map step: the output and the updated state and z."""
+    name = _MAP_NAMES[map_]
+    eps, scale = _map_params(map_, g)
+    rng = torch.Generator().manual_seed(d + dv + map_)
+    B, H = 3, 5
+    kp = torch.randn(B, H, 16, d, generator=rng) / d ** 0.5
+    vp = torch.randn(B, H, 16, dv, generator=rng)
+    S0, z0 = oracle.prefix_state_map(to_f64(kp), to_f64(vp), name, g, eps, scale)
+    q = (torch.randn(B, H, d, generator=rng) / d ** 0.5).to(dtype)
+    k = (torch.randn(B, H, d, generator=rng) / d ** 0.5).to(dtype)
+    v = torch.randn(B, H, dv, generator=rng).to(dtype)
+    S = torch.from_numpy(S0).float().cuda()
+    z = torch.from_numpy(z0).float().cuda()
+    Sf, zf = to_f64(S), to_f64(z)
+    o = kg.kata_decode_step_map(S, z, q.cuda(), k.cuda(), v.cuda(), map_, g, eps, scale)
+    torch.cuda.synchronize()
+    S1, z1, oref = oracle.decode_step_map(Sf, zf, to_f64(q), to_f64(k), to_f64(v), name, g, eps,
+                                          scale)
+    assert slice_rel_err(to_f64(o)[:, :, None, :], oref[:, :, None, :]) <= TOL[dtype]
+    assert _state_err(to_f64(S), S1) <= 1e-5 and _state_err(to_f64(z), z1) <= 1e-5
