@@ -108,13 +108,15 @@ const char *kata_status_str(int status);
  * The output is the same function for every C (Eq. 17-20 regroup one sum);
  * C changes only the rounding.  bf16 inputs run on the tensor-core path, which
  * rounds the lifted features and the chunk-state prefix to bf16 as MMA
- * operands (fp32 accumulation), for every d and dv except d = 64 with fewer
- * than 38 (b, h) heads.  Its kernels take d = 32 or 64 with dv = 64; other head
+ * operands (fp32 accumulation), for every d and dv.  At d = 64 each head's
+ * chunks run in order on four CTAs (fewer than 38 heads leave SMs idle; the
+ * quadratic form, which kata_fwd takes there, is then faster for longer T).  Its
+ * kernels take d = 32 or 64 with dv = 64; other head
  * sizes run on them through scratch copies: q and k padded with zero columns
  * to d = 32 (d = 16), v cut into 64-column parts (dv = 16, 32 zero-padded; dv =
  * 128 as two parts, each a full pass of the kernels).  Both are exact
- * rewritings of Eq. 17-20.  fp32 inputs, and d = 64 with fewer heads, run on
- * CUDA cores in fp32 (kata_fwd_path tells which).
+ * rewritings of Eq. 17-20.  fp32 inputs run on CUDA cores in fp32
+ * (kata_fwd_path tells which).
  *
  * Scratch: per-call device workspace (kata_fwd_workspace_size bytes) taken
  * from the device's stream-ordered memory pool and released on `stream`.
@@ -292,9 +294,8 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
  * (kata_fwd_quadratic_gated), which evaluates the same weights tile by tile.
  * The state is sum_s A_s psi(k_s) v_s^T, A_s the product of the gates after s,
  * and psi is quadratic, so the state comes from the chunked d = 64 tensor path
- * run on the keys sqrt(A_s) k_s (rounded to bf16).  That part needs 4 B H >=
- * the SM count; with fewer heads a call that exports the state runs on CUDA
- * cores.  Other shapes run on CUDA cores in fp32 FFMA.
+ * run on the keys sqrt(A_s) k_s (rounded to bf16).  Other shapes run on CUDA
+ * cores in fp32 FFMA.
  *
  *   gamma    [B][H][T] fp32 device, read only, 16-byte aligned; values in [0, 1]
  *            (not checked on the device: other values give the recurrence's
@@ -312,8 +313,8 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
 
 /* kata_fwd_path_gated -- the path kata_fwd_chunked_gated takes for a shape
  * without the state export: KATA_PATH_TC (tensor cores), KATA_PATH_SIMT (CUDA
- * cores) or KATA_PATH_NONE (invalid shape or no device).  With the state
- * exported at d = 64, the tensor path also needs 4 B H >= the SM count. */
+ * cores) or KATA_PATH_NONE (invalid shape or no device); the same with the
+ * state exported. */
 int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype);
 
 /*
@@ -387,11 +388,13 @@ typedef enum {
 
 /*
  * kata_fwd -- the forward in whichever exact form is faster for the shape:
- * the quadratic form (kata_fwd_quadratic) where it is supported and T is at
- * most a head-dimension-dependent crossover (6144 tokens at d = 32 and d = 16,
- * which runs the d = 32 kernels; 8192 at d = 64; from measurements of both
- * forms on GB300), else the chunked form
- * (kata_fwd_chunked).  Both compute the same o_t; they differ in rounding
+ * the quadratic form (kata_fwd_quadratic) where it is supported and faster,
+ * else the chunked form (kata_fwd_chunked).  At d = 32 (and d = 16, which runs
+ * the d = 32 kernels) the quadratic form is faster up to T = 6144.  At d = 64 the
+ * chunked kernels walk each head's chunks in order, so the bound depends on the
+ * head count: the quadratic form is taken while B H T < 420000 x ceil(4 B H /
+ * SMs) (T = 8192 at 128 heads, T = 26000 at 16, T = 420000 at one head; fitted to
+ * GB300 timings of both forms).  Both compute the same o_t; they differ in rounding
  * only.  Arguments, layouts and errors as kata_fwd_chunked (C is used by the
  * chunked form).  kata_fwd_form tells which form a shape takes.
  */

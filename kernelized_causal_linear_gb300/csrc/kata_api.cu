@@ -469,10 +469,19 @@ int kata_fwd_quadratic_gated(const void *q, const void *k, const void *v, const 
     return KATA_OK;
 }
 
-// The quadratic form's crossover against the chunked form: the largest T at
-// which it is the faster of the two (measured on GB300 at d = 32: 0.6x the
-// chunked time at T = 4096, 1.37x at T = 8192; at d = 64: 0.26x at T = 2048).
-static int quadratic_crossover(int d) { return d == 64 ? 8192 : 6144; }
+// The quadratic form's crossover against the chunked form.  At d = 32 (and
+// d = 16, which runs the d = 32 kernels) the chunked form's segments fill the GPU
+// at any head count, and the quadratic form is faster up to T = 6144 (measured on
+// GB300: 0.6x the chunked time at T = 4096, 1.37x at T = 8192).  At d = 64 the
+// chunked kernels walk each head's chunks in order on four CTAs, so their time is
+// ~T x 4.2e-5 ms per wave of 152 / 4 heads, while the quadratic form's is ~BH T^2
+// x 1.0e-10 ms (both fitted to GB300 timings at 1 .. 128 heads, T = 2048 .. 65536):
+// the quadratic form wins while BH T < 4.2e5 x waves.
+static bool quadratic_is_faster(int BH, int T, int d, int num_sms) {
+    if (d != 64) return T <= 6144;
+    const int64_t waves = ((int64_t)4 * BH + num_sms - 1) / num_sms;
+    return (int64_t)BH * T < (int64_t)420000 * waves;
+}
 
 int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype) {
     if (check_fwd_shape(B, H, T, d, dv, C, dtype)) return KATA_FORM_NONE;
@@ -481,9 +490,8 @@ int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype) {
     const FwdShape s{B, H, T, d, dv, 64, dtype};
     const bool quad = kata::quad_supported(s, di.major, di.minor) ||
                       kata::adapt_quad_supported(s, di.major, di.minor);
-    // d = 16 runs the kernels of d = 32
-    return (quad && T <= quadratic_crossover(d < 32 ? 32 : d)) ? KATA_FORM_QUADRATIC
-                                                               : KATA_FORM_CHUNKED;
+    return (quad && quadratic_is_faster(B * H, T, d, di.sms)) ? KATA_FORM_QUADRATIC
+                                                            : KATA_FORM_CHUNKED;
 }
 
 int kata_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int T, int d,

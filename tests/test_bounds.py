@@ -59,7 +59,8 @@ def _fwd_case(kg, w, call):
     ("mid_bf16", dict(B=1, H=2, T=77, dv=128)),  # tensor path, two v parts
     ("mid_bf16", dict(B=1, H=3, T=130, d=16, dv=16)),   # q, k padded to d = 32
     ("lm_layer_bf16", dict(B=1, H=38, T=129, dv=32)),   # d = 64 kernels, one v part
-    ("lm_layer_bf16", dict(B=1, H=37, T=100, dv=128)),  # CUDA cores, dv = 128
+    ("lm_layer_bf16", dict(B=1, H=37, T=100, dv=128)),  # d = 64 kernels, 37 heads, two v parts
+    ("small_fp32", dict(B=2, H=3, T=97, d=64, dv=128)),  # CUDA cores, fp32
 ])
 def test_chunked_forward_stays_in_bounds(kg, name, overrides):
     w = workloads.WORKLOADS[name].scaled(**overrides)

@@ -237,7 +237,8 @@ _ADAPTED = [
     (32, 16, 1, 2, 1100),
     (32, 32, 2, 2, 517),
     (32, 128, 1, 3, 1100),
-    (64, 16, 1, 38, 300),    # the d = 64 kernels (38 heads or more)
+    (64, 16, 1, 38, 300),    # the d = 64 kernels
+    (64, 32, 1, 2, 300),     # two heads: SMs left idle
     (64, 32, 2, 19, 129),
     (64, 128, 1, 38, 300),
 ]
@@ -272,13 +273,25 @@ def test_adapted_shapes_deterministic(kg):
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("dv", [64, 128])
-def test_d64_few_heads_use_cuda_cores(kg, dv):
-    """Fewer than 38 heads at d = 64 would leave SMs idle on the split path."""
-    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=37, T=200, dv=dv)
-    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_SIMT
+@pytest.mark.parametrize("B,H,T,dv", [(1, 37, 200, 64), (1, 1, 1100, 64), (1, 3, 300, 128),
+                                      (2, 1, 129, 32)])
+def test_d64_few_heads_tensor_path(kg, B, H, T, dv):
+    """Fewer than 38 heads at d = 64: the four CTAs per head leave SMs idle but
+    still outpace the CUDA cores; every head's chunks run in order."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, dv=dv)
+    assert kg.kata_fwd_path(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
     q, k, v = workloads.make_qkv(w)
     _check_full(kg, q, k, v, w.C)
+    assert kg.kata_sync_status() == kg.KATA_OK
+
+
+@pytest.mark.parametrize("B,H,T,form", [(1, 1, 65536, "quadratic"), (1, 16, 16384, "quadratic"),
+                                        (1, 16, 32768, "chunked"), (8, 16, 16384, "chunked")])
+def test_d64_form_follows_the_head_count(kg, B, H, T, form):
+    """At d = 64 the quadratic form is taken while B H T < 420000 x the waves of
+    four CTAs per head (the chunked kernels walk a head's chunks in order)."""
+    want = kg.KATA_FORM_QUADRATIC if form == "quadratic" else kg.KATA_FORM_CHUNKED
+    assert kg.kata_fwd_form(B, H, T, 64, 64, 64, torch.bfloat16) == want
 
 
 def test_d64_tensor_path_deterministic(kg):

@@ -476,9 +476,9 @@ def test_gated_d64_prefill_then_decode(kg):
     assert slice_rel_err(to_f64(o)[:, :, None, :], full[:, :, Tp:Tp + 1, :]) <= TOL[w.dtype]
 
 
-def test_gated_d64_few_heads_state_on_cuda_cores(kg):
-    """Fewer than 38 heads with the state exported: the call runs on CUDA cores
-    and still matches the oracle."""
+def test_gated_d64_few_heads_state(kg):
+    """Fewer than 38 heads with the state exported: the state comes from the d = 64
+    chunked kernels with SMs left idle."""
     w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=200)
     q, k, v = workloads.make_qkv(w)
     g = _gates(w)
@@ -488,7 +488,8 @@ def test_gated_d64_few_heads_state_on_cuda_cores(kg):
     ref = oracle.forward_gated(to_f64(q), to_f64(k), to_f64(v), to_f64(g))
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
     S_ref, _ = oracle.prefix_state_gated(to_f64(k), to_f64(v), to_f64(g))
-    assert slice_rel_err(to_f64(S), S_ref) <= 1e-4
+    assert kg.kata_fwd_path_gated(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype) == kg.KATA_PATH_TC
+    assert slice_rel_err(to_f64(S), S_ref) <= 1e-2
 
 
 # ---- other bf16 head sizes (d = 16, dv != 64) on the gated tensor routes: q, k
