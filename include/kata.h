@@ -410,8 +410,8 @@ int kata_fwd_form(int B, int H, int T, int d, int dv, int C, int dtype);
  * measured per-token costs of both forms on GB300 (bf16, dv = 64): the
  * quadratic form's grows with T (1.1 ns per token and head at T = 8192, 1.9 at
  * 16384, d = 32); the chunked form's does not (1.3 ns at d = 32 on the tensor
- * cores, ~35 ns at d = 64 on CUDA cores, where the quadratic form is faster up
- * to the largest measured T = 65536).  Arguments,
+ * cores).  At d = 64 the chunked call takes its output from the same gated
+ * quadratic kernel up to T = 262144.  Arguments,
  * layouts, ownership and errors as kata_fwd_chunked_gated with state = z = NULL
  * (gamma [B][H][T] fp32 device; normalize 0 or 1).  kata_fwd_gated_form tells
  * which form a shape takes (a kata_form value).

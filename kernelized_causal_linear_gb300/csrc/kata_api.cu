@@ -725,8 +725,9 @@ int kata_fwd_chunked_gated(const void *q, const void *k, const void *v, const fl
 // constant.  Measured on GB300 (bf16, dv = 64, per token and head): at d = 32
 // the chunked form runs on the tensor cores at 1.3 ns for every T, the
 // quadratic form at 1.10 ns at T = 8192 and 1.90 ns at T = 16384, so they level
-// near T = 10k; at d = 64 the chunked form runs on CUDA cores at ~35 ns and the
-// quadratic form is faster at every measured T (7.1 ns at T = 65536).
+// near T = 10k.  At d = 64 the chunked call takes its output from the same gated
+// quadratic kernel up to T = 262144 (7.1 ns at T = 65536), so the bound matters
+// only past that, where the chunked form runs on CUDA cores at ~35 ns.
 static int gated_quadratic_max_t(int d) { return d == 32 ? 10240 : 65536; }
 
 int kata_fwd_path_gated(int B, int H, int T, int d, int dv, int C, int dtype) {
