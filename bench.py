@@ -921,9 +921,8 @@ def main(argv=None):
     ap.add_argument("--algo", default="chunked",
                     choices=["chunked", "quadratic", "gated", "gated_quadratic"],
                     help="chunked O(T) form (the default), the quadratic flash-style form, "
-                         "GatedKATA chunked (tensor cores for bf16 d=32 dv=64, else CUDA "
-                         "cores) or GatedKATA quadratic (tensor cores); the gated forms draw "
-                         "seeded gates")
+                         "GatedKATA chunked (tensor cores for bf16, else CUDA cores) or "
+                         "GatedKATA quadratic (tensor cores); the gated forms draw seeded gates")
     ap.add_argument("--shape", default=None, metavar="B,H,T",
                     help="the workload's recipe at another batch, head count and length "
                          "(for profiles of other shapes; the bench line uses the named sizes)")
