@@ -163,6 +163,41 @@ def _sampled_check(kg, w, name):
     assert worst <= TOL[w.dtype], f"{name}: {worst:.3e} (element-wise {worst_elem:.3e})"
 
 
+def test_long_context_dense_sampled_rows(kg):
+    """The long-context configuration (B=1, H=16, T=131072, d=32, dv=64, C=128) on
+    a dense row sample: for the first and the last head, the first and last 256
+    rows, the last row of every 8th chunk and both sides of every segment seam;
+    64 random rows of four more heads.  About 1500 rows, each computed by the
+    oracle's direct O(T) sum."""
+    w = workloads.WORKLOADS["long_ctx_bf16"]
+    q, k, v = workloads.make_qkv(w, device="cuda")
+    out = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    BH, T = w.B * w.H, w.T
+    seams = _seam_rows(kg, w)
+    dense = sorted(set(list(range(256)) + list(range(T - 256, T)) +
+                   list(range(127, T, 8 * 128)) + seams))
+    rng = np.random.default_rng(11)
+    plan = {0: dense, BH - 1: dense}
+    for h in (3, 6, 9, 12):
+        plan[h] = sorted(set(rng.integers(0, T, size=64).tolist()))
+    worst = worst_elem = 0.0
+    nrows = 0
+    for h, ts in plan.items():
+        flat = np.array(ts, dtype=np.int64)
+        ref = oracle.forward_rows(to_f64(q.reshape(BH, 1, T, w.d)[h:h + 1]),
+                                  to_f64(k.reshape(BH, 1, T, w.d)[h:h + 1]),
+                                  to_f64(v.reshape(BH, 1, T, w.dv)[h:h + 1]), flat)
+        got = to_f64(out.reshape(BH, T, w.dv)[h][flat])
+        worst = max(worst, slice_rel_err(got, ref))
+        worst_elem = max(worst_elem, elem_rel_err(got, ref))
+        nrows += len(ts)
+    print(f"long context: {nrows} rows, slice metric {worst:.3e}, element-wise {worst_elem:.3e}")
+    assert nrows > 1400
+    assert worst <= TOL[w.dtype], f"{worst:.3e} (element-wise {worst_elem:.3e})"
+
+
 # Segmentations (one-CTA output kernel: G = min(152 // BH, chunks) segments per
 # head, segment sums from m = 152 // ((G - 1) BH) pieces per segment)
 _SEGMENTATIONS = [
