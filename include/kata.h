@@ -186,9 +186,12 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  * that can be much smaller than the features; bf16 parts alone would leave
  * them ~2^-9 |psi(q)| |psi(k)| off) and Psi(Q) S_pre from the hi part.  Scratch
  * per token and head: 8 n bytes of features plus the records, about 260 n
- * bytes per 128-token chunk.  The other reduced maps run on CUDA cores in fp32
- * (bf16 inputs are widened; the output is written in the input type).
- * kata_fwd_path_map tells which.
+ * bytes per 128-token chunk.  bf16 with dv in {16, 32, 128} runs the dv = 64
+ * route of the map on 64-column parts of v (the last one zero-padded; an
+ * output column depends only on its own v column), the parts' outputs copied
+ * back.  The other reduced maps run on CUDA cores in fp32 (bf16 inputs are
+ * widened; the output is written in the input type).  kata_fwd_path_map tells
+ * which.
  */
 int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out, int B, int H,
                          int T, int d, int dv, int C, int dtype, int map, int g, float eps,

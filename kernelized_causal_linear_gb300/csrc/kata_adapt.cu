@@ -174,6 +174,31 @@ cudaError_t run_parts(const FwdShape &s, const void *q, const void *k, const voi
 
 }  // namespace
 
+// ---- copies for the parts of the reduced maps (kata_api.cu) ------------------
+__global__ void __launch_bounds__(64)
+state_cols_kernel(const float *__restrict__ sp, const float *__restrict__ zp, int n,
+                  float *__restrict__ state, float *__restrict__ z, int dv, int col, int width,
+                  int write_z) {
+    const int f = blockIdx.x, bh = blockIdx.y;
+    const float *src = sp + ((size_t)bh * n + f) * kPartDv;
+    float *dst = state + ((size_t)bh * n + f) * dv + col;
+    for (int c = threadIdx.x; c < width; c += blockDim.x) dst[c] = src[c];
+    if (write_z && threadIdx.x == 0) z[(size_t)bh * n + f] = zp[(size_t)bh * n + f];
+}
+
+cudaError_t part_copy_cols(const void *src, int sstride, int scol, int width, void *dst, int dstride,
+                           int dcol, int64_t rows, bool zero_rest, cudaStream_t stream) {
+    return copy_cols(src, sstride, scol, width, dst, dstride, dcol, rows, zero_rest, stream);
+}
+
+cudaError_t part_copy_state(const float *sp, const float *zp, int n, float *state, float *z, int BH,
+                            int dv, int col, int width, bool write_z, cudaStream_t stream) {
+    if (n == 0 || BH == 0) return cudaSuccess;
+    state_cols_kernel<<<dim3(n, BH), 64, 0, stream>>>(sp, zp, n, state, z, dv, col, width,
+                                                      write_z ? 1 : 0);
+    return cudaGetLastError();
+}
+
 // ---- plain chunked forward ---------------------------------------------------
 FwdKernels adapt_kernels(const FwdShape &s, int cc_major, int cc_minor, int num_sms) {
     if (!adapted_shape(s)) return FwdKernels::Simt;

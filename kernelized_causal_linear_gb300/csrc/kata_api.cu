@@ -235,6 +235,90 @@ int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype) {
 }  // extern "C"
 
 namespace {
+// Workspace and launch of one kernel family for a (map, shape).
+size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::MapSpec &map,
+                bool with_state) {
+    return kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
+           : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
+           : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
+           : kn == kFeat      ? kata::feat_workspace_bytes(s, map)
+           : map.kind == 0    ? workspace_for(s, kn, di, with_state)
+                              : kata::simt_workspace_bytes(s, map);
+}
+
+cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
+                      void *out, void *ws, const DevInfo &di, cudaStream_t st,
+                      const kata::StateOut &so, const kata::MapSpec &map) {
+    return kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
+           : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
+           : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
+           : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map, so)
+           : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
+                              : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
+}
+
+// A reduced map with bf16 inputs and dv in {16, 32, 128} whose route at dv = 64
+// is a tensor path runs that route on 64-column parts of v (the last one
+// zero-padded): each output column depends on its own v column and every part
+// shares the weights, so the parts are independent forwards whose outputs are
+// the result's columns and whose states are its column blocks.
+bool map_parts(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map, bool with_state,
+               Kernels &core) {
+    if (map.kind == KATA_MAP_FULL || s.dtype != KATA_BF16 || s.dv == 64) return false;
+    FwdShape c = s;
+    c.dv = 64;
+    core = select_map_kernels(c, di, map, with_state);
+    return core != kSimt;
+}
+
+size_t round_up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Workspace: [one v part] [its output] [its state and z] [the route's workspace].
+size_t parts_ws(const FwdShape &s, Kernels core, const DevInfo &di, const kata::MapSpec &map,
+                bool with_state) {
+    FwdShape c = s;
+    c.dv = 64;
+    const size_t rows = (size_t)s.BH() * s.T, n = (size_t)map.n(s.d);
+    const size_t vo = 2 * round_up256(rows * 64 * 2);
+    const size_t sz = with_state ? round_up256((size_t)s.BH() * n * 64 * 4) +
+                                       round_up256((size_t)s.BH() * n * 4)
+                                 : 0;
+    return vo + sz + route_ws(c, core, di, map, with_state);
+}
+
+cudaError_t parts_run(const FwdShape &s, Kernels core, const void *q, const void *k, const void *v,
+                      void *out, void *ws, const DevInfo &di, cudaStream_t st,
+                      const kata::StateOut &so, const kata::MapSpec &map) {
+    FwdShape c = s;
+    c.dv = 64;
+    const int64_t rows = (int64_t)s.BH() * s.T;
+    const size_t n = (size_t)map.n(s.d), half = round_up256((size_t)rows * 64 * 2);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    void *vp = b, *op = b + half;
+    float *sp = reinterpret_cast<float *>(b + 2 * half);
+    float *zp = sp + round_up256((size_t)s.BH() * n * 64 * 4) / 4;
+    const bool with_state = so.state != nullptr;
+    void *cw = b + 2 * half +
+               (with_state ? round_up256((size_t)s.BH() * n * 64 * 4) + round_up256((size_t)s.BH() * n * 4)
+                           : 0);
+    kata::StateOut cso;
+    if (with_state) {
+        cso.state = sp;
+        cso.z = zp;
+    }
+    cudaError_t e = cudaSuccess;
+    for (int col = 0; col < s.dv; col += 64) {
+        const int w = s.dv - col < 64 ? s.dv - col : 64;
+        if ((e = kata::part_copy_cols(v, s.dv, col, w, vp, 64, 0, rows, true, st)) != cudaSuccess) return e;
+        if ((e = route_run(c, core, q, k, vp, op, cw, di, st, cso, map)) != cudaSuccess) return e;
+        if ((e = kata::part_copy_cols(op, 64, 0, w, out, s.dv, col, rows, false, st)) != cudaSuccess) return e;
+        if (with_state && (e = kata::part_copy_state(sp, zp, (int)n, so.state, so.z, s.BH(), s.dv, col, w,
+                                                     col == 0, st)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
 // Shared body of kata_fwd_chunked and kata_fwd_chunked_state.
 int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int B, int H, int T,
                      int d, int dv, int C, int dtype, kata_stream_t stream,
@@ -255,25 +339,18 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
     const Kernels kn = select_map_kernels(s, di, map, with_state);
-    const size_t wsb = kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
-                       : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
-                       : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
-                       : kn == kFeat      ? kata::feat_workspace_bytes(s, map)
-                       : map.kind == 0    ? workspace_for(s, kn, di, with_state)
-                                          : kata::simt_workspace_bytes(s, map);
+    Kernels core = kSimt;
+    const bool parts = kn == kSimt && map_parts(s, di, map, with_state, core);
+    const size_t wsb = parts ? parts_ws(s, core, di, map, with_state)
+                             : route_ws(s, kn, di, map, with_state);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (wsb && cudaMallocAsync(&ws, wsb, st) != cudaSuccess) {
         cudaGetLastError();
         return KATA_ERR_ALLOC;
     }
-    cudaError_t e =
-        kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
-        : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
-        : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
-        : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map, so)
-        : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
-                           : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
+    cudaError_t e = parts ? parts_run(s, core, q, k, v, out, ws, di, st, so, map)
+                          : route_run(s, kn, q, k, v, out, ws, di, st, so, map);
     if (ws) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
@@ -309,7 +386,9 @@ int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int 
     kata::MapSpec ms;
     ms.kind = map;
     ms.g = g;
-    return select_map_kernels(FwdShape{B, H, T, d, dv, C, dtype}, di, ms, false) == kSimt
+    const FwdShape s{B, H, T, d, dv, C, dtype};
+    Kernels core;
+    return select_map_kernels(s, di, ms, false) == kSimt && !map_parts(s, di, ms, false, core)
                ? KATA_PATH_SIMT
                : KATA_PATH_TC;
 }

@@ -53,4 +53,14 @@ cudaError_t decode_map_launch(float *S, float *z, const void *q, const void *k, 
                               void *out, int BH, int d, int dv, int dtype, const MapSpec &map,
                               cudaStream_t stream);
 
+// Copies for running a reduced map's dv = 64 route on 64-column parts of v
+// (kata_api.cu): columns of bf16 rows as copy_cols of kata_adapt.cu (zero_rest:
+// the rest of each destination row zero), and a part's state sp [BH][n][64],
+// zp [BH][n] into columns col .. col + width of state [BH][n][dv] (z as well
+// when write_z).
+cudaError_t part_copy_cols(const void *src, int sstride, int scol, int width, void *dst, int dstride,
+                           int dcol, int64_t rows, bool zero_rest, cudaStream_t stream);
+cudaError_t part_copy_state(const float *sp, const float *zp, int n, float *state, float *z, int BH,
+                            int dv, int col, int width, bool write_z, cudaStream_t stream);
+
 }  // namespace kata

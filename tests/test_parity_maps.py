@@ -223,7 +223,8 @@ def test_map_paths(kg):
         assert path(d=32, map_=map_, g=g) == kg.KATA_PATH_TC
     assert path(d=32, map_=1, g=2) == kg.KATA_PATH_SIMT     # 272 features
     assert path(d=32, map_=2, g=1) == kg.KATA_PATH_SIMT     # 528 features
-    assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_SIMT
+    assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_TC     # 64-column parts of v
+    assert path(d=32, dv=128, dtype=torch.float32, map_=2, g=2) == kg.KATA_PATH_SIMT
     for d in (16, 32, 64):
         assert path(d=d, map_=kg.KATA_MAP_ORTHANT, g=1) == kg.KATA_PATH_TC
 
@@ -348,3 +349,26 @@ def test_two_level_scan(kg, monkeypatch, mapname, d, dv):
         S_ref, z_ref = oracle.prefix_state(to_f64(k), to_f64(v))
         assert slice_rel_err(to_f64(S), S_ref) <= 1e-5
         assert slice_rel_err(to_f64(z)[..., None], z_ref[..., None]) <= 1e-5
+
+
+@pytest.mark.parametrize("map_,g,d,dv", [
+    (1, 2, 64, 128),   # M_2 sub-heads, two parts
+    (2, 2, 64, 32),    # Sigma_2 crosswise sub-heads, one zero-padded part
+    (1, 4, 64, 16),    # M_4 padded sub-heads
+    (2, 4, 64, 128),   # Sigma_4, explicit features
+    (2, 2, 32, 16),
+    (3, 1, 64, 32),    # orthant
+])
+def test_map_value_parts(kg, map_, g, d, dv):
+    """bf16 with dv != 64: the map's dv = 64 route on 64-column parts of v."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=3, T=300, d=d, dv=dv)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
+        kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    eps, scale = _feat_params(kg, map_, g)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), _feat_name(map_), g, eps, scale)
+    err = slice_rel_err(to_f64(out), ref)
+    assert err <= TOL[w.dtype], f"{_feat_name(map_)}_{g} d={d} dv={dv}: {err:.3e}"

@@ -183,11 +183,12 @@ def _map_params(map_, g):
     (1, 2, 64, torch.bfloat16),   # M_2 at d = 64: the sub-heads keep no map state -> CUDA cores
     (2, 2, 16, torch.float32),    # fp32: CUDA cores
 ])
-def test_map_prefill_then_decode(kg, map_, g, d, dtype):
+@pytest.mark.parametrize("dv", [64, 128])
+def test_map_prefill_then_decode(kg, map_, g, d, dtype, dv):
     """kata_fwd_chunked_map_state over T-1 tokens: its state against the oracle's
     map recurrence, its output against the direct definition; then
     kata_decode_step_map with token T-1: the direct definition's row T-1."""
-    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=2, T=301, d=d, dtype=dtype)
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=2, H=2, T=301, d=d, dv=dv, dtype=dtype)
     name = _MAP_NAMES[map_]
     eps, scale = _map_params(map_, g)
     q, k, v = workloads.make_qkv(w)
