@@ -31,6 +31,18 @@ bool valid_map(int map, int d, int g, float eps, float scale) {
     return true;
 }
 
+// The map descriptor of a validated (map, g, eps, scale).  KATA-M_1 is the full
+// rank-one map (one block of width d), so it takes the full map's paths, whose
+// intra-chunk weights are (q.k)^2 formed from q and k.
+kata::MapSpec map_spec(int map, int g, float eps, float scale) {
+    kata::MapSpec ms;
+    ms.kind = (map == KATA_MAP_BLOCK && g == 1) ? KATA_MAP_FULL : map;
+    ms.g = g;
+    ms.eps = eps;
+    ms.scale = scale;
+    return ms;
+}
+
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -383,9 +395,7 @@ int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int 
     if (!valid_map(map, d, g, 0.f, 1.f)) return KATA_PATH_NONE;
     DevInfo di;
     if (device_info(di)) return KATA_PATH_NONE;
-    kata::MapSpec ms;
-    ms.kind = map;
-    ms.g = g;
+    const kata::MapSpec ms = map_spec(map, g, 0.f, 1.f);
     const FwdShape s{B, H, T, d, dv, C, dtype};
     Kernels core;
     return select_map_kernels(s, di, ms, false) == kSimt && !map_parts(s, di, ms, false, core)
@@ -397,12 +407,8 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
                          int T, int d, int dv, int C, int dtype, int map, int g, float eps,
                          float scale, kata_stream_t stream) {
     if (!valid_map(map, d, g, eps, scale)) return KATA_ERR_ARG;
-    kata::MapSpec ms;
-    ms.kind = map;
-    ms.g = g;
-    ms.eps = eps;
-    ms.scale = scale;
-    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{}, ms);
+    return fwd_chunked_impl(q, k, v, out, B, H, T, d, dv, C, dtype, stream, kata::StateOut{},
+                            map_spec(map, g, eps, scale));
 }
 
 // The quadratic form of a shape its kernels take through the rewritings of
@@ -435,11 +441,7 @@ int kata_fwd_chunked_map_state(const void *q, const void *k, const void *v, void
     if (!aligned16(state) || !aligned16(z)) return KATA_ERR_ARG;
     const int rc = check_fwd_shape(B, H, T, d, dv, C, dtype);
     if (rc) return rc;
-    kata::MapSpec ms;
-    ms.kind = map;
-    ms.g = g;
-    ms.eps = eps;
-    ms.scale = scale;
+    const kata::MapSpec ms = map_spec(map, g, eps, scale);
     const size_t es = elem_size(dtype), BH = (size_t)B * H, n = (size_t)ms.n(d);
     const size_t nqk = BH * T * d * es, nvo = BH * T * dv * es;
     const size_t ns = BH * n * dv * 4, nz = BH * n * 4;

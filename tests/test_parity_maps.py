@@ -240,9 +240,9 @@ _FEAT_MAPS = [
     (2, 2, 16),
     (1, 4, 16),
     (2, 4, 16),   # 10 features
-    (1, 1, 16),   # M_1 = the rank-one lift at d = 16: 136 features, weights
-                  # (q.k)^2 near zero for near-orthogonal pairs (the hi/lo X)
-    (2, 1, 16),   # Sigma_1: eps I + s x x^T
+    (1, 1, 16),   # M_1 = the rank-one lift: the full map's path
+    (2, 1, 16),   # Sigma_1: eps I + s x x^T, 136 features; weights s^2 (q.k)^2 + eps
+                  # terms near zero for near-orthogonal pairs (the hi/lo X)
     (3, 1, 64),   # orthant: n = d
     (3, 1, 32),
     (3, 1, 16),
