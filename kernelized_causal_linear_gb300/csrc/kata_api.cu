@@ -104,7 +104,9 @@ int device_info(DevInfo &out) {
 // two tensor-core paths through padded copies and 64-column parts of v.
 // kFeat: a reduced map with at most kFeatMax packed features on the explicit-
 // feature tensor path (kata_feat.cu).
-enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt, kFeat };
+// kTc32SubPad: KATA-M_2 at d = 32 as M_2 at d = 64 on the rows [u_1 0 | u_2 0].
+enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt, kFeat,
+               kTc32SubPad };
 
 Kernels from_fwd(kata::FwdKernels k) {
     switch (k) {
@@ -138,6 +140,9 @@ Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::Map
         }
     }
     if (kata::feat_supported(s, map, di.major, di.minor)) return kFeat;
+    if (s.d == 32 && !with_state && map.kind == KATA_MAP_BLOCK && map.g == 2 &&
+        kata::tc_supported(s, di.major, di.minor))
+        return kTc32SubPad;   // 272 features: above the explicit-feature path's limit
     return kSimt;
 }
 
@@ -247,9 +252,40 @@ int kata_fwd_path(int B, int H, int T, int d, int dv, int C, int dtype) {
 }  // extern "C"
 
 namespace {
+size_t round_up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// KATA-M_2 at d = 32 through the d = 64 sub-head route: q and k rows copied to
+// [u_1 0 | u_2 0] (64 columns); the zero coordinates add nothing to either
+// block's (q_a . k_a)^2.  Workspace: the padded q and k, then the route's.
+FwdShape padded64(const FwdShape &s) {
+    FwdShape c = s;
+    c.d = 64;
+    return c;
+}
+
+cudaError_t m2_pad_run(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
+                       void *ws, const DevInfo &di, cudaStream_t st) {
+    const int64_t rows = (int64_t)s.BH() * s.T;
+    const size_t np = round_up256((size_t)rows * 64 * 2);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    void *qp = b, *kp = b + np;
+    cudaError_t e = cudaSuccess;
+    for (int side = 0; side < 2; ++side) {
+        const void *src = side ? k : q;
+        void *dst = side ? kp : qp;
+        if ((e = kata::part_copy_cols(src, 32, 0, 16, dst, 64, 0, rows, true, st)) != cudaSuccess ||
+            (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
+            return e;
+    }
+    return kata::tc_forward(padded64(s), qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
+}
+
 // Workspace and launch of one kernel family for a (map, shape).
 size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::MapSpec &map,
                 bool with_state) {
+    if (kn == kTc32SubPad)
+        return 2 * round_up256((size_t)s.BH() * s.T * 64 * 2) +
+               kata::tc_workspace_bytes(padded64(s), di.sms, false, 2);
     return kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
            : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
            : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
@@ -261,6 +297,7 @@ size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::Ma
 cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
                       void *out, void *ws, const DevInfo &di, cudaStream_t st,
                       const kata::StateOut &so, const kata::MapSpec &map) {
+    if (kn == kTc32SubPad) return m2_pad_run(s, q, k, v, out, ws, di, st);
     return kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
            : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
            : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
@@ -282,8 +319,6 @@ bool map_parts(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map, b
     core = select_map_kernels(c, di, map, with_state);
     return core != kSimt;
 }
-
-size_t round_up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Workspace: [one v part] [its output] [its state and z] [the route's workspace].
 size_t parts_ws(const FwdShape &s, Kernels core, const DevInfo &di, const kata::MapSpec &map,

@@ -221,7 +221,7 @@ def test_map_paths(kg):
         assert path(dtype=torch.float32, map_=map_, g=g) == kg.KATA_PATH_SIMT
     for map_, g in ((2, 2), (1, 4), (2, 4)):
         assert path(d=32, map_=map_, g=g) == kg.KATA_PATH_TC
-    assert path(d=32, map_=1, g=2) == kg.KATA_PATH_SIMT     # 272 features
+    assert path(d=32, map_=1, g=2) == kg.KATA_PATH_TC       # padded d = 64 sub-heads
     assert path(d=32, map_=2, g=1) == kg.KATA_PATH_SIMT     # 528 features
     assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_TC     # 64-column parts of v
     assert path(d=32, dv=128, dtype=torch.float32, map_=2, g=2) == kg.KATA_PATH_SIMT
@@ -372,3 +372,18 @@ def test_map_value_parts(kg, map_, g, d, dv):
     ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), _feat_name(map_), g, eps, scale)
     err = slice_rel_err(to_f64(out), ref)
     assert err <= TOL[w.dtype], f"{_feat_name(map_)}_{g} d={d} dv={dv}: {err:.3e}"
+
+
+@pytest.mark.parametrize("B,H,T,dv", [(1, 3, 300, 64), (2, 2, 129, 64), (1, 2, 1100, 64),
+                                      (1, 2, 300, 128)])
+def test_m2_d32_padded_sub_heads(kg, B, H, T, dv):
+    """KATA-M_2 at d = 32 (272 features) as M_2 at d = 64 on [u_1 0 | u_2 0]: two
+    d = 32 sub-heads whose padded halves add nothing."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, d=32, dv=dv)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 1, 2) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 1, 2)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "M", 2)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
