@@ -177,7 +177,8 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   KATA-M_4: four sub-heads on the 16-wide blocks, each zero-padded to 32
  *   columns in scratch (the zero coordinates add nothing to (q_a . k_a)^2).
  * KATA-M_2 at d = 32 runs as M_2 at d = 64 on the rows [u_1 0 | u_2 0] (copied
- * to scratch), i.e. two zero-padded d = 32 sub-heads.
+ * to scratch), i.e. two zero-padded d = 32 sub-heads; KATA-Sigma_1 at d = 32 as
+ * Sigma_2 at d = 64 on [u 0] (the same matrix eps I + s u u^T, m = 32).
  * With bf16 inputs and dv = 64, the other maps with at most 192 packed features
  * (KATA-Sigma_4 at d = 64; Sigma_2, Sigma_4 and M_4 at d = 32; every map at
  * d = 16; the orthant map) run on the tensor cores with their features written

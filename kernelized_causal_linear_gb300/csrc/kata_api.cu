@@ -104,9 +104,10 @@ int device_info(DevInfo &out) {
 // two tensor-core paths through padded copies and 64-column parts of v.
 // kFeat: a reduced map with at most kFeatMax packed features on the explicit-
 // feature tensor path (kata_feat.cu).
-// kTc32SubPad: KATA-M_2 at d = 32 as M_2 at d = 64 on the rows [u_1 0 | u_2 0].
+// kTc32SubPad: KATA-M_2 at d = 32 as M_2 at d = 64 on the rows [u_1 0 | u_2 0];
+// kTc32SigmaPad: KATA-Sigma_1 at d = 32 as Sigma_2 at d = 64 on the rows [u 0].
 enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt, kFeat,
-               kTc32SubPad };
+               kTc32SubPad, kTc32SigmaPad };
 
 Kernels from_fwd(kata::FwdKernels k) {
     switch (k) {
@@ -143,6 +144,9 @@ Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::Map
     if (s.d == 32 && !with_state && map.kind == KATA_MAP_BLOCK && map.g == 2 &&
         kata::tc_supported(s, di.major, di.minor))
         return kTc32SubPad;   // 272 features: above the explicit-feature path's limit
+    if (s.d == 32 && !with_state && map.kind == KATA_MAP_SUM && map.g == 1 &&
+        kata::tc_supported(s, di.major, di.minor))
+        return kTc32SigmaPad;   // 528 features
     return kSimt;
 }
 
@@ -263,8 +267,18 @@ FwdShape padded64(const FwdShape &s) {
     return c;
 }
 
-cudaError_t m2_pad_run(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                       void *ws, const DevInfo &di, cudaStream_t st) {
+// KATA-Sigma_1 at d = 32 (eps I + s u u^T) is Sigma_2 at d = 64 on [u 0]: with
+// u_2 = 0, eps I_32 + s (u_1 u_1^T + u_2 u_2^T) is the same matrix (m = 32 in
+// both), so the Sigma_2 route (four crosswise sub-heads, three of them zero,
+// and its eps terms) gives the map exactly.
+kata::MapSpec sigma2_of(const kata::MapSpec &m) {
+    kata::MapSpec c = m;
+    c.g = 2;
+    return c;
+}
+
+cudaError_t pad_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
+                    void *out, void *ws, const DevInfo &di, cudaStream_t st, const kata::MapSpec &map) {
     const int64_t rows = (int64_t)s.BH() * s.T;
     const size_t np = round_up256((size_t)rows * 64 * 2);
     uint8_t *b = static_cast<uint8_t *>(ws);
@@ -273,19 +287,31 @@ cudaError_t m2_pad_run(const FwdShape &s, const void *q, const void *k, const vo
     for (int side = 0; side < 2; ++side) {
         const void *src = side ? k : q;
         void *dst = side ? kp : qp;
-        if ((e = kata::part_copy_cols(src, 32, 0, 16, dst, 64, 0, rows, true, st)) != cudaSuccess ||
-            (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
-            return e;
+        if (kn == kTc32SubPad) {   // [u_1 0 | u_2 0]
+            if ((e = kata::part_copy_cols(src, 32, 0, 16, dst, 64, 0, rows, true, st)) != cudaSuccess ||
+                (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
+                return e;
+        } else {                   // [u 0]
+            if ((e = kata::part_copy_cols(src, 32, 0, 32, dst, 64, 0, rows, true, st)) != cudaSuccess)
+                return e;
+        }
     }
-    return kata::tc_forward(padded64(s), qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
+    const FwdShape c = padded64(s);
+    if (kn == kTc32SubPad)
+        return kata::tc_forward(c, qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
+    const kata::MapSpec m2 = sigma2_of(map);
+    return kata::tc_forward(c, qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 4, &m2);
 }
 
 // Workspace and launch of one kernel family for a (map, shape).
 size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::MapSpec &map,
                 bool with_state) {
-    if (kn == kTc32SubPad)
+    if (kn == kTc32SubPad || kn == kTc32SigmaPad) {
+        const kata::MapSpec m2 = sigma2_of(map);
         return 2 * round_up256((size_t)s.BH() * s.T * 64 * 2) +
-               kata::tc_workspace_bytes(padded64(s), di.sms, false, 2);
+               (kn == kTc32SubPad ? kata::tc_workspace_bytes(padded64(s), di.sms, false, 2)
+                                  : kata::tc_workspace_bytes(padded64(s), di.sms, false, 4, &m2));
+    }
     return kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
            : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
            : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
@@ -297,7 +323,7 @@ size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::Ma
 cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
                       void *out, void *ws, const DevInfo &di, cudaStream_t st,
                       const kata::StateOut &so, const kata::MapSpec &map) {
-    if (kn == kTc32SubPad) return m2_pad_run(s, q, k, v, out, ws, di, st);
+    if (kn == kTc32SubPad || kn == kTc32SigmaPad) return pad_run(s, kn, q, k, v, out, ws, di, st, map);
     return kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
            : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
            : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)

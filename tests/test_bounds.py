@@ -68,7 +68,7 @@ def test_chunked_forward_stays_in_bounds(kg, name, overrides):
 
 
 @pytest.mark.parametrize("map_,g,d", [(1, 2, 64), (2, 2, 64), (1, 4, 64), (2, 4, 64), (1, 4, 32),
-                                      (1, 2, 32), (3, 1, 16)])
+                                      (1, 2, 32), (2, 1, 32), (3, 1, 16)])
 def test_map_sub_heads_stay_in_bounds(kg, map_, g, d):
     """Sub-head routes at d = 64 and the explicit-feature path (Sigma_4, M_4 at
     d = 32, the orthant map)."""

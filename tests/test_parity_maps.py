@@ -222,7 +222,8 @@ def test_map_paths(kg):
     for map_, g in ((2, 2), (1, 4), (2, 4)):
         assert path(d=32, map_=map_, g=g) == kg.KATA_PATH_TC
     assert path(d=32, map_=1, g=2) == kg.KATA_PATH_TC       # padded d = 64 sub-heads
-    assert path(d=32, map_=2, g=1) == kg.KATA_PATH_SIMT     # 528 features
+    assert path(d=32, map_=2, g=1) == kg.KATA_PATH_TC       # Sigma_2 at d = 64 on [u 0]
+    assert path(map_=2, g=1) == kg.KATA_PATH_SIMT           # Sigma_1 at d = 64: 2080 features
     assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_TC     # 64-column parts of v
     assert path(d=32, dv=128, dtype=torch.float32, map_=2, g=2) == kg.KATA_PATH_SIMT
     for d in (16, 32, 64):
@@ -386,4 +387,19 @@ def test_m2_d32_padded_sub_heads(kg, B, H, T, dv):
     torch.cuda.synchronize()
     assert kg.kata_sync_status() == kg.KATA_OK
     ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "M", 2)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("B,H,T,dv", [(1, 3, 300, 64), (2, 2, 129, 64), (1, 2, 300, 128)])
+@pytest.mark.parametrize("eps,scale", [(1e-4, 1.0), (0.05, 0.5)])
+def test_sigma1_d32_padded(kg, B, H, T, dv, eps, scale):
+    """KATA-Sigma_1 at d = 32 (eps I + s u u^T, 528 features) as Sigma_2 at d = 64 on
+    [u 0]: with u_2 = 0 the matrix is the same (m = 32 in both)."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, d=32, dv=dv)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 1) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 2, 1, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 1, eps, scale)
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
