@@ -366,12 +366,17 @@ def test_host_entry_point(kg, name):
     assert worst <= TOL[w.dtype], f"{worst:.3e}"
 
 
-@pytest.mark.parametrize("form", ["simt_fp32", "tc_bf16", "quadratic", "gated"])
+@pytest.mark.parametrize("form", ["simt_fp32", "tc_bf16", "quadratic", "gated", "tc64_bf16",
+                                  "sigma4_features", "d16_dv128"])
 def test_maximum_head_count(kg, form):
     """B * H = 65535 (the grid limit every path checks) at T = 3: one partial chunk
     per head.  Sampled heads against the oracle."""
     if form == "simt_fp32":
         w = workloads.WORKLOADS["small_fp32"].scaled(B=3, H=21845, T=3)
+    elif form in ("tc64_bf16", "sigma4_features"):
+        w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=3, H=21845, T=3)
+    elif form == "d16_dv128":
+        w = workloads.WORKLOADS["mid_bf16"].scaled(B=3, H=21845, T=3, d=16, dv=128)
     else:
         w = workloads.WORKLOADS["mid_bf16"].scaled(B=3, H=21845, T=3)
     q, k, v = workloads.make_qkv(w)
@@ -382,6 +387,8 @@ def test_maximum_head_count(kg, form):
     elif form == "gated":
         g = workloads.make_gate(w)
         out = kg.kata_fwd_chunked_gated(qd, kd, vd, g.cuda(), w.C)
+    elif form == "sigma4_features":
+        out = kg.kata_fwd_chunked_map(qd, kd, vd, w.C, 2, 4, 1e-4, 0.25)
     else:
         out = kg.kata_fwd_chunked(qd, kd, vd, w.C)
     torch.cuda.synchronize()
@@ -389,10 +396,13 @@ def test_maximum_head_count(kg, form):
     heads = [(0, 0), (1, 12345), (2, w.H - 1)]
     for b, h in heads:
         sl = (slice(b, b + 1), slice(h, h + 1))
-        if g is None:
-            ref = oracle.forward(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]))
-        else:
+        if g is not None:
             ref = oracle.forward_gated(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(g[sl]))
+        elif form == "sigma4_features":
+            ref = oracle.forward_map(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), "Sigma", 4, 1e-4,
+                                     0.25)
+        else:
+            ref = oracle.forward(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]))
         assert slice_rel_err(to_f64(out[sl]), ref) <= TOL[w.dtype], (form, b, h)
 
 
