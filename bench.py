@@ -164,16 +164,19 @@ def stage_work(stage: str, w, num_sms: int = SMS, fm: FeatureMap = FULL_MAP):
     if stage == "tc_m4_pad":
         # q and k rows in, zero-padded to four 32-wide blocks out
         return float(BH * T) * 2 * (d * 2 + 4 * 32 * 2), "GB/s", "hbm"
-    # Sigma_2 finalize: 128-token chunk sums of v, |k|^2 v, |k|^2 (reads k, v, writes
-    # one record per chunk), their exclusive scan, and the pass that reads the four
-    # sub-heads' fp32 numerators and denominators with q, k, v and writes bf16 out
+    # Sigma_g finalize: 128-token chunk sums of v, |k|^2 v, |k|^2 (reads k, v, writes
+    # one record per chunk), their exclusive scan, and the pass that reads the fp32
+    # partial numerators and denominators with q, k, v and writes bf16 out: four of
+    # each for Sigma_2 (crosswise sub-heads), four numerators (feature groups) and one
+    # denominator for Sigma_1 at d = 64, one of each for Sigma_1 at d = 32
     rec_sigma = 4.0 * (2 * dv + 4)
+    nn, nd = (1, 1) if (fm.g == 1 and d == 32) else (4, 1) if fm.g == 1 else (4, 4)
     if stage == "tc_sigma_sums":
         return float(BH * T) * (d + dv) * 2 + rec_sigma * -(-T // 128) * BH, "GB/s", "hbm"
     if stage == "tc_sigma_scan":
         return 2.0 * rec_sigma * -(-T // 128) * BH, "GB/s", "hbm"
     if stage == "tc_sigma_finalize":
-        return (float(BH * T) * (4 * (dv + 1) * 4 + (2 * d + dv) * 2 + dv * 2)
+        return (float(BH * T) * ((nn * dv + nd) * 4 + (2 * d + dv) * 2 + dv * 2)
                 + rec_sigma * -(-T // 128) * BH), "GB/s", "hbm"
     if stage == "tc64_output":
         intra128 = 2.0 * (d + dv + 1) * _intra_pairs(T, 128) * BH

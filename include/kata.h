@@ -177,8 +177,10 @@ int kata_fwd_chunked_state(const void *q, const void *k, const void *v, void *ou
  *   KATA-M_4: four sub-heads on the 16-wide blocks, each zero-padded to 32
  *   columns in scratch (the zero coordinates add nothing to (q_a . k_a)^2).
  * KATA-M_2 at d = 32 runs as M_2 at d = 64 on the rows [u_1 0 | u_2 0] (copied
- * to scratch), i.e. two zero-padded d = 32 sub-heads; KATA-Sigma_1 at d = 32 as
- * Sigma_2 at d = 64 on [u 0] (the same matrix eps I + s u u^T, m = 32).
+ * to scratch), i.e. two zero-padded d = 32 sub-heads.  KATA-Sigma_1 (eps I +
+ * s u u^T, m = d) at d = 32 and d = 64 runs as the full map on the tensor path of
+ * that d, its numerators and denominator kept in fp32, scaled by scale^2, plus
+ * the same eps terms.
  * With bf16 inputs and dv = 64, the other maps with at most 192 packed features
  * (KATA-Sigma_4 at d = 64; Sigma_2, Sigma_4 and M_4 at d = 32; every map at
  * d = 16; the orthant map) run on the tensor cores with their features written
@@ -209,8 +211,9 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
  *   order of kata_lift_map (each matrix row-major over its upper triangle,
  *   sqrt(2) off the diagonal, M_g's matrices block by block).
  * state and z 16-byte aligned, not overlapping each other or the other buffers
- * (KATA_ERR_ARG).  The d = 64 sub-head routes of M_2, Sigma_2 and M_4 keep no
- * state of the map, so with the state exported those maps take the CUDA cores;
+ * (KATA_ERR_ARG).  The sub-head routes (M_2, Sigma_2 and M_4 at d = 64, M_2 at
+ * d = 32) and the Sigma_1 routes keep no state of the map, so with the state
+ * exported those maps take the CUDA cores;
  * the explicit-feature path exports its scanned records (products of the bf16
  * hi feature parts with v, accumulated in fp32).  Other arguments and errors as
  * kata_fwd_chunked_map.

@@ -104,10 +104,11 @@ int device_info(DevInfo &out) {
 // two tensor-core paths through padded copies and 64-column parts of v.
 // kFeat: a reduced map with at most kFeatMax packed features on the explicit-
 // feature tensor path (kata_feat.cu).
-// kTc32SubPad: KATA-M_2 at d = 32 as M_2 at d = 64 on the rows [u_1 0 | u_2 0];
-// kTc32SigmaPad: KATA-Sigma_1 at d = 32 as Sigma_2 at d = 64 on the rows [u 0].
+// kTc32SubPad: KATA-M_2 at d = 32 as M_2 at d = 64 on the rows [u_1 0 | u_2 0].
+// kTc32Sigma1 / kTc64Sigma1: KATA-Sigma_1 (eps I + s u u^T) at d = 32 / 64 as the
+// full map on the d = 32 / d = 64 tensor path plus its eps terms.
 enum Kernels { kSimt, kTc32, kTc64, kTc32Sub, kTc32Sigma, kTc32M4, kTc32Adapt, kTc64Adapt, kFeat,
-               kTc32SubPad, kTc32SigmaPad };
+               kTc32SubPad, kTc32Sigma1, kTc64Sigma1 };
 
 Kernels from_fwd(kata::FwdKernels k) {
     switch (k) {
@@ -124,13 +125,17 @@ Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
 }
 
 // Kernels for a reduced map: KATA-M_2, KATA-Sigma_2 and KATA-M_4 at d = 64 are
-// d = 32 sub-heads on the d = 32 tensor path (bf16, dv = 64); the other maps
-// with at most kFeatMax packed features (KATA-Sigma_4 at d = 64; Sigma_2,
-// Sigma_4 and M_4 at d = 32; every map at d = 16; the orthant map) take the
-// explicit-feature tensor path (bf16, dv = 64); the rest runs on CUDA cores.
+// d = 32 sub-heads on the d = 32 tensor path (bf16, dv = 64); KATA-Sigma_1 is
+// the full map plus its eps terms; the other maps with at most kFeatMax packed
+// features (KATA-Sigma_4 at d = 64; Sigma_2, Sigma_4 and M_4 at d = 32; every
+// map at d = 16; the orthant map) take the explicit-feature tensor path (bf16,
+// dv = 64); the rest runs on CUDA cores.
 Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
                            bool with_state) {
     if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
+    if (s.d == 64 && !with_state && map.kind == KATA_MAP_SUM && map.g == 1 &&
+        kata::tc64_supported(s, di.major, di.minor, di.sms))
+        return kTc64Sigma1;   // 2080 features
     if (s.d == 64 && !with_state) {
         FwdShape half = s;
         half.d = 32;
@@ -146,7 +151,7 @@ Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::Map
         return kTc32SubPad;   // 272 features: above the explicit-feature path's limit
     if (s.d == 32 && !with_state && map.kind == KATA_MAP_SUM && map.g == 1 &&
         kata::tc_supported(s, di.major, di.minor))
-        return kTc32SigmaPad;   // 528 features
+        return kTc32Sigma1;   // 528 features
     return kSimt;
 }
 
@@ -267,53 +272,33 @@ FwdShape padded64(const FwdShape &s) {
     return c;
 }
 
-// KATA-Sigma_1 at d = 32 (eps I + s u u^T) is Sigma_2 at d = 64 on [u 0]: with
-// u_2 = 0, eps I_32 + s (u_1 u_1^T + u_2 u_2^T) is the same matrix (m = 32 in
-// both), so the Sigma_2 route (four crosswise sub-heads, three of them zero,
-// and its eps terms) gives the map exactly.
-kata::MapSpec sigma2_of(const kata::MapSpec &m) {
-    kata::MapSpec c = m;
-    c.g = 2;
-    return c;
-}
-
-cudaError_t pad_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
-                    void *out, void *ws, const DevInfo &di, cudaStream_t st, const kata::MapSpec &map) {
+cudaError_t pad_run(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
+                    void *ws, const DevInfo &di, cudaStream_t st) {
     const int64_t rows = (int64_t)s.BH() * s.T;
     const size_t np = round_up256((size_t)rows * 64 * 2);
     uint8_t *b = static_cast<uint8_t *>(ws);
     void *qp = b, *kp = b + np;
     cudaError_t e = cudaSuccess;
-    for (int side = 0; side < 2; ++side) {
+    for (int side = 0; side < 2; ++side) {   // [u_1 0 | u_2 0]
         const void *src = side ? k : q;
         void *dst = side ? kp : qp;
-        if (kn == kTc32SubPad) {   // [u_1 0 | u_2 0]
-            if ((e = kata::part_copy_cols(src, 32, 0, 16, dst, 64, 0, rows, true, st)) != cudaSuccess ||
-                (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
-                return e;
-        } else {                   // [u 0]
-            if ((e = kata::part_copy_cols(src, 32, 0, 32, dst, 64, 0, rows, true, st)) != cudaSuccess)
-                return e;
-        }
+        if ((e = kata::part_copy_cols(src, 32, 0, 16, dst, 64, 0, rows, true, st)) != cudaSuccess ||
+            (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
+            return e;
     }
-    const FwdShape c = padded64(s);
-    if (kn == kTc32SubPad)
-        return kata::tc_forward(c, qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
-    const kata::MapSpec m2 = sigma2_of(map);
-    return kata::tc_forward(c, qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 4, &m2);
+    return kata::tc_forward(padded64(s), qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
 }
 
 // Workspace and launch of one kernel family for a (map, shape).
 size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::MapSpec &map,
                 bool with_state) {
-    if (kn == kTc32SubPad || kn == kTc32SigmaPad) {
-        const kata::MapSpec m2 = sigma2_of(map);
+    if (kn == kTc32SubPad)
         return 2 * round_up256((size_t)s.BH() * s.T * 64 * 2) +
-               (kn == kTc32SubPad ? kata::tc_workspace_bytes(padded64(s), di.sms, false, 2)
-                                  : kata::tc_workspace_bytes(padded64(s), di.sms, false, 4, &m2));
-    }
-    return kn == kTc32Sub     ? kata::tc_workspace_bytes(s, di.sms, false, 2)
-           : kn == kTc32Sigma ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
+               kata::tc_workspace_bytes(padded64(s), di.sms, false, 2);
+    return kn == kTc32Sub      ? kata::tc_workspace_bytes(s, di.sms, false, 2)
+           : kn == kTc32Sigma  ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
+           : kn == kTc32Sigma1 ? kata::tc_workspace_bytes(s, di.sms, false, 1, &map)
+           : kn == kTc64Sigma1 ? kata::tc64_workspace_bytes(s, false, &map)
            : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
            : kn == kFeat      ? kata::feat_workspace_bytes(s, map)
            : map.kind == 0    ? workspace_for(s, kn, di, with_state)
@@ -323,9 +308,11 @@ size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::Ma
 cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
                       void *out, void *ws, const DevInfo &di, cudaStream_t st,
                       const kata::StateOut &so, const kata::MapSpec &map) {
-    if (kn == kTc32SubPad || kn == kTc32SigmaPad) return pad_run(s, kn, q, k, v, out, ws, di, st, map);
-    return kn == kTc32Sub     ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
-           : kn == kTc32Sigma ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
+    if (kn == kTc32SubPad) return pad_run(s, q, k, v, out, ws, di, st);
+    return kn == kTc32Sub      ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
+           : kn == kTc32Sigma  ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
+           : kn == kTc32Sigma1 ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 1, &map)
+           : kn == kTc64Sigma1 ? kata::tc64_forward(s, q, k, v, out, ws, st, so, &map)
            : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
            : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map, so)
            : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)

@@ -114,9 +114,10 @@ cudaError_t gated_forward(const FwdShape &s, const void *q, const void *k, const
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
 // nsub > 1: the head's q/k columns are nsub sub-heads of width d / nsub, each run
 // as a d / nsub head (KATA-M_2 at d = 64); their numerators and denominators are
-// summed.  No state export then.  sigma (KATA-Sigma_2 at d = 64, nsub = 4): the
-// four sub-heads pair query half a with key half b, and the map's eps terms are
-// added in the finalize pass (kata_sigma.cu).
+// summed.  No state export then.  sigma: KATA-Sigma_2 at d = 64 (nsub = 4, the
+// four sub-heads pair query half a with key half b) or KATA-Sigma_1 at d = 32
+// (nsub = 1, the full map); the map's eps terms are added in the finalize pass
+// (kata_sigma.cu), and there is no state export either.
 size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false, int nsub = 1,
                           const MapSpec *sigma = nullptr);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
@@ -147,12 +148,17 @@ cudaError_t gated_wide_forward(const FwdShape &s, const void *q, const void *k, 
 size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms);
 cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
                           void *workspace, int num_sms, cudaStream_t stream);
-// KATA-Sigma_2 finalize (kata_sigma.cu): the scratch it needs after the
-// sub-head partials, and the pass that sums them with the eps terms.
+// KATA-Sigma_g finalize (kata_sigma.cu): the scratch it needs after the
+// partials, and the pass that sums them with the eps terms.  The partials'
+// layouts: Sub4, the four crosswise d = 32 sub-heads of Sigma_2 at d = 64
+// (N [BH * 4][T][64], then D [BH * 4][T]); Sub1, Sigma_1 at d = 32 as one
+// d = 32 sub-head (N [BH][T][64], then D [BH][T]); Wide, Sigma_1 at d = 64 on the
+// d = 64 path (N [4][BH][T][64] of its feature groups, then D [BH][T]).
+enum class SigmaParts { Sub4, Sub1, Wide };
 size_t sigma_workspace_bytes(const FwdShape &s);
-cudaError_t sigma_finalize_launch(const FwdShape &s, const float *part, float *ws, const void *q,
-                                  const void *k, const void *v, void *out, const MapSpec &map,
-                                  cudaStream_t stream);
+cudaError_t sigma_finalize_launch(const FwdShape &s, SigmaParts parts, const float *part,
+                                  float *ws, const void *q, const void *k, const void *v, void *out,
+                                  const MapSpec &map, cudaStream_t stream);
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();
@@ -164,10 +170,14 @@ int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens);
 
 // ---- tcgen05 path at d = 64 (state split over four CTAs): kata_tc64.cu -----
 bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
-size_t tc64_workspace_bytes(const FwdShape &s, bool with_state = false);
+// sigma (KATA-Sigma_1 at d = 64, eps I + s u u^T): the full map's numerators and
+// denominator stay in fp32 and the finalize pass of kata_sigma.cu adds the
+// map's eps terms.  No state export then.
+size_t tc64_workspace_bytes(const FwdShape &s, bool with_state = false,
+                            const MapSpec *sigma = nullptr);
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v,
                          void *out, void *workspace, cudaStream_t stream,
-                         const StateOut &so = StateOut{});
+                         const StateOut &so = StateOut{}, const MapSpec *sigma = nullptr);
 int tc64_take_error();
 
 // ---- quadratic (flash-style) forward: kata_quad.cu ------------------------

@@ -984,9 +984,16 @@ FwdShape sub_shape(const FwdShape &s, int nsub, bool cross = false) {
     ss.d = cross ? s.d / 2 : s.d / nsub;
     return ss;
 }
-// Sub-head partials (N and D, fp32) come first in the workspace, rounded to 256 bytes.
-size_t sub_part_floats(const FwdShape &ss, int nsub) {
-    return nsub > 1 ? (((size_t)ss.BH() * ss.T * 65 + 63) & ~(size_t)63) : 0;
+// Sub-head partials (N and D, fp32) come first in the workspace, rounded to 256
+// bytes: with several sub-heads, or with a map's eps terms still to add.
+size_t sub_part_floats(const FwdShape &ss, bool partials) {
+    return partials ? (((size_t)ss.BH() * ss.T * 65 + 63) & ~(size_t)63) : 0;
+}
+// The shapes a map's eps terms are added to: Sigma_2 at d = 64 as four crosswise
+// sub-heads, Sigma_1 at d = 32 as the full map.
+bool sigma_shape_ok(const FwdShape &s0, int nsub, const MapSpec *sigma) {
+    return sigma == nullptr || (nsub == 4 && s0.d == 64 && sigma->g == 2) ||
+           (nsub == 1 && s0.d == 32 && sigma->g == 1);
 }
 }  // namespace
 
@@ -1021,8 +1028,8 @@ Plan plan(const FwdShape &s, int num_sms, bool with_state, int span) {
 // The CTA-pair output kernel (kata_tc_pair.cu) splits the feature blocks of a
 // segment over two SMs.  It is exact, but slower than the one-CTA kernel on
 // every measured shape, so it runs only when KATA_TC_OUTPUT=pair is set.
-bool use_pair(int nsub) {
-    if (nsub != 1) return false;
+bool use_pair(int nsub, const MapSpec *sigma) {
+    if (nsub != 1 || sigma != nullptr) return false;
     const char *e = getenv("KATA_TC_OUTPUT");
     return e != nullptr && strcmp(e, "pair") == 0;
 }
@@ -1030,19 +1037,19 @@ bool use_pair(int nsub) {
 
 size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int nsub,
                           const MapSpec *sigma) {
-    const bool cross = sigma != nullptr;
+    const bool cross = sigma != nullptr && nsub == 4;
     const FwdShape s = sub_shape(s0, nsub, cross);
     // piece records (of the key sub-heads: 2 per head when crosswise), plus the
     // inclusive totals when the state is exported
-    const Plan p = plan(s, num_sms, with_state, use_pair(nsub) ? 2 : 1);
+    const Plan p = plan(s, num_sms, with_state, use_pair(nsub, sigma) ? 2 : 1);
     const size_t recs = (size_t)p.NR + (with_state ? 1 : 0);
     const size_t heads = cross ? (size_t)s0.BH() * 2 : (size_t)s.BH();
-    return sizeof(float) * (sub_part_floats(s, nsub) + heads * recs * Cfg<32, 64>::E) +
-           (cross ? sigma_workspace_bytes(s0) : 0);
+    return sizeof(float) * (sub_part_floats(s, nsub > 1 || sigma) + heads * recs * Cfg<32, 64>::E) +
+           (sigma ? sigma_workspace_bytes(s0) : 0);
 }
 
 int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens) {
-    const Plan p = plan(s, num_sms, false, use_pair(1) ? 2 : 1);
+    const Plan p = plan(s, num_sms, false, use_pair(1, nullptr) ? 2 : 1);
     if (seg_tokens) *seg_tokens = p.Lc * kTile;
     return p.G;
 }
@@ -1051,19 +1058,20 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
                        const StateOut &so, int nsub, const MapSpec *sigma) {
     using C = Cfg<32, 64>;
-    if (nsub > 1 && so.state != nullptr) return cudaErrorInvalidValue;   // no sub-head state export
-    const bool cross = sigma != nullptr;
-    if (cross && (nsub != 4 || s0.d != 64)) return cudaErrorInvalidValue;
+    // no state export from sub-heads or with eps terms
+    if ((nsub > 1 || sigma) && so.state != nullptr) return cudaErrorInvalidValue;
+    if (!sigma_shape_ok(s0, nsub, sigma)) return cudaErrorInvalidValue;
+    const bool cross = sigma != nullptr && nsub == 4, partials = nsub > 1 || sigma;
     const FwdShape s = sub_shape(s0, nsub, cross);
-    const bool with_state = so.state != nullptr, pair = use_pair(nsub);
+    const bool with_state = so.state != nullptr, pair = use_pair(nsub, sigma);
     const Plan p = plan(s, num_sms, with_state, pair ? 2 : 1);
     CUtensorMap mq, mk, mv;
     // q, k: rows of s0.d columns, read s.d at a time; v: one head's rows, shared by its sub-heads
     if (!make_map(mq, q, s0.d, s.T, s0.BH(), s.d) || !make_map(mk, k, s0.d, s.T, s0.BH(), s.d) ||
         !make_map(mv, v, s.dv, s.T, s0.BH()))
         return cudaErrorInvalidValue;
-    float *part = nsub > 1 ? static_cast<float *>(workspace) : nullptr;
-    float *seg = static_cast<float *>(workspace) + sub_part_floats(s, nsub);
+    float *part = partials ? static_cast<float *>(workspace) : nullptr;
+    float *seg = static_cast<float *>(workspace) + sub_part_floats(s, partials);
     // crosswise, the segment sums depend on the key half only: 2 per head
     const int state_heads = cross ? s0.BH() * 2 : s.BH(), state_nsub = cross ? 2 : nsub;
     // Segment sums: of every segment but the last (the output kernel carries the
@@ -1107,10 +1115,11 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
                 OutGate{nullptr, nullptr, 1});
         }
     }
-    if (cross) {
-        const size_t off = sub_part_floats(s, nsub) + (size_t)state_heads * p.NR * C::E;
-        return sigma_finalize_launch(s0, part, static_cast<float *>(workspace) + off, q, k, v, out,
-                                     *sigma, stream);
+    if (sigma) {
+        const size_t off = sub_part_floats(s, partials) + (size_t)state_heads * p.NR * C::E;
+        return sigma_finalize_launch(s0, cross ? SigmaParts::Sub4 : SigmaParts::Sub1, part,
+                                     static_cast<float *>(workspace) + off, q, k, v, out, *sigma,
+                                     stream);
     }
     if (part != nullptr) {
         TraceScope tr("tc_sub_finalize", stream);

@@ -761,16 +761,19 @@ bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms) 
 // (their 32-byte stores need it).
 size_t srec_offset_floats(size_t rows) { return (rows * 64 * 4 + rows + 63) & ~(size_t)63; }
 
-size_t tc64_workspace_bytes(const FwdShape &s, bool with_state) {
+size_t tc64_workspace_bytes(const FwdShape &s, bool with_state, const MapSpec *sigma) {
     const size_t rows = (size_t)s.BH() * s.T;
+    if (sigma != nullptr) return sizeof(float) * srec_offset_floats(rows) + sigma_workspace_bytes(s);
     return sizeof(float) * (with_state ? srec_offset_floats(rows) + (size_t)s.BH() * kRec64
                                        : rows * 64 * 4 + rows);
 }
 
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                         void *workspace, cudaStream_t stream, const StateOut &so) {
+                         void *workspace, cudaStream_t stream, const StateOut &so,
+                         const MapSpec *sigma) {
     const int NCt = (s.T + kTile - 1) / kTile;
     const size_t rows = (size_t)s.BH() * s.T;
+    if (sigma != nullptr && so.state != nullptr) return cudaErrorInvalidValue;
     if (rows == 0) return cudaSuccess;
     float *part = static_cast<float *>(workspace);
     float *dden = part + rows * 64 * 4;
@@ -786,6 +789,9 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
         wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, mp16, dden,
                                                                         srec, s.T, NCt);
     }
+    if (sigma != nullptr)   // the eps scratch after the partials, from a 256-byte boundary
+        return sigma_finalize_launch(s, SigmaParts::Wide, part, part + srec_offset_floats(rows), q, k,
+                                     v, out, *sigma, stream);
     {
         TraceScope tr("tc64_finalize", stream);
         const int64_t n4 = (int64_t)rows * 16;

@@ -78,10 +78,10 @@ def test_map_lift_parity(kg, map_, g, d, dtype):
     assert err <= 1e-6
 
 
-@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4), (2, 4)])
+@pytest.mark.parametrize("map_,g", [(1, 2), (2, 2), (1, 4), (2, 4), (2, 1)])
 def test_map_full_size_sampled_rows(kg, map_, g):
-    """The LM-layer workload with M_2 / Sigma_2 / M_4 / Sigma_4, sampled rows
-    against the oracle."""
+    """The LM-layer workload with M_2 / Sigma_2 / M_4 / Sigma_4 / Sigma_1, sampled
+    rows against the oracle."""
     w = workloads.WORKLOADS["lm_layer_bf16"]
     q, k, v = workloads.make_qkv(w, device="cuda")
     eps, scale = _params(kg, map_, g)
@@ -206,10 +206,10 @@ def test_m4_tensor_path_zero_block(kg):
 
 
 def test_map_paths(kg):
-    """bf16, dv = 64: M_2, Sigma_2, M_4 at d = 64 as d = 32 sub-heads; Sigma_4 at
-    d = 64, every map at d = 16 and all but M_2 / M_1 / Sigma_1 at d = 32 (more
-    than 192 features) on the explicit-feature path; fp32, other dv and the
-    larger maps on CUDA cores."""
+    """bf16, dv = 64: M_2, Sigma_2, M_4 at d = 64 as d = 32 sub-heads; Sigma_1 as
+    the full map plus its eps terms; Sigma_4 at d = 64, every map at d = 16 and
+    all but M_2 / M_1 / Sigma_1 at d = 32 (more than 192 features) on the
+    explicit-feature path; fp32 on CUDA cores."""
     w = workloads.WORKLOADS["lm_layer_bf16"]
 
     def path(d=w.d, dv=w.dv, dtype=w.dtype, map_=1, g=2):
@@ -222,8 +222,10 @@ def test_map_paths(kg):
     for map_, g in ((2, 2), (1, 4), (2, 4)):
         assert path(d=32, map_=map_, g=g) == kg.KATA_PATH_TC
     assert path(d=32, map_=1, g=2) == kg.KATA_PATH_TC       # padded d = 64 sub-heads
-    assert path(d=32, map_=2, g=1) == kg.KATA_PATH_TC       # Sigma_2 at d = 64 on [u 0]
-    assert path(map_=2, g=1) == kg.KATA_PATH_SIMT           # Sigma_1 at d = 64: 2080 features
+    assert path(d=32, map_=2, g=1) == kg.KATA_PATH_TC       # the d = 32 full map + eps terms
+    assert path(map_=2, g=1) == kg.KATA_PATH_TC             # the d = 64 full map + eps terms
+    assert path(dv=128, map_=2, g=1) == kg.KATA_PATH_TC     # 64-column parts of v
+    assert path(dtype=torch.float32, map_=2, g=1) == kg.KATA_PATH_SIMT
     assert path(d=32, dv=128, map_=2, g=2) == kg.KATA_PATH_TC     # 64-column parts of v
     assert path(d=32, dv=128, dtype=torch.float32, map_=2, g=2) == kg.KATA_PATH_SIMT
     for d in (16, 32, 64):
@@ -359,6 +361,7 @@ def test_two_level_scan(kg, monkeypatch, mapname, d, dv):
     (2, 4, 64, 128),   # Sigma_4, explicit features
     (2, 2, 32, 16),
     (3, 1, 64, 32),    # orthant
+    (2, 1, 64, 128),   # Sigma_1: the d = 64 full map plus eps terms, two parts
 ])
 def test_map_value_parts(kg, map_, g, d, dv):
     """bf16 with dv != 64: the map's dv = 64 route on 64-column parts of v."""
@@ -392,9 +395,10 @@ def test_m2_d32_padded_sub_heads(kg, B, H, T, dv):
 
 @pytest.mark.parametrize("B,H,T,dv", [(1, 3, 300, 64), (2, 2, 129, 64), (1, 2, 300, 128)])
 @pytest.mark.parametrize("eps,scale", [(1e-4, 1.0), (0.05, 0.5)])
-def test_sigma1_d32_padded(kg, B, H, T, dv, eps, scale):
-    """KATA-Sigma_1 at d = 32 (eps I + s u u^T, 528 features) as Sigma_2 at d = 64 on
-    [u 0]: with u_2 = 0 the matrix is the same (m = 32 in both)."""
+def test_sigma1_d32_tensor_path(kg, B, H, T, dv, eps, scale):
+    """KATA-Sigma_1 at d = 32 (eps I + s u u^T, 528 features): s^2 times the full
+    map's (q . k)^2 on the d = 32 tensor path, plus eps s (|q|^2 + |k|^2) + eps^2 m
+    as a linear attention (m = 32)."""
     w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, d=32, dv=dv)
     assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 1) == kg.KATA_PATH_TC
     q, k, v = workloads.make_qkv(w)
@@ -403,3 +407,47 @@ def test_sigma1_d32_padded(kg, B, H, T, dv, eps, scale):
     assert kg.kata_sync_status() == kg.KATA_OK
     ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 1, eps, scale)
     assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+@pytest.mark.parametrize("B,H,T", [
+    (1, 2, 1100),    # 8 CTAs: each head's chunks in order, ragged tail
+    (4, 10, 700),    # 160 CTAs, ragged tail
+    (2, 3, 129),     # last chunk holds one token
+    (3, 1, 5),       # a single partial chunk
+])
+@pytest.mark.parametrize("eps,scale", [
+    (1e-4, 1.0),     # the Sigma configuration
+    (0.5, 0.25),     # eps terms of the size of the s^2 (q . k)^2 term
+    (3.0, 1.0),      # eps terms dominant
+])
+def test_sigma1_d64_tensor_path(kg, B, H, T, eps, scale):
+    """KATA-Sigma_1 at d = 64 (eps I + s u u^T, 2080 features): s^2 times the full
+    map on the d = 64 tensor path (four feature groups' fp32 numerators and one
+    denominator), plus the eps terms as a linear attention (m = 64)."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, 2, 1) == kg.KATA_PATH_TC
+    q, k, v = workloads.make_qkv(w)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 2, 1, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 1, eps, scale)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+def test_sigma1_d64_eps_only_rows(kg):
+    """Zero queries: <psi(0), psi(k)> = eps^2 m + eps s |k|^2, so those rows come
+    from the eps terms alone; with eps = 0 the map is s^2 (q . k)^2 and the scale
+    cancels, leaving the plain forward."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=2, T=300)
+    q, k, v = workloads.make_qkv(w)
+    q[:, :, ::3] = 0
+    for eps, scale in ((1e-4, 1.0), (0.5, 0.25)):
+        out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, 2, 1, eps, scale)
+        torch.cuda.synchronize()
+        ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), "Sigma", 1, eps, scale)
+        assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype], (eps, scale)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    a = kg.kata_fwd_chunked_map(q, k, v, w.C, 2, 1, 0.0, 0.5)
+    b = kg.kata_fwd_chunked(q, k, v, w.C)
+    torch.cuda.synchronize()
+    assert slice_rel_err(to_f64(a), to_f64(b)) <= 1e-2
