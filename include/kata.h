@@ -211,9 +211,12 @@ int kata_fwd_chunked_map(const void *q, const void *k, const void *v, void *out,
  *   order of kata_lift_map (each matrix row-major over its upper triangle,
  *   sqrt(2) off the diagonal, M_g's matrices block by block).
  * state and z 16-byte aligned, not overlapping each other or the other buffers
- * (KATA_ERR_ARG).  The sub-head routes (M_2, Sigma_2 and M_4 at d = 64, M_2 at
- * d = 32) and the Sigma_1 routes keep no state of the map, so with the state
- * exported those maps take the CUDA cores;
+ * (KATA_ERR_ARG).  The routes built from full-map heads (M_2, Sigma_2, M_4 and
+ * Sigma_1 at d = 64; M_2 and Sigma_1 at d = 32) compose the map's state from
+ * their heads' full-map states: M_g's blocks are its sub-heads' (the first
+ * m = d / g coordinates of a zero-padded one), and Sigma_g's is
+ * scale (S_1 + ... + S_g) + eps sum_t v_t on the diagonal features (z the same
+ * with T), S_a the full-map state of key block a;
  * the explicit-feature path exports its scanned records (products of the bf16
  * hi feature parts with v, accumulated in fp32).  Other arguments and errors as
  * kata_fwd_chunked_map.

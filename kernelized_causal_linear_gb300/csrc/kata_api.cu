@@ -130,26 +130,28 @@ Kernels select_kernels(const FwdShape &s, const DevInfo &di) {
 // features (KATA-Sigma_4 at d = 64; Sigma_2, Sigma_4 and M_4 at d = 32; every
 // map at d = 16; the orthant map) take the explicit-feature tensor path (bf16,
 // dv = 64); the rest runs on CUDA cores.
-Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map,
-                           bool with_state) {
+// Every route exports the map's state.  The sub-head routes launch nsub
+// sub-heads per head along grid.y, so they need B H nsub <= 65535.
+Kernels select_map_kernels(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map) {
     if (map.kind == KATA_MAP_FULL) return select_kernels(s, di);
-    if (s.d == 64 && !with_state && map.kind == KATA_MAP_SUM && map.g == 1 &&
+    const int64_t bh = s.BH();
+    if (s.d == 64 && map.kind == KATA_MAP_SUM && map.g == 1 &&
         kata::tc64_supported(s, di.major, di.minor, di.sms))
         return kTc64Sigma1;   // 2080 features
-    if (s.d == 64 && !with_state) {
+    if (s.d == 64) {
         FwdShape half = s;
         half.d = 32;
         if (kata::tc_supported(half, di.major, di.minor)) {
-            if (map.kind == KATA_MAP_BLOCK && map.g == 2) return kTc32Sub;
-            if (map.kind == KATA_MAP_SUM && map.g == 2) return kTc32Sigma;
-            if (map.kind == KATA_MAP_BLOCK && map.g == 4) return kTc32M4;
+            if (map.kind == KATA_MAP_BLOCK && map.g == 2 && bh * 2 <= 65535) return kTc32Sub;
+            if (map.kind == KATA_MAP_SUM && map.g == 2 && bh * 4 <= 65535) return kTc32Sigma;
+            if (map.kind == KATA_MAP_BLOCK && map.g == 4 && bh * 4 <= 65535) return kTc32M4;
         }
     }
     if (kata::feat_supported(s, map, di.major, di.minor)) return kFeat;
-    if (s.d == 32 && !with_state && map.kind == KATA_MAP_BLOCK && map.g == 2 &&
+    if (s.d == 32 && map.kind == KATA_MAP_BLOCK && map.g == 2 && bh * 2 <= 65535 &&
         kata::tc_supported(s, di.major, di.minor))
         return kTc32SubPad;   // 272 features: above the explicit-feature path's limit
-    if (s.d == 32 && !with_state && map.kind == KATA_MAP_SUM && map.g == 1 &&
+    if (s.d == 32 && map.kind == KATA_MAP_SUM && map.g == 1 &&
         kata::tc_supported(s, di.major, di.minor))
         return kTc32Sigma1;   // 528 features
     return kSimt;
@@ -273,7 +275,7 @@ FwdShape padded64(const FwdShape &s) {
 }
 
 cudaError_t pad_run(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                    void *ws, const DevInfo &di, cudaStream_t st) {
+                    void *ws, const DevInfo &di, cudaStream_t st, const kata::StateOut &so) {
     const int64_t rows = (int64_t)s.BH() * s.T;
     const size_t np = round_up256((size_t)rows * 64 * 2);
     uint8_t *b = static_cast<uint8_t *>(ws);
@@ -286,37 +288,85 @@ cudaError_t pad_run(const FwdShape &s, const void *q, const void *k, const void 
             (e = kata::part_copy_cols(src, 32, 16, 16, dst, 64, 32, rows, false, st)) != cudaSuccess)
             return e;
     }
-    return kata::tc_forward(padded64(s), qp, kp, v, out, b + 2 * np, di.sms, st, kata::StateOut{}, 2);
+    return kata::tc_forward(padded64(s), qp, kp, v, out, b + 2 * np, di.sms, st, so, 2);
+}
+
+// The routes whose map state is composed from full-map states (kata_map_state.cu):
+// nsrc of dimension dsrc per head.  M_2 at d = 64 needs no composition: its two
+// sub-heads' states are its two blocks, in its own order.
+bool composed_state(Kernels kn, int &nsrc, int &dsrc) {
+    switch (kn) {
+        case kTc32SubPad: nsrc = 2; dsrc = 32; return true;    // M_2 at d = 32, blocks [u_a 0]
+        case kTc32M4: nsrc = 4; dsrc = 32; return true;        // M_4 at d = 64, blocks [u_a 0]
+        case kTc32Sigma: nsrc = 2; dsrc = 32; return true;     // Sigma_2 at d = 64: the key halves
+        case kTc32Sigma1: nsrc = 1; dsrc = 32; return true;
+        case kTc64Sigma1: nsrc = 1; dsrc = 64; return true;
+        default: return false;
+    }
+}
+
+// Scratch of a composed state, ahead of the route's: the sources' states and z,
+// then the eps totals.
+struct ComposeWs {
+    size_t state, z, tot;
+    size_t total() const { return state + z + tot; }
+};
+ComposeWs compose_ws(const FwdShape &s, int nsrc, int dsrc) {
+    const size_t heads = (size_t)s.BH() * nsrc, ns = (size_t)dsrc * (dsrc + 1) / 2;
+    return ComposeWs{round_up256(heads * ns * 64 * 4), round_up256(heads * ns * 4),
+                     round_up256((size_t)s.BH() * kata::kSigmaRec * 4)};
 }
 
 // Workspace and launch of one kernel family for a (map, shape).
 size_t route_ws(const FwdShape &s, Kernels kn, const DevInfo &di, const kata::MapSpec &map,
                 bool with_state) {
+    int nsrc = 0, dsrc = 0;
+    const size_t pre = with_state && composed_state(kn, nsrc, dsrc) ? compose_ws(s, nsrc, dsrc).total() : 0;
     if (kn == kTc32SubPad)
-        return 2 * round_up256((size_t)s.BH() * s.T * 64 * 2) +
-               kata::tc_workspace_bytes(padded64(s), di.sms, false, 2);
-    return kn == kTc32Sub      ? kata::tc_workspace_bytes(s, di.sms, false, 2)
-           : kn == kTc32Sigma  ? kata::tc_workspace_bytes(s, di.sms, false, 4, &map)
-           : kn == kTc32Sigma1 ? kata::tc_workspace_bytes(s, di.sms, false, 1, &map)
-           : kn == kTc64Sigma1 ? kata::tc64_workspace_bytes(s, false, &map)
-           : kn == kTc32M4    ? kata::tc_m4_workspace_bytes(s, di.sms)
-           : kn == kFeat      ? kata::feat_workspace_bytes(s, map)
-           : map.kind == 0    ? workspace_for(s, kn, di, with_state)
-                              : kata::simt_workspace_bytes(s, map);
+        return pre + 2 * round_up256((size_t)s.BH() * s.T * 64 * 2) +
+               kata::tc_workspace_bytes(padded64(s), di.sms, with_state, 2);
+    return pre + (kn == kTc32Sub      ? kata::tc_workspace_bytes(s, di.sms, with_state, 2)
+                  : kn == kTc32Sigma  ? kata::tc_workspace_bytes(s, di.sms, with_state, 4, &map)
+                  : kn == kTc32Sigma1 ? kata::tc_workspace_bytes(s, di.sms, with_state, 1, &map)
+                  : kn == kTc64Sigma1 ? kata::tc64_workspace_bytes(s, with_state, &map)
+                  : kn == kTc32M4     ? kata::tc_m4_workspace_bytes(s, di.sms, with_state)
+                  : kn == kFeat       ? kata::feat_workspace_bytes(s, map)
+                  : map.kind == 0     ? workspace_for(s, kn, di, with_state)
+                                      : kata::simt_workspace_bytes(s, map));
 }
 
-cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
-                      void *out, void *ws, const DevInfo &di, cudaStream_t st,
-                      const kata::StateOut &so, const kata::MapSpec &map) {
-    if (kn == kTc32SubPad) return pad_run(s, q, k, v, out, ws, di, st);
+cudaError_t route_launch(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
+                         void *out, void *ws, const DevInfo &di, cudaStream_t st,
+                         const kata::StateOut &so, const kata::MapSpec &map) {
+    if (kn == kTc32SubPad) return pad_run(s, q, k, v, out, ws, di, st, so);
     return kn == kTc32Sub      ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 2)
            : kn == kTc32Sigma  ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 4, &map)
            : kn == kTc32Sigma1 ? kata::tc_forward(s, q, k, v, out, ws, di.sms, st, so, 1, &map)
            : kn == kTc64Sigma1 ? kata::tc64_forward(s, q, k, v, out, ws, st, so, &map)
-           : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st)
+           : kn == kTc32M4    ? kata::tc_forward_m4(s, q, k, v, out, ws, di.sms, st, so)
            : kn == kFeat      ? kata::feat_forward(s, q, k, v, out, ws, st, map, so)
            : map.kind == 0    ? kata::fwd_launch(s, to_fwd(kn), q, k, v, out, ws, di.sms, st, so)
                               : kata::simt_forward(s, q, k, v, out, ws, st, so, map);
+}
+
+// The route, and with a state asked for on a composed route, its sources'
+// states into scratch followed by the map's state from them.
+cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *k, const void *v,
+                      void *out, void *ws, const DevInfo &di, cudaStream_t st,
+                      const kata::StateOut &so, const kata::MapSpec &map) {
+    int nsrc = 0, dsrc = 0;
+    if (so.state == nullptr || !composed_state(kn, nsrc, dsrc))
+        return route_launch(s, kn, q, k, v, out, ws, di, st, so, map);
+    const ComposeWs c = compose_ws(s, nsrc, dsrc);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    kata::StateOut src;
+    src.state = reinterpret_cast<float *>(b);
+    src.z = reinterpret_cast<float *>(b + c.state);
+    if (map.kind == KATA_MAP_SUM) src.eps_totals = reinterpret_cast<float *>(b + c.state + c.z);
+    cudaError_t e = route_launch(s, kn, q, k, v, out, b + c.total(), di, st, src, map);
+    if (e != cudaSuccess) return e;
+    return kata::map_state_compose(src.state, src.z, nsrc, dsrc, map, s.d, src.eps_totals, s.T,
+                                   so.state, so.z, s.BH(), st);
 }
 
 // A reduced map with bf16 inputs and dv in {16, 32, 128} whose route at dv = 64
@@ -324,12 +374,11 @@ cudaError_t route_run(const FwdShape &s, Kernels kn, const void *q, const void *
 // zero-padded): each output column depends on its own v column and every part
 // shares the weights, so the parts are independent forwards whose outputs are
 // the result's columns and whose states are its column blocks.
-bool map_parts(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map, bool with_state,
-               Kernels &core) {
+bool map_parts(const FwdShape &s, const DevInfo &di, const kata::MapSpec &map, Kernels &core) {
     if (map.kind == KATA_MAP_FULL || s.dtype != KATA_BF16 || s.dv == 64) return false;
     FwdShape c = s;
     c.dv = 64;
-    core = select_map_kernels(c, di, map, with_state);
+    core = select_map_kernels(c, di, map);
     return core != kSimt;
 }
 
@@ -398,9 +447,9 @@ int fwd_chunked_impl(const void *q, const void *k, const void *v, void *out, int
 
     const FwdShape s{B, H, T, d, dv, C, dtype};
     const bool with_state = so.state != nullptr;
-    const Kernels kn = select_map_kernels(s, di, map, with_state);
+    const Kernels kn = select_map_kernels(s, di, map);
     Kernels core = kSimt;
-    const bool parts = kn == kSimt && map_parts(s, di, map, with_state, core);
+    const bool parts = kn == kSimt && map_parts(s, di, map, core);
     const size_t wsb = parts ? parts_ws(s, core, di, map, with_state)
                              : route_ws(s, kn, di, map, with_state);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -446,7 +495,7 @@ int kata_fwd_path_map(int B, int H, int T, int d, int dv, int C, int dtype, int 
     const kata::MapSpec ms = map_spec(map, g, 0.f, 1.f);
     const FwdShape s{B, H, T, d, dv, C, dtype};
     Kernels core;
-    return select_map_kernels(s, di, ms, false) == kSimt && !map_parts(s, di, ms, false, core)
+    return select_map_kernels(s, di, ms) == kSimt && !map_parts(s, di, ms, core)
                ? KATA_PATH_SIMT
                : KATA_PATH_TC;
 }

@@ -81,7 +81,11 @@ struct MapSpec {
 struct StateOut {
     float *state = nullptr;
     float *z = nullptr;
+    // A Sigma map's eps terms (tensor routes): the inclusive totals of their chunk
+    // sums per head, [BH][kSigmaRec] = [sum v (64) | sum |k|^2 v (64) | sum |k|^2 | 3 unused].
+    float *eps_totals = nullptr;
 };
+constexpr int kSigmaRec = 2 * 64 + 4;
 
 // ---- CUDA-core (SIMT) path: kata_simt.cu ----------------------------------
 size_t simt_workspace_bytes(const FwdShape &s, const MapSpec &map = MapSpec{});
@@ -114,10 +118,12 @@ cudaError_t gated_forward(const FwdShape &s, const void *q, const void *k, const
 bool tc_supported(const FwdShape &s, int cc_major, int cc_minor);
 // nsub > 1: the head's q/k columns are nsub sub-heads of width d / nsub, each run
 // as a d / nsub head (KATA-M_2 at d = 64); their numerators and denominators are
-// summed.  No state export then.  sigma: KATA-Sigma_2 at d = 64 (nsub = 4, the
-// four sub-heads pair query half a with key half b) or KATA-Sigma_1 at d = 32
-// (nsub = 1, the full map); the map's eps terms are added in the finalize pass
-// (kata_sigma.cu), and there is no state export either.
+// summed.  sigma: KATA-Sigma_2 at d = 64 (nsub = 4, the four sub-heads pair
+// query half a with key half b) or KATA-Sigma_1 at d = 32 (nsub = 1, the full
+// map); the map's eps terms are added in the finalize pass (kata_sigma.cu).
+// With sub-heads or eps terms, so receives the full-map (d = 32) state of every
+// key sub-head: [BH * nsub] of them (two per head when crosswise) in the decode
+// layout, and so.eps_totals the eps sums; map_state_compose forms the map's.
 size_t tc_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false, int nsub = 1,
                           const MapSpec *sigma = nullptr);
 cudaError_t tc_forward(const FwdShape &s, const void *q, const void *k, const void *v,
@@ -145,9 +151,11 @@ cudaError_t gated_wide_forward(const FwdShape &s, const void *q, const void *k, 
                                const StateOut &so, int normalize);
 // KATA-M_4 at d = 64: q and k rows padded to four 32-wide blocks [u_a | 0], run
 // as four d = 32 sub-heads (nsub = 4) whose numerators and denominators add.
-size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms);
+// so: the four padded sub-heads' d = 32 states, as tc_forward with nsub = 4.
+size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms, bool with_state = false);
 cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                          void *workspace, int num_sms, cudaStream_t stream);
+                          void *workspace, int num_sms, cudaStream_t stream,
+                          const StateOut &so = StateOut{});
 // KATA-Sigma_g finalize (kata_sigma.cu): the scratch it needs after the
 // partials, and the pass that sums them with the eps terms.  The partials'
 // layouts: Sub4, the four crosswise d = 32 sub-heads of Sigma_2 at d = 64
@@ -156,9 +164,25 @@ cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const
 // d = 64 path (N [4][BH][T][64] of its feature groups, then D [BH][T]).
 enum class SigmaParts { Sub4, Sub1, Wide };
 size_t sigma_workspace_bytes(const FwdShape &s);
+// eps_totals: if set, receives the inclusive totals of the eps chunk sums.
 cudaError_t sigma_finalize_launch(const FwdShape &s, SigmaParts parts, const float *part,
                                   float *ws, const void *q, const void *k, const void *v, void *out,
-                                  const MapSpec &map, cudaStream_t stream);
+                                  const MapSpec &map, cudaStream_t stream,
+                                  float *eps_totals = nullptr);
+// The state of a reduced map from the full-map states its tensor route leaves
+// (kata_map_state.cu): src [BH * nsrc][n(dsrc)][64] and z [BH * nsrc][n(dsrc)]
+// in the decode layout, to the map's state [BH][n][64] and z [BH][n] in the
+// packed order of its lift.
+//   KATA-M_g: source a (of nsrc = g) is block a's full map, in the first
+//     m = d / g coordinates of its dsrc (the rest zero padding); the map's block
+//     a takes the features of those m coordinates.
+//   KATA-Sigma_g: the sources are the full maps of the key blocks (nsrc = g,
+//     dsrc = m); psi = eps I + s sum_a u_a u_a^T gives
+//     S = s sum_a S_a + eps [f diagonal] sum_t v_t and z = s sum_a z_a + eps [f diagonal] T,
+//     sum_t v_t from eps_totals.
+cudaError_t map_state_compose(const float *src_state, const float *src_z, int nsrc, int dsrc,
+                              const MapSpec &map, int d, const float *eps_totals, int T,
+                              float *state, float *z, int BH, cudaStream_t stream);
 // Reads and clears the sticky device error word of the tensor-core kernels
 // (nonzero: a bounded wait expired); -1 if it could not be read.
 int tc_take_error();
@@ -172,7 +196,8 @@ int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens);
 bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms);
 // sigma (KATA-Sigma_1 at d = 64, eps I + s u u^T): the full map's numerators and
 // denominator stay in fp32 and the finalize pass of kata_sigma.cu adds the
-// map's eps terms.  No state export then.
+// map's eps terms; so then receives the full map's state and so.eps_totals the
+// eps sums, for map_state_compose.
 size_t tc64_workspace_bytes(const FwdShape &s, bool with_state = false,
                             const MapSpec *sigma = nullptr);
 cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const void *v,

@@ -34,6 +34,7 @@ using bf16 = __nv_bfloat16;
 constexpr int kChunk = 128;
 constexpr int kDv = 64;                  // value columns
 constexpr int kRec = 2 * kDv + 4;        // [sum v | sum |k|^2 v | sum |k|^2 | 3 unused]
+static_assert(kRec == kSigmaRec, "the record layout StateOut::eps_totals documents");
 constexpr int kThreads = 64;             // one thread per value column
 
 // |x|^2 of one D-wide bf16 row, summed in fp32 in a fixed order.
@@ -152,7 +153,7 @@ size_t sigma_workspace_bytes(const FwdShape &s) {
 
 cudaError_t sigma_finalize_launch(const FwdShape &s, SigmaParts parts, const float *part,
                                   float *ws, const void *q, const void *k, const void *v, void *out,
-                                  const MapSpec &map, cudaStream_t stream) {
+                                  const MapSpec &map, cudaStream_t stream, float *eps_totals) {
     if (s.dv != kDv || s.dtype != 1 || map.kind != 2) return cudaErrorInvalidValue;
     const bool sub4 = parts == SigmaParts::Sub4 && s.d == 64 && map.g == 2;
     const bool sub1 = parts == SigmaParts::Sub1 && s.d == 32 && map.g == 1;
@@ -169,7 +170,8 @@ cudaError_t sigma_finalize_launch(const FwdShape &s, SigmaParts parts, const flo
             sigma_chunk_sums_kernel<32><<<grid, kThreads, 0, stream>>>((const bf16 *)k, (const bf16 *)v,
                                                                        ws, s.T, NC);
     }
-    cudaError_t e = scan_exclusive_launch(ws, s.BH(), NC, kRec, "tc_sigma_scan", stream);
+    cudaError_t e = scan_exclusive_launch(ws, s.BH(), NC, kRec, "tc_sigma_scan", stream, StateOut{}, 0,
+                                          eps_totals);
     if (e != cudaSuccess) return e;
     const float eps = map.eps, sc = map.scale;
     const float s2 = sc * sc, es = eps * sc, e2m = eps * eps * (float)(s.d / map.g);

@@ -828,19 +828,20 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // upper-triangle feature f of (i, j), sqrt(2) on the off-diagonal entries.
 // The grouped layout carries a factor 2 on the key side off the diagonal, so
 // those rows are scaled by 1/sqrt(2); z_f is G_ij (sqrt(2) G_ij for i < j).
-// Grid: one CTA per head, 128 threads.
+// Grid (NBLK + 1, heads), 128 threads: CTA b < NBLK moves feature block b (one
+// thread per feature slot), CTA NBLK the Gram into z.
 template <int D, int DV>
 __global__ void __launch_bounds__(128)
 state_export_kernel(const float *__restrict__ total, float *__restrict__ state,
                     float *__restrict__ z) {
     using C = Cfg<D, DV>;
     constexpr int kN = D * (D + 1) / 2;
-    const int bh = blockIdx.x, p = threadIdx.x;
+    const int b = blockIdx.x, bh = blockIdx.y, p = threadIdx.x;
     const float *rec = total + (size_t)bh * C::E;
     float *st = state + (size_t)bh * kN * DV;
-    for (int b = 0; b < C::NBLK; ++b) {
+    if (b < C::NBLK) {
         int i = 0, j = 0;
-        if (!grouped_slot_pair(b, p, i, j)) continue;
+        if (!grouped_slot_pair(b, p, i, j)) return;
         const int f = i * D - i * (i - 1) / 2 + (j - i);
         const float sc = i == j ? 1.f : 0.70710678118654752f;
         const float4 *src = reinterpret_cast<const float4 *>(rec + (size_t)(b * 128 + p) * DV);
@@ -850,6 +851,7 @@ state_export_kernel(const float *__restrict__ total, float *__restrict__ state,
             const float4 x = src[e];
             dst[e] = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
         }
+        return;
     }
     const float *gram = rec + (size_t)C::NBLK * 128 * DV;
     for (int e = p; e < D * D; e += blockDim.x) {
@@ -1058,8 +1060,6 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
                        void *out, void *workspace, int num_sms, cudaStream_t stream,
                        const StateOut &so, int nsub, const MapSpec *sigma) {
     using C = Cfg<32, 64>;
-    // no state export from sub-heads or with eps terms
-    if ((nsub > 1 || sigma) && so.state != nullptr) return cudaErrorInvalidValue;
     if (!sigma_shape_ok(s0, nsub, sigma)) return cudaErrorInvalidValue;
     const bool cross = sigma != nullptr && nsub == 4, partials = nsub > 1 || sigma;
     const FwdShape s = sub_shape(s0, nsub, cross);
@@ -1084,13 +1084,20 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
             seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, state_heads), 352, kSmemState, stream>>>(
                 mk, mv, seg, p.NCt, p.Lc, p.m, p.NR, state_nsub, g_stall_next.exchange(0));
         }
-        float *totals = with_state ? seg + (size_t)s.BH() * p.NR * C::E : nullptr;
-        cudaError_t e = scan_exclusive_launch(seg, state_heads, p.NR, C::E, "tc_segment_scan", stream,
-                                              StateOut{}, 0, totals);
-        if (e != cudaSuccess) return e;
-        if (with_state) {
+        float *totals = with_state ? seg + (size_t)state_heads * p.NR * C::E : nullptr;
+        if (with_state && p.NR == 1) {
+            // one segment in one piece: its record is the total, and the
+            // output kernel reads no prefix for a head's first segment
+            totals = seg;
+        } else {
+            cudaError_t e = scan_exclusive_launch(seg, state_heads, p.NR, C::E, "tc_segment_scan",
+                                                  stream, StateOut{}, 0, totals);
+            if (e != cudaSuccess) return e;
+        }
+        if (with_state) {   // the full-map state of every key sub-head
             TraceScope tr("tc_state_export", stream);
-            state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
+            state_export_kernel<32, 64><<<dim3(C::NBLK + 1, state_heads), 128, 0, stream>>>(
+                totals, so.state, so.z);
         }
     }
     if (pair) {
@@ -1115,11 +1122,12 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
                 OutGate{nullptr, nullptr, 1});
         }
     }
-    if (sigma) {
-        const size_t off = sub_part_floats(s, partials) + (size_t)state_heads * p.NR * C::E;
+    if (sigma) {   // its scratch follows the records (and the totals)
+        const size_t off = sub_part_floats(s, partials) +
+                           (size_t)state_heads * (p.NR + (with_state ? 1 : 0)) * C::E;
         return sigma_finalize_launch(s0, cross ? SigmaParts::Sub4 : SigmaParts::Sub1, part,
                                      static_cast<float *>(workspace) + off, q, k, v, out, *sigma,
-                                     stream);
+                                     stream, so.eps_totals);
     }
     if (part != nullptr) {
         TraceScope tr("tc_sub_finalize", stream);
@@ -1196,7 +1204,8 @@ cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, co
         }
         if (with_state) {
             TraceScope tr("tc_state_export", stream);
-            state_export_kernel<32, 64><<<s.BH(), 128, 0, stream>>>(totals, so.state, so.z);
+            state_export_kernel<32, 64><<<dim3(C::NBLK + 1, s.BH()), 128, 0, stream>>>(
+                totals, so.state, so.z);
         }
     }
     {
@@ -1234,13 +1243,13 @@ FwdShape padded_m4(const FwdShape &s) {
 }
 }  // namespace
 
-size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms) {
+size_t tc_m4_workspace_bytes(const FwdShape &s, int num_sms, bool with_state) {
     const size_t np = (size_t)s.BH() * s.T * 128 * sizeof(bf16);
-    return 2 * np + tc_workspace_bytes(padded_m4(s), num_sms, false, 4);
+    return 2 * np + tc_workspace_bytes(padded_m4(s), num_sms, with_state, 4);
 }
 
 cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const void *v, void *out,
-                          void *workspace, int num_sms, cudaStream_t stream) {
+                          void *workspace, int num_sms, cudaStream_t stream, const StateOut &so) {
     if (s.d != 64) return cudaErrorInvalidValue;
     const int64_t rows = (int64_t)s.BH() * s.T;
     const size_t np = (size_t)rows * 128;
@@ -1251,7 +1260,7 @@ cudaError_t tc_forward_m4(const FwdShape &s, const void *q, const void *k, const
         pad_blocks16_kernel<<<blocks, 256, 0, stream>>>((const uint4 *)q, (uint4 *)qp, rows);
         pad_blocks16_kernel<<<blocks, 256, 0, stream>>>((const uint4 *)k, (uint4 *)kp, rows);
     }
-    return tc_forward(padded_m4(s), qp, kp, v, out, kp + np, num_sms, stream, StateOut{}, 4);
+    return tc_forward(padded_m4(s), qp, kp, v, out, kp + np, num_sms, stream, so, 4);
 }
 
 void tc_arm_stall() { g_stall_next.store(1); }

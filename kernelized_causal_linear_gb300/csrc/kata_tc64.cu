@@ -697,17 +697,19 @@ wide_finalize_kernel(const float *__restrict__ part, const float *__restrict__ d
 // state[f][c] and z[f] for the row-major upper-triangle feature f of (i, j),
 // sqrt(2) on the off-diagonal entries.  The grouped layout carries a factor 2 on
 // the key side off the diagonal, so those rows are scaled by 1/sqrt(2); z_f is
-// G_ij (sqrt(2) G_ij for i < j).  One CTA per head, 128 threads.
+// G_ij (sqrt(2) G_ij for i < j).  Grid (kBlocks64 + 1, BH), 128 threads: CTA
+// b < kBlocks64 moves feature block b (one thread per feature slot), the last
+// one the Gram into z.
 __global__ void __launch_bounds__(128)
 state_export64_kernel(const float *__restrict__ srec, float *__restrict__ state,
                       float *__restrict__ z) {
     constexpr int D = 64, DV = 64, kN = D * (D + 1) / 2;
-    const int bh = blockIdx.x, p = threadIdx.x;
+    const int b = blockIdx.x, bh = blockIdx.y, p = threadIdx.x;
     const float *rec = srec + (size_t)bh * kRec64;
     float *st = state + (size_t)bh * kN * DV;
-    for (int b = 0; b < kBlocks64; ++b) {
+    if (b < kBlocks64) {
         int i = 0, j = 0;
-        if (!grouped_slot_pair64(b, p, i, j)) continue;
+        if (!grouped_slot_pair64(b, p, i, j)) return;
         const int f = i * D - i * (i - 1) / 2 + (j - i);
         const float sc = i == j ? 1.f : 0.70710678118654752f;
         const float4 *src = reinterpret_cast<const float4 *>(rec + ((size_t)b * 128 + p) * DV);
@@ -717,6 +719,7 @@ state_export64_kernel(const float *__restrict__ srec, float *__restrict__ state,
             const float4 x = src[e];
             dst[e] = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
         }
+        return;
     }
     const float *gram = rec + (size_t)kBlocks64 * 128 * DV;
     for (int e = p; e < D * D; e += blockDim.x) {
@@ -758,12 +761,18 @@ bool tc64_supported(const FwdShape &s, int cc_major, int cc_minor, int num_sms) 
 
 // Workspace: partial numerators [4][rows][64] fp32, D [rows] fp32, then (state
 // export) the final-state records [BH][kRec64] fp32 from a 256-byte boundary
-// (their 32-byte stores need it).
+// (their 32-byte stores need it), then (eps terms) the finalize's scratch from
+// the next 256-byte boundary.
 size_t srec_offset_floats(size_t rows) { return (rows * 64 * 4 + rows + 63) & ~(size_t)63; }
+size_t sigma_offset_floats(const FwdShape &s, bool with_state) {
+    const size_t o = srec_offset_floats((size_t)s.BH() * s.T);
+    return with_state ? (o + (size_t)s.BH() * kRec64 + 63) & ~(size_t)63 : o;
+}
 
 size_t tc64_workspace_bytes(const FwdShape &s, bool with_state, const MapSpec *sigma) {
     const size_t rows = (size_t)s.BH() * s.T;
-    if (sigma != nullptr) return sizeof(float) * srec_offset_floats(rows) + sigma_workspace_bytes(s);
+    if (sigma != nullptr)
+        return sizeof(float) * sigma_offset_floats(s, with_state) + sigma_workspace_bytes(s);
     return sizeof(float) * (with_state ? srec_offset_floats(rows) + (size_t)s.BH() * kRec64
                                        : rows * 64 * 4 + rows);
 }
@@ -773,7 +782,6 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
                          const MapSpec *sigma) {
     const int NCt = (s.T + kTile - 1) / kTile;
     const size_t rows = (size_t)s.BH() * s.T;
-    if (sigma != nullptr && so.state != nullptr) return cudaErrorInvalidValue;
     if (rows == 0) return cudaSuccess;
     float *part = static_cast<float *>(workspace);
     float *dden = part + rows * 64 * 4;
@@ -789,10 +797,12 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
         wide_output_kernel<<<dim3(4, s.BH()), 608, kSmemWide, stream>>>(mq, mk, mv, mp, mp16, dden,
                                                                         srec, s.T, NCt);
     }
-    if (sigma != nullptr)   // the eps scratch after the partials, from a 256-byte boundary
-        return sigma_finalize_launch(s, SigmaParts::Wide, part, part + srec_offset_floats(rows), q, k,
-                                     v, out, *sigma, stream);
-    {
+    if (sigma != nullptr) {
+        cudaError_t e = sigma_finalize_launch(s, SigmaParts::Wide, part,
+                                              part + sigma_offset_floats(s, srec != nullptr), q, k, v,
+                                              out, *sigma, stream, so.eps_totals);
+        if (e != cudaSuccess) return e;
+    } else {
         TraceScope tr("tc64_finalize", stream);
         const int64_t n4 = (int64_t)rows * 16;
         const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 16);
@@ -801,7 +811,7 @@ cudaError_t tc64_forward(const FwdShape &s, const void *q, const void *k, const 
     }
     if (srec != nullptr) {
         TraceScope tr("tc64_state_export", stream);
-        state_export64_kernel<<<s.BH(), 128, 0, stream>>>(srec, so.state, so.z);
+        state_export64_kernel<<<dim3(kBlocks64 + 1, s.BH()), 128, 0, stream>>>(srec, so.state, so.z);
     }
     return cudaGetLastError();
 }

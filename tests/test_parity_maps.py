@@ -451,3 +451,29 @@ def test_sigma1_d64_eps_only_rows(kg):
     b = kg.kata_fwd_chunked(q, k, v, w.C)
     torch.cuda.synchronize()
     assert slice_rel_err(to_f64(a), to_f64(b)) <= 1e-2
+
+
+@pytest.mark.parametrize("map_,g,B,H,path", [
+    (1, 2, 1, 32767, "tc"),      # M_2: 65534 sub-heads along grid.y
+    (2, 2, 1, 16383, "tc"),      # Sigma_2: 65532 crosswise sub-heads
+    (2, 2, 1, 16384, "simt"),    # one head more would pass grid.y: the CUDA cores
+    (1, 4, 1, 16384, "simt"),
+    (2, 1, 3, 21845, "tc"),      # Sigma_1 on the d = 64 path: 65535 heads
+])
+def test_map_head_count_limits(kg, map_, g, B, H, path):
+    """The sub-head routes launch nsub sub-heads per head along grid.y (at most
+    65535); past that the map takes the CUDA cores.  T = 3, sampled heads
+    against the oracle."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=3)
+    want = kg.KATA_PATH_TC if path == "tc" else kg.KATA_PATH_SIMT
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == want
+    q, k, v = workloads.make_qkv(w)
+    eps, scale = (0.5, 0.25) if map_ == 2 else (0.0, 1.0)
+    out = kg.kata_fwd_chunked_map(q.cuda(), k.cuda(), v.cuda(), w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    for b, h in [(0, 0), (B - 1, H - 1), (0, H // 2)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.forward_map(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), NAMES[map_], g, eps,
+                                 scale)
+        assert slice_rel_err(to_f64(out[sl]), ref) <= TOL[w.dtype], (b, h)

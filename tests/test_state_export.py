@@ -180,7 +180,9 @@ def _map_params(map_, g):
     (2, 2, 32, torch.bfloat16),
     (3, 1, 64, torch.bfloat16),   # orthant
     (1, 4, 16, torch.bfloat16),
-    (1, 2, 64, torch.bfloat16),   # M_2 at d = 64: the sub-heads keep no map state -> CUDA cores
+    (1, 2, 64, torch.bfloat16),   # M_2 at d = 64: its sub-heads' states are its blocks
+    (2, 2, 64, torch.bfloat16),   # Sigma_2 at d = 64: composed from the key halves' states
+    (2, 1, 32, torch.bfloat16),   # Sigma_1 at d = 32: the full map's state plus the eps terms
     (2, 2, 16, torch.float32),    # fp32: CUDA cores
 ])
 @pytest.mark.parametrize("dv", [64, 128])
@@ -238,3 +240,48 @@ def test_map_decode_step_parity(kg, map_, g, d, dv, dtype):
                                           scale)
     assert slice_rel_err(to_f64(o)[:, :, None, :], oref[:, :, None, :]) <= TOL[dtype]
     assert _state_err(to_f64(S), S1) <= 1e-5 and _state_err(to_f64(z), z1) <= 1e-5
+
+
+# (map, g, d, eps, scale): the tensor routes built from full-map sub-heads, whose
+# map state is composed from the sub-heads' states; eps of the size of the
+# s^2 (q.k)^2 terms puts weight on the eps diagonal of the Sigma states
+_COMPOSED = [(1, 2, 64, 0.0, 1.0), (1, 4, 64, 0.0, 1.0), (2, 2, 64, 1e-4, 1.0),
+             (2, 2, 64, 0.5, 0.25), (2, 1, 64, 1e-4, 1.0), (2, 1, 64, 3.0, 1.0),
+             (1, 2, 32, 0.0, 1.0), (2, 1, 32, 1e-4, 1.0), (2, 1, 32, 0.5, 0.25)]
+
+
+@pytest.mark.parametrize("map_,g,d,eps,scale", _COMPOSED)
+@pytest.mark.parametrize("B,H,T,dv", [(2, 2, 300, 64), (1, 2, 1100, 64), (1, 3, 129, 128)])
+def test_map_state_composed_routes(kg, map_, g, d, eps, scale, B, H, T, dv):
+    """M_2, M_4, Sigma_2, Sigma_1 at d = 64 and M_2, Sigma_1 at d = 32 on the tensor
+    cores with the state exported: S and z against the oracle's map recurrence
+    (several segments at T = 1100; 64-column parts of v at dv = 128), the output
+    against the direct definition."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=B, H=H, T=T, d=d, dv=dv)
+    assert kg.kata_fwd_path_map(w.B, w.H, w.T, w.d, w.dv, w.C, w.dtype, map_, g) == \
+        kg.KATA_PATH_TC
+    name = _MAP_NAMES[map_]
+    q, k, v = workloads.make_qkv(w)
+    out, S, z = kg.kata_fwd_chunked_map_state(q.cuda(), k.cuda(), v.cuda(), w.C, map_, g, eps, scale)
+    torch.cuda.synchronize()
+    assert kg.kata_sync_status() == kg.KATA_OK
+    S_ref, z_ref = oracle.prefix_state_map(to_f64(k), to_f64(v), name, g, eps, scale)
+    es, ez = _state_err(to_f64(S), S_ref), _state_err(to_f64(z), z_ref)
+    tol = STATE_TOL[w.dtype]
+    assert es <= tol and ez <= tol, f"state {es:.2e}, z {ez:.2e} (bar {tol:.0e})"
+    ref = oracle.forward_map(to_f64(q), to_f64(k), to_f64(v), name, g, eps, scale)
+    assert slice_rel_err(to_f64(out), ref) <= TOL[w.dtype]
+
+
+def test_map_state_composed_eps_diagonal(kg):
+    """Zero keys: psi(0) = eps I for Sigma_g, so the state is eps sum_t v_t on the
+    diagonal features and zero elsewhere, and z is eps T there: the eps terms
+    alone, checked exactly up to fp32 rounding."""
+    w = workloads.WORKLOADS["lm_layer_bf16"].scaled(B=1, H=2, T=300)
+    q, k, v = workloads.make_qkv(w)
+    k.zero_()
+    for g in (1, 2):
+        out, S, z = kg.kata_fwd_chunked_map_state(q.cuda(), k.cuda(), v.cuda(), w.C, 2, g, 0.5, 0.25)
+        torch.cuda.synchronize()
+        S_ref, z_ref = oracle.prefix_state_map(to_f64(k), to_f64(v), "Sigma", g, 0.5, 0.25)
+        assert _state_err(to_f64(S), S_ref) <= 1e-5 and _state_err(to_f64(z), z_ref) <= 1e-6, g
