@@ -323,17 +323,23 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
 //   D_t = b_t q_t^T G_pre q_t      + sum_{s<=t} 2^(l_t - l_s) (q_t . k_s)^2,
 // b_t = 2^l_t.  The convert warps decay S_run block by block as they read it,
 // the P warps decay G as they read it; O = N / D, or N when !normalize.
+// kFin (not gated): fin receives the state after the head's last token.  S_run
+// starts from the segment's exclusive prefix, so after the last segment's last
+// chunk it is the head's whole state, and so is G; that CTA writes both in the
+// record layout to fin[sbh] (crosswise: the query-half-0 sub-heads, one per key
+// half).  A compile-time variant, so the kernel without it carries no export code.
 struct OutGate {
     const float *lam2;     // [BH][T] chunk-local cumulative log2 of the gates
     const float *gchunk;   // [BH][NC] gate product of each 128-token chunk
     int normalize;
 };
-template <int D, int DV, bool kSub, bool kGated>
+template <int D, int DV, bool kSub, bool kGated, bool kFin = false>
 __global__ void __launch_bounds__(608, 1)
 seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kg,
                   bf16 *__restrict__ out, const float *__restrict__ seg, int T, int NCt, int Lc,
-                  int m_pieces, int NR, int nsub, int cross, float *__restrict__ part, OutGate ga) {
+                  int m_pieces, int NR, int nsub, int cross, float *__restrict__ part, OutGate ga,
+                  float *__restrict__ fin) {
     using C = Cfg<D, DV>;
     static_assert(DV == 64 && D == 32 && C::NBLK == 5, "layouts below are written for d = 32, dv = 64");
     constexpr int NB = C::NBLK;
@@ -369,6 +375,10 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const bool xc = kSub && cross;
     const int qx = (xc ? j >> 1 : j) * D, kx = (xc ? j & 1 : j) * D;
     const int sbh = xc ? hz * 2 + (j & 1) : bh;   // records of this sub-head's keys
+    static_assert(!(kFin && kGated), "the gated path exports its state from the scan");
+    float *const frec = (kFin && g == (int)gridDim.x - 1 && (!xc || (j >> 1) == 0))
+                            ? fin + (size_t)sbh * C::E
+                            : nullptr;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = g * Lc;
     const int nch = min(NCt, c0 + Lc) - c0;
@@ -617,6 +627,23 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (elect_lane0()) mbar_arrive(&block_ready[ss]);
             }
         }
+        // the final state: each block once its last state MMA is done
+        for (int b = 0; kFin && b < NB && ok && frec != nullptr; ++b) {
+            ok = __all_sync(0xffffffffu, sy.wait(&state_done[b], nch - 1));
+            if (!ok) break;
+            tc_fence_after();
+            if (quarter * 32 >= C::NF - b * 128) continue;   // no real features in these rows
+            float4 *dst = reinterpret_cast<float4 *>(frec + (size_t)(b * 128 + row) * DV);
+#pragma unroll
+            for (int c32 = 0; c32 < DV; c32 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tS + lsel + b * DV + c32, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[c32 / 4 + e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            }
+        }
     } else if (warp < kWarpLift) {
         // ================= P warps: lane quarter q owns query rows 32q..32q+31
         const int quarter = warp & 3;
@@ -717,8 +744,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             return true;
         };
-        // gscale (gated): the factor G is left with in TMEM for the next Gram update
-        auto gram_to_smem = [&](bool from_tmem, const float *pre, float gscale) {
+        // gscale (gated): the factor G is left with in TMEM for the next Gram update;
+        // gout: also the fp32 rows of G there
+        auto gram_to_smem = [&](bool from_tmem, const float *pre, float gscale, float *gout) {
             // G rows i = lane (quarter 0 only): bf16 [D][D] K-major, 64-byte swizzle
             if (quarter != 0) return;
             float gv[D];
@@ -733,6 +761,12 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             } else {
 #pragma unroll
                 for (int e = 0; e < D; ++e) gv[e] = pre ? pre[lane * D + e] : 0.f;
+            }
+            if (kFin && gout != nullptr) {
+                float4 *go = reinterpret_cast<float4 *>(gout + lane * D);
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e)
+                    go[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
             }
 #pragma unroll
             for (int chunk = 0; chunk < D / 8; ++chunk) {
@@ -774,7 +808,9 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             if constexpr (kGated) di *= exp2f(lam2[min(i * kTile + row, nvalid - 1)]);   // b_t
             dsum += di;
-            gram_to_smem(true, nullptr, (kGated && i + 1 < nch) ? gch[i + 1] : 1.f);
+            // after the last chunk, G is the head's whole Gram
+            gram_to_smem(true, nullptr, (kGated && i + 1 < nch) ? gch[i + 1] : 1.f,
+                         kFin && frec != nullptr && i == nch - 1 ? frec + (size_t)NB * 128 * DV : nullptr);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -787,7 +823,7 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
         {   // initial Gram: the segment's exclusive prefix (zero for g == 0)
             const float *pre = g > 0 ? seg + ((size_t)sbh * NR + (size_t)g * m_pieces) * C::E : nullptr;
-            gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr, kGated ? gch[0] : 1.f);
+            gram_to_smem(false, pre ? pre + (size_t)NB * 128 * DV : nullptr, kGated ? gch[0] : 1.f, nullptr);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1029,9 +1065,10 @@ Plan plan(const FwdShape &s, int num_sms, bool with_state, int span) {
 
 // The CTA-pair output kernel (kata_tc_pair.cu) splits the feature blocks of a
 // segment over two SMs.  It is exact, but slower than the one-CTA kernel on
-// every measured shape, so it runs only when KATA_TC_OUTPUT=pair is set.
-bool use_pair(int nsub, const MapSpec *sigma) {
-    if (nsub != 1 || sigma != nullptr) return false;
+// every measured shape, so it runs only when KATA_TC_OUTPUT=pair is set (and
+// without a state export, which the one-CTA kernel writes).
+bool use_pair(int nsub, const MapSpec *sigma, bool with_state) {
+    if (nsub != 1 || sigma != nullptr || with_state) return false;
     const char *e = getenv("KATA_TC_OUTPUT");
     return e != nullptr && strcmp(e, "pair") == 0;
 }
@@ -1042,8 +1079,8 @@ size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int 
     const bool cross = sigma != nullptr && nsub == 4;
     const FwdShape s = sub_shape(s0, nsub, cross);
     // piece records (of the key sub-heads: 2 per head when crosswise), plus the
-    // inclusive totals when the state is exported
-    const Plan p = plan(s, num_sms, with_state, use_pair(nsub, sigma) ? 2 : 1);
+    // final states when the state is exported
+    const Plan p = plan(s, num_sms, false, use_pair(nsub, sigma, with_state) ? 2 : 1);
     const size_t recs = (size_t)p.NR + (with_state ? 1 : 0);
     const size_t heads = cross ? (size_t)s0.BH() * 2 : (size_t)s.BH();
     return sizeof(float) * (sub_part_floats(s, nsub > 1 || sigma) + heads * recs * Cfg<32, 64>::E) +
@@ -1051,7 +1088,7 @@ size_t tc_workspace_bytes(const FwdShape &s0, int num_sms, bool with_state, int 
 }
 
 int tc_segments(const FwdShape &s, int num_sms, int *seg_tokens) {
-    const Plan p = plan(s, num_sms, false, use_pair(1, nullptr) ? 2 : 1);
+    const Plan p = plan(s, num_sms, false, use_pair(1, nullptr, false) ? 2 : 1);
     if (seg_tokens) *seg_tokens = p.Lc * kTile;
     return p.G;
 }
@@ -1063,8 +1100,10 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     if (!sigma_shape_ok(s0, nsub, sigma)) return cudaErrorInvalidValue;
     const bool cross = sigma != nullptr && nsub == 4, partials = nsub > 1 || sigma;
     const FwdShape s = sub_shape(s0, nsub, cross);
-    const bool with_state = so.state != nullptr, pair = use_pair(nsub, sigma);
-    const Plan p = plan(s, num_sms, with_state, pair ? 2 : 1);
+    const bool with_state = so.state != nullptr, pair = use_pair(nsub, sigma, with_state);
+    // the state after the last token comes from the output kernel's last segment,
+    // so the segmentation is the one without it
+    const Plan p = plan(s, num_sms, false, pair ? 2 : 1);
     CUtensorMap mq, mk, mv;
     // q, k: rows of s0.d columns, read s.d at a time; v: one head's rows, shared by its sub-heads
     if (!make_map(mq, q, s0.d, s.T, s0.BH(), s.d) || !make_map(mk, k, s0.d, s.T, s0.BH(), s.d) ||
@@ -1075,7 +1114,8 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     // crosswise, the segment sums depend on the key half only: 2 per head
     const int state_heads = cross ? s0.BH() * 2 : s.BH(), state_nsub = cross ? 2 : nsub;
     // Segment sums: of every segment but the last (the output kernel carries the
-    // last one on chip), and of the last one too when the final state is wanted.
+    // last one on chip).  fin: the final states, [state_heads][E] after the records.
+    float *fin = with_state ? seg + (size_t)state_heads * p.NR * C::E : nullptr;
     if (p.nsum > 0) {
         cudaFuncSetAttribute(seg_state_kernel<32, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemState);
@@ -1084,21 +1124,8 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
             seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, state_heads), 352, kSmemState, stream>>>(
                 mk, mv, seg, p.NCt, p.Lc, p.m, p.NR, state_nsub, g_stall_next.exchange(0));
         }
-        float *totals = with_state ? seg + (size_t)state_heads * p.NR * C::E : nullptr;
-        if (with_state && p.NR == 1) {
-            // one segment in one piece: its record is the total, and the
-            // output kernel reads no prefix for a head's first segment
-            totals = seg;
-        } else {
-            cudaError_t e = scan_exclusive_launch(seg, state_heads, p.NR, C::E, "tc_segment_scan",
-                                                  stream, StateOut{}, 0, totals);
-            if (e != cudaSuccess) return e;
-        }
-        if (with_state) {   // the full-map state of every key sub-head
-            TraceScope tr("tc_state_export", stream);
-            state_export_kernel<32, 64><<<dim3(C::NBLK + 1, state_heads), 128, 0, stream>>>(
-                totals, so.state, so.z);
-        }
+        cudaError_t e = scan_exclusive_launch(seg, state_heads, p.NR, C::E, "tc_segment_scan", stream);
+        if (e != cudaSuccess) return e;
     }
     if (pair) {
         cudaError_t e = pair_output_launch(mq, mk, mv, out, seg, s.BH(), s.T, p.NCt, p.Lc, p.G, p.m,
@@ -1108,21 +1135,40 @@ cudaError_t tc_forward(const FwdShape &s0, const void *q, const void *k, const v
     }
     {
         TraceScope tr("tc_segment_output", stream);
-        if (part == nullptr) {
+        const dim3 grid(p.G, s.BH());
+        const OutGate none{nullptr, nullptr, 1};
+        if (part == nullptr && fin == nullptr) {
             cudaFuncSetAttribute(seg_output_kernel<32, 64, false, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
-            seg_output_kernel<32, 64, false, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part,
-                OutGate{nullptr, nullptr, 1});
-        } else {
+            seg_output_kernel<32, 64, false, false><<<grid, 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part, none,
+                nullptr);
+        } else if (part == nullptr) {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
+            seg_output_kernel<32, 64, false, false, true><<<grid, 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part, none,
+                fin);
+        } else if (fin == nullptr) {
             cudaFuncSetAttribute(seg_output_kernel<32, 64, true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
-            seg_output_kernel<32, 64, true, false><<<dim3(p.G, s.BH()), 608, kSmemOutput, stream>>>(
-                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part,
-                OutGate{nullptr, nullptr, 1});
+            seg_output_kernel<32, 64, true, false><<<grid, 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part, none,
+                nullptr);
+        } else {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, true, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutput);
+            seg_output_kernel<32, 64, true, false, true><<<grid, 608, kSmemOutput, stream>>>(
+                mq, mk, mv, mk, (bf16 *)out, seg, s.T, p.NCt, p.Lc, p.m, p.NR, nsub, cross, part, none,
+                fin);
         }
     }
-    if (sigma) {   // its scratch follows the records (and the totals)
+    if (with_state) {   // the full-map state of every key sub-head, in the decode layout
+        TraceScope tr("tc_state_export", stream);
+        state_export_kernel<32, 64><<<dim3(C::NBLK + 1, state_heads), 128, 0, stream>>>(fin, so.state,
+                                                                                          so.z);
+    }
+    if (sigma) {   // its scratch follows the records (and the final states)
         const size_t off = sub_part_floats(s, partials) +
                            (size_t)state_heads * (p.NR + (with_state ? 1 : 0)) * C::E;
         return sigma_finalize_launch(s0, cross ? SigmaParts::Sub4 : SigmaParts::Sub1, part,
@@ -1214,7 +1260,7 @@ cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, co
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutputGated);
         seg_output_kernel<32, 64, false, true><<<dim3(p.G, s.BH()), 608, kSmemOutputGated, stream>>>(
             mq, mk, mv, mkc, (bf16 *)out, w.rec, s.T, p.NCt, p.Lc, p.m, p.NR, 1, 0, nullptr,
-            OutGate{w.lam2, w.gch, normalize});
+            OutGate{w.lam2, w.gch, normalize}, nullptr);
     }
     return cudaGetLastError();
 }
