@@ -323,11 +323,13 @@ __device__ __noinline__ void output_lift_role(const uint8_t *tile, uint8_t *ring
 //   D_t = b_t q_t^T G_pre q_t      + sum_{s<=t} 2^(l_t - l_s) (q_t . k_s)^2,
 // b_t = 2^l_t.  The convert warps decay S_run block by block as they read it,
 // the P warps decay G as they read it; O = N / D, or N when !normalize.
-// kFin (not gated): fin receives the state after the head's last token.  S_run
-// starts from the segment's exclusive prefix, so after the last segment's last
-// chunk it is the head's whole state, and so is G; that CTA writes both in the
-// record layout to fin[sbh] (crosswise: the query-half-0 sub-heads, one per key
-// half).  A compile-time variant, so the kernel without it carries no export code.
+// kFin: fin receives the state after the head's last token.  S_run starts from
+// the segment's exclusive prefix, so after the last segment's last chunk it is
+// the head's whole state, and so is G (gated: S_run is decayed before each
+// chunk's update and G's decay for the next chunk is 1 after the last one, so
+// both are the gated totals); that CTA writes both in the record layout to
+// fin[sbh] (crosswise: the query-half-0 sub-heads, one per key half).  A
+// compile-time variant, so the kernel without it carries no export code.
 struct OutGate {
     const float *lam2;     // [BH][T] chunk-local cumulative log2 of the gates
     const float *gchunk;   // [BH][NC] gate product of each 128-token chunk
@@ -375,7 +377,6 @@ seg_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const bool xc = kSub && cross;
     const int qx = (xc ? j >> 1 : j) * D, kx = (xc ? j & 1 : j) * D;
     const int sbh = xc ? hz * 2 + (j & 1) : bh;   // records of this sub-head's keys
-    static_assert(!(kFin && kGated), "the gated path exports its state from the scan");
     float *const frec = (kFin && g == (int)gridDim.x - 1 && (!xc || (j >> 1) == 0))
                             ? fin + (size_t)sbh * C::E
                             : nullptr;
@@ -1210,8 +1211,10 @@ GatedWs gated_ws(const FwdShape &s, const Plan &p, bool with_state, void *base) 
 }
 }  // namespace
 
+// The final state comes from the output kernel's last segment, so the plan is the
+// one without it; the records gain one final record per head.
 size_t tc_gated_workspace_bytes(const FwdShape &s, int num_sms, bool with_state) {
-    return gated_ws(s, plan(s, num_sms, with_state, 1), with_state, nullptr).bytes;
+    return gated_ws(s, plan(s, num_sms, false, 1), with_state, nullptr).bytes;
 }
 
 cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, const void *v,
@@ -1219,8 +1222,9 @@ cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, co
                              cudaStream_t stream, const StateOut &so, int normalize) {
     using C = Cfg<32, 64>;
     const bool with_state = so.state != nullptr;
-    const Plan p = plan(s, num_sms, with_state, 1);
+    const Plan p = plan(s, num_sms, false, 1);
     const GatedWs w = gated_ws(s, p, with_state, workspace);
+    float *fin = with_state ? w.rec + (size_t)s.BH() * p.NR * C::E : nullptr;   // the final records
     CUtensorMap mq, mk, mv, mkc, mkpc;
     if (!make_map(mq, q, s.d, s.T, s.BH()) || !make_map(mk, k, s.d, s.T, s.BH()) ||
         !make_map(mv, v, s.dv, s.T, s.BH()) || !make_map(mkc, w.kc, s.d, s.T, s.BH()) ||
@@ -1242,25 +1246,33 @@ cudaError_t tc_forward_gated(const FwdShape &s, const void *q, const void *k, co
             seg_state_kernel<32, 64><<<dim3(p.nsum * p.m, s.BH()), 352, kSmemState, stream>>>(
                 mkpc, mv, w.rec, p.NCt, p.Lc, p.m, p.NR, 1, g_stall_next.exchange(0));
         }
-        float *totals = with_state ? w.rec + (size_t)s.BH() * p.NR * C::E : nullptr;
         {
             TraceScope tr("tc_gated_scan", stream);
             gated_record_scan_kernel<<<dim3((unsigned)((C::E / 4 + 255) / 256), s.BH()), 256, 0, stream>>>(
-                w.rec, w.pgate, p.NR, C::E, totals);
-        }
-        if (with_state) {
-            TraceScope tr("tc_state_export", stream);
-            state_export_kernel<32, 64><<<dim3(C::NBLK + 1, s.BH()), 128, 0, stream>>>(
-                totals, so.state, so.z);
+                w.rec, w.pgate, p.NR, C::E, nullptr);
         }
     }
     {
         TraceScope tr("tc_segment_output_gated", stream);
-        cudaFuncSetAttribute(seg_output_kernel<32, 64, false, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutputGated);
-        seg_output_kernel<32, 64, false, true><<<dim3(p.G, s.BH()), 608, kSmemOutputGated, stream>>>(
-            mq, mk, mv, mkc, (bf16 *)out, w.rec, s.T, p.NCt, p.Lc, p.m, p.NR, 1, 0, nullptr,
-            OutGate{w.lam2, w.gch, normalize}, nullptr);
+        const dim3 grid(p.G, s.BH());
+        const OutGate ga{w.lam2, w.gch, normalize};
+        if (fin == nullptr) {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutputGated);
+            seg_output_kernel<32, 64, false, true><<<grid, 608, kSmemOutputGated, stream>>>(
+                mq, mk, mv, mkc, (bf16 *)out, w.rec, s.T, p.NCt, p.Lc, p.m, p.NR, 1, 0, nullptr, ga,
+                nullptr);
+        } else {
+            cudaFuncSetAttribute(seg_output_kernel<32, 64, false, true, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOutputGated);
+            seg_output_kernel<32, 64, false, true, true><<<grid, 608, kSmemOutputGated, stream>>>(
+                mq, mk, mv, mkc, (bf16 *)out, w.rec, s.T, p.NCt, p.Lc, p.m, p.NR, 1, 0, nullptr, ga,
+                fin);
+        }
+    }
+    if (with_state) {
+        TraceScope tr("tc_state_export", stream);
+        state_export_kernel<32, 64><<<dim3(C::NBLK + 1, s.BH()), 128, 0, stream>>>(fin, so.state, so.z);
     }
     return cudaGetLastError();
 }

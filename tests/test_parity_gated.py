@@ -338,9 +338,11 @@ def test_gated_tensor_path_zero_gates(kg):
 
 
 @pytest.mark.parametrize("normalize", [True, False])
-@pytest.mark.parametrize("B,H,T", [(1, 2, 1100), (4, 15, 1000), (1, 4, 5000)])
+@pytest.mark.parametrize("B,H,T", [(1, 2, 1100), (4, 15, 1000), (1, 4, 5000), (16, 10, 700)])
 def test_gated_tensor_path_state(kg, normalize, B, H, T):
-    """The state after the last token (every segment summed, gated scan totals)."""
+    """The state after the last token: the last segment's running state and Gram,
+    which start from the gated prefix of the segments before (160 heads at
+    T = 700: one segment each)."""
     w = workloads.WORKLOADS["long_ctx_bf16"].scaled(B=B, H=H, T=T)
     q, k, v = workloads.make_qkv(w)
     g = _gates(w)
