@@ -328,3 +328,51 @@ def test_decode_read_before_update_fails_the_pin():
     wrong = (pq @ S[0, 0]) / (pq @ z[0, 0])
     ref = oracle.forward_map(q, k, v, "Sigma", 2, 1e-4, 1.0)[0, 0, T]
     assert _rel(wrong, ref) > 1e-6
+
+
+# ---- a reduced map's state from full-map states of its blocks (the composition
+# the tensor routes use), checked on the oracle alone
+def _vech_index(i, j, m):
+    return i * m - i * (i - 1) // 2 + (j - i)
+
+
+@pytest.mark.parametrize("map_name,d,g,eps,s,pad", [
+    ("M", 32, 2, 0.0, 1.0, 0), ("M", 64, 4, 0.0, 1.0, 16), ("M", 32, 2, 0.0, 1.0, 16),
+    ("Sigma", 64, 2, 1e-4, 1.0, 0), ("Sigma", 32, 2, 0.5, 0.25, 0), ("Sigma", 32, 1, 3.0, 1.0, 0),
+])
+def test_map_state_is_composed_from_block_states(map_name, d, g, eps, s, pad):
+    """M_g: block a's features are those of the full-map state of u_a (here also
+    of u_a zero-padded to m + pad coordinates, restricted to the first m);
+    Sigma_g: s sum_a S(u_a) + eps sum_t v_t on the diagonal features, and
+    z = s sum_a z(u_a) + eps T there (psi = eps I + s sum_a u_a u_a^T, term by term)."""
+    q, k, v = _rand_qkv(np.random.default_rng(d + 7 * g + pad), B=1, H=2, T=21, d=d, dv=5)
+    m = d // g
+    S, z = oracle.prefix_state_map(k, v, map_name, g, eps, s)
+    blocks = []
+    for a in range(g):
+        ka = k[..., a * m:(a + 1) * m]
+        if pad:
+            ka = np.concatenate([ka, np.zeros(ka.shape[:-1] + (pad,))], axis=-1)
+        blocks.append(oracle.prefix_state(ka, v))   # the full map of width m + pad
+    nm, mp = m * (m + 1) // 2, m + pad
+    sel = [_vech_index(i, j, mp) for i in range(m) for j in range(i, m)]   # first m coordinates
+    if map_name == "M":
+        S_c = np.concatenate([Sa[:, :, sel] for Sa, _ in blocks], axis=2)
+        z_c = np.concatenate([za[:, :, sel] for _, za in blocks], axis=2)
+    else:
+        diag = np.zeros(nm)
+        diag[[_vech_index(i, i, m) for i in range(m)]] = 1.0
+        T = k.shape[2]
+        S_c = s * sum(Sa[:, :, sel] for Sa, _ in blocks) + eps * diag[None, None, :, None] * \
+            v.sum(axis=2)[:, :, None, :]
+        z_c = s * sum(za[:, :, sel] for _, za in blocks) + eps * T * diag[None, None, :]
+    assert _rel(S_c, S) < 1e-12 and _rel(z_c, z) < 1e-12
+
+
+def test_map_state_composition_without_eps_fails_the_pin():
+    """Leaving out the eps diagonal (or the scale) breaks the Sigma composition."""
+    q, k, v = _rand_qkv(np.random.default_rng(77), B=1, H=1, T=15, d=32, dv=4)
+    S, _ = oracle.prefix_state_map(k, v, "Sigma", 2, 0.5, 0.25)
+    S_a = sum(oracle.prefix_state(k[..., a * 16:(a + 1) * 16], v)[0] for a in range(2))
+    assert _rel(0.25 * S_a, S) > 1e-3
+    assert _rel(S_a, S) > 1e-3
