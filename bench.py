@@ -342,7 +342,8 @@ def _ncu_traffic(kernel_stage: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle samples every 20 ms, each stamped with the
+    """nvidia-smi clocks/throttle samples every 5 ms (about 160 a second on
+    GB300, so a 20 ms timed region still holds a few), each stamped with the
     host time it arrived; summary() keeps the samples inside mark_start() ..
     mark_stop() (the timed region)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -365,7 +366,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "20", "-i", str(self.idx)],
+                 "-lms", "5", "-i", str(self.idx)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             self.thread = threading.Thread(target=self._reader, daemon=True)
             self.thread.start()
